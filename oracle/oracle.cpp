@@ -1,0 +1,473 @@
+// Plain CPU oracle for tree-based speculative verification.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+// statement of what the GPU library computes.  Only the test suite, the
+// smoke check and the bench's CPU-baseline leg may build, load or call it;
+// the GPU path never does, and the two share no code.
+//
+// Everything is written as the plain definition: explicit ancestor sets
+// obtained by walking parent links, fp64 arithmetic, full sorts, brute force.
+// No blocking, fusion or reordering beyond what the definition states.
+//
+// Sources (page title, section):
+//   [OPT]   "OPT-Tree: Speculative Decoding with Adaptive Draft Tree Structure",
+//           §2 Preliminaries (tree attention mask; longest matching branch
+//           under greedy sampling) and §3 (node scores, monotone path scores).
+//   [SPEC]  "Speculative Decoding" concept page, "The protocol" steps 1-4
+//           (accept with min(1, p/q), residual (p-q)+ resampling, lossless).
+//   [TALON] "TALON: confidence-aware speculative decoding with adaptive token
+//           trees", §5.1 (token budget B), §5.2.1 (confidence-gated
+//           expansion: candidate pool, path score s(c) = prod p_d, anchor,
+//           alpha gate, budget truncation), §5.2.2 (root Top-K).
+//   [GOOSE] "GOOSE: Anisotropic Speculation Trees", §2C (one forward pass
+//           verifies the whole tree; greedy walk).
+//   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+//           1, 2, 3" (SC'11): the Philox4x64-10 counter-based generator.
+//
+// Readings where the pages are silent (each also listed in the design notes):
+//   * node 0 is the token right after the cached prefix and is always
+//     accepted; logits row v is the target distribution over v's children;
+//     accept_len counts accepted draft tokens (node 0 excluded).
+//   * argmax ties go to the lowest token index; "longest branch" ties go to
+//     the lowest node index.
+//   * tree K/V of node j lives at cache slot kv_len[b] + j; GQA kv head of
+//     query head h is h / (Hq / Hkv); scale 0 means 1/sqrt(D).
+//   * stochastic acceptance on a tree tests children in ascending index;
+//     after a rejection the target becomes norm((r - q)+) with the same q.
+//
+// Decisions taken on floating point (accept tests, sampling, gating) also
+// report a margin: the distance of the decision quantity from its threshold,
+// so tests can tell a genuine disagreement from a rounding-order tie.
+
+#include <stdint.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+namespace {
+
+const int ST_OK = 0;
+const int ST_INVALID_ARG = 1;
+const int ST_INVALID_TREE = 2;
+const int ST_INVALID_TOKEN = 6;
+
+double bf16_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+// A tree is valid when node 0 is the only root and every other node's parent
+// comes earlier (a topological numbering).
+bool tree_is_valid(const int32_t* parent, int N) {
+  if (N < 1 || parent[0] != -1) return false;
+  for (int i = 1; i < N; ++i)
+    if (parent[i] < 0 || parent[i] >= i) return false;
+  return true;
+}
+
+// Explicit ancestor-or-self set of node i, from i up to the root.
+std::vector<int> ancestors_of(const int32_t* parent, int i) {
+  std::vector<int> a;
+  for (int x = i; x >= 0; x = parent[x]) a.push_back(x);
+  return a;
+}
+
+int depth_of(const int32_t* parent, int i) {
+  int d = 0;
+  for (int x = i; parent[x] >= 0; x = parent[x]) ++d;
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 [PHILOX]: ten rounds of two 64x64->128 multiplies with the
+// published multipliers, key bumped by the published Weyl constants.
+// ---------------------------------------------------------------------------
+void philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ULL, M1 = 0xCA5A826395121157ULL;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ULL, W1 = 0xBB67AE8584CAA73BULL;
+  uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) { k0 += W0; k1 += W1; }
+    unsigned __int128 p0 = (unsigned __int128)M0 * x0;
+    unsigned __int128 p1 = (unsigned __int128)M1 * x2;
+    uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+    uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+    x0 = hi1 ^ x1 ^ k0;
+    x1 = lo1;
+    x2 = hi0 ^ x3 ^ k1;
+    x3 = lo0;
+  }
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+// The single random word used by a decision: counter (offset, sequence,
+// node, purpose<<32 | ordinal), key (seed, 0); first output word.
+const uint64_t PURPOSE_ACCEPT = 0;  // accept test of the ordinal-th child
+const uint64_t PURPOSE_SAMPLE = 1;  // the final draw (residual or bonus)
+
+uint64_t draw_word(uint64_t seed, uint64_t offset, int b, int node, uint64_t purpose,
+                   uint32_t ordinal) {
+  uint64_t ctr[4] = {offset, (uint64_t)b, (uint64_t)node, (purpose << 32) | ordinal};
+  uint64_t key[2] = {seed, 0};
+  uint64_t out[4];
+  philox4x64_10(ctr, key, out);
+  return out[0];
+}
+
+// 53-bit uniform in [0,1): the top 53 bits of the word, scaled by 2^-53.
+double uniform53(uint64_t w) { return (double)(w >> 11) * (1.0 / 9007199254740992.0); }
+
+// Natural-log partition of a logits row at temperature T: log sum exp(l/T).
+double row_logsumexp(const float* row, int V, double T) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v) m = std::max(m, (double)row[v] / T);
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += exp((double)row[v] / T - m);
+  return m + log(s);
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// Tree encoding [OPT §2, §3]: the tree attention mask lets node i see exactly
+// its ancestors and itself.  depth[i] = number of edges from the root;
+// anc_mask[i] has bit j set iff j is on the path root..i.
+// ---------------------------------------------------------------------------
+int or_tree_build(const int32_t* parent, int B, int N, int32_t* depth, uint64_t* anc_mask,
+                  int32_t* status) {
+  if (B < 0 || N < 1) return ST_INVALID_ARG;
+  const int W = (N + 63) / 64;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent + (size_t)b * N;
+    int32_t* dep = depth + (size_t)b * N;
+    uint64_t* anc = anc_mask + (size_t)b * N * W;
+    memset(anc, 0, sizeof(uint64_t) * N * W);
+    if (!tree_is_valid(par, N)) {
+      status[b] = ST_INVALID_TREE;
+      for (int i = 0; i < N; ++i) dep[i] = -1;
+      continue;
+    }
+    status[b] = ST_OK;
+    for (int i = 0; i < N; ++i) {
+      dep[i] = depth_of(par, i);
+      for (int a : ancestors_of(par, i)) anc[(size_t)i * W + a / 64] |= 1ULL << (a % 64);
+    }
+  }
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Tree-verify attention [OPT §2; GOOSE §2C; SPEC "Why it is a win"]: for the
+// query of node i and head h, attend over the cached prefix 0..L_b-1 and the
+// tree slots L_b + j of the ancestors-or-self j of i.  The kv head of query
+// head h is h / (Hq/Hkv).  Computed for the requested rows only:
+// rows[3r..3r+2] = (b, i, h).  out[r*D + d] gets the output, lse[r] the
+// natural-log normaliser log sum_j exp(scale * q.k_j).
+// ---------------------------------------------------------------------------
+int or_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                 const int32_t* kv_len, const int32_t* parent, int B, int N, int Hq,
+                 int Hkv, int D, int Lcap, double scale, const int32_t* rows, int n_rows,
+                 double* out, double* lse) {
+  if (Hkv < 1 || Hq % Hkv != 0 || N < 1 || D < 1) return ST_INVALID_ARG;
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  const int G = Hq / Hkv;
+  for (int r = 0; r < n_rows; ++r) {
+    const int b = rows[3 * r], i = rows[3 * r + 1], h = rows[3 * r + 2];
+    if (b < 0 || b >= B || i < 0 || i >= N || h < 0 || h >= Hq) return ST_INVALID_ARG;
+    const int32_t* par = parent + (size_t)b * N;
+    if (!tree_is_valid(par, N)) return ST_INVALID_TREE;
+    const int L = kv_len[b];
+    if (L < 0 || L + N > Lcap) return ST_INVALID_ARG;
+    const int kvh = h / G;
+
+    std::vector<int> keys;  // cache positions visible to (b, i)
+    for (int j = 0; j < L; ++j) keys.push_back(j);
+    std::vector<int> anc = ancestors_of(par, i);
+    std::sort(anc.begin(), anc.end());
+    for (int a : anc) keys.push_back(L + a);
+
+    const uint16_t* qrow = q + (((size_t)b * N + i) * Hq + h) * D;
+    const uint16_t* kbase = k + ((size_t)b * Hkv + kvh) * (size_t)Lcap * D;
+    const uint16_t* vbase = v + ((size_t)b * Hkv + kvh) * (size_t)Lcap * D;
+
+    std::vector<double> s(keys.size());
+    double m = -INFINITY;
+    for (size_t t = 0; t < keys.size(); ++t) {
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d)
+        dot += bf16_to_double(qrow[d]) * bf16_to_double(kbase[(size_t)keys[t] * D + d]);
+      s[t] = dot * scale;
+      m = std::max(m, s[t]);
+    }
+    double denom = 0.0;
+    for (size_t t = 0; t < keys.size(); ++t) denom += exp(s[t] - m);
+    for (int d = 0; d < D; ++d) {
+      double acc = 0.0;
+      for (size_t t = 0; t < keys.size(); ++t)
+        acc += exp(s[t] - m) * bf16_to_double(vbase[(size_t)keys[t] * D + d]);
+      out[(size_t)r * D + d] = acc / denom;
+    }
+    lse[r] = m + log(denom);
+  }
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Greedy acceptance [OPT §2 "longest branch matching the target's
+// highest-probability sequence"; GOOSE §2C greedy walk].
+//   argmax[i]  = first index of the largest logit in row i;
+//   a node is valid iff every edge p->c on its root path has
+//              tokens[c] == argmax[p]   (checked by brute force per node);
+//   end        = deepest valid node, ties to the lowest index;
+//   accept_len = depth[end]; path = root..end padded with -1;
+//   bonus      = argmax[end] (the target's own next token).
+// ---------------------------------------------------------------------------
+int or_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* parent, int B,
+                     int N, int V, int32_t* argmax, int32_t* accept_len, int32_t* end_node,
+                     int32_t* path, int32_t* bonus, int32_t* status) {
+  if (B < 0 || N < 1 || V < 1) return ST_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent + (size_t)b * N;
+    const int32_t* tok = tokens + (size_t)b * N;
+    int32_t* am = argmax + (size_t)b * N;
+    for (int i = 0; i < N; ++i) {
+      const float* row = logits + ((size_t)b * N + i) * V;
+      int best = 0;
+      for (int t = 1; t < V; ++t)
+        if (row[t] > row[best]) best = t;
+      am[i] = best;
+    }
+    for (int i = 0; i < N; ++i) path[(size_t)b * N + i] = -1;
+    accept_len[b] = end_node[b] = bonus[b] = -1;
+    if (!tree_is_valid(par, N)) { status[b] = ST_INVALID_TREE; continue; }
+    bool tok_ok = true;
+    for (int i = 1; i < N; ++i)
+      if (tok[i] < 0 || tok[i] >= V) tok_ok = false;
+    if (!tok_ok) { status[b] = ST_INVALID_TOKEN; continue; }
+    status[b] = ST_OK;
+
+    int end = 0, end_depth = 0;
+    for (int e = 0; e < N; ++e) {
+      bool valid = true;
+      for (int c = e; par[c] >= 0; c = par[c])
+        if (tok[c] != am[par[c]]) valid = false;
+      const int de = depth_of(par, e);
+      if (valid && de > end_depth) { end = e; end_depth = de; }
+    }
+    std::vector<int> anc = ancestors_of(par, end);  // end .. root
+    for (size_t t = 0; t < anc.size(); ++t) path[(size_t)b * N + (anc.size() - 1 - t)] = anc[t];
+    accept_len[b] = end_depth;
+    end_node[b] = end;
+    bonus[b] = am[end];
+  }
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Stochastic acceptance [SPEC "The protocol", step 3 and the lossless
+// remark], extended to a tree: start at node 0 with target r = p_0.  At node
+// v, test its children c (ascending index, draft token x = tokens[c]):
+// accept with probability min(1, r(x)/q_v(x)) -- draw u, accept iff
+// u < r(x)/q_v(x), and always when q_v(x) = 0.  On acceptance descend to c
+// (r := p_c).  On rejection r := norm((r - q_v)+) (unchanged if that mass is
+// not positive).  If every child is rejected, draw the output token from r;
+// if v has no children, draw the bonus token from p_v.  p_v, q_v are
+// softmax(logits/T) of row v.
+//
+// Random words: Philox4x64-10 keyed by (seed, 0), counter (offset, b, v,
+// purpose<<32 | ordinal), each turned into a 53-bit uniform u.  Accept
+// tests compare u with the fp64 ratio.  The final draw keeps an fp64 running
+// sum of the probabilities rounded to fp32 (the precision in which the GPU
+// holds them element by element): the token is the smallest k whose
+// cumulative mass exceeds u * (total mass); if rounding leaves none, the last
+// token with positive mass.
+//
+// margin[b] = smallest relative distance of any decision of tree b from its
+// threshold (accept tests: |u - ratio| / ratio; draws: distance of u*total to
+// the nearest cumulative boundary / total).
+// ---------------------------------------------------------------------------
+int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t* tokens,
+                     const int32_t* parent, int B, int N, int V, float temperature,
+                     uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* end_node,
+                     int32_t* path, int32_t* out_token, int32_t* status, double* margin) {
+  if (B < 0 || N < 1 || V < 1 || !(temperature > 0.0f)) return ST_INVALID_ARG;
+  const double T = (double)temperature;
+  std::vector<double> r(V), q(V);
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent + (size_t)b * N;
+    const int32_t* tok = tokens + (size_t)b * N;
+    for (int i = 0; i < N; ++i) path[(size_t)b * N + i] = -1;
+    accept_len[b] = end_node[b] = out_token[b] = -1;
+    margin[b] = INFINITY;
+    if (!tree_is_valid(par, N)) { status[b] = ST_INVALID_TREE; continue; }
+    bool tok_ok = true;
+    for (int i = 1; i < N; ++i)
+      if (tok[i] < 0 || tok[i] >= V) tok_ok = false;
+    if (!tok_ok) { status[b] = ST_INVALID_TOKEN; continue; }
+    status[b] = ST_OK;
+
+    int node = 0;
+    int out = -1;
+    for (;;) {
+      const float* prow = p_logits + ((size_t)b * N + node) * V;
+      const float* qrow = q_logits + ((size_t)b * N + node) * V;
+      const double lp = row_logsumexp(prow, V, T);
+      const double lq = row_logsumexp(qrow, V, T);
+      for (int t = 0; t < V; ++t) {
+        r[t] = exp((double)prow[t] / T - lp);
+        q[t] = exp((double)qrow[t] / T - lq);
+      }
+      std::vector<int> kids;
+      for (int c = node + 1; c < N; ++c)
+        if (par[c] == node) kids.push_back(c);
+
+      int accepted = -1;
+      for (size_t o = 0; o < kids.size(); ++o) {
+        const int x = tok[kids[o]];
+        const double u = uniform53(draw_word(seed, offset, b, node, PURPOSE_ACCEPT, (uint32_t)o));
+        bool acc;
+        if (q[x] == 0.0) {
+          acc = true;
+        } else {
+          const double ratio = r[x] / q[x];
+          acc = u < ratio;
+          if (ratio > 0.0) margin[b] = std::min(margin[b], fabs(u - ratio) / ratio);
+        }
+        if (acc) { accepted = kids[o]; break; }
+        double z = 0.0;
+        for (int t = 0; t < V; ++t) z += std::max(r[t] - q[t], 0.0);
+        if (z > 0.0)
+          for (int t = 0; t < V; ++t) r[t] = std::max(r[t] - q[t], 0.0) / z;
+      }
+      if (accepted >= 0) { node = accepted; continue; }
+
+      // Final draw from r (the residual, or p_node at a leaf).
+      const double u = uniform53(draw_word(seed, offset, b, node, PURPOSE_SAMPLE, 0));
+      double total = 0.0;
+      for (int t = 0; t < V; ++t) total += (double)(float)r[t];
+      const double target = u * total;
+      double cum = 0.0;
+      int last_pos = -1;
+      for (int t = 0; t < V; ++t) {
+        const double rt = (double)(float)r[t];
+        if (rt > 0.0) last_pos = t;
+        const double before = cum;
+        cum += rt;
+        if (out < 0 && cum > target) {
+          out = t;
+          margin[b] = std::min(margin[b], std::min(cum - target, target - before) / total);
+        }
+      }
+      if (out < 0) out = last_pos;
+      break;
+    }
+    std::vector<int> anc = ancestors_of(par, node);
+    for (size_t t = 0; t < anc.size(); ++t) path[(size_t)b * N + (anc.size() - 1 - t)] = anc[t];
+    accept_len[b] = depth_of(par, node);
+    end_node[b] = node;
+    out_token[b] = out;
+  }
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TALON layer expansion [TALON §5.1, §5.2.1, §5.2.2].
+//   Row v of draft_logits is the draft distribution p_d(. | path to
+//   frontier_node[v]); frontier_logscore[v] = log s(frontier_node[v]).
+//   Candidate (v, c) has log s = frontier_logscore[v] + log softmax(row v)[c].
+//   layer == 1: keep the Top-K tokens of the single (root) row -- no gate.
+//   layer >= 2: anchor = max log s over all candidates; keep those with
+//              log s >= log(alpha) + anchor.
+//   Either way at most R = budget - n_nodes are kept, the best scores first
+//   (ties: parent node ascending, token ascending).  Kept nodes are appended
+//   at ids n_nodes.. in (parent asc, score desc, token asc) order.
+// margin = smallest |log s - threshold| over candidates, and the gap between
+// the last kept and the first dropped score when they have different
+// parents (absolute, log domain).  Candidates of one row differ only by their
+// fp32 logits, so their order is exact and carries no margin.
+// ---------------------------------------------------------------------------
+struct Cand {
+  double ls;
+  int parent;
+  int token;
+};
+
+int or_expand_gated(const float* draft_logits, const int32_t* frontier_node,
+                    const float* frontier_logscore, int F, int V, int layer, int topk,
+                    float alpha, int budget, int32_t* tree_parent, int32_t* tree_token,
+                    float* tree_logscore, int32_t* n_nodes, double* margin) {
+  *margin = INFINITY;
+  if (F < 0 || V < 1 || layer < 1 || budget < 1) return ST_INVALID_ARG;
+  if (layer == 1 && (F != 1 || topk < 1)) return ST_INVALID_ARG;
+  if (layer >= 2 && !(alpha > 0.0f && alpha <= 1.0f)) return ST_INVALID_ARG;
+  const int n0 = *n_nodes;
+  const int R = budget - n0;
+  if (R <= 0 || F == 0) return ST_OK;
+
+  std::vector<Cand> all;
+  all.reserve((size_t)F * V);
+  for (int v = 0; v < F; ++v) {
+    const float* row = draft_logits + (size_t)v * V;
+    const double lse = row_logsumexp(row, V, 1.0);
+    for (int c = 0; c < V; ++c)
+      all.push_back({(double)frontier_logscore[v] + ((double)row[c] - lse), frontier_node[v], c});
+  }
+  auto better = [](const Cand& a, const Cand& b) {
+    if (a.ls != b.ls) return a.ls > b.ls;
+    if (a.parent != b.parent) return a.parent < b.parent;
+    return a.token < b.token;
+  };
+  std::vector<Cand> pass;
+  int limit = R;
+  if (layer == 1) {
+    pass = all;
+    limit = std::min(topk, R);
+  } else {
+    double anchor = -INFINITY;
+    for (const Cand& c : all) anchor = std::max(anchor, c.ls);
+    const double thr = log((double)alpha) + anchor;
+    for (const Cand& c : all) {
+      if (c.ls >= thr) pass.push_back(c);
+      if (c.ls != thr) *margin = std::min(*margin, fabs(c.ls - thr));
+    }
+  }
+  std::sort(pass.begin(), pass.end(), better);
+  if ((int)pass.size() > limit) {
+    if (pass[limit - 1].parent != pass[limit].parent)
+      *margin = std::min(*margin, pass[limit - 1].ls - pass[limit].ls);
+    pass.resize(limit);
+  }
+  std::sort(pass.begin(), pass.end(), [](const Cand& a, const Cand& b) {
+    if (a.parent != b.parent) return a.parent < b.parent;
+    if (a.ls != b.ls) return a.ls > b.ls;
+    return a.token < b.token;
+  });
+  for (size_t t = 0; t < pass.size(); ++t) {
+    tree_parent[n0 + t] = pass[t].parent;
+    tree_token[n0 + t] = pass[t].token;
+    tree_logscore[n0 + t] = (float)pass[t].ls;
+  }
+  *n_nodes = n0 + (int)pass.size();
+  return ST_OK;
+}
+
+// Philox4x64-10 block (exposed for the generator's own pins).
+void or_philox4x64_10(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
+  philox4x64_10(ctr, key, out);
+}
+
+// The random word a decision uses (see or_accept_sample).
+uint64_t or_draw_word(uint64_t seed, uint64_t offset, int b, int node, int purpose,
+                      uint32_t ordinal) {
+  return draw_word(seed, offset, b, node, (uint64_t)purpose, ordinal);
+}
+
+}  // extern "C"
