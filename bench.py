@@ -1,0 +1,518 @@
+#!/usr/bin/env python
+"""Tree-verify step throughput on GB300.
+
+One step = one pass of the verify hot path over one synthetic draft tree:
+tv_tree_build -> tv_attn_verify (one attention layer over the KV prefix plus
+the tree) -> tv_accept_greedy (argmax over every node's vocabulary row and
+the longest matching branch).  Workload: Llama-3-8B-shaped GOOSE spine tree
+(batch 1, KV prefix 2048, 32 query / 8 KV heads, head_dim 128, 60 nodes,
+vocab 128256).
+
+Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs,
+bracketed by a barrier and cudaDeviceSynchronize, timed with CUDA events on
+the launching stream.  Steps rotate over input sets whose total size is at
+least 3x the L2 cache, so every step reads HBM.  Under torchrun each rank runs
+an independent replica (the path needs no exchange between GPUs) and the
+slowest rank's time is reported.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify steps/s & achieved HBM GB/s (Llama-3-8B shape, 60-node tree)"
+UNIT = "steps/s"
+WORKLOAD = ("llama3-8b-spine60-L2048: batch 1, KV prefix 2048, 32 q / 8 kv heads, head_dim 128, "
+            "bf16 Q/K/V; 60-node GOOSE spine tree; fp32 target logits over vocab 128256; "
+            "greedy acceptance")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100000)
+    p.add_argument("--warmup", type=int, default=1000)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--graph-steps", type=int, default=200)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# environment helpers
+# ----------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background (200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), util=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_busy": len(busy)}
+
+
+# ----------------------------------------------------------------------------
+# workload
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(case):
+    """Bytes each kernel must move at minimum (one launch), per the step's
+    definition: K and V of every visible key once, Q and O once, the mask
+    once; every logit once plus the small per-node integer arrays."""
+    B, N, Hq, Hkv, D, V = case.B, case.N, case.Hq, case.Hkv, case.D, case.V
+    W = (N + 63) // 64
+    keys = int(np.sum(case.kv_len.astype(np.int64) + N))
+    attn = 4 * D * Hkv * keys + 4 * B * N * Hq * D + 8 * B * N * W
+    greedy = 4 * B * N * V + 12 * B * N
+    tree = 4 * B * N + 4 * B * N + 8 * B * N * W
+    return dict(tree=tree, attn=attn, greedy=greedy)
+
+
+def attention_flops(case):
+    """4 * Hq * D per visible (query, key) pair: prefix plus ancestors-or-self."""
+    from workloads import gen
+    tot = 0
+    for b in range(case.B):
+        d = gen.depth_of(case.parent[b])
+        tot += int(np.sum(case.kv_len[b] + d + 1))
+    return 4 * case.Hq * case.D * tot
+
+
+def make_sets(case, torch, device, l2_bytes):
+    def bf16(u):
+        return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).to(device).view(
+            torch.bfloat16)
+
+    base = dict(
+        parent=torch.from_numpy(case.parent).to(device),
+        tokens=torch.from_numpy(case.tokens).to(device),
+        kv_len=torch.from_numpy(case.kv_len).to(device),
+        q=bf16(case.q), k=bf16(case.k), v=bf16(case.v),
+        logits=torch.from_numpy(case.logits).to(device))
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values())
+    M = max(2, int(np.ceil(3 * l2_bytes / set_bytes)))
+    sets = [base] + [{k: t.clone() for k, t in base.items()} for _ in range(M - 1)]
+    return sets, set_bytes
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import speculative_decoding_tree_tv_gb300 as tv
+    from workloads import gen
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    case = gen.config2()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    sets, set_bytes = make_sets(case, torch, device, l2)
+    M = len(sets)
+    B, N, Hq = case.B, case.N, case.Hq
+    W = (N + 63) // 64
+    depth = torch.empty((B, N), dtype=torch.int32, device=device)
+    anc = torch.empty((B, N, W), dtype=torch.int64, device=device)
+    tstat = torch.empty(B, dtype=torch.int32, device=device)
+    out = torch.empty_like(sets[0]["q"])
+    lse = torch.empty((B, N, Hq), dtype=torch.float32, device=device)
+    astat = torch.empty(B, dtype=torch.int32, device=device)
+    gouts = dict(argmax=torch.empty((B, N), dtype=torch.int32, device=device),
+                 accept_len=torch.empty(B, dtype=torch.int32, device=device),
+                 end_node=torch.empty(B, dtype=torch.int32, device=device),
+                 path=torch.empty((B, N), dtype=torch.int32, device=device),
+                 bonus=torch.empty(B, dtype=torch.int32, device=device),
+                 status=torch.empty(B, dtype=torch.int32, device=device))
+
+    def k_tree(s):
+        tv.tree_build(s["parent"], depth, anc, tstat)
+
+    def k_attn(s):
+        tv.attn_verify(s["q"], s["k"], s["v"], s["kv_len"], anc, out=out, lse=lse, status=astat)
+
+    def k_greedy(s):
+        tv.accept_greedy(s["logits"], s["tokens"], s["parent"], depth, outs=gouts)
+
+    def step(s):
+        k_tree(s)
+        k_attn(s)
+        k_greedy(s)
+
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(min(args.warmup, 3 * M)):     # eager warm-up: workspaces, sanity
+            step(sets[i % M])
+    torch.cuda.synchronize()
+    assert int(gouts["status"][0]) == 0 and int(astat[0]) == 0
+
+    def capture(fn, count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(count):
+                fn(sets[j % M])
+        return g
+
+    C = max(M, (args.graph_steps // M) * M)
+    g_full = capture(step, C)
+    rem = args.steps % C
+    g_rem = capture(step, rem) if rem else None
+
+    def replay_steps(n, g_full=g_full, g_rem=g_rem):
+        for _ in range(n // C):
+            g_full.replay()
+        if n % C:
+            (g_rem if n % C == rem else capture(step, n % C)).replay()
+
+    # warm-up through the graphs
+    with torch.cuda.stream(stream):
+        replay_steps(max(args.warmup, 0))
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay_steps(args.steps)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    clocks = sampler.stop()
+    assert int(gouts["status"][0]) == 0
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # per-kernel average launch time, each kernel replayed alone over the same rotation
+    per_kernel = {}
+    nk = min(args.steps, 20000)
+    for name, fn in (("tv_tree_build", k_tree), ("tv_attn_verify", k_attn),
+                     ("tv_accept_greedy", k_greedy)):
+        g = capture(fn, C)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(max(1, nk // C)):
+                g.replay()
+            z.record(stream)
+        torch.cuda.synchronize()
+        per_kernel[name] = a.elapsed_time(z) * 1e3 / (max(1, nk // C) * C)   # us per launch
+        del g
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, torch, tv, case, sets, step, gouts, stream, device)
+
+    return dict(case=case, elapsed_ms=elapsed_ms, per_kernel=per_kernel, clocks=clocks, M=M,
+                set_bytes=set_bytes, l2=l2, e2e=e2e)
+
+
+def measure_e2e(args, torch, tv, case, sets, step, gouts, stream, device):
+    """Same step through the public API from pinned host buffers: every step
+    copies its inputs host->device (tree, tokens, queries, the tree's own K/V
+    slots, target logits) and reads the acceptance result back."""
+    B, N, Hkv = case.B, case.N, case.Hkv
+    L = int(case.kv_len[0])
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h = dict(parent=pin(case.parent), tokens=pin(case.tokens), kv_len=pin(case.kv_len),
+             q=pin(case.q.view(np.int16)), logits=pin(case.logits),
+             ktree=pin(case.k[0, :, L:L + N].view(np.int16)),
+             vtree=pin(case.v[0, :, L:L + N].view(np.int16)))
+    hout = {k: torch.empty_like(gouts[k], device="cpu").pin_memory()
+            for k in ("accept_len", "end_node", "path", "bonus")}
+    M = len(sets)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+
+    def e2e_step(s):
+        s["parent"].copy_(h["parent"], non_blocking=True)
+        s["tokens"].copy_(h["tokens"], non_blocking=True)
+        s["kv_len"].copy_(h["kv_len"], non_blocking=True)
+        s["q"].view(torch.int16).copy_(h["q"], non_blocking=True)
+        s["logits"].copy_(h["logits"], non_blocking=True)
+        kv16 = s["k"].view(torch.int16)
+        vv16 = s["v"].view(torch.int16)
+        for kvh in range(Hkv):
+            kv16[0, kvh, L:L + N].copy_(h["ktree"][kvh], non_blocking=True)
+            vv16[0, kvh, L:L + N].copy_(h["vtree"][kvh], non_blocking=True)
+        step(s)
+        for k in hout:
+            hout[k].copy_(gouts[k], non_blocking=True)
+
+    steps = min(args.steps, 2000)
+    mode = "graph"
+    try:
+        C = M * max(1, 50 // M)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(C):
+                e2e_step(sets[j % M])
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // C)
+        steps = reps * C
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            z.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(z)
+        del g
+    except Exception:
+        mode = "eager"
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for j in range(3):
+                e2e_step(sets[j % M])
+            a.record(stream)
+            for j in range(steps):
+                e2e_step(sets[j % M])
+            z.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(z)
+    assert int(hout["accept_len"][0]) == int(gouts["accept_len"][0])
+    return {"value": steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "mode": mode}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ----------------------------------------------------------------------------
+def oracle_step_sample(case, rows_attn, rows_greedy, rng):
+    """One bounded sample of a step on the oracle: the tree encoding, the
+    attention rows `rows_attn` of the (node, head) grid and the greedy
+    acceptance over `rows_greedy` node rows (a whole tree when equal to N)."""
+    import oracle
+    oracle.tree_build(case.parent)
+    if rows_attn:
+        idx = rng.choice(case.N * case.Hq, size=rows_attn, replace=False)
+        rows = np.stack([np.zeros(rows_attn, np.int64), idx // case.Hq, idx % case.Hq], axis=1)
+        oracle.attn_rows(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq, case.Hkv, rows)
+    if rows_greedy >= case.N:
+        oracle.accept_greedy(case.logits, case.tokens, case.parent)
+    elif rows_greedy:
+        # argmax rows only (the tree scan needs every row)
+        oracle.accept_greedy(case.logits[:, :rows_greedy], case.tokens[:, :rows_greedy],
+                             np.ascontiguousarray(case.parent[:, :rows_greedy]))
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """Whole oracle steps on one host core until about budget_s seconds."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        oracle_step_sample(case, case.N * case.Hq, case.N, rng)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} full step(s) of the workload (tree encoding, all "
+                      f"{case.N * case.Hq} attention rows in fp64, greedy over all {case.N} "
+                      f"rows), single thread, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each timed step is a bounded sample of
+    the workload, scaled to whole steps in the reported rate."""
+    from workloads import gen
+    import oracle
+    if rank != 0:
+        return None
+    oracle.build()
+    case = gen.config2()
+    rng = np.random.default_rng(1)
+    # size the per-step sample so the whole run takes about 90 s
+    t0 = time.perf_counter()
+    oracle_step_sample(case, 8, 1, rng)
+    t_probe = (time.perf_counter() - t0) / 8
+    total = max(1, args.steps + args.warmup)
+    per_step_s = 90.0 / total
+    rows = int(min(case.N * case.Hq, max(1, per_step_s / max(t_probe, 1e-6))))
+    g_rows = max(1, min(case.N, rows * case.N // (case.N * case.Hq) or 1))
+    for _ in range(args.warmup):
+        oracle_step_sample(case, rows, g_rows, rng)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step_sample(case, rows, g_rows, rng)
+    dt = time.perf_counter() - t0
+    frac = rows / (case.N * case.Hq)
+    value = args.steps * frac / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_per_step": f"{rows} of {case.N * case.Hq} "
+                       f"attention rows + {g_rows} greedy rows, scaled to whole steps"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} attention rows per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    return line
+
+
+# ----------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        return
+    case = r["case"]
+    hbm, tflops, peak_src = load_peaks()
+    nbytes = algorithmic_bytes(case)
+    flops = attention_flops(case)
+    sec = r["elapsed_ms"] / 1e3
+    steps_total = args.steps * world
+    value = steps_total / sec
+    ms_per_step = r["elapsed_ms"] / args.steps
+    step_bytes = sum(nbytes.values())
+    pk = r["per_kernel"]
+    g_us = pk["tv_accept_greedy"]
+    a_us = pk["tv_attn_verify"]
+    greedy_gbs = nbytes["greedy"] / (g_us * 1e-6) / 1e9
+    attn_gbs = nbytes["attn"] / (a_us * 1e-6) / 1e9
+    t_roof_us = sum(max(nbytes[k] / (hbm * 1e9), (flops if k == "attn" else 0) / (tflops * 1e12))
+                    for k in nbytes) * 1e6
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD,
+                   "l2": f"{r['M']} rotating input sets of {r['set_bytes'] / 1e6:.1f} MB "
+                         f"(>= 3x the {r['l2'] / 1e6:.0f} MB L2)",
+                   "timing": "CUDA graphs of whole steps, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "tree_tokens_per_s": value * case.B * case.N,
+        "achieved_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "roofline_step_us": t_roof_us,
+        "roofline_step_frac": t_roof_us / (ms_per_step * 1e3),
+        "roofline": {"bound": "hbm", "kernel": "tv_accept_greedy",
+                     "achieved": greedy_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": greedy_gbs / hbm, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "bytes_per_launch": nbytes["greedy"]},
+        "kernels": {k: {"us_per_launch": v} for k, v in pk.items()},
+        "gpu_launches": 3 * args.steps,
+        "clocks": r["clocks"],
+    }
+    line["kernels"]["tv_attn_verify"].update(
+        {"algorithmic_bytes": nbytes["attn"], "flops": flops, "achieved_gbs": attn_gbs,
+         "achieved_tflops": flops / (a_us * 1e-6) / 1e12})
+    line["kernels"]["tv_accept_greedy"].update(
+        {"algorithmic_bytes": nbytes["greedy"], "achieved_gbs": greedy_gbs})
+    line["kernels"]["tv_tree_build"].update({"algorithmic_bytes": nbytes["tree"]})
+    if r["e2e"] is not None:
+        line["e2e"] = r["e2e"]
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

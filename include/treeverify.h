@@ -1,0 +1,235 @@
+/*
+ * libtreeverify -- the GPU hot path of tree-based speculative decoding on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One verify step of tree speculative decoding (OPT-Tree: Speculative Decoding
+ * with Adaptive Draft Tree Structure, §2 Preliminaries; GOOSE: Anisotropic
+ * Speculation Trees, §2C; Speculative Decoding concept page, "The protocol"):
+ * a drafter proposes a tree of tokens, the target model scores every tree
+ * node in one forward pass under a tree attention mask, and an acceptance rule
+ * keeps the longest acceptable branch plus one token from the target.  This
+ * library provides the data-parallel steps of that pass:
+ *
+ *   tv_tree_build     parent[] -> depth[], ancestor bitmasks (the tree mask)
+ *   tv_attn_verify    GQA attention of every tree node over the KV prefix and
+ *                     its own ancestors (one layer of the verify pass)
+ *   tv_accept_greedy  longest branch matching the target's argmax sequence
+ *   tv_accept_sample  stochastic acceptance min(1, p/q) with (p-q)+ residual
+ *                     resampling, Philox4x64-10 random numbers
+ *   tv_expand_gated   one layer of TALON's budget-driven, confidence-gated
+ *                     tree expansion (root Top-K, anchor, alpha gate, budget)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *    its comment says otherwise.  The library keeps no state between calls
+ *    and allocates no device memory; scratch comes from the caller's
+ *    workspace argument, sized by the matching *_workspace_size() call.
+ *  - Every call enqueues its kernels on `stream` and returns without waiting.
+ *  - Errors the host can see (bad sizes, null pointers, unsupported shapes,
+ *    a workspace that is too small) return a non-zero tv_status before
+ *    anything is launched.  A failed kernel launch returns TV_ERR_CUDA.
+ *  - Errors in device-resident data (a malformed parent[] array, a token
+ *    outside [0, V), a kv_len that does not fit the cache) are written to the
+ *    per-sequence `status[b]` array (0 = ok) and that sequence's outputs are
+ *    set to -1 (indices) or 0 (values).  No kernel traps, asserts or
+ *    spin-waits.
+ *  - Trees: node 0 is the root (the token right after the cached prefix,
+ *    always accepted), parent[b*N + 0] = -1 and 0 <= parent[b*N + i] < i for
+ *    i > 0, i.e. the nodes are numbered in a topological order.  N <= 512.
+ *  - Row v of a logits tensor is the distribution over the children of v.
+ *  - bf16 tensors are passed as their 16-bit patterns (tv_bf16).
+ *  - Workspaces marked "zero-filled" must be zero-filled before their first
+ *    use (tv_workspace_clear) and are returned zero-filled by every call that
+ *    completes.  Calls that share one workspace must not run concurrently.
+ */
+#ifndef TREEVERIFY_H_
+#define TREEVERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t tv_bf16; /* IEEE bfloat16 bit pattern */
+
+typedef enum {
+  TV_OK = 0,
+  TV_ERR_INVALID_ARG = 1,   /* bad size, null pointer, bad hyperparameter */
+  TV_ERR_INVALID_TREE = 2,  /* parent[] is not a single-root topological tree */
+  TV_ERR_UNSUPPORTED = 3,   /* shape outside the supported set (e.g. D not 64/128) */
+  TV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  TV_ERR_TIMEOUT = 5,       /* reserved: a bounded device wait gave up */
+  TV_ERR_INVALID_TOKEN = 6, /* a draft token outside [0, V) */
+  TV_ERR_WORKSPACE = 7      /* workspace missing or smaller than required */
+} tv_status;
+
+/* Maximum tree size (nodes per sequence) handled by every entry point. */
+#define TV_MAX_NODES 512
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tv_status_string(tv_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int tv_version(void);
+
+/* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
+tv_status tv_workspace_clear(void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tv_tree_build -- encode draft trees as the tree attention mask.
+ * (OPT-Tree §2 and §3: the target verifies all tree tokens in parallel using
+ * a tree attention mask in which a node sees its ancestors and itself.)
+ *
+ *   parent    int32 [B, N]          parent of each node, see Conventions.
+ *   depth     int32 [B, N]   out    depth[i] = edges from the root (root 0).
+ *   anc_mask  uint64 [B, N, W] out  W = ceil(N / 64); bit (j % 64) of word
+ *                                   j / 64 of node i is set iff j is i or an
+ *                                   ancestor of i.
+ *   status    int32 [B]      out    0, or TV_ERR_INVALID_TREE (then depth is
+ *                                   -1 and anc_mask 0 for that sequence).
+ * Requires 1 <= N <= TV_MAX_NODES, B >= 0 (B = 0 is a no-op).
+ */
+tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
+                        uint64_t* anc_mask, int32_t* status, cudaStream_t stream);
+
+/*
+ * tv_attn_verify -- one attention layer of the tree verify pass.
+ * (OPT-Tree §2: all tree tokens are verified in one target pass under the tree
+ * mask; GOOSE §2C: a single forward pass verifies the entire tree;
+ * Speculative Decoding concept page, "Why it is a win": the pass reads the
+ * KV cache once for all positions.)
+ *
+ * For sequence b, node i, query head h (kv head h / (Hq / Hkv)):
+ *   out[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:] . k[b,kvh,j,:]) v[b,kvh,j,:]
+ * over the key slots j in {0 .. kv_len[b]-1} (the cached prefix) and
+ * {kv_len[b] + a : a an ancestor of i or i itself} (the tree's own keys,
+ * which the caller has written to the cache at slots kv_len[b] .. kv_len[b]+N-1).
+ *
+ *   q         bf16 [B, N, Hq, D]     queries (already rotary-embedded; node i
+ *                                    sits at position kv_len[b] + depth[i]).
+ *   k, v      bf16 [B, Hkv, Lcap, D] KV cache.  Slots >= kv_len[b] + N are
+ *                                    never read into a result (their values
+ *                                    may be anything, including NaN).
+ *   kv_len    int32 [B]              prefix length of each sequence.
+ *   anc_mask  uint64 [B, N, W]       from tv_tree_build.
+ *   scale     softmax scale; 0 selects 1/sqrt(D).
+ *   out       bf16 [B, N, Hq, D] out
+ *   lse       float [B, N, Hq]   out natural-log normaliser log(sum_j exp(s_j));
+ *                                    may be NULL.
+ *   status    int32 [B] out          0, or TV_ERR_INVALID_ARG when kv_len[b] < 0
+ *                                    or kv_len[b] + N > Lcap (outputs zeroed);
+ *                                    may be NULL.
+ *   workspace zero-filled, >= tv_attn_workspace_size(B, N, Hq, Hkv, D, Lcap) bytes.
+ * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= TV_MAX_NODES; Lcap >= N.
+ */
+size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap);
+tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
+                         const int32_t* kv_len, const uint64_t* anc_mask, int B, int N,
+                         int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,
+                         float* lse, int32_t* status, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/*
+ * tv_accept_greedy -- greedy acceptance over a verified tree.
+ * (OPT-Tree §2: under greedy sampling the longest branch matching the target
+ * model's highest-probability sequence is accepted; GOOSE §2C: unified greedy
+ * walk over the tree.)
+ *
+ *   logits     float [B, N, V]  target logits; row i scores i's children.
+ *   tokens     int32 [B, N]     draft token of each node (node 0's is unused).
+ *   parent     int32 [B, N]     tree; depth int32 [B, N] from tv_tree_build.
+ *   argmax     int32 [B, N] out first index of the row maximum (ties -> lowest).
+ *   accept_len int32 [B] out    accepted draft tokens = depth[end].
+ *   end_node   int32 [B] out    deepest node whose whole root path matches
+ *                               (tokens[c] == argmax[parent[c]] on every edge);
+ *                               ties -> lowest node index.
+ *   path       int32 [B, N] out path[d] = the depth-d node on root..end, -1 after.
+ *   bonus      int32 [B] out    argmax[end]: the target's own next token.
+ *   status     int32 [B] out    0, TV_ERR_INVALID_TREE (parent/depth
+ *                               inconsistent) or TV_ERR_INVALID_TOKEN.
+ *   workspace  zero-filled, >= tv_accept_greedy_workspace_size(B, N, V) bytes.
+ * Logits must be finite.  V >= 1.
+ */
+size_t tv_accept_greedy_workspace_size(int B, int N, int V);
+tv_status tv_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* parent,
+                           const int32_t* depth, int B, int N, int V, int32_t* argmax,
+                           int32_t* accept_len, int32_t* end_node, int32_t* path,
+                           int32_t* bonus, int32_t* status, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tv_accept_sample -- stochastic (lossless) acceptance over a verified tree.
+ * (Speculative Decoding concept page, "The protocol" step 3: accept a draft
+ * token x with probability min(1, p(x)/q(x)); on rejection resample from the
+ * normalised (p - q)+; the output is distributed exactly as the target.)
+ *
+ * p = softmax(p_logits / T), q = softmax(q_logits / T) per node row.  Walk
+ * from the root with r = p_root: test the children of the current node in
+ * ascending index; child c with token x is accepted iff u < r(x) / q(x)
+ * (always when q(x) = 0); accepting descends to c with r = p_c; a rejection
+ * replaces r by (r - q)+ / sum((r - q)+) (kept when that sum is not positive).
+ * When all children are rejected out_token is drawn from r; at a leaf it is
+ * drawn from p_leaf (the bonus token).  Draws are inverse-CDF in ascending
+ * token order.
+ *
+ * Random numbers: Philox4x64-10 (Salmon et al., "Parallel Random Numbers:
+ * As Easy as 1, 2, 3", SC'11), key (seed, 0), counter (offset, b, node,
+ * purpose << 32 | ordinal) with purpose 0 = accept test of the ordinal-th
+ * child, 1 = the final draw; u = (first output word >> 11) * 2^-53.
+ * (seed, offset) fully determine the result: advance offset between steps.
+ *
+ *   p_logits, q_logits float [B, N, V]; tokens, parent, depth int32 [B, N].
+ *   temperature > 0.
+ *   accept_len, end_node, out_token int32 [B] out; path int32 [B, N] out;
+ *   status int32 [B] out (as tv_accept_greedy).
+ *   workspace >= tv_accept_sample_workspace_size(B, N, V) bytes (any content).
+ */
+size_t tv_accept_sample_workspace_size(int B, int N, int V);
+tv_status tv_accept_sample(const float* p_logits, const float* q_logits,
+                           const int32_t* tokens, const int32_t* parent,
+                           const int32_t* depth, int B, int N, int V, float temperature,
+                           uint64_t seed, uint64_t offset, int32_t* accept_len,
+                           int32_t* end_node, int32_t* path, int32_t* out_token,
+                           int32_t* status, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/*
+ * tv_expand_gated -- one layer of TALON tree expansion.
+ * (TALON: confidence-aware speculative decoding with adaptive token trees,
+ * §5.1 token budget B = maximum nodes in the tree; §5.2.2 layer 1 is the
+ * Top-K of the root's draft distribution; §5.2.1 deeper layers: candidate
+ * pool = all children of the frontier, path score s(c) = product of draft
+ * probabilities, anchor = max s, keep s >= alpha * s_anchor, and when more
+ * survive than the remaining budget keep the highest-scoring ones.)
+ *
+ *   draft_logits      float [F, V]  draft logits of the F frontier nodes.
+ *   frontier_node     int32 [F]     their node ids (ascending).
+ *   frontier_logscore float [F]     their log path scores (root: 0).
+ *   layer             1 (Top-K of the single root row, F must be 1) or >= 2.
+ *   topk, alpha       K (layer 1) and the gate 0 < alpha <= 1 (layers >= 2).
+ *   budget            maximum nodes in the tree, counting the root.
+ *   tree_parent, tree_token int32 [budget], tree_logscore float [budget]:
+ *                     the kept candidates are appended at ids n_nodes.. in
+ *                     (parent asc, score desc, token asc) order; ties in the
+ *                     budget cut go to (parent asc, token asc).
+ *   n_nodes           int32 [1], device, in/out: nodes in the tree.
+ *   workspace         >= tv_expand_workspace_size(F, V) bytes (any content).
+ * Scores are compared in fp64 (log domain) from fp32 logits.
+ */
+size_t tv_expand_workspace_size(int F, int V);
+tv_status tv_expand_gated(const float* draft_logits, const int32_t* frontier_node,
+                          const float* frontier_logscore, int F, int V, int layer, int topk,
+                          float alpha, int budget, int32_t* tree_parent, int32_t* tree_token,
+                          float* tree_logscore, int32_t* n_nodes, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H_ */

@@ -1,0 +1,77 @@
+"""Loading libtreeverify.so and declaring its C signatures for ctypes."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH
+
+TV_OK = 0
+TV_ERR_INVALID_ARG = 1
+TV_ERR_INVALID_TREE = 2
+TV_ERR_UNSUPPORTED = 3
+TV_ERR_CUDA = 4
+TV_ERR_TIMEOUT = 5
+TV_ERR_INVALID_TOKEN = 6
+TV_ERR_WORKSPACE = 7
+TV_MAX_NODES = 512
+
+
+class TVError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libtreeverify.so not found at {LIB_PATH}; build it first "
+        "(python -c 'import __graft_entry__ as g; g.build()' or "
+        "python speculative_decoding_tree_tv_gb300/_build.py)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_U64 = ctypes.c_uint64
+
+_SIGS = {
+    "tv_status_string": (ctypes.c_char_p, [_I]),
+    "tv_version": (_I, []),
+    "tv_workspace_clear": (_I, [_P, _SZ, _P]),
+    "tv_tree_build": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "tv_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "tv_attn_verify": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ,
+                            _P]),
+    "tv_accept_greedy_workspace_size": (_SZ, [_I, _I, _I]),
+    "tv_accept_greedy": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tv_accept_sample_workspace_size": (_SZ, [_I, _I, _I]),
+    "tv_accept_sample": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _U64, _U64, _P, _P, _P, _P, _P,
+                              _P, _SZ, _P]),
+    "tv_expand_workspace_size": (_SZ, [_I, _I]),
+    "tv_expand_gated": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+}
+
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def status_string(code: int) -> str:
+    return lib.tv_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(lib.tv_version())
+
+
+def check(fn: str, code: int) -> None:
+    if code != TV_OK:
+        raise TVError(fn, code)

@@ -1,0 +1,233 @@
+"""Torch-tensor front end of libtreeverify (argument marshalling only)."""
+from __future__ import annotations
+
+from typing import Callable, Optional
+
+import torch
+
+from ._lib import TV_MAX_NODES, check, lib
+
+__all__ = ["tree_build", "attn_verify", "accept_greedy", "accept_sample", "expand_gated",
+           "expand_tree", "workspace", "attn_workspace_size", "greedy_workspace_size",
+           "sample_workspace_size", "expand_workspace_size"]
+
+_workspaces: dict = {}
+
+
+def workspace(name: str, nbytes: int, device: torch.device) -> torch.Tensor:
+    """A zero-filled scratch buffer cached per (device, name), grown on demand.
+
+    The library returns zero-filled workspaces zero-filled, so a cached buffer
+    can be reused by the next call on the same stream."""
+    key = (torch.device(device), name)
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    return buf
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def attn_workspace_size(B, N, Hq, Hkv, D, Lcap) -> int:
+    return int(lib.tv_attn_workspace_size(B, N, Hq, Hkv, D, Lcap))
+
+
+def greedy_workspace_size(B, N, V) -> int:
+    return int(lib.tv_accept_greedy_workspace_size(B, N, V))
+
+
+def sample_workspace_size(B, N, V) -> int:
+    return int(lib.tv_accept_sample_workspace_size(B, N, V))
+
+
+def expand_workspace_size(F, V) -> int:
+    return int(lib.tv_expand_workspace_size(F, V))
+
+
+# ---------------------------------------------------------------------------
+def tree_build(parent: torch.Tensor, depth=None, anc_mask=None, status=None):
+    """parent int32 [B, N] -> (depth int32 [B,N], anc_mask int64 [B,N,W], status int32 [B]).
+
+    anc_mask holds the uint64 ancestor-or-self bitmasks (torch has no uint64;
+    the bits are the same)."""
+    _need(parent, "parent", torch.int32)
+    B, N = parent.shape
+    dev = parent.device
+    W = (N + 63) // 64
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev) if depth is None else depth
+    anc_mask = (torch.empty((B, N, W), dtype=torch.int64, device=dev)
+                if anc_mask is None else anc_mask)
+    status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+    _need(depth, "depth", torch.int32, (B, N), dev)
+    _need(anc_mask, "anc_mask", torch.int64, (B, N, W), dev)
+    _need(status, "status", torch.int32, (B,), dev)
+    check("tv_tree_build", lib.tv_tree_build(parent.data_ptr(), B, N, depth.data_ptr(),
+                                             anc_mask.data_ptr(), status.data_ptr(),
+                                             _stream(dev)))
+    return depth, anc_mask, status
+
+
+def attn_verify(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_len: torch.Tensor,
+                anc_mask: torch.Tensor, scale: float = 0.0, out=None, lse=None, status=None,
+                want_lse: bool = True, ws: Optional[torch.Tensor] = None):
+    """Tree-verify attention.  q bf16 [B,N,Hq,D]; k, v bf16 [B,Hkv,Lcap,D];
+    kv_len int32 [B]; anc_mask int64 [B,N,W].  Returns (out, lse, status)."""
+    _need(q, "q", torch.bfloat16)
+    B, N, Hq, D = q.shape
+    dev = q.device
+    _need(k, "k", torch.bfloat16, device=dev)
+    _, Hkv, Lcap, Dk = k.shape
+    if k.shape[0] != B or Dk != D:
+        raise ValueError("k must be [B, Hkv, Lcap, D]")
+    _need(v, "v", torch.bfloat16, tuple(k.shape), dev)
+    _need(kv_len, "kv_len", torch.int32, (B,), dev)
+    _need(anc_mask, "anc_mask", torch.int64, (B, N, (N + 63) // 64), dev)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if want_lse and lse is None:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, N, Hq), dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+    _need(status, "status", torch.int32, (B,), dev)
+    need = attn_workspace_size(B, N, Hq, Hkv, D, Lcap)
+    ws = workspace("attn", need, dev) if ws is None else ws
+    check("tv_attn_verify", lib.tv_attn_verify(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), kv_len.data_ptr(), anc_mask.data_ptr(), B, N,
+        Hq, Hkv, D, Lcap, float(scale), out.data_ptr(), _ptr(lse), status.data_ptr(),
+        ws.data_ptr(), ws.numel(), _stream(dev)))
+    return out, lse, status
+
+
+def accept_greedy(logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tensor,
+                  depth: torch.Tensor, outs: Optional[dict] = None,
+                  ws: Optional[torch.Tensor] = None) -> dict:
+    """Greedy acceptance.  logits float32 [B,N,V]; tokens, parent, depth int32 [B,N].
+    Returns dict(argmax, accept_len, end_node, path, bonus, status)."""
+    _need(logits, "logits", torch.float32)
+    B, N, V = logits.shape
+    dev = logits.device
+    for name, t in (("tokens", tokens), ("parent", parent), ("depth", depth)):
+        _need(t, name, torch.int32, (B, N), dev)
+    if outs is None:
+        outs = dict(argmax=torch.empty((B, N), dtype=torch.int32, device=dev),
+                    accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                    end_node=torch.empty(B, dtype=torch.int32, device=dev),
+                    path=torch.empty((B, N), dtype=torch.int32, device=dev),
+                    bonus=torch.empty(B, dtype=torch.int32, device=dev),
+                    status=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = workspace("greedy", greedy_workspace_size(B, N, V), dev) if ws is None else ws
+    check("tv_accept_greedy", lib.tv_accept_greedy(
+        logits.data_ptr(), tokens.data_ptr(), parent.data_ptr(), depth.data_ptr(), B, N, V,
+        outs["argmax"].data_ptr(), outs["accept_len"].data_ptr(), outs["end_node"].data_ptr(),
+        outs["path"].data_ptr(), outs["bonus"].data_ptr(), outs["status"].data_ptr(),
+        ws.data_ptr(), ws.numel(), _stream(dev)))
+    return outs
+
+
+def accept_sample(p_logits: torch.Tensor, q_logits: torch.Tensor, tokens: torch.Tensor,
+                  parent: torch.Tensor, depth: torch.Tensor, temperature: float, seed: int,
+                  offset: int, outs: Optional[dict] = None,
+                  ws: Optional[torch.Tensor] = None) -> dict:
+    """Stochastic acceptance.  Returns dict(accept_len, end_node, path, out_token, status)."""
+    _need(p_logits, "p_logits", torch.float32)
+    B, N, V = p_logits.shape
+    dev = p_logits.device
+    _need(q_logits, "q_logits", torch.float32, (B, N, V), dev)
+    for name, t in (("tokens", tokens), ("parent", parent), ("depth", depth)):
+        _need(t, name, torch.int32, (B, N), dev)
+    if outs is None:
+        outs = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                    end_node=torch.empty(B, dtype=torch.int32, device=dev),
+                    path=torch.empty((B, N), dtype=torch.int32, device=dev),
+                    out_token=torch.empty(B, dtype=torch.int32, device=dev),
+                    status=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = workspace("sample", sample_workspace_size(B, N, V), dev) if ws is None else ws
+    check("tv_accept_sample", lib.tv_accept_sample(
+        p_logits.data_ptr(), q_logits.data_ptr(), tokens.data_ptr(), parent.data_ptr(),
+        depth.data_ptr(), B, N, V, float(temperature), int(seed) & (2**64 - 1),
+        int(offset) & (2**64 - 1), outs["accept_len"].data_ptr(), outs["end_node"].data_ptr(),
+        outs["path"].data_ptr(), outs["out_token"].data_ptr(), outs["status"].data_ptr(),
+        ws.data_ptr(), ws.numel(), _stream(dev)))
+    return outs
+
+
+def expand_gated(draft_logits: torch.Tensor, frontier_node: torch.Tensor,
+                 frontier_logscore: torch.Tensor, layer: int, topk: int, alpha: float,
+                 budget: int, tree_parent: torch.Tensor, tree_token: torch.Tensor,
+                 tree_logscore: torch.Tensor, n_nodes: torch.Tensor,
+                 ws: Optional[torch.Tensor] = None) -> None:
+    """One TALON layer; appends to the tree_* tensors and bumps n_nodes (device int32[1])."""
+    _need(draft_logits, "draft_logits", torch.float32)
+    F, V = draft_logits.shape
+    dev = draft_logits.device
+    _need(frontier_node, "frontier_node", torch.int32, (F,), dev)
+    _need(frontier_logscore, "frontier_logscore", torch.float32, (F,), dev)
+    _need(tree_parent, "tree_parent", torch.int32, device=dev)
+    _need(tree_token, "tree_token", torch.int32, device=dev)
+    _need(tree_logscore, "tree_logscore", torch.float32, device=dev)
+    _need(n_nodes, "n_nodes", torch.int32, (1,), dev)
+    if min(tree_parent.numel(), tree_token.numel(), tree_logscore.numel()) < budget:
+        raise ValueError("tree arrays must hold `budget` nodes")
+    ws = workspace("expand", expand_workspace_size(F, V), dev) if ws is None else ws
+    check("tv_expand_gated", lib.tv_expand_gated(
+        draft_logits.data_ptr(), frontier_node.data_ptr(), frontier_logscore.data_ptr(), F, V,
+        int(layer), int(topk), float(alpha), int(budget), tree_parent.data_ptr(),
+        tree_token.data_ptr(), tree_logscore.data_ptr(), n_nodes.data_ptr(), ws.data_ptr(),
+        ws.numel(), _stream(dev)))
+
+
+def expand_tree(draft_rows: Callable, root_key, child_key: Callable, topk: int, alpha: float,
+                budget: int, device, max_layers: int = 100000) -> dict:
+    """Grow a TALON tree until the budget is spent (TALON §5.1), calling the
+    drafter between layers.  draft_rows(keys) -> float32 [F, V] (host numpy or
+    torch); root_key / child_key(key, token) name tree positions for the
+    drafter.  One host round trip per layer (the new node count sizes the next
+    frontier).  Returns dict(parent, token, logscore (cpu tensors), n, layers)."""
+    dev = torch.device(device)
+    par = torch.full((budget,), -1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(budget, dtype=torch.int32, device=dev)
+    ls = torch.zeros(budget, dtype=torch.float32, device=dev)
+    node_ids = torch.arange(budget, dtype=torch.int32, device=dev)
+    n_dev = torch.ones(1, dtype=torch.int32, device=dev)
+    keys = [root_key]
+    n = 1
+    lo, hi = 0, 1          # the frontier is always the id range [lo, hi)
+    layer = 1
+    while n < budget and hi > lo and layer <= max_layers:
+        rows = draft_rows(keys[lo:hi])
+        rows = torch.as_tensor(rows, dtype=torch.float32).to(dev).contiguous()
+        expand_gated(rows, node_ids[lo:hi], ls[lo:hi], layer, topk, alpha, budget, par, tok, ls,
+                     n_dev)
+        n_new = int(n_dev.item())
+        new_par = par[n:n_new].cpu().tolist()
+        new_tok = tok[n:n_new].cpu().tolist()
+        for p, t in zip(new_par, new_tok):
+            keys.append(child_key(keys[p], t))
+        lo, hi = n, n_new
+        n = n_new
+        layer += 1
+    return dict(parent=par[:n].cpu(), token=tok[:n].cpu(), logscore=ls[:n].cpu(), n=n,
+                layers=layer - 1)

@@ -1,0 +1,143 @@
+// Shared device helpers for libtreeverify (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "treeverify.h"
+
+#define TV_CHECK_LAUNCH()                                   \
+  do {                                                      \
+    if (cudaPeekAtLastError() != cudaSuccess) {             \
+      (void)cudaGetLastError();                             \
+      return TV_ERR_CUDA;                                   \
+    }                                                       \
+  } while (0)
+
+namespace tv {
+
+constexpr int kMaxNodes = TV_MAX_NODES;
+constexpr int kMaxWords = (kMaxNodes + 63) / 64;
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Order-preserving map of a finite float to uint32 (larger float -> larger
+// key).  -0 is folded onto +0 so that the two compare equal.
+__device__ __forceinline__ uint32_t float_key(float x) {
+  uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Order-preserving map of a double to uint64.
+__device__ __forceinline__ uint64_t double_key(double x) {
+  uint64_t u = (uint64_t)__double_as_longlong(x == 0.0 ? 0.0 : x);
+  return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// (value, index) argmax combine: larger value wins, ties -> lower index.
+struct ArgMax {
+  float v;
+  int i;
+};
+__device__ __forceinline__ ArgMax argmax_combine(ArgMax a, ArgMax b) {
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgMax b;
+    b.v = __shfl_xor_sync(0xffffffffu, a.v, o);
+    b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+    a = argmax_combine(a, b);
+  }
+  return a;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ int warp_sum_i(int x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Streaming 16-byte load that does not allocate in L1.
+__device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
+  float4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Compensated (Kahan) fp32 accumulation.
+struct KahanF {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    float y = x - c;
+    float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+// Easy as 1, 2, 3", SC'11): ten rounds of two 64x64 -> 128-bit multiplies
+// with the published multipliers; the key is bumped by the published Weyl
+// increments between rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void philox4x64_10(const uint64_t ctr[4], uint64_t k0, uint64_t k1,
+                                              uint64_t out[4]) {
+  const uint64_t kMul0 = 0xD2E7470EE14C6C93ull, kMul1 = 0xCA5A826395121157ull;
+  const uint64_t kWeyl0 = 0x9E3779B97F4A7C15ull, kWeyl1 = 0xBB67AE8584CAA73Bull;
+  uint64_t a = ctr[0], b = ctr[1], c = ctr[2], d = ctr[3];
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round) {
+      k0 += kWeyl0;
+      k1 += kWeyl1;
+    }
+    const uint64_t lo_a = kMul0 * a, hi_a = __umul64hi(kMul0, a);
+    const uint64_t lo_c = kMul1 * c, hi_c = __umul64hi(kMul1, c);
+    a = hi_c ^ b ^ k0;
+    b = lo_c;
+    c = hi_a ^ d ^ k1;
+    d = lo_a;
+  }
+  out[0] = a;
+  out[1] = b;
+  out[2] = c;
+  out[3] = d;
+}
+
+// Uniform in [0, 1) for one decision of the stochastic acceptance walk.
+__device__ __forceinline__ double decision_uniform(uint64_t seed, uint64_t offset, int b, int node,
+                                                   uint32_t purpose, uint32_t ordinal) {
+  const uint64_t ctr[4] = {offset, (uint64_t)b, (uint64_t)node,
+                           ((uint64_t)purpose << 32) | ordinal};
+  uint64_t out[4];
+  philox4x64_10(ctr, seed, 0ull, out);
+  return (double)(out[0] >> 11) * (1.0 / 9007199254740992.0);
+}
+
+}  // namespace tv

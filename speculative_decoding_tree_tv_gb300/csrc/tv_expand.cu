@@ -1,0 +1,421 @@
+// tv_expand_gated: one layer of TALON's budget-driven tree expansion
+// (TALON §5.1 token budget; §5.2.2 root Top-K; §5.2.1 confidence-gated
+// expansion: candidate pool = all children of the frontier, path score
+// s(c) = prod p_d, anchor = max s, keep s >= alpha * s_anchor, and keep the
+// best-scoring ones when more survive than the remaining budget).
+//
+// Four launches, all on the caller's stream:
+//   1. stats:   per (frontier row, 8192-logit chunk) max and sum exp;
+//   2. control: per-row log-normaliser lse_v, offset off_v = logscore_v - lse_v
+//               (log s of token c in row v is off_v + logit), the anchor, and
+//               a per-row fp32 logit threshold equivalent to the fp64 gate;
+//               resets the candidate counter;
+//   3. filter:  streams the rows again and appends every (row, token) that
+//               passes the gate to a candidate list;
+//   4. select:  one CTA keeps the best `limit` candidates (radix select on
+//               order-preserving fp64 score keys, ties to the lower
+//               (parent, token)), orders them (parent asc, score desc, token
+//               asc) and appends them to the tree.
+// Scores are fp64 in the log domain; logits stay fp32.
+#include <climits>
+
+#include "tv_common.cuh"
+
+namespace tv {
+namespace {
+
+constexpr int kExpThreads = 256;
+constexpr int kExpChunk = 8192;
+constexpr int kSelThreads = 1024;
+constexpr int kMaxBudget = 2048;
+constexpr int kTieCap = 1024;
+
+struct ExpPartial {
+  double s;
+  float m;
+  float pad;
+};
+struct ExpRow {
+  double off;   // logscore_v - lse_v
+  float thr;    // smallest fp32 logit that passes the gate in this row
+  float pad;
+};
+struct ExpCtl {
+  int count;   // candidates appended by the filter
+  int limit;   // how many may be kept
+  int n0;      // nodes in the tree before this layer
+  int pad;
+};
+
+struct ExpWs {
+  ExpCtl* ctl;
+  ExpRow* rows;
+  ExpPartial* part;
+  unsigned long long* list;  // (row << 32) | token
+};
+
+__host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, size_t* part_off,
+                                              size_t* list_off) {
+  const int chunks = (V + kExpChunk - 1) / kExpChunk;
+  size_t o = align_up(sizeof(ExpCtl), 256);
+  *rows_off = o;
+  o += align_up((size_t)F * sizeof(ExpRow), 256);
+  *part_off = o;
+  o += align_up((size_t)F * chunks * sizeof(ExpPartial), 256);
+  *list_off = o;
+  o += align_up((size_t)F * V * sizeof(unsigned long long), 256);
+  return o;
+}
+
+__global__ void __launch_bounds__(kExpThreads)
+exp_stats_kernel(const float* __restrict__ logits, int V, int chunks, ExpPartial* __restrict__ part) {
+  const int row = blockIdx.y;
+  const float* x = logits + (size_t)row * V;
+  const int start = blockIdx.x * kExpChunk;
+  const int stop = min(V, start + kExpChunk);
+  const int tid = threadIdx.x;
+  constexpr int kPer = kExpChunk / kExpThreads;
+  float a[kPer];
+  if ((V & 3) == 0) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+#pragma unroll
+    for (int u = 0; u < kPer / 4; ++u) {
+      const int e = start + 4 * (tid + u * kExpThreads);
+      const float4 f = (e < stop) ? ld_stream_f4(x4 + (e >> 2))
+                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      a[4 * u + 0] = f.x;
+      a[4 * u + 1] = f.y;
+      a[4 * u + 2] = f.z;
+      a[4 * u + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = start + tid + u * kExpThreads;
+      a[u] = (e < stop) ? __ldg(x + e) : -INFINITY;
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) m = fmaxf(m, a[u]);
+  __shared__ float s_m[kExpThreads / 32];
+  __shared__ double s_s[kExpThreads / 32];
+  m = warp_max(m);
+  if ((tid & 31) == 0) s_m[tid >> 5] = m;
+  __syncthreads();
+  m = s_m[0];
+#pragma unroll
+  for (int w = 1; w < kExpThreads / 32; ++w) m = fmaxf(m, s_m[w]);
+  float s = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) s += (a[u] == -INFINITY) ? 0.0f : expf(a[u] - m);
+  const double sd = warp_sum_d((double)s);
+  if ((tid & 31) == 0) s_s[tid >> 5] = sd;
+  __syncthreads();
+  if (tid == 0) {
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < kExpThreads / 32; ++w) tot += s_s[w];
+    part[(size_t)row * chunks + blockIdx.x] = ExpPartial{tot, m, 0.0f};
+  }
+}
+
+// Smallest fp32 value >= x (x finite).
+__device__ __forceinline__ float float_ceil_of(double x) {
+  float f = (float)x;
+  if ((double)f < x) f = nextafterf(f, INFINITY);
+  return f;
+}
+
+__global__ void __launch_bounds__(kExpThreads)
+exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunks, int layer,
+                   int topk, float alpha, int budget, const int32_t* __restrict__ n_nodes,
+                   ExpWs ws) {
+  __shared__ unsigned long long s_anchor;
+  __shared__ double s_m_row[kMaxBudget];
+  const int tid = threadIdx.x;
+  if (tid == 0) s_anchor = 0ull;
+  __syncthreads();
+  // per row: lse, offset, best score (row max); anchor = max best score
+  for (int v = tid; v < F; v += kExpThreads) {
+    const ExpPartial* p = ws.part + (size_t)v * chunks;
+    float m = -INFINITY;
+    for (int c = 0; c < chunks; ++c) m = fmaxf(m, p[c].m);
+    double s = 0.0;
+    for (int c = 0; c < chunks; ++c) s += p[c].s * exp((double)p[c].m - (double)m);
+    const double off = (double)frontier_logscore[v] - ((double)m + log(s));
+    ws.rows[v].off = off;
+    s_m_row[v] = (double)m;
+    atomicMax(&s_anchor, double_key(off + (double)m));
+  }
+  __syncthreads();
+  const int n0 = *n_nodes;
+  const int remaining = budget - n0;
+  int limit = remaining > 0 ? remaining : 0;
+  if (layer == 1) limit = min(limit, topk);
+  // decode the anchor back to a double
+  const unsigned long long ak = s_anchor;
+  const unsigned long long au = (ak & 0x8000000000000000ull) ? (ak & 0x7fffffffffffffffull) : ~ak;
+  const double anchor = __longlong_as_double((long long)au);
+  const double log_alpha = log((double)alpha);
+  for (int v = tid; v < F; v += kExpThreads) {
+    float thr;
+    if (layer == 1 || limit == 0) {
+      thr = limit == 0 ? INFINITY : -INFINITY;
+    } else {
+      // s = off_v + logit >= log(alpha) + anchor  <=>  logit >= m_v + (log(alpha) - d_v),
+      // d_v = anchor - best_v >= 0, exactly 0 in the anchor's own row
+      const double best = ws.rows[v].off + s_m_row[v];
+      const double d = anchor - best;
+      thr = float_ceil_of(s_m_row[v] + (log_alpha - d));
+    }
+    ws.rows[v].thr = thr;
+  }
+  if (tid == 0) *ws.ctl = ExpCtl{0, limit, n0, 0};
+}
+
+__global__ void __launch_bounds__(kExpThreads)
+exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
+  const int row = blockIdx.y;
+  const float thr = ws.rows[row].thr;
+  if (!(thr < INFINITY)) return;
+  const float* x = logits + (size_t)row * V;
+  const int start = blockIdx.x * kExpChunk;
+  const int stop = min(V, start + kExpChunk);
+  const int lane = threadIdx.x & 31;
+  for (int base = start; base < stop; base += kExpThreads) {
+    const int e = base + threadIdx.x;
+    const bool pass = (e < stop) && (__ldg(x + e) >= thr);
+    const unsigned int bal = __ballot_sync(0xffffffffu, pass);
+    if (bal == 0u) continue;
+    int slot0 = 0;
+    if (lane == 0) slot0 = atomicAdd(&ws.ctl->count, __popc(bal));
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    if (pass) {
+      const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+      ws.list[slot] = ((unsigned long long)row << 32) | (unsigned int)e;
+    }
+  }
+}
+
+struct Kept {
+  unsigned long long key;  // order-preserving score key
+  int row;
+  int token;
+};
+
+// order of the output: row (parent) asc, score desc, token asc
+__device__ __forceinline__ bool out_before(const Kept& a, const Kept& b) {
+  if (a.row != b.row) return a.row < b.row;
+  if (a.key != b.key) return a.key > b.key;
+  return a.token < b.token;
+}
+
+__device__ void bitonic_sort_kept(Kept* s, int n_pow2) {
+  for (int k = 2; k <= n_pow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const bool swap = up ? out_before(s[ixj], s[i]) : out_before(s[i], s[ixj]);
+          if (swap) {
+            const Kept t = s[i];
+            s[i] = s[ixj];
+            s[ixj] = t;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ void bitonic_sort_u64(unsigned long long* s, int n_pow2) {
+  for (int k = 2; k <= n_pow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const bool swap = up ? (s[ixj] < s[i]) : (s[i] < s[ixj]);
+          if (swap) {
+            const unsigned long long t = s[i];
+            s[i] = s[ixj];
+            s[ixj] = t;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned long long cand_key(const float* __restrict__ logits, int V,
+                                                       const ExpRow* rows, unsigned long long c) {
+  const int row = (int)(c >> 32), tok = (int)(c & 0xffffffffu);
+  return double_key(rows[row].off + (double)__ldg(logits + (size_t)row * V + tok));
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __restrict__ frontier_node,
+                  int32_t* __restrict__ tree_parent, int32_t* __restrict__ tree_token,
+                  float* __restrict__ tree_logscore, int32_t* __restrict__ n_nodes, ExpWs ws) {
+  __shared__ Kept s_kept[kMaxBudget];
+  __shared__ unsigned long long s_ties[kTieCap];
+  __shared__ unsigned int s_hist[256];
+  __shared__ int s_n, s_nt, s_digit, s_need;
+  __shared__ unsigned long long s_min;
+  const int tid = threadIdx.x;
+  const ExpCtl ctl = *ws.ctl;
+  const int count = ctl.count, limit = ctl.limit;
+  if (tid == 0) {
+    s_n = 0;
+    s_nt = 0;
+  }
+  __syncthreads();
+  if (count <= limit) {
+    for (int j = tid; j < count; j += kSelThreads) {
+      const unsigned long long c = ws.list[j];
+      s_kept[j] = Kept{cand_key(logits, V, ws.rows, c), (int)(c >> 32), (int)(c & 0xffffffffu)};
+    }
+    if (tid == 0) s_n = count;
+  } else {
+    // radix select: T = the limit-th largest key, need = how many keys == T to take
+    unsigned long long prefix = 0ull, mask = 0ull;
+    int need = limit;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kSelThreads) s_hist[i] = 0u;
+      __syncthreads();
+      for (int j = tid; j < count; j += kSelThreads) {
+        const unsigned long long k = cand_key(logits, V, ws.rows, ws.list[j]);
+        if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255ull], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int cum = 0;
+        for (int d = 255; d >= 0; --d) {
+          if (cum + (int)s_hist[d] >= need) {
+            s_digit = d;
+            s_need = need - cum;
+            break;
+          }
+          cum += (int)s_hist[d];
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)s_digit << shift;
+      mask |= 0xffull << shift;
+      need = s_need;
+      __syncthreads();
+    }
+    const unsigned long long T = prefix;
+    for (int j = tid; j < count; j += kSelThreads) {
+      const unsigned long long c = ws.list[j];
+      const unsigned long long k = cand_key(logits, V, ws.rows, c);
+      if (k > T) {
+        const int slot = atomicAdd(&s_n, 1);
+        s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
+      } else if (k == T) {
+        const int slot = atomicAdd(&s_nt, 1);
+        if (slot < kTieCap) s_ties[slot] = c;
+      }
+    }
+    __syncthreads();
+    const int n_gt = s_n, n_ties = s_nt;
+    if (n_ties <= kTieCap) {
+      // take the `need` lowest (row, token) among the ties
+      int p2 = 1;
+      while (p2 < n_ties) p2 <<= 1;
+      for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
+      __syncthreads();
+      bitonic_sort_u64(s_ties, p2);
+      for (int i = tid; i < need; i += kSelThreads)
+        s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
+    } else {
+      // very many exact ties: pick them one by one in (row, token) order
+      unsigned long long last = 0ull;
+      bool first = true;
+      for (int r = 0; r < need; ++r) {
+        if (tid == 0) s_min = ~0ull;
+        __syncthreads();
+        unsigned long long mine = ~0ull;
+        for (int j = tid; j < count; j += kSelThreads) {
+          const unsigned long long c = ws.list[j];
+          if ((first || c > last) && c < mine && cand_key(logits, V, ws.rows, c) == T) mine = c;
+        }
+        atomicMin(&s_min, mine);
+        __syncthreads();
+        last = s_min;
+        first = false;
+        if (tid == 0) s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
+        __syncthreads();
+      }
+    }
+    if (tid == 0) s_n = limit;
+  }
+  __syncthreads();
+  const int k = s_n;
+  int p2 = 1;
+  while (p2 < k) p2 <<= 1;
+  for (int i = k + tid; i < p2; i += kSelThreads) s_kept[i] = Kept{0ull, INT_MAX, INT_MAX};
+  __syncthreads();
+  bitonic_sort_kept(s_kept, p2);
+  const int n0 = ctl.n0;
+  for (int i = tid; i < k; i += kSelThreads) {
+    const Kept c = s_kept[i];
+    tree_parent[n0 + i] = frontier_node[c.row];
+    tree_token[n0 + i] = c.token;
+    tree_logscore[n0 + i] = (float)(ws.rows[c.row].off + (double)__ldg(logits + (size_t)c.row * V + c.token));
+  }
+  if (tid == 0) *n_nodes = n0 + k;
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" size_t tv_expand_workspace_size(int F, int V) {
+  if (F <= 0 || V <= 0) return 256;
+  size_t a, b, c;
+  return tv::exp_offsets(F, V, &a, &b, &c);
+}
+
+extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* frontier_node,
+                                     const float* frontier_logscore, int F, int V, int layer,
+                                     int topk, float alpha, int budget, int32_t* tree_parent,
+                                     int32_t* tree_token, float* tree_logscore, int32_t* n_nodes,
+                                     void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (F < 0 || V < 1 || layer < 1 || budget < 1) return TV_ERR_INVALID_ARG;
+  if (budget > tv::kMaxBudget || F > tv::kMaxBudget) return TV_ERR_UNSUPPORTED;
+  if (layer == 1 && (F != 1 || topk < 1)) return TV_ERR_INVALID_ARG;
+  if (layer >= 2 && !(alpha > 0.0f && alpha <= 1.0f)) return TV_ERR_INVALID_ARG;
+  if (F == 0) return TV_OK;
+  if (!draft_logits || !frontier_node || !frontier_logscore || !tree_parent || !tree_token ||
+      !tree_logscore || !n_nodes)
+    return TV_ERR_INVALID_ARG;
+  if ((size_t)F * V >= (1ull << 31)) return TV_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < tv_expand_workspace_size(F, V)) return TV_ERR_WORKSPACE;
+  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(draft_logits) & 15)) return TV_ERR_INVALID_ARG;
+  size_t rows_off, part_off, list_off;
+  tv::exp_offsets(F, V, &rows_off, &part_off, &list_off);
+  char* base = static_cast<char*>(workspace);
+  tv::ExpWs ws;
+  ws.ctl = reinterpret_cast<tv::ExpCtl*>(base);
+  ws.rows = reinterpret_cast<tv::ExpRow*>(base + rows_off);
+  ws.part = reinterpret_cast<tv::ExpPartial*>(base + part_off);
+  ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
+  const int chunks = tv::ceil_div(V, tv::kExpChunk);
+  dim3 grid(chunks, F);
+  tv::exp_stats_kernel<<<grid, tv::kExpThreads, 0, stream>>>(draft_logits, V, chunks, ws.part);
+  TV_CHECK_LAUNCH();
+  tv::exp_control_kernel<<<1, tv::kExpThreads, 0, stream>>>(frontier_logscore, F, chunks, layer,
+                                                            topk, alpha, budget, n_nodes, ws);
+  TV_CHECK_LAUNCH();
+  tv::exp_filter_kernel<<<grid, tv::kExpThreads, 0, stream>>>(draft_logits, V, ws);
+  TV_CHECK_LAUNCH();
+  tv::exp_select_kernel<<<1, tv::kSelThreads, 0, stream>>>(draft_logits, V, frontier_node,
+                                                           tree_parent, tree_token, tree_logscore,
+                                                           n_nodes, ws);
+  TV_CHECK_LAUNCH();
+  return TV_OK;
+}

@@ -1,0 +1,63 @@
+// tv_tree_build: parent[] -> depth[] and ancestor-or-self bitmasks, the tree
+// attention mask of OPT-Tree §2 (a node attends to its ancestors and itself).
+#include "tv_common.cuh"
+
+namespace tv {
+namespace {
+
+constexpr int kTreeThreads = 256;
+
+// One CTA per sequence.  Each thread walks its nodes up to the root; the
+// walk length is the node depth (<= N - 1), and N <= 512, so the whole tree
+// costs at most N * depth shared-memory steps spread over 256 threads.
+__global__ void __launch_bounds__(kTreeThreads)
+tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __restrict__ depth,
+                  uint64_t* __restrict__ anc_mask, int32_t* __restrict__ status) {
+  __shared__ int32_t s_par[kMaxNodes];
+  __shared__ uint64_t s_anc[kMaxNodes * kMaxWords];
+  const int b = blockIdx.x;
+  const int32_t* par = parent + (size_t)b * N;
+  int32_t* dep = depth + (size_t)b * N;
+  uint64_t* anc = anc_mask + (size_t)b * N * W;
+
+  int bad = 0;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int p = par[i];
+    s_par[i] = p;
+    bad |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
+  }
+  for (int w = threadIdx.x; w < N * W; w += blockDim.x) s_anc[w] = 0ull;
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    for (int i = threadIdx.x; i < N; i += blockDim.x) dep[i] = -1;
+    for (int w = threadIdx.x; w < N * W; w += blockDim.x) anc[w] = 0ull;
+    if (threadIdx.x == 0) status[b] = TV_ERR_INVALID_TREE;
+    return;
+  }
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    int d = -1;
+    uint64_t* row = s_anc + i * W;
+    for (int x = i; x >= 0; x = s_par[x]) {
+      row[x >> 6] |= 1ull << (x & 63);
+      ++d;
+    }
+    dep[i] = d;
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < N * W; w += blockDim.x) anc[w] = s_anc[w];
+  if (threadIdx.x == 0) status[b] = TV_OK;
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
+                                   uint64_t* anc_mask, int32_t* status, cudaStream_t stream) {
+  if (B < 0 || N < 1 || N > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
+  if (B == 0) return TV_OK;
+  if (!parent || !depth || !anc_mask || !status) return TV_ERR_INVALID_ARG;
+  const int W = tv::ceil_div(N, 64);
+  tv::tree_build_kernel<<<B, tv::kTreeThreads, 0, stream>>>(parent, N, W, depth, anc_mask, status);
+  TV_CHECK_LAUNCH();
+  return TV_OK;
+}

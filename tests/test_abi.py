@@ -1,0 +1,91 @@
+"""The C ABI: libtreeverify.so loads without a GPU, exports every function
+declared in include/treeverify.h, and rejects bad host-side arguments before
+launching anything (these calls never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treeverify.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def tvlib():
+    from speculative_decoding_tree_tv_gb300 import _build
+    _build.build()
+    import speculative_decoding_tree_tv_gb300 as tv
+    return tv
+
+
+def test_header_declares_the_five_steps():
+    names = declared_functions()
+    for f in ("tv_tree_build", "tv_attn_verify", "tv_accept_greedy", "tv_accept_sample",
+              "tv_expand_gated"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(tvlib):
+    lib = ctypes.CDLL(tvlib.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(tvlib):
+    assert tvlib.status_string(0) == "TV_OK"
+    assert tvlib.status_string(2) == "TV_ERR_INVALID_TREE"
+    assert tvlib.status_string(99) == "TV_ERR_UNKNOWN"
+    assert tvlib.version() >= 100
+
+
+def test_workspace_sizes_are_positive(tvlib):
+    assert tvlib.greedy_workspace_size(1, 60, 128256) >= 60 * 8
+    assert tvlib.sample_workspace_size(16, 64, 128256) >= 2 * 16 * 64 * 16
+    assert tvlib.expand_workspace_size(511, 32000) >= 511 * 32000 * 8
+    assert tvlib.attn_workspace_size(1, 60, 32, 8, 128, 2108) > 0
+
+
+def test_host_side_argument_errors_launch_nothing(tvlib):
+    lib = tvlib.lib
+    dummy = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails its checks first
+    # N = 0, N > 512
+    assert lib.tv_tree_build(dummy, 1, 0, dummy, dummy, dummy, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_tree_build(dummy, 1, 513, dummy, dummy, dummy, None) == tvlib.TV_ERR_INVALID_ARG
+    # B = 0 is a no-op
+    assert lib.tv_tree_build(dummy, 0, 4, dummy, dummy, dummy, None) == tvlib.TV_OK
+    # unsupported head_dim, Hq % Hkv != 0, negative scale
+    args = [dummy] * 5
+    assert lib.tv_attn_verify(*args, 1, 4, 8, 8, 96, 64, 0.0, dummy, None, None, dummy, 256,
+                              None) == tvlib.TV_ERR_UNSUPPORTED
+    assert lib.tv_attn_verify(*args, 1, 4, 8, 3, 64, 64, 0.0, dummy, None, None, dummy, 256,
+                              None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_attn_verify(*args, 1, 4, 8, 8, 64, 64, -1.0, dummy, None, None, dummy, 256,
+                              None) == tvlib.TV_ERR_INVALID_ARG
+    # greedy: workspace too small
+    assert lib.tv_accept_greedy(dummy, dummy, dummy, dummy, 2, 8, 100, dummy, dummy, dummy,
+                                dummy, dummy, dummy, dummy, 8, None) == tvlib.TV_ERR_WORKSPACE
+    # sample: temperature 0
+    assert lib.tv_accept_sample(dummy, dummy, dummy, dummy, dummy, 1, 4, 10, 0.0, 1, 0, dummy,
+                                dummy, dummy, dummy, dummy, dummy, 1 << 20,
+                                None) == tvlib.TV_ERR_INVALID_ARG
+    # expand: layer 1 needs exactly one frontier row; alpha out of range
+    assert lib.tv_expand_gated(dummy, dummy, dummy, 2, 10, 1, 3, 0.3, 20, dummy, dummy, dummy,
+                               dummy, dummy, 1 << 20, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_expand_gated(dummy, dummy, dummy, 2, 10, 2, 3, 1.5, 20, dummy, dummy, dummy,
+                               dummy, dummy, 1 << 20, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_expand_gated(dummy, dummy, dummy, 1, 10, 1, 3, 0.3, 5000, dummy, dummy, dummy,
+                               dummy, dummy, 1 << 20, None) == tvlib.TV_ERR_UNSUPPORTED
+
+
+def test_binding_refuses_cpu_tensors(tvlib):
+    import torch
+    parent = torch.tensor([[-1, 0]], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        tvlib.tree_build(parent)

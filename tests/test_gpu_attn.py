@@ -1,0 +1,118 @@
+"""GPU parity: tv_attn_verify against the fp64 oracle (OPT-Tree §2: one target
+pass over the whole tree under the tree attention mask; GQA kv head h / G).
+
+Tolerance: bf16 inputs with fp32 accumulation and a bf16 output, compared with
+fp64: max-abs <= 3e-2 and relative L2 <= 1e-2 per case; the natural-log
+normaliser (fp32 output) within 2e-3 absolute."""
+import numpy as np
+import pytest
+import torch
+
+from workloads import gen
+
+from _gpu_util import bf16, bf16_np, case_tensors, check_attn, dev, i32, np_
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tv():
+    import speculative_decoding_tree_tv_gb300 as m
+    return m
+
+
+def run_attn(tv, case, scale=0.0, k=None, v=None):
+    t = case_tensors(case)
+    depth, anc, _ = tv.tree_build(t["parent"])
+    out, lse, status = tv.attn_verify(t["q"], t["k"] if k is None else k,
+                                      t["v"] if v is None else v, t["kv_len"], anc, scale)
+    torch.cuda.synchronize()
+    return bf16_np(out), np_(lse), np_(status)
+
+
+def full_check(tv, oracle_mod, case, what, scale=0.0):
+    out, lse, status = run_attn(tv, case, scale)
+    ref, ref_lse = oracle_mod.attn_all(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq,
+                                       case.Hkv, scale)
+    assert (status == 0).all()
+    check_attn(out, ref, what)
+    np.testing.assert_allclose(lse, ref_lse, atol=2e-3, rtol=0)
+
+
+def sampled_check(tv, oracle_mod, case, n_rows, seed, what):
+    out, lse, status = run_attn(tv, case)
+    r = gen.rng(seed)
+    rows = np.stack([r.integers(0, case.B, n_rows), r.integers(0, case.N, n_rows),
+                     r.integers(0, case.Hq, n_rows)], axis=1)
+    # always include the deepest node and the root of sequence 0
+    depth = gen.depth_of(case.parent[0])
+    rows[0] = (0, int(np.argmax(depth)), 0)
+    rows[1] = (0, 0, case.Hq - 1)
+    ref, ref_lse = oracle_mod.attn_rows(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq,
+                                        case.Hkv, rows)
+    assert (status == 0).all()
+    got = out[rows[:, 0], rows[:, 1], rows[:, 2]]
+    check_attn(got, ref, what)
+    np.testing.assert_allclose(lse[rows[:, 0], rows[:, 1], rows[:, 2]], ref_lse, atol=2e-3)
+
+
+def test_config1_tiny(tv, oracle_mod):
+    full_check(tv, oracle_mod, gen.config1(), "config1")
+
+
+@pytest.mark.parametrize("seed,B,N,L,Hq,Hkv,D,tree", [
+    (1, 1, 1, 0, 8, 8, 64, "chain"),          # a single node with no prefix
+    (2, 1, 37, 300, 8, 2, 128, "random"),     # ragged prefix tail, GQA 4
+    (3, 2, 64, (1, 700), 16, 2, 64, "random"),  # ragged batch, GQA 8
+    (4, 1, 65, 129, 4, 4, 128, "chain"),      # chain tree crossing a mask word
+    (5, 3, 20, (0, 260), 32, 8, 128, "star"),
+    (6, 1, 130, 1000, 4, 1, 64, "random"),
+    (7, 1, 60, 2048, 32, 8, 128, "spine60"),  # the Llama-3-8B spine case, full size
+])
+def test_attention_full(tv, oracle_mod, seed, B, N, L, Hq, Hkv, D, tree):
+    case = gen.make_case(seed, B=B, N=N, L=L, Hq=Hq, Hkv=Hkv, D=D, V=max(64, N), tree=tree,
+                         max_depth=12)
+    full_check(tv, oracle_mod, case, f"case{seed}")
+
+
+def test_explicit_scale(tv, oracle_mod):
+    case = gen.make_case(20, B=1, N=24, L=200, Hq=8, Hkv=4, D=64, V=64)
+    full_check(tv, oracle_mod, case, "scale", scale=0.05)
+
+
+def test_unused_cache_slots_may_hold_nan(tv, oracle_mod):
+    """Slots at and beyond kv_len + N are never part of a result."""
+    case = gen.make_case(21, B=2, N=30, L=(100, 180), Hq=8, Hkv=2, D=128, V=64,
+                         Lcap=400)
+    k = case.k.copy()
+    v = case.v.copy()
+    for b in range(case.B):
+        end = case.kv_len[b] + case.N
+        k[b, :, end:] = 0x7FC0   # bf16 NaN
+        v[b, :, end:] = 0x7FC0
+    out, lse, status = run_attn(tv, case, k=bf16(k), v=bf16(v))
+    ref, ref_lse = oracle_mod.attn_all(case.q, case.k, case.v, case.kv_len, case.parent, 8, 2)
+    check_attn(out, ref, "nan-tail")
+
+
+def test_bad_kv_len_is_flagged(tv):
+    case = gen.make_case(22, B=3, N=8, L=16, Hq=4, Hkv=4, D=64, V=64)
+    case.kv_len = np.array([16, case.Lcap, -1], np.int32)
+    out, lse, status = run_attn(tv, case)
+    assert status.tolist() == [0, 1, 1]
+    assert (out[1:] == 0).all()
+
+
+def test_config4_ragged_batch_sampled(tv, oracle_mod):
+    sampled_check(tv, oracle_mod, gen.config4(V=8), 48, 5, "config4")
+
+
+def test_config5_long_context_sampled(tv, oracle_mod):
+    sampled_check(tv, oracle_mod, gen.config5(256, V=5000), 24, 6, "config5")
+
+
+def test_config3_talon_tree_sampled(tv, oracle_mod):
+    d = gen.config3_drafter(1)
+    tree = oracle_mod.expand_tree(d, 10, 0.3, 512)
+    case = gen.config3_verify(tree["parent"], 1, tokens=tree["token"])
+    sampled_check(tv, oracle_mod, case, 24, 7, "config3")
