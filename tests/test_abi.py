@@ -19,8 +19,8 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def tvlib():
-    from speculative_decoding_tree_tv_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import speculative_decoding_tree_tv_gb300 as tv
     return tv
 
