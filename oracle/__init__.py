@@ -47,7 +47,7 @@ def _load():
         lib.or_attn_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, I, P, P]
         lib.or_accept_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P, P]
         lib.or_accept_sample.argtypes = [P, P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64,
-                                         ctypes.c_uint64, P, P, P, P, P, P]
+                                         ctypes.c_uint64, P, P, P, P, P, P, P]
         lib.or_expand_gated.argtypes = [P, P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, P]
         lib.or_philox4x64_10.argtypes = [P, P, P]
         lib.or_philox4x64_10.restype = None
@@ -138,12 +138,14 @@ def accept_sample(p_logits, q_logits, tokens, parent, temperature: float, seed: 
     par, pp = _c(parent, np.int32)
     r = dict(accept_len=np.zeros(B, np.int32), end_node=np.zeros(B, np.int32),
              path=np.zeros((B, N), np.int32), out_token=np.zeros(B, np.int32),
-             status=np.zeros(B, np.int32), margin=np.zeros(B, np.float64))
+             status=np.zeros(B, np.int32), margin_accept=np.zeros(B, np.float64),
+             margin_draw=np.zeros(B, np.float64))
     _check(_load().or_accept_sample(ppl, qpl, tp, pp, B, N, V, float(temperature),
                                     int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
                                     r["accept_len"].ctypes.data, r["end_node"].ctypes.data,
                                     r["path"].ctypes.data, r["out_token"].ctypes.data,
-                                    r["status"].ctypes.data, r["margin"].ctypes.data))
+                                    r["status"].ctypes.data, r["margin_accept"].ctypes.data,
+                                    r["margin_draw"].ctypes.data))
     return r
 
 

@@ -290,14 +290,15 @@ int or_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* 
 // cumulative mass exceeds u * (total mass); if rounding leaves none, the last
 // token with positive mass.
 //
-// margin[b] = smallest relative distance of any decision of tree b from its
-// threshold (accept tests: |u - ratio| / ratio; draws: distance of u*total to
-// the nearest cumulative boundary / total).
+// margin_accept[b] = smallest |u - ratio| / ratio over tree b's accept tests;
+// margin_draw[b] = distance of u * total from the nearest cumulative boundary
+// of its final draw, divided by total.
 // ---------------------------------------------------------------------------
 int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t* tokens,
                      const int32_t* parent, int B, int N, int V, float temperature,
                      uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* end_node,
-                     int32_t* path, int32_t* out_token, int32_t* status, double* margin) {
+                     int32_t* path, int32_t* out_token, int32_t* status, double* margin_accept,
+                     double* margin_draw) {
   if (B < 0 || N < 1 || V < 1 || !(temperature > 0.0f)) return ST_INVALID_ARG;
   const double T = (double)temperature;
   std::vector<double> r(V), q(V);
@@ -306,7 +307,7 @@ int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t
     const int32_t* tok = tokens + (size_t)b * N;
     for (int i = 0; i < N; ++i) path[(size_t)b * N + i] = -1;
     accept_len[b] = end_node[b] = out_token[b] = -1;
-    margin[b] = INFINITY;
+    margin_accept[b] = margin_draw[b] = INFINITY;
     if (!tree_is_valid(par, N)) { status[b] = ST_INVALID_TREE; continue; }
     bool tok_ok = true;
     for (int i = 1; i < N; ++i)
@@ -339,7 +340,7 @@ int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t
         } else {
           const double ratio = r[x] / q[x];
           acc = u < ratio;
-          if (ratio > 0.0) margin[b] = std::min(margin[b], fabs(u - ratio) / ratio);
+          if (ratio > 0.0) margin_accept[b] = std::min(margin_accept[b], fabs(u - ratio) / ratio);
         }
         if (acc) { accepted = kids[o]; break; }
         double z = 0.0;
@@ -363,7 +364,7 @@ int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t
         cum += rt;
         if (out < 0 && cum > target) {
           out = t;
-          margin[b] = std::min(margin[b], std::min(cum - target, target - before) / total);
+          margin_draw[b] = std::min(cum - target, target - before) / total;
         }
       }
       if (out < 0) out = last_pos;

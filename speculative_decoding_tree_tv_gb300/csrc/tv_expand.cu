@@ -163,11 +163,11 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
     if (layer == 1 || limit == 0) {
       thr = limit == 0 ? INFINITY : -INFINITY;
     } else {
-      // s = off_v + logit >= log(alpha) + anchor  <=>  logit >= m_v + (log(alpha) - d_v),
-      // d_v = anchor - best_v >= 0, exactly 0 in the anchor's own row
+      // s = off_v + logit >= log(alpha) + anchor  <=>  logit >= m_v + (d_v + log(alpha)),
+      // d_v = anchor - best_v >= 0 (best_v = off_v + m_v), exactly 0 in the anchor's row
       const double best = ws.rows[v].off + s_m_row[v];
       const double d = anchor - best;
-      thr = float_ceil_of(s_m_row[v] + (log_alpha - d));
+      thr = float_ceil_of(s_m_row[v] + (d + log_alpha));
     }
     ws.rows[v].thr = thr;
   }

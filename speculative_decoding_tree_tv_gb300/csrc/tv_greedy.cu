@@ -43,10 +43,10 @@ greedy_kernel(const float* __restrict__ logits, const int32_t* __restrict__ toke
               int chunks, int32_t* __restrict__ argmax_out, int32_t* __restrict__ accept_len,
               int32_t* __restrict__ end_node, int32_t* __restrict__ path,
               int32_t* __restrict__ bonus, int32_t* __restrict__ status, GreedyWs ws) {
-  const int row = blockIdx.y;
+  const int row = blockIdx.x / chunks;
   const int b = row / N;
   const int tid = threadIdx.x;
-  const int start = blockIdx.x * kGreedyChunk;
+  const int start = (blockIdx.x % chunks) * kGreedyChunk;
   const int stop = min(V, start + kGreedyChunk);
   const float* x = logits + (size_t)row * V;
 
@@ -208,8 +208,7 @@ extern "C" tv_status tv_accept_greedy(const float* logits, const int32_t* tokens
   if (!logits || !tokens || !parent || !depth || !argmax || !accept_len || !end_node || !path ||
       !bonus || !status)
     return TV_ERR_INVALID_ARG;
-  if (B > 65535) return TV_ERR_UNSUPPORTED;
-  if ((size_t)B * N > 65535) return TV_ERR_UNSUPPORTED;  // grid.y
+  if ((size_t)B * N * tv::ceil_div(V, tv::kGreedyChunk) > 0x7fffffffu) return TV_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < tv_accept_greedy_workspace_size(B, N, V)) return TV_ERR_WORKSPACE;
   if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) != 0) return TV_ERR_INVALID_ARG;
   tv::GreedyWs ws;
@@ -217,7 +216,7 @@ extern "C" tv_status tv_accept_greedy(const float* logits, const int32_t* tokens
   ws.arrivals = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
                                                 tv::greedy_keys_bytes(B, N));
   const int chunks = tv::ceil_div(V, tv::kGreedyChunk);
-  dim3 grid(chunks, B * N);
+  dim3 grid(chunks * B * N);
   tv::greedy_kernel<<<grid, tv::kGreedyThreads, 0, stream>>>(
       logits, tokens, parent, depth, N, V, chunks, argmax, accept_len, end_node, path, bonus,
       status, ws);

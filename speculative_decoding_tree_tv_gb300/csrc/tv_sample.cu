@@ -31,10 +31,11 @@ struct RowPartial {
 __global__ void __launch_bounds__(kStatThreads)
 row_stats_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logits, int rows,
                  int V, int chunks, float inv_t, RowPartial* __restrict__ part) {
-  const int row = blockIdx.y;
-  const int which = blockIdx.z;  // 0: p, 1: q
+  const int row = blockIdx.x / chunks;
+  const int chunk = blockIdx.x % chunks;
+  const int which = blockIdx.y;  // 0: p, 1: q
   const float* x = (which ? q_logits : p_logits) + (size_t)row * V;
-  const int start = blockIdx.x * kStatChunk;
+  const int start = chunk * kStatChunk;
   const int stop = min(V, start + kStatChunk);
   const int tid = threadIdx.x;
   constexpr int kPer = kStatChunk / kStatThreads;  // 32 values per thread
@@ -83,7 +84,7 @@ row_stats_kernel(const float* __restrict__ p_logits, const float* __restrict__ q
     r.s = tot;
     r.m = m;
     r.pad = 0.0f;
-    part[((size_t)which * rows + row) * chunks + blockIdx.x] = r;
+    part[((size_t)which * rows + row) * chunks + chunk] = r;
   }
 }
 
@@ -320,14 +321,14 @@ extern "C" tv_status tv_accept_sample(const float* p_logits, const float* q_logi
   if (!p_logits || !q_logits || !tokens || !parent || !depth || !accept_len || !end_node ||
       !path || !out_token || !status)
     return TV_ERR_INVALID_ARG;
-  if ((size_t)B * N > 65535 || B > 2147483647 / N) return TV_ERR_UNSUPPORTED;
+  if ((size_t)B * N * tv::ceil_div(V, tv::kStatChunk) > 0x7fffffffu) return TV_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < tv_accept_sample_workspace_size(B, N, V)) return TV_ERR_WORKSPACE;
   if ((V & 3) == 0 && ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits)) & 15))
     return TV_ERR_INVALID_ARG;
   const int chunks = tv::ceil_div(V, tv::kStatChunk);
   const float inv_t = 1.0f / temperature;
   auto* part = static_cast<tv::RowPartial*>(workspace);
-  dim3 g1(chunks, B * N, 2);
+  dim3 g1(chunks * B * N, 2);
   tv::row_stats_kernel<<<g1, tv::kStatThreads, 0, stream>>>(p_logits, q_logits, B * N, V, chunks,
                                                             inv_t, part);
   TV_CHECK_LAUNCH();

