@@ -580,6 +580,13 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.tps = sp.tps;
   p.nsplit = sp.nsplit;
   p.scale_log2 = scale_log2;
+  if (sp.nsplit > 1) {
+    // the arrival counters start at zero whatever the workspace held before
+    if (cudaMemsetAsync(workspace, 0, counters_bytes(B, Hkv, sp.mtiles), stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TV_ERR_CUDA;
+    }
+  }
   dim3 grid(sp.nsplit, sp.mtiles, B * Hkv);
   attn_tc_kernel<D><<<grid, kThreads, Lay::kDyn, stream>>>(tmK, tmV, p);
   TV_CHECK_LAUNCH();
