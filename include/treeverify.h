@@ -124,8 +124,8 @@ tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
  *   status    int32 [B] out          0, or TV_ERR_INVALID_ARG when kv_len[b] < 0
  *                                    or kv_len[b] + N > Lcap (outputs zeroed);
  *                                    may be NULL.
- *   workspace >= tv_attn_workspace_size(B, N, Hq, Hkv, D, Lcap) bytes (any content;
- *             the call clears the few words it needs zeroed).
+ *   workspace unused: tv_attn_workspace_size() returns 0 and workspace may be
+ *             NULL (the split-KV merge runs in distributed shared memory).
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= TV_MAX_NODES; Lcap >= N.
  */
 size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap);

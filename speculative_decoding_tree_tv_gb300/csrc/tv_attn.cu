@@ -5,20 +5,23 @@
 //
 // One CTA owns 128 query rows of one (sequence, kv head) -- the GQA group's
 // rows (node, head) flattened as node * G + g -- and a range of 128-key tiles
-// of that kv head's key range [0, kv_len + N) (split-KV).  Warp roles:
-//   warps 0-3  softmax: one TMEM lane (= query row) per thread; load Q into
-//              shared memory, read S tiles from TMEM, apply the tree mask and
-//              the online softmax (log2 domain, lazy rescaling), write P (bf16)
-//              to shared memory, rescale O in TMEM when the running max grows;
-//   warp 4     producer: TMA loads of K and V tiles (128-byte swizzle) into a
+// of that kv head's key range [0, kv_len + N).  Warp roles (320 threads):
+//   warps 0-7  softmax, two groups of four warps.  Group h owns keys
+//              64h .. 64h+63 of every tile and runs its own online softmax
+//              (log2 domain, lazy rescaling) with its own accumulator O_h in
+//              TMEM; thread (group h, lane) = one query row = one TMEM lane.
+//              The tree mask is applied as 32-bit visibility words;
+//   warp 8     producer: TMA loads of K and V tiles (128-byte swizzle) into a
 //              two-stage ring;
-//   warp 5     MMA: S = Q K^T and O += P V with tcgen05.mma (bf16 operands
-//              from shared memory, fp32 accumulators in TMEM); zeroes V rows
-//              past the end of the key range so that stale cache slots never
-//              reach a result.
-// Splits write unnormalised (O, max, sum) partials to the workspace; the last
-// split to finish a (sequence, kv head, row tile) merges them (arrival
-// counter, no waiting).  Every mbarrier wait is bounded.
+//   warp 9     MMA: S = Q K^T, then O_h += P_h V_h for each key half, with
+//              tcgen05.mma (bf16 operands in shared memory, fp32 accumulators
+//              in TMEM); zeroes V rows past the end of the key range so that
+//              stale cache slots never reach a result.
+// The two halves are merged in shared memory.  When the key range is split
+// across CTAs, the splits of one row tile form a thread-block cluster: each
+// pushes its (max, sum, O) partial into the owner CTA's shared memory with
+// remote stores, and after one cluster barrier each owner reduces its rows.
+// No global scratch, no second launch; every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -31,15 +34,16 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBM = 128;             // query rows per CTA = TMEM lanes
-constexpr int kBN = 128;             // keys per tile
-constexpr int kStages = 2;           // K/V ring depth
-constexpr int kThreads = 192;        // 4 softmax warps + producer + MMA
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 256;  // S at [0, 128), O at [128, 128 + D)
+constexpr int kBM = 128;              // query rows per CTA = TMEM lanes
+constexpr int kBN = 128;              // keys per tile (two halves of 64)
+constexpr int kStages = 2;            // K/V ring depth
+constexpr int kSoftmaxThreads = 256;  // two groups of four warps
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale max while within 2^8
-constexpr int kAtomBytes = 16384;    // 128 rows x 128 bytes
+constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
+constexpr int kMaxCluster = 16;
 
 struct AttnParams {
   const uint16_t* q;
@@ -48,10 +52,8 @@ struct AttnParams {
   int32_t* status;
   const int32_t* kv_len;
   const uint64_t* anc;
-  float* part;               // split partials
-  unsigned int* arrivals;    // per (sequence, kv head, row tile)
   int N, Hq, Hkv, G, Lcap, W;
-  int mtiles, tps, nsplit;
+  int nsplit;  // splits per row tile (= cluster size when > 1)
   float scale_log2;
 };
 
@@ -64,16 +66,18 @@ struct Layout {
   static constexpr int kStage = 2 * A * kAtomBytes;
   static constexpr int kBytes = kKV + kStages * kStage;
   static constexpr int kDyn = kBytes + 1024;       // slack for 1024-byte alignment
-  static constexpr int kPartFloats = kBM * (D + 2);
+  static constexpr int kRowBytes = D * 4;          // one fp32 O row
+  // TMEM: S at [0, 128), O_0 at [128, 128 + D), O_1 at [128 + D, 128 + 2D)
+  static constexpr uint32_t kTmemCols = (128 + 2 * D <= 256) ? 256u : 512u;
+  // half merge buffer at kQ (Q and P are dead by then): 128 fp32 rows
+  static_assert(kBM * kRowBytes <= kKV, "half-merge buffer must fit Q + P");
+  // receive buffer at kKV: one slot per rank, ceil(128 / nsplit) rows each
+  static_assert((kBM + kMaxCluster) * kRowBytes <= kStages * kStage, "receive buffer");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void set_status(int32_t* status, int b, int code) {
-  if (status) atomicMax(status + b, code);
 }
 
 // Every lane of the warp waits; the warp goes on only if all of them saw the
@@ -82,38 +86,77 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// 32 bits of the ancestor bit-string starting at bit `pos` (0 <= pos < 64*W).
+__device__ __forceinline__ uint32_t anc_bits32(const uint64_t* anc, int W, int pos) {
+  const int wi = pos >> 6, sh = pos & 63;
+  const uint64_t lo = __ldg(anc + wi);
+  const uint64_t hi = (sh != 0 && wi + 1 < W) ? __ldg(anc + wi + 1) : 0ull;
+  return (uint32_t)((lo >> sh) | (sh ? (hi << (64 - sh)) : 0ull));
+}
+
+// Visibility of the 32 keys j0 + 32c .. j0 + 32c + 31 for one query row:
+// prefix keys (< L) always, tree slot L + a iff a is an ancestor-or-self of
+// the row's node, nothing at or beyond L + N.
+__device__ __forceinline__ uint32_t visibility32(int c, int j0, int L, int keys, int N,
+                                                 const uint64_t* anc, int W) {
+  const int lo = 32 * c;
+  const int pre = L - j0;   // columns [0, pre) are prefix keys
+  const int end = keys - j0;
+  const uint32_t pm = (pre >= lo + 32) ? 0xffffffffu : (pre <= lo ? 0u : ((1u << (pre - lo)) - 1u));
+  const uint32_t em = (end >= lo + 32) ? 0xffffffffu : (end <= lo ? 0u : ((1u << (end - lo)) - 1u));
+  uint32_t tm = 0u;
+  const int x = lo - pre;   // tree index of column lo
+  if (x + 32 > 0 && x < N) tm = (x >= 0) ? anc_bits32(anc, W, x) : (anc_bits32(anc, W, 0) << (-x));
+  return (pm | tm) & em;
+}
+
+// fp32 row buffers are stored with the 16-byte chunks of a row XOR-swizzled by
+// the row index, so that threads writing different rows hit different banks.
+__device__ __forceinline__ int swz_chunk(int row, int chunk) { return chunk ^ (row & 7); }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const AttnParams p) {
   using Lay = Layout<D>;
   constexpr int A = Lay::A;
+  constexpr int kChunks = D / 4;  // 16-byte chunks per fp32 row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + Lay::kQ;
   uint8_t* sP = smem + Lay::kP;
   uint8_t* sKV = smem + Lay::kKV;
+  float* sHalf = reinterpret_cast<float*>(smem + Lay::kQ);  // group 1's O rows, at the end
+  float* sRecv = reinterpret_cast<float*>(sKV);             // cluster partials, at the end
 
   __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
-  __shared__ __align__(8) uint64_t bar_q, bar_s_full, bar_s_free, bar_p_full, bar_o_done, bar_drain;
+  __shared__ __align__(8) uint64_t bar_q, bar_s_full, bar_s_free, bar_drain;
+  __shared__ __align__(8) uint64_t bar_p_full[2], bar_o_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_last;
+  __shared__ float s_m1[kBM], s_l1[kBM];                             // group 1's (max, sum)
+  __shared__ float s_rm[kMaxCluster * (kBM / 2 + 1)], s_rl[kMaxCluster * (kBM / 2 + 1)];
+  __shared__ float s_rw[kMaxCluster * (kBM / 2 + 1)];
 
   const int split = blockIdx.x, mt = blockIdx.y, bh = blockIdx.z;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = (tid < kSoftmaxThreads) ? (tid >> 7) : 0;  // softmax group: key half
+  const int row = tid & (kBM - 1);                            // softmax threads: query row
   const int N = p.N;
   const int L = p.kv_len[b];
   const int rows_total = N * p.G;
-  const int r = mt * kBM + tid;  // query row of softmax threads
-  const bool valid_row = (tid < kBM) && (r < rows_total);
+  const int r = mt * kBM + row;
+  const bool is_softmax = tid < kSoftmaxThreads;
+  const bool valid_row = is_softmax && (r < rows_total);
   const int node = valid_row ? r / p.G : 0;
   const int h = kvh * p.G + (valid_row ? r % p.G : 0);
+  const int nranks = p.nsplit;
+  const bool clustered = nranks > 1;
 
-  if (L < 0 || L + N > p.Lcap) {
-    if (split == 0 && valid_row) {
+  if (L < 0 || L + N > p.Lcap) {  // uniform over the whole cluster: all of it leaves
+    if (split == 0 && valid_row && grp == 0) {
       uint4* o = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
@@ -125,36 +168,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   if (split == 0 && mt == 0 && kvh == 0 && tid == 0 && p.status) p.status[b] = TV_OK;
   const int keys = L + N;
   const int tiles = ceil_div(keys, kBN);
-  const int nsplit_b = ceil_div(tiles, p.tps);
-  if (split >= nsplit_b) return;
-  const int t_begin = split * p.tps;
-  const int T = min(tiles, t_begin + p.tps) - t_begin;
+  // balanced split of this sequence's tiles; an empty split still merges
+  const int t_begin = (int)(((long long)split * tiles) / nranks);
+  const int T = (int)(((long long)(split + 1) * tiles) / nranks) - t_begin;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_kv_full[s], 1);
       mbar_init(&bar_kv_empty[s], 1);
     }
-    mbar_init(&bar_q, kBM);
+    mbar_init(&bar_q, kSoftmaxThreads);
     mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_s_free, kBM);
-    mbar_init(&bar_p_full, kBM);
-    mbar_init(&bar_o_done, 1);
+    mbar_init(&bar_s_free, kSoftmaxThreads);
+    mbar_init(&bar_p_full[0], kBM);
+    mbar_init(&bar_p_full[1], kBM);
+    mbar_init(&bar_o_done[0], 1);
+    mbar_init(&bar_o_done[1], 1);
     mbar_init(&bar_drain, 1);
     mbar_fence_init();
     s_abort = 0;
-    s_last = 0;
   }
-  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == 0) tmem_alloc(&s_tmem, Lay::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tS = tmem;
+  const uint32_t tO0 = tmem + 128, tO1 = tmem + 128 + D;
 
   float m_run = -INFINITY, l_run = 0.0f;  // softmax threads: running max (log2) and sum
 
-  if (warp == kProducerWarp) {
+  if (T > 0 && warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
@@ -179,11 +223,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         issued = t + 1;
       }
-      // the CTA must not retire while its copies are in flight
+      // the CTA must not move on while its copies are in flight
       for (int t = max(0, issued - kStages); t < issued; ++t)
         mbar_wait(&bar_kv_full[t % kStages], (t / kStages) & 1);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (T > 0 && warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
@@ -224,89 +268,83 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         mma_commit(&bar_s_full);
       }
       __syncwarp();
-      ok = warp_wait(&bar_p_full, t & 1);
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t p0 = smem_u32(sP), v0 = smem_u32(sV);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t offp = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          mma_bf16(tO, sw128_desc(p0 + offp, 16, 1024),
-                   sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
+      for (int hf = 0; hf < 2; ++hf) {
+        ok = warp_wait(&bar_p_full[hf], t & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          // O_hf += P[:, 64hf .. 64hf+63] * V[64hf .. 64hf+63, :]
+          const uint32_t p0 = smem_u32(sP) + hf * kAtomBytes;
+          const uint32_t v0 = smem_u32(sV) + hf * 64 * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(hf ? tO1 : tO0, sw128_desc(p0 + kk * 32, 16, 1024),
+                     sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
+          mma_commit(&bar_o_done[hf]);
         }
-        mma_commit(&bar_o_done);
-        mma_commit(&bar_kv_empty[s]);
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&bar_kv_empty[s]);
       __syncwarp();
     }
     if (!ok) s_abort = 1;
-    if (lane == 0) {  // all issued tensor-core work retires before TMEM is released
+    if (lane == 0) {  // all issued tensor-core work retires before TMEM is read or released
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0);
     }
-  } else {
+  } else if (T > 0 && is_softmax) {
     // ------------------------------------------------------------- softmax
     {
-      const uint16_t* qrow = p.q + (((size_t)b * N + node) * p.Hq + h) * D;
+      const uint4* qrow =
+          reinterpret_cast<const uint4*>(p.q + (((size_t)b * N + node) * p.Hq + h) * D);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = valid_row ? __ldg(reinterpret_cast<const uint4*>(qrow) + c)
-                                  : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + (c >> 3) * kAtomBytes + tid * 128 +
-                                  (((c & 7) ^ (tid & 7)) << 4)) = v;
+      for (int cc = 0; cc < D / 16; ++cc) {  // this group's half of the row's chunks
+        const int c = grp * (D / 16) + cc;
+        const uint4 v = valid_row ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sQ + (c >> 3) * kAtomBytes + row * 128 +
+                                  (((c & 7) ^ (row & 7)) << 4)) = v;
       }
       fence_async_smem();
       mbar_arrive(&bar_q);
     }
     const uint64_t* anc = p.anc + ((size_t)b * N + node) * p.W;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tO = grp ? tO1 : tO0;
+    const float sc = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       ok = warp_wait(&bar_s_full, t & 1);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_base + c * 32, sr[c]);
+      uint32_t sr[2][32];
+      tmem_ld32(tS + lane_base + grp * 64, sr[0]);
+      tmem_ld32(tS + lane_base + grp * 64 + 32, sr[1]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bar_s_free);
 
       const int j0 = (t_begin + t) * kBN;
-      const bool prefix_only = valid_row && (j0 + kBN <= L);
-      // ancestor words covering tree slots a = j0 + k - L of this tile
-      const int a0 = j0 - L;
-      const int wb = a0 > 0 ? (a0 >> 6) : 0;
-      uint64_t w0 = 0, w1 = 0, w2 = 0;
-      if (valid_row && !prefix_only && j0 + kBN > L) {
-        w0 = (wb < p.W) ? __ldg(anc + wb) : 0;
-        w1 = (wb + 1 < p.W) ? __ldg(anc + wb + 1) : 0;
-        w2 = (wb + 2 < p.W) ? __ldg(anc + wb + 2) : 0;
-      }
-      float tmax = -INFINITY;
+      float mx[2] = {-INFINITY, -INFINITY};
+      if (valid_row && j0 + kBN <= L) {  // all prefix keys: nothing to mask
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k = c * 32 + e;
-          bool vis = prefix_only;
-          if (!prefix_only && valid_row) {
-            const int j = j0 + k;
-            if (j < L) {
-              vis = true;
-            } else if (j < keys) {
-              const int a = j - L;
-              const int w = (a >> 6) - wb;
-              const uint64_t word = (w == 0) ? w0 : ((w == 1) ? w1 : w2);
-              vis = (word >> (a & 63)) & 1ull;
-            }
+          for (int e = 0; e < 32; ++e) mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][e]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t vis = valid_row ? visibility32(2 * grp + c, j0, L, keys, N, anc, p.W) : 0u;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = ((vis >> e) & 1u) ? __uint_as_float(sr[c][e]) : -INFINITY;
+            sr[c][e] = __float_as_uint(x);
+            mx[c] = fmaxf(mx[c], x);
           }
-          const float sv = vis ? __uint_as_float(sr[c][e]) * p.scale_log2 : -INFINITY;
-          sr[c][e] = __float_as_uint(sv);
-          tmax = fmaxf(tmax, sv);
         }
       }
+      const float tmax = fmaxf(mx[0], mx[1]) * sc;
       float corr = 1.0f;
       bool need = false;
       const float m_new = fmaxf(m_run, tmax);
@@ -317,23 +355,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         m_run = m_new;
         need = true;
       }
-      float psum = 0.0f;
-      uint32_t pk[64];
+      uint32_t pk[32];
+      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (m_run == -INFINITY) {  // nothing visible yet: P = 0
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      } else {
+        const float neg_m = -m_run;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float x0 = (m_run == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[c][e]) - m_run);
-          const float x1 =
-              (m_run == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[c][e + 1]) - m_run);
-          psum += x0 + x1;
-          pk[(c * 32 + e) >> 1] = pack_bf16(x0, x1);
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float x0 = exp2f(fmaf(__uint_as_float(sr[c][e]), sc, neg_m));
+            const float x1 = exp2f(fmaf(__uint_as_float(sr[c][e + 1]), sc, neg_m));
+            ps[2 * c + ((e >> 4) & 1)] += x0 + x1;
+            pk[(c * 32 + e) >> 1] = pack_bf16(x0, x1);
+          }
         }
       }
-      l_run = l_run * corr + psum;
-      // P and O are free once the previous tile's PV has retired
+      l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      // this group's P half and O_h are free once its previous PV retired
       if (t > 0) {
-        ok = warp_wait(&bar_o_done, (t - 1) & 1);
+        ok = warp_wait(&bar_o_done[grp], (t - 1) & 1);
         if (!ok) break;
         tc_fence_after();
       }
@@ -349,118 +392,171 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         tmem_wait_st();
       }
+      uint8_t* prow = sP + grp * kAtomBytes + row * 128;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(sP + (c >> 3) * kAtomBytes + tid * 128 +
-                                  (((c & 7) ^ (tid & 7)) << 4)) =
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p_full);
+      mbar_arrive(&bar_p_full[grp]);
     }
-    if (ok) ok = warp_wait(&bar_o_done, (T - 1) & 1);
+    if (ok) ok = warp_wait(&bar_o_done[grp], (T - 1) & 1);
     if (!ok) s_abort = 1;
     tc_fence_after();
-    // ------------------------------------------------------------ epilogue
-    const size_t orow = ((size_t)b * N + node) * p.Hq + h;
-    if (nsplit_b == 1) {
-      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+  }
+
+  // ------------------------------------------------------------ epilogue
+  tc_fence_before();
+  __syncthreads();  // every role is done; TMA and MMA work has retired
+  tc_fence_after();
+  if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+  // 1. group 1 hands its (max, sum, O_1) rows to group 0 through shared memory
+  if (is_softmax && grp == 1) {
+    s_m1[row] = m_run;
+    s_l1[row] = l_run;
+    if (T > 0) {
+      float* dst = sHalf + row * D;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_base + c, o);
+        tmem_ld32(tO1 + lane_base + c, o);
         tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(dst + 4 * swz_chunk(row, c / 4 + e)) =
+              make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                          __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+      }
+    }
+  }
+  // Every CTA of the cluster must be past its main loop before anyone writes
+  // into its K/V ring (the receive buffer); without a cluster this is a CTA
+  // barrier for the half hand-off.
+  if (clustered)
+    cluster_sync();
+  else
+    __syncthreads();
+  // 2. group 0 merges both halves of its row: (m, l, O) of this CTA
+  const int per = ceil_div(kBM, nranks);  // rows per owner rank
+  if (is_softmax && grp == 0) {
+    const float m1 = s_m1[row], l1 = s_l1[row];
+    const float mc = fmaxf(m_run, m1);
+    const float w0 = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mc);
+    const float w1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - mc);
+    const float lc = w0 * l_run + w1 * l1;
+    const size_t orow = ((size_t)b * N + node) * p.Hq + h;
+    const float inv = lc > 0.0f ? 1.0f / lc : 0.0f;
+    const int owner = row / per, slot_row = row - owner * per;
+    uint32_t recv_base = 0;
+    if (clustered) {
+      recv_base = dsmem_map(smem_u32(sRecv) + (uint32_t)((split * per + slot_row) * Lay::kRowBytes),
+                            (uint32_t)owner);
+      const uint32_t mi = (uint32_t)(split * (kBM / 2 + 1) + slot_row);
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(&s_rm[mi]), owner)),
+                   "f"(mc)
+                   : "memory");
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(&s_rl[mi]), owner)),
+                   "f"(lc)
+                   : "memory");
+    }
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      if (T > 0) {
+        tmem_ld32(tO0 + lane_base + c, o);
+        tmem_wait_ld();
+      }
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (T > 0 && w1 != 0.0f) x1 = *reinterpret_cast<const float4*>(sHalf + row * D + 4 * swz_chunk(row, c / 4 + e));
+        const float a0 = T > 0 ? __uint_as_float(o[4 * e + 0]) : 0.f;
+        const float a1 = T > 0 ? __uint_as_float(o[4 * e + 1]) : 0.f;
+        const float a2 = T > 0 ? __uint_as_float(o[4 * e + 2]) : 0.f;
+        const float a3 = T > 0 ? __uint_as_float(o[4 * e + 3]) : 0.f;
+        v[4 * e + 0] = w0 * a0 + w1 * x1.x;
+        v[4 * e + 1] = w0 * a1 + w1 * x1.y;
+        v[4 * e + 2] = w0 * a2 + w1 * x1.z;
+        v[4 * e + 3] = w0 * a3 + w1 * x1.w;
+      }
+      if (!clustered) {
         if (valid_row) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l);
-            v.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l);
-            v.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l);
-            v.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l);
-            dst[e] = v;
+            uint4 u;
+            u.x = pack_bf16(v[8 * e + 0] * inv, v[8 * e + 1] * inv);
+            u.y = pack_bf16(v[8 * e + 2] * inv, v[8 * e + 3] * inv);
+            u.z = pack_bf16(v[8 * e + 4] * inv, v[8 * e + 5] * inv);
+            u.w = pack_bf16(v[8 * e + 6] * inv, v[8 * e + 7] * inv);
+            dst[e] = u;
           }
         }
-      }
-      if (valid_row && p.lse)
-        p.lse[orow] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-    } else {
-      float* part = p.part + (((size_t)bh * p.mtiles + mt) * p.nsplit + split) * Lay::kPartFloats;
+      } else {
+        // push the partial row into the owner's receive slot (remote stores)
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_base + c, o);
-        tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(part + (size_t)tid * D + c);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                               __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t addr = recv_base + (uint32_t)(4 * swz_chunk(slot_row, c / 4 + e) * 4);
+          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "f"(v[4 * e]), "f"(v[4 * e + 1]), "f"(v[4 * e + 2]), "f"(v[4 * e + 3])
+                       : "memory");
+        }
       }
-      part[kBM * D + tid] = m_run;
-      part[kBM * D + kBM + tid] = l_run;
-      __threadfence();
     }
+    if (!clustered && valid_row && p.lse)
+      p.lse[orow] = lc > 0.0f ? (mc + log2f(lc)) * 0.69314718055994531f : -INFINITY;
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (s_abort && tid == 0) set_status(p.status, b, TV_ERR_TIMEOUT);
-  if (nsplit_b > 1) {
-    if (tid == 0) {
-      __threadfence();
-      const unsigned int prev = atomicAdd(p.arrivals + (size_t)bh * p.mtiles + mt, 1u);
-      s_last = (prev == (unsigned int)(nsplit_b - 1));
+  if (clustered) {
+    cluster_sync();  // every partial has landed in its owner's shared memory
+    // 3. owners reduce their rows over the ranks' partials
+    const int row0 = split * per, nrows = max(0, min(kBM, row0 + per) - row0);
+    for (int lr = tid; lr < nrows; lr += kThreads) {
+      float M = -INFINITY;
+      for (int rk = 0; rk < nranks; ++rk) M = fmaxf(M, s_rm[rk * (kBM / 2 + 1) + lr]);
+      float lsum = 0.0f;
+      for (int rk = 0; rk < nranks; ++rk) {
+        const float mr = s_rm[rk * (kBM / 2 + 1) + lr];
+        const float w = (mr == -INFINITY) ? 0.0f : exp2f(mr - M);
+        s_rw[rk * (kBM / 2 + 1) + lr] = w;
+        lsum += w * s_rl[rk * (kBM / 2 + 1) + lr];
+      }
+      s_rl[lr] = lsum;   // slot 0's sum is no longer needed
+      s_rm[lr] = M;
     }
     __syncthreads();
-    if (s_last) {
-      __threadfence();
-      if (tid == 0) p.arrivals[(size_t)bh * p.mtiles + mt] = 0u;
-      if (valid_row) {
-        const float* base = p.part + ((size_t)bh * p.mtiles + mt) * p.nsplit * Lay::kPartFloats;
-        float M = -INFINITY;
-        for (int s = 0; s < nsplit_b; ++s)
-          M = fmaxf(M, __ldcg(base + (size_t)s * Lay::kPartFloats + kBM * D + tid));
-        float acc[D];
-#pragma unroll
-        for (int d = 0; d < D; ++d) acc[d] = 0.0f;
-        float lsum = 0.0f;
-        for (int s = 0; s < nsplit_b; ++s) {
-          const float* ps = base + (size_t)s * Lay::kPartFloats;
-          const float ms = __ldcg(ps + kBM * D + tid);
-          const float ls = __ldcg(ps + kBM * D + kBM + tid);
-          const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-          lsum += w * ls;
-          const float4* os = reinterpret_cast<const float4*>(ps + (size_t)tid * D);
-#pragma unroll
-          for (int d4 = 0; d4 < D / 4; ++d4) {
-            const float4 v = __ldcg(os + d4);
-            acc[4 * d4 + 0] += w * v.x;
-            acc[4 * d4 + 1] += w * v.y;
-            acc[4 * d4 + 2] += w * v.z;
-            acc[4 * d4 + 3] += w * v.w;
-          }
-        }
-        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-        const size_t orow = ((size_t)b * N + node) * p.Hq + h;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
-#pragma unroll
-        for (int e = 0; e < D / 8; ++e) {
-          uint4 v;
-          v.x = pack_bf16(acc[8 * e + 0] * inv, acc[8 * e + 1] * inv);
-          v.y = pack_bf16(acc[8 * e + 2] * inv, acc[8 * e + 3] * inv);
-          v.z = pack_bf16(acc[8 * e + 4] * inv, acc[8 * e + 5] * inv);
-          v.w = pack_bf16(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv);
-          dst[e] = v;
-        }
-        if (p.lse) p.lse[orow] = lsum > 0.0f ? (M + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+    for (int idx = tid; idx < nrows * kChunks; idx += kThreads) {
+      const int lr = idx / kChunks, ch = idx % kChunks;
+      const int gr = mt * kBM + row0 + lr;
+      if (gr >= rows_total) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int rk = 0; rk < nranks; ++rk) {
+        const float w = s_rw[rk * (kBM / 2 + 1) + lr];
+        if (w == 0.0f) continue;
+        const float4 x = *reinterpret_cast<const float4*>(
+            sRecv + (size_t)(rk * per + lr) * D + 4 * swz_chunk(lr, ch));
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
       }
+      const float lsum = s_rl[lr];
+      const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+      const size_t orow = ((size_t)b * N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
+      uint2 u;
+      u.x = pack_bf16(acc.x * inv, acc.y * inv);
+      u.y = pack_bf16(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(p.out + orow * D + 4 * ch) = u;
+      if (ch == 0 && p.lse)
+        p.lse[orow] = lsum > 0.0f ? (s_rm[lr] + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, Lay::kTmemCols);
 }
 
 // --------------------------------------------------------------------- host
@@ -479,73 +575,88 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else {
+// How many clusters of each size (1..16) of this kernel the device can hold
+// at once; entry 1 is the number of CTAs that fit (one per SM).
+template <int D>
+const int* cluster_capacity() {
+  static int cap[kMaxCluster + 1] = {0};
+  static bool done = false;
+  if (!done) {
+    using Lay = Layout<D>;
+    cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDyn);
+    cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    (void)cudaGetLastError();
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 0;
+    (void)cudaGetLastError();
+    cap[1] = sms;
+    for (int cs = 2; cs <= kMaxCluster; ++cs) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = Lay::kDyn;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = cs;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D>, &cfg) != cudaSuccess) n = 0;
       (void)cudaGetLastError();
-      n = 152;
+      cap[cs] = n;
     }
+    done = true;
   }
-  return n;
+  return cap;
 }
 
 struct SplitPlan {
-  int mtiles, tps, nsplit;
+  int mtiles, nsplit;
 };
 
-// Split the key range so that the grid fills the SMs: minimise
-// (waves of CTAs) x (tiles per split), preferring fewer splits on ties.
-SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
+// Choose the split count (= cluster size) that minimises
+// (waves of clusters) x (tiles per CTA + fixed cost), preferring fewer splits.
+// Without a device (capacities unknown) the plan assumes 152 SMs and clusters
+// of up to 8.
+SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap, const int* cap) {
   SplitPlan sp;
   const int G = Hq / Hkv;
   sp.mtiles = ceil_div(N * G, kBM);
   const long long units = (long long)B * Hkv * sp.mtiles;
   const int tiles_max = ceil_div(Lcap, kBN);
-  const int sms = sm_count();
   long long best = -1;
-  sp.tps = tiles_max;
   sp.nsplit = 1;
-  for (int ns = 1; ns <= tiles_max && ns <= 64; ++ns) {
-    const int tps = ceil_div(tiles_max, ns);
-    const int nsplit = ceil_div(tiles_max, tps);
-    if (nsplit != ns) continue;
-    const long long waves = (units * nsplit + sms - 1) / sms;
-    const long long cost = waves * (tps + 1) * 4 + (nsplit > 1 ? 2 : 0);
+  for (int ns = 1; ns <= kMaxCluster && ns <= tiles_max; ++ns) {
+    long long slots;
+    if (cap[1] > 0)
+      slots = (ns == 1) ? cap[1] : cap[ns];
+    else
+      slots = (ns <= 8) ? 152 / ns : 0;
+    if (slots <= 0) continue;
+    const long long waves = (units + slots - 1) / slots;
+    const long long tiles_per_cta = (tiles_max + ns - 1) / ns;
+    const long long cost = waves * (tiles_per_cta * 4 + 10) + (ns > 1 ? 4 : 0);
     if (best < 0 || cost < best) {
       best = cost;
-      sp.tps = tps;
-      sp.nsplit = nsplit;
+      sp.nsplit = ns;
     }
   }
   return sp;
-}
-
-size_t counters_bytes(int B, int Hkv, int mtiles) {
-  return align_up((size_t)B * Hkv * mtiles * sizeof(unsigned int), 256);
 }
 
 template <int D>
 tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, const int32_t* kv_len,
                       const uint64_t* anc_mask, int B, int N, int Hq, int Hkv, int Lcap,
                       float scale_log2, tv_bf16* out, float* lse, int32_t* status,
-                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                      cudaStream_t stream) {
   using Lay = Layout<D>;
   auto encode = tensor_map_encoder();
   if (!encode) return TV_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay::kDyn) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
-    attr_set = true;
-  }
+  const int* cap = cluster_capacity<D>();
   CUtensorMap tmK, tmV;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)B * Hkv * Lcap};
   const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
@@ -559,7 +670,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return TV_ERR_INVALID_ARG;
-  const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap);
+  const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap, cap);
   AttnParams p;
   p.q = q;
   p.out = out;
@@ -567,29 +678,30 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.status = status;
   p.kv_len = kv_len;
   p.anc = anc_mask;
-  p.arrivals = static_cast<unsigned int*>(workspace);
-  p.part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                    counters_bytes(B, Hkv, sp.mtiles));
   p.N = N;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
   p.Lcap = Lcap;
   p.W = ceil_div(N, 64);
-  p.mtiles = sp.mtiles;
-  p.tps = sp.tps;
   p.nsplit = sp.nsplit;
   p.scale_log2 = scale_log2;
-  if (sp.nsplit > 1) {
-    // the arrival counters start at zero whatever the workspace held before
-    if (cudaMemsetAsync(workspace, 0, counters_bytes(B, Hkv, sp.mtiles), stream) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sp.nsplit, sp.mtiles, B * Hkv);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Lay::kDyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = sp.nsplit;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = sp.nsplit > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tmK, tmV, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
   }
-  dim3 grid(sp.nsplit, sp.mtiles, B * Hkv);
-  attn_tc_kernel<D><<<grid, kThreads, Lay::kDyn, stream>>>(tmK, tmV, p);
-  TV_CHECK_LAUNCH();
   return TV_OK;
 }
 
@@ -597,13 +709,8 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
 }  // namespace tv
 
 extern "C" size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap) {
-  if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Lcap < N || (D != 64 && D != 128))
-    return 256;
-  const tv::SplitPlan sp = tv::plan_splits(B, N, Hq, Hkv, Lcap);
-  size_t bytes = tv::counters_bytes(B, Hkv, sp.mtiles);
-  if (sp.nsplit > 1)
-    bytes += (size_t)B * Hkv * sp.mtiles * sp.nsplit * tv::kBM * (D + 2) * sizeof(float);
-  return bytes;
+  (void)B; (void)N; (void)Hq; (void)Hkv; (void)D; (void)Lcap;
+  return 0;
 }
 
 extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
@@ -611,6 +718,8 @@ extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv
                                     int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,
                                     float* lse, int32_t* status, void* workspace, size_t ws_bytes,
                                     cudaStream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Lcap < N) return TV_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return TV_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return TV_ERR_UNSUPPORTED;
@@ -621,13 +730,11 @@ extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
     return TV_ERR_INVALID_ARG;
-  if (!workspace || ws_bytes < tv_attn_workspace_size(B, N, Hq, Hkv, D, Lcap))
-    return TV_ERR_WORKSPACE;
   const float sc = (scale == 0.0f) ? 1.0f / sqrtf((float)D) : scale;
   const float scale_log2 = sc * 1.4426950408889634f;
   if (D == 128)
     return tv::launch_attn<128>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out,
-                                lse, status, workspace, ws_bytes, stream);
+                                lse, status, stream);
   return tv::launch_attn<64>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out, lse,
-                             status, workspace, ws_bytes, stream);
+                             status, stream);
 }
