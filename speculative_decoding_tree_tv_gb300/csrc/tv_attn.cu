@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "tv_common.cuh"
 #include "tv_sm100.cuh"
@@ -66,13 +67,13 @@ struct Layout {
   static constexpr int kStage = 2 * A * kAtomBytes;
   static constexpr int kBytes = kKV + kStages * kStage;
   static constexpr int kDyn = kBytes + 1024;       // slack for 1024-byte alignment
-  static constexpr int kRowBytes = D * 4;          // one fp32 O row
   // TMEM: S at [0, 128), O_0 at [128, 128 + D), O_1 at [128 + D, 128 + 2D)
   static constexpr uint32_t kTmemCols = (128 + 2 * D <= 256) ? 256u : 512u;
-  // half merge buffer at kQ (Q and P are dead by then): 128 fp32 rows
-  static_assert(kBM * kRowBytes <= kKV, "half-merge buffer must fit Q + P");
-  // receive buffer at kKV: one slot per rank, ceil(128 / nsplit) rows each
-  static_assert((kBM + kMaxCluster) * kRowBytes <= kStages * kStage, "receive buffer");
+  // merge statistics at kQ (Q and P are dead by then): three [slot][row]
+  // float arrays of 2 * 16 slots x 64 rows (or 2 slots x 128 rows)
+  static_assert(3 * 2 * kMaxCluster * (kBM / 2) * 4 <= kKV, "merge statistics must fit Q + P");
+  // receive buffer at kKV: fp16 rows, two slots per rank, ceil(128 / nsplit) rows each
+  static_assert(2 * (kBM + kMaxCluster) * D * 2 <= kStages * kStage, "receive buffer");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -120,24 +121,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                const AttnParams p) {
   using Lay = Layout<D>;
   constexpr int A = Lay::A;
-  constexpr int kChunks = D / 4;  // 16-byte chunks per fp32 row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + Lay::kQ;
   uint8_t* sP = smem + Lay::kP;
   uint8_t* sKV = smem + Lay::kKV;
-  float* sHalf = reinterpret_cast<float*>(smem + Lay::kQ);  // group 1's O rows, at the end
-  float* sRecv = reinterpret_cast<float*>(sKV);             // cluster partials, at the end
+  float* sStat = reinterpret_cast<float*>(smem + Lay::kQ);  // merge statistics, at the end
+  __half* sRecv = reinterpret_cast<__half*>(sKV);           // partial O rows, at the end
 
   __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ __align__(8) uint64_t bar_q, bar_s_full, bar_s_free, bar_drain;
   __shared__ __align__(8) uint64_t bar_p_full[2], bar_o_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ float s_m1[kBM], s_l1[kBM];                             // group 1's (max, sum)
-  __shared__ float s_rm[kMaxCluster * (kBM / 2 + 1)], s_rl[kMaxCluster * (kBM / 2 + 1)];
-  __shared__ float s_rw[kMaxCluster * (kBM / 2 + 1)];
+  __shared__ float s_M[kBM], s_L[kBM];  // merged max and sum of the rows this CTA owns
 
   const int split = blockIdx.x, mt = blockIdx.y, bh = blockIdx.z;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
@@ -413,146 +411,125 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  // 1. group 1 hands its (max, sum, O_1) rows to group 0 through shared memory
-  if (is_softmax && grp == 1) {
-    s_m1[row] = m_run;
-    s_l1[row] = l_run;
-    if (T > 0) {
-      float* dst = sHalf + row * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO1 + lane_base + c, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<float4*>(dst + 4 * swz_chunk(row, c / 4 + e)) =
-              make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                          __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-      }
-    }
-  }
-  // Every CTA of the cluster must be past its main loop before anyone writes
-  // into its K/V ring (the receive buffer); without a cluster this is a CTA
-  // barrier for the half hand-off.
-  if (clustered)
+  // 1. Every CTA of the cluster must be past its main loop before anyone
+  //    writes into its Q/P and K/V space, which now hold the merge buffers.
+  if (clustered) {
     cluster_sync();
-  else
+  } else {
     __syncthreads();
-  // 2. group 0 merges both halves of its row: (m, l, O) of this CTA
+  }
+  // 2. Every softmax thread hands its group's partial for its row -- running
+  //    max, sum and the normalised O row in fp16 -- to the rank owning the row
+  //    (itself without a cluster), slot 2 * split + group.
   const int per = ceil_div(kBM, nranks);  // rows per owner rank
-  if (is_softmax && grp == 0) {
-    const float m1 = s_m1[row], l1 = s_l1[row];
-    const float mc = fmaxf(m_run, m1);
-    const float w0 = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mc);
-    const float w1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - mc);
-    const float lc = w0 * l_run + w1 * l1;
-    const size_t orow = ((size_t)b * N + node) * p.Hq + h;
-    const float inv = lc > 0.0f ? 1.0f / lc : 0.0f;
-    const int owner = row / per, slot_row = row - owner * per;
-    uint32_t recv_base = 0;
+  const int slots = 2 * nranks;
+  float* s_mx = sStat;                    // [slot][per] partial max (log2)
+  float* s_sm = sStat + 2 * kMaxCluster * kBM / 2;          // [slot][per] partial sum
+  float* s_cf = sStat + 2 * (2 * kMaxCluster * kBM / 2);    // [slot][per] merge weight
+  if (is_softmax) {
+    const int owner = row / per, lr = row - owner * per;
+    const int sl = 2 * split + grp;
+    const int si = sl * per + lr;
+    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    const uint32_t rrow = smem_u32(sRecv) + (uint32_t)(si * D * 2);
     if (clustered) {
-      recv_base = dsmem_map(smem_u32(sRecv) + (uint32_t)((split * per + slot_row) * Lay::kRowBytes),
-                            (uint32_t)owner);
-      const uint32_t mi = (uint32_t)(split * (kBM / 2 + 1) + slot_row);
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(&s_rm[mi]), owner)),
-                   "f"(mc)
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(s_mx + si), owner)),
+                   "f"(m_run)
                    : "memory");
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(&s_rl[mi]), owner)),
-                   "f"(lc)
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(s_sm + si), owner)),
+                   "f"(l_run)
                    : "memory");
+    } else {
+      s_mx[si] = m_run;
+      s_sm[si] = l_run;
     }
+    const uint32_t rbase = clustered ? dsmem_map(rrow, owner) : rrow;
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
       uint32_t o[32];
       if (T > 0) {
-        tmem_ld32(tO0 + lane_base + c, o);
+        tmem_ld32((grp ? tO1 : tO0) + lane_base + c, o);
         tmem_wait_ld();
-      }
-      float v[32];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (T > 0 && w1 != 0.0f) x1 = *reinterpret_cast<const float4*>(sHalf + row * D + 4 * swz_chunk(row, c / 4 + e));
-        const float a0 = T > 0 ? __uint_as_float(o[4 * e + 0]) : 0.f;
-        const float a1 = T > 0 ? __uint_as_float(o[4 * e + 1]) : 0.f;
-        const float a2 = T > 0 ? __uint_as_float(o[4 * e + 2]) : 0.f;
-        const float a3 = T > 0 ? __uint_as_float(o[4 * e + 3]) : 0.f;
-        v[4 * e + 0] = w0 * a0 + w1 * x1.x;
-        v[4 * e + 1] = w0 * a1 + w1 * x1.y;
-        v[4 * e + 2] = w0 * a2 + w1 * x1.z;
-        v[4 * e + 3] = w0 * a3 + w1 * x1.w;
-      }
-      if (!clustered) {
-        if (valid_row) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 u;
-            u.x = pack_bf16(v[8 * e + 0] * inv, v[8 * e + 1] * inv);
-            u.y = pack_bf16(v[8 * e + 2] * inv, v[8 * e + 3] * inv);
-            u.z = pack_bf16(v[8 * e + 4] * inv, v[8 * e + 5] * inv);
-            u.w = pack_bf16(v[8 * e + 6] * inv, v[8 * e + 7] * inv);
-            dst[e] = u;
-          }
-        }
       } else {
-        // push the partial row into the owner's receive slot (remote stores)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t addr = recv_base + (uint32_t)(4 * swz_chunk(slot_row, c / 4 + e) * 4);
-          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "f"(v[4 * e]), "f"(v[4 * e + 1]), "f"(v[4 * e + 2]), "f"(v[4 * e + 3])
-                       : "memory");
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {  // four 16-byte chunks of 8 halves
+        uint32_t hw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half2 hv = __floats2half2_rn(__uint_as_float(o[8 * e + 2 * j]) * inv,
+                                               __uint_as_float(o[8 * e + 2 * j + 1]) * inv);
+          hw[j] = *reinterpret_cast<const uint32_t*>(&hv);
         }
+        const uint32_t addr = rbase + (uint32_t)(swz_chunk(lr, c / 8 + e) * 16);
+        if (clustered)
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hw[0]),
+                       "r"(hw[1]), "r"(hw[2]), "r"(hw[3])
+                       : "memory");
+        else
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hw[0]),
+                       "r"(hw[1]), "r"(hw[2]), "r"(hw[3])
+                       : "memory");
       }
     }
-    if (!clustered && valid_row && p.lse)
-      p.lse[orow] = lc > 0.0f ? (mc + log2f(lc)) * 0.69314718055994531f : -INFINITY;
   }
   if (clustered) {
     cluster_sync();  // every partial has landed in its owner's shared memory
-    // 3. owners reduce their rows over the ranks' partials
-    const int row0 = split * per, nrows = max(0, min(kBM, row0 + per) - row0);
-    for (int lr = tid; lr < nrows; lr += kThreads) {
-      float M = -INFINITY;
-      for (int rk = 0; rk < nranks; ++rk) M = fmaxf(M, s_rm[rk * (kBM / 2 + 1) + lr]);
-      float lsum = 0.0f;
-      for (int rk = 0; rk < nranks; ++rk) {
-        const float mr = s_rm[rk * (kBM / 2 + 1) + lr];
-        const float w = (mr == -INFINITY) ? 0.0f : exp2f(mr - M);
-        s_rw[rk * (kBM / 2 + 1) + lr] = w;
-        lsum += w * s_rl[rk * (kBM / 2 + 1) + lr];
-      }
-      s_rl[lr] = lsum;   // slot 0's sum is no longer needed
-      s_rm[lr] = M;
-    }
+  } else {
     __syncthreads();
-    for (int idx = tid; idx < nrows * kChunks; idx += kThreads) {
-      const int lr = idx / kChunks, ch = idx % kChunks;
-      const int gr = mt * kBM + row0 + lr;
-      if (gr >= rows_total) continue;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int rk = 0; rk < nranks; ++rk) {
-        const float w = s_rw[rk * (kBM / 2 + 1) + lr];
-        if (w == 0.0f) continue;
-        const float4 x = *reinterpret_cast<const float4*>(
-            sRecv + (size_t)(rk * per + lr) * D + 4 * swz_chunk(lr, ch));
-        acc.x += w * x.x;
-        acc.y += w * x.y;
-        acc.z += w * x.z;
-        acc.w += w * x.w;
-      }
-      const float lsum = s_rl[lr];
-      const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-      const size_t orow = ((size_t)b * N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
-      uint2 u;
-      u.x = pack_bf16(acc.x * inv, acc.y * inv);
-      u.y = pack_bf16(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(p.out + orow * D + 4 * ch) = u;
-      if (ch == 0 && p.lse)
-        p.lse[orow] = lsum > 0.0f ? (s_rm[lr] + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+  }
+  // 3. owners merge their rows: weights exp2(m_s - M) * l_s / sum, then a
+  //    weighted sum of the normalised partial rows
+  const int row0 = split * per, nrows = max(0, min(kBM, row0 + per) - row0);
+  for (int lr = tid; lr < nrows; lr += kThreads) {
+    float M = -INFINITY;
+    for (int sl = 0; sl < slots; ++sl) M = fmaxf(M, s_mx[sl * per + lr]);
+    float lsum = 0.0f;
+    for (int sl = 0; sl < slots; ++sl) {
+      const float ms = s_mx[sl * per + lr];
+      const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M) * s_sm[sl * per + lr];
+      s_cf[sl * per + lr] = w;
+      lsum += w;
     }
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+    for (int sl = 0; sl < slots; ++sl) s_cf[sl * per + lr] *= inv;
+    s_M[lr] = M;
+    s_L[lr] = lsum;
+  }
+  __syncthreads();
+  constexpr int kC16 = D / 8;  // 16-byte chunks of an fp16 row
+  for (int idx = tid; idx < nrows * kC16; idx += kThreads) {
+    const int lr = idx / kC16, ch = idx % kC16;
+    const int gr = mt * kBM + row0 + lr;
+    if (gr >= rows_total) continue;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int sl = 0; sl < slots; ++sl) {
+      const float cw = s_cf[sl * per + lr];
+      if (cw == 0.0f) continue;
+      const uint4 x = *reinterpret_cast<const uint4*>(
+          reinterpret_cast<const uint8_t*>(sRecv) + (size_t)(sl * per + lr) * D * 2 +
+          swz_chunk(lr, ch) * 16);
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[j]));
+        acc[2 * j] += cw * f.x;
+        acc[2 * j + 1] += cw * f.y;
+      }
+    }
+    const size_t orow = ((size_t)b * N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
+    uint4 u;
+    u.x = pack_bf16(acc[0], acc[1]);
+    u.y = pack_bf16(acc[2], acc[3]);
+    u.z = pack_bf16(acc[4], acc[5]);
+    u.w = pack_bf16(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) = u;
+    if (ch == 0 && p.lse)
+      p.lse[orow] = s_L[lr] > 0.0f ? (s_M[lr] + log2f(s_L[lr])) * 0.69314718055994531f : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
