@@ -164,6 +164,32 @@ tv_status tv_accept_greedy(const float* logits, const int32_t* tokens, const int
                            size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * tv_accept_greedy_noalloc -- tv_accept_greedy without a workspace.
+ * The method description has no counterpart for this call: it exists for
+ * callers that cannot allocate device memory where they run acceptance (a
+ * serving loop whose memory plan is fixed at start-up, a plug-in that is
+ * handed no allocator, a real-time path that must not allocate).
+ *
+ * Same arguments, outputs and status codes as tv_accept_greedy, minus the
+ * workspace.  Scratch (one 64-bit key per node row, one counter per
+ * sequence) lives in a fixed array of 528 KiB inside the library, present on
+ * every GPU that loads it until the process exits.  Limits: B * N <= 65536
+ * and B <= 4096; larger calls return TV_ERR_UNSUPPORTED without launching.
+ * The call allocates nothing: it clears the part of the array it uses
+ * (cudaMemsetAsync on `stream`) and launches the greedy kernel.
+ * Every call on a device shares that array, so calls whose kernels may
+ * overlap on the GPU (different streams, no ordering between them) race and
+ * must not be issued.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.
+ */
+tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t* tokens,
+                                   const int32_t* parent, const int32_t* depth, int B, int N,
+                                   int V, int32_t* argmax, int32_t* accept_len, int32_t* end_node,
+                                   int32_t* path, int32_t* bonus, int32_t* status,
+                                   cudaStream_t stream);
+
+/*
  * tv_accept_sample -- stochastic (lossless) acceptance over a verified tree.
  * (Speculative Decoding concept page, "The protocol" step 3: accept a draft
  * token x with probability min(1, p(x)/q(x)); on rejection resample from the

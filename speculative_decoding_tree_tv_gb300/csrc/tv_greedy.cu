@@ -223,3 +223,86 @@ extern "C" tv_status tv_accept_greedy(const float* logits, const int32_t* tokens
   TV_CHECK_LAUNCH();
   return TV_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of tv_accept_greedy.
+//
+// Some callers cannot allocate device memory where they need acceptance: a
+// serving loop whose device memory was planned and reserved once at start-up,
+// a plug-in running inside another framework's execution that is handed no
+// allocator, or a real-time path where an allocation (and the synchronisation
+// it may imply) is not allowed.  This entry point takes no workspace.  Its
+// scratch -- one 64-bit key per node row and one arrival counter per sequence
+// -- lives in a fixed-size file-scope __device__ array, which every GPU that
+// loads this library holds until the process exits.
+#include <mutex>
+
+namespace tv {
+namespace {
+
+constexpr long long kStaticMaxRows = 65536;  // B * N
+constexpr int kStaticMaxSeqs = 4096;         // B
+constexpr size_t kStaticKeyBytes = (size_t)kStaticMaxRows * sizeof(unsigned long long);
+constexpr size_t kStaticScratchBytes = kStaticKeyBytes + (size_t)kStaticMaxSeqs * sizeof(unsigned int);
+
+__device__ __align__(256) unsigned char g_greedy_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_greedy_scratch_addr[kMaxDevices];  // device address of the array, per device
+std::mutex g_greedy_scratch_mu;
+
+}  // namespace
+}  // namespace tv
+
+extern "C" tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t* tokens,
+                                              const int32_t* parent, const int32_t* depth, int B,
+                                              int N, int V, int32_t* argmax, int32_t* accept_len,
+                                              int32_t* end_node, int32_t* path, int32_t* bonus,
+                                              int32_t* status, cudaStream_t stream) {
+  if (B < 0 || N < 1 || N > TV_MAX_NODES || V < 1) return TV_ERR_INVALID_ARG;
+  if (B == 0) return TV_OK;
+  if (!logits || !tokens || !parent || !depth || !argmax || !accept_len || !end_node || !path ||
+      !bonus || !status)
+    return TV_ERR_INVALID_ARG;
+  if ((long long)B * N > tv::kStaticMaxRows || B > tv::kStaticMaxSeqs) return TV_ERR_UNSUPPORTED;
+  if ((size_t)B * N * tv::ceil_div(V, tv::kGreedyChunk) > 0x7fffffffu) return TV_ERR_UNSUPPORTED;
+  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) != 0) return TV_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= tv::kMaxDevices) return TV_ERR_UNSUPPORTED;
+  void* base = nullptr;
+  {
+    // first call on this device: look up where the array lives on it
+    std::lock_guard<std::mutex> lock(tv::g_greedy_scratch_mu);
+    if (!tv::g_greedy_scratch_addr[dev]) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, tv::g_greedy_scratch) != cudaSuccess || !addr) {
+        (void)cudaGetLastError();
+        return TV_ERR_CUDA;
+      }
+      tv::g_greedy_scratch_addr[dev] = addr;
+    }
+    base = tv::g_greedy_scratch_addr[dev];
+  }
+  // The array keeps whatever the previous call left; the keys and counters
+  // this call uses must start at zero.
+  char* b8 = static_cast<char*>(base);
+  if (cudaMemsetAsync(b8, 0, (size_t)B * N * sizeof(unsigned long long), stream) != cudaSuccess ||
+      cudaMemsetAsync(b8 + tv::kStaticKeyBytes, 0, (size_t)B * sizeof(unsigned int), stream) !=
+          cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
+  tv::GreedyWs ws;
+  ws.keys = reinterpret_cast<unsigned long long*>(b8);
+  ws.arrivals = reinterpret_cast<unsigned int*>(b8 + tv::kStaticKeyBytes);
+  const int chunks = tv::ceil_div(V, tv::kGreedyChunk);
+  tv::greedy_kernel<<<dim3(chunks * B * N), tv::kGreedyThreads, 0, stream>>>(
+      logits, tokens, parent, depth, N, V, chunks, argmax, accept_len, end_node, path, bonus,
+      status, ws);
+  TV_CHECK_LAUNCH();
+  return TV_OK;
+}
