@@ -137,6 +137,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __shared__ volatile int s_abort;
   __shared__ float s_M[kBM], s_L[kBM];  // merged max and sum of the rows this CTA owns
 
+  pdl_wait();  // everything below may read what the previous kernel wrote
+  pdl_trigger();
   const int split = blockIdx.x, mt = blockIdx.y, bh = blockIdx.z;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -668,13 +670,15 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Lay::kDyn;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = sp.nsplit;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = sp.nsplit > 1 ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = sp.nsplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = sp.nsplit > 1 ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tmK, tmV, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;

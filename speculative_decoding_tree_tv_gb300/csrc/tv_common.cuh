@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "treeverify.h"
 
 #define TV_CHECK_LAUNCH()                                   \
@@ -89,6 +91,16 @@ __device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
   return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream is still
+// running; it must call pdl_wait() before touching anything that kernel
+// writes, and it calls pdl_trigger() (after its own pdl_wait()) to let the
+// next kernel start early.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Compensated (Kahan) fp32 accumulation.
 struct KahanF {
   float s = 0.0f, c = 0.0f;
@@ -138,6 +150,40 @@ __device__ __forceinline__ double decision_uniform(uint64_t seed, uint64_t offse
   uint64_t out[4];
   philox4x64_10(ctr, seed, 0ull, out);
   return (double)(out[0] >> 11) * (1.0 / 9007199254740992.0);
+}
+
+// ------------------------------------------------------------------- host
+// SMs of the current device (152 on GB300 when no device can be queried).
+inline int device_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else {
+      (void)cudaGetLastError();
+      n = 152;
+    }
+  }
+  return n;
+}
+
+// Launch with programmatic stream serialisation (see pdl_wait/pdl_trigger).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace tv

@@ -69,6 +69,8 @@ __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, si
 
 __global__ void __launch_bounds__(kExpThreads)
 exp_stats_kernel(const float* __restrict__ logits, int V, int chunks, ExpPartial* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y;
   const float* x = logits + (size_t)row * V;
   const int start = blockIdx.x * kExpChunk;
@@ -133,6 +135,8 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
                    ExpWs ws) {
   __shared__ unsigned long long s_anchor;
   __shared__ double s_m_row[kMaxBudget];
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   if (tid == 0) s_anchor = 0ull;
   __syncthreads();
@@ -176,6 +180,8 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
 
 __global__ void __launch_bounds__(kExpThreads)
 exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y;
   const float thr = ws.rows[row].thr;
   if (!(thr < INFINITY)) return;
@@ -266,6 +272,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
   __shared__ unsigned int s_hist[256];
   __shared__ int s_n, s_nt, s_digit, s_need;
   __shared__ unsigned long long s_min;
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   const ExpCtl ctl = *ws.ctl;
   const int count = ctl.count, limit = ctl.limit;
@@ -406,16 +414,18 @@ extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* f
   ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
   const int chunks = tv::ceil_div(V, tv::kExpChunk);
   dim3 grid(chunks, F);
-  tv::exp_stats_kernel<<<grid, tv::kExpThreads, 0, stream>>>(draft_logits, V, chunks, ws.part);
-  TV_CHECK_LAUNCH();
-  tv::exp_control_kernel<<<1, tv::kExpThreads, 0, stream>>>(frontier_logscore, F, chunks, layer,
-                                                            topk, alpha, budget, n_nodes, ws);
-  TV_CHECK_LAUNCH();
-  tv::exp_filter_kernel<<<grid, tv::kExpThreads, 0, stream>>>(draft_logits, V, ws);
-  TV_CHECK_LAUNCH();
-  tv::exp_select_kernel<<<1, tv::kSelThreads, 0, stream>>>(draft_logits, V, frontier_node,
-                                                           tree_parent, tree_token, tree_logscore,
-                                                           n_nodes, ws);
-  TV_CHECK_LAUNCH();
+  if (tv::launch_pdl(tv::exp_stats_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
+                     chunks, ws.part) != cudaSuccess ||
+      tv::launch_pdl(tv::exp_control_kernel, dim3(1), dim3(tv::kExpThreads), 0, stream,
+                     frontier_logscore, F, chunks, layer, topk, alpha, budget,
+                     (const int32_t*)n_nodes, ws) != cudaSuccess ||
+      tv::launch_pdl(tv::exp_filter_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
+                     ws) != cudaSuccess ||
+      tv::launch_pdl(tv::exp_select_kernel, dim3(1), dim3(tv::kSelThreads), 0, stream, draft_logits,
+                     V, frontier_node, tree_parent, tree_token, tree_logscore, n_nodes,
+                     ws) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
   return TV_OK;
 }

@@ -3,17 +3,22 @@
 // sampling the longest branch matching the target's highest-probability
 // sequence is accepted; GOOSE §2C greedy walk).
 //
-// One launch.  CTA (chunk, row) streams 8192 logits of one row with 16-byte
-// non-allocating loads, reduces them to (max, lowest index) and folds that
-// into the row's 64-bit key (order-preserving float bits, inverted index)
-// with atomicMax.  The CTA that finishes a sequence last (per-sequence
-// arrival counter) runs the tree scan for it:
+// One launch.  CTA c handles work item c = (row, chunk): a contiguous chunk
+// of one row's logits.  Items are numbered row-major, so the CTAs resident at
+// any moment sweep one contiguous stretch of memory (which keeps every DRAM
+// channel busy), and the chunk length is chosen so that all items fit in one
+// wave of resident CTAs.  Each thread keeps 8 16-byte non-allocating loads in
+// flight; the CTA reduces its chunk to (max, lowest index) and folds it into
+// the row's 64-bit key (order-preserving float bits, inverted index) with
+// atomicMax.  The CTA that completes a sequence's N * chunks arrivals runs
+// that tree's scan:
 //   match[i] = tokens[i] == argmax[parent[i]],
 //   valid[i] = AND of match over the root path (pointer jumping),
 //   end      = deepest valid node, ties to the lowest index,
-// and returns the workspace to zero (keys swapped out with atomicExch, the
-// counter reset).
+// and returns the workspace to zero (keys swapped out with atomicExch,
+// counter reset).  No CTA waits for another.
 #include <climits>
+#include <mutex>
 
 #include "tv_common.cuh"
 
@@ -21,12 +26,30 @@ namespace tv {
 namespace {
 
 constexpr int kGreedyThreads = 256;
-constexpr int kGreedyChunk = 8192;  // logits per CTA: 8 float4 per thread
+constexpr int kGreedyCtasPerSm = 4;  // resident CTAs per SM assumed when sizing chunks
+constexpr int kLoadsInFlight = 8;  // vector loads per thread per batch
 constexpr int kScanNodesPerThread = (kMaxNodes + kGreedyThreads - 1) / kGreedyThreads;
 
 struct GreedyWs {
   unsigned long long* keys;  // [B*N]
   unsigned int* arrivals;    // [B]
+};
+
+struct GreedyArgs {
+  const float* logits;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* depth;
+  int B, N, V;
+  int chunks;          // work items per row
+  int chunk_units;     // vectors (or scalars) per work item
+  int32_t* argmax;
+  int32_t* accept_len;
+  int32_t* end_node;
+  int32_t* path;
+  int32_t* bonus;
+  int32_t* status;
+  GreedyWs ws;
 };
 
 __host__ __device__ inline size_t greedy_keys_bytes(int B, int N) {
@@ -37,90 +60,47 @@ __device__ __forceinline__ unsigned long long pack_key(ArgMax a) {
   return ((unsigned long long)float_key(a.v) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)a.i);
 }
 
-__global__ void __launch_bounds__(kGreedyThreads)
-greedy_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
-              const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int N, int V,
-              int chunks, int32_t* __restrict__ argmax_out, int32_t* __restrict__ accept_len,
-              int32_t* __restrict__ end_node, int32_t* __restrict__ path,
-              int32_t* __restrict__ bonus, int32_t* __restrict__ status, GreedyWs ws) {
-  const int row = blockIdx.x / chunks;
-  const int b = row / N;
+// Block-wide argmax; every thread gets the result.
+__device__ ArgMax block_argmax(ArgMax a, ArgMax* s_red) {
+  a = warp_argmax(a);
   const int tid = threadIdx.x;
-  const int start = (blockIdx.x % chunks) * kGreedyChunk;
-  const int stop = min(V, start + kGreedyChunk);
-  const float* x = logits + (size_t)row * V;
-
-  ArgMax best{-INFINITY, INT_MAX};
-  if ((V & 3) == 0) {
-    // rows start 16-byte aligned: vector body, all loads issued first
-    const float4* x4 = reinterpret_cast<const float4*>(x);
-    float4 buf[kGreedyChunk / (4 * kGreedyThreads)];
-#pragma unroll
-    for (int u = 0; u < kGreedyChunk / (4 * kGreedyThreads); ++u) {
-      const int e = start + 4 * (tid + u * kGreedyThreads);
-      buf[u] = (e < stop) ? ld_stream_f4(x4 + (e >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-#pragma unroll
-    for (int u = 0; u < kGreedyChunk / (4 * kGreedyThreads); ++u) {
-      const int e = start + 4 * (tid + u * kGreedyThreads);
-      if (e < stop) {
-        if (buf[u].x > best.v) best = {buf[u].x, e};
-        if (buf[u].y > best.v) best = {buf[u].y, e + 1};
-        if (buf[u].z > best.v) best = {buf[u].z, e + 2};
-        if (buf[u].w > best.v) best = {buf[u].w, e + 3};
-      }
-    }
-  } else {
-    for (int e = start + tid; e < stop; e += kGreedyThreads) {
-      const float v = __ldg(x + e);
-      if (v > best.v) best = {v, e};
-    }
-  }
-  if (best.i == INT_MAX) best.i = start;  // all -inf: any index of the chunk, lowest first
-
-  __shared__ ArgMax s_red[kGreedyThreads / 32];
-  __shared__ int s_last;
-  best = warp_argmax(best);
-  if ((tid & 31) == 0) s_red[tid >> 5] = best;
   __syncthreads();
-  if (tid < 32) {
-    ArgMax a = (tid < kGreedyThreads / 32) ? s_red[tid] : ArgMax{-INFINITY, INT_MAX};
-    a = warp_argmax(a);
-    if (tid == 0) {
-      atomicMax(ws.keys + row, pack_key(a));
-      __threadfence();
-      const unsigned int prev = atomicAdd(ws.arrivals + b, 1u);
-      s_last = (prev == (unsigned int)(N * chunks - 1));
-    }
-  }
+  if ((tid & 31) == 0) s_red[tid >> 5] = a;
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  ArgMax r = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kGreedyThreads / 32; ++w) r = argmax_combine(r, s_red[w]);
+  return r;
+}
 
-  // ---------------- tree scan for sequence b (last CTA only) ----------------
+// Longest matching branch of tree b (run by one CTA after every row key of b is final).
+__device__ void tree_scan(const GreedyArgs& g, int b) {
   __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes], s_am[kMaxNodes];
   __shared__ int32_t s_valid[kMaxNodes], s_jump[kMaxNodes];
   __shared__ unsigned int s_best;
-  const int32_t* par = parent + (size_t)b * N;
-  const int32_t* tok = tokens + (size_t)b * N;
-  const int32_t* dep = depth + (size_t)b * N;
+  const int tid = threadIdx.x;
+  const int N = g.N;
+  const int32_t* par = g.parent + (size_t)b * N;
+  const int32_t* tok = g.tokens + (size_t)b * N;
+  const int32_t* dep = g.depth + (size_t)b * N;
   int bad_tree = 0, bad_tok = 0;
+  __syncthreads();
   for (int i = tid; i < N; i += kGreedyThreads) {
-    const unsigned long long key = atomicExch(ws.keys + (size_t)b * N + i, 0ull);
+    const unsigned long long key = atomicExch(g.ws.keys + (size_t)b * N + i, 0ull);
     const int am = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
     s_am[i] = am;
-    argmax_out[(size_t)b * N + i] = am;
+    g.argmax[(size_t)b * N + i] = am;
     const int p = par[i];
     s_par[i] = p;
     s_dep[i] = dep[i];
     bad_tree |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
     if (i > 0) {
       const int t = tok[i];
-      bad_tok |= (t < 0 || t >= V);
+      bad_tok |= (t < 0 || t >= g.V);
     }
   }
   if (tid == 0) {
-    ws.arrivals[b] = 0u;
+    g.ws.arrivals[b] = 0u;
     s_best = 0u;
   }
   bad_tree = __syncthreads_or(bad_tree);
@@ -130,12 +110,12 @@ greedy_kernel(const float* __restrict__ logits, const int32_t* __restrict__ toke
   }
   bad_tree = __syncthreads_or(bad_tree);
   bad_tok = __syncthreads_or(bad_tok);
-  int32_t* pth = path + (size_t)b * N;
+  int32_t* pth = g.path + (size_t)b * N;
   if (bad_tree || bad_tok) {
     for (int i = tid; i < N; i += kGreedyThreads) pth[i] = -1;
     if (tid == 0) {
-      accept_len[b] = end_node[b] = bonus[b] = -1;
-      status[b] = bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
+      g.accept_len[b] = g.end_node[b] = g.bonus[b] = -1;
+      g.status[b] = bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
     }
     return;
   }
@@ -180,12 +160,108 @@ greedy_kernel(const float* __restrict__ logits, const int32_t* __restrict__ toke
   for (int i = tid; i < N; i += kGreedyThreads)
     if (i > end_depth) pth[i] = -1;
   if (tid == 0) {
-    for (int x2 = end, d = end_depth; x2 >= 0; x2 = s_par[x2], --d) pth[d] = x2;
-    accept_len[b] = end_depth;
-    end_node[b] = end;
-    bonus[b] = s_am[end];
-    status[b] = TV_OK;
+    for (int x = end, d = end_depth; x >= 0; x = s_par[x], --d) pth[d] = x;
+    g.accept_len[b] = end_depth;
+    g.end_node[b] = end;
+    g.bonus[b] = s_am[end];
+    g.status[b] = TV_OK;
   }
+}
+
+// VEC = 4: rows are 16-byte aligned and read as float4; VEC = 1: scalars.
+template <int VEC>
+__global__ void __launch_bounds__(kGreedyThreads)
+greedy_kernel(const GreedyArgs g) {
+  __shared__ ArgMax s_red[kGreedyThreads / 32];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
+  pdl_wait();  // the logits may come from the previous kernel
+  pdl_trigger();
+  const int U = g.V / VEC;  // units per row
+  const long long row = blockIdx.x / g.chunks;
+  const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;
+  const int n = min(g.chunk_units, U - base);
+  const int b = (int)(row / g.N);
+  ArgMax best{-INFINITY, INT_MAX};
+  if (VEC == 4) {
+    const float4* x4 = reinterpret_cast<const float4*>(g.logits + row * (long long)g.V) + base;
+    for (int k0 = 0; k0 < n; k0 += kLoadsInFlight * kGreedyThreads) {
+      float4 buf[kLoadsInFlight];
+#pragma unroll
+      for (int j = 0; j < kLoadsInFlight; ++j) {
+        const int k = k0 + j * kGreedyThreads + tid;
+        buf[j] = (k < n) ? ld_stream_f4(x4 + k)
+                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int j = 0; j < kLoadsInFlight; ++j) {
+        const int k = k0 + j * kGreedyThreads + tid;
+        const int e = 4 * (base + k);
+        if (k < n) {
+          if (buf[j].x > best.v) best = {buf[j].x, e};
+          if (buf[j].y > best.v) best = {buf[j].y, e + 1};
+          if (buf[j].z > best.v) best = {buf[j].z, e + 2};
+          if (buf[j].w > best.v) best = {buf[j].w, e + 3};
+        }
+      }
+    }
+  } else {
+    const float* x = g.logits + row * (long long)g.V + base;
+    for (int k = tid; k < n; k += kGreedyThreads) {
+      const float v = __ldg(x + k);
+      if (v > best.v) best = {v, base + k};
+    }
+  }
+  if (best.i == INT_MAX) best.i = VEC * base;  // only -inf seen: lowest index of the chunk
+  best = block_argmax(best, s_red);
+  if (tid == 0) {
+    atomicMax(g.ws.keys + row, pack_key(best));
+    __threadfence();
+    const unsigned int prev = atomicAdd(g.ws.arrivals + b, 1u);
+    s_last = (prev == (unsigned int)(g.N * g.chunks - 1));
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    tree_scan(g, b);
+  }
+}
+
+tv_status launch_greedy(const GreedyArgs& in, cudaStream_t stream) {
+  GreedyArgs g = in;
+  const int VEC = ((g.V & 3) == 0) ? 4 : 1;
+  const int U = g.V / VEC;
+  const long long rows = (long long)g.B * g.N;
+  // chunks per row: as many as fit one wave of resident CTAs, at least one
+  const long long slots = (long long)device_sm_count() * kGreedyCtasPerSm;
+  int chunks = (int)(slots / rows);
+  chunks = max(1, min(chunks, ceil_div(U, kGreedyThreads)));
+  g.chunk_units = ceil_div(U, chunks);
+  g.chunks = ceil_div(U, g.chunk_units);
+  const long long ctas = rows * g.chunks;
+  const cudaError_t err =
+      VEC == 4 ? launch_pdl(greedy_kernel<4>, dim3((unsigned)ctas), dim3(kGreedyThreads), 0, stream, g)
+               : launch_pdl(greedy_kernel<1>, dim3((unsigned)ctas), dim3(kGreedyThreads), 0, stream, g);
+  if (err != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
+  return TV_OK;
+}
+
+tv_status check_greedy_args(const float* logits, const int32_t* tokens, const int32_t* parent,
+                            const int32_t* depth, int B, int N, int V, int32_t* argmax,
+                            int32_t* accept_len, int32_t* end_node, int32_t* path, int32_t* bonus,
+                            int32_t* status) {
+  if (B < 0 || N < 1 || N > TV_MAX_NODES || V < 1) return TV_ERR_INVALID_ARG;
+  if (B == 0) return TV_OK;
+  if (!logits || !tokens || !parent || !depth || !argmax || !accept_len || !end_node || !path ||
+      !bonus || !status)
+    return TV_ERR_INVALID_ARG;
+  if ((long long)B * N * (long long)V >= (1ll << 40) || (long long)B * N * ((V + 255) / 256) > 0x7fffffffll)
+    return TV_ERR_UNSUPPORTED;
+  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) != 0) return TV_ERR_INVALID_ARG;
+  return TV_OK;
 }
 
 }  // namespace
@@ -203,25 +279,28 @@ extern "C" tv_status tv_accept_greedy(const float* logits, const int32_t* tokens
                                       int32_t* end_node, int32_t* path, int32_t* bonus,
                                       int32_t* status, void* workspace, size_t ws_bytes,
                                       cudaStream_t stream) {
-  if (B < 0 || N < 1 || N > TV_MAX_NODES || V < 1) return TV_ERR_INVALID_ARG;
-  if (B == 0) return TV_OK;
-  if (!logits || !tokens || !parent || !depth || !argmax || !accept_len || !end_node || !path ||
-      !bonus || !status)
-    return TV_ERR_INVALID_ARG;
-  if ((size_t)B * N * tv::ceil_div(V, tv::kGreedyChunk) > 0x7fffffffu) return TV_ERR_UNSUPPORTED;
+  const tv_status st = tv::check_greedy_args(logits, tokens, parent, depth, B, N, V, argmax,
+                                             accept_len, end_node, path, bonus, status);
+  if (st != TV_OK || B == 0) return st;
   if (!workspace || ws_bytes < tv_accept_greedy_workspace_size(B, N, V)) return TV_ERR_WORKSPACE;
-  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) != 0) return TV_ERR_INVALID_ARG;
-  tv::GreedyWs ws;
-  ws.keys = static_cast<unsigned long long*>(workspace);
-  ws.arrivals = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
-                                                tv::greedy_keys_bytes(B, N));
-  const int chunks = tv::ceil_div(V, tv::kGreedyChunk);
-  dim3 grid(chunks * B * N);
-  tv::greedy_kernel<<<grid, tv::kGreedyThreads, 0, stream>>>(
-      logits, tokens, parent, depth, N, V, chunks, argmax, accept_len, end_node, path, bonus,
-      status, ws);
-  TV_CHECK_LAUNCH();
-  return TV_OK;
+  tv::GreedyArgs g = {};
+  g.logits = logits;
+  g.tokens = tokens;
+  g.parent = parent;
+  g.depth = depth;
+  g.B = B;
+  g.N = N;
+  g.V = V;
+  g.argmax = argmax;
+  g.accept_len = accept_len;
+  g.end_node = end_node;
+  g.path = path;
+  g.bonus = bonus;
+  g.status = status;
+  g.ws.keys = static_cast<unsigned long long*>(workspace);
+  g.ws.arrivals = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
+                                                  tv::greedy_keys_bytes(B, N));
+  return tv::launch_greedy(g, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -235,8 +314,6 @@ extern "C" tv_status tv_accept_greedy(const float* logits, const int32_t* tokens
 // scratch -- one 64-bit key per node row and one arrival counter per sequence
 // -- lives in a fixed-size file-scope __device__ array, which every GPU that
 // loads this library holds until the process exits.
-#include <mutex>
-
 namespace tv {
 namespace {
 
@@ -259,14 +336,10 @@ extern "C" tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t
                                               int N, int V, int32_t* argmax, int32_t* accept_len,
                                               int32_t* end_node, int32_t* path, int32_t* bonus,
                                               int32_t* status, cudaStream_t stream) {
-  if (B < 0 || N < 1 || N > TV_MAX_NODES || V < 1) return TV_ERR_INVALID_ARG;
-  if (B == 0) return TV_OK;
-  if (!logits || !tokens || !parent || !depth || !argmax || !accept_len || !end_node || !path ||
-      !bonus || !status)
-    return TV_ERR_INVALID_ARG;
+  const tv_status st = tv::check_greedy_args(logits, tokens, parent, depth, B, N, V, argmax,
+                                             accept_len, end_node, path, bonus, status);
+  if (st != TV_OK || B == 0) return st;
   if ((long long)B * N > tv::kStaticMaxRows || B > tv::kStaticMaxSeqs) return TV_ERR_UNSUPPORTED;
-  if ((size_t)B * N * tv::ceil_div(V, tv::kGreedyChunk) > 0x7fffffffu) return TV_ERR_UNSUPPORTED;
-  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) != 0) return TV_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -296,13 +369,21 @@ extern "C" tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t
     (void)cudaGetLastError();
     return TV_ERR_CUDA;
   }
-  tv::GreedyWs ws;
-  ws.keys = reinterpret_cast<unsigned long long*>(b8);
-  ws.arrivals = reinterpret_cast<unsigned int*>(b8 + tv::kStaticKeyBytes);
-  const int chunks = tv::ceil_div(V, tv::kGreedyChunk);
-  tv::greedy_kernel<<<dim3(chunks * B * N), tv::kGreedyThreads, 0, stream>>>(
-      logits, tokens, parent, depth, N, V, chunks, argmax, accept_len, end_node, path, bonus,
-      status, ws);
-  TV_CHECK_LAUNCH();
-  return TV_OK;
+  tv::GreedyArgs g = {};
+  g.logits = logits;
+  g.tokens = tokens;
+  g.parent = parent;
+  g.depth = depth;
+  g.B = B;
+  g.N = N;
+  g.V = V;
+  g.argmax = argmax;
+  g.accept_len = accept_len;
+  g.end_node = end_node;
+  g.path = path;
+  g.bonus = bonus;
+  g.status = status;
+  g.ws.keys = reinterpret_cast<unsigned long long*>(b8);
+  g.ws.arrivals = reinterpret_cast<unsigned int*>(b8 + tv::kStaticKeyBytes);
+  return tv::launch_greedy(g, stream);
 }

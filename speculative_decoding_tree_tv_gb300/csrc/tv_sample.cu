@@ -31,6 +31,8 @@ struct RowPartial {
 __global__ void __launch_bounds__(kStatThreads)
 row_stats_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logits, int rows,
                  int V, int chunks, float inv_t, RowPartial* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x / chunks;
   const int chunk = blockIdx.x % chunks;
   const int which = blockIdx.y;  // 0: p, 1: q
@@ -130,6 +132,8 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
             int32_t* __restrict__ accept_len, int32_t* __restrict__ end_node,
             int32_t* __restrict__ path, int32_t* __restrict__ out_token,
             int32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int rows = gridDim.x * N;
@@ -329,13 +333,14 @@ extern "C" tv_status tv_accept_sample(const float* p_logits, const float* q_logi
   const float inv_t = 1.0f / temperature;
   auto* part = static_cast<tv::RowPartial*>(workspace);
   dim3 g1(chunks * B * N, 2);
-  tv::row_stats_kernel<<<g1, tv::kStatThreads, 0, stream>>>(p_logits, q_logits, B * N, V, chunks,
-                                                            inv_t, part);
-  TV_CHECK_LAUNCH();
-  tv::walk_kernel<<<B, tv::kWalkThreads, 0, stream>>>(p_logits, q_logits, tokens, parent, depth,
-                                                      N, V, chunks, inv_t, seed, offset, part,
-                                                      accept_len, end_node, path, out_token,
-                                                      status);
-  TV_CHECK_LAUNCH();
+  if (tv::launch_pdl(tv::row_stats_kernel, g1, dim3(tv::kStatThreads), 0, stream, p_logits,
+                     q_logits, B * N, V, chunks, inv_t, part) != cudaSuccess ||
+      tv::launch_pdl(tv::walk_kernel, dim3(B), dim3(tv::kWalkThreads), 0, stream, p_logits,
+                     q_logits, tokens, parent, depth, N, V, chunks, inv_t, seed, offset,
+                     (const tv::RowPartial*)part, accept_len, end_node, path, out_token,
+                     status) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
   return TV_OK;
 }

@@ -15,6 +15,8 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
                   uint64_t* __restrict__ anc_mask, int32_t* __restrict__ status) {
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ uint64_t s_anc[kMaxNodes * kMaxWords];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int32_t* par = parent + (size_t)b * N;
   int32_t* dep = depth + (size_t)b * N;
@@ -57,7 +59,10 @@ extern "C" tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t*
   if (B == 0) return TV_OK;
   if (!parent || !depth || !anc_mask || !status) return TV_ERR_INVALID_ARG;
   const int W = tv::ceil_div(N, 64);
-  tv::tree_build_kernel<<<B, tv::kTreeThreads, 0, stream>>>(parent, N, W, depth, anc_mask, status);
-  TV_CHECK_LAUNCH();
+  if (tv::launch_pdl(tv::tree_build_kernel, dim3(B), dim3(tv::kTreeThreads), 0, stream, parent, N,
+                     W, depth, anc_mask, status) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
   return TV_OK;
 }
