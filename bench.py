@@ -292,8 +292,11 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = measure_e2e(args, torch, tv, case, sets, step, gouts, stream, device)
 
+    # tree, attention (+ its split-KV merge when the plan splits), greedy
+    launches = 3 + int(tv.attn_workspace_size(case.B, case.N, case.Hq, case.Hkv, case.D,
+                                               case.Lcap) > 0)
     return dict(case=case, elapsed_ms=elapsed_ms, per_kernel=per_kernel, clocks=clocks, M=M,
-                set_bytes=set_bytes, l2=l2, e2e=e2e)
+                set_bytes=set_bytes, l2=l2, e2e=e2e, launches_per_step=launches)
 
 
 def measure_e2e(args, torch, tv, case, sets, step, gouts, stream, device):
@@ -498,7 +501,7 @@ def main():
                      "peak_source": f"{peak_src} hbm_gbs",
                      "bytes_per_launch": nbytes["greedy"]},
         "kernels": {k: {"us_per_launch": v} for k, v in pk.items()},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
     line["kernels"]["tv_attn_verify"].update(

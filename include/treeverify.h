@@ -124,8 +124,13 @@ tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
  *   status    int32 [B] out          0, or TV_ERR_INVALID_ARG when kv_len[b] < 0
  *                                    or kv_len[b] + N > Lcap (outputs zeroed);
  *                                    may be NULL.
- *   workspace unused: tv_attn_workspace_size() returns 0 and workspace may be
- *             NULL (the split-KV merge runs in distributed shared memory).
+ *   workspace scratch of tv_attn_workspace_size() bytes, 256-byte aligned,
+ *             any contents (not zero-filled; left holding the split-KV
+ *             partials).  The size is 0 when the plan keeps each row tile's
+ *             key range in one CTA; workspace may then be NULL.  Otherwise
+ *             the key range of every 128-row tile is split over several CTAs
+ *             and the call launches a second (merge) kernel; a workspace that
+ *             is NULL, misaligned or smaller returns TV_ERR_WORKSPACE.
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= TV_MAX_NODES; Lcap >= N.
  */
 size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap);

@@ -17,11 +17,12 @@
 //              tcgen05.mma (bf16 operands in shared memory, fp32 accumulators
 //              in TMEM); zeroes V rows past the end of the key range so that
 //              stale cache slots never reach a result.
-// The two halves are merged in shared memory.  When the key range is split
-// across CTAs, the splits of one row tile form a thread-block cluster: each
-// pushes its (max, sum, O) partial into the owner CTA's shared memory with
-// remote stores, and after one cluster barrier each owner reduces its rows.
-// No global scratch, no second launch; every mbarrier wait is bounded.
+// When one CTA covers the whole key range, the two halves are merged in shared
+// memory and the CTA writes the output rows.  When the key range is split
+// across CTAs, each split stages its two normalised fp16 partials and stores
+// them to the workspace with one bulk copy, its (max, sum) statistics beside
+// them; a merge kernel, chained by programmatic dependent launch, combines
+// the 2 x nsplit partials of every row.  Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,7 +45,7 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale max while within 2^8
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
-constexpr int kMaxCluster = 16;
+constexpr int kMaxSplit = 32;         // splits of one row tile's key range
 
 struct AttnParams {
   const uint16_t* q;
@@ -53,8 +54,10 @@ struct AttnParams {
   int32_t* status;
   const int32_t* kv_len;
   const uint64_t* anc;
+  __half* part;    // split partials [unit][2 * nsplit][128][D] fp16, chunks swizzled
+  float2* part_ml; // their (running max in the log2 domain, running sum) [unit][2 * nsplit][128]
   int N, Hq, Hkv, G, Lcap, W;
-  int nsplit;  // splits per row tile (= cluster size when > 1)
+  int nsplit;      // splits per row tile
   float scale_log2;
 };
 
@@ -69,11 +72,8 @@ struct Layout {
   static constexpr int kDyn = kBytes + 1024;       // slack for 1024-byte alignment
   // TMEM: S at [0, 128), O_0 at [128, 128 + D), O_1 at [128 + D, 128 + 2D)
   static constexpr uint32_t kTmemCols = (128 + 2 * D <= 256) ? 256u : 512u;
-  // merge statistics at kQ (Q and P are dead by then): three [slot][row]
-  // float arrays of 2 * 16 slots x 64 rows (or 2 slots x 128 rows)
-  static_assert(3 * 2 * kMaxCluster * (kBM / 2) * 4 <= kKV, "merge statistics must fit Q + P");
-  // receive buffer at kKV: fp16 rows, two slots per rank, ceil(128 / nsplit) rows each
-  static_assert(2 * (kBM + kMaxCluster) * D * 2 <= kStages * kStage, "receive buffer");
+  // epilogue staging at kQ (Q and P are dead by then): 2 groups x 128 fp16 rows
+  static_assert(2 * kBM * D * 2 <= kKV, "staging must fit Q + P");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -127,15 +127,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   uint8_t* sQ = smem + Lay::kQ;
   uint8_t* sP = smem + Lay::kP;
   uint8_t* sKV = smem + Lay::kKV;
-  float* sStat = reinterpret_cast<float*>(smem + Lay::kQ);  // merge statistics, at the end
-  __half* sRecv = reinterpret_cast<__half*>(sKV);           // partial O rows, at the end
 
   __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ __align__(8) uint64_t bar_q, bar_s_full, bar_s_free, bar_drain;
   __shared__ __align__(8) uint64_t bar_p_full[2], bar_o_done[2];
+  __shared__ float s_gm[2][kBM], s_gl[2][kBM];  // per group: running max and sum of each row
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ float s_M[kBM], s_L[kBM];  // merged max and sum of the rows this CTA owns
 
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_trigger();
@@ -153,9 +151,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int node = valid_row ? r / p.G : 0;
   const int h = kvh * p.G + (valid_row ? r % p.G : 0);
   const int nranks = p.nsplit;
-  const bool clustered = nranks > 1;
 
-  if (L < 0 || L + N > p.Lcap) {  // uniform over the whole cluster: all of it leaves
+  if (L < 0 || L + N > p.Lcap) {  // the merge kernel skips this sequence too
     if (split == 0 && valid_row && grp == 0) {
       uint4* o = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
 #pragma unroll
@@ -412,130 +409,192 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   tc_fence_after();
   if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-
-  // 1. Every CTA of the cluster must be past its main loop before anyone
-  //    writes into its Q/P and K/V space, which now hold the merge buffers.
-  if (clustered) {
-    cluster_sync();
-  } else {
-    __syncthreads();
-  }
-  // 2. Every softmax thread hands its group's partial for its row -- running
-  //    max, sum and the normalised O row in fp16 -- to the rank owning the row
-  //    (itself without a cluster), slot 2 * split + group.
-  const int per = ceil_div(kBM, nranks);  // rows per owner rank
-  const int slots = 2 * nranks;
-  float* s_mx = sStat;                    // [slot][per] partial max (log2)
-  float* s_sm = sStat + 2 * kMaxCluster * kBM / 2;          // [slot][per] partial sum
-  float* s_cf = sStat + 2 * (2 * kMaxCluster * kBM / 2);    // [slot][per] merge weight
+  // Each softmax thread stages its group's normalised O row in fp16 at kQ
+  // (Q and P are dead now) as [group][row][D], 16-byte chunks swizzled by the
+  // row, with the group's running (max, sum) beside it.
+  uint8_t* sStage = smem + Lay::kQ;
+  const bool split_kv = p.nsplit > 1;
+  const size_t unit = (size_t)bh * gridDim.y + mt;  // (sequence, kv head, row tile)
   if (is_softmax) {
-    const int owner = row / per, lr = row - owner * per;
-    const int sl = 2 * split + grp;
-    const int si = sl * per + lr;
-    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-    const uint32_t rrow = smem_u32(sRecv) + (uint32_t)(si * D * 2);
-    if (clustered) {
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(s_mx + si), owner)),
-                   "f"(m_run)
-                   : "memory");
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dsmem_map(smem_u32(s_sm + si), owner)),
-                   "f"(l_run)
-                   : "memory");
-    } else {
-      s_mx[si] = m_run;
-      s_sm[si] = l_run;
+    s_gm[grp][row] = m_run;
+    s_gl[grp][row] = l_run;
+    if (split_kv) {
+      const size_t si = (unit * (2 * p.nsplit) + 2 * split + grp) * kBM + row;
+      p.part_ml[si] = make_float2(m_run, l_run);
     }
-    const uint32_t rbase = clustered ? dsmem_map(rrow, owner) : rrow;
+    uint32_t o[D / 32][32];
+    if (T > 0) {
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t o[32];
-      if (T > 0) {
-        tmem_ld32((grp ? tO1 : tO0) + lane_base + c, o);
-        tmem_wait_ld();
-      } else {
+      for (int c = 0; c < D / 32; ++c) tmem_ld32((grp ? tO1 : tO0) + lane_base + 32 * c, o[c]);
+      tmem_wait_ld();
+    } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-      }
+      for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[c][e] = 0u;
+    }
+    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    uint8_t* srow = sStage + (size_t)(grp * kBM + row) * D * 2;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {  // four 16-byte chunks of 8 halves
         uint32_t hw[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const __half2 hv = __floats2half2_rn(__uint_as_float(o[8 * e + 2 * j]) * inv,
-                                               __uint_as_float(o[8 * e + 2 * j + 1]) * inv);
+          const __half2 hv = __floats2half2_rn(__uint_as_float(o[c][8 * e + 2 * j]) * inv,
+                                               __uint_as_float(o[c][8 * e + 2 * j + 1]) * inv);
           hw[j] = *reinterpret_cast<const uint32_t*>(&hv);
         }
-        const uint32_t addr = rbase + (uint32_t)(swz_chunk(lr, c / 8 + e) * 16);
-        if (clustered)
-          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hw[0]),
-                       "r"(hw[1]), "r"(hw[2]), "r"(hw[3])
-                       : "memory");
-        else
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hw[0]),
-                       "r"(hw[1]), "r"(hw[2]), "r"(hw[3])
-                       : "memory");
+        *reinterpret_cast<uint4*>(srow + swz_chunk(row, 4 * c + e) * 16) =
+            make_uint4(hw[0], hw[1], hw[2], hw[3]);
       }
     }
-  }
-  if (clustered) {
-    cluster_sync();  // every partial has landed in its owner's shared memory
-  } else {
-    __syncthreads();
-  }
-  // 3. owners merge their rows: weights exp2(m_s - M) * l_s / sum, then a
-  //    weighted sum of the normalised partial rows
-  const int row0 = split * per, nrows = max(0, min(kBM, row0 + per) - row0);
-  for (int lr = tid; lr < nrows; lr += kThreads) {
-    float M = -INFINITY;
-    for (int sl = 0; sl < slots; ++sl) M = fmaxf(M, s_mx[sl * per + lr]);
-    float lsum = 0.0f;
-    for (int sl = 0; sl < slots; ++sl) {
-      const float ms = s_mx[sl * per + lr];
-      const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M) * s_sm[sl * per + lr];
-      s_cf[sl * per + lr] = w;
-      lsum += w;
-    }
-    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-    for (int sl = 0; sl < slots; ++sl) s_cf[sl * per + lr] *= inv;
-    s_M[lr] = M;
-    s_L[lr] = lsum;
+    if (split_kv) fence_async_smem();  // the bulk store reads the staging area
   }
   __syncthreads();
-  constexpr int kC16 = D / 8;  // 16-byte chunks of an fp16 row
-  for (int idx = tid; idx < nrows * kC16; idx += kThreads) {
-    const int lr = idx / kC16, ch = idx % kC16;
-    const int gr = mt * kBM + row0 + lr;
-    if (gr >= rows_total) continue;
-    float acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int sl = 0; sl < slots; ++sl) {
-      const float cw = s_cf[sl * per + lr];
-      if (cw == 0.0f) continue;
-      const uint4 x = *reinterpret_cast<const uint4*>(
-          reinterpret_cast<const uint8_t*>(sRecv) + (size_t)(sl * per + lr) * D * 2 +
-          swz_chunk(lr, ch) * 16);
-      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  if (split_kv) {
+    // the partial rows go to the workspace; tv_attn_merge finishes them
+    if (tid == 0 && T > 0) {
+      __half* dst = p.part + (unit * (2 * p.nsplit) + 2 * split) * kBM * D;
+      bulk_store_global(dst, smem_u32(sStage), (uint32_t)(2 * kBM * D * 2));
+      bulk_commit();
+      bulk_wait_all();
+    }
+  } else {
+    // merge the two key halves of each row here.  A warp takes 32 / (D / 8)
+    // rows; the lanes of a row cover its 16-byte fp16 chunks.
+    constexpr int kC16 = D / 8;
+    constexpr int kRowsPerWarp = 32 / kC16;
+    const int sub = lane / kC16, ch = lane % kC16;
+    for (int rb = warp * kRowsPerWarp; rb < kBM; rb += (kThreads / 32) * kRowsPerWarp) {
+      const int lr = rb + sub;
+      const int gr = mt * kBM + lr;
+      if (gr >= rows_total) continue;
+      const float m0 = s_gm[0][lr], m1 = s_gm[1][lr];
+      const float M = fmaxf(m0, m1);
+      const float w0 = (m0 == -INFINITY) ? 0.0f : exp2f(m0 - M) * s_gl[0][lr];
+      const float w1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - M) * s_gl[1][lr];
+      const float L = w0 + w1;
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      const uint4 x0 = *reinterpret_cast<const uint4*>(sStage + (size_t)lr * D * 2 + swz_chunk(lr, ch) * 16);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(sStage + (size_t)(kBM + lr) * D * 2 + swz_chunk(lr, ch) * 16);
+      const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c1[4] = {x1.x, x1.y, x1.z, x1.w};
+      uint32_t u[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[j]));
-        acc[2 * j] += cw * f.x;
-        acc[2 * j + 1] += cw * f.y;
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&a[j]));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&c1[j]));
+        u[j] = pack_bf16((w0 * f0.x + w1 * f1.x) * inv, (w0 * f0.y + w1 * f1.y) * inv);
       }
+      const size_t orow = ((size_t)b * N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
+      *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) = make_uint4(u[0], u[1], u[2], u[3]);
+      if (ch == 0 && p.lse)
+        p.lse[orow] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
-    const size_t orow = ((size_t)b * N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
-    uint4 u;
-    u.x = pack_bf16(acc[0], acc[1]);
-    u.y = pack_bf16(acc[2], acc[3]);
-    u.z = pack_bf16(acc[4], acc[5]);
-    u.w = pack_bf16(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) = u;
-    if (ch == 0 && p.lse)
-      p.lse[orow] = s_L[lr] > 0.0f ? (s_M[lr] + log2f(s_L[lr])) * 0.69314718055994531f : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, Lay::kTmemCols);
+}
+
+// Merge of the split-KV partials: for every query row, weights
+// exp2(m_s - M) * l_s over the 2 * nsplit partials (two key halves per
+// split), normalised, applied to the normalised fp16 partial rows.  A CTA
+// takes kRows = 256 / (D / 8) rows of one row tile; kC16 = D / 8 threads per
+// row.  Every load of a phase is issued before the first one is used, so the
+// kernel pays about one L2 round trip per phase.
+template <int D>
+__global__ void __launch_bounds__(256)
+attn_merge_kernel(const AttnParams p, int mtiles) {
+  constexpr int kC16 = D / 8;
+  constexpr int kRows = 256 / kC16;
+  constexpr int kMaxSlots = 2 * kMaxSplit;
+  constexpr int kSPT = kMaxSlots / kC16;  // statistics phase: slots per thread
+  constexpr int kBatch = 16;              // accumulation phase: loads in flight per thread
+  __shared__ float s_w[kMaxSlots][kRows];
+  __shared__ float s_inv[kRows], s_lse[kRows];
+  pdl_wait();  // the partials come from the attention kernel
+  pdl_trigger();
+  const int cpu = kBM / kRows;  // CTAs per row tile
+  const int unit = blockIdx.x / cpu;
+  const int rbase = (blockIdx.x % cpu) * kRows;
+  const int bh = unit / mtiles, mt = unit % mtiles;
+  const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+  const int L = p.kv_len[b];
+  if (L < 0 || L + p.N > p.Lcap) return;  // the attention kernel zeroed these outputs
+  const int nslots = 2 * p.nsplit;
+  const int tid = threadIdx.x;
+  const int r = tid / kC16, j = tid % kC16;  // row of this CTA; lane within the row's group
+  const int row = rbase + r;
+  const size_t sbase = (size_t)unit * nslots * kBM;
+  {
+    // statistics: the kC16 threads of a row take slots j, j + kC16, ...
+    float2 ml[kSPT];
+#pragma unroll
+    for (int k = 0; k < kSPT; ++k) {
+      const int sl = j + kC16 * k;
+      ml[k] = sl < nslots ? __ldg(p.part_ml + sbase + (size_t)sl * kBM + row)
+                          : make_float2(-INFINITY, 0.0f);
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kSPT; ++k) M = fmaxf(M, ml[k].x);
+#pragma unroll
+    for (int o = kC16 / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Ls = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kSPT; ++k) {
+      const int sl = j + kC16 * k;
+      const float w = (ml[k].x == -INFINITY) ? 0.0f : exp2f(ml[k].x - M) * ml[k].y;
+      if (sl < nslots) s_w[sl][r] = w;
+      Ls += w;
+    }
+#pragma unroll
+    for (int o = kC16 / 2; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    if (j == 0) {
+      s_inv[r] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+      s_lse[r] = Ls > 0.0f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  __syncthreads();
+  const int gr = mt * kBM + row;
+  if (gr >= p.N * p.G) return;
+  const int ch = j;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part) +
+                       ((size_t)unit * nslots * kBM + row) * D * 2 + swz_chunk(row, ch) * 16;
+  for (int s0 = 0; s0 < nslots; s0 += kBatch) {
+    uint4 x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      x[k] = (s0 + k < nslots) ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(s0 + k) * kBM * D * 2))
+                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (s0 + k >= nslots) break;
+      const float w = s_w[s0 + k][r];
+      if (w == 0.0f) continue;  // an empty split: its rows were never written
+      const uint32_t xw[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[e]));
+        acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
+      }
+    }
+  }
+  const float inv = s_inv[r];
+  const size_t orow = ((size_t)b * p.N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
+  uint4 u;
+  u.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  u.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  u.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  u.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) = u;
+  if (ch == 0 && p.lse) p.lse[orow] = s_lse[r];
 }
 
 // --------------------------------------------------------------------- host
@@ -554,71 +613,27 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// How many clusters of each size (1..16) of this kernel the device can hold
-// at once; entry 1 is the number of CTAs that fit (one per SM).
-template <int D>
-const int* cluster_capacity() {
-  static int cap[kMaxCluster + 1] = {0};
-  static bool done = false;
-  if (!done) {
-    using Lay = Layout<D>;
-    cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDyn);
-    cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    (void)cudaGetLastError();
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 0;
-    (void)cudaGetLastError();
-    cap[1] = sms;
-    for (int cs = 2; cs <= kMaxCluster; ++cs) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(cs, 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = Lay::kDyn;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = cs;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D>, &cfg) != cudaSuccess) n = 0;
-      (void)cudaGetLastError();
-      cap[cs] = n;
-    }
-    done = true;
-  }
-  return cap;
-}
-
 struct SplitPlan {
   int mtiles, nsplit;
+  long long units;  // (sequence, kv head, row tile) triples
 };
 
-// Choose the split count (= cluster size) that minimises
-// (waves of clusters) x (tiles per CTA + fixed cost), preferring fewer splits.
-// Without a device (capacities unknown) the plan assumes 152 SMs and clusters
-// of up to 8.
-SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap, const int* cap) {
+// Choose the split count that minimises
+// (waves of CTAs) x (tiles per CTA + fixed cost) + merge cost, preferring
+// fewer splits.  One CTA fits an SM (its shared memory decides that).
+SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
   SplitPlan sp;
   const int G = Hq / Hkv;
   sp.mtiles = ceil_div(N * G, kBM);
-  const long long units = (long long)B * Hkv * sp.mtiles;
+  sp.units = (long long)B * Hkv * sp.mtiles;
   const int tiles_max = ceil_div(Lcap, kBN);
+  const long long slots = device_sm_count();
   long long best = -1;
   sp.nsplit = 1;
-  for (int ns = 1; ns <= kMaxCluster && ns <= tiles_max; ++ns) {
-    long long slots;
-    if (cap[1] > 0)
-      slots = (ns == 1) ? cap[1] : cap[ns];
-    else
-      slots = (ns <= 8) ? 152 / ns : 0;
-    if (slots <= 0) continue;
-    const long long waves = (units + slots - 1) / slots;
+  for (int ns = 1; ns <= kMaxSplit && ns <= tiles_max; ++ns) {
+    const long long waves = (sp.units * ns + slots - 1) / slots;
     const long long tiles_per_cta = (tiles_max + ns - 1) / ns;
-    const long long cost = waves * (tiles_per_cta * 4 + 10) + (ns > 1 ? 4 : 0);
+    const long long cost = waves * (tiles_per_cta * 4 + 10) + (ns > 1 ? 6 : 0);
     if (best < 0 || cost < best) {
       best = cost;
       sp.nsplit = ns;
@@ -627,15 +642,35 @@ SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap, const int* cap) {
   return sp;
 }
 
+// Workspace bytes of a plan: fp16 partial rows, then their (max, sum) pairs.
+size_t plan_workspace(const SplitPlan& sp, int D) {
+  if (sp.nsplit <= 1) return 0;
+  const size_t rows = (size_t)sp.units * 2 * sp.nsplit * kBM;
+  return align_up(rows * D * 2, 256) + align_up(rows * 8, 256);
+}
+
 template <int D>
 tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, const int32_t* kv_len,
                       const uint64_t* anc_mask, int B, int N, int Hq, int Hkv, int Lcap,
                       float scale_log2, tv_bf16* out, float* lse, int32_t* status,
-                      cudaStream_t stream) {
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
   using Lay = Layout<D>;
+  const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap);
+  const size_t need = plan_workspace(sp, D);
+  if (need > 0 && (workspace == nullptr || ws_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255)))
+    return TV_ERR_WORKSPACE;
   auto encode = tensor_map_encoder();
   if (!encode) return TV_ERR_CUDA;
-  const int* cap = cluster_capacity<D>();
+  static bool smem_set = false;
+  if (!smem_set) {
+    if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay::kDyn) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TV_ERR_CUDA;
+    }
+    smem_set = true;
+  }
   CUtensorMap tmK, tmV;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)B * Hkv * Lcap};
   const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
@@ -649,7 +684,6 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return TV_ERR_INVALID_ARG;
-  const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap, cap);
   AttnParams p;
   p.q = q;
   p.out = out;
@@ -657,6 +691,14 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.status = status;
   p.kv_len = kv_len;
   p.anc = anc_mask;
+  p.part = nullptr;
+  p.part_ml = nullptr;
+  if (need > 0) {
+    const size_t rows = (size_t)sp.units * 2 * sp.nsplit * kBM;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.part = reinterpret_cast<__half*>(ws);
+    p.part_ml = reinterpret_cast<float2*>(ws + align_up(rows * D * 2, 256));
+  }
   p.N = N;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -665,33 +707,34 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.W = ceil_div(N, 64);
   p.nsplit = sp.nsplit;
   p.scale_log2 = scale_log2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sp.nsplit, sp.mtiles, B * Hkv);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Lay::kDyn;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = sp.nsplit;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = sp.nsplit > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tmK, tmV, p) != cudaSuccess) {
+  if (launch_pdl(attn_tc_kernel<D>, dim3(sp.nsplit, sp.mtiles, B * Hkv), dim3(kThreads, 1, 1),
+                 (size_t)Lay::kDyn, stream, tmK, tmV, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;
   }
+  if (sp.nsplit > 1) {
+    constexpr int kRows = 256 / (D / 8);
+    const long long ctas = sp.units * (kBM / kRows);
+    if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)ctas, 1, 1), dim3(256, 1, 1), 0, stream, p,
+                   sp.mtiles) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TV_ERR_CUDA;
+    }
+  }
   return TV_OK;
+}
+
+bool attn_shape_ok(int B, int N, int Hq, int Hkv, int D, int Lcap) {
+  return B >= 0 && N >= 1 && N <= TV_MAX_NODES && Hq >= 1 && Hkv >= 1 && Lcap >= N &&
+         Hq % Hkv == 0 && (D == 64 || D == 128);
 }
 
 }  // namespace
 }  // namespace tv
 
 extern "C" size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap) {
-  (void)B; (void)N; (void)Hq; (void)Hkv; (void)D; (void)Lcap;
-  return 0;
+  if (!tv::attn_shape_ok(B, N, Hq, Hkv, D, Lcap) || B == 0) return 0;
+  return tv::plan_workspace(tv::plan_splits(B, N, Hq, Hkv, Lcap), D);
 }
 
 extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
@@ -699,8 +742,6 @@ extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv
                                     int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,
                                     float* lse, int32_t* status, void* workspace, size_t ws_bytes,
                                     cudaStream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Lcap < N) return TV_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return TV_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return TV_ERR_UNSUPPORTED;
@@ -715,7 +756,7 @@ extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv
   const float scale_log2 = sc * 1.4426950408889634f;
   if (D == 128)
     return tv::launch_attn<128>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out,
-                                lse, status, stream);
+                                lse, status, workspace, ws_bytes, stream);
   return tv::launch_attn<64>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out, lse,
-                             status, stream);
+                             status, workspace, ws_bytes, stream);
 }

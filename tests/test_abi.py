@@ -49,7 +49,11 @@ def test_workspace_sizes_are_positive(tvlib):
     assert tvlib.greedy_workspace_size(1, 60, 128256) >= 60 * 8
     assert tvlib.sample_workspace_size(16, 64, 128256) >= 2 * 16 * 64 * 16
     assert tvlib.expand_workspace_size(511, 32000) >= 511 * 32000 * 8
-    assert tvlib.attn_workspace_size(1, 60, 32, 8, 128, 2108) == 0   # merge runs in DSMEM
+    # a 2108-slot cache over 16 row tiles is split across CTAs: partials + stats
+    ws = tvlib.attn_workspace_size(1, 60, 32, 8, 128, 2108)
+    assert ws >= 2 * 16 * 128 * (128 * 2 + 8)
+    # one 128-key tile cannot be split: no workspace
+    assert tvlib.attn_workspace_size(1, 60, 32, 8, 128, 128) == 0
 
 
 def test_host_side_argument_errors_launch_nothing(tvlib):
@@ -68,6 +72,9 @@ def test_host_side_argument_errors_launch_nothing(tvlib):
                               None) == tvlib.TV_ERR_INVALID_ARG
     assert lib.tv_attn_verify(*args, 1, 4, 8, 8, 64, 64, -1.0, dummy, None, None, dummy, 256,
                               None) == tvlib.TV_ERR_INVALID_ARG
+    # attention: a split key range needs the partials workspace
+    assert lib.tv_attn_verify(*args, 1, 60, 32, 8, 128, 2108, 0.0, dummy, None, None, None, 0,
+                              None) == tvlib.TV_ERR_WORKSPACE
     # greedy: workspace too small
     assert lib.tv_accept_greedy(dummy, dummy, dummy, dummy, 2, 8, 100, dummy, dummy, dummy,
                                 dummy, dummy, dummy, dummy, 8, None) == tvlib.TV_ERR_WORKSPACE
