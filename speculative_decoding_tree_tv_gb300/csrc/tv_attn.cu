@@ -3,26 +3,29 @@
 // tree attention mask; a node sees the cached prefix, its ancestors and
 // itself).
 //
-// One CTA owns 128 query rows of one (sequence, kv head) -- the GQA group's
-// rows (node, head) flattened as node * G + g -- and a range of 128-key tiles
-// of that kv head's key range [0, kv_len + N).  Warp roles (320 threads):
-//   warps 0-7  softmax, two groups of four warps.  Group h owns keys
-//              64h .. 64h+63 of every tile and runs its own online softmax
-//              (log2 domain, lazy rescaling) with its own accumulator O_h in
-//              TMEM; thread (group h, lane) = one query row = one TMEM lane.
-//              The tree mask is applied as 32-bit visibility words;
-//   warp 8     producer: TMA loads of K and V tiles (128-byte swizzle) into a
-//              two-stage ring;
-//   warp 9     MMA: S = Q K^T, then O_h += P_h V_h for each key half, with
-//              tcgen05.mma (bf16 operands in shared memory, fp32 accumulators
-//              in TMEM); zeroes V rows past the end of the key range so that
-//              stale cache slots never reach a result.
-// When one CTA covers the whole key range, the two halves are merged in shared
-// memory and the CTA writes the output rows.  When the key range is split
-// across CTAs, each split stages its two normalised fp16 partials and stores
-// them to the workspace with one bulk copy, its (max, sum) statistics beside
-// them; a merge kernel, chained by programmatic dependent launch, combines
-// the 2 x nsplit partials of every row.  Every mbarrier wait is bounded.
+// One CTA owns up to 256 query rows of one (sequence, kv head): two row
+// blocks of 128 TMEM lanes.  Rows are the GQA group's (node, head) pairs,
+// node-major; a row block holds nb = floor(128 / G) whole nodes, so both
+// blocks share every K/V tile and the cache is streamed once per kv head.
+// The CTA covers a range of 128-key tiles of the key range [0, kv_len + N).
+// Warp roles (320 threads):
+//   warps 0-3, 4-7  softmax of row block 0, 1: one thread per query row (TMEM
+//                   lane), online softmax over the tile's 128 keys in the
+//                   log2 domain with lazy rescaling; the tree mask is applied
+//                   as 32-bit visibility words;
+//   warp 8          producer: TMA loads (128-byte swizzle) of Q once and of
+//                   the K tiles (lane 0) and V tiles (lane 1);
+//   warp 9          MMA issuer: S_r = Q_r K^T and O_r += P_r V with
+//                   tcgen05.mma (bf16 operands in shared memory, fp32
+//                   accumulators in TMEM), each issued as soon as its inputs
+//                   are ready, so the next tile's S overlaps this tile's
+//                   softmax; zeroes V rows past the end of the key range so
+//                   that stale cache slots never reach a result.
+// Unsplit, each softmax thread normalises its row and writes it.  When the
+// key range is split across CTAs, each split stores its normalised fp16
+// partial rows to the workspace with one bulk copy, with (max, sum) pairs
+// beside them, and a merge kernel chained by programmatic dependent launch
+// combines the partials of every row.  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -36,48 +39,51 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBM = 128;              // query rows per CTA = TMEM lanes
-constexpr int kBN = 128;              // keys per tile (two halves of 64)
-constexpr int kStages = 2;            // K/V ring depth
-constexpr int kSoftmaxThreads = 256;  // two groups of four warps
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kRB = 128;              // rows per row block = TMEM lanes
+constexpr int kRows = 2 * kRB;        // rows per CTA
+constexpr int kBN = 128;              // keys per tile
+constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale max while within 2^8
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
-constexpr int kMaxSplit = 32;         // splits of one row tile's key range
+constexpr int kMaxSplit = 64;         // splits of one CTA's key range
+constexpr uint32_t kTmemCols = 512;   // S_0, S_1 at 0, 128; O_0, O_1 at 256, 384
 
 struct AttnParams {
-  const uint16_t* q;
   uint16_t* out;
   float* lse;
   int32_t* status;
   const int32_t* kv_len;
   const uint64_t* anc;
-  __half* part;    // split partials [unit][2 * nsplit][128][D] fp16, chunks swizzled
-  float2* part_ml; // their (running max in the log2 domain, running sum) [unit][2 * nsplit][128]
+  __half* part;     // split partials [unit][nsplit][256][D] fp16, 16-byte chunks swizzled by row
+  float2* part_ml;  // their (running max in the log2 domain, running sum) [unit][nsplit][256]
   int N, Hq, Hkv, G, Lcap, W;
-  int nsplit;      // splits per row tile
+  int nb;           // nodes per row block: floor(128 / G)
+  int mtiles;       // CTAs along the node axis: ceil(N / (2 nb))
+  int nsplit;       // splits of the key range
   float scale_log2;
 };
 
 template <int D>
 struct Layout {
-  static constexpr int A = D / 64;                 // 128-byte atoms per row of Q, K, V
-  static constexpr int kQ = 0;
-  static constexpr int kP = kQ + A * kAtomBytes;
-  static constexpr int kKV = kP + 2 * kAtomBytes;  // P: 128 rows x 128 keys bf16
-  static constexpr int kStage = 2 * A * kAtomBytes;
-  static constexpr int kBytes = kKV + kStages * kStage;
-  static constexpr int kDyn = kBytes + 1024;       // slack for 1024-byte alignment
-  // TMEM: S at [0, 128), O_0 at [128, 128 + D), O_1 at [128 + D, 128 + 2D)
-  static constexpr uint32_t kTmemCols = (128 + 2 * D <= 256) ? 256u : 512u;
-  // epilogue staging at kQ (Q and P are dead by then): 2 groups x 128 fp16 rows
-  static_assert(2 * kBM * D * 2 <= kKV, "staging must fit Q + P");
+  static constexpr int A = D / 64;                   // 128-byte atoms per row of Q, K, V
+  static constexpr int kQ = 0;                       // Q [row block][atom]
+  static constexpr int kP = kQ + 2 * A * kAtomBytes; // P [row block][key half], bf16
+  static constexpr int kK = kP + 4 * kAtomBytes;
+  static constexpr int kV = kK + A * kAtomBytes;
+  static constexpr int kBytes = kV + A * kAtomBytes;
+  static constexpr int kDyn = kBytes + 1024;         // slack for 1024-byte alignment
+  // the fp16 partial rows are staged where Q was (dead by then)
+  static_assert(kRows * D * 2 <= kP, "staging must fit the Q area");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
@@ -111,14 +117,14 @@ __device__ __forceinline__ uint32_t visibility32(int c, int j0, int L, int keys,
   return (pm | tm) & em;
 }
 
-// fp32 row buffers are stored with the 16-byte chunks of a row XOR-swizzled by
-// the row index, so that threads writing different rows hit different banks.
+// Row buffers are stored with the 16-byte chunks of a row XOR-swizzled by the
+// row index, so that threads writing different rows hit different banks.
 __device__ __forceinline__ int swz_chunk(int row, int chunk) { return chunk ^ (row & 7); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-               const AttnParams p) {
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Lay = Layout<D>;
   constexpr int A = Lay::A;
   extern __shared__ uint8_t smem_raw[];
@@ -126,12 +132,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + Lay::kQ;
   uint8_t* sP = smem + Lay::kP;
-  uint8_t* sKV = smem + Lay::kKV;
+  uint8_t* sK = smem + Lay::kK;
+  uint8_t* sV = smem + Lay::kV;
 
-  __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
-  __shared__ __align__(8) uint64_t bar_q, bar_s_full, bar_s_free, bar_drain;
-  __shared__ __align__(8) uint64_t bar_p_full[2], bar_o_done[2];
-  __shared__ float s_gm[2][kBM], s_gl[2][kBM];  // per group: running max and sum of each row
+  __shared__ __align__(8) uint64_t bar_q, bar_k_full, bar_k_empty, bar_v_full, bar_v_empty;
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_free[2], bar_p_full[2], bar_o_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -140,199 +146,231 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int split = blockIdx.x, mt = blockIdx.y, bh = blockIdx.z;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int grp = (tid < kSoftmaxThreads) ? (tid >> 7) : 0;  // softmax group: key half
-  const int row = tid & (kBM - 1);                            // softmax threads: query row
-  const int N = p.N;
-  const int L = p.kv_len[b];
-  const int rows_total = N * p.G;
-  const int r = mt * kBM + row;
-  const bool is_softmax = tid < kSoftmaxThreads;
-  const bool valid_row = is_softmax && (r < rows_total);
-  const int node = valid_row ? r / p.G : 0;
-  const int h = kvh * p.G + (valid_row ? r % p.G : 0);
-  const int nranks = p.nsplit;
+  const int N = p.N, G = p.G, nb = p.nb;
+  const int L = __ldg(p.kv_len + b);
+  const int node0 = mt * 2 * nb;                 // first node of this CTA
+  const int nrb = (node0 + nb < N) ? 2 : 1;      // row blocks holding a node
+  const bool is_softmax = warp < 8;
+  const int rb = (warp >> 2) & 1;                // softmax warps: row block
+  const int row = tid & (kRB - 1);               // softmax warps: row = TMEM lane
+  const int nodel = row / G;
+  const int node = node0 + rb * nb + nodel;
+  const bool act = is_softmax && rb < nrb;       // warp-uniform
+  const bool valid_row = act && nodel < nb && node < N;
+  const int h = kvh * G + row % G;
 
-  if (L < 0 || L + N > p.Lcap) {  // the merge kernel skips this sequence too
-    if (split == 0 && valid_row && grp == 0) {
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_k_full, 1);
+    mbar_init(&bar_k_empty, 1);
+    mbar_init(&bar_v_full, 1);
+    mbar_init(&bar_v_empty, 1);
+    mbar_init(&bar_drain, 1);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&bar_s_full[r], 1);
+      mbar_init(&bar_s_free[r], kRB);
+      mbar_init(&bar_p_full[r], kRB);
+      mbar_init(&bar_o_done[r], 1);
+    }
+    mbar_fence_init();
+    s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (L < 0 || L + N > p.Lcap) {  // uniform over the CTA; the merge kernel skips it too
+    if (split == 0 && valid_row) {
       uint4* o = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
       if (p.lse) p.lse[((size_t)b * N + node) * p.Hq + h] = 0.0f;
     }
     if (split == 0 && mt == 0 && kvh == 0 && tid == 0 && p.status) p.status[b] = TV_ERR_INVALID_ARG;
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
     return;
   }
   if (split == 0 && mt == 0 && kvh == 0 && tid == 0 && p.status) p.status[b] = TV_OK;
   const int keys = L + N;
   const int tiles = ceil_div(keys, kBN);
-  // balanced split of this sequence's tiles; an empty split still merges
-  const int t_begin = (int)(((long long)split * tiles) / nranks);
-  const int T = (int)(((long long)(split + 1) * tiles) / nranks) - t_begin;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
-    }
-    mbar_init(&bar_q, kSoftmaxThreads);
-    mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_s_free, kSoftmaxThreads);
-    mbar_init(&bar_p_full[0], kBM);
-    mbar_init(&bar_p_full[1], kBM);
-    mbar_init(&bar_o_done[0], 1);
-    mbar_init(&bar_o_done[1], 1);
-    mbar_init(&bar_drain, 1);
-    mbar_fence_init();
-    s_abort = 0;
-  }
-  if (warp == 0) tmem_alloc(&s_tmem, Lay::kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  const uint32_t tS = tmem;
-  const uint32_t tO0 = tmem + 128, tO1 = tmem + 128 + D;
+  // balanced split of this sequence's tiles; an empty split only writes its statistics
+  const int t_begin = (int)(((long long)split * tiles) / p.nsplit);
+  const int T = (int)(((long long)(split + 1) * tiles) / p.nsplit) - t_begin;
 
   float m_run = -INFINITY, l_run = 0.0f;  // softmax threads: running max (log2) and sum
 
   if (T > 0 && warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    const int y0 = bh * p.Lcap + t_begin * kBN;
     if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int row0 = bh * p.Lcap;
+      // Q: box {64 dims, G heads, nb nodes} per (row block, atom); rows come
+      // out node-major, matching the row numbering
+      mbar_expect_tx(&bar_q, (uint32_t)(nrb * A * 64 * G * nb * 2));
+      for (int r = 0; r < nrb; ++r)
+#pragma unroll
+        for (int a = 0; a < A; ++a)
+          tma_load_3d(sQ + (r * A + a) * kAtomBytes, &tmQ, &bar_q, a * 64, kvh * G,
+                      b * N + node0 + r * nb);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % kStages;
-        const uint32_t ph = (t / kStages) & 1;
-        if (!mbar_wait(&bar_kv_empty[s], ph ^ 1u) || s_abort) {
+        if (!mbar_wait(&bar_k_empty, (t & 1) ^ 1) || s_abort) {
           s_abort = 1;
           break;
         }
-        uint8_t* sK = sKV + s * Lay::kStage;
-        uint8_t* sV = sK + A * kAtomBytes;
-        mbar_expect_tx(&bar_kv_full[s], 2 * A * kAtomBytes);
-        const int y = row0 + (t_begin + t) * kBN;
+        mbar_expect_tx(&bar_k_full, A * kAtomBytes);
 #pragma unroll
-        for (int a = 0; a < A; ++a) {
-          tma_load_2d(sK + a * kAtomBytes, &tmK, &bar_kv_full[s], a * 64, y);
-          tma_load_2d(sV + a * kAtomBytes, &tmV, &bar_kv_full[s], a * 64, y);
-        }
+        for (int a = 0; a < A; ++a)
+          tma_load_2d(sK + a * kAtomBytes, &tmK, &bar_k_full, a * 64, y0 + t * kBN);
         issued = t + 1;
       }
       // the CTA must not move on while its copies are in flight
-      for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait(&bar_kv_full[t % kStages], (t / kStages) & 1);
+      mbar_wait(&bar_q, 0);
+      if (issued > 0) mbar_wait(&bar_k_full, (issued - 1) & 1);
+    } else if (lane == 1) {
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        if (!mbar_wait(&bar_v_empty, (t & 1) ^ 1) || s_abort) {
+          s_abort = 1;
+          break;
+        }
+        mbar_expect_tx(&bar_v_full, A * kAtomBytes);
+#pragma unroll
+        for (int a = 0; a < A; ++a)
+          tma_load_2d(sV + a * kAtomBytes, &tmV, &bar_v_full, a * 64, y0 + t * kBN);
+        issued = t + 1;
+      }
+      if (issued > 0) mbar_wait(&bar_v_full, (issued - 1) & 1);
     }
   } else if (T > 0 && warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
-    constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
+    // Two streams of work, each in tile order: S(t) needs K(t) and both S
+    // buffers read (softmax of t-1); PV(t) needs V(t) and P(t) of both row
+    // blocks.  S(t+1) is issued as soon as it can be, ahead of PV(t).
+    constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
+    constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
     bool ok = warp_wait(&bar_q, 0);
-    for (int t = 0; ok && t < T; ++t) {
-      const int s = t % kStages;
-      uint8_t* sK = sKV + s * Lay::kStage;
-      uint8_t* sV = sK + A * kAtomBytes;
-      ok = warp_wait(&bar_kv_full[s], (t / kStages) & 1);
-      if (!ok) break;
-      const int j0 = (t_begin + t) * kBN;
-      const int valid = min(kBN, keys - j0);
-      if (valid < kBN) {
-        // V rows past the key range: whatever the cache holds there, make it 0
-        const int rows = kBN - valid;
-        for (int idx = lane; idx < rows * 8 * A; idx += 32) {
-          const int a = idx / (rows * 8);
-          const int rem = idx - a * rows * 8;
-          *reinterpret_cast<uint4*>(sV + a * kAtomBytes + (valid + (rem >> 3)) * 128 +
-                                    ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
-        }
-        fence_async_smem();
-      }
-      __syncwarp();
-      if (t > 0) {
-        ok = warp_wait(&bar_s_free, (t - 1) & 1);
-        if (!ok) break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          mma_bf16(tS, sw128_desc(q0 + off, 16, 1024), sw128_desc(k0 + off, 16, 1024), idS,
-                   kk > 0);
-        }
-        mma_commit(&bar_s_full);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        ok = warp_wait(&bar_p_full[hf], t & 1);
-        if (!ok) break;
-        tc_fence_after();
+    int ns = 0, npv = 0;  // next S tile, next PV tile
+    long long t_idle = clock64();
+    while (ok && npv < T) {
+      bool prog = false;
+      if (ns < T && ns <= npv + 1) {
+        bool ready = false;
         if (lane == 0) {
-          // O_hf += P[:, 64hf .. 64hf+63] * V[64hf .. 64hf+63, :]
-          const uint32_t p0 = smem_u32(sP) + hf * kAtomBytes;
-          const uint32_t v0 = smem_u32(sV) + hf * 64 * 128;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(hf ? tO1 : tO0, sw128_desc(p0 + kk * 32, 16, 1024),
-                     sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
-          mma_commit(&bar_o_done[hf]);
+          ready = mbar_test(&bar_k_full, ns & 1);
+          if (ready && ns > 0)
+            ready = mbar_test(&bar_s_free[0], (ns - 1) & 1) &&
+                    (nrb < 2 || mbar_test(&bar_s_free[1], (ns - 1) & 1));
         }
-        __syncwarp();
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t k0 = smem_u32(sK);
+            for (int r = 0; r < nrb; ++r) {
+              const uint32_t q0 = smem_u32(sQ) + r * A * kAtomBytes;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+                mma_bf16(tmem + 128 * r, sw128_desc(q0 + off, 16, 1024),
+                         sw128_desc(k0 + off, 16, 1024), idS, kk > 0);
+              }
+              mma_commit(&bar_s_full[r]);
+            }
+            mma_commit(&bar_k_empty);
+          }
+          __syncwarp();
+          ++ns;
+          prog = true;
+        }
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&bar_kv_empty[s]);
-      __syncwarp();
+      if (npv < ns) {
+        bool ready = false;
+        if (lane == 0)
+          ready = mbar_test(&bar_v_full, npv & 1) && mbar_test(&bar_p_full[0], npv & 1) &&
+                  (nrb < 2 || mbar_test(&bar_p_full[1], npv & 1));
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          tc_fence_after();
+          const int j0 = (t_begin + npv) * kBN;
+          const int valid = min(kBN, keys - j0);
+          if (valid < kBN) {
+            // V rows past the key range: whatever the cache holds there, make it 0
+            const int rows = kBN - valid;
+            for (int idx = lane; idx < rows * 8 * A; idx += 32) {
+              const int a = idx / (rows * 8);
+              const int rem = idx - a * rows * 8;
+              *reinterpret_cast<uint4*>(sV + a * kAtomBytes + (valid + (rem >> 3)) * 128 +
+                                        ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t v0 = smem_u32(sV);
+            for (int r = 0; r < nrb; ++r) {
+              const uint32_t p0 = smem_u32(sP) + r * 2 * kAtomBytes;
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_bf16(tmem + 256 + 128 * r,
+                         sw128_desc(p0 + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
+                         sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO,
+                         (npv > 0) || (kk > 0));
+              mma_commit(&bar_o_done[r]);
+            }
+            mma_commit(&bar_v_empty);
+          }
+          __syncwarp();
+          ++npv;
+          prog = true;
+        }
+      }
+      if (prog) {
+        t_idle = clock64();
+      } else {
+        const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
+        if (__shfl_sync(0xffffffffu, late, 0)) ok = false;
+      }
     }
     if (!ok) s_abort = 1;
     if (lane == 0) {  // all issued tensor-core work retires before TMEM is read or released
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0);
     }
-  } else if (T > 0 && is_softmax) {
+    __syncwarp();
+  } else if (T > 0 && act) {
     // ------------------------------------------------------------- softmax
-    {
-      const uint4* qrow =
-          reinterpret_cast<const uint4*>(p.q + (((size_t)b * N + node) * p.Hq + h) * D);
-#pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {  // this group's half of the row's chunks
-        const int c = grp * (D / 16) + cc;
-        const uint4 v = valid_row ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + (c >> 3) * kAtomBytes + row * 128 +
-                                  (((c & 7) ^ (row & 7)) << 4)) = v;
-      }
-      fence_async_smem();
-      mbar_arrive(&bar_q);
-    }
-    const uint64_t* anc = p.anc + ((size_t)b * N + node) * p.W;
+    const uint64_t* anc = p.anc + ((size_t)b * N + (valid_row ? node : 0)) * p.W;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tO = grp ? tO1 : tO0;
+    const uint32_t tS = tmem + 128 * rb, tO = tmem + 256 + 128 * rb;
     const float sc = p.scale_log2;
+    uint8_t* prow = sP + rb * 2 * kAtomBytes + row * 128;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      ok = warp_wait(&bar_s_full, t & 1);
+      ok = warp_wait(&bar_s_full[rb], t & 1);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(tS + lane_base + grp * 64, sr[0]);
-      tmem_ld32(tS + lane_base + grp * 64 + 32, sr[1]);
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_base + 32 * c, sr[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar_s_free);
+      mbar_arrive(&bar_s_free[rb]);  // the MMA warp may write the next S now
 
       const int j0 = (t_begin + t) * kBN;
-      float mx[2] = {-INFINITY, -INFINITY};
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (valid_row && j0 + kBN <= L) {  // all prefix keys: nothing to mask
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][e]));
       } else {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t vis = valid_row ? visibility32(2 * grp + c, j0, L, keys, N, anc, p.W) : 0u;
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t vis = valid_row ? visibility32(c, j0, L, keys, N, anc, p.W) : 0u;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float x = ((vis >> e) & 1u) ? __uint_as_float(sr[c][e]) : -INFINITY;
@@ -341,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           }
         }
       }
-      const float tmax = fmaxf(mx[0], mx[1]) * sc;
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
       float corr = 1.0f;
       bool need = false;
       const float m_new = fmaxf(m_run, tmax);
@@ -352,31 +390,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         m_run = m_new;
         need = true;
       }
-      uint32_t pk[32];
+      // the P buffer and O are free once the previous PV retired
+      if (t > 0) {
+        ok = warp_wait(&bar_o_done[rb], (t - 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+      }
       float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if (m_run == -INFINITY) {  // nothing visible yet: P = 0
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(prow + (c >> 1) * kAtomBytes +
+                                      ((((c & 1) * 4 + q) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
       } else {
         const float neg_m = -m_run;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float x0 = exp2f(fmaf(__uint_as_float(sr[c][e]), sc, neg_m));
-            const float x1 = exp2f(fmaf(__uint_as_float(sr[c][e + 1]), sc, neg_m));
-            ps[2 * c + ((e >> 4) & 1)] += x0 + x1;
-            pk[(c * 32 + e) >> 1] = pack_bf16(x0, x1);
+          for (int q = 0; q < 4; ++q) {  // 8 keys -> one 16-byte chunk of P
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = exp2f(fmaf(__uint_as_float(sr[c][8 * q + 2 * e]), sc, neg_m));
+              const float x1 = exp2f(fmaf(__uint_as_float(sr[c][8 * q + 2 * e + 1]), sc, neg_m));
+              ps[c] += x0 + x1;
+              w[e] = pack_bf16(x0, x1);
+            }
+            *reinterpret_cast<uint4*>(prow + (c >> 1) * kAtomBytes +
+                                      ((((c & 1) * 4 + q) ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
       l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      // this group's P half and O_h are free once its previous PV retired
-      if (t > 0) {
-        ok = warp_wait(&bar_o_done[grp], (t - 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-      }
+      // rescale O after the exponentials, when S no longer holds registers
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -389,16 +438,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         tmem_wait_st();
       }
-      uint8_t* prow = sP + grp * kAtomBytes + row * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p_full[grp]);
+      mbar_arrive(&bar_p_full[rb]);
     }
-    if (ok) ok = warp_wait(&bar_o_done[grp], (T - 1) & 1);
+    if (ok) ok = warp_wait(&bar_o_done[rb], (T - 1) & 1);
     if (!ok) s_abort = 1;
     tc_fence_after();
   }
@@ -408,134 +452,107 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();  // every role is done; TMA and MMA work has retired
   tc_fence_after();
   if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  // Each softmax thread stages its group's normalised O row in fp16 at kQ
-  // (Q and P are dead now) as [group][row][D], 16-byte chunks swizzled by the
-  // row, with the group's running (max, sum) beside it.
-  uint8_t* sStage = smem + Lay::kQ;
   const bool split_kv = p.nsplit > 1;
-  const size_t unit = (size_t)bh * gridDim.y + mt;  // (sequence, kv head, row tile)
-  if (is_softmax) {
-    s_gm[grp][row] = m_run;
-    s_gl[grp][row] = l_run;
-    if (split_kv) {
-      const size_t si = (unit * (2 * p.nsplit) + 2 * split + grp) * kBM + row;
-      p.part_ml[si] = make_float2(m_run, l_run);
-    }
-    uint32_t o[D / 32][32];
-    if (T > 0) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32((grp ? tO1 : tO0) + lane_base + 32 * c, o[c]);
-      tmem_wait_ld();
-    } else {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[c][e] = 0u;
-    }
+  const size_t unit = (size_t)bh * p.mtiles + mt;  // (sequence, kv head, node tile)
+  uint8_t* sStage = smem + Lay::kQ;
+  if (act) {
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tO = tmem + 256 + 128 * rb;
     const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-    uint8_t* srow = sStage + (size_t)(grp * kBM + row) * D * 2;
+    const int crow = rb * kRB + row;  // row of the CTA
+    if (split_kv) {
+      p.part_ml[(unit * p.nsplit + split) * kRows + crow] = make_float2(m_run, l_run);
+      if (T > 0) {
+        // normalised fp16 row, staged for the bulk store
+        uint8_t* dst = sStage + (size_t)crow * D * 2;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_base + 32 * c, o);
+          tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {  // four 16-byte chunks of 8 halves
-        uint32_t hw[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __half2 hv = __floats2half2_rn(__uint_as_float(o[c][8 * e + 2 * j]) * inv,
-                                               __uint_as_float(o[c][8 * e + 2 * j + 1]) * inv);
-          hw[j] = *reinterpret_cast<const uint32_t*>(&hv);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + swz_chunk(crow, 4 * c + q) * 16) = make_uint4(
+                pack_f16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                pack_f16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                pack_f16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                pack_f16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
         }
-        *reinterpret_cast<uint4*>(srow + swz_chunk(row, 4 * c + e) * 16) =
-            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        fence_async_smem();  // the bulk store reads the staging area
       }
+    } else {
+      // the whole key range was here: write the output row
+      uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + lane_base + 32 * c, o);  // warp-wide; only valid rows store
+        tmem_wait_ld();
+        if (valid_row) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            orow[4 * c + q] = make_uint4(
+                pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+        }
+      }
+      if (valid_row && p.lse)
+        p.lse[((size_t)b * N + node) * p.Hq + h] =
+            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
-    if (split_kv) fence_async_smem();  // the bulk store reads the staging area
   }
   __syncthreads();
-  if (split_kv) {
-    // the partial rows go to the workspace; tv_attn_merge finishes them
-    if (tid == 0 && T > 0) {
-      __half* dst = p.part + (unit * (2 * p.nsplit) + 2 * split) * kBM * D;
-      bulk_store_global(dst, smem_u32(sStage), (uint32_t)(2 * kBM * D * 2));
-      bulk_commit();
-      bulk_wait_all();
-    }
-  } else {
-    // merge the two key halves of each row here.  A warp takes 32 / (D / 8)
-    // rows; the lanes of a row cover its 16-byte fp16 chunks.
-    constexpr int kC16 = D / 8;
-    constexpr int kRowsPerWarp = 32 / kC16;
-    const int sub = lane / kC16, ch = lane % kC16;
-    for (int rb = warp * kRowsPerWarp; rb < kBM; rb += (kThreads / 32) * kRowsPerWarp) {
-      const int lr = rb + sub;
-      const int gr = mt * kBM + lr;
-      if (gr >= rows_total) continue;
-      const float m0 = s_gm[0][lr], m1 = s_gm[1][lr];
-      const float M = fmaxf(m0, m1);
-      const float w0 = (m0 == -INFINITY) ? 0.0f : exp2f(m0 - M) * s_gl[0][lr];
-      const float w1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - M) * s_gl[1][lr];
-      const float L = w0 + w1;
-      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-      const uint4 x0 = *reinterpret_cast<const uint4*>(sStage + (size_t)lr * D * 2 + swz_chunk(lr, ch) * 16);
-      const uint4 x1 = *reinterpret_cast<const uint4*>(sStage + (size_t)(kBM + lr) * D * 2 + swz_chunk(lr, ch) * 16);
-      const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c1[4] = {x1.x, x1.y, x1.z, x1.w};
-      uint32_t u[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&a[j]));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&c1[j]));
-        u[j] = pack_bf16((w0 * f0.x + w1 * f1.x) * inv, (w0 * f0.y + w1 * f1.y) * inv);
-      }
-      const size_t orow = ((size_t)b * N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
-      *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) = make_uint4(u[0], u[1], u[2], u[3]);
-      if (ch == 0 && p.lse)
-        p.lse[orow] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-    }
+  if (split_kv && T > 0 && tid == 0) {
+    // the partial rows go to the workspace; the merge kernel finishes them
+    bulk_store_global(p.part + (unit * p.nsplit + split) * kRows * D, smem_u32(sStage),
+                      (uint32_t)(nrb * kRB * D * 2));
+    bulk_commit();
+    bulk_wait_read();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, Lay::kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Merge of the split-KV partials: for every query row, weights
-// exp2(m_s - M) * l_s over the 2 * nsplit partials (two key halves per
-// split), normalised, applied to the normalised fp16 partial rows.  A CTA
-// takes kRows = 256 / (D / 8) rows of one row tile; kC16 = D / 8 threads per
-// row.  Every load of a phase is issued before the first one is used, so the
-// kernel pays about one L2 round trip per phase.
+// exp2(m_s - M) * l_s over the nsplit partials, normalised, applied to the
+// normalised fp16 partial rows.  A CTA takes kMR = 256 / (D / 8) rows of one
+// unit, D / 8 threads per row (one 16-byte chunk each).  Every load of a
+// phase is issued before the first one is used, so each phase costs about
+// one L2 round trip.
 template <int D>
 __global__ void __launch_bounds__(256)
-attn_merge_kernel(const AttnParams p, int mtiles) {
+attn_merge_kernel(const AttnParams p) {
   constexpr int kC16 = D / 8;
-  constexpr int kRows = 256 / kC16;
-  constexpr int kMaxSlots = 2 * kMaxSplit;
-  constexpr int kSPT = kMaxSlots / kC16;  // statistics phase: slots per thread
+  constexpr int kMR = 256 / kC16;
+  constexpr int kSPT = kMaxSplit / kC16;  // statistics phase: slots per thread
   constexpr int kBatch = 16;              // accumulation phase: loads in flight per thread
-  __shared__ float s_w[kMaxSlots][kRows];
-  __shared__ float s_inv[kRows], s_lse[kRows];
+  __shared__ float s_w[kMaxSplit][kMR];
+  __shared__ float s_inv[kMR], s_lse[kMR];
   pdl_wait();  // the partials come from the attention kernel
   pdl_trigger();
-  const int cpu = kBM / kRows;  // CTAs per row tile
+  constexpr int cpu = kRows / kMR;  // CTAs per unit
   const int unit = blockIdx.x / cpu;
-  const int rbase = (blockIdx.x % cpu) * kRows;
-  const int bh = unit / mtiles, mt = unit % mtiles;
+  const int rbase = (blockIdx.x % cpu) * kMR;
+  const int bh = unit / p.mtiles, mt = unit % p.mtiles;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
-  const int L = p.kv_len[b];
+  const int L = __ldg(p.kv_len + b);
   if (L < 0 || L + p.N > p.Lcap) return;  // the attention kernel zeroed these outputs
-  const int nslots = 2 * p.nsplit;
+  const int ns = p.nsplit;
   const int tid = threadIdx.x;
-  const int r = tid / kC16, j = tid % kC16;  // row of this CTA; lane within the row's group
-  const int row = rbase + r;
-  const size_t sbase = (size_t)unit * nslots * kBM;
+  const int r = tid / kC16, j = tid % kC16;  // row of this CTA; thread within the row
+  const int crow = rbase + r;                // row of the unit
+  const size_t sbase = (size_t)unit * ns * kRows;
   {
     // statistics: the kC16 threads of a row take slots j, j + kC16, ...
     float2 ml[kSPT];
 #pragma unroll
     for (int k = 0; k < kSPT; ++k) {
       const int sl = j + kC16 * k;
-      ml[k] = sl < nslots ? __ldg(p.part_ml + sbase + (size_t)sl * kBM + row)
-                          : make_float2(-INFINITY, 0.0f);
+      ml[k] = sl < ns ? __ldg(p.part_ml + sbase + (size_t)sl * kRows + crow)
+                      : make_float2(-INFINITY, 0.0f);
     }
     float M = -INFINITY;
 #pragma unroll
@@ -547,7 +564,7 @@ attn_merge_kernel(const AttnParams p, int mtiles) {
     for (int k = 0; k < kSPT; ++k) {
       const int sl = j + kC16 * k;
       const float w = (ml[k].x == -INFINITY) ? 0.0f : exp2f(ml[k].x - M) * ml[k].y;
-      if (sl < nslots) s_w[sl][r] = w;
+      if (sl < ns) s_w[sl][r] = w;
       Ls += w;
     }
 #pragma unroll
@@ -558,23 +575,26 @@ attn_merge_kernel(const AttnParams p, int mtiles) {
     }
   }
   __syncthreads();
-  const int gr = mt * kBM + row;
-  if (gr >= p.N * p.G) return;
-  const int ch = j;
+  const int rbk = crow / kRB, rl = crow % kRB;
+  const int nodel = rl / p.G;
+  const int node = mt * 2 * p.nb + rbk * p.nb + nodel;
+  if (nodel >= p.nb || node >= p.N) return;
+  const int h = kvh * p.G + rl % p.G;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part) +
-                       ((size_t)unit * nslots * kBM + row) * D * 2 + swz_chunk(row, ch) * 16;
-  for (int s0 = 0; s0 < nslots; s0 += kBatch) {
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part) + (sbase + crow) * D * 2 +
+                       swz_chunk(crow, j) * 16;
+  for (int s0 = 0; s0 < ns; s0 += kBatch) {
     uint4 x[kBatch];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
-      x[k] = (s0 + k < nslots) ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(s0 + k) * kBM * D * 2))
-                               : make_uint4(0, 0, 0, 0);
+      x[k] = (s0 + k < ns)
+                 ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(s0 + k) * kRows * D * 2))
+                 : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
-      if (s0 + k >= nslots) break;
+      if (s0 + k >= ns) break;
       const float w = s_w[s0 + k][r];
       if (w == 0.0f) continue;  // an empty split: its rows were never written
       const uint32_t xw[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
@@ -587,14 +607,11 @@ attn_merge_kernel(const AttnParams p, int mtiles) {
     }
   }
   const float inv = s_inv[r];
-  const size_t orow = ((size_t)b * p.N + gr / p.G) * p.Hq + kvh * p.G + gr % p.G;
-  uint4 u;
-  u.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  u.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  u.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  u.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) = u;
-  if (ch == 0 && p.lse) p.lse[orow] = s_lse[r];
+  const size_t orow = ((size_t)b * p.N + node) * p.Hq + h;
+  *reinterpret_cast<uint4*>(p.out + orow * D + 8 * j) =
+      make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                 pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+  if (j == 0 && p.lse) p.lse[orow] = s_lse[r];
 }
 
 // --------------------------------------------------------------------- host
@@ -614,17 +631,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 struct SplitPlan {
-  int mtiles, nsplit;
-  long long units;  // (sequence, kv head, row tile) triples
+  int nb, mtiles, nsplit;
+  long long units;  // (sequence, kv head, node tile) triples
 };
 
+// Rough per-CTA costs (about a microsecond each) of a 128-key tile, of the
+// fixed part of a CTA (setup, first loads, epilogue) and of the merge kernel.
+constexpr long long kCostTile = 2, kCostFixed = 4, kCostMerge = 4;
+
 // Choose the split count that minimises
-// (waves of CTAs) x (tiles per CTA + fixed cost) + merge cost, preferring
-// fewer splits.  One CTA fits an SM (its shared memory decides that).
+// (waves of CTAs) x (tiles per CTA x tile cost + fixed cost) + merge cost,
+// preferring fewer splits.  One CTA fits an SM (its shared memory decides).
 SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
   SplitPlan sp;
   const int G = Hq / Hkv;
-  sp.mtiles = ceil_div(N * G, kBM);
+  sp.nb = kRB / G;
+  sp.mtiles = ceil_div(N, 2 * sp.nb);
   sp.units = (long long)B * Hkv * sp.mtiles;
   const int tiles_max = ceil_div(Lcap, kBN);
   const long long slots = device_sm_count();
@@ -633,7 +655,8 @@ SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
   for (int ns = 1; ns <= kMaxSplit && ns <= tiles_max; ++ns) {
     const long long waves = (sp.units * ns + slots - 1) / slots;
     const long long tiles_per_cta = (tiles_max + ns - 1) / ns;
-    const long long cost = waves * (tiles_per_cta * 4 + 10) + (ns > 1 ? 6 : 0);
+    const long long cost =
+        waves * (tiles_per_cta * kCostTile + kCostFixed) + (ns > 1 ? kCostMerge : 0);
     if (best < 0 || cost < best) {
       best = cost;
       sp.nsplit = ns;
@@ -645,7 +668,7 @@ SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
 // Workspace bytes of a plan: fp16 partial rows, then their (max, sum) pairs.
 size_t plan_workspace(const SplitPlan& sp, int D) {
   if (sp.nsplit <= 1) return 0;
-  const size_t rows = (size_t)sp.units * 2 * sp.nsplit * kBM;
+  const size_t rows = (size_t)sp.units * sp.nsplit * kRows;
   return align_up(rows * D * 2, 256) + align_up(rows * 8, 256);
 }
 
@@ -671,21 +694,34 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
     }
     smem_set = true;
   }
-  CUtensorMap tmK, tmV;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)B * Hkv * Lcap};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {64, kBN};
-  const cuuint32_t estr[2] = {1, 1};
-  if (encode(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<tv_bf16*>(k), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return TV_ERR_INVALID_ARG;
-  if (encode(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<tv_bf16*>(v), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return TV_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  // Q as [B * N tokens][Hq heads][D]; a box is {64 dims, G heads, nb nodes}
+  CUtensorMap tmQ, tmK, tmV;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)B * N};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)sp.nb};
+    if (encode(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<tv_bf16*>(q), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TV_ERR_INVALID_ARG;
+  }
+  // K and V as [B * Hkv * Lcap slots][D]; a box is {64 dims, 128 keys}
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)B * Hkv * Lcap};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, kBN};
+    if (encode(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<tv_bf16*>(k), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TV_ERR_INVALID_ARG;
+    if (encode(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<tv_bf16*>(v), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TV_ERR_INVALID_ARG;
+  }
   AttnParams p;
-  p.q = q;
   p.out = out;
   p.lse = lse;
   p.status = status;
@@ -694,7 +730,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.part = nullptr;
   p.part_ml = nullptr;
   if (need > 0) {
-    const size_t rows = (size_t)sp.units * 2 * sp.nsplit * kBM;
+    const size_t rows = (size_t)sp.units * sp.nsplit * kRows;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.part = reinterpret_cast<__half*>(ws);
     p.part_ml = reinterpret_cast<float2*>(ws + align_up(rows * D * 2, 256));
@@ -702,21 +738,23 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.N = N;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.G = Hq / Hkv;
+  p.G = G;
   p.Lcap = Lcap;
   p.W = ceil_div(N, 64);
+  p.nb = sp.nb;
+  p.mtiles = sp.mtiles;
   p.nsplit = sp.nsplit;
   p.scale_log2 = scale_log2;
   if (launch_pdl(attn_tc_kernel<D>, dim3(sp.nsplit, sp.mtiles, B * Hkv), dim3(kThreads, 1, 1),
-                 (size_t)Lay::kDyn, stream, tmK, tmV, p) != cudaSuccess) {
+                 (size_t)Lay::kDyn, stream, tmQ, tmK, tmV, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;
   }
   if (sp.nsplit > 1) {
-    constexpr int kRows = 256 / (D / 8);
-    const long long ctas = sp.units * (kBM / kRows);
-    if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)ctas, 1, 1), dim3(256, 1, 1), 0, stream, p,
-                   sp.mtiles) != cudaSuccess) {
+    constexpr int kMR = 256 / (D / 8);
+    const long long ctas = sp.units * (kRows / kMR);
+    if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)ctas, 1, 1), dim3(256, 1, 1), 0, stream,
+                   p) != cudaSuccess) {
       (void)cudaGetLastError();
       return TV_ERR_CUDA;
     }
@@ -726,7 +764,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
 
 bool attn_shape_ok(int B, int N, int Hq, int Hkv, int D, int Lcap) {
   return B >= 0 && N >= 1 && N <= TV_MAX_NODES && Hq >= 1 && Hkv >= 1 && Lcap >= N &&
-         Hq % Hkv == 0 && (D == 64 || D == 128);
+         Hq % Hkv == 0 && Hq / Hkv <= kRB && (D == 64 || D == 128);
 }
 
 }  // namespace
@@ -745,10 +783,13 @@ extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Lcap < N) return TV_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return TV_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return TV_ERR_UNSUPPORTED;
+  if (Hq / Hkv > tv::kRB) return TV_ERR_UNSUPPORTED;
   if (!(scale >= 0.0f) || !isfinite(scale)) return TV_ERR_INVALID_ARG;
   if (B == 0) return TV_OK;
   if (!q || !k || !v || !kv_len || !anc_mask || !out) return TV_ERR_INVALID_ARG;
-  if ((long long)B * Hkv > 65535 || (long long)B * Hkv * Lcap > 0x7fffffffll) return TV_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv > 65535 || (long long)B * Hkv * Lcap > 0x7fffffffll ||
+      (long long)B * N > 0x7fffffffll)
+    return TV_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
     return TV_ERR_INVALID_ARG;

@@ -68,6 +68,8 @@ def test_config1_tiny(tv, oracle_mod):
     (5, 3, 20, (0, 260), 32, 8, 128, "star"),
     (6, 1, 130, 1000, 4, 1, 64, "random"),
     (7, 1, 60, 2048, 32, 8, 128, "spine60"),  # the Llama-3-8B spine case, full size
+    (8, 2, 50, (90, 400), 12, 4, 64, "random"),  # GQA 3: a row block holds 42 nodes (126 rows)
+    (9, 1, 100, 500, 6, 1, 128, "random"),     # GQA 6: 21 nodes (126 rows), three node tiles
 ])
 def test_attention_full(tv, oracle_mod, seed, B, N, L, Hq, Hkv, D, tree):
     case = gen.make_case(seed, B=B, N=N, L=L, Hq=Hq, Hkv=Hkv, D=D, V=max(64, N), tree=tree,
