@@ -56,7 +56,7 @@ struct AttnParams {
   int32_t* status;
   const int32_t* kv_len;
   const uint64_t* anc;
-  __half* part;     // split partials [unit][nsplit][256][D] fp16, 16-byte chunks swizzled by row
+  __half* part;     // split partials [unit][nsplit][D / 8][256 rows] 16-byte chunks of 8 fp16
   float2* part_ml;  // their (running max in the log2 domain, running sum) [unit][nsplit][256]
   int N, Hq, Hkv, G, Lcap, W;
   int nb;           // nodes per row block: floor(128 / G)
@@ -74,8 +74,6 @@ struct Layout {
   static constexpr int kV = kK + A * kAtomBytes;
   static constexpr int kBytes = kV + A * kAtomBytes;
   static constexpr int kDyn = kBytes + 1024;         // slack for 1024-byte alignment
-  // the fp16 partial rows are staged where Q was (dead by then)
-  static_assert(kRows * D * 2 <= kP, "staging must fit the Q area");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -85,6 +83,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 2^x on the special-function unit (ex2.approx, flush-to-zero); 2^-inf = +0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Every lane of the warp waits; the warp goes on only if all of them saw the
@@ -116,10 +121,6 @@ __device__ __forceinline__ uint32_t visibility32(int c, int j0, int L, int keys,
   if (x + 32 > 0 && x < N) tm = (x >= 0) ? anc_bits32(anc, W, x) : (anc_bits32(anc, W, 0) << (-x));
   return (pm | tm) & em;
 }
-
-// Row buffers are stored with the 16-byte chunks of a row XOR-swizzled by the
-// row index, so that threads writing different rows hit different banks.
-__device__ __forceinline__ int swz_chunk(int row, int chunk) { return chunk ^ (row & 7); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -159,6 +160,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const bool valid_row = act && nodel < nb && node < N;
   const int h = kvh * G + row % G;
 
+  // Split ranges come from the cache capacity, so the first tile's loads can
+  // be issued before kv_len arrives; tiles past the key range are dropped.
+  const int tiles_cap = ceil_div(p.Lcap, kBN);
+  const int t_begin = (int)(((long long)split * tiles_cap) / p.nsplit);
+  const int t_end = (int)(((long long)(split + 1) * tiles_cap) / p.nsplit);
+  const bool first_issued = t_end > t_begin;
+  const int y0 = bh * p.Lcap + t_begin * kBN;
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     mbar_init(&bar_k_full, 1);
@@ -174,6 +182,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
     mbar_fence_init();
     s_abort = 0;
+    if (first_issued) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      // Q: box {64 dims, G heads, nb nodes} per (row block, atom); rows come
+      // out node-major, matching the row numbering
+      mbar_expect_tx(&bar_q, (uint32_t)(nrb * A * 64 * G * nb * 2));
+      for (int r = 0; r < nrb; ++r)
+#pragma unroll
+        for (int a = 0; a < A; ++a)
+          tma_load_3d(sQ + (r * A + a) * kAtomBytes, &tmQ, &bar_q, a * 64, kvh * G,
+                      b * N + node0 + r * nb);
+      mbar_expect_tx(&bar_k_full, A * kAtomBytes);
+      mbar_expect_tx(&bar_v_full, A * kAtomBytes);
+#pragma unroll
+      for (int a = 0; a < A; ++a) {
+        tma_load_2d(sK + a * kAtomBytes, &tmK, &bar_k_full, a * 64, y0);
+        tma_load_2d(sV + a * kAtomBytes, &tmV, &bar_v_full, a * 64, y0);
+      }
+    }
   }
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
   tc_fence_before();
@@ -189,62 +217,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (p.lse) p.lse[((size_t)b * N + node) * p.Hq + h] = 0.0f;
     }
     if (split == 0 && mt == 0 && kvh == 0 && tid == 0 && p.status) p.status[b] = TV_ERR_INVALID_ARG;
+    if (tid == 0 && first_issued) {  // no copy may be in flight when the CTA leaves
+      mbar_wait(&bar_q, 0);
+      mbar_wait(&bar_k_full, 0);
+      mbar_wait(&bar_v_full, 0);
+    }
+    __syncwarp();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
     return;
   }
   if (split == 0 && mt == 0 && kvh == 0 && tid == 0 && p.status) p.status[b] = TV_OK;
   const int keys = L + N;
-  const int tiles = ceil_div(keys, kBN);
-  // balanced split of this sequence's tiles; an empty split only writes its statistics
-  const int t_begin = (int)(((long long)split * tiles) / p.nsplit);
-  const int T = (int)(((long long)(split + 1) * tiles) / p.nsplit) - t_begin;
+  // tiles of this split inside the key range; an empty split only writes its statistics
+  const int T = max(0, min(t_end, ceil_div(keys, kBN)) - t_begin);
 
   float m_run = -INFINITY, l_run = 0.0f;  // softmax threads: running max (log2) and sum
 
-  if (T > 0 && warp == kProducerWarp) {
+  if (first_issued && warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    const int y0 = bh * p.Lcap + t_begin * kBN;
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      // Q: box {64 dims, G heads, nb nodes} per (row block, atom); rows come
-      // out node-major, matching the row numbering
-      mbar_expect_tx(&bar_q, (uint32_t)(nrb * A * 64 * G * nb * 2));
-      for (int r = 0; r < nrb; ++r)
-#pragma unroll
-        for (int a = 0; a < A; ++a)
-          tma_load_3d(sQ + (r * A + a) * kAtomBytes, &tmQ, &bar_q, a * 64, kvh * G,
-                      b * N + node0 + r * nb);
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
-        if (!mbar_wait(&bar_k_empty, (t & 1) ^ 1) || s_abort) {
+    // tile 0 (and Q) were issued during setup; lane 0 loads K, lane 1 V
+    if (lane < 2) {
+      uint64_t* full = lane ? &bar_v_full : &bar_k_full;
+      uint64_t* empty = lane ? &bar_v_empty : &bar_k_empty;
+      const CUtensorMap* map = lane ? &tmV : &tmK;
+      uint8_t* dst = lane ? sV : sK;
+      int issued = 1;
+      for (int t = 1; t < T; ++t) {
+        if (!mbar_wait(empty, (t & 1) ^ 1) || s_abort) {
           s_abort = 1;
           break;
         }
-        mbar_expect_tx(&bar_k_full, A * kAtomBytes);
+        mbar_expect_tx(full, A * kAtomBytes);
 #pragma unroll
-        for (int a = 0; a < A; ++a)
-          tma_load_2d(sK + a * kAtomBytes, &tmK, &bar_k_full, a * 64, y0 + t * kBN);
+        for (int a = 0; a < A; ++a) tma_load_2d(dst + a * kAtomBytes, map, full, a * 64, y0 + t * kBN);
         issued = t + 1;
       }
       // the CTA must not move on while its copies are in flight
-      mbar_wait(&bar_q, 0);
-      if (issued > 0) mbar_wait(&bar_k_full, (issued - 1) & 1);
-    } else if (lane == 1) {
-      tma_prefetch_desc(&tmV);
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
-        if (!mbar_wait(&bar_v_empty, (t & 1) ^ 1) || s_abort) {
-          s_abort = 1;
-          break;
-        }
-        mbar_expect_tx(&bar_v_full, A * kAtomBytes);
-#pragma unroll
-        for (int a = 0; a < A; ++a)
-          tma_load_2d(sV + a * kAtomBytes, &tmV, &bar_v_full, a * 64, y0 + t * kBN);
-        issued = t + 1;
-      }
-      if (issued > 0) mbar_wait(&bar_v_full, (issued - 1) & 1);
+      if (lane == 0) mbar_wait(&bar_q, 0);
+      mbar_wait(full, (issued - 1) & 1);
     }
   } else if (T > 0 && warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
@@ -350,6 +360,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint8_t* prow = sP + rb * 2 * kAtomBytes + row * 128;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
+      // the mask words (their ancestor loads) are ready before S is
+      const int j0 = (t_begin + t) * kBN;
+      const bool unmasked = valid_row && j0 + kBN <= L;  // all prefix keys
+      uint32_t vis[4] = {0u, 0u, 0u, 0u};
+      if (!unmasked && valid_row) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vis[c] = visibility32(c, j0, L, keys, N, anc, p.W);
+      }
       ok = warp_wait(&bar_s_full[rb], t & 1);
       if (!ok) break;
       tc_fence_after();
@@ -360,9 +378,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&bar_s_free[rb]);  // the MMA warp may write the next S now
 
-      const int j0 = (t_begin + t) * kBN;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (valid_row && j0 + kBN <= L) {  // all prefix keys: nothing to mask
+      if (unmasked) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -370,10 +387,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint32_t vis = valid_row ? visibility32(c, j0, L, keys, N, anc, p.W) : 0u;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float x = ((vis >> e) & 1u) ? __uint_as_float(sr[c][e]) : -INFINITY;
+            const float x = ((vis[c] >> e) & 1u) ? __uint_as_float(sr[c][e]) : -INFINITY;
             sr[c][e] = __float_as_uint(x);
             mx[c] = fmaxf(mx[c], x);
           }
@@ -386,7 +402,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (m_run == -INFINITY) {
         m_run = m_new;
       } else if (m_new > m_run + kRescaleLog2) {
-        corr = exp2f(m_run - m_new);
+        corr = ex2(m_run - m_new);
         m_run = m_new;
         need = true;
       }
@@ -413,8 +429,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float x0 = exp2f(fmaf(__uint_as_float(sr[c][8 * q + 2 * e]), sc, neg_m));
-              const float x1 = exp2f(fmaf(__uint_as_float(sr[c][8 * q + 2 * e + 1]), sc, neg_m));
+              const float x0 = ex2(fmaf(__uint_as_float(sr[c][8 * q + 2 * e]), sc, neg_m));
+              const float x1 = ex2(fmaf(__uint_as_float(sr[c][8 * q + 2 * e + 1]), sc, neg_m));
               ps[c] += x0 + x1;
               w[e] = pack_bf16(x0, x1);
             }
@@ -454,17 +470,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
   const bool split_kv = p.nsplit > 1;
   const size_t unit = (size_t)bh * p.mtiles + mt;  // (sequence, kv head, node tile)
-  uint8_t* sStage = smem + Lay::kQ;
   if (act) {
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + 256 + 128 * rb;
     const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
     const int crow = rb * kRB + row;  // row of the CTA
     if (split_kv) {
-      p.part_ml[(unit * p.nsplit + split) * kRows + crow] = make_float2(m_run, l_run);
+      const size_t slot = unit * p.nsplit + split;
+      p.part_ml[slot * kRows + crow] = make_float2(m_run, l_run);
       if (T > 0) {
-        // normalised fp16 row, staged for the bulk store
-        uint8_t* dst = sStage + (size_t)crow * D * 2;
+        // normalised fp16 partial row, chunk-major: the lanes of a warp hold
+        // consecutive rows, so every store instruction writes 512 contiguous bytes
+        uint4* dst = reinterpret_cast<uint4*>(p.part) + slot * (D / 8) * kRows + crow;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -472,13 +489,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + swz_chunk(crow, 4 * c + q) * 16) = make_uint4(
+            dst[(size_t)(4 * c + q) * kRows] = make_uint4(
                 pack_f16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
                 pack_f16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
                 pack_f16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
                 pack_f16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
         }
-        fence_async_smem();  // the bulk store reads the staging area
       }
     } else {
       // the whole key range was here: write the output row
@@ -503,100 +519,73 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
   }
-  __syncthreads();
-  if (split_kv && T > 0 && tid == 0) {
-    // the partial rows go to the workspace; the merge kernel finishes them
-    bulk_store_global(p.part + (unit * p.nsplit + split) * kRows * D, smem_u32(sStage),
-                      (uint32_t)(nrb * kRB * D * 2));
-    bulk_commit();
-    bulk_wait_read();
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Merge of the split-KV partials: for every query row, weights
-// exp2(m_s - M) * l_s over the nsplit partials, normalised, applied to the
-// normalised fp16 partial rows.  A CTA takes kMR = 256 / (D / 8) rows of one
-// unit, D / 8 threads per row (one 16-byte chunk each).  Every load of a
-// phase is issued before the first one is used, so each phase costs about
-// one L2 round trip.
+// 2^(m_s - M) * l_s over the nsplit partials, normalised, applied to the
+// normalised fp16 partial rows.  A CTA takes 32 rows x 8 chunks of one unit;
+// a warp is 32 consecutive rows of one chunk, so every load is one contiguous
+// 512-byte (chunk) or 256-byte (statistics) segment.  The statistics and the
+// partial chunks of up to kBatch splits are loaded together, then combined
+// with a running maximum, so the kernel pays about one L2 round trip per
+// kBatch splits.
+constexpr int kMergeRows = 32, kMergeChunks = 8, kMergeBatch = 24;
+
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const AttnParams p) {
   constexpr int kC16 = D / 8;
-  constexpr int kMR = 256 / kC16;
-  constexpr int kSPT = kMaxSplit / kC16;  // statistics phase: slots per thread
-  constexpr int kBatch = 16;              // accumulation phase: loads in flight per thread
-  __shared__ float s_w[kMaxSplit][kMR];
-  __shared__ float s_inv[kMR], s_lse[kMR];
+  constexpr int kCtaPerUnit = (kRows / kMergeRows) * (kC16 / kMergeChunks);
   pdl_wait();  // the partials come from the attention kernel
   pdl_trigger();
-  constexpr int cpu = kRows / kMR;  // CTAs per unit
-  const int unit = blockIdx.x / cpu;
-  const int rbase = (blockIdx.x % cpu) * kMR;
+  const int unit = blockIdx.x / kCtaPerUnit;
+  const int sub = blockIdx.x % kCtaPerUnit;
+  const int crow = (sub % (kRows / kMergeRows)) * kMergeRows + (threadIdx.x & 31);
+  const int ch = (sub / (kRows / kMergeRows)) * kMergeChunks + (threadIdx.x >> 5);
   const int bh = unit / p.mtiles, mt = unit % p.mtiles;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int L = __ldg(p.kv_len + b);
   if (L < 0 || L + p.N > p.Lcap) return;  // the attention kernel zeroed these outputs
-  const int ns = p.nsplit;
-  const int tid = threadIdx.x;
-  const int r = tid / kC16, j = tid % kC16;  // row of this CTA; thread within the row
-  const int crow = rbase + r;                // row of the unit
-  const size_t sbase = (size_t)unit * ns * kRows;
-  {
-    // statistics: the kC16 threads of a row take slots j, j + kC16, ...
-    float2 ml[kSPT];
-#pragma unroll
-    for (int k = 0; k < kSPT; ++k) {
-      const int sl = j + kC16 * k;
-      ml[k] = sl < ns ? __ldg(p.part_ml + sbase + (size_t)sl * kRows + crow)
-                      : make_float2(-INFINITY, 0.0f);
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kSPT; ++k) M = fmaxf(M, ml[k].x);
-#pragma unroll
-    for (int o = kC16 / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Ls = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kSPT; ++k) {
-      const int sl = j + kC16 * k;
-      const float w = (ml[k].x == -INFINITY) ? 0.0f : exp2f(ml[k].x - M) * ml[k].y;
-      if (sl < ns) s_w[sl][r] = w;
-      Ls += w;
-    }
-#pragma unroll
-    for (int o = kC16 / 2; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    if (j == 0) {
-      s_inv[r] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-      s_lse[r] = Ls > 0.0f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-    }
-  }
-  __syncthreads();
   const int rbk = crow / kRB, rl = crow % kRB;
   const int nodel = rl / p.G;
   const int node = mt * 2 * p.nb + rbk * p.nb + nodel;
   if (nodel >= p.nb || node >= p.N) return;
   const int h = kvh * p.G + rl % p.G;
+  const int ns = p.nsplit;
+  const float2* ml = p.part_ml + (size_t)unit * ns * kRows + crow;
+  const uint4* src = reinterpret_cast<const uint4*>(p.part) + (size_t)unit * ns * kC16 * kRows +
+                     (size_t)ch * kRows + crow;
+  float M = -INFINITY, Ls = 0.0f;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part) + (sbase + crow) * D * 2 +
-                       swz_chunk(crow, j) * 16;
-  for (int s0 = 0; s0 < ns; s0 += kBatch) {
-    uint4 x[kBatch];
+  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
+    float2 st[kMergeBatch];
+    uint4 x[kMergeBatch];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k)
-      x[k] = (s0 + k < ns)
-                 ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(s0 + k) * kRows * D * 2))
-                 : make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const bool in = s0 + k < ns;
+      st[k] = in ? __ldg(ml + (size_t)(s0 + k) * kRows) : make_float2(-INFINITY, 0.0f);
+      x[k] = in ? __ldg(src + (size_t)(s0 + k) * kC16 * kRows) : make_uint4(0, 0, 0, 0);
+    }
+    float mb = M;
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      if (s0 + k >= ns) break;
-      const float w = s_w[s0 + k][r];
-      if (w == 0.0f) continue;  // an empty split: its rows were never written
+    for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, st[k].x);
+    if (mb == -INFINITY) continue;  // nothing visible so far
+    const float rs = (M == -INFINITY) ? 0.0f : ex2(M - mb);
+    Ls *= rs;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= rs;
+    M = mb;
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      // an empty split (max -inf) never wrote its rows: select, do not multiply
+      if (st[k].x == -INFINITY) continue;
+      const float w = ex2(st[k].x - M) * st[k].y;
+      Ls += w;
       const uint32_t xw[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -606,12 +595,13 @@ attn_merge_kernel(const AttnParams p) {
       }
     }
   }
-  const float inv = s_inv[r];
+  const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
   const size_t orow = ((size_t)b * p.N + node) * p.Hq + h;
-  *reinterpret_cast<uint4*>(p.out + orow * D + 8 * j) =
+  *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) =
       make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
                  pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-  if (j == 0 && p.lse) p.lse[orow] = s_lse[r];
+  if (ch == 0 && p.lse)
+    p.lse[orow] = Ls > 0.0f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
 }
 
 // --------------------------------------------------------------------- host
@@ -751,8 +741,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
     return TV_ERR_CUDA;
   }
   if (sp.nsplit > 1) {
-    constexpr int kMR = 256 / (D / 8);
-    const long long ctas = sp.units * (kRows / kMR);
+    const long long ctas = sp.units * (kRows / kMergeRows) * ((D / 8) / kMergeChunks);
     if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)ctas, 1, 1), dim3(256, 1, 1), 0, stream,
                    p) != cudaSuccess) {
       (void)cudaGetLastError();
