@@ -258,17 +258,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
   } else if (T > 0 && warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    // Two streams of work, each in tile order: S(t) needs K(t) and both S
-    // buffers read (softmax of t-1); PV(t) needs V(t) and P(t) of both row
-    // blocks.  S(t+1) is issued as soon as it can be, ahead of PV(t).
+    // Three streams of work, each in tile order: S(t) needs K(t) and both S
+    // buffers read (softmax of t-1); PV_r(t) needs V(t) and P_r(t).  Each is
+    // issued as soon as its inputs are ready: S(t+1) ahead of PV(t), and the
+    // row block whose P is ready first goes first.
     constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
     bool ok = warp_wait(&bar_q, 0);
-    int ns = 0, npv = 0;  // next S tile, next PV tile
+    int ns = 0;                          // next S tile
+    int npv[2] = {0, (nrb < 2) ? T : 0};  // next PV tile of each row block
+    int vzero = -1;                      // tile whose V tail was zeroed
     long long t_idle = clock64();
-    while (ok && npv < T) {
+    while (ok && min(npv[0], npv[1]) < T) {
       bool prog = false;
-      if (ns < T && ns <= npv + 1) {
+      if (ns < T && ns <= min(npv[0], npv[1]) + 1) {
         bool ready = false;
         if (lane == 0) {
           ready = mbar_test(&bar_k_full, ns & 1);
@@ -297,46 +300,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           prog = true;
         }
       }
-      if (npv < ns) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int t = npv[r];
+        if (t >= ns) continue;
         bool ready = false;
-        if (lane == 0)
-          ready = mbar_test(&bar_v_full, npv & 1) && mbar_test(&bar_p_full[0], npv & 1) &&
-                  (nrb < 2 || mbar_test(&bar_p_full[1], npv & 1));
-        if (__shfl_sync(0xffffffffu, ready, 0)) {
-          tc_fence_after();
-          const int j0 = (t_begin + npv) * kBN;
-          const int valid = min(kBN, keys - j0);
-          if (valid < kBN) {
-            // V rows past the key range: whatever the cache holds there, make it 0
-            const int rows = kBN - valid;
-            for (int idx = lane; idx < rows * 8 * A; idx += 32) {
-              const int a = idx / (rows * 8);
-              const int rem = idx - a * rows * 8;
-              *reinterpret_cast<uint4*>(sV + a * kAtomBytes + (valid + (rem >> 3)) * 128 +
-                                        ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
-            }
+        if (lane == 0) ready = mbar_test(&bar_v_full, t & 1) && mbar_test(&bar_p_full[r], t & 1);
+        if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
+        tc_fence_after();
+        // PV runs over the 16-key steps that hold a key of the range; the V
+        // rows of the last step past the range (at most 15) are cleared, as
+        // the cache may hold anything there
+        const int valid = min(kBN, keys - (t_begin + t) * kBN);
+        const int nk = (valid + 15) >> 4;
+        if (vzero < t) {
+          const int z1 = min(kBN, nk * 16);
+          if (valid < z1) {
+#pragma unroll
+            for (int a = 0; a < A; ++a)
+              for (int zr = valid + (lane >> 3); zr < z1; zr += 4)
+                *reinterpret_cast<uint4*>(sV + a * kAtomBytes + zr * 128 + ((lane & 7) << 4)) =
+                    make_uint4(0, 0, 0, 0);
             fence_async_smem();
           }
-          __syncwarp();
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t v0 = smem_u32(sV);
-            for (int r = 0; r < nrb; ++r) {
-              const uint32_t p0 = smem_u32(sP) + r * 2 * kAtomBytes;
-#pragma unroll
-              for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_bf16(tmem + 256 + 128 * r,
-                         sw128_desc(p0 + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
-                         sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO,
-                         (npv > 0) || (kk > 0));
-              mma_commit(&bar_o_done[r]);
-            }
-            mma_commit(&bar_v_empty);
-          }
-          __syncwarp();
-          ++npv;
-          prog = true;
+          vzero = t;
         }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t v0 = smem_u32(sV);
+          const uint32_t p0 = smem_u32(sP) + r * 2 * kAtomBytes;
+          for (int kk = 0; kk < nk; ++kk)
+            mma_bf16(tmem + 256 + 128 * r,
+                     sw128_desc(p0 + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
+          mma_commit(&bar_o_done[r]);
+          // V(t) is free once both row blocks' PV(t) are done
+          if (npv[r ^ 1] > t) mma_commit(&bar_v_empty);
+        }
+        __syncwarp();
+        npv[r] = t + 1;
+        prog = true;
       }
       if (prog) {
         t_idle = clock64();
@@ -362,11 +366,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     for (int t = 0; t < T; ++t) {
       // the mask words (their ancestor loads) are ready before S is
       const int j0 = (t_begin + t) * kBN;
-      const bool unmasked = valid_row && j0 + kBN <= L;  // all prefix keys
       uint32_t vis[4] = {0u, 0u, 0u, 0u};
-      if (!unmasked && valid_row) {
+      if (valid_row) {
+        if (j0 + kBN <= L) {  // all prefix keys
 #pragma unroll
-        for (int c = 0; c < 4; ++c) vis[c] = visibility32(c, j0, L, keys, N, anc, p.W);
+          for (int c = 0; c < 4; ++c) vis[c] = 0xffffffffu;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) vis[c] = visibility32(c, j0, L, keys, N, anc, p.W);
+        }
       }
       ok = warp_wait(&bar_s_full[rb], t & 1);
       if (!ok) break;
@@ -378,15 +386,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&bar_s_free[rb]);  // the MMA warp may write the next S now
 
+      // a 32-key chunk is all visible, all hidden, or masked key by key
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (unmasked) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        if (vis[c] == 0xffffffffu) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][e]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        } else if (vis[c] != 0u) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float x = ((vis[c] >> e) & 1u) ? __uint_as_float(sr[c][e]) : -INFINITY;
@@ -424,6 +431,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const float neg_m = -m_run;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          if (vis[c] == 0u) {  // hidden chunk: P = 0
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(prow + (c >> 1) * kAtomBytes +
+                                        ((((c & 1) * 4 + q) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            continue;
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {  // 8 keys -> one 16-byte chunk of P
             uint32_t w[4];
@@ -464,10 +478,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   }
 
   // ------------------------------------------------------------ epilogue
-  tc_fence_before();
-  __syncthreads();  // every role is done; TMA and MMA work has retired
-  tc_fence_after();
-  if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
+  // Each softmax warpgroup finishes its row block as soon as its last PV
+  // retired, while the other one may still be working.
   const bool split_kv = p.nsplit > 1;
   const size_t unit = (size_t)bh * p.mtiles + mt;  // (sequence, kv head, node tile)
   if (act) {
@@ -475,52 +487,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const uint32_t tO = tmem + 256 + 128 * rb;
     const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
     const int crow = rb * kRB + row;  // row of the CTA
-    if (split_kv) {
-      const size_t slot = unit * p.nsplit + split;
-      p.part_ml[slot * kRows + crow] = make_float2(m_run, l_run);
-      if (T > 0) {
+    const size_t slot = unit * p.nsplit + split;
+    if (split_kv) p.part_ml[slot * kRows + crow] = make_float2(m_run, l_run);
+    if (T > 0) {
+      uint32_t o[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + lane_base + 32 * c, o[c]);  // warp-wide
+      tmem_wait_ld();
+      if (split_kv) {
         // normalised fp16 partial row, chunk-major: the lanes of a warp hold
         // consecutive rows, so every store instruction writes 512 contiguous bytes
         uint4* dst = reinterpret_cast<uint4*>(p.part) + slot * (D / 8) * kRows + crow;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + lane_base + 32 * c, o);
-          tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             dst[(size_t)(4 * c + q) * kRows] = make_uint4(
-                pack_f16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                pack_f16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                pack_f16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                pack_f16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-        }
-      }
-    } else {
-      // the whole key range was here: write the output row
-      uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
+                pack_f16(__uint_as_float(o[c][8 * q + 0]) * inv, __uint_as_float(o[c][8 * q + 1]) * inv),
+                pack_f16(__uint_as_float(o[c][8 * q + 2]) * inv, __uint_as_float(o[c][8 * q + 3]) * inv),
+                pack_f16(__uint_as_float(o[c][8 * q + 4]) * inv, __uint_as_float(o[c][8 * q + 5]) * inv),
+                pack_f16(__uint_as_float(o[c][8 * q + 6]) * inv, __uint_as_float(o[c][8 * q + 7]) * inv));
+      } else if (valid_row) {
+        // the whole key range was here: write the output row
+        uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_base + 32 * c, o);  // warp-wide; only valid rows store
-        tmem_wait_ld();
-        if (valid_row) {
+        for (int c = 0; c < D / 32; ++c)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             orow[4 * c + q] = make_uint4(
-                pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-        }
+                pack_bf16(__uint_as_float(o[c][8 * q + 0]) * inv, __uint_as_float(o[c][8 * q + 1]) * inv),
+                pack_bf16(__uint_as_float(o[c][8 * q + 2]) * inv, __uint_as_float(o[c][8 * q + 3]) * inv),
+                pack_bf16(__uint_as_float(o[c][8 * q + 4]) * inv, __uint_as_float(o[c][8 * q + 5]) * inv),
+                pack_bf16(__uint_as_float(o[c][8 * q + 6]) * inv, __uint_as_float(o[c][8 * q + 7]) * inv));
+        if (p.lse)
+          p.lse[((size_t)b * N + node) * p.Hq + h] =
+              l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       }
-      if (valid_row && p.lse)
-        p.lse[((size_t)b * N + node) * p.Hq + h] =
-            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // every role is done; TMA and MMA work has retired
+  if (s_abort && tid == 0 && p.status) atomicMax(p.status + b, (int)TV_ERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
