@@ -533,34 +533,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
 // Merge of the split-KV partials: for every query row, weights
 // 2^(m_s - M) * l_s over the nsplit partials, normalised, applied to the
-// normalised fp16 partial rows.  A CTA takes 32 rows x 8 chunks of one unit;
-// a warp is 32 consecutive rows of one chunk, so every load is one contiguous
-// 512-byte (chunk) or 256-byte (statistics) segment.  The statistics and the
-// partial chunks of up to kBatch splits are loaded together, then combined
-// with a running maximum, so the kernel pays about one L2 round trip per
-// kBatch splits.
-constexpr int kMergeRows = 32, kMergeChunks = 8, kMergeBatch = 24;
+// normalised fp16 partial rows.  A CTA takes 32 rows x 2 chunks of one unit;
+// its 8 warps are (chunk, slot group): warp (c, g) takes slots g, g + 4, ...
+// of chunk c for 32 consecutive rows, so every load is one contiguous 512-byte
+// (chunk) or 256-byte (statistics) segment and all of a thread's loads are in
+// flight together (in batches of 6).  The four slot groups are folded in
+// shared memory.  Four CTAs fit an SM, so a unit's 64 CTAs of the merge of a
+// one-wave attention grid run in one wave too.
+constexpr int kMergeRows = 32, kMergeChunks = 2, kMergeGroups = 4, kMergeBatch = 6;
 
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 attn_merge_kernel(const AttnParams p) {
   constexpr int kC16 = D / 8;
   constexpr int kCtaPerUnit = (kRows / kMergeRows) * (kC16 / kMergeChunks);
+  constexpr int kSPT = kMaxSplit / kMergeGroups;  // slots per thread at most
+  __shared__ float s_m[kMergeGroups][kMergeChunks][kMergeRows];
+  __shared__ float s_l[kMergeGroups][kMergeChunks][kMergeRows];
+  __shared__ float4 s_acc[kMergeGroups][kMergeChunks][2][kMergeRows];
   pdl_wait();  // the partials come from the attention kernel
   pdl_trigger();
   const int unit = blockIdx.x / kCtaPerUnit;
   const int sub = blockIdx.x % kCtaPerUnit;
-  const int crow = (sub % (kRows / kMergeRows)) * kMergeRows + (threadIdx.x & 31);
-  const int ch = (sub / (kRows / kMergeRows)) * kMergeChunks + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cl = warp % kMergeChunks, g = warp / kMergeChunks;
+  const int crow = (sub % (kRows / kMergeRows)) * kMergeRows + lane;
+  const int ch = (sub / (kRows / kMergeRows)) * kMergeChunks + cl;
   const int bh = unit / p.mtiles, mt = unit % p.mtiles;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
-  const int L = __ldg(p.kv_len + b);
-  if (L < 0 || L + p.N > p.Lcap) return;  // the attention kernel zeroed these outputs
-  const int rbk = crow / kRB, rl = crow % kRB;
-  const int nodel = rl / p.G;
-  const int node = mt * 2 * p.nb + rbk * p.nb + nodel;
-  if (nodel >= p.nb || node >= p.N) return;
-  const int h = kvh * p.G + rl % p.G;
+  const int L = __ldg(p.kv_len + b);  // checked once the loads below are in flight
   const int ns = p.nsplit;
   const float2* ml = p.part_ml + (size_t)unit * ns * kRows + crow;
   const uint4* src = reinterpret_cast<const uint4*>(p.part) + (size_t)unit * ns * kC16 * kRows +
@@ -569,14 +570,16 @@ attn_merge_kernel(const AttnParams p) {
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
+  for (int k0 = 0; k0 < kSPT; k0 += kMergeBatch) {
+    if (g + kMergeGroups * k0 >= ns) break;
     float2 st[kMergeBatch];
     uint4 x[kMergeBatch];
 #pragma unroll
     for (int k = 0; k < kMergeBatch; ++k) {
-      const bool in = s0 + k < ns;
-      st[k] = in ? __ldg(ml + (size_t)(s0 + k) * kRows) : make_float2(-INFINITY, 0.0f);
-      x[k] = in ? __ldg(src + (size_t)(s0 + k) * kC16 * kRows) : make_uint4(0, 0, 0, 0);
+      const int sl = g + kMergeGroups * (k0 + k);
+      const bool in = sl < ns;
+      st[k] = in ? __ldg(ml + (size_t)sl * kRows) : make_float2(-INFINITY, 0.0f);
+      x[k] = in ? __ldg(src + (size_t)sl * kC16 * kRows) : make_uint4(0, 0, 0, 0);
     }
     float mb = M;
 #pragma unroll
@@ -602,13 +605,48 @@ attn_merge_kernel(const AttnParams p) {
       }
     }
   }
-  const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+  s_m[g][cl][lane] = M;
+  s_l[g][cl][lane] = Ls;
+  s_acc[g][cl][0][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  s_acc[g][cl][1][lane] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (g != 0) return;
+  if (L < 0 || L + p.N > p.Lcap) return;  // the attention kernel zeroed these outputs
+  const int rbk = crow / kRB, rl = crow % kRB;
+  const int nodel = rl / p.G;
+  const int node = mt * 2 * p.nb + rbk * p.nb + nodel;
+  if (nodel >= p.nb || node >= p.N) return;
+  const int h = kvh * p.G + rl % p.G;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kMergeGroups; ++q) Mt = fmaxf(Mt, s_m[q][cl][lane]);
+  float Lt = 0.0f;
+  float o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.0f;
+#pragma unroll
+  for (int q = 0; q < kMergeGroups; ++q) {
+    const float mq = s_m[q][cl][lane];
+    if (mq == -INFINITY) continue;
+    const float sc = ex2(mq - Mt);
+    Lt = fmaf(sc, s_l[q][cl][lane], Lt);
+    const float4 a0 = s_acc[q][cl][0][lane], a1 = s_acc[q][cl][1][lane];
+    o[0] = fmaf(sc, a0.x, o[0]);
+    o[1] = fmaf(sc, a0.y, o[1]);
+    o[2] = fmaf(sc, a0.z, o[2]);
+    o[3] = fmaf(sc, a0.w, o[3]);
+    o[4] = fmaf(sc, a1.x, o[4]);
+    o[5] = fmaf(sc, a1.y, o[5]);
+    o[6] = fmaf(sc, a1.z, o[6]);
+    o[7] = fmaf(sc, a1.w, o[7]);
+  }
+  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
   const size_t orow = ((size_t)b * p.N + node) * p.Hq + h;
   *reinterpret_cast<uint4*>(p.out + orow * D + 8 * ch) =
-      make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                 pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+      make_uint4(pack_bf16(o[0] * inv, o[1] * inv), pack_bf16(o[2] * inv, o[3] * inv),
+                 pack_bf16(o[4] * inv, o[5] * inv), pack_bf16(o[6] * inv, o[7] * inv));
   if (ch == 0 && p.lse)
-    p.lse[orow] = Ls > 0.0f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+    p.lse[orow] = Lt > 0.0f ? (Mt + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
 }
 
 // --------------------------------------------------------------------- host
