@@ -142,13 +142,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
-  pdl_wait();  // everything below may read what the previous kernel wrote
+  // Barriers, TMEM and descriptor prefetches need nothing from the previous
+  // kernel, so they are set up before waiting for it.
   pdl_trigger();
   const int split = blockIdx.x, mt = blockIdx.y, bh = blockIdx.z;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N, G = p.G, nb = p.nb;
-  const int L = __ldg(p.kv_len + b);
   const int node0 = mt * 2 * nb;                 // first node of this CTA
   const int nrb = (node0 + nb < N) ? 2 : 1;      // row blocks holding a node
   const bool is_softmax = warp < 8;
@@ -186,6 +186,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+    }
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+  pdl_wait();  // everything below may read what the previous kernel wrote
+  const int L = __ldg(p.kv_len + b);
+  if (tid == 0) {
+    if (first_issued) {
       // Q: box {64 dims, G heads, nb nodes} per (row block, atom); rows come
       // out node-major, matching the row numbering
       mbar_expect_tx(&bar_q, (uint32_t)(nrb * A * 64 * G * nb * 2));
@@ -203,7 +210,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
     }
   }
-  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -551,8 +557,8 @@ attn_merge_kernel(const AttnParams p) {
   __shared__ float s_m[kMergeGroups][kMergeChunks][kMergeRows];
   __shared__ float s_l[kMergeGroups][kMergeChunks][kMergeRows];
   __shared__ float4 s_acc[kMergeGroups][kMergeChunks][2][kMergeRows];
-  pdl_wait();  // the partials come from the attention kernel
   pdl_trigger();
+  pdl_wait();  // the partials come from the attention kernel
   const int unit = blockIdx.x / kCtaPerUnit;
   const int sub = blockIdx.x % kCtaPerUnit;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

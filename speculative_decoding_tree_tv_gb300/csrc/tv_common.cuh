@@ -94,8 +94,10 @@ __device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialisation may start while the previous kernel on the stream is still
 // running; it must call pdl_wait() before touching anything that kernel
-// writes, and it calls pdl_trigger() (after its own pdl_wait()) to let the
-// next kernel start early.  Without the launch attribute both are no-ops.
+// writes (the wait returns once that kernel has completed and its memory
+// operations are visible).  pdl_trigger() lets the next kernel start early;
+// since that kernel waits in turn, every kernel here triggers first thing.
+// Without the launch attribute both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -69,8 +69,8 @@ __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, si
 
 __global__ void __launch_bounds__(kExpThreads)
 exp_stats_kernel(const float* __restrict__ logits, int V, int chunks, ExpPartial* __restrict__ part) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const float* x = logits + (size_t)row * V;
   const int start = blockIdx.x * kExpChunk;
@@ -135,8 +135,8 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
                    ExpWs ws) {
   __shared__ unsigned long long s_anchor;
   __shared__ double s_m_row[kMaxBudget];
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   if (tid == 0) s_anchor = 0ull;
   __syncthreads();
@@ -180,8 +180,8 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
 
 __global__ void __launch_bounds__(kExpThreads)
 exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const float thr = ws.rows[row].thr;
   if (!(thr < INFINITY)) return;
@@ -272,8 +272,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
   __shared__ unsigned int s_hist[256];
   __shared__ int s_n, s_nt, s_digit, s_need;
   __shared__ unsigned long long s_min;
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   const ExpCtl ctl = *ws.ctl;
   const int count = ctl.count, limit = ctl.limit;

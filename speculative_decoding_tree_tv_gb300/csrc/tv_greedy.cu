@@ -175,8 +175,8 @@ greedy_kernel(const GreedyArgs g) {
   __shared__ ArgMax s_red[kGreedyThreads / 32];
   __shared__ int s_last;
   const int tid = threadIdx.x;
-  pdl_wait();  // the logits may come from the previous kernel
   pdl_trigger();
+  pdl_wait();  // the logits may come from the previous kernel
   const int U = g.V / VEC;  // units per row
   const long long row = blockIdx.x / g.chunks;
   const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;

@@ -31,8 +31,8 @@ struct RowPartial {
 __global__ void __launch_bounds__(kStatThreads)
 row_stats_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logits, int rows,
                  int V, int chunks, float inv_t, RowPartial* __restrict__ part) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x / chunks;
   const int chunk = blockIdx.x % chunks;
   const int which = blockIdx.y;  // 0: p, 1: q
@@ -132,8 +132,8 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
             int32_t* __restrict__ accept_len, int32_t* __restrict__ end_node,
             int32_t* __restrict__ path, int32_t* __restrict__ out_token,
             int32_t* __restrict__ status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int rows = gridDim.x * N;

@@ -15,8 +15,8 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
                   uint64_t* __restrict__ anc_mask, int32_t* __restrict__ status) {
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ uint64_t s_anc[kMaxNodes * kMaxWords];
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int32_t* par = parent + (size_t)b * N;
   int32_t* dep = depth + (size_t)b * N;

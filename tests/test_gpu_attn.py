@@ -118,3 +118,41 @@ def test_config3_talon_tree_sampled(tv, oracle_mod):
     tree = oracle_mod.expand_tree(d, 10, 0.3, 512)
     case = gen.config3_verify(tree["parent"], 1, tokens=tree["token"])
     sampled_check(tv, oracle_mod, case, 24, 7, "config3")
+
+
+def test_merge_kernel_path_large_batch(tv, oracle_mod):
+    """160 (sequence, kv head) units: the split plan is more than one wave, so
+    the splits cannot wait for one another and a separate kernel merges them."""
+    case = gen.make_case(23, B=40, N=60, L=1500, Hq=16, Hkv=4, D=64, V=64)
+    assert tv.attn_workspace_size(40, 60, 16, 4, 64, case.Lcap) > 0
+    sampled_check(tv, oracle_mod, case, 48, 8, "merge-kernel")
+
+
+def test_split_plan_repeats_bitwise(tv, oracle_mod):
+    """A split plan on a reused workspace: repeated calls agree bit for bit
+    (the merge order is fixed) and match the oracle."""
+    case = gen.make_case(24, B=1, N=60, L=1500, Hq=32, Hkv=8, D=128, V=64, tree="spine60")
+    assert tv.attn_workspace_size(1, 60, 32, 8, 128, case.Lcap) > 0
+    first = run_attn(tv, case)
+    for _ in range(3):
+        again = run_attn(tv, case)
+        assert np.array_equal(first[0], again[0])
+        assert np.array_equal(first[1], again[1])
+    ref, ref_lse = oracle_mod.attn_all(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq,
+                                       case.Hkv)
+    check_attn(first[0], ref, "coop")
+
+
+def test_bad_kv_len_in_a_split_plan(tv, oracle_mod):
+    """A sequence whose kv_len does not fit the cache is flagged and zeroed
+    while the others of the batch, split across CTAs, are still right."""
+    case = gen.make_case(25, B=3, N=40, L=900, Hq=8, Hkv=2, D=64, V=64)
+    assert tv.attn_workspace_size(3, 40, 8, 2, 64, case.Lcap) > 0
+    good = case.kv_len.copy()
+    case.kv_len = np.array([good[0], case.Lcap, -1], np.int32)
+    out, lse, status = run_attn(tv, case)
+    assert status.tolist() == [0, 1, 1]
+    assert (out[1:] == 0).all()
+    rows = np.array([(0, n, h) for n in range(0, 40, 3) for h in range(8)], np.int64)
+    ref, ref_lse = oracle_mod.attn_rows(case.q, case.k, case.v, good, case.parent, 8, 2, rows)
+    check_attn(out[rows[:, 0], rows[:, 1], rows[:, 2]], ref, "split-bad-kv")
