@@ -7,11 +7,13 @@
 // of one row's logits.  Items are numbered row-major, so the CTAs resident at
 // any moment sweep one contiguous stretch of memory (which keeps every DRAM
 // channel busy), and the chunk length is chosen so that all items fit in one
-// wave of resident CTAs.  Each thread keeps 8 16-byte non-allocating loads in
-// flight; the CTA reduces its chunk to (max, lowest index) and folds it into
-// the row's 64-bit key (order-preserving float bits, inverted index) with
-// atomicMax.  The CTA that completes a sequence's N * chunks arrivals runs
-// that tree's scan:
+// wave of resident CTAs.  With 16-byte-aligned rows the chunk (about 51 KB for
+// a 128K vocabulary) is brought into shared memory by bulk copies, so every
+// byte of the logits is requested at once without holding registers.  The
+// CTA reduces its chunk to (max, lowest index) and folds it into the row's
+// 64-bit key (order-preserving float bits, inverted index) with atomicMax.
+// The CTA that completes a sequence's N * chunks arrivals runs that tree's
+// scan:
 //   match[i] = tokens[i] == argmax[parent[i]],
 //   valid[i] = AND of match over the root path (pointer jumping),
 //   end      = deepest valid node, ties to the lowest index,
@@ -21,13 +23,13 @@
 #include <mutex>
 
 #include "tv_common.cuh"
+#include "tv_sm100.cuh"
 
 namespace tv {
 namespace {
 
 constexpr int kGreedyThreads = 256;
 constexpr int kGreedyCtasPerSm = 4;  // resident CTAs per SM assumed when sizing chunks
-constexpr int kLoadsInFlight = 8;  // vector loads per thread per batch
 constexpr int kScanNodesPerThread = (kMaxNodes + kGreedyThreads - 1) / kGreedyThreads;
 
 struct GreedyWs {
@@ -73,67 +75,82 @@ __device__ ArgMax block_argmax(ArgMax a, ArgMax* s_red) {
   return r;
 }
 
-// Longest matching branch of tree b (run by one CTA after every row key of b is final).
-__device__ void tree_scan(const GreedyArgs& g, int b) {
-  __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes], s_am[kMaxNodes];
-  __shared__ int32_t s_valid[kMaxNodes], s_jump[kMaxNodes];
-  __shared__ unsigned int s_best;
+// Shared-memory arrays of one tree scan.
+struct ScanSmem {
+  int32_t par[kMaxNodes], tok[kMaxNodes], dep[kMaxNodes];
+  int32_t am[kMaxNodes], valid[kMaxNodes], jump[kMaxNodes];
+  unsigned int best;
+};
+
+// Pull sequence b's parent, token and depth arrays into L2 while the logits
+// stream, so that the scan's reads of them are L2 hits.
+__device__ __forceinline__ void prefetch_tree(const GreedyArgs& g, int b) {
+  const int lines = ceil_div(g.N * (int)sizeof(int32_t), 128);
+  const int t = threadIdx.x;
+  if (t < 3 * lines) {
+    const int32_t* arr = (t < lines) ? g.parent : (t < 2 * lines) ? g.tokens : g.depth;
+    const char* addr = reinterpret_cast<const char*>(arr + (size_t)b * g.N) + (t % lines) * 128;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+  }
+}
+
+// Longest matching branch of tree b (run by one CTA after every row key of b
+// is final).  `err` is a status to report instead of success (a timed-out
+// copy in some CTA of the sequence), or TV_OK.
+__device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
   const int tid = threadIdx.x;
   const int N = g.N;
-  const int32_t* par = g.parent + (size_t)b * N;
-  const int32_t* tok = g.tokens + (size_t)b * N;
-  const int32_t* dep = g.depth + (size_t)b * N;
+  const size_t o = (size_t)b * N;
   int bad_tree = 0, bad_tok = 0;
   __syncthreads();
   for (int i = tid; i < N; i += kGreedyThreads) {
-    const unsigned long long key = atomicExch(g.ws.keys + (size_t)b * N + i, 0ull);
+    const unsigned long long key = atomicExch(g.ws.keys + o + i, 0ull);
     const int am = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
-    s_am[i] = am;
-    g.argmax[(size_t)b * N + i] = am;
-    const int p = par[i];
-    s_par[i] = p;
-    s_dep[i] = dep[i];
+    sm.am[i] = am;
+    g.argmax[o + i] = am;
+    const int p = __ldcg(g.parent + o + i);
+    sm.par[i] = p;
+    sm.dep[i] = __ldcg(g.depth + o + i);
+    const int tk = __ldcg(g.tokens + o + i);
+    sm.tok[i] = tk;
     bad_tree |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
-    if (i > 0) {
-      const int t = tok[i];
-      bad_tok |= (t < 0 || t >= g.V);
-    }
+    if (i > 0) bad_tok |= (tk < 0 || tk >= g.V);
   }
   if (tid == 0) {
     g.ws.arrivals[b] = 0u;
-    s_best = 0u;
+    sm.best = 0u;
   }
   bad_tree = __syncthreads_or(bad_tree);
   if (!bad_tree) {
     for (int i = tid; i < N; i += kGreedyThreads)
-      bad_tree |= (i == 0) ? (s_dep[0] != 0) : (s_dep[i] != s_dep[s_par[i]] + 1);
+      bad_tree |= (i == 0) ? (sm.dep[0] != 0) : (sm.dep[i] != sm.dep[sm.par[i]] + 1);
   }
   bad_tree = __syncthreads_or(bad_tree);
   bad_tok = __syncthreads_or(bad_tok);
-  int32_t* pth = g.path + (size_t)b * N;
-  if (bad_tree || bad_tok) {
+  int32_t* pth = g.path + o;
+  if (bad_tree || bad_tok || err != TV_OK) {
     for (int i = tid; i < N; i += kGreedyThreads) pth[i] = -1;
     if (tid == 0) {
       g.accept_len[b] = g.end_node[b] = g.bonus[b] = -1;
-      g.status[b] = bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
+      g.status[b] = err != TV_OK ? err : bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
     }
     return;
   }
   for (int i = tid; i < N; i += kGreedyThreads) {
-    s_valid[i] = (i == 0) ? 1 : (tok[i] == s_am[s_par[i]]);
-    s_jump[i] = s_par[i];
+    sm.valid[i] = (i == 0) ? 1 : (sm.tok[i] == sm.am[sm.par[i]]);
+    sm.jump[i] = sm.par[i];
   }
   __syncthreads();
-  // pointer jumping: after r rounds s_valid[i] covers 2^r edges above i
+  // pointer jumping: after r rounds valid[i] covers 2^r edges above i
   for (int span = 1; span < N; span <<= 1) {
     int nv[kScanNodesPerThread], nj[kScanNodesPerThread];
 #pragma unroll
     for (int k = 0; k < kScanNodesPerThread; ++k) {
       const int i = tid + k * kGreedyThreads;
       if (i < N) {
-        const int j = s_jump[i];
-        nv[k] = s_valid[i] & (j < 0 ? 1 : s_valid[j]);
-        nj[k] = j < 0 ? -1 : s_jump[j];
+        const int j = sm.jump[i];
+        nv[k] = sm.valid[i] & (j < 0 ? 1 : sm.valid[j]);
+        nj[k] = j < 0 ? -1 : sm.jump[j];
       }
     }
     __syncthreads();
@@ -141,8 +158,8 @@ __device__ void tree_scan(const GreedyArgs& g, int b) {
     for (int k = 0; k < kScanNodesPerThread; ++k) {
       const int i = tid + k * kGreedyThreads;
       if (i < N) {
-        s_valid[i] = nv[k];
-        s_jump[i] = nj[k];
+        sm.valid[i] = nv[k];
+        sm.jump[i] = nj[k];
       }
     }
     __syncthreads();
@@ -150,98 +167,302 @@ __device__ void tree_scan(const GreedyArgs& g, int b) {
   // deepest valid node, lowest index on ties
   unsigned int mine = 0u;
   for (int i = tid; i < N; i += kGreedyThreads)
-    if (s_valid[i]) mine = max(mine, ((unsigned int)s_dep[i] << 16) | (0xffffu - (unsigned int)i));
+    if (sm.valid[i]) mine = max(mine, ((unsigned int)sm.dep[i] << 16) | (0xffffu - (unsigned int)i));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, o));
-  if ((tid & 31) == 0) atomicMax(&s_best, mine);
+  for (int w = 16; w > 0; w >>= 1) mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, w));
+  if ((tid & 31) == 0) atomicMax(&sm.best, mine);
   __syncthreads();
-  const int end = (int)(0xffffu - (s_best & 0xffffu));
-  const int end_depth = s_dep[end];
+  const int end = (int)(0xffffu - (sm.best & 0xffffu));
+  const int end_depth = sm.dep[end];
   for (int i = tid; i < N; i += kGreedyThreads)
     if (i > end_depth) pth[i] = -1;
   if (tid == 0) {
-    for (int x = end, d = end_depth; x >= 0; x = s_par[x], --d) pth[d] = x;
+    for (int x = end, d = end_depth; x >= 0; x = sm.par[x], --d) pth[d] = x;
     g.accept_len[b] = end_depth;
     g.end_node[b] = end;
-    g.bonus[b] = s_am[end];
+    g.bonus[b] = sm.am[end];
     g.status[b] = TV_OK;
   }
 }
 
-// VEC = 4: rows are 16-byte aligned and read as float4; VEC = 1: scalars.
-template <int VEC>
+__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// The same scan for trees of at most 64 nodes, by one warp in registers:
+// node i lives in lane i % 32, slot i / 32, and an array is read at another
+// node with two shuffles.  Pointer jumping keeps each round's jump table
+// (ancestor at distance 2^r), from which every lane lifts the end node to the
+// depth of the path entries it writes.
+constexpr int kWarpScanMax = 64;
+
+__device__ __forceinline__ int gather2(const int (&v)[2], int j) {
+  const int lo = __shfl_sync(0xffffffffu, v[0], j & 31);
+  const int hi = __shfl_sync(0xffffffffu, v[1], j & 31);
+  return (j < 32) ? lo : hi;
+}
+
+__device__ void warp_scan(const GreedyArgs& g, int b, int err) {
+  const int lane = threadIdx.x & 31;
+  const int N = g.N;
+  const size_t o = (size_t)b * N;
+  int par[2], dep[2], tok[2], am[2];
+  bool in[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    in[s] = i < N;
+    const unsigned long long key = in[s] ? atomicExch(g.ws.keys + o + i, 0ull) : 0ull;
+    am[s] = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
+    par[s] = in[s] ? __ldcg(g.parent + o + i) : -1;
+    dep[s] = in[s] ? __ldcg(g.depth + o + i) : 0;
+    tok[s] = in[s] ? __ldcg(g.tokens + o + i) : 0;
+    if (in[s]) g.argmax[o + i] = am[s];
+  }
+  if (lane == 0) g.ws.arrivals[b] = 0u;
+  int bad_tree = 0, bad_tok = 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    if (in[s]) {
+      bad_tree |= (i == 0) ? (par[s] != -1) : (par[s] < 0 || par[s] >= i);
+      if (i > 0) bad_tok |= (tok[s] < 0 || tok[s] >= g.V);
+    }
+  }
+  bad_tree = __any_sync(0xffffffffu, bad_tree);
+  if (!bad_tree) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int i = lane + 32 * s;
+      const int dp = gather2(dep, max(par[s], 0));
+      if (in[s]) bad_tree |= (i == 0) ? (dep[s] != 0) : (dep[s] != dp + 1);
+    }
+    bad_tree = __any_sync(0xffffffffu, bad_tree);
+  }
+  bad_tok = __any_sync(0xffffffffu, bad_tok);
+  int32_t* pth = g.path + o;
+  if (bad_tree || bad_tok || err != TV_OK) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      if (in[s]) pth[lane + 32 * s] = -1;
+    if (lane == 0) {
+      g.accept_len[b] = g.end_node[b] = g.bonus[b] = -1;
+      g.status[b] = err != TV_OK ? err : bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
+    }
+    return;
+  }
+  int val[2], jmp[2], lift[6][2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    const int amp = gather2(am, max(par[s], 0));
+    val[s] = in[s] ? ((i == 0) ? 1 : (tok[s] == amp)) : 0;
+    jmp[s] = par[s];
+  }
+  // after round r, val[i] covers 2^(r+1) edges above i; lift[r] = ancestor at distance 2^r
+#pragma unroll
+  for (int r = 0; r < 6; ++r) {
+    lift[r][0] = jmp[0];
+    lift[r][1] = jmp[1];
+    if ((1 << r) >= N) continue;  // uniform
+    int nv[2], nj[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int j = jmp[s];
+      const int vj = gather2(val, max(j, 0));
+      const int jj = gather2(jmp, max(j, 0));
+      nv[s] = val[s] & (j < 0 ? 1 : vj);
+      nj[s] = j < 0 ? -1 : jj;
+    }
+    val[0] = nv[0];
+    val[1] = nv[1];
+    jmp[0] = nj[0];
+    jmp[1] = nj[1];
+  }
+  // deepest valid node, lowest index on ties
+  unsigned int mine = 0u;
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+    if (in[s] && val[s])
+      mine = max(mine, ((unsigned int)dep[s] << 16) | (0xffffu - (unsigned int)(lane + 32 * s)));
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, w));
+  const int end = (int)(0xffffu - (mine & 0xffffu));
+  const int end_depth = (int)(mine >> 16);
+  // path[d] = ancestor of end at distance end_depth - d, for d <= end_depth
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int d = lane + 32 * s;
+    const int k = max(end_depth - d, 0);
+    int x = end;
+#pragma unroll
+    for (int r = 0; r < 6; ++r) {
+      int lr[2] = {lift[r][0], lift[r][1]};
+      const int up = gather2(lr, max(x, 0));
+      if ((k >> r) & 1) x = up;
+    }
+    if (d < N) pth[d] = (d <= end_depth) ? x : -1;
+  }
+  const int bonus = gather2(am, end);
+  if (lane == 0) {
+    g.accept_len[b] = end_depth;
+    g.end_node[b] = end;
+    g.bonus[b] = bonus;
+    g.status[b] = TV_OK;
+  }
+}
+
+// Fold the CTA's (max, lowest index) into the row key, count the arrival, and
+// run the tree scan if this CTA completes the sequence.  A timed-out copy
+// sets bit 31 of the arrival counter, which the scan reports.
+__device__ __forceinline__ void finish_item(const GreedyArgs& g, long long row, int b, ArgMax best,
+                                            ArgMax* s_red, int* s_last, bool timed_out,
+                                            ScanSmem& sm) {
+  best = block_argmax(best, s_red);
+  if (threadIdx.x == 0) {
+    // the key update needs no answer; the arrival is a release (ordering the
+    // update before it) and an acquire (the last arrival sees every update)
+    red_max_u64(g.ws.keys + row, pack_key(best));
+    const unsigned int prev = atom_add_acq_rel(g.ws.arrivals + b, timed_out ? 0x80000001u : 1u);
+    const bool last = ((prev & 0x7fffffffu) == (unsigned int)(g.N * g.chunks - 1));
+    *s_last = last ? (((prev >> 31) | (timed_out ? 1u : 0u)) ? 2 : 1) : 0;
+  }
+  __syncthreads();
+  if (*s_last) {
+    const int err = *s_last == 2 ? TV_ERR_TIMEOUT : TV_OK;
+    if (g.N <= kWarpScanMax) {
+      if (threadIdx.x < 32) warp_scan(g, b, err);
+    } else {
+      tree_scan(g, b, sm, err);
+    }
+  }
+}
+
+// Rows 16-byte aligned (V % 4 == 0): the CTA's chunk of one row is brought
+// into shared memory by bulk copies (two pieces, each on its own mbarrier),
+// so the whole chunk is in flight at once without holding registers; the
+// reduction then reads shared memory.  The chunk buffer is reused by the scan.
+constexpr int kGreedyPieces = 2;
+
 __global__ void __launch_bounds__(kGreedyThreads)
-greedy_kernel(const GreedyArgs g) {
+greedy_bulk_kernel(const GreedyArgs g) {
+  extern __shared__ __align__(128) uint8_t g_smem[];
+  __shared__ __align__(8) uint64_t s_bar[kGreedyPieces];
   __shared__ ArgMax s_red[kGreedyThreads / 32];
   __shared__ int s_last;
   const int tid = threadIdx.x;
-  pdl_trigger();
-  pdl_wait();  // the logits may come from the previous kernel
-  const int U = g.V / VEC;  // units per row
+  const int U = g.V / 4;
   const long long row = blockIdx.x / g.chunks;
   const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;
   const int n = min(g.chunk_units, U - base);
   const int b = (int)(row / g.N);
-  ArgMax best{-INFINITY, INT_MAX};
-  if (VEC == 4) {
-    const float4* x4 = reinterpret_cast<const float4*>(g.logits + row * (long long)g.V) + base;
-    for (int k0 = 0; k0 < n; k0 += kLoadsInFlight * kGreedyThreads) {
-      float4 buf[kLoadsInFlight];
-#pragma unroll
-      for (int j = 0; j < kLoadsInFlight; ++j) {
-        const int k = k0 + j * kGreedyThreads + tid;
-        buf[j] = (k < n) ? ld_stream_f4(x4 + k)
-                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
-#pragma unroll
-      for (int j = 0; j < kLoadsInFlight; ++j) {
-        const int k = k0 + j * kGreedyThreads + tid;
-        const int e = 4 * (base + k);
-        if (k < n) {
-          if (buf[j].x > best.v) best = {buf[j].x, e};
-          if (buf[j].y > best.v) best = {buf[j].y, e + 1};
-          if (buf[j].z > best.v) best = {buf[j].z, e + 2};
-          if (buf[j].w > best.v) best = {buf[j].w, e + 3};
-        }
-      }
-    }
-  } else {
-    const float* x = g.logits + row * (long long)g.V + base;
-    for (int k = tid; k < n; k += kGreedyThreads) {
-      const float v = __ldg(x + k);
-      if (v > best.v) best = {v, base + k};
-    }
-  }
-  if (best.i == INT_MAX) best.i = VEC * base;  // only -inf seen: lowest index of the chunk
-  best = block_argmax(best, s_red);
+  const int per = ceil_div(n, kGreedyPieces);
   if (tid == 0) {
-    atomicMax(g.ws.keys + row, pack_key(best));
-    __threadfence();
-    const unsigned int prev = atomicAdd(g.ws.arrivals + b, 1u);
-    s_last = (prev == (unsigned int)(g.N * g.chunks - 1));
+    for (int q = 0; q < kGreedyPieces; ++q) sm100::mbar_init(&s_bar[q], 1);
+    sm100::mbar_fence_init();
   }
   __syncthreads();
-  if (s_last) {
-    __threadfence();
-    tree_scan(g, b);
+  pdl_trigger();
+  pdl_wait();  // the logits may come from the previous kernel
+  if (tid == 0) {
+    const float4* src = reinterpret_cast<const float4*>(g.logits + row * (long long)g.V) + base;
+    for (int q = 0; q < kGreedyPieces; ++q) {
+      const int q0 = q * per, qn = min(per, n - q0);
+      if (qn <= 0) break;
+      sm100::mbar_expect_tx(&s_bar[q], (uint32_t)qn * 16u);
+      sm100::bulk_load_global(g_smem + (size_t)q0 * 16, src + q0, (uint32_t)qn * 16u, &s_bar[q]);
+    }
   }
+  prefetch_tree(g, b);
+  ArgMax best{-INFINITY, INT_MAX};
+  bool ok = true;
+  const float4* x4 = reinterpret_cast<const float4*>(g_smem);
+  for (int q = 0; q < kGreedyPieces; ++q) {
+    const int q0 = q * per, qn = min(per, n - q0);
+    if (qn <= 0) break;
+    if (!sm100::mbar_wait(&s_bar[q], 0)) {
+      ok = false;  // every copy of this CTA is waited for (bounded) below
+      continue;
+    }
+    for (int k = q0 + tid; k < q0 + qn; k += kGreedyThreads) {
+      const float4 v = x4[k];
+      const int e = 4 * (base + k);
+      if (v.x > best.v) best = {v.x, e};
+      if (v.y > best.v) best = {v.y, e + 1};
+      if (v.z > best.v) best = {v.z, e + 2};
+      if (v.w > best.v) best = {v.w, e + 3};
+    }
+  }
+  if (best.i == INT_MAX) best.i = 4 * base;  // only -inf seen: lowest index of the chunk
+  const bool timed_out = __syncthreads_or(!ok) != 0;
+  // the chunk buffer is dead once every thread has reduced it (the block
+  // reduction below starts with a barrier)
+  finish_item(g, row, b, best, s_red, &s_last, timed_out, *reinterpret_cast<ScanSmem*>(g_smem));
 }
+
+// Rows not 16-byte aligned (V % 4 != 0): scalar loads.
+__global__ void __launch_bounds__(kGreedyThreads)
+greedy_scalar_kernel(const GreedyArgs g) {
+  __shared__ ArgMax s_red[kGreedyThreads / 32];
+  __shared__ int s_last;
+  __shared__ ScanSmem s_scan;
+  const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the logits may come from the previous kernel
+  const long long row = blockIdx.x / g.chunks;
+  const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;
+  const int n = min(g.chunk_units, g.V - base);
+  const int b = (int)(row / g.N);
+  prefetch_tree(g, b);
+  ArgMax best{-INFINITY, INT_MAX};
+  const float* x = g.logits + row * (long long)g.V + base;
+  for (int k = tid; k < n; k += kGreedyThreads) {
+    const float v = __ldg(x + k);
+    if (v > best.v) best = {v, base + k};
+  }
+  if (best.i == INT_MAX) best.i = base;  // only -inf seen: lowest index of the chunk
+  finish_item(g, row, b, best, s_red, &s_last, false, s_scan);
+}
+
+// Largest chunk a CTA stages (4 CTAs of this size, plus their static shared
+// memory, fit the 228 KB of an SM); bigger rows take more chunks per row.
+constexpr int kGreedyChunkMaxBytes = 55296;
 
 tv_status launch_greedy(const GreedyArgs& in, cudaStream_t stream) {
   GreedyArgs g = in;
-  const int VEC = ((g.V & 3) == 0) ? 4 : 1;
-  const int U = g.V / VEC;
+  const bool bulk = (g.V & 3) == 0;
+  const int U = bulk ? g.V / 4 : g.V;
   const long long rows = (long long)g.B * g.N;
   // chunks per row: as many as fit one wave of resident CTAs, at least one
   const long long slots = (long long)device_sm_count() * kGreedyCtasPerSm;
   int chunks = (int)(slots / rows);
   chunks = max(1, min(chunks, ceil_div(U, kGreedyThreads)));
+  if (bulk)  // a staged chunk must fit its shared-memory budget
+    while ((long long)ceil_div(U, chunks) * 16 > kGreedyChunkMaxBytes) ++chunks;
   g.chunk_units = ceil_div(U, chunks);
   g.chunks = ceil_div(U, g.chunk_units);
   const long long ctas = rows * g.chunks;
-  const cudaError_t err =
-      VEC == 4 ? launch_pdl(greedy_kernel<4>, dim3((unsigned)ctas), dim3(kGreedyThreads), 0, stream, g)
-               : launch_pdl(greedy_kernel<1>, dim3((unsigned)ctas), dim3(kGreedyThreads), 0, stream, g);
+  cudaError_t err;
+  if (bulk) {
+    const size_t smem = max((size_t)g.chunk_units * 16, sizeof(ScanSmem));
+    static bool smem_set = false;
+    if (!smem_set) {
+      if (cudaFuncSetAttribute(greedy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGreedyChunkMaxBytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TV_ERR_CUDA;
+      }
+      smem_set = true;
+    }
+    err = launch_pdl(greedy_bulk_kernel, dim3((unsigned)ctas), dim3(kGreedyThreads), smem, stream, g);
+  } else {
+    err = launch_pdl(greedy_scalar_kernel, dim3((unsigned)ctas), dim3(kGreedyThreads), 0, stream, g);
+  }
   if (err != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;

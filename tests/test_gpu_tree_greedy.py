@@ -83,6 +83,7 @@ def test_greedy_batched_ragged_shapes(tv, oracle_mod):
     (1, 1, 1, 2, "chain"), (2, 3, 5, 3, "random"), (3, 2, 17, 257, "random"),
     (4, 4, 64, 300, "random"), (5, 1, 40, 8193, "chain"), (6, 2, 33, 16384, "star"),
     (7, 5, 12, 1001, "random"), (8, 1, 512, 50, "random"), (9, 2, 100, 24577, "random"),
+    (10, 1, 3, 262148, "chain"),  # 1 MB rows: many staged chunks per row
 ])
 def test_greedy_fuzz(tv, oracle_mod, seed, B, N, V, tree):
     r = gen.rng(seed)
@@ -127,3 +128,27 @@ def test_greedy_repeated_calls_reuse_workspace(tv, oracle_mod):
         compare_greedy(run_greedy(tv, case), o)
     ws = tv.workspace("greedy", 0, dev())
     assert int(ws.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("N", [10, 64, 65, 100])
+def test_greedy_bad_inputs_both_scan_paths(tv, oracle_mod, N):
+    """Trees of up to 64 nodes are scanned by one warp, larger ones by the
+    whole CTA; both flag a bad token, a forward edge and a depth that does
+    not match the parents, sequence by sequence."""
+    case = gen.make_case(220 + N, B=5, N=N, L=4, V=300, with_attn=False)
+    case.tokens[1, N - 1] = 300       # out of range
+    case.parent[2, N // 2] = N - 1    # forward edge
+    t = case_tensors(case)
+    depth, anc, st = tv.tree_build(t["parent"])
+    depth[3, N - 1] += 1              # depth inconsistent with the parents
+    res = tv.accept_greedy(t["logits"], t["tokens"], t["parent"], depth)
+    g = {k: np_(v) for k, v in res.items()}
+    o = oracle_mod.accept_greedy(case.logits, case.tokens, case.parent)
+    assert g["status"].tolist() == [0, 6, 2, 2, 0]
+    for b in (0, 4):
+        for k in ("accept_len", "end_node", "path", "bonus"):
+            assert np.array_equal(g[k][b], o[k][b]), (k, b)
+    for b in (1, 2, 3):
+        assert g["accept_len"][b] == g["end_node"][b] == g["bonus"][b] == -1
+        assert (g["path"][b] == -1).all()
+    assert np.array_equal(g["argmax"], o["argmax"])
