@@ -51,6 +51,9 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph-steps", type=int, default=200)
+    p.add_argument("--ncu-steps", type=int, default=0,
+                   help="profiling driver: run this many eager steps of the workload on "
+                        "one input set (no graphs, no timing) and exit; for ncu captures")
     return p.parse_args()
 
 
@@ -60,6 +63,42 @@ def parse_args():
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# entry point, from the ncu captures summarised under profiles/.  A figure is
+# reported only while the kernel sources hash to the value recorded when the
+# counters were taken; after any change to them it is null until re-captured.
+KERNEL_SOURCES = {
+    "tv_tree_build": ["tv_tree.cu", "tv_common.cuh"],
+    "tv_attn_verify": ["tv_attn.cu", "tv_sm100.cuh", "tv_common.cuh"],
+    "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
+}
+NCU_TRAFFIC = {
+    # attention kernel, cold (9,509,120) + merge kernel with L2 warm (768 + 389,632)
+    "tv_attn_verify": {"sha256": "6dba0f253d24ade2317211855cfb343c0fa46f323b23ca0fcaab92bcb6e05a08", "bytes": 9899520,
+                       "profile": "profiles/attn_verify_llama3-8b-spine60.md"},
+    "tv_accept_greedy": {"sha256": "b5a20f8a7fbc7d8c3f0aae88ea7f6450bcc4b5f6e3ae90fc80e609f80885715e", "bytes": 30823424,
+                         "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},
+    "tv_tree_build": {"sha256": "7525175311d2e607c52b62e3cebfc56ca5e70ff278fa81af761f2aad43ad32ea", "bytes": 6656,
+                      "profile": "profiles/tree_build_kernel_llama3-8b-spine60.md"},
+}
+
+
+def sources_sha256(name):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[name]:
+        with open(os.path.join(ROOT, "speculative_decoding_tree_tv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(name):
+    rec = NCU_TRAFFIC.get(name)
+    if rec is None or rec["sha256"] != sources_sha256(name):
+        return None
+    return rec["bytes"]
 
 
 def load_peaks():
@@ -171,6 +210,26 @@ def make_sets(case, torch, device, l2_bytes):
 # ----------------------------------------------------------------------------
 # our implementation
 # ----------------------------------------------------------------------------
+def run_ncu_steps(args):
+    """K eager steps (tree -> attention -> greedy) on one input set, for ncu:
+    each launch is a separate, serialised kernel there, so the per-launch
+    counters of the same kernels as in the timed run can be read."""
+    import torch
+    import speculative_decoding_tree_tv_gb300 as tv
+    from workloads import gen
+
+    device = torch.device("cuda", 0)
+    case = gen.config2()
+    s = make_sets(case, torch, device, 0)[0][0]
+    for _ in range(args.ncu_steps):
+        depth, anc, tstat = tv.tree_build(s["parent"])
+        out, lse, astat = tv.attn_verify(s["q"], s["k"], s["v"], s["kv_len"], anc)
+        res = tv.accept_greedy(s["logits"], s["tokens"], s["parent"], depth)
+    torch.cuda.synchronize()
+    assert int(tstat[0]) == 0 and int(astat[0]) == 0 and int(res["status"][0]) == 0
+    print(json.dumps({"ncu_steps": args.ncu_steps, "workload": WORKLOAD}), flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import speculative_decoding_tree_tv_gb300 as tv
@@ -462,6 +521,9 @@ def main():
             print(json.dumps(line), flush=True)
         return
 
+    if args.ncu_steps > 0:
+        run_ncu_steps(args)
+        return
     r = run_ours(args, rank, world, local_rank)
     if rank != 0:
         return
@@ -481,6 +543,16 @@ def main():
     attn_gbs = nbytes["attn"] / (a_us * 1e-6) / 1e9
     t_roof_us = sum(max(nbytes[k] / (hbm * 1e9), (flops if k == "attn" else 0) / (tflops * 1e12))
                     for k in nbytes) * 1e6
+    # roofline of the dominant entry point (largest measured time per launch).
+    # Attention: its algorithmic bytes take longer at the HBM peak than its
+    # flops at the bf16 tensor peak, so it is HBM-bound too.
+    key = {"tv_tree_build": "tree", "tv_attn_verify": "attn", "tv_accept_greedy": "greedy"}
+    dom = max(pk, key=lambda k: pk[k])
+    dom_gbs = nbytes[key[dom]] / (pk[dom] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": dom_gbs / hbm, "traffic": ncu_traffic(dom),
+                "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": nbytes[key[dom]],
+                "us_per_launch": pk[dom]}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -495,21 +567,20 @@ def main():
         "achieved_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "roofline_step_us": t_roof_us,
         "roofline_step_frac": t_roof_us / (ms_per_step * 1e3),
-        "roofline": {"bound": "hbm", "kernel": "tv_accept_greedy",
-                     "achieved": greedy_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": greedy_gbs / hbm, "traffic": None,
-                     "peak_source": f"{peak_src} hbm_gbs",
-                     "bytes_per_launch": nbytes["greedy"]},
+        "roofline": roofline,
         "kernels": {k: {"us_per_launch": v} for k, v in pk.items()},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
     line["kernels"]["tv_attn_verify"].update(
         {"algorithmic_bytes": nbytes["attn"], "flops": flops, "achieved_gbs": attn_gbs,
-         "achieved_tflops": flops / (a_us * 1e-6) / 1e12})
+         "achieved_tflops": flops / (a_us * 1e-6) / 1e12, "hbm_frac": attn_gbs / hbm,
+         "traffic": ncu_traffic("tv_attn_verify")})
     line["kernels"]["tv_accept_greedy"].update(
-        {"algorithmic_bytes": nbytes["greedy"], "achieved_gbs": greedy_gbs})
-    line["kernels"]["tv_tree_build"].update({"algorithmic_bytes": nbytes["tree"]})
+        {"algorithmic_bytes": nbytes["greedy"], "achieved_gbs": greedy_gbs,
+         "hbm_frac": greedy_gbs / hbm, "traffic": ncu_traffic("tv_accept_greedy")})
+    line["kernels"]["tv_tree_build"].update({"algorithmic_bytes": nbytes["tree"],
+                                             "traffic": ncu_traffic("tv_tree_build")})
     if r["e2e"] is not None:
         line["e2e"] = r["e2e"]
     if world == 1 and not args.no_cpu_baseline:

@@ -28,7 +28,8 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
     s_par[i] = p;
     bad |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
   }
-  for (int w = threadIdx.x; w < N * W; w += blockDim.x) s_anc[w] = 0ull;
+  if (W > 1)
+    for (int w = threadIdx.x; w < N * W; w += blockDim.x) s_anc[w] = 0ull;
   bad = __syncthreads_or(bad);
   if (bad) {
     for (int i = threadIdx.x; i < N; i += blockDim.x) dep[i] = -1;
@@ -36,17 +37,32 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
     if (threadIdx.x == 0) status[b] = TV_ERR_INVALID_TREE;
     return;
   }
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    int d = -1;
-    uint64_t* row = s_anc + i * W;
-    for (int x = i; x >= 0; x = s_par[x]) {
-      row[x >> 6] |= 1ull << (x & 63);
-      ++d;
+  if (W == 1) {
+    // up to 64 nodes: the mask of a node is one word, built in a register and
+    // stored straight to global memory
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+      int d = -1;
+      uint64_t m = 0ull;
+      for (int x = i; x >= 0; x = s_par[x]) {
+        m |= 1ull << x;
+        ++d;
+      }
+      dep[i] = d;
+      anc[i] = m;
     }
-    dep[i] = d;
+  } else {
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+      int d = -1;
+      uint64_t* row = s_anc + i * W;
+      for (int x = i; x >= 0; x = s_par[x]) {
+        row[x >> 6] |= 1ull << (x & 63);
+        ++d;
+      }
+      dep[i] = d;
+    }
+    __syncthreads();
+    for (int w = threadIdx.x; w < N * W; w += blockDim.x) anc[w] = s_anc[w];
   }
-  __syncthreads();
-  for (int w = threadIdx.x; w < N * W; w += blockDim.x) anc[w] = s_anc[w];
   if (threadIdx.x == 0) status[b] = TV_OK;
 }
 
