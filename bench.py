@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph-steps", type=int, default=200)
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the secondary measurements on the other configurations")
     p.add_argument("--ncu-steps", type=int, default=0,
                    help="profiling driver: run this many eager steps of the workload on "
                         "one input set (no graphs, no timing) and exit; for ncu captures")
@@ -205,6 +207,194 @@ def make_sets(case, torch, device, l2_bytes):
     M = max(2, int(np.ceil(3 * l2_bytes / set_bytes)))
     sets = [base] + [{k: t.clone() for k, t in base.items()} for _ in range(M - 1)]
     return sets, set_bytes
+
+
+# ----------------------------------------------------------------------------
+# the other configurations: every hot-path row measured on its own workload
+# ----------------------------------------------------------------------------
+def graph_time_us(torch, stream, fn, glen, reps):
+    """Average time of one fn() call: a CUDA graph of glen calls, replayed
+    reps times after one warm replay, CUDA events on the launching stream."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(glen):
+            fn()
+    with torch.cuda.stream(stream):
+        g.replay()
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        z.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(z) * 1e3 / (reps * glen)
+
+
+def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tflops, l2):
+    """One verify step of a configuration: tree -> attention -> acceptance,
+    inputs resident (one set; the step's bytes are stated against L2)."""
+    def bf16(u):
+        return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).to(device).view(
+            torch.bfloat16)
+
+    B, N, V = case.B, case.N, case.V
+    t = dict(parent=torch.from_numpy(case.parent).to(device),
+             tokens=torch.from_numpy(case.tokens).to(device),
+             kv_len=torch.from_numpy(case.kv_len).to(device),
+             q=bf16(case.q), k=bf16(case.k), v=bf16(case.v))
+    if accept == "greedy":
+        t["logits"] = torch.from_numpy(case.logits).to(device)
+    else:
+        t["p"] = torch.from_numpy(case.p_logits).to(device)
+        t["q_l"] = torch.from_numpy(case.q_logits).to(device)
+    W = (N + 63) // 64
+    depth = torch.empty((B, N), dtype=torch.int32, device=device)
+    anc = torch.empty((B, N, W), dtype=torch.int64, device=device)
+    tst = torch.empty(B, dtype=torch.int32, device=device)
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((B, N, case.Hq), dtype=torch.float32, device=device)
+    ast = torch.empty(B, dtype=torch.int32, device=device)
+    if accept == "greedy":
+        aouts = dict(argmax=torch.empty((B, N), dtype=torch.int32, device=device),
+                     accept_len=torch.empty(B, dtype=torch.int32, device=device),
+                     end_node=torch.empty(B, dtype=torch.int32, device=device),
+                     path=torch.empty((B, N), dtype=torch.int32, device=device),
+                     bonus=torch.empty(B, dtype=torch.int32, device=device),
+                     status=torch.empty(B, dtype=torch.int32, device=device))
+    else:
+        aouts = dict(accept_len=torch.empty(B, dtype=torch.int32, device=device),
+                     end_node=torch.empty(B, dtype=torch.int32, device=device),
+                     path=torch.empty((B, N), dtype=torch.int32, device=device),
+                     out_token=torch.empty(B, dtype=torch.int32, device=device),
+                     status=torch.empty(B, dtype=torch.int32, device=device))
+
+    def f_tree():
+        tv.tree_build(t["parent"], depth, anc, tst)
+
+    def f_attn():
+        tv.attn_verify(t["q"], t["k"], t["v"], t["kv_len"], anc, out=out, lse=lse, status=ast)
+
+    def f_acc():
+        if accept == "greedy":
+            tv.accept_greedy(t["logits"], t["tokens"], t["parent"], depth, outs=aouts)
+        else:
+            tv.accept_sample(t["p"], t["q_l"], t["tokens"], t["parent"], depth, 1.0, 1234, 0,
+                             outs=aouts)
+
+    def f_step():
+        f_tree()
+        f_attn()
+        f_acc()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            f_step()
+    torch.cuda.synchronize()
+    assert int(tst.max()) == 0 and int(ast.max()) == 0 and int(aouts["status"].max()) == 0
+    us = {k: graph_time_us(torch, stream, f, 20, 5)
+          for k, f in (("step", f_step), ("tv_tree_build", f_tree), ("tv_attn_verify", f_attn),
+                       ("tv_accept_" + accept, f_acc))}
+    nb = algorithmic_bytes(case)
+    acc_bytes = nb["greedy"] if accept == "greedy" else 8 * B * N * V + 12 * B * N
+    flops = attention_flops(case)
+    t_attn = max(nb["attn"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+    t_acc = acc_bytes / (hbm * 1e9) * 1e6
+    t_tree = nb["tree"] / (hbm * 1e9) * 1e6
+    resident = sum(x.numel() * x.element_size() for x in t.values())
+    return {
+        "workload": name, "us_per_step": us["step"],
+        "us_per_launch": {k: v for k, v in us.items() if k != "step"},
+        "roofline_step_us": t_attn + t_acc + t_tree,
+        "roofline_step_frac": (t_attn + t_acc + t_tree) / us["step"],
+        "attn": {"bound": "tensor" if flops / (tflops * 1e12) > nb["attn"] / (hbm * 1e9)
+                 else "hbm", "bytes": nb["attn"], "flops": flops, "roofline_us": t_attn,
+                 "frac": t_attn / us["tv_attn_verify"]},
+        "accept": {"bound": "hbm", "bytes": acc_bytes, "roofline_us": t_acc,
+                   "frac": t_acc / us["tv_accept_" + accept]},
+        "inputs_resident_mb": resident / 1e6,
+        "l2": f"inputs resident, {resident / 1e6:.0f} MB against the {l2 / 1e6:.0f} MB L2",
+    }
+
+
+def measure_talon_expansion(torch, tv, device, stream, hbm):
+    """TALON workload (context 0): grow the tree once with the host drafter,
+    recording each layer's draft rows, then time the whole device expansion
+    (every layer's tv_expand_gated, from the root) replayed in one graph."""
+    from workloads import gen
+    K, alpha, budget = 10, 0.3, 512
+    drafter = gen.config3_drafter(0)
+    rec = []
+
+    def rows_of(keys):
+        r = drafter.rows(keys)
+        rec.append(r)
+        return r
+
+    tree = tv.expand_tree(rows_of, drafter.root_key(), drafter.child_key, K, alpha, budget,
+                          device)
+    V = drafter.V
+    dev_rows = [torch.from_numpy(r).to(device) for r in rec]
+    F = [r.shape[0] for r in rec]
+    par = torch.full((budget,), -1, dtype=torch.int32, device=device)
+    tok = torch.zeros(budget, dtype=torch.int32, device=device)
+    ls = torch.zeros(budget, dtype=torch.float32, device=device)
+    ids = torch.arange(budget, dtype=torch.int32, device=device)
+    n_dev = torch.ones(1, dtype=torch.int32, device=device)
+    tv.workspace("expand", tv.expand_workspace_size(max(F), V), device)
+    lo = [0]
+    for f in F[:-1]:
+        lo.append(lo[-1] + f)
+
+    def f_expand():
+        n_dev.fill_(1)
+        for layer, (rows, l0, f) in enumerate(zip(dev_rows, lo, F), start=1):
+            tv.expand_gated(rows, ids[l0:l0 + f], ls[l0:l0 + f], layer, K, alpha, budget, par,
+                            tok, ls, n_dev)
+
+    with torch.cuda.stream(stream):
+        f_expand()
+    torch.cuda.synchronize()
+    assert int(n_dev.item()) == tree["n"]
+    assert torch.equal(par[:tree["n"]].cpu(), tree["parent"])
+    us = graph_time_us(torch, stream, f_expand, 5, 5)
+    nbytes = sum(2 * 4 * f * V for f in F)
+    return tree, {
+        "workload": f"TALON context 0: K {K}, alpha {alpha}, budget {budget}, vocab {V}; "
+                    f"{len(F)} layers, {tree['n']} nodes",
+        "us_per_expansion": us, "layers": len(F), "frontier_rows": int(sum(F)),
+        "bytes": nbytes, "roofline_us": nbytes / (hbm * 1e9) * 1e6,
+        "frac": nbytes / (hbm * 1e9) * 1e6 / us,
+    }
+
+
+def measure_other_configs(torch, tv, device, hbm, tflops):
+    """Long context (greedy), batched stochastic acceptance, TALON expansion
+    and its 512-node verify."""
+    from workloads import gen
+    stream = torch.cuda.Stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    res = {}
+    case = gen.config5(256)
+    res["long_context"] = measure_verify_config(
+        "long context: prefix 32768, 32/8 heads, head_dim 128, 256-node OPT-Tree-style tree, "
+        "vocab 128256, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2)
+    del case
+    case = gen.config4()
+    res["batched_stochastic"] = measure_verify_config(
+        "batched stochastic: 16 sequences, prefixes in [512, 8192], 64-node trees, 32/8 heads, "
+        "head_dim 128, vocab 128256, p/q acceptance at T = 1", case, "sample", torch, tv, device,
+        stream, hbm, tflops, l2)
+    del case
+    tree, res["talon_expansion"] = measure_talon_expansion(torch, tv, device, stream, hbm)
+    case = gen.config3_verify(tree["parent"].numpy().astype(np.int32), 0,
+                              tokens=tree["token"].numpy().astype(np.int32))
+    res["talon_verify"] = measure_verify_config(
+        f"TALON verify: prefix 4096, 64/8 heads, head_dim 128, the {case.N}-node expanded tree, "
+        "vocab 32000, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2)
+    torch.cuda.synchronize()
+    return res
 
 
 # ----------------------------------------------------------------------------
@@ -583,6 +773,11 @@ def main():
                                              "traffic": ncu_traffic("tv_tree_build")})
     if r["e2e"] is not None:
         line["e2e"] = r["e2e"]
+    if world == 1 and not args.no_configs:
+        import torch
+        import speculative_decoding_tree_tv_gb300 as tv
+        line["other_configs"] = measure_other_configs(
+            torch, tv, torch.device("cuda", local_rank), hbm, tflops)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case)
     print(json.dumps(line), flush=True)
