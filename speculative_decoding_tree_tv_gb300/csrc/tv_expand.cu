@@ -11,9 +11,11 @@
 //               a per-row fp32 logit threshold equivalent to the fp64 gate;
 //               resets the candidate counter;
 //   3. filter:  streams the rows again and appends every (row, token) that
-//               passes the gate to a candidate list;
-//   4. select:  one CTA keeps the best `limit` candidates (radix select on
-//               order-preserving fp64 score keys, ties to the lower
+//               passes the gate to a candidate list, with its order-preserving
+//               fp64 score key beside it;
+//   4. select:  one CTA keeps the best `limit` candidates (radix select on the
+//               score keys, starting at the first byte in which the keys
+//               differ, one histogram per warp; ties to the lower
 //               (parent, token)), orders them (parent asc, score desc, token
 //               asc) and appends them to the tree.
 // Scores are fp64 in the log domain; logits stay fp32.
@@ -25,10 +27,11 @@ namespace tv {
 namespace {
 
 constexpr int kExpThreads = 256;
-constexpr int kExpChunk = 8192;
+constexpr int kExpChunk = 2048;
 constexpr int kSelThreads = 1024;
 constexpr int kMaxBudget = 2048;
 constexpr int kTieCap = 1024;
+constexpr int kSelBatch = 8;  // key loads in flight per thread in the select passes
 
 struct ExpPartial {
   double s;
@@ -52,10 +55,11 @@ struct ExpWs {
   ExpRow* rows;
   ExpPartial* part;
   unsigned long long* list;  // (row << 32) | token
+  unsigned long long* keys;  // order-preserving fp64 score key of list[i]
 };
 
 __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, size_t* part_off,
-                                              size_t* list_off) {
+                                              size_t* list_off, size_t* keys_off) {
   const int chunks = (V + kExpChunk - 1) / kExpChunk;
   size_t o = align_up(sizeof(ExpCtl), 256);
   *rows_off = o;
@@ -63,6 +67,8 @@ __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, si
   *part_off = o;
   o += align_up((size_t)F * chunks * sizeof(ExpPartial), 256);
   *list_off = o;
+  o += align_up((size_t)F * V * sizeof(unsigned long long), 256);
+  *keys_off = o;
   o += align_up((size_t)F * V * sizeof(unsigned long long), 256);
   return o;
 }
@@ -145,8 +151,10 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
     const ExpPartial* p = ws.part + (size_t)v * chunks;
     float m = -INFINITY;
     for (int c = 0; c < chunks; ++c) m = fmaxf(m, p[c].m);
+    // chunk scale factors on the SFU (fp32, within a few ulp; fp64 runs at a
+    // small fraction of the fp32 rate here), the sum itself in fp64
     double s = 0.0;
-    for (int c = 0; c < chunks; ++c) s += p[c].s * exp((double)p[c].m - (double)m);
+    for (int c = 0; c < chunks; ++c) s += p[c].s * (double)expf(p[c].m - m);
     const double off = (double)frontier_logscore[v] - ((double)m + log(s));
     ws.rows[v].off = off;
     s_m_row[v] = (double)m;
@@ -184,6 +192,7 @@ exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
   pdl_wait();
   const int row = blockIdx.y;
   const float thr = ws.rows[row].thr;
+  const double off = ws.rows[row].off;
   if (!(thr < INFINITY)) return;
   const float* x = logits + (size_t)row * V;
   const int start = blockIdx.x * kExpChunk;
@@ -191,7 +200,8 @@ exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
   const int lane = threadIdx.x & 31;
   for (int base = start; base < stop; base += kExpThreads) {
     const int e = base + threadIdx.x;
-    const bool pass = (e < stop) && (__ldg(x + e) >= thr);
+    const float lg = (e < stop) ? __ldg(x + e) : -INFINITY;
+    const bool pass = (e < stop) && (lg >= thr);
     const unsigned int bal = __ballot_sync(0xffffffffu, pass);
     if (bal == 0u) continue;
     int slot0 = 0;
@@ -200,6 +210,7 @@ exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
     if (pass) {
       const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
       ws.list[slot] = ((unsigned long long)row << 32) | (unsigned int)e;
+      ws.keys[slot] = double_key(off + (double)lg);
     }
   }
 }
@@ -257,58 +268,121 @@ __device__ void bitonic_sort_u64(unsigned long long* s, int n_pow2) {
   }
 }
 
-__device__ __forceinline__ unsigned long long cand_key(const float* __restrict__ logits, int V,
-                                                       const ExpRow* rows, unsigned long long c) {
-  const int row = (int)(c >> 32), tok = (int)(c & 0xffffffffu);
-  return double_key(rows[row].off + (double)__ldg(logits + (size_t)row * V + tok));
-}
-
 __global__ void __launch_bounds__(kSelThreads)
 exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __restrict__ frontier_node,
                   int32_t* __restrict__ tree_parent, int32_t* __restrict__ tree_token,
                   float* __restrict__ tree_logscore, int32_t* __restrict__ n_nodes, ExpWs ws) {
-  __shared__ Kept s_kept[kMaxBudget];
+  // the per-warp histograms of the radix passes and the kept list are never
+  // live at the same time: they share one buffer
+  static_assert((kSelThreads / 32) * 256 * sizeof(unsigned int) <= kMaxBudget * sizeof(Kept), "");
+  __shared__ __align__(16) unsigned char s_buf[kMaxBudget * sizeof(Kept)];
+  Kept* s_kept = reinterpret_cast<Kept*>(s_buf);
+  auto s_hist = reinterpret_cast<unsigned int (*)[256]>(s_buf);  // [warp][digit]
   __shared__ unsigned long long s_ties[kTieCap];
-  __shared__ unsigned int s_hist[256];
   __shared__ int s_n, s_nt, s_digit, s_need;
-  __shared__ unsigned long long s_min;
+  __shared__ unsigned long long s_min, s_kmin, s_kmax;
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x;
   const ExpCtl ctl = *ws.ctl;
   const int count = ctl.count, limit = ctl.limit;
+  const int lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_n = 0;
     s_nt = 0;
+    s_kmin = ~0ull;
+    s_kmax = 0ull;
   }
   __syncthreads();
   if (count <= limit) {
     for (int j = tid; j < count; j += kSelThreads) {
       const unsigned long long c = ws.list[j];
-      s_kept[j] = Kept{cand_key(logits, V, ws.rows, c), (int)(c >> 32), (int)(c & 0xffffffffu)};
+      s_kept[j] = Kept{ws.keys[j], (int)(c >> 32), (int)(c & 0xffffffffu)};
     }
     if (tid == 0) s_n = count;
   } else {
-    // radix select: T = the limit-th largest key, need = how many keys == T to take
-    unsigned long long prefix = 0ull, mask = 0ull;
+    // radix select: T = the limit-th largest key, need = how many keys == T to
+    // take.  The bytes above the highest one in which the smallest and the
+    // largest key differ are common to all keys and skipped.
+    unsigned long long kmin = ~0ull, kmax = 0ull;
+    for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
+      unsigned long long kb[kSelBatch];
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int j = j0 + u * kSelThreads;
+        kb[u] = (j < count) ? ws.keys[j] : ws.keys[0];
+      }
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        kmin = min(kmin, kb[u]);
+        kmax = max(kmax, kb[u]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) {
+      atomicMin(&s_kmin, kmin);
+      atomicMax(&s_kmax, kmax);
+    }
+    __syncthreads();
+    const unsigned long long diff = s_kmin ^ s_kmax;
+    const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
+    unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
+    unsigned long long prefix = s_kmax & mask;
     int need = limit;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kSelThreads) s_hist[i] = 0u;
+    for (int shift = top; shift >= 0; shift -= 8) {
+      for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&s_hist[0][0])[i] = 0u;
       __syncthreads();
-      for (int j = tid; j < count; j += kSelThreads) {
-        const unsigned long long k = cand_key(logits, V, ws.rows, ws.list[j]);
-        if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255ull], 1u);
+      for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
+        unsigned long long kb[kSelBatch];
+#pragma unroll
+        for (int u = 0; u < kSelBatch; ++u) {
+          const int j = j0 + u * kSelThreads;
+          kb[u] = (j < count) ? ws.keys[j] : ~prefix;  // ~prefix never matches the prefix
+        }
+#pragma unroll
+        for (int u = 0; u < kSelBatch; ++u)
+          if ((kb[u] & mask) == prefix && (j0 + u * kSelThreads) < count)
+            atomicAdd(&s_hist[warp][(kb[u] >> shift) & 255ull], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        int cum = 0;
-        for (int d = 255; d >= 0; --d) {
-          if (cum + (int)s_hist[d] >= need) {
-            s_digit = d;
-            s_need = need - cum;
-            break;
+      if (tid < 256) {
+        unsigned int t = 0u;
+#pragma unroll 8
+        for (int w = 0; w < kSelThreads / 32; ++w) t += s_hist[w][tid];
+        s_hist[0][tid] = t;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // digits from the top: lane l sums digits 255 - 8l .. 248 - 8l, an
+        // exclusive scan over lanes gives the count above each lane's digits
+        int cnt[8], lsum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          cnt[i] = (int)s_hist[0][255 - 8 * lane - i];
+          lsum += cnt[i];
+        }
+        int incl = lsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int above = incl - lsum;
+        if (above < need && incl >= need) {
+          int cum = above;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (cum + cnt[i] >= need) {
+              s_digit = 255 - 8 * lane - i;
+              s_need = need - cum;
+              break;
+            }
+            cum += cnt[i];
           }
-          cum += (int)s_hist[d];
         }
       }
       __syncthreads();
@@ -320,7 +394,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     const unsigned long long T = prefix;
     for (int j = tid; j < count; j += kSelThreads) {
       const unsigned long long c = ws.list[j];
-      const unsigned long long k = cand_key(logits, V, ws.rows, c);
+      const unsigned long long k = ws.keys[j];
       if (k > T) {
         const int slot = atomicAdd(&s_n, 1);
         s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
@@ -350,7 +424,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
         unsigned long long mine = ~0ull;
         for (int j = tid; j < count; j += kSelThreads) {
           const unsigned long long c = ws.list[j];
-          if ((first || c > last) && c < mine && cand_key(logits, V, ws.rows, c) == T) mine = c;
+          if ((first || c > last) && c < mine && ws.keys[j] == T) mine = c;
         }
         atomicMin(&s_min, mine);
         __syncthreads();
@@ -384,8 +458,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
 
 extern "C" size_t tv_expand_workspace_size(int F, int V) {
   if (F <= 0 || V <= 0) return 256;
-  size_t a, b, c;
-  return tv::exp_offsets(F, V, &a, &b, &c);
+  size_t a, b, c, d;
+  return tv::exp_offsets(F, V, &a, &b, &c, &d);
 }
 
 extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* frontier_node,
@@ -404,14 +478,15 @@ extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* f
   if ((size_t)F * V >= (1ull << 31)) return TV_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < tv_expand_workspace_size(F, V)) return TV_ERR_WORKSPACE;
   if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(draft_logits) & 15)) return TV_ERR_INVALID_ARG;
-  size_t rows_off, part_off, list_off;
-  tv::exp_offsets(F, V, &rows_off, &part_off, &list_off);
+  size_t rows_off, part_off, list_off, keys_off;
+  tv::exp_offsets(F, V, &rows_off, &part_off, &list_off, &keys_off);
   char* base = static_cast<char*>(workspace);
   tv::ExpWs ws;
   ws.ctl = reinterpret_cast<tv::ExpCtl*>(base);
   ws.rows = reinterpret_cast<tv::ExpRow*>(base + rows_off);
   ws.part = reinterpret_cast<tv::ExpPartial*>(base + part_off);
   ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
+  ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
   const int chunks = tv::ceil_div(V, tv::kExpChunk);
   dim3 grid(chunks, F);
   if (tv::launch_pdl(tv::exp_stats_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
