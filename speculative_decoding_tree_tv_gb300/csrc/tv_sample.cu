@@ -6,20 +6,24 @@
 // Two launches on the caller's stream:
 //   1. row_stats_kernel streams every p and q row once (8192 logits per CTA)
 //      and leaves per-chunk (max, sum exp) partials in the workspace;
-//   2. walk_kernel, one 1024-thread CTA per sequence, combines the partials of
-//      the rows it visits into fp64 normalisers and walks the tree.  A
-//      rejection triggers one pass over the node's row to normalise the next
-//      residual; the final draw is an inverse-CDF search over the residual.
+//   2. walk_kernel, one cluster of 8 CTAs per sequence, combines the partials
+//      of the rows it visits into fp64 normalisers and walks the tree.  A
+//      rejection triggers one pass over the node's row (each CTA an eighth
+//      of it) to normalise the next residual; the final draw is an
+//      inverse-CDF search over the residual across the cluster.
 // Element values are fp32 (expf); every sum is carried in fp64 and every
 // decision (accept test, draw) is taken in fp64.
 #include "tv_common.cuh"
+#include "tv_sm100.cuh"
 
 namespace tv {
 namespace {
 
 constexpr int kStatThreads = 256;
 constexpr int kStatChunk = 8192;
-constexpr int kWalkThreads = 1024;
+constexpr int kWalkThreads = 512;
+constexpr int kWalkCluster = 8;  // CTAs per tree in the walk
+constexpr int kWalkTile = 32;    // tokens a walk thread holds per round
 constexpr int kMaxRejects = kMaxNodes;
 
 struct RowPartial {
@@ -90,7 +94,8 @@ row_stats_kernel(const float* __restrict__ p_logits, const float* __restrict__ q
   }
 }
 
-// Block-wide fp64 sum over kWalkThreads threads.
+// Block-wide fp64 sum over kWalkThreads threads (fixed order); every thread
+// gets the result.
 __device__ double block_sum_d(double v, double* scratch) {
   v = warp_sum_d(v);
   const int tid = threadIdx.x;
@@ -98,7 +103,7 @@ __device__ double block_sum_d(double v, double* scratch) {
   if ((tid & 31) == 0) scratch[tid >> 5] = v;
   __syncthreads();
   if (tid < 32) {
-    double w = scratch[tid];
+    double w = (tid < kWalkThreads / 32) ? scratch[tid] : 0.0;
     w = warp_sum_d(w);
     if (tid == 0) scratch[32] = w;
   }
@@ -112,18 +117,73 @@ struct RowNorm {
   double s;      // sum exp(a - m)
 };
 
+// Chunk partials -> row normaliser.  The chunk scale factors are fp32
+// exponentials (a few ulp; fp64 runs at a small fraction of the fp32 rate),
+// the sum is fp64.
 __device__ RowNorm combine_partials(const RowPartial* p, int chunks) {
   RowNorm r;
   float m = -INFINITY;
   for (int c = 0; c < chunks; ++c) m = fmaxf(m, p[c].m);
   double s = 0.0;
-  for (int c = 0; c < chunks; ++c) s += p[c].s * exp((double)p[c].m - (double)m);
+  for (int c = 0; c < chunks; ++c) s += p[c].s * (double)expf(p[c].m - m);
   r.m = m;
   r.s = s;
   r.inv_s = (float)(1.0 / s);
   return r;
 }
 
+// The residual chain of one token: r = p, then r <- (r - q)+ / Z_j for each
+// rejection so far (Z_j its normaliser).
+__device__ __forceinline__ float residual(float a, float bq, float inv_t, const RowNorm& pn,
+                                          const RowNorm& qn, int n_rej, const float* invz,
+                                          float* q_out) {
+  float r = expf(a * inv_t - pn.m) * pn.inv_s;
+  const float q = expf(bq * inv_t - qn.m) * qn.inv_s;
+  for (int j = 0; j < n_rej; ++j) r = fmaxf(r - q, 0.0f) * invz[j];
+  *q_out = q;
+  return r;
+}
+
+// Calls fn(token, p_logit, q_logit) for the tokens [t0, t1) in order, loading
+// up to kWalkTile of them at a time (all loads of a round in flight; 16-byte
+// loads when the rows are 16-byte aligned and t0 is a multiple of 4).
+template <class Fn>
+__device__ __forceinline__ void for_tokens(const float* prow, const float* qrow, int t0, int t1,
+                                           bool vec, Fn&& fn) {
+  for (int base = t0; base < t1; base += kWalkTile) {
+    float pa[kWalkTile], qa[kWalkTile];
+    if (vec) {
+#pragma unroll
+      for (int u = 0; u < kWalkTile / 4; ++u) {
+        const int e = base + 4 * u;
+        const float4 x = (e < t1) ? ld_stream_f4(reinterpret_cast<const float4*>(prow + e))
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const float4 y = (e < t1) ? ld_stream_f4(reinterpret_cast<const float4*>(qrow + e))
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        pa[4 * u] = x.x; pa[4 * u + 1] = x.y; pa[4 * u + 2] = x.z; pa[4 * u + 3] = x.w;
+        qa[4 * u] = y.x; qa[4 * u + 1] = y.y; qa[4 * u + 2] = y.z; qa[4 * u + 3] = y.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kWalkTile; ++u) {
+        const int e = base + u;
+        pa[u] = (e < t1) ? __ldg(prow + e) : 0.0f;
+        qa[u] = (e < t1) ? __ldg(qrow + e) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kWalkTile; ++u)
+      if (base + u < t1) fn(base + u, pa[u], qa[u]);
+  }
+}
+
+// One tree per thread-block cluster of kWalkCluster CTAs.  CTA `rank` owns
+// the vocabulary slice [rank * S, (rank + 1) * S) and, inside it, thread t a
+// contiguous run of P tokens, so (rank, thread) order is token order.  Every
+// CTA takes the same decisions from the same inputs (the accept tests in
+// fp64 by its thread 0, the normalisers from cluster-wide sums added in rank
+// order), so all of them follow the same walk; sums over the row are
+// exchanged through distributed shared memory, one cluster barrier each.
 __global__ void __launch_bounds__(kWalkThreads)
 walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logits,
             const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
@@ -134,15 +194,37 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
             int32_t* __restrict__ status) {
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x;
+  const int rank = (int)sm100::cluster_ctarank();
+  const int b = blockIdx.x / kWalkCluster;
   const int tid = threadIdx.x;
-  const int rows = gridDim.x * N;
+  const int rows = (gridDim.x / kWalkCluster) * N;
   __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes];
   __shared__ float s_invz[kMaxRejects];
   __shared__ double s_red[33];
   __shared__ RowNorm s_pn, s_qn;
   __shared__ int s_found, s_last_pos;
   __shared__ double s_scan[kWalkThreads / 32];
+  // what this CTA shows the cluster: two phases, so that writing the next
+  // value never races with another CTA still reading the previous one
+  __shared__ double s_pub_d[2];
+  __shared__ int s_pub_i[2];
+  __shared__ double s_all_d[kWalkCluster];
+  __shared__ int s_all_i[kWalkCluster];
+  int phase = 0;
+  // publish (d, i), wait for the cluster, read everyone's in rank order
+  auto exchange = [&](double d, int i) {
+    if (tid == 0) {
+      s_pub_d[phase] = d;
+      s_pub_i[phase] = i;
+    }
+    sm100::cluster_sync();
+    if (tid < kWalkCluster) {
+      s_all_d[tid] = sm100::dsmem_ld_f64(sm100::dsmem_map(sm100::smem_u32(&s_pub_d[phase]), tid));
+      s_all_i[tid] = sm100::dsmem_ld_s32(sm100::dsmem_map(sm100::smem_u32(&s_pub_i[phase]), tid));
+    }
+    __syncthreads();
+    phase ^= 1;
+  };
 
   const int32_t* par = parent + (size_t)b * N;
   const int32_t* tok = tokens + (size_t)b * N;
@@ -161,19 +243,22 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
   bad_tree = __syncthreads_or(bad_tree);
   bad_tok = __syncthreads_or(bad_tok);
   int32_t* pth = path + (size_t)b * N;
-  if (bad_tree || bad_tok) {
-    for (int i = tid; i < N; i += kWalkThreads) pth[i] = -1;
-    if (tid == 0) {
-      accept_len[b] = end_node[b] = out_token[b] = -1;
-      status[b] = bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
+  if (bad_tree || bad_tok) {  // the same in every CTA of the cluster: all leave here
+    if (rank == 0) {
+      for (int i = tid; i < N; i += kWalkThreads) pth[i] = -1;
+      if (tid == 0) {
+        accept_len[b] = end_node[b] = out_token[b] = -1;
+        status[b] = bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
+      }
     }
     return;
   }
 
-  // contiguous slice of the vocabulary per thread, so that thread order is
-  // token order for the inverse-CDF search
-  const int per = ceil_div(V, kWalkThreads);
-  const int t0 = min(V, tid * per), t1 = min(V, t0 + per);
+  const bool vec = (V & 3) == 0;
+  const int S = ((ceil_div(V, kWalkCluster) + 3) / 4) * 4;
+  const int P = ((ceil_div(S, kWalkThreads) + 3) / 4) * 4;
+  const int s_lo = min(V, rank * S), s_hi = min(V, s_lo + S);
+  const int t0 = min(s_hi, s_lo + tid * P), t1 = min(s_hi, t0 + P);
 
   int node = 0;
   int result = -1;
@@ -186,7 +271,7 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     }
     __syncthreads();
     const RowNorm pn = s_pn, qn = s_qn;
-    int n_rej = 0;      // residual normalisations applied so far
+    int n_rej = 0;  // residual normalisations applied so far
     int accepted = -1;
     int ordinal = 0;
     for (int c = node + 1; c < N; ++c) {
@@ -207,15 +292,17 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
         accepted = c;
         break;
       }
-      // rejection: Z = sum_t (r(t) - q(t))+ over the row
+      // rejection: Z = sum_t (r(t) - q(t))+ over the row, from every CTA's slice
       KahanF acc;
-      for (int t = t0; t < t1; ++t) {
-        float r = expf(__ldg(prow + t) * inv_t - pn.m) * pn.inv_s;
-        const float q = expf(__ldg(qrow + t) * inv_t - qn.m) * qn.inv_s;
-        for (int j = 0; j < n_rej; ++j) r = fmaxf(r - q, 0.0f) * s_invz[j];
+      for_tokens(prow, qrow, t0, t1, vec, [&](int, float a, float bq) {
+        float q;
+        const float r = residual(a, bq, inv_t, pn, qn, n_rej, s_invz, &q);
         acc.add(fmaxf(r - q, 0.0f));
-      }
-      const double z = block_sum_d((double)acc.s, s_red);
+      });
+      const double zc = block_sum_d((double)acc.s, s_red);
+      exchange(zc, 0);
+      double z = 0.0;
+      for (int r = 0; r < kWalkCluster; ++r) z += s_all_d[r];
       if (z > 0.0 && n_rej < kMaxRejects) {
         if (tid == 0) s_invz[n_rej] = (float)(1.0 / z);
         ++n_rej;
@@ -230,15 +317,14 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     // final draw from the current residual (p_node itself when nothing was rejected)
     KahanF acc;
     int last_pos = -1;
-    for (int t = t0; t < t1; ++t) {
-      float r = expf(__ldg(prow + t) * inv_t - pn.m) * pn.inv_s;
-      const float q = expf(__ldg(qrow + t) * inv_t - qn.m) * qn.inv_s;
-      for (int j = 0; j < n_rej; ++j) r = fmaxf(r - q, 0.0f) * s_invz[j];
+    for_tokens(prow, qrow, t0, t1, vec, [&](int t, float a, float bq) {
+      float q;
+      const float r = residual(a, bq, inv_t, pn, qn, n_rej, s_invz, &q);
       acc.add(r);
       if (r > 0.0f) last_pos = t;
-    }
-    // exclusive scan of per-thread masses (fp64)
-    double mass = (double)acc.s;
+    });
+    // exclusive scan of per-thread masses (fp64) inside the CTA
+    const double mass = (double)acc.s;
     double incl = mass;
     const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
@@ -253,44 +339,57 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     }
     __syncthreads();
     if (warp == 0) {
-      double w = s_scan[lane];
+      double w = (lane < kWalkThreads / 32) ? s_scan[lane] : 0.0;
       double wi = w;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const double y = __shfl_up_sync(0xffffffffu, wi, o);
         if (lane >= o) wi += y;
       }
-      s_scan[lane] = wi - w;  // exclusive prefix of warp totals
-      if (lane == 31) s_red[32] = wi;
+      if (lane < kWalkThreads / 32) s_scan[lane] = wi - w;  // exclusive prefix of warp totals
+      if (lane == kWalkThreads / 32 - 1) s_red[32] = wi;    // this CTA's mass
     }
-    __syncthreads();
-    const double total = s_red[32];
-    const double before = s_scan[warp] + (incl - mass);
     atomicMax(&s_last_pos, last_pos);
+    __syncthreads();
+    // the cluster's masses and last positive tokens, in rank order
+    exchange(s_red[32], s_last_pos);
+    double before_cta = 0.0, total = 0.0;
+    int last_all = -1;
+    for (int r = 0; r < kWalkCluster; ++r) {
+      if (r < rank) before_cta += s_all_d[r];
+      total += s_all_d[r];
+      last_all = max(last_all, s_all_i[r]);
+    }
     const double u = decision_uniform(seed, offset, b, node, 1u, 0u);
     const double target = u * total;
+    const double before = before_cta + s_scan[warp] + (incl - mass);
     if (mass > 0.0 && before + mass > target && before <= target) {
       // This slice holds the boundary (the lowest such slice wins if rounding
       // makes several).  Replaying the slice's compensated sum in the same
       // order ends exactly at `mass`, so the search always finds a token.
       KahanF run;
       int pick = -1;
-      for (int t = t0; t < t1; ++t) {
-        float r = expf(__ldg(prow + t) * inv_t - pn.m) * pn.inv_s;
-        const float q = expf(__ldg(qrow + t) * inv_t - qn.m) * qn.inv_s;
-        for (int j = 0; j < n_rej; ++j) r = fmaxf(r - q, 0.0f) * s_invz[j];
+      for_tokens(prow, qrow, t0, t1, vec, [&](int t, float a, float bq) {
+        if (pick >= 0) return;
+        float q;
+        const float r = residual(a, bq, inv_t, pn, qn, n_rej, s_invz, &q);
         run.add(r);
-        if (before + (double)run.s > target) {
-          pick = t;
-          break;
-        }
-      }
+        if (before + (double)run.s > target) pick = t;
+      });
       if (pick >= 0) atomicMin(reinterpret_cast<unsigned int*>(&s_found), (unsigned int)pick);
     }
     __syncthreads();
-    result = (s_found >= 0) ? s_found : s_last_pos;
+    // the lowest pick of the cluster, else the last token with positive mass
+    exchange(0.0, s_found);
+    int pick = -1;
+    for (int r = 0; r < kWalkCluster; ++r)
+      if (s_all_i[r] >= 0 && (pick < 0 || s_all_i[r] < pick)) pick = s_all_i[r];
+    result = (pick >= 0) ? pick : last_all;
     break;
   }
+  // no CTA may leave while another still reads its shared memory
+  sm100::cluster_sync();
+  if (rank != 0) return;
   const int end_depth = s_dep[node];
   for (int i = tid; i < N; i += kWalkThreads)
     if (i > end_depth) pth[i] = -1;
@@ -301,6 +400,27 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     out_token[b] = result;
     status[b] = TV_OK;
   }
+}
+
+// The walk kernel as clusters of kWalkCluster CTAs, with programmatic
+// dependent launch.
+template <typename... Args>
+cudaError_t launch_walk(dim3 grid, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kWalkThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kWalkCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, walk_kernel, args...);
 }
 
 }  // namespace
@@ -335,10 +455,9 @@ extern "C" tv_status tv_accept_sample(const float* p_logits, const float* q_logi
   dim3 g1(chunks * B * N, 2);
   if (tv::launch_pdl(tv::row_stats_kernel, g1, dim3(tv::kStatThreads), 0, stream, p_logits,
                      q_logits, B * N, V, chunks, inv_t, part) != cudaSuccess ||
-      tv::launch_pdl(tv::walk_kernel, dim3(B), dim3(tv::kWalkThreads), 0, stream, p_logits,
-                     q_logits, tokens, parent, depth, N, V, chunks, inv_t, seed, offset,
-                     (const tv::RowPartial*)part, accept_len, end_node, path, out_token,
-                     status) != cudaSuccess) {
+      tv::launch_walk(dim3(B * tv::kWalkCluster), stream, p_logits, q_logits, tokens, parent,
+                      depth, N, V, chunks, inv_t, seed, offset, (const tv::RowPartial*)part,
+                      accept_len, end_node, path, out_token, status) != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;
   }
