@@ -219,7 +219,11 @@ tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t* tokens,
  *   temperature > 0.
  *   accept_len, end_node, out_token int32 [B] out; path int32 [B, N] out;
  *   status int32 [B] out (as tv_accept_greedy).
- *   workspace >= tv_accept_sample_workspace_size(B, N, V) bytes (any content).
+ *   workspace unused: tv_accept_sample_workspace_size() returns 0 and
+ *             workspace may be NULL (each sequence's walk keeps its state in
+ *             the shared memory of one thread-block cluster).
+ * Supported: V <= 409,600 (a cluster's shared memory holds the visited row
+ * pair); larger vocabularies return TV_ERR_UNSUPPORTED.
  */
 size_t tv_accept_sample_workspace_size(int B, int N, int V);
 tv_status tv_accept_sample(const float* p_logits, const float* q_logits,

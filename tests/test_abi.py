@@ -45,9 +45,9 @@ def test_status_strings_and_version(tvlib):
     assert tvlib.version() >= 100
 
 
-def test_workspace_sizes_are_positive(tvlib):
+def test_workspace_sizes(tvlib):
     assert tvlib.greedy_workspace_size(1, 60, 128256) >= 60 * 8
-    assert tvlib.sample_workspace_size(16, 64, 128256) >= 2 * 16 * 64 * 16
+    assert tvlib.sample_workspace_size(16, 64, 128256) == 0  # the walk keeps its state on chip
     assert tvlib.expand_workspace_size(511, 32000) >= 511 * 32000 * 8
     # a 2108-slot cache over 16 row tiles is split across CTAs: partials + stats
     ws = tvlib.attn_workspace_size(1, 60, 32, 8, 128, 2108)
