@@ -40,15 +40,37 @@ namespace {
 using namespace sm100;
 
 constexpr int kRB = 128;              // rows per row block = TMEM lanes
-constexpr int kRows = 2 * kRB;        // rows per CTA
 constexpr int kBN = 128;              // keys per tile
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale max while within 2^8
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
 constexpr int kMaxSplit = 64;         // splits of one CTA's key range
-constexpr uint32_t kTmemCols = 512;   // S_0, S_1 at 0, 128; O_0, O_1 at 256, 384
+
+// Shape of a CTA: RBS row blocks of 128 query rows (one or two), 128 softmax
+// threads per row block, then the K producer, MMA and V producer warps (the
+// two loads wait on different barriers, so each has a warp of its own).  Two row
+// blocks share every K/V tile (the cache is streamed once per kv head); one
+// row block gives twice the CTAs.  Both fill 224 KB of shared memory (D = 128):
+//   two row blocks: Q 64 KB, one P buffer 64 KB, one K stage, two V stages;
+//   one row block:  Q 32 KB, two P buffers, two K stages, two V stages.
+// The second V stage takes the V load off the PV critical path; the second P
+// buffer lets the softmax of tile t + 1 run while PV(t) still reads P(t).
+// One row block also double-buffers S in TMEM, so that S(t + 1) is computed
+// while the softmax of tile t still reads S(t).
+// TMEM: S of (row block r, buffer u) at column 128 (r kSBufs + u), O_r at
+// 128 RBS kSBufs + 128 r; 512 columns either way.
+template <int RBS>
+struct Shape {
+  static constexpr int kRows = RBS * kRB;
+  static constexpr int kThreads = RBS * kRB + 96;
+  static constexpr int kProducerWarp = RBS * 4;  // K loads
+  static constexpr int kMmaWarp = RBS * 4 + 1;
+  static constexpr int kVProducerWarp = RBS * 4 + 2;
+  static constexpr int kKStages = (RBS == 1) ? 2 : 1;
+  static constexpr int kVStages = 2;
+  static constexpr int kPBufs = (RBS == 1) ? 2 : 1;
+  static constexpr int kSBufs = (RBS == 1) ? 2 : 1;
+  static constexpr uint32_t kTmemCols = 512u;
+};
 
 struct AttnParams {
   uint16_t* out;
@@ -56,23 +78,24 @@ struct AttnParams {
   int32_t* status;
   const int32_t* kv_len;
   const uint64_t* anc;
-  __half* part;     // split partials [unit][nsplit][D / 8][256 rows] 16-byte chunks of 8 fp16
-  float2* part_ml;  // their (running max in the log2 domain, running sum) [unit][nsplit][256]
+  __half* part;     // split partials [unit][nsplit][D / 8][CTA rows] 16-byte chunks of 8 fp16
+  float2* part_ml;  // their (running max in the log2 domain, running sum) [unit][nsplit][CTA rows]
   int N, Hq, Hkv, G, Lcap, W;
   int nb;           // nodes per row block: floor(128 / G)
-  int mtiles;       // CTAs along the node axis: ceil(N / (2 nb))
+  int mtiles;       // CTAs along the node axis: ceil(N / (row blocks x nb))
   int nsplit;       // splits of the key range
   float scale_log2;
 };
 
-template <int D>
+template <int D, int RBS>
 struct Layout {
   static constexpr int A = D / 64;                   // 128-byte atoms per row of Q, K, V
+  static constexpr int kTile = A * kAtomBytes;       // one K or V tile (128 keys)
   static constexpr int kQ = 0;                       // Q [row block][atom]
-  static constexpr int kP = kQ + 2 * A * kAtomBytes; // P [row block][key half], bf16
-  static constexpr int kK = kP + 4 * kAtomBytes;
-  static constexpr int kV = kK + A * kAtomBytes;
-  static constexpr int kBytes = kV + A * kAtomBytes;
+  static constexpr int kP = kQ + RBS * A * kAtomBytes;  // P [row block][buffer][key half], bf16
+  static constexpr int kK = kP + RBS * Shape<RBS>::kPBufs * 2 * kAtomBytes;  // K ring [stage][atom]
+  static constexpr int kV = kK + Shape<RBS>::kKStages * kTile;  // V ring [stage][atom]
+  static constexpr int kBytes = kV + Shape<RBS>::kVStages * kTile;
   static constexpr int kDyn = kBytes + 1024;         // slack for 1024-byte alignment
 };
 
@@ -83,6 +106,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Two fp32 lanes at once (Blackwell f32x2 instructions), round to nearest.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<const float2*>(&d);
 }
 
 // 2^x on the special-function unit (ex2.approx, flush-to-zero); 2^-inf = +0.
@@ -122,12 +162,19 @@ __device__ __forceinline__ uint32_t visibility32(int c, int j0, int L, int keys,
   return (pm | tm) & em;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int RBS>
+__global__ void __launch_bounds__(Shape<RBS>::kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using Lay = Layout<D>;
+  using Lay = Layout<D, RBS>;
+  using Sh = Shape<RBS>;
   constexpr int A = Lay::A;
+  constexpr int kKStages = Sh::kKStages, kVStages = Sh::kVStages, kPBufs = Sh::kPBufs;
+  constexpr int kSBufs = Sh::kSBufs;
+  constexpr uint32_t kOCol = 128u * RBS * kSBufs;  // first O column
+  constexpr int kProducerWarp = Sh::kProducerWarp, kMmaWarp = Sh::kMmaWarp;
+  constexpr int kVProducerWarp = Sh::kVProducerWarp;
+  constexpr uint32_t kTmemCols = Sh::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -136,9 +183,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   uint8_t* sK = smem + Lay::kK;
   uint8_t* sV = smem + Lay::kV;
 
-  __shared__ __align__(8) uint64_t bar_q, bar_k_full, bar_k_empty, bar_v_full, bar_v_empty;
+  __shared__ __align__(8) uint64_t bar_q;
+  __shared__ __align__(8) uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
+  __shared__ __align__(8) uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
   __shared__ __align__(8) uint64_t bar_drain;
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_free[2], bar_p_full[2], bar_o_done[2];
+  __shared__ __align__(8) uint64_t bar_s_full[2][kSBufs], bar_s_free[2][kSBufs];
+  // one P barrier per P buffer: with two buffers the softmax may finish P(t + 1)
+  // before the MMA warp has seen P(t), and a shared barrier would then be two
+  // phases ahead of the parity it is tested for
+  __shared__ __align__(8) uint64_t bar_p_full[2][kPBufs];
+  __shared__ __align__(8) uint64_t bar_o_done[2][kPBufs];  // PV(t) of a row block, per P buffer
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -149,9 +203,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N, G = p.G, nb = p.nb;
-  const int node0 = mt * 2 * nb;                 // first node of this CTA
-  const int nrb = (node0 + nb < N) ? 2 : 1;      // row blocks holding a node
-  const bool is_softmax = warp < 8;
+  const int node0 = mt * RBS * nb;               // first node of this CTA
+  const int nrb = (RBS == 2 && node0 + nb < N) ? 2 : 1;  // row blocks holding a node
+  const bool is_softmax = warp < 4 * RBS;
   const int rb = (warp >> 2) & 1;                // softmax warps: row block
   const int row = tid & (kRB - 1);               // softmax warps: row = TMEM lane
   const int nodel = row / G;
@@ -165,20 +219,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int tiles_cap = ceil_div(p.Lcap, kBN);
   const int t_begin = (int)(((long long)split * tiles_cap) / p.nsplit);
   const int t_end = (int)(((long long)(split + 1) * tiles_cap) / p.nsplit);
-  const bool first_issued = t_end > t_begin;
+  // tiles issued during setup, one per stage
+  const int preK = min(kKStages, t_end - t_begin), preV = min(kVStages, t_end - t_begin);
+  const bool first_issued = preK > 0;
   const int y0 = bh * p.Lcap + t_begin * kBN;
   if (tid == 0) {
     mbar_init(&bar_q, 1);
-    mbar_init(&bar_k_full, 1);
-    mbar_init(&bar_k_empty, 1);
-    mbar_init(&bar_v_full, 1);
-    mbar_init(&bar_v_empty, 1);
+    for (int st = 0; st < kKStages; ++st) {
+      mbar_init(&bar_k_full[st], 1);
+      mbar_init(&bar_k_empty[st], 1);
+    }
+    for (int st = 0; st < kVStages; ++st) {
+      mbar_init(&bar_v_full[st], 1);
+      mbar_init(&bar_v_empty[st], 1);
+    }
     mbar_init(&bar_drain, 1);
     for (int r = 0; r < 2; ++r) {
-      mbar_init(&bar_s_full[r], 1);
-      mbar_init(&bar_s_free[r], kRB);
-      mbar_init(&bar_p_full[r], kRB);
-      mbar_init(&bar_o_done[r], 1);
+      for (int u = 0; u < kSBufs; ++u) {
+        mbar_init(&bar_s_full[r][u], 1);
+        mbar_init(&bar_s_free[r][u], kRB);
+      }
+      for (int u = 0; u < kPBufs; ++u) mbar_init(&bar_p_full[r][u], kRB);
+      for (int u = 0; u < kPBufs; ++u) mbar_init(&bar_o_done[r][u], 1);
     }
     mbar_fence_init();
     s_abort = 0;
@@ -201,12 +263,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int a = 0; a < A; ++a)
           tma_load_3d(sQ + (r * A + a) * kAtomBytes, &tmQ, &bar_q, a * 64, kvh * G,
                       b * N + node0 + r * nb);
-      mbar_expect_tx(&bar_k_full, A * kAtomBytes);
-      mbar_expect_tx(&bar_v_full, A * kAtomBytes);
+      for (int t = 0; t < preV; ++t) {
+        if (t < preK) {
+          mbar_expect_tx(&bar_k_full[t], Lay::kTile);
 #pragma unroll
-      for (int a = 0; a < A; ++a) {
-        tma_load_2d(sK + a * kAtomBytes, &tmK, &bar_k_full, a * 64, y0);
-        tma_load_2d(sV + a * kAtomBytes, &tmV, &bar_v_full, a * 64, y0);
+          for (int a = 0; a < A; ++a)
+            tma_load_2d(sK + t * Lay::kTile + a * kAtomBytes, &tmK, &bar_k_full[t], a * 64,
+                        y0 + t * kBN);
+        }
+        mbar_expect_tx(&bar_v_full[t], Lay::kTile);
+#pragma unroll
+        for (int a = 0; a < A; ++a)
+          tma_load_2d(sV + t * Lay::kTile + a * kAtomBytes, &tmV, &bar_v_full[t], a * 64,
+                      y0 + t * kBN);
       }
     }
   }
@@ -225,8 +294,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (split == 0 && mt == 0 && kvh == 0 && tid == 0 && p.status) p.status[b] = TV_ERR_INVALID_ARG;
     if (tid == 0 && first_issued) {  // no copy may be in flight when the CTA leaves
       mbar_wait(&bar_q, 0);
-      mbar_wait(&bar_k_full, 0);
-      mbar_wait(&bar_v_full, 0);
+      for (int t = 0; t < preK; ++t) mbar_wait(&bar_k_full[t], 0);
+      for (int t = 0; t < preV; ++t) mbar_wait(&bar_v_full[t], 0);
     }
     __syncwarp();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -239,28 +308,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
   float m_run = -INFINITY, l_run = 0.0f;  // softmax threads: running max (log2) and sum
 
-  if (first_issued && warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    // tile 0 (and Q) were issued during setup; lane 0 loads K, lane 1 V
-    if (lane < 2) {
-      uint64_t* full = lane ? &bar_v_full : &bar_k_full;
-      uint64_t* empty = lane ? &bar_v_empty : &bar_k_empty;
-      const CUtensorMap* map = lane ? &tmV : &tmK;
-      uint8_t* dst = lane ? sV : sK;
-      int issued = 1;
-      for (int t = 1; t < T; ++t) {
-        if (!mbar_wait(empty, (t & 1) ^ 1) || s_abort) {
+  if (first_issued && (warp == kProducerWarp || warp == kVProducerWarp)) {
+    // ----------------------------------------------------------- producers
+    // the first tiles of each ring (and Q) were issued during setup; lane 0
+    // of one warp loads K, lane 0 of another V, each into a ring of its own depth
+    if (lane == 0) {
+      const bool isV = warp == kVProducerWarp;
+      uint64_t* full = isV ? bar_v_full : bar_k_full;
+      uint64_t* empty = isV ? bar_v_empty : bar_k_empty;
+      const CUtensorMap* map = isV ? &tmV : &tmK;
+      uint8_t* dst = isV ? sV : sK;
+      const int stages = isV ? kVStages : kKStages;
+      int issued = isV ? preV : preK;
+      for (int t = issued; t < T; ++t) {
+        const int st = t % stages;
+        if (!mbar_wait(&empty[st], ((t / stages) & 1) ^ 1) || s_abort) {
           s_abort = 1;
           break;
         }
-        mbar_expect_tx(full, A * kAtomBytes);
+        mbar_expect_tx(&full[st], Lay::kTile);
 #pragma unroll
-        for (int a = 0; a < A; ++a) tma_load_2d(dst + a * kAtomBytes, map, full, a * 64, y0 + t * kBN);
+        for (int a = 0; a < A; ++a)
+          tma_load_2d(dst + st * Lay::kTile + a * kAtomBytes, map, &full[st], a * 64,
+                      y0 + t * kBN);
         issued = t + 1;
       }
-      // the CTA must not move on while its copies are in flight
-      if (lane == 0) mbar_wait(&bar_q, 0);
-      mbar_wait(full, (issued - 1) & 1);
+      // the CTA must not move on while its copies are in flight: the last
+      // tile issued into each stage has landed
+      if (!isV) mbar_wait(&bar_q, 0);
+      for (int t = max(0, issued - stages); t < issued; ++t)
+        mbar_wait(&full[t % stages], (t / stages) & 1);
     }
   } else if (T > 0 && warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
@@ -277,29 +354,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     long long t_idle = clock64();
     while (ok && min(npv[0], npv[1]) < T) {
       bool prog = false;
-      if (ns < T && ns <= min(npv[0], npv[1]) + 1) {
+      // S(t + 1) may go ahead of PV(t); with two P buffers also ahead of PV(t - 1)
+      if (ns < T && ns <= min(npv[0], npv[1]) + kPBufs) {
         bool ready = false;
         if (lane == 0) {
-          ready = mbar_test(&bar_k_full, ns & 1);
-          if (ready && ns > 0)
-            ready = mbar_test(&bar_s_free[0], (ns - 1) & 1) &&
-                    (nrb < 2 || mbar_test(&bar_s_free[1], (ns - 1) & 1));
+          ready = mbar_test(&bar_k_full[ns % kKStages], (ns / kKStages) & 1);
+          if (ready && ns >= kSBufs) {  // the softmax read S(ns - kSBufs) from this buffer
+            const int u = ns % kSBufs, ph = ((ns - kSBufs) / kSBufs) & 1;
+            ready = mbar_test(&bar_s_free[0][u], ph) &&
+                    (nrb < 2 || mbar_test(&bar_s_free[1][u], ph));
+          }
         }
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t k0 = smem_u32(sK);
+            const uint32_t k0 = smem_u32(sK) + (ns % kKStages) * Lay::kTile;
             for (int r = 0; r < nrb; ++r) {
               const uint32_t q0 = smem_u32(sQ) + r * A * kAtomBytes;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-                mma_bf16(tmem + 128 * r, sw128_desc(q0 + off, 16, 1024),
+                mma_bf16(tmem + 128 * (r * kSBufs + ns % kSBufs), sw128_desc(q0 + off, 16, 1024),
                          sw128_desc(k0 + off, 16, 1024), idS, kk > 0);
               }
-              mma_commit(&bar_s_full[r]);
+              mma_commit(&bar_s_full[r][ns % kSBufs]);
             }
-            mma_commit(&bar_k_empty);
+            mma_commit(&bar_k_empty[ns % kKStages]);
           }
           __syncwarp();
           ++ns;
@@ -311,7 +391,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const int t = npv[r];
         if (t >= ns) continue;
         bool ready = false;
-        if (lane == 0) ready = mbar_test(&bar_v_full, t & 1) && mbar_test(&bar_p_full[r], t & 1);
+        if (lane == 0)
+          ready = mbar_test(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
+                  mbar_test(&bar_p_full[r][t % kPBufs], (t / kPBufs) & 1);
         if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
         tc_fence_after();
         // PV runs over the 16-key steps that hold a key of the range; the V
@@ -325,7 +407,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
             for (int a = 0; a < A; ++a)
               for (int zr = valid + (lane >> 3); zr < z1; zr += 4)
-                *reinterpret_cast<uint4*>(sV + a * kAtomBytes + zr * 128 + ((lane & 7) << 4)) =
+                *reinterpret_cast<uint4*>(sV + (t % kVStages) * Lay::kTile + a * kAtomBytes +
+                                          zr * 128 + ((lane & 7) << 4)) =
                     make_uint4(0, 0, 0, 0);
             fence_async_smem();
           }
@@ -334,15 +417,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t v0 = smem_u32(sV);
-          const uint32_t p0 = smem_u32(sP) + r * 2 * kAtomBytes;
+          const uint32_t v0 = smem_u32(sV) + (t % kVStages) * Lay::kTile;
+          const uint32_t p0 = smem_u32(sP) + (r * kPBufs + t % kPBufs) * 2 * kAtomBytes;
           for (int kk = 0; kk < nk; ++kk)
-            mma_bf16(tmem + 256 + 128 * r,
+            mma_bf16(tmem + kOCol + 128 * r,
                      sw128_desc(p0 + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
                      sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
-          mma_commit(&bar_o_done[r]);
+          mma_commit(&bar_o_done[r][t % kPBufs]);
           // V(t) is free once both row blocks' PV(t) are done
-          if (npv[r ^ 1] > t) mma_commit(&bar_v_empty);
+          if (npv[r ^ 1] > t) mma_commit(&bar_v_empty[t % kVStages]);
         }
         __syncwarp();
         npv[r] = t + 1;
@@ -365,11 +448,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     // ------------------------------------------------------------- softmax
     const uint64_t* anc = p.anc + ((size_t)b * N + (valid_row ? node : 0)) * p.W;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + 128 * rb, tO = tmem + 256 + 128 * rb;
+    const uint32_t tS0 = tmem + 128 * (rb * kSBufs), tO = tmem + kOCol + 128 * rb;
     const float sc = p.scale_log2;
-    uint8_t* prow = sP + rb * 2 * kAtomBytes + row * 128;
+    uint8_t* const prow0 = sP + rb * kPBufs * 2 * kAtomBytes + row * 128;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
+      uint8_t* const prow = prow0 + (t % kPBufs) * 2 * kAtomBytes;
       // the mask words (their ancestor loads) are ready before S is
       const int j0 = (t_begin + t) * kBN;
       uint32_t vis[4] = {0u, 0u, 0u, 0u};
@@ -382,33 +466,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           for (int c = 0; c < 4; ++c) vis[c] = visibility32(c, j0, L, keys, N, anc, p.W);
         }
       }
-      ok = warp_wait(&bar_s_full[rb], t & 1);
+      ok = warp_wait(&bar_s_full[rb][t % kSBufs], (t / kSBufs) & 1);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
+      const uint32_t tS = tS0 + 128 * (t % kSBufs);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_base + 32 * c, sr[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar_s_free[rb]);  // the MMA warp may write the next S now
+      mbar_arrive(&bar_s_free[rb][t % kSBufs]);  // the MMA warp may write this S buffer again
 
-      // a 32-key chunk is all visible, all hidden, or masked key by key
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // hidden keys become -inf; most tiles are all visible (prefix keys)
+      if ((vis[0] & vis[1] & vis[2] & vis[3]) != 0xffffffffu) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (vis[c] == 0xffffffffu) {
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][e]));
-        } else if (vis[c] != 0u) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = ((vis[c] >> e) & 1u) ? __uint_as_float(sr[c][e]) : -INFINITY;
-            sr[c][e] = __float_as_uint(x);
-            mx[c] = fmaxf(mx[c], x);
-          }
-        }
+          for (int e = 0; e < 32; ++e)
+            if (!((vis[c] >> e) & 1u)) sr[c][e] = __float_as_uint(-INFINITY);
       }
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+      // row maximum over eight independent chains
+      float mx8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = __uint_as_float(sr[0][j]);
+#pragma unroll
+      for (int k = 8; k < kBN; k += 8)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(mx8[j], __uint_as_float(sr[k >> 5][(k & 31) + j]));
+      const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sc;
       float corr = 1.0f;
       bool need = false;
       const float m_new = fmaxf(m_run, tmax);
@@ -419,50 +505,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         m_run = m_new;
         need = true;
       }
-      // the P buffer and O are free once the previous PV retired
-      if (t > 0) {
-        ok = warp_wait(&bar_o_done[rb], (t - 1) & 1);
+      // P buffer t % kPBufs is free once PV(t - kPBufs) retired
+      if (t >= kPBufs) {
+        const int u = t - kPBufs;
+        ok = warp_wait(&bar_o_done[rb][u % kPBufs], (u / kPBufs) & 1);
         if (!ok) break;
         tc_fence_after();
       }
-      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // 2^(s sc - m) pairwise (f32x2 FMA, then the special-function unit); a
+      // hidden key gives 2^-inf = 0.  Four pairwise partial sums.
+      float2 ps2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       if (m_run == -INFINITY) {  // nothing visible yet: P = 0
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(prow + (c >> 1) * kAtomBytes +
-                                      ((((c & 1) * 4 + q) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        for (int g = 0; g < kBN / 8; ++g)
+          *reinterpret_cast<uint4*>(prow + (g >> 3) * kAtomBytes + (((g & 7) ^ (row & 7)) << 4)) =
+              make_uint4(0, 0, 0, 0);
       } else {
-        const float neg_m = -m_run;
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (vis[c] == 0u) {  // hidden chunk: P = 0
+        for (int g = 0; g < kBN / 8; ++g) {  // 8 keys -> one 16-byte chunk of P
+          uint32_t w[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(prow + (c >> 1) * kAtomBytes +
-                                        ((((c & 1) * 4 + q) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-            continue;
+          for (int e = 0; e < 4; ++e) {
+            const int k = 8 * g + 2 * e;
+            const float2 y = ffma2(make_float2(__uint_as_float(sr[k >> 5][k & 31]),
+                                               __uint_as_float(sr[k >> 5][(k & 31) + 1])),
+                                   sc2, nm2);
+            const float2 x = make_float2(ex2(y.x), ex2(y.y));
+            ps2[e] = fadd2(ps2[e], x);
+            w[e] = pack_bf16(x.x, x.y);
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 8 keys -> one 16-byte chunk of P
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float x0 = ex2(fmaf(__uint_as_float(sr[c][8 * q + 2 * e]), sc, neg_m));
-              const float x1 = ex2(fmaf(__uint_as_float(sr[c][8 * q + 2 * e + 1]), sc, neg_m));
-              ps[c] += x0 + x1;
-              w[e] = pack_bf16(x0, x1);
-            }
-            *reinterpret_cast<uint4*>(prow + (c >> 1) * kAtomBytes +
-                                      ((((c & 1) * 4 + q) ^ (row & 7)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          *reinterpret_cast<uint4*>(prow + (g >> 3) * kAtomBytes + (((g & 7) ^ (row & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      const float2 ps_a = fadd2(ps2[0], ps2[1]), ps_b = fadd2(ps2[2], ps2[3]);
+      const float2 ps_ab = fadd2(ps_a, ps_b);
+      l_run = l_run * corr + (ps_ab.x + ps_ab.y);
       // rescale O after the exponentials, when S no longer holds registers
       if (__any_sync(0xffffffffu, need)) {
+        if (kPBufs > 1) {  // O holds every tile up to t - 1 once PV(t - 1) retired
+          ok = warp_wait(&bar_o_done[rb][(t - 1) % kPBufs], ((t - 1) / kPBufs) & 1);
+          if (!ok) break;
+          tc_fence_after();
+        }
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
@@ -476,9 +563,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p_full[rb]);
+      mbar_arrive(&bar_p_full[rb][t % kPBufs]);
     }
-    if (ok) ok = warp_wait(&bar_o_done[rb], (T - 1) & 1);
+    if (ok) ok = warp_wait(&bar_o_done[rb][(T - 1) % kPBufs], ((T - 1) / kPBufs) & 1);
     if (!ok) s_abort = 1;
     tc_fence_after();
   }
@@ -490,11 +577,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const size_t unit = (size_t)bh * p.mtiles + mt;  // (sequence, kv head, node tile)
   if (act) {
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + 256 + 128 * rb;
+    const uint32_t tO = tmem + kOCol + 128 * rb;
     const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
     const int crow = rb * kRB + row;  // row of the CTA
     const size_t slot = unit * p.nsplit + split;
-    if (split_kv) p.part_ml[slot * kRows + crow] = make_float2(m_run, l_run);
+    if (split_kv) p.part_ml[slot * Sh::kRows + crow] = make_float2(m_run, l_run);
     if (T > 0) {
       uint32_t o[D / 32][32];
 #pragma unroll
@@ -503,12 +590,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (split_kv) {
         // normalised fp16 partial row, chunk-major: the lanes of a warp hold
         // consecutive rows, so every store instruction writes 512 contiguous bytes
-        uint4* dst = reinterpret_cast<uint4*>(p.part) + slot * (D / 8) * kRows + crow;
+        uint4* dst = reinterpret_cast<uint4*>(p.part) + slot * (D / 8) * Sh::kRows + crow;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            dst[(size_t)(4 * c + q) * kRows] = make_uint4(
+            dst[(size_t)(4 * c + q) * Sh::kRows] = make_uint4(
                 pack_f16(__uint_as_float(o[c][8 * q + 0]) * inv, __uint_as_float(o[c][8 * q + 1]) * inv),
                 pack_f16(__uint_as_float(o[c][8 * q + 2]) * inv, __uint_as_float(o[c][8 * q + 3]) * inv),
                 pack_f16(__uint_as_float(o[c][8 * q + 4]) * inv, __uint_as_float(o[c][8 * q + 5]) * inv),
@@ -548,10 +635,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 // one-wave attention grid run in one wave too.
 constexpr int kMergeRows = 32, kMergeChunks = 2, kMergeGroups = 4, kMergeBatch = 6;
 
-template <int D>
+template <int D, int RBS>
 __global__ void __launch_bounds__(256, 4)
 attn_merge_kernel(const AttnParams p) {
   constexpr int kC16 = D / 8;
+  constexpr int kRows = Shape<RBS>::kRows;
   constexpr int kCtaPerUnit = (kRows / kMergeRows) * (kC16 / kMergeChunks);
   constexpr int kSPT = kMaxSplit / kMergeGroups;  // slots per thread at most
   __shared__ float s_m[kMergeGroups][kMergeChunks][kMergeRows];
@@ -620,7 +708,7 @@ attn_merge_kernel(const AttnParams p) {
   if (L < 0 || L + p.N > p.Lcap) return;  // the attention kernel zeroed these outputs
   const int rbk = crow / kRB, rl = crow % kRB;
   const int nodel = rl / p.G;
-  const int node = mt * 2 * p.nb + rbk * p.nb + nodel;
+  const int node = mt * RBS * p.nb + rbk * p.nb + nodel;
   if (nodel >= p.nb || node >= p.N) return;
   const int h = kvh * p.G + rl % p.G;
   float Mt = -INFINITY;
@@ -672,45 +760,82 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 struct SplitPlan {
+  int rbs;          // row blocks of 128 rows per CTA (1 or 2)
   int nb, mtiles, nsplit;
   long long units;  // (sequence, kv head, node tile) triples
 };
 
-// Rough per-CTA costs (about a microsecond each) of a 128-key tile, of the
-// fixed part of a CTA (setup, first loads, epilogue) and of the merge kernel.
-constexpr long long kCostTile = 2, kCostFixed = 4, kCostMerge = 4;
+// Rough costs in tenths of a microsecond, measured on the kernels: the fixed
+// part of a CTA (setup, first loads, epilogue), its first 128-key tile, each
+// further tile, and the merge kernel.  The period of a 256-row CTA is set by
+// its single K stage (a load per tile on the critical path), that of a
+// 128-row CTA by its two-stage K ring against the load latency.
+constexpr long long kCostFixed = 40, kCostFirst = 20, kCostMerge = 40;
+constexpr long long kCostTile[3] = {0, 15, 27};
 
-// Choose the split count that minimises
-// (waves of CTAs) x (tiles per CTA x tile cost + fixed cost) + merge cost,
-// preferring fewer splits.  One CTA fits an SM (its shared memory decides).
+// Choose the CTA height and split count that minimise
+// (waves of CTAs) x (CTA cost) + merge cost, preferring the taller CTA and
+// fewer splits on ties.  One CTA fits an SM (its shared memory decides).
 SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
-  SplitPlan sp;
+  SplitPlan best_sp{};
   const int G = Hq / Hkv;
-  sp.nb = kRB / G;
-  sp.mtiles = ceil_div(N, 2 * sp.nb);
-  sp.units = (long long)B * Hkv * sp.mtiles;
+  const int nb = kRB / G;
   const int tiles_max = ceil_div(Lcap, kBN);
   const long long slots = device_sm_count();
   long long best = -1;
-  sp.nsplit = 1;
-  for (int ns = 1; ns <= kMaxSplit && ns <= tiles_max; ++ns) {
-    const long long waves = (sp.units * ns + slots - 1) / slots;
-    const long long tiles_per_cta = (tiles_max + ns - 1) / ns;
-    const long long cost =
-        waves * (tiles_per_cta * kCostTile + kCostFixed) + (ns > 1 ? kCostMerge : 0);
-    if (best < 0 || cost < best) {
-      best = cost;
-      sp.nsplit = ns;
+  for (int rbs = 2; rbs >= 1; --rbs) {
+    SplitPlan sp;
+    sp.rbs = rbs;
+    sp.nb = nb;
+    sp.mtiles = ceil_div(N, rbs * nb);
+    sp.units = (long long)B * Hkv * sp.mtiles;
+    for (int ns = 1; ns <= kMaxSplit && ns <= tiles_max; ++ns) {
+      const long long waves = (sp.units * ns + slots - 1) / slots;
+      const long long tiles_per_cta = (tiles_max + ns - 1) / ns;
+      const long long cta = kCostFixed + kCostFirst + (tiles_per_cta - 1) * kCostTile[rbs];
+      const long long cost = waves * cta + (ns > 1 ? kCostMerge : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        sp.nsplit = ns;
+        best_sp = sp;
+      }
     }
   }
-  return sp;
+  return best_sp;
 }
 
 // Workspace bytes of a plan: fp16 partial rows, then their (max, sum) pairs.
 size_t plan_workspace(const SplitPlan& sp, int D) {
   if (sp.nsplit <= 1) return 0;
-  const size_t rows = (size_t)sp.units * sp.nsplit * kRows;
+  const size_t rows = (size_t)sp.units * sp.nsplit * kRB * sp.rbs;
   return align_up(rows * D * 2, 256) + align_up(rows * 8, 256);
+}
+
+template <int D, int RBS>
+bool set_smem_once() {
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(attn_tc_kernel<D, RBS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<D, RBS>::kDyn) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    done = true;
+  }
+  return true;
+}
+
+template <int D, int RBS>
+cudaError_t launch_grids(const SplitPlan& sp, int BH, cudaStream_t stream, const CUtensorMap& tmQ,
+                         const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p) {
+  cudaError_t e = launch_pdl(attn_tc_kernel<D, RBS>, dim3(sp.nsplit, sp.mtiles, BH),
+                             dim3(Shape<RBS>::kThreads, 1, 1), (size_t)Layout<D, RBS>::kDyn,
+                             stream, tmQ, tmK, tmV, p);
+  if (e != cudaSuccess || sp.nsplit <= 1) return e;
+  const long long ctas =
+      sp.units * (Shape<RBS>::kRows / kMergeRows) * ((D / 8) / kMergeChunks);
+  return launch_pdl(attn_merge_kernel<D, RBS>, dim3((unsigned)ctas, 1, 1), dim3(256, 1, 1), 0,
+                    stream, p);
 }
 
 template <int D>
@@ -718,7 +843,6 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
                       const uint64_t* anc_mask, int B, int N, int Hq, int Hkv, int Lcap,
                       float scale_log2, tv_bf16* out, float* lse, int32_t* status,
                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  using Lay = Layout<D>;
   const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap);
   const size_t need = plan_workspace(sp, D);
   if (need > 0 && (workspace == nullptr || ws_bytes < need ||
@@ -726,15 +850,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
     return TV_ERR_WORKSPACE;
   auto encode = tensor_map_encoder();
   if (!encode) return TV_ERR_CUDA;
-  static bool smem_set = false;
-  if (!smem_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay::kDyn) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
-    smem_set = true;
-  }
+  if (!(sp.rbs == 2 ? set_smem_once<D, 2>() : set_smem_once<D, 1>())) return TV_ERR_CUDA;
   const int G = Hq / Hkv;
   const cuuint32_t estr[3] = {1, 1, 1};
   // Q as [B * N tokens][Hq heads][D]; a box is {64 dims, G heads, nb nodes}
@@ -771,7 +887,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.part = nullptr;
   p.part_ml = nullptr;
   if (need > 0) {
-    const size_t rows = (size_t)sp.units * sp.nsplit * kRows;
+    const size_t rows = (size_t)sp.units * sp.nsplit * kRB * sp.rbs;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.part = reinterpret_cast<__half*>(ws);
     p.part_ml = reinterpret_cast<float2*>(ws + align_up(rows * D * 2, 256));
@@ -786,18 +902,11 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.mtiles = sp.mtiles;
   p.nsplit = sp.nsplit;
   p.scale_log2 = scale_log2;
-  if (launch_pdl(attn_tc_kernel<D>, dim3(sp.nsplit, sp.mtiles, B * Hkv), dim3(kThreads, 1, 1),
-                 (size_t)Lay::kDyn, stream, tmQ, tmK, tmV, p) != cudaSuccess) {
+  const cudaError_t e = sp.rbs == 2 ? launch_grids<D, 2>(sp, B * Hkv, stream, tmQ, tmK, tmV, p)
+                                     : launch_grids<D, 1>(sp, B * Hkv, stream, tmQ, tmK, tmV, p);
+  if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;
-  }
-  if (sp.nsplit > 1) {
-    const long long ctas = sp.units * (kRows / kMergeRows) * ((D / 8) / kMergeChunks);
-    if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)ctas, 1, 1), dim3(256, 1, 1), 0, stream,
-                   p) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
   }
   return TV_OK;
 }

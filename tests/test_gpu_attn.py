@@ -121,11 +121,24 @@ def test_config3_talon_tree_sampled(tv, oracle_mod):
 
 
 def test_merge_kernel_path_large_batch(tv, oracle_mod):
-    """160 (sequence, kv head) units: the split plan is more than one wave, so
-    the splits cannot wait for one another and a separate kernel merges them."""
-    case = gen.make_case(23, B=40, N=60, L=1500, Hq=16, Hkv=4, D=64, V=64)
-    assert tv.attn_workspace_size(40, 60, 16, 4, 64, case.Lcap) > 0
+    """96 (sequence, kv head) pairs over 6,000 prefix keys: the plan takes
+    128-row CTAs in several splits and more than one wave of CTAs, whose
+    partials a separate kernel merges."""
+    case = gen.make_case(23, B=24, N=60, L=6000, Hq=16, Hkv=4, D=64, V=64)
+    assert tv.attn_workspace_size(24, 60, 16, 4, 64, case.Lcap) > 0
     sampled_check(tv, oracle_mod, case, 48, 8, "merge-kernel")
+
+
+@pytest.mark.parametrize("B,L", [(1, 1500), (1, 6000)])
+def test_split_plans_single_wave(tv, oracle_mod, B, L):
+    """One sequence, 60 nodes: 1,500 keys split 256-row CTAs, 6,000 keys
+    split 128-row CTAs with a two-stage K/V ring; every row is compared."""
+    case = gen.make_case(24 + L, B=B, N=60, L=L, Hq=16, Hkv=4, D=64, V=64)
+    assert tv.attn_workspace_size(B, 60, 16, 4, 64, case.Lcap) > 0
+    out, lse, status = run_attn(tv, case)
+    assert (status == 0).all()
+    ref, ref_lse = oracle_mod.attn_all(case.q, case.k, case.v, case.kv_len, case.parent, 16, 4)
+    check_attn(out, ref, f"split-L{L}")
 
 
 def test_split_plan_repeats_bitwise(tv, oracle_mod):
