@@ -207,11 +207,37 @@ __device__ __forceinline__ int gather2(const int (&v)[2], int j) {
   return (j < 32) ? lo : hi;
 }
 
-__device__ void warp_scan(const GreedyArgs& g, int b, int err) {
+// A tree of at most 64 nodes as one warp holds it: node i in lane i % 32,
+// slot i / 32.  Every CTA's first warp loads its sequence's tree while the
+// logits stream, so that the CTA which completes the sequence only has the
+// row keys left to fetch.
+struct TreeRegs {
+  int par[2], dep[2], tok[2];
+};
+
+__device__ __forceinline__ TreeRegs load_tree_regs(const GreedyArgs& g, int b) {
+  const int lane = threadIdx.x & 31;
+  const size_t o = (size_t)b * g.N;
+  TreeRegs t;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    const bool in = i < g.N;
+    t.par[s] = in ? __ldcg(g.parent + o + i) : -1;
+    t.dep[s] = in ? __ldcg(g.depth + o + i) : 0;
+    t.tok[s] = in ? __ldcg(g.tokens + o + i) : 0;
+  }
+  return t;
+}
+
+__device__ void warp_scan(const GreedyArgs& g, int b, int err, const TreeRegs& tr) {
   const int lane = threadIdx.x & 31;
   const int N = g.N;
   const size_t o = (size_t)b * N;
-  int par[2], dep[2], tok[2], am[2];
+  int am[2];
+  const int(&par)[2] = tr.par;
+  const int(&dep)[2] = tr.dep;
+  const int(&tok)[2] = tr.tok;
   bool in[2];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
@@ -219,9 +245,6 @@ __device__ void warp_scan(const GreedyArgs& g, int b, int err) {
     in[s] = i < N;
     const unsigned long long key = in[s] ? atomicExch(g.ws.keys + o + i, 0ull) : 0ull;
     am[s] = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
-    par[s] = in[s] ? __ldcg(g.parent + o + i) : -1;
-    dep[s] = in[s] ? __ldcg(g.depth + o + i) : 0;
-    tok[s] = in[s] ? __ldcg(g.tokens + o + i) : 0;
     if (in[s]) g.argmax[o + i] = am[s];
   }
   if (lane == 0) g.ws.arrivals[b] = 0u;
@@ -322,7 +345,7 @@ __device__ void warp_scan(const GreedyArgs& g, int b, int err) {
 // sets bit 31 of the arrival counter, which the scan reports.
 __device__ __forceinline__ void finish_item(const GreedyArgs& g, long long row, int b, ArgMax best,
                                             ArgMax* s_red, int* s_last, bool timed_out,
-                                            ScanSmem& sm) {
+                                            ScanSmem& sm, const TreeRegs& tr) {
   best = block_argmax(best, s_red);
   if (threadIdx.x == 0) {
     // the key update needs no answer; the arrival is a release (ordering the
@@ -336,7 +359,7 @@ __device__ __forceinline__ void finish_item(const GreedyArgs& g, long long row, 
   if (*s_last) {
     const int err = *s_last == 2 ? TV_ERR_TIMEOUT : TV_OK;
     if (g.N <= kWarpScanMax) {
-      if (threadIdx.x < 32) warp_scan(g, b, err);
+      if (threadIdx.x < 32) warp_scan(g, b, err, tr);
     } else {
       tree_scan(g, b, sm, err);
     }
@@ -378,8 +401,18 @@ greedy_bulk_kernel(const GreedyArgs g) {
       sm100::bulk_load_global(g_smem + (size_t)q0 * 16, src + q0, (uint32_t)qn * 16u, &s_bar[q]);
     }
   }
-  prefetch_tree(g, b);
-  ArgMax best{-INFINITY, INT_MAX};
+  TreeRegs tr{};
+  if (g.N <= kWarpScanMax) {
+    if (tid < 32) tr = load_tree_regs(g, b);
+  } else {
+    prefetch_tree(g, b);
+  }
+  // four independent compare chains, one per float4 lane: each sees its
+  // indices in increasing order, so a strict compare keeps the lowest index
+  // of its maximum, and the combine below breaks ties to the lower index
+  ArgMax c4[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c4[j] = {-INFINITY, INT_MAX};
   bool ok = true;
   const float4* x4 = reinterpret_cast<const float4*>(g_smem);
   for (int q = 0; q < kGreedyPieces; ++q) {
@@ -389,20 +422,23 @@ greedy_bulk_kernel(const GreedyArgs g) {
       ok = false;  // every copy of this CTA is waited for (bounded) below
       continue;
     }
+#pragma unroll 4
     for (int k = q0 + tid; k < q0 + qn; k += kGreedyThreads) {
       const float4 v = x4[k];
       const int e = 4 * (base + k);
-      if (v.x > best.v) best = {v.x, e};
-      if (v.y > best.v) best = {v.y, e + 1};
-      if (v.z > best.v) best = {v.z, e + 2};
-      if (v.w > best.v) best = {v.w, e + 3};
+      if (v.x > c4[0].v) c4[0] = {v.x, e};
+      if (v.y > c4[1].v) c4[1] = {v.y, e + 1};
+      if (v.z > c4[2].v) c4[2] = {v.z, e + 2};
+      if (v.w > c4[3].v) c4[3] = {v.w, e + 3};
     }
   }
+  ArgMax best = argmax_combine(argmax_combine(c4[0], c4[1]), argmax_combine(c4[2], c4[3]));
   if (best.i == INT_MAX) best.i = 4 * base;  // only -inf seen: lowest index of the chunk
   const bool timed_out = __syncthreads_or(!ok) != 0;
   // the chunk buffer is dead once every thread has reduced it (the block
   // reduction below starts with a barrier)
-  finish_item(g, row, b, best, s_red, &s_last, timed_out, *reinterpret_cast<ScanSmem*>(g_smem));
+  finish_item(g, row, b, best, s_red, &s_last, timed_out, *reinterpret_cast<ScanSmem*>(g_smem),
+              tr);
 }
 
 // Rows not 16-byte aligned (V % 4 != 0): scalar loads.
@@ -418,7 +454,12 @@ greedy_scalar_kernel(const GreedyArgs g) {
   const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;
   const int n = min(g.chunk_units, g.V - base);
   const int b = (int)(row / g.N);
-  prefetch_tree(g, b);
+  TreeRegs tr{};
+  if (g.N <= kWarpScanMax) {
+    if (tid < 32) tr = load_tree_regs(g, b);
+  } else {
+    prefetch_tree(g, b);
+  }
   ArgMax best{-INFINITY, INT_MAX};
   const float* x = g.logits + row * (long long)g.V + base;
   for (int k = tid; k < n; k += kGreedyThreads) {
@@ -426,7 +467,7 @@ greedy_scalar_kernel(const GreedyArgs g) {
     if (v > best.v) best = {v, base + k};
   }
   if (best.i == INT_MAX) best.i = base;  // only -inf seen: lowest index of the chunk
-  finish_item(g, row, b, best, s_red, &s_last, false, s_scan);
+  finish_item(g, row, b, best, s_red, &s_last, false, s_scan, tr);
 }
 
 // Largest chunk a CTA stages (4 CTAs of this size, plus their static shared
