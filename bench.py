@@ -77,10 +77,10 @@ KERNEL_SOURCES = {
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
-    # attention kernel, cold (9,509,120) + merge kernel with L2 warm (768 + 389,632)
-    "tv_attn_verify": {"sha256": "6dba0f253d24ade2317211855cfb343c0fa46f323b23ca0fcaab92bcb6e05a08", "bytes": 9899520,
+    # attention kernel, cold (9,196,032) + merge kernel with L2 warm (1,280 + 164,864)
+    "tv_attn_verify": {"sha256": "b132124cce3f133a82d1dcbd6b31963764c6c5855455e49e83e1ba63997cd6b9", "bytes": 9362176,
                        "profile": "profiles/attn_verify_llama3-8b-spine60.md"},
-    "tv_accept_greedy": {"sha256": "b5a20f8a7fbc7d8c3f0aae88ea7f6450bcc4b5f6e3ae90fc80e609f80885715e", "bytes": 30823424,
+    "tv_accept_greedy": {"sha256": "a32564354c402d20b7b443e7ca5c4f0102270046fc5301c5a15ebd0c48b1d70b", "bytes": 30822144,
                          "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},
     "tv_tree_build": {"sha256": "7525175311d2e607c52b62e3cebfc56ca5e70ff278fa81af761f2aad43ad32ea", "bytes": 6656,
                       "profile": "profiles/tree_build_kernel_llama3-8b-spine60.md"},
@@ -297,7 +297,14 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
           for k, f in (("step", f_step), ("tv_tree_build", f_tree), ("tv_attn_verify", f_attn),
                        ("tv_accept_" + accept, f_acc))}
     nb = algorithmic_bytes(case)
-    acc_bytes = nb["greedy"] if accept == "greedy" else 8 * B * N * V + 12 * B * N
+    if accept == "greedy":
+        acc_bytes = nb["greedy"]
+    else:
+        # the walk reads the p and q rows of the nodes it visits (the accepted
+        # path, root included) and nothing else; rejections reuse the cached
+        # rows, so the method's minimum is 8 V bytes per visited node
+        visited = int((aouts["accept_len"].to(torch.int64) + 1).sum())
+        acc_bytes = 8 * V * visited + 12 * B * N
     flops = attention_flops(case)
     t_attn = max(nb["attn"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
     t_acc = acc_bytes / (hbm * 1e9) * 1e6
@@ -312,6 +319,7 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
                  else "hbm", "bytes": nb["attn"], "flops": flops, "roofline_us": t_attn,
                  "frac": t_attn / us["tv_attn_verify"]},
         "accept": {"bound": "hbm", "bytes": acc_bytes, "roofline_us": t_acc,
+                   **({} if accept == "greedy" else {"visited_nodes": visited}),
                    "frac": t_acc / us["tv_accept_" + accept]},
         "inputs_resident_mb": resident / 1e6,
         "l2": f"inputs resident, {resident / 1e6:.0f} MB against the {l2 / 1e6:.0f} MB L2",

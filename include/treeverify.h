@@ -134,6 +134,22 @@ tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= TV_MAX_NODES; Lcap >= N.
  */
 size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap);
+/*
+ * tv_attn_plan -- the launch plan tv_attn_verify takes for a shape (the pages
+ * describe no kernels; this reports this library's own choice, for sizing and
+ * testing).  Host only, launches nothing; the choice depends on the shape and
+ * the current device's SM count (152 when no device can be queried).
+ *   info  int32 [4] host out: query rows per CTA (128 or 256), node tiles per
+ *         (sequence, kv head), splits of the key range, CTAs of the attention
+ *         kernel.  With more than one split the merge kernel follows.
+ * The environment variable TV_ATTN_PLAN="rows,splits" (rows 128 or 256,
+ * splits from 1 to min(64, ceil(Lcap / 128))) overrides the choice for every
+ * later call of tv_attn_plan, tv_attn_workspace_size and tv_attn_verify (for
+ * tests and tuning; it is read on every call, so it must not change between
+ * sizing a workspace and the call that uses it).  Other values are ignored.
+ * Returns TV_ERR_INVALID_ARG for an unsupported shape, B = 0 or a NULL info.
+ */
+tv_status tv_attn_plan(int B, int N, int Hq, int Hkv, int D, int Lcap, int32_t* info);
 tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
                          const int32_t* kv_len, const uint64_t* anc_mask, int B, int N,
                          int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,

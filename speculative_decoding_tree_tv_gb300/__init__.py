@@ -13,6 +13,6 @@ from ._lib import (  # noqa: F401
 )
 from .api import (  # noqa: F401
     tree_build, attn_verify, accept_greedy, accept_sample, expand_gated, expand_tree,
-    workspace, attn_workspace_size, greedy_workspace_size, sample_workspace_size,
+    workspace, attn_workspace_size, attn_plan, greedy_workspace_size, sample_workspace_size,
     expand_workspace_size,
 )

@@ -47,6 +47,7 @@ _SIGS = {
     "tv_workspace_clear": (_I, [_P, _SZ, _P]),
     "tv_tree_build": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "tv_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "tv_attn_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "tv_attn_verify": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ,
                             _P]),
     "tv_accept_greedy_workspace_size": (_SZ, [_I, _I, _I]),

@@ -8,7 +8,7 @@ import torch
 from ._lib import TV_MAX_NODES, check, lib
 
 __all__ = ["tree_build", "attn_verify", "accept_greedy", "accept_sample", "expand_gated",
-           "expand_tree", "workspace", "attn_workspace_size", "greedy_workspace_size",
+           "expand_tree", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
            "sample_workspace_size", "expand_workspace_size"]
 
 _workspaces: dict = {}
@@ -52,6 +52,14 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None, device=None):
 
 def attn_workspace_size(B, N, Hq, Hkv, D, Lcap) -> int:
     return int(lib.tv_attn_workspace_size(B, N, Hq, Hkv, D, Lcap))
+
+
+def attn_plan(B, N, Hq, Hkv, D, Lcap) -> dict:
+    """The launch plan tv_attn_verify takes for this shape on the current device."""
+    import ctypes
+    info = (ctypes.c_int32 * 4)()
+    check("tv_attn_plan", lib.tv_attn_plan(B, N, Hq, Hkv, D, Lcap, info))
+    return {"rows_per_cta": info[0], "node_tiles": info[1], "splits": info[2], "ctas": info[3]}
 
 
 def greedy_workspace_size(B, N, V) -> int:

@@ -28,6 +28,8 @@
 // combines the partials of every row.  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cstdio>
+#include <cstdlib>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -765,22 +767,51 @@ struct SplitPlan {
   long long units;  // (sequence, kv head, node tile) triples
 };
 
-// Rough costs in tenths of a microsecond, measured on the kernels: the fixed
-// part of a CTA (setup, first loads, epilogue), its first 128-key tile, each
-// further tile, and the merge kernel.  The period of a 256-row CTA is set by
-// its single K stage (a load per tile on the critical path), that of a
-// 128-row CTA by its two-stage K ring against the load latency.
-constexpr long long kCostFixed = 40, kCostFirst = 20, kCostMerge = 40;
-constexpr long long kCostTile[3] = {0, 15, 27};
+// Rough costs in tenths of a microsecond, fitted to the measured times of
+// forced plans on GB300 over the tiny, Llama-3-8B spine, TALON, ragged-batch
+// and long-context shapes:
+//   * a CTA's fixed part (launch into the SM, setup, the first tile's loads
+//     and compute, epilogue), for 128-row and 256-row CTAs;
+//   * each further 128-key tile.  A 256-row CTA has a single K stage, so each
+//     tile waits for its own K load.  A 128-row CTA pipelines two tiles, but
+//     the L2 serves each kv head's tile once per node tile, and its period
+//     grows with the number of node tiles streaming the same cache;
+//   * the merge kernel: mostly its launch boundary, plus the partial bytes.
+constexpr long long kCostFixed[3] = {0, 43, 54};
+constexpr long long kCostMergeBase = 45;
+constexpr long long kCostMergePer10MB = 5;  // tenths of a microsecond per 10 MB of partials
+
+long long tile_cost(int rbs, int mtiles) {
+  return rbs == 2 ? 28 : 9 + (long long)min(mtiles - 1, 6);
+}
 
 // Choose the CTA height and split count that minimise
 // (waves of CTAs) x (CTA cost) + merge cost, preferring the taller CTA and
 // fewer splits on ties.  One CTA fits an SM (its shared memory decides).
-SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
+// The environment variable TV_ATTN_PLAN="rows,splits" (rows 128 or 256,
+// splits 1 .. min(64, key tiles)) replaces the choice, for tests and tuning;
+// anything else in it is ignored.  It is read on every call.
+bool plan_override(int N, int nb, int tiles_max, SplitPlan& sp) {
+  const char* e = getenv("TV_ATTN_PLAN");
+  int rows = 0, ns = 0;
+  if (!e || sscanf(e, "%d,%d", &rows, &ns) != 2) return false;
+  if ((rows != kRB && rows != 2 * kRB) || ns < 1 || ns > kMaxSplit || ns > tiles_max) return false;
+  sp.rbs = rows / kRB;
+  sp.nb = nb;
+  sp.mtiles = ceil_div(N, sp.rbs * nb);
+  sp.nsplit = ns;
+  return true;
+}
+
+SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap, int D) {
   SplitPlan best_sp{};
   const int G = Hq / Hkv;
   const int nb = kRB / G;
   const int tiles_max = ceil_div(Lcap, kBN);
+  if (plan_override(N, nb, tiles_max, best_sp)) {
+    best_sp.units = (long long)B * Hkv * best_sp.mtiles;
+    return best_sp;
+  }
   const long long slots = device_sm_count();
   long long best = -1;
   for (int rbs = 2; rbs >= 1; --rbs) {
@@ -789,11 +820,15 @@ SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap) {
     sp.nb = nb;
     sp.mtiles = ceil_div(N, rbs * nb);
     sp.units = (long long)B * Hkv * sp.mtiles;
+    const long long tile = tile_cost(rbs, sp.mtiles);
     for (int ns = 1; ns <= kMaxSplit && ns <= tiles_max; ++ns) {
       const long long waves = (sp.units * ns + slots - 1) / slots;
       const long long tiles_per_cta = (tiles_max + ns - 1) / ns;
-      const long long cta = kCostFixed + kCostFirst + (tiles_per_cta - 1) * kCostTile[rbs];
-      const long long cost = waves * cta + (ns > 1 ? kCostMerge : 0);
+      const long long cta = kCostFixed[rbs] + (tiles_per_cta - 1) * tile;
+      const long long part_bytes = sp.units * ns * kRB * rbs * (long long)D * 2;
+      const long long merge =
+          ns > 1 ? kCostMergeBase + kCostMergePer10MB * part_bytes / 10000000ll : 0;
+      const long long cost = waves * cta + merge;
       if (best < 0 || cost < best) {
         best = cost;
         sp.nsplit = ns;
@@ -843,7 +878,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
                       const uint64_t* anc_mask, int B, int N, int Hq, int Hkv, int Lcap,
                       float scale_log2, tv_bf16* out, float* lse, int32_t* status,
                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap);
+  const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap, D);
   const size_t need = plan_workspace(sp, D);
   if (need > 0 && (workspace == nullptr || ws_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255)))
@@ -921,7 +956,17 @@ bool attn_shape_ok(int B, int N, int Hq, int Hkv, int D, int Lcap) {
 
 extern "C" size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap) {
   if (!tv::attn_shape_ok(B, N, Hq, Hkv, D, Lcap) || B == 0) return 0;
-  return tv::plan_workspace(tv::plan_splits(B, N, Hq, Hkv, Lcap), D);
+  return tv::plan_workspace(tv::plan_splits(B, N, Hq, Hkv, Lcap, D), D);
+}
+
+extern "C" tv_status tv_attn_plan(int B, int N, int Hq, int Hkv, int D, int Lcap, int32_t* info) {
+  if (!info || !tv::attn_shape_ok(B, N, Hq, Hkv, D, Lcap) || B == 0) return TV_ERR_INVALID_ARG;
+  const tv::SplitPlan sp = tv::plan_splits(B, N, Hq, Hkv, Lcap, D);
+  info[0] = tv::kRB * sp.rbs;
+  info[1] = sp.mtiles;
+  info[2] = sp.nsplit;
+  info[3] = (int32_t)(sp.units * sp.nsplit);
+  return TV_OK;
 }
 
 extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,

@@ -96,3 +96,44 @@ def test_binding_refuses_cpu_tensors(tvlib):
     parent = torch.tensor([[-1, 0]], dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         tvlib.tree_build(parent)
+
+
+# --------------------------------------------------------------- attention plan
+# Host-only: the plan tv_attn_verify takes for the benchmark shapes (152 SMs,
+# the GB300 count, which is also the fallback when no GPU can be queried).
+PLAN_CASES = {
+    # name: (B, N, Hq, Hkv, D, Lcap) -> (rows per CTA, node tiles, splits)
+    "tiny": ((1, 16, 8, 8, 64, 144), (128, 1, 1)),
+    "llama3-8b spine, 60 nodes": ((1, 60, 32, 8, 128, 2108), (128, 2, 9)),
+    "TALON verify, 512 nodes": ((1, 512, 64, 8, 128, 4608), (256, 16, 1)),
+    "ragged batch of 16": ((16, 64, 32, 8, 128, 8256), (128, 2, 1)),
+    "long context, 256 nodes": ((1, 256, 32, 8, 128, 33024), (256, 4, 9)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLAN_CASES))
+def test_attention_plan_of_the_benchmark_shapes(tvlib, monkeypatch, name):
+    monkeypatch.delenv("TV_ATTN_PLAN", raising=False)
+    shape, (rows, tiles, splits) = PLAN_CASES[name]
+    plan = tvlib.attn_plan(*shape)
+    assert (plan["rows_per_cta"], plan["node_tiles"], plan["splits"]) == (rows, tiles, splits)
+    B, N, Hq, Hkv, D, Lcap = shape
+    assert plan["ctas"] == B * Hkv * tiles * splits
+    # a workspace exactly when the key range is split
+    assert (tvlib.attn_workspace_size(*shape) > 0) == (splits > 1)
+
+
+def test_attention_plan_override(tvlib, monkeypatch):
+    shape = (1, 60, 32, 8, 128, 2108)  # 17 key tiles
+    monkeypatch.setenv("TV_ATTN_PLAN", "256,3")
+    assert tvlib.attn_plan(*shape) == {"rows_per_cta": 256, "node_tiles": 1, "splits": 3,
+                                       "ctas": 24}
+    assert tvlib.attn_workspace_size(*shape) == 3 * 8 * 256 * 128 * 2 + 3 * 8 * 256 * 8
+    for bad in ("256,18", "64,2", "128,0", "junk", "128"):  # ignored: the model decides
+        monkeypatch.setenv("TV_ATTN_PLAN", bad)
+        assert tvlib.attn_plan(*shape)["splits"] == 9
+    monkeypatch.delenv("TV_ATTN_PLAN")
+    with pytest.raises(tvlib.TVError):
+        tvlib.attn_plan(0, 60, 32, 8, 128, 2108)
+    with pytest.raises(tvlib.TVError):
+        tvlib.attn_plan(1, 60, 32, 8, 96, 2108)

@@ -77,6 +77,25 @@ def test_attention_full(tv, oracle_mod, seed, B, N, L, Hq, Hkv, D, tree):
     full_check(tv, oracle_mod, case, f"case{seed}")
 
 
+@pytest.mark.parametrize("plan", ["128,1", "128,4", "256,1", "256,3"])
+@pytest.mark.parametrize("seed,B,N,L,Hq,Hkv,D,tree", [
+    (31, 1, 60, 700, 32, 8, 128, "spine60"),    # two row blocks of 32 nodes each
+    (32, 2, 20, (100, 900), 8, 2, 64, "random"),  # 256-row CTAs with an empty second block
+    (33, 1, 130, 300, 4, 1, 64, "random"),      # three node tiles, the last one ragged
+])
+def test_attention_every_plan_kind(tv, oracle_mod, monkeypatch, plan, seed, B, N, L, Hq, Hkv, D,
+                                   tree):
+    """Both CTA heights, with and without a split key range (and so with and
+    without the merge kernel), forced through TV_ATTN_PLAN and compared row by
+    row with the oracle."""
+    monkeypatch.setenv("TV_ATTN_PLAN", plan)
+    case = gen.make_case(seed, B=B, N=N, L=L, Hq=Hq, Hkv=Hkv, D=D, V=64, tree=tree, max_depth=12)
+    rows, splits = (int(x) for x in plan.split(","))
+    got = tv.attn_plan(B, N, Hq, Hkv, D, case.Lcap)
+    assert (got["rows_per_cta"], got["splits"]) == (rows, splits)
+    full_check(tv, oracle_mod, case, f"case{seed}-plan{plan}")
+
+
 def test_explicit_scale(tv, oracle_mod):
     case = gen.make_case(20, B=1, N=24, L=200, Hq=8, Hkv=4, D=64, V=64)
     full_check(tv, oracle_mod, case, "scale", scale=0.05)
