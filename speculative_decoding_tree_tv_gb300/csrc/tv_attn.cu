@@ -52,10 +52,12 @@ constexpr int kMaxSplit = 64;         // splits of one CTA's key range
 // two loads wait on different barriers, so each has a warp of its own).  Two row
 // blocks share every K/V tile (the cache is streamed once per kv head); one
 // row block gives twice the CTAs.  Both fill 224 KB of shared memory (D = 128):
-//   two row blocks: Q 64 KB, one P buffer 64 KB, one K stage, two V stages;
+//   two row blocks: Q 64 KB, one P buffer 64 KB, two K stages, one V stage;
 //   one row block:  Q 32 KB, two P buffers, two K stages, two V stages.
-// The second V stage takes the V load off the PV critical path; the second P
-// buffer lets the softmax of tile t + 1 run while PV(t) still reads P(t).
+// Two K stages let S(t + 1) run during the softmax of tile t; with one V
+// stage, V(t + 1) loads once both PV(t) retired, and the softmax of t + 1
+// covers part of that load.  The second P buffer lets the softmax of tile
+// t + 1 run while PV(t) still reads P(t).
 // One row block also double-buffers S in TMEM, so that S(t + 1) is computed
 // while the softmax of tile t still reads S(t).
 // TMEM: S of (row block r, buffer u) at column 128 (r kSBufs + u), O_r at
@@ -67,8 +69,8 @@ struct Shape {
   static constexpr int kProducerWarp = RBS * 4;  // K loads
   static constexpr int kMmaWarp = RBS * 4 + 1;
   static constexpr int kVProducerWarp = RBS * 4 + 2;
-  static constexpr int kKStages = (RBS == 1) ? 2 : 1;
-  static constexpr int kVStages = 2;
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = (RBS == 1) ? 2 : 1;
   static constexpr int kPBufs = (RBS == 1) ? 2 : 1;
   static constexpr int kSBufs = (RBS == 1) ? 2 : 1;
   static constexpr uint32_t kTmemCols = 512u;
@@ -265,7 +267,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int a = 0; a < A; ++a)
           tma_load_3d(sQ + (r * A + a) * kAtomBytes, &tmQ, &bar_q, a * 64, kvh * G,
                       b * N + node0 + r * nb);
-      for (int t = 0; t < preV; ++t) {
+      for (int t = 0; t < max(preK, preV); ++t) {
         if (t < preK) {
           mbar_expect_tx(&bar_k_full[t], Lay::kTile);
 #pragma unroll
@@ -273,11 +275,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             tma_load_2d(sK + t * Lay::kTile + a * kAtomBytes, &tmK, &bar_k_full[t], a * 64,
                         y0 + t * kBN);
         }
-        mbar_expect_tx(&bar_v_full[t], Lay::kTile);
+        if (t < preV) {
+          mbar_expect_tx(&bar_v_full[t], Lay::kTile);
 #pragma unroll
-        for (int a = 0; a < A; ++a)
-          tma_load_2d(sV + t * Lay::kTile + a * kAtomBytes, &tmV, &bar_v_full[t], a * 64,
-                      y0 + t * kBN);
+          for (int a = 0; a < A; ++a)
+            tma_load_2d(sV + t * Lay::kTile + a * kAtomBytes, &tmV, &bar_v_full[t], a * 64,
+                        y0 + t * kBN);
+        }
       }
     }
   }
@@ -772,8 +776,8 @@ struct SplitPlan {
 // and long-context shapes:
 //   * a CTA's fixed part (launch into the SM, setup, the first tile's loads
 //     and compute, epilogue), for 128-row and 256-row CTAs;
-//   * each further 128-key tile.  A 256-row CTA has a single K stage, so each
-//     tile waits for its own K load.  A 128-row CTA pipelines two tiles, but
+//   * each further 128-key tile.  A 256-row CTA has a single V stage, so each
+//     tile's PV waits for its own V load.  A 128-row CTA pipelines two tiles, but
 //     the L2 serves each kv head's tile once per node tile, and its period
 //     grows with the number of node tiles streaming the same cache;
 //   * the merge kernel: mostly its launch boundary, plus the partial bytes.
@@ -782,7 +786,7 @@ constexpr long long kCostMergeBase = 45;
 constexpr long long kCostMergePer10MB = 5;  // tenths of a microsecond per 10 MB of partials
 
 long long tile_cost(int rbs, int mtiles) {
-  return rbs == 2 ? 28 : 9 + (long long)min(mtiles - 1, 6);
+  return rbs == 2 ? 26 : 9 + (long long)min(mtiles - 1, 6);
 }
 
 // Choose the CTA height and split count that minimise

@@ -5,20 +5,30 @@
 //
 // One launch: a thread-block cluster of 8 CTAs (16 for vocabularies above
 // 204,800) per sequence walks that sequence's tree.  CTA `rank` owns a slice
-// of the vocabulary and keeps, for the node being visited, the slice of p and
-// q in shared memory.  Visiting a node loads its two rows once (16-byte
-// loads, all in flight), forms the softmax normalisers from cluster-wide
-// maxima and sums, and turns the cached slice into probabilities; every
-// rejection is then one in-place update of the cached residual, and the
-// final draw an inverse-CDF search across the cluster.  Only the rows of the
-// nodes the walk visits are ever read.
+// of the vocabulary and keeps, for the node being visited, its slice of the p
+// and q rows in shared memory, token-major; thread t owns the float4 groups
+// t, t + 512, t + 1024, ... of the slice, so global and shared accesses are
+// both contiguous across a warp.  A visit
+//   * brings the node's two row slices in by bulk copies (rows 16-byte
+//     aligned; plain coalesced loads otherwise) and asks the L2 for the first
+//     child's slices, the likeliest next visit;
+//   * forms the softmax normalisers with one cluster exchange: every CTA
+//     publishes its slice's (max, sum of exp(x - max)) and each combines the
+//     pairs in rank order;
+//   * scales its slice to probabilities and computes, in parallel, p(x) and
+//     q(x) of every child's token in fp64 for the accept tests;
+//   * tests the children in index order; a rejection is one pass that sums
+//     (r - q)+ over the slice (the update of r itself is applied lazily by
+//     the next pass) and one cluster exchange of the sums.
+// The final draw sums the residual per (round, warp) segment of 128 tokens,
+// exchanges the slices' masses, and only the CTA holding the target searches
+// it: segment, then lane, then the lane's four tokens, replayed in fp64.
 //
-// All CTAs of a cluster take the same decisions from the same inputs (the
-// accept tests in fp64 by each CTA's thread 0, the normalisers from sums
-// combined in rank order), so they follow the same walk; sums over a row are
-// exchanged through distributed shared memory, one cluster barrier each.
-// Element values are fp32 (expf); every sum is carried in fp64 across
-// threads and CTAs and every decision (accept test, draw) is taken in fp64.
+// All CTAs of a cluster take the same decisions from the same inputs (accept
+// tests by each CTA's thread 0 from the exchanged normalisers; the draw's
+// owner from the exchanged masses), so they follow the same walk.  Element
+// values are fp32; sums across threads are compensated fp32 pairs (TwoSum),
+// across CTAs fp64 in rank order; every decision is taken in fp64.
 #include <climits>
 
 #include "tv_common.cuh"
@@ -28,37 +38,28 @@ namespace tv {
 namespace {
 
 constexpr int kWalkThreads = 512;
+constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxRejects = kMaxNodes;
-constexpr size_t kWalkCacheMax = 200 * 1024;  // shared memory for the cached slice
+constexpr int kMaxRounds = 16;                // float4 groups per thread and row slice
+constexpr size_t kWalkCacheMax = 200 * 1024;  // shared memory for the two row slices
 
-// Vocabulary slice of a CTA and its per-thread runs, so that (rank, thread)
-// order is token order: slice [rank * S, (rank + 1) * S), thread t the P
-// tokens [t * P, (t + 1) * P) of it; S and P multiples of 4.
-struct Slicing {
-  int S, P;
-};
-__host__ __device__ inline Slicing slicing(int V, int cluster) {
-  Slicing s;
-  s.S = ((ceil_div(V, cluster) + 3) / 4) * 4;
-  s.P = ((ceil_div(s.S, kWalkThreads) + 3) / 4) * 4;
-  return s;
+// Tokens in the slice of each CTA (a multiple of 4): CTA `rank` owns
+// [rank * S, min(V, (rank + 1) * S)).
+__host__ __device__ inline int slice_len(int V, int cluster) {
+  return ((ceil_div(V, cluster) + 3) / 4) * 4;
 }
 __host__ __device__ inline size_t cache_bytes(int V, int cluster) {
-  return (size_t)2 * slicing(V, cluster).P * kWalkThreads * sizeof(float);
+  return (size_t)2 * slice_len(V, cluster) * sizeof(float);
 }
-// 8 CTAs per tree when the cache fits, else 16, else 0 (unsupported).
+// 8 CTAs per tree when the slices fit, else 16, else 0 (unsupported).
 inline int walk_cluster(int V) {
-  if (cache_bytes(V, 8) <= kWalkCacheMax) return 8;
-  if (cache_bytes(V, 16) <= kWalkCacheMax) return 16;
+  for (int cl = 8; cl <= kMaxCluster; cl *= 2)
+    if (cache_bytes(V, cl) <= kWalkCacheMax &&
+        ceil_div(slice_len(V, cl) / 4, kWalkThreads) <= kMaxRounds)
+      return cl;
   return 0;
 }
-
-struct RowNorm {
-  float m;       // row max of logit / T
-  float inv_s;   // 1 / sum exp(a - m), rounded to fp32
-  double s;      // sum exp(a - m)
-};
 
 // Sums across threads as unevaluated pairs hi + lo of fp32 values, each
 // addition exact up to the last bits of lo (Knuth's TwoSum), so about twice
@@ -75,88 +76,50 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
   const float hi = s + e;
   return DF{hi, e - (hi - s)};
 }
-__device__ __forceinline__ DF df_of(const KahanF& k) {  // k.s - k.c
-  return df_add(DF{k.s, 0.0f}, DF{-k.c, 0.0f});
-}
+__device__ __forceinline__ double df_val(DF a) { return (double)a.hi + (double)a.lo; }
 __device__ __forceinline__ DF df_shfl_xor(DF a, int o) {
   return DF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
 }
 __device__ __forceinline__ DF df_shfl_up(DF a, int o) {
   return DF{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
 }
-
-// Block-wide sum over kWalkThreads threads (fixed order); every thread gets
-// the result as a double.
-__device__ double block_sum_df(DF v, DF* scratch, double* out) {
+__device__ __forceinline__ DF warp_sum_df(DF v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
-  const int tid = threadIdx.x;
-  __syncthreads();
-  if ((tid & 31) == 0) scratch[tid >> 5] = v;
-  __syncthreads();
-  if (tid < 32) {
-    DF w = (tid < kWalkThreads / 32) ? scratch[tid] : DF{0.0f, 0.0f};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) w = df_add(w, df_shfl_xor(w, o));
-    if (tid == 0) *out = (double)w.hi + (double)w.lo;
-  }
-  __syncthreads();
-  return *out;
+  return v;
 }
-__device__ float block_max_f(float v, float* scratch) {
-  v = warp_max(v);
-  const int tid = threadIdx.x;
-  __syncthreads();
-  if ((tid & 31) == 0) scratch[tid >> 5] = v;
-  __syncthreads();
-  if (tid < 32) {
-    float w = (tid < kWalkThreads / 32) ? scratch[tid] : -INFINITY;
-    w = warp_max(w);
-    if (tid == 0) scratch[32] = w;
+// Inclusive prefix over the lanes of a warp.
+__device__ __forceinline__ DF warp_scan_df(DF v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y = df_shfl_up(v, o);
+    if (lane >= o) v = df_add(v, y);
   }
-  __syncthreads();
-  return scratch[32];
+  return v;
 }
 
-// Loads this thread's tokens [t0, t1) of a row pair and calls
-// fn(k, p_logit, q_logit) with k = index of the token in the run, up to 32
-// tokens per round with every load of the round in flight (16-byte loads when
-// the rows are 16-byte aligned; t0 is then a multiple of 4).
-template <class Fn>
-__device__ __forceinline__ void load_run(const float* prow, const float* qrow, int t0, int t1,
-                                         bool vec, Fn&& fn) {
-  constexpr int kTile = 32;
-  for (int base = t0; base < t1; base += kTile) {
-    float pa[kTile], qa[kTile];
-    if (vec) {
-#pragma unroll
-      for (int u = 0; u < kTile / 4; ++u) {
-        const int e = base + 4 * u;
-        const float4 x = (e < t1) ? ld_stream_f4(reinterpret_cast<const float4*>(prow + e))
-                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        const float4 y = (e < t1) ? ld_stream_f4(reinterpret_cast<const float4*>(qrow + e))
-                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        pa[4 * u] = x.x; pa[4 * u + 1] = x.y; pa[4 * u + 2] = x.z; pa[4 * u + 3] = x.w;
-        qa[4 * u] = y.x; qa[4 * u + 1] = y.y; qa[4 * u + 2] = y.z; qa[4 * u + 3] = y.w;
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < kTile; ++u) {
-        const int e = base + u;
-        pa[u] = (e < t1) ? __ldg(prow + e) : 0.0f;
-        qa[u] = (e < t1) ? __ldg(qrow + e) : 0.0f;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kTile; ++u)
-      if (base + u < t1) fn(base + u - t0, pa[u], qa[u]);
-  }
+// exp(d) in fp64 to about fp32 relative precision over the whole fp64 range:
+// d log2(e) = n + f with n an integer and f in [0, 1), 2^f by exp2f, 2^n
+// exactly by ldexp (so tiny probabilities do not underflow as fp32 would).
+__device__ __forceinline__ double exp_wide(double d) {
+  if (d == -INFINITY) return 0.0;
+  const double t = d * 1.4426950408889634;
+  const double n = floor(t);
+  return ldexp((double)exp2f((float)(t - n)), (int)fmax(n, -1100.0));
 }
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
+}
+__device__ __forceinline__ void dsmem_st_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Ask the L2 for `bytes` (a multiple of 16, 16-byte aligned) of global memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __global__ void __launch_bounds__(kWalkThreads)
@@ -166,48 +129,50 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
             uint64_t offset, int32_t* __restrict__ accept_len, int32_t* __restrict__ end_node,
             int32_t* __restrict__ path, int32_t* __restrict__ out_token,
             int32_t* __restrict__ status) {
-  // this CTA's slice of the visited node's rows, [2][P][kWalkThreads]:
-  // p-side (logit / T, then the residual r) and q-side (logit / T, then q),
-  // element-major so that the threads of a warp hit distinct banks
-  extern __shared__ float s_cache[];
-  __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes];
-  __shared__ int32_t s_first[kMaxNodes], s_next[kMaxNodes];  // children lists, index order
-  __shared__ int32_t s_kids[kMaxNodes];                      // children of the visited node
-  __shared__ float s_kp[kMaxNodes], s_kq[kMaxNodes];         // their tokens' logits
-  __shared__ int s_nkids;
-  __shared__ RowNorm s_pn, s_qn;
+  // this CTA's slices of the visited node's rows, token-major: p side (logit,
+  // then probability, then residual), then q side
+  extern __shared__ __align__(16) float s_cache[];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes], s_kids[kMaxNodes];
+  __shared__ double s_kpx[kMaxNodes], s_kqx[kMaxNodes];  // p(x), q(x) of each child's token
   __shared__ float s_invz[kMaxRejects];
-  __shared__ double s_red[33];
-  __shared__ DF s_redd[kWalkThreads / 32];
-  __shared__ DF s_scan[kWalkThreads / 32];
-  __shared__ float s_redf[33];
-  __shared__ int s_found, s_last_pos;
+  __shared__ int s_wcount[kWalkWarps];
+  __shared__ float s_wmax[2][kWalkWarps];
+  __shared__ DF s_wsum[2][kWalkWarps];
+  __shared__ DF s_seg[kMaxRounds * kWalkWarps];      // draw: mass of each 128-token segment
+  __shared__ DF s_segbase[kMaxRounds * kWalkWarps];  // and the mass before it in the slice
+  __shared__ double s_norm[4];  // 1/S_p, 1/S_q, M_p, M_q
+  __shared__ float s_scale[2];  // this slice's factors exp(m - M) / S
+  __shared__ double s_lt;       // draw: target minus the mass before this slice (owner only)
+  __shared__ int s_found, s_zpos, s_last, s_seg_pick, s_result;
+  __shared__ int s_err;
   // what this CTA shows the cluster: two phases, so that writing the next
   // value never races with another CTA still reading the previous one
-  __shared__ double s_pub_d[2][2];
+  __shared__ double s_pub_d[2][4];
   __shared__ int s_pub_i[2];
-  __shared__ double s_all_d[kMaxCluster][2];
+  __shared__ double s_all_d[kMaxCluster][4];
   __shared__ int s_all_i[kMaxCluster];
   pdl_trigger();
   pdl_wait();
   const int cl = (int)cluster_nctarank();
   const int rank = (int)sm100::cluster_ctarank();
   const int b = blockIdx.x / cl;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int phase = 0;
-  // publish (d0, d1, i), wait for the cluster, read everyone's in rank order
-  auto exchange = [&](double d0, double d1, int i) {
+  // publish (d0..d3, i), wait for the cluster, read everyone's in rank order
+  auto exchange = [&](double d0, double d1, double d2, double d3, int i) {
     if (tid == 0) {
       s_pub_d[phase][0] = d0;
       s_pub_d[phase][1] = d1;
+      s_pub_d[phase][2] = d2;
+      s_pub_d[phase][3] = d3;
       s_pub_i[phase] = i;
     }
     sm100::cluster_sync();
-    if (tid < cl) {
-      const uint32_t a = sm100::dsmem_map(sm100::smem_u32(&s_pub_d[phase][0]), tid);
-      s_all_d[tid][0] = sm100::dsmem_ld_f64(a);
-      s_all_d[tid][1] = sm100::dsmem_ld_f64(a + 8);
-      s_all_i[tid] = sm100::dsmem_ld_s32(sm100::dsmem_map(sm100::smem_u32(&s_pub_i[phase]), tid));
+    if (tid < 4 * cl) {
+      const int r = tid >> 2, k = tid & 3;
+      s_all_d[r][k] = sm100::dsmem_ld_f64(sm100::dsmem_map(sm100::smem_u32(&s_pub_d[phase][k]), r));
+      if (k == 0) s_all_i[r] = sm100::dsmem_ld_s32(sm100::dsmem_map(sm100::smem_u32(&s_pub_i[phase]), r));
     }
     __syncthreads();
     phase ^= 1;
@@ -215,6 +180,11 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
 
   const int32_t* par = parent + (size_t)b * N;
   const int32_t* tok = tokens + (size_t)b * N;
+  if (tid == 0) {
+    sm100::mbar_init(&s_bar, 1);
+    sm100::mbar_fence_init();
+    s_err = 0;
+  }
   int bad_tree = 0, bad_tok = 0;
   for (int i = tid; i < N; i += kWalkThreads) {
     const int p = par[i];
@@ -241,219 +211,366 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     return;
   }
 
-  if (tid == 0) {
-    for (int i = 0; i < N; ++i) s_first[i] = -1;
-    for (int c = N - 1; c >= 1; --c) {
-      s_next[c] = s_first[s_par[c]];
-      s_first[s_par[c]] = c;
-    }
-  }
-  __syncthreads();
-
-  const bool vec = (V & 3) == 0;
-  const Slicing sl = slicing(V, cl);
-  const int s_lo = min(V, rank * sl.S), s_hi = min(V, s_lo + sl.S);
-  const int t0 = min(s_hi, s_lo + tid * sl.P), t1 = min(s_hi, t0 + sl.P);
-  const int nmine = t1 - t0;
-  float* s_r = s_cache;
-  float* s_q = s_cache + (size_t)sl.P * kWalkThreads;
-  auto at = [&](int k) { return (size_t)k * kWalkThreads + tid; };
+  const bool bulk = (V & 3) == 0;
+  const int S = slice_len(V, cl);
+  const int s_lo = min(V, rank * S), s_hi = min(V, s_lo + S);
+  const int n4 = (s_hi - s_lo + 3) / 4;  // float4 groups; a ragged last one is padded
+  const int rounds = ceil_div(n4, kWalkThreads);
+  float4* const c_p = reinterpret_cast<float4*>(s_cache);
+  float4* const c_q = reinterpret_cast<float4*>(s_cache + S);
+  const uint32_t slice_bytes = (uint32_t)(s_hi - s_lo) * 4u;
+  uint32_t bar_parity = 0;
 
   int node = 0;
   int result = -1;
   for (;;) {
     const float* prow = p_logits + ((size_t)b * N + node) * V;
     const float* qrow = q_logits + ((size_t)b * N + node) * V;
-    // ---- visit: the children's logits for the accept tests, fetched while the
-    // slice loads; softmax normalisers from cluster-wide maxima and sums
-    if (tid == 0) {
-      int n = 0;
-      for (int c = s_first[node]; c >= 0; c = s_next[c]) s_kids[n++] = c;
-      s_nkids = n;
+    // ---- the node's two row slices into shared memory (every thread's
+    // reads of the previous visit's slices are ordered before the copy)
+    sm100::fence_async_smem();
+    __syncthreads();
+    if (bulk) {
+      if (tid == 0 && slice_bytes > 0) {
+        sm100::mbar_expect_tx(&s_bar, 2u * slice_bytes);
+        sm100::bulk_load_global(c_p, prow + s_lo, slice_bytes, &s_bar);
+        sm100::bulk_load_global(c_q, qrow + s_lo, slice_bytes, &s_bar);
+      }
+    } else {
+      float* cp = s_cache;
+      float* cq = s_cache + S;
+      for (int k = tid; k < 4 * n4; k += kWalkThreads) {
+        const int t = s_lo + k;
+        cp[k] = (t < s_hi) ? __ldg(prow + t) : -INFINITY;
+        cq[k] = (t < s_hi) ? __ldg(qrow + t) : -INFINITY;
+      }
+    }
+    // ---- the children, in index order (one per thread: N <= kWalkThreads)
+    const bool is_kid = tid > node && tid < N && s_par[tid] == node;
+    const unsigned kb = __ballot_sync(0xffffffffu, is_kid);
+    if (lane == 0) s_wcount[warp] = __popc(kb);
+    __syncthreads();
+    int before = 0, nkids = 0;
+#pragma unroll
+    for (int w = 0; w < kWalkWarps; ++w) {
+      before += (w < warp) ? s_wcount[w] : 0;
+      nkids += s_wcount[w];
+    }
+    if (is_kid) s_kids[before + __popc(kb & ((1u << lane) - 1u))] = tid;
+    __syncthreads();
+    float kp = 0.0f, kq = 0.0f;
+    if (tid < nkids) {  // the children's tokens' logits, for the accept tests
+      const int x = tok[s_kids[tid]];
+      kp = __ldg(prow + x) * inv_t;
+      kq = __ldg(qrow + x) * inv_t;
+    }
+    if (bulk && tid == 0 && nkids > 0 && slice_bytes > 0) {  // the likeliest next visit
+      const size_t row1 = (size_t)b * N + s_kids[0];
+      prefetch_l2_bulk(p_logits + row1 * V + s_lo, slice_bytes);
+      prefetch_l2_bulk(q_logits + row1 * V + s_lo, slice_bytes);
+    }
+    if (bulk && slice_bytes > 0) {
+      bool ok = sm100::mbar_wait(&s_bar, bar_parity);
+      if (!ok) ok = sm100::mbar_wait(&s_bar, bar_parity);  // a copy must not outlive the CTA
+      if (!ok) s_err = 1;
+      bar_parity ^= 1u;
+    } else {
+      __syncthreads();
+    }
+    // ---- slice maxima of logit / T (inv_t > 0 keeps the order, so the
+    // maximum of the scaled values is the scaled maximum)
+    float mp = -INFINITY, mq = -INFINITY;
+#pragma unroll 4
+    for (int j = 0; j < rounds; ++j) {
+      const int f = tid + j * kWalkThreads;
+      if (f < n4) {
+        const float4 a = c_p[f], c = c_q[f];
+        mp = fmaxf(mp, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+        mq = fmaxf(mq, fmaxf(fmaxf(c.x, c.y), fmaxf(c.z, c.w)));
+      }
+    }
+    mp = warp_max(mp) * inv_t;
+    mq = warp_max(mq) * inv_t;
+    if (lane == 0) {
+      s_wmax[0][warp] = mp;
+      s_wmax[1][warp] = mq;
     }
     __syncthreads();
-    const int nkids = s_nkids;
-    for (int j = tid; j < nkids; j += kWalkThreads) {
-      const int x = tok[s_kids[j]];
-      s_kp[j] = __ldg(prow + x);
-      s_kq[j] = __ldg(qrow + x);
+    mp = -INFINITY;
+    mq = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWalkWarps; ++w) {
+      mp = fmaxf(mp, s_wmax[0][w]);
+      mq = fmaxf(mq, s_wmax[1][w]);
     }
-    float mp = -INFINITY, mq = -INFINITY;
-    load_run(prow, qrow, t0, t1, vec, [&](int k, float a, float bq) {
-      const float x = a * inv_t, y = bq * inv_t;
-      s_r[at(k)] = x;
-      s_q[at(k)] = y;
-      mp = fmaxf(mp, x);
-      mq = fmaxf(mq, y);
-    });
-    mp = block_max_f(mp, s_redf);
-    mq = block_max_f(mq, s_redf);
-    exchange((double)mp, (double)mq, 0);
-    float Mp = -INFINITY, Mq = -INFINITY;
-    for (int r = 0; r < cl; ++r) {
-      Mp = fmaxf(Mp, (float)s_all_d[r][0]);
-      Mq = fmaxf(Mq, (float)s_all_d[r][1]);
+    // ---- exp(x - slice max), kept in place; sums per thread, then per CTA
+    float sp = 0.0f, sq = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < rounds; ++j) {
+      const int f = tid + j * kWalkThreads;
+      if (f < n4) {
+        float4 a = c_p[f], c = c_q[f];
+        a = make_float4(expf(a.x * inv_t - mp), expf(a.y * inv_t - mp), expf(a.z * inv_t - mp),
+                        expf(a.w * inv_t - mp));
+        c = make_float4(expf(c.x * inv_t - mq), expf(c.y * inv_t - mq), expf(c.z * inv_t - mq),
+                        expf(c.w * inv_t - mq));
+        c_p[f] = a;
+        c_q[f] = c;
+        sp += (a.x + a.y) + (a.z + a.w);
+        sq += (c.x + c.y) + (c.z + c.w);
+      }
     }
-    // exponentials once, kept in the cache; their sums
-    KahanF sp, sq;
-    for (int k = 0; k < nmine; ++k) {
-      const float ep = expf(s_r[at(k)] - Mp), eq = expf(s_q[at(k)] - Mq);
-      s_r[at(k)] = ep;
-      s_q[at(k)] = eq;
-      sp.add(ep);
-      sq.add(eq);
+    {
+      const DF wp = warp_sum_df(DF{sp, 0.0f}), wq = warp_sum_df(DF{sq, 0.0f});
+      if (lane == 0) {
+        s_wsum[0][warp] = wp;
+        s_wsum[1][warp] = wq;
+      }
     }
-    const double sp_cta = block_sum_df(df_of(sp), s_redd, &s_red[32]);
-    const double sq_cta = block_sum_df(df_of(sq), s_redd, &s_red[32]);
-    exchange(sp_cta, sq_cta, 0);
-    if (tid == 0) {  // fp64 runs at a small fraction of the fp32 rate: once per CTA
+    __syncthreads();
+    DF tp{0.0f, 0.0f}, tq{0.0f, 0.0f};
+    if (tid == 0)
+      for (int w = 0; w < kWalkWarps; ++w) {
+        tp = df_add(tp, s_wsum[0][w]);
+        tq = df_add(tq, s_wsum[1][w]);
+      }
+    // ---- one exchange: every slice's (max, sum); normalisers in rank order
+    exchange((double)mp, df_val(tp), (double)mq, df_val(tq), 0);
+    if (tid == 0) {
+      float Mp = -INFINITY, Mq = -INFINITY;
+      for (int r = 0; r < cl; ++r) {
+        Mp = fmaxf(Mp, (float)s_all_d[r][0]);
+        Mq = fmaxf(Mq, (float)s_all_d[r][2]);
+      }
       double Sp = 0.0, Sq = 0.0;
       for (int r = 0; r < cl; ++r) {
-        Sp += s_all_d[r][0];
-        Sq += s_all_d[r][1];
+        if (s_all_d[r][1] > 0.0) Sp += s_all_d[r][1] * (double)expf((float)s_all_d[r][0] - Mp);
+        if (s_all_d[r][3] > 0.0) Sq += s_all_d[r][3] * (double)expf((float)s_all_d[r][2] - Mq);
       }
-      s_pn = RowNorm{Mp, (float)(1.0 / Sp), Sp};
-      s_qn = RowNorm{Mq, (float)(1.0 / Sq), Sq};
+      const double ip = 1.0 / Sp, iq = 1.0 / Sq;
+      s_norm[0] = ip;
+      s_norm[1] = iq;
+      s_norm[2] = (double)Mp;
+      s_norm[3] = (double)Mq;
+      s_scale[0] = (mp == -INFINITY) ? 0.0f : (float)((double)expf(mp - Mp) * ip);
+      s_scale[1] = (mq == -INFINITY) ? 0.0f : (float)((double)expf(mq - Mq) * iq);
     }
     __syncthreads();
-    const RowNorm pn = s_pn, qn = s_qn;
-    // the slice as probabilities: r = p, q
-    for (int k = 0; k < nmine; ++k) {
-      s_r[at(k)] *= pn.inv_s;
-      s_q[at(k)] *= qn.inv_s;
-    }
-    int n_rej = 0;    // residual normalisations so far
-    int applied = 0;  // of them applied to s_r
-    // calls fn(token, r, q) for this thread's tokens in token order, r brought
-    // up to date (n_rej updates r <- (r - q)+ / Z_j)
-    auto visit = [&](auto&& fn) {
-      for (int k = 0; k < nmine; ++k) {
-        float r = s_r[at(k)];
-        const float q = s_q[at(k)];
-        if (applied < n_rej) {
-          for (int j = applied; j < n_rej; ++j) r = fmaxf(r - q, 0.0f) * s_invz[j];
-          s_r[at(k)] = r;
+    // ---- the slice as probabilities r = p, q; the children's p(x), q(x) in fp64
+    {
+      const float cp = s_scale[0], cq = s_scale[1];
+#pragma unroll 4
+      for (int j = 0; j < rounds; ++j) {
+        const int f = tid + j * kWalkThreads;
+        if (f < n4) {
+          const float4 a = c_p[f], c = c_q[f];
+          c_p[f] = make_float4(a.x * cp, a.y * cp, a.z * cp, a.w * cp);
+          c_q[f] = make_float4(c.x * cq, c.y * cq, c.z * cq, c.w * cq);
         }
-        fn(t0 + k, r, q);
       }
-      applied = n_rej;
+    }
+    if (tid < nkids) {
+      s_kpx[tid] = exp_wide((double)kp - s_norm[2]) * s_norm[0];
+      s_kqx[tid] = exp_wide((double)kq - s_norm[3]) * s_norm[1];
+    }
+    __syncthreads();
+
+    int n_rej = 0;    // residual normalisations so far
+    int applied = 0;  // of them applied to the p side of the cache
+    // the residual r of group f with every pending normalisation applied
+    // (r <- (r - q)+ / Z_j), stored back when one was pending
+    auto residual = [&](int f) {
+      float4 r = c_p[f];
+      if (applied < n_rej) {
+        const float4 q = c_q[f];
+        for (int j = applied; j < n_rej; ++j) {
+          const float z = s_invz[j];
+          r = make_float4(fmaxf(r.x - q.x, 0.0f) * z, fmaxf(r.y - q.y, 0.0f) * z,
+                          fmaxf(r.z - q.z, 0.0f) * z, fmaxf(r.w - q.w, 0.0f) * z);
+        }
+        c_p[f] = r;
+      }
+      return r;
     };
     int accepted = -1;
-    int ordinal = 0;
     for (int kid = 0; kid < nkids; ++kid) {
-      const int c = s_kids[kid];
-      // accept test in fp64 on the single token x
+      // accept test in fp64 on the child's token x
       if (tid == 0) {
-        const double ax = (double)(s_kp[kid] * inv_t);
-        const double bx = (double)(s_kq[kid] * inv_t);
-        double r = exp(ax - (double)pn.m) / pn.s;
-        const double qx = exp(bx - (double)qn.m) / qn.s;
+        double r = s_kpx[kid];
+        const double qx = s_kqx[kid];
         for (int j = 0; j < n_rej; ++j) r = fmax(r - qx, 0.0) * (double)s_invz[j];
-        const double u = decision_uniform(seed, offset, b, node, 0u, (uint32_t)ordinal);
+        const double u = decision_uniform(seed, offset, b, node, 0u, (uint32_t)kid);
         s_found = (qx == 0.0) || (u < r / qx);
       }
       __syncthreads();
       if (s_found) {
-        accepted = c;
+        accepted = s_kids[kid];
         break;
       }
       // rejection: Z = sum_t (r(t) - q(t))+ over the row, from every CTA's slice
-      KahanF acc;
-      visit([&](int, float r, float q) { acc.add(fmaxf(r - q, 0.0f)); });
-      const double zc = block_sum_df(df_of(acc), s_redd, &s_red[32]);
-      exchange(zc, 0.0, 0);
-      double z = 0.0;
-      for (int r = 0; r < cl; ++r) z += s_all_d[r][0];
-      if (z > 0.0 && n_rej < kMaxRejects) {
-        if (tid == 0) s_invz[n_rej] = (float)(1.0 / z);
-        ++n_rej;
+      float zs = 0.0f;
+#pragma unroll 4
+      for (int j = 0; j < rounds; ++j) {
+        const int f = tid + j * kWalkThreads;
+        if (f < n4) {
+          const float4 r = residual(f), q = c_q[f];
+          zs += (fmaxf(r.x - q.x, 0.0f) + fmaxf(r.y - q.y, 0.0f)) +
+                (fmaxf(r.z - q.z, 0.0f) + fmaxf(r.w - q.w, 0.0f));
+        }
+      }
+      applied = n_rej;
+      {
+        const DF wz = warp_sum_df(DF{zs, 0.0f});
+        if (lane == 0) s_wsum[0][warp] = wz;
       }
       __syncthreads();
-      ++ordinal;
+      DF tz{0.0f, 0.0f};
+      if (tid == 0)
+        for (int w = 0; w < kWalkWarps; ++w) tz = df_add(tz, s_wsum[0][w]);
+      exchange(df_val(tz), 0.0, 0.0, 0.0, 0);
+      if (tid == 0) {
+        double z = 0.0;
+        for (int r = 0; r < cl; ++r) z += s_all_d[r][0];
+        s_zpos = (z > 0.0) ? 1 : 0;
+        if (z > 0.0 && n_rej < kMaxRejects) s_invz[n_rej] = (float)(1.0 / z);
+      }
+      __syncthreads();
+      if (s_zpos && n_rej < kMaxRejects) ++n_rej;  // z <= 0 leaves r as it is
     }
     if (accepted >= 0) {
       node = accepted;
       continue;
     }
-    // final draw from the current residual (p_node itself when nothing was rejected)
-    KahanF acc;
+    // ---- final draw from the current residual (p_node itself when nothing
+    // was rejected).  Token order is (rank, round, warp, lane, element): a
+    // (round, warp) segment holds 128 consecutive tokens.
+    float m[kMaxRounds];
     int last_pos = -1;
-    visit([&](int t, float r, float) {
-      acc.add(r);
-      if (r > 0.0f) last_pos = t;
-    });
-    // exclusive scan of per-thread masses inside the CTA (compensated pairs)
-    // the scan adds the same per-thread values the boundary test and the
-    // replay use (the compensated sums' leading parts), so that the runs'
-    // intervals tile [0, total) without gaps or overlaps
-    const DF dmass = DF{acc.s, 0.0f};
-    const double mass = (double)acc.s;
-    DF incl = dmass;
-    const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const DF y = df_shfl_up(incl, o);
-      if (lane >= o) incl = df_add(incl, y);
-    }
-    if (lane == 31) s_scan[warp] = incl;
-    if (tid == 0) {
-      s_found = -1;
-      s_last_pos = -1;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const DF w = (lane < kWalkThreads / 32) ? s_scan[lane] : DF{0.0f, 0.0f};
-      DF wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const DF y = df_shfl_up(wi, o);
-        if (lane >= o) wi = df_add(wi, y);
+    for (int j = 0; j < kMaxRounds; ++j) {
+      m[j] = 0.0f;
+      const int f = tid + j * kWalkThreads;
+      if (j < rounds && f < n4) {
+        const float4 r = residual(f);
+        m[j] = ((r.x + r.y) + r.z) + r.w;
+        const int t = s_lo + 4 * f;
+        if (r.w > 0.0f) last_pos = t + 3;
+        else if (r.z > 0.0f) last_pos = t + 2;
+        else if (r.y > 0.0f) last_pos = t + 1;
+        else if (r.x > 0.0f) last_pos = t;
       }
-      // exclusive prefix of warp totals; this CTA's mass
-      if (lane < kWalkThreads / 32) s_scan[lane] = df_add(wi, DF{-w.hi, -w.lo});
-      if (lane == kWalkThreads / 32 - 1) s_red[32] = (double)wi.hi + (double)wi.lo;
+      if (j < rounds) {  // uniform over the CTA
+        const DF sg = warp_sum_df(DF{m[j], 0.0f});
+        if (lane == 0) s_seg[j * kWalkWarps + warp] = sg;
+      }
     }
-    atomicMax(&s_last_pos, last_pos);
-    __syncthreads();
-    // the cluster's masses and last positive tokens, in rank order
-    exchange(s_red[32], 0.0, s_last_pos);
-    double before_cta = 0.0, total = 0.0;
-    int last_all = -1;
-    for (int r = 0; r < cl; ++r) {
-      if (r < rank) before_cta += s_all_d[r][0];
-      total += s_all_d[r][0];
-      last_all = max(last_all, s_all_i[r]);
-    }
-    const double u = decision_uniform(seed, offset, b, node, 1u, 0u);
-    const double target = u * total;
-    const DF excl = df_add(incl, DF{-dmass.hi, -dmass.lo});  // this thread's exclusive prefix
-    const double before = before_cta + ((double)s_scan[warp].hi + (double)s_scan[warp].lo) +
-                          ((double)excl.hi + (double)excl.lo);
-    if (mass > 0.0 && before + mass > target && before <= target) {
-      // This run holds the boundary (the lowest such run wins if rounding
-      // makes several).  Replaying the run's compensated sum in the same
-      // order ends exactly at `mass`, so the search always finds a token.
-      KahanF run;
-      int pick = -1;
-      visit([&](int t, float r, float) {
-        if (pick >= 0) return;
-        run.add(r);
-        if (before + (double)run.s > target) pick = t;
-      });
-      if (pick >= 0) atomicMin(reinterpret_cast<unsigned int*>(&s_found), (unsigned int)pick);
+    applied = n_rej;
+    if (tid == 0) {
+      s_last = -1;
+      s_result = -1;
+      s_seg_pick = -1;
     }
     __syncthreads();
-    // the lowest pick of the cluster, else the last token with positive mass
-    exchange(0.0, 0.0, s_found);
-    int pick = -1;
-    for (int r = 0; r < cl; ++r)
-      if (s_all_i[r] >= 0 && (pick < 0 || s_all_i[r] < pick)) pick = s_all_i[r];
-    result = (pick >= 0) ? pick : last_all;
+    atomicMax(&s_last, last_pos);
+    const int nseg = rounds * kWalkWarps;
+    if (warp == 0) {  // mass before every segment of the slice, and the slice's mass
+      constexpr int kPer = kMaxRounds * kWalkWarps / 32;
+      DF loc[kPer];
+      DF run{0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = lane * kPer + k;
+        loc[k] = run;
+        if (i < nseg) run = df_add(run, s_seg[i]);
+      }
+      const DF incl = warp_scan_df(run);
+      const DF excl = df_add(incl, DF{-run.hi, -run.lo});
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = lane * kPer + k;
+        if (i < nseg) s_segbase[i] = df_add(excl, loc[k]);
+      }
+      if (lane == 31) s_lt = df_val(incl);  // the slice's mass, until the exchange
+    }
+    __syncthreads();
+    // the slices' masses and last positive tokens, in rank order
+    exchange(s_lt, 0.0, 0.0, 0.0, s_last);
+    if (tid == 0) {
+      double before_cta = 0.0, total = 0.0;
+      int last_all = -1;
+      for (int r = 0; r < cl; ++r) {
+        if (r < rank) before_cta += s_all_d[r][0];
+        total += s_all_d[r][0];
+        last_all = max(last_all, s_all_i[r]);
+      }
+      const double target = decision_uniform(seed, offset, b, node, 1u, 0u) * total;
+      const double mine = s_all_d[rank][0];
+      s_found = (mine > 0.0 && target >= before_cta && target < before_cta + mine) ? 1 : 0;
+      s_lt = target - before_cta;
+      s_last = last_all;
+    }
+    __syncthreads();
+    if (s_found) {  // this slice holds the target: find the segment, then the lane
+      const double lt = s_lt;
+      if (warp == 0) {
+        constexpr int kPer = kMaxRounds * kWalkWarps / 32;
+        int hit = INT_MAX;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = lane * kPer + k;
+          if (i < nseg) {
+            const double lo = df_val(s_segbase[i]);
+            if (hit == INT_MAX && lo <= lt && lt < lo + df_val(s_seg[i])) hit = i;
+          }
+        }
+        hit = __reduce_min_sync(0xffffffffu, hit);
+        if (lane == 0) s_seg_pick = (hit == INT_MAX) ? -1 : hit;
+      }
+      __syncthreads();
+      const int sp_i = s_seg_pick;
+      if (sp_i >= 0 && warp == sp_i % kWalkWarps) {
+        const int j = sp_i / kWalkWarps;
+        float mj = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kMaxRounds; ++k)
+          if (k == j) mj = m[k];
+        const DF incl = warp_scan_df(DF{mj, 0.0f});
+        const double seg_lo = df_val(s_segbase[sp_i]);
+        const double hi = seg_lo + df_val(incl);
+        const double lo = seg_lo + df_val(df_add(incl, DF{-mj, 0.0f}));
+        const bool in = mj > 0.0f && lo <= lt && lt < hi;
+        const unsigned owner = __ballot_sync(0xffffffffu, in);
+        if (owner != 0u && lane == __ffs(owner) - 1) {
+          // replay the lane's four tokens in order
+          const int f = tid + j * kWalkThreads;
+          const float4 r = c_p[f];
+          const float e[4] = {r.x, r.y, r.z, r.w};
+          double cum = lo;
+          int pick = -1;
+          for (int k = 0; k < 4 && pick < 0; ++k) {
+            cum += (double)e[k];
+            if (cum > lt && e[k] > 0.0f) pick = s_lo + 4 * f + k;
+          }
+          if (pick < 0)  // rounding at the lane's end: its last token with mass
+            for (int k = 3; k >= 0 && pick < 0; --k)
+              if (e[k] > 0.0f) pick = s_lo + 4 * f + k;
+          dsmem_st_s32(sm100::dsmem_map(sm100::smem_u32(&s_result), 0), pick);
+        }
+      }
+    }
+    result = -2;  // rank 0 reads s_result after the final cluster barrier
     break;
   }
-  // no CTA may leave while another still reads its shared memory
+  // no CTA may leave while another still reads its shared memory; the draw's
+  // pick reaches rank 0 before this barrier.  A CTA whose copy timed out
+  // reports it after rank 0 has written the status.
+  if (rank == 0 && tid == 0) status[b] = s_err ? TV_ERR_TIMEOUT : TV_OK;
   sm100::cluster_sync();
-  if (rank != 0) return;
+  if (rank != 0) {
+    if (tid == 0 && s_err) atomicMax(status + b, (int)TV_ERR_TIMEOUT);
+    return;
+  }
+  if (result == -2) result = (s_result >= 0) ? s_result : s_last;
   const int end_depth = s_dep[node];
   for (int i = tid; i < N; i += kWalkThreads)
     if (i > end_depth) pth[i] = -1;
@@ -462,7 +579,6 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     accept_len[b] = end_depth;
     end_node[b] = node;
     out_token[b] = result;
-    status[b] = TV_OK;
   }
 }
 
