@@ -27,8 +27,10 @@
 // All CTAs of a cluster take the same decisions from the same inputs (accept
 // tests by each CTA's thread 0 from the exchanged normalisers; the draw's
 // owner from the exchanged masses), so they follow the same walk.  Element
-// values are fp32; sums across threads are compensated fp32 pairs (TwoSum),
-// across CTAs fp64 in rank order; every decision is taken in fp64.
+// values are fp32; sums across threads and CTAs are compensated fp32 pairs
+// (TwoSum), combined in a fixed order.  fp64 runs at a small fraction of the
+// fp32 rate on this part, so it is used only where the 53-bit uniform meets a
+// probability: the accept comparison and the draw's target.
 #include <climits>
 
 #include "tv_common.cuh"
@@ -77,6 +79,32 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
   return DF{hi, e - (hi - s)};
 }
 __device__ __forceinline__ double df_val(DF a) { return (double)a.hi + (double)a.lo; }
+__device__ __forceinline__ DF df_of_double(double d) {
+  const float hi = (float)d;
+  return DF{hi, (float)(d - (double)hi)};
+}
+// Order of normalised pairs (|lo| at most half an ulp of hi, as df_add leaves them).
+__device__ __forceinline__ bool df_le(DF a, DF b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo);
+}
+__device__ __forceinline__ bool df_lt(DF a, DF b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+// DF times a float (TwoProd by fma), normalised.
+__device__ __forceinline__ DF df_mul_f(DF a, float b) {
+  const float p = a.hi * b;
+  const float e = fmaf(a.hi, b, -p) + a.lo * b;
+  const float hi = p + e;
+  return DF{hi, e - (hi - p)};
+}
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x on the special-function unit (ex2.approx.ftz): relative error about
+// 2^-22, below the fp32 rounding of the probabilities it makes.
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ DF df_shfl_xor(DF a, int o) {
   return DF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
 }
@@ -97,16 +125,6 @@ __device__ __forceinline__ DF warp_scan_df(DF v) {
     if (lane >= o) v = df_add(v, y);
   }
   return v;
-}
-
-// exp(d) in fp64 to about fp32 relative precision over the whole fp64 range:
-// d log2(e) = n + f with n an integer and f in [0, 1), 2^f by exp2f, 2^n
-// exactly by ldexp (so tiny probabilities do not underflow as fp32 would).
-__device__ __forceinline__ double exp_wide(double d) {
-  if (d == -INFINITY) return 0.0;
-  const double t = d * 1.4426950408889634;
-  const double n = floor(t);
-  return ldexp((double)exp2f((float)(t - n)), (int)fmax(n, -1100.0));
 }
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
@@ -133,24 +151,25 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
   // then probability, then residual), then q side
   extern __shared__ __align__(16) float s_cache[];
   __shared__ __align__(8) uint64_t s_bar;
-  __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes], s_kids[kMaxNodes];
-  __shared__ double s_kpx[kMaxNodes], s_kqx[kMaxNodes];  // p(x), q(x) of each child's token
+  __shared__ int32_t s_par[kMaxNodes], s_dep[kMaxNodes], s_tok[kMaxNodes], s_kids[kMaxNodes];
+  __shared__ float s_kpx[kMaxNodes], s_kqx[kMaxNodes];  // p(x), q(x) of each child's token
   __shared__ float s_invz[kMaxRejects];
   __shared__ int s_wcount[kWalkWarps];
   __shared__ float s_wmax[2][kWalkWarps];
   __shared__ DF s_wsum[2][kWalkWarps];
   __shared__ DF s_seg[kMaxRounds * kWalkWarps];      // draw: mass of each 128-token segment
   __shared__ DF s_segbase[kMaxRounds * kWalkWarps];  // and the mass before it in the slice
-  __shared__ double s_norm[4];  // 1/S_p, 1/S_q, M_p, M_q
+  __shared__ float s_norm[4];  // 1/S_p, 1/S_q, M_p, M_q
   __shared__ float s_scale[2];  // this slice's factors exp(m - M) / S
-  __shared__ double s_lt;       // draw: target minus the mass before this slice (owner only)
+  __shared__ DF s_lt;           // draw: the slice's mass, then the target minus the mass
+                                // before this slice (owner only)
   __shared__ int s_found, s_zpos, s_last, s_seg_pick, s_result;
   __shared__ int s_err;
   // what this CTA shows the cluster: two phases, so that writing the next
   // value never races with another CTA still reading the previous one
-  __shared__ double s_pub_d[2][4];
+  __shared__ __align__(16) float s_pub_f[2][8];
   __shared__ int s_pub_i[2];
-  __shared__ double s_all_d[kMaxCluster][4];
+  __shared__ __align__(16) float s_all_f[kMaxCluster][8];
   __shared__ int s_all_i[kMaxCluster];
   pdl_trigger();
   pdl_wait();
@@ -159,19 +178,19 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
   const int b = blockIdx.x / cl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int phase = 0;
-  // publish (d0..d3, i), wait for the cluster, read everyone's in rank order
-  auto exchange = [&](double d0, double d1, double d2, double d3, int i) {
+  // publish eight floats and an int, wait for the cluster, read everyone's in
+  // rank order
+  auto exchange = [&](float4 a, float4 c, int i) {
     if (tid == 0) {
-      s_pub_d[phase][0] = d0;
-      s_pub_d[phase][1] = d1;
-      s_pub_d[phase][2] = d2;
-      s_pub_d[phase][3] = d3;
+      *reinterpret_cast<float4*>(&s_pub_f[phase][0]) = a;
+      *reinterpret_cast<float4*>(&s_pub_f[phase][4]) = c;
       s_pub_i[phase] = i;
     }
     sm100::cluster_sync();
-    if (tid < 4 * cl) {
-      const int r = tid >> 2, k = tid & 3;
-      s_all_d[r][k] = sm100::dsmem_ld_f64(sm100::dsmem_map(sm100::smem_u32(&s_pub_d[phase][k]), r));
+    if (tid < 2 * cl) {
+      const int r = tid >> 1, k = tid & 1;
+      *reinterpret_cast<float4*>(&s_all_f[r][4 * k]) =
+          sm100::dsmem_ld_f32x4(sm100::dsmem_map(sm100::smem_u32(&s_pub_f[phase][4 * k]), r));
       if (k == 0) s_all_i[r] = sm100::dsmem_ld_s32(sm100::dsmem_map(sm100::smem_u32(&s_pub_i[phase]), r));
     }
     __syncthreads();
@@ -191,7 +210,9 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     s_par[i] = p;
     s_dep[i] = depth[(size_t)b * N + i];
     bad_tree |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
-    if (i > 0) bad_tok |= (tok[i] < 0 || tok[i] >= V);
+    const int x = tok[i];
+    s_tok[i] = x;
+    if (i > 0) bad_tok |= (x < 0 || x >= V);
   }
   bad_tree = __syncthreads_or(bad_tree);
   if (!bad_tree)
@@ -260,7 +281,7 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     __syncthreads();
     float kp = 0.0f, kq = 0.0f;
     if (tid < nkids) {  // the children's tokens' logits, for the accept tests
-      const int x = tok[s_kids[tid]];
+      const int x = s_tok[s_kids[tid]];
       kp = __ldg(prow + x) * inv_t;
       kq = __ldg(qrow + x) * inv_t;
     }
@@ -310,10 +331,10 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       const int f = tid + j * kWalkThreads;
       if (f < n4) {
         float4 a = c_p[f], c = c_q[f];
-        a = make_float4(expf(a.x * inv_t - mp), expf(a.y * inv_t - mp), expf(a.z * inv_t - mp),
-                        expf(a.w * inv_t - mp));
-        c = make_float4(expf(c.x * inv_t - mq), expf(c.y * inv_t - mq), expf(c.z * inv_t - mq),
-                        expf(c.w * inv_t - mq));
+        a = make_float4(ex2f(fmaf(a.x, inv_t, -mp) * kLog2e), ex2f(fmaf(a.y, inv_t, -mp) * kLog2e),
+                        ex2f(fmaf(a.z, inv_t, -mp) * kLog2e), ex2f(fmaf(a.w, inv_t, -mp) * kLog2e));
+        c = make_float4(ex2f(fmaf(c.x, inv_t, -mq) * kLog2e), ex2f(fmaf(c.y, inv_t, -mq) * kLog2e),
+                        ex2f(fmaf(c.z, inv_t, -mq) * kLog2e), ex2f(fmaf(c.w, inv_t, -mq) * kLog2e));
         c_p[f] = a;
         c_q[f] = c;
         sp += (a.x + a.y) + (a.z + a.w);
@@ -335,25 +356,27 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
         tq = df_add(tq, s_wsum[1][w]);
       }
     // ---- one exchange: every slice's (max, sum); normalisers in rank order
-    exchange((double)mp, df_val(tp), (double)mq, df_val(tq), 0);
+    exchange(make_float4(mp, tp.hi, tp.lo, 0.0f), make_float4(mq, tq.hi, tq.lo, 0.0f), 0);
     if (tid == 0) {
       float Mp = -INFINITY, Mq = -INFINITY;
       for (int r = 0; r < cl; ++r) {
-        Mp = fmaxf(Mp, (float)s_all_d[r][0]);
-        Mq = fmaxf(Mq, (float)s_all_d[r][2]);
+        Mp = fmaxf(Mp, s_all_f[r][0]);
+        Mq = fmaxf(Mq, s_all_f[r][4]);
       }
-      double Sp = 0.0, Sq = 0.0;
+      DF Sp{0.0f, 0.0f}, Sq{0.0f, 0.0f};
       for (int r = 0; r < cl; ++r) {
-        if (s_all_d[r][1] > 0.0) Sp += s_all_d[r][1] * (double)expf((float)s_all_d[r][0] - Mp);
-        if (s_all_d[r][3] > 0.0) Sq += s_all_d[r][3] * (double)expf((float)s_all_d[r][2] - Mq);
+        if (s_all_f[r][1] > 0.0f)
+          Sp = df_add(Sp, df_mul_f(DF{s_all_f[r][1], s_all_f[r][2]}, ex2f((s_all_f[r][0] - Mp) * kLog2e)));
+        if (s_all_f[r][5] > 0.0f)
+          Sq = df_add(Sq, df_mul_f(DF{s_all_f[r][5], s_all_f[r][6]}, ex2f((s_all_f[r][4] - Mq) * kLog2e)));
       }
-      const double ip = 1.0 / Sp, iq = 1.0 / Sq;
+      const float ip = 1.0f / (Sp.hi + Sp.lo), iq = 1.0f / (Sq.hi + Sq.lo);
       s_norm[0] = ip;
       s_norm[1] = iq;
-      s_norm[2] = (double)Mp;
-      s_norm[3] = (double)Mq;
-      s_scale[0] = (mp == -INFINITY) ? 0.0f : (float)((double)expf(mp - Mp) * ip);
-      s_scale[1] = (mq == -INFINITY) ? 0.0f : (float)((double)expf(mq - Mq) * iq);
+      s_norm[2] = Mp;
+      s_norm[3] = Mq;
+      s_scale[0] = (mp == -INFINITY) ? 0.0f : ex2f((mp - Mp) * kLog2e) * ip;
+      s_scale[1] = (mq == -INFINITY) ? 0.0f : ex2f((mq - Mq) * kLog2e) * iq;
     }
     __syncthreads();
     // ---- the slice as probabilities r = p, q; the children's p(x), q(x) in fp64
@@ -370,8 +393,8 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       }
     }
     if (tid < nkids) {
-      s_kpx[tid] = exp_wide((double)kp - s_norm[2]) * s_norm[0];
-      s_kqx[tid] = exp_wide((double)kq - s_norm[3]) * s_norm[1];
+      s_kpx[tid] = ex2f((kp - s_norm[2]) * kLog2e) * s_norm[0];
+      s_kqx[tid] = ex2f((kq - s_norm[3]) * kLog2e) * s_norm[1];
     }
     __syncthreads();
 
@@ -396,11 +419,11 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     for (int kid = 0; kid < nkids; ++kid) {
       // accept test in fp64 on the child's token x
       if (tid == 0) {
-        double r = s_kpx[kid];
-        const double qx = s_kqx[kid];
-        for (int j = 0; j < n_rej; ++j) r = fmax(r - qx, 0.0) * (double)s_invz[j];
+        float r = s_kpx[kid];
+        const float qx = s_kqx[kid];
+        for (int j = 0; j < n_rej; ++j) r = fmaxf(r - qx, 0.0f) * s_invz[j];
         const double u = decision_uniform(seed, offset, b, node, 0u, (uint32_t)kid);
-        s_found = (qx == 0.0) || (u < r / qx);
+        s_found = (qx == 0.0f) || (u < (double)(r / qx));
       }
       __syncthreads();
       if (s_found) {
@@ -427,12 +450,13 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       DF tz{0.0f, 0.0f};
       if (tid == 0)
         for (int w = 0; w < kWalkWarps; ++w) tz = df_add(tz, s_wsum[0][w]);
-      exchange(df_val(tz), 0.0, 0.0, 0.0, 0);
+      exchange(make_float4(tz.hi, tz.lo, 0.0f, 0.0f), make_float4(0.0f, 0.0f, 0.0f, 0.0f), 0);
       if (tid == 0) {
-        double z = 0.0;
-        for (int r = 0; r < cl; ++r) z += s_all_d[r][0];
-        s_zpos = (z > 0.0) ? 1 : 0;
-        if (z > 0.0 && n_rej < kMaxRejects) s_invz[n_rej] = (float)(1.0 / z);
+        DF z{0.0f, 0.0f};
+        for (int r = 0; r < cl; ++r) z = df_add(z, DF{s_all_f[r][0], s_all_f[r][1]});
+        const float zf = z.hi + z.lo;
+        s_zpos = (zf > 0.0f) ? 1 : 0;
+        if (zf > 0.0f && n_rej < kMaxRejects) s_invz[n_rej] = 1.0f / zf;
       }
       __syncthreads();
       if (s_zpos && n_rej < kMaxRejects) ++n_rej;  // z <= 0 leaves r as it is
@@ -471,7 +495,8 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       s_seg_pick = -1;
     }
     __syncthreads();
-    atomicMax(&s_last, last_pos);
+    last_pos = __reduce_max_sync(0xffffffffu, last_pos);
+    if (lane == 0) atomicMax(&s_last, last_pos);
     const int nseg = rounds * kWalkWarps;
     if (warp == 0) {  // mass before every segment of the slice, and the slice's mass
       constexpr int kPer = kMaxRounds * kWalkWarps / 32;
@@ -490,28 +515,31 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
         const int i = lane * kPer + k;
         if (i < nseg) s_segbase[i] = df_add(excl, loc[k]);
       }
-      if (lane == 31) s_lt = df_val(incl);  // the slice's mass, until the exchange
+      if (lane == 31) s_lt = incl;  // the slice's mass, until the exchange
     }
     __syncthreads();
     // the slices' masses and last positive tokens, in rank order
-    exchange(s_lt, 0.0, 0.0, 0.0, s_last);
+    exchange(make_float4(s_lt.hi, s_lt.lo, 0.0f, 0.0f), make_float4(0.0f, 0.0f, 0.0f, 0.0f), s_last);
     if (tid == 0) {
-      double before_cta = 0.0, total = 0.0;
+      DF before_cta{0.0f, 0.0f}, total{0.0f, 0.0f};
       int last_all = -1;
       for (int r = 0; r < cl; ++r) {
-        if (r < rank) before_cta += s_all_d[r][0];
-        total += s_all_d[r][0];
+        const DF m_r{s_all_f[r][0], s_all_f[r][1]};
+        if (r < rank) before_cta = df_add(before_cta, m_r);
+        total = df_add(total, m_r);
         last_all = max(last_all, s_all_i[r]);
       }
-      const double target = decision_uniform(seed, offset, b, node, 1u, 0u) * total;
-      const double mine = s_all_d[rank][0];
-      s_found = (mine > 0.0 && target >= before_cta && target < before_cta + mine) ? 1 : 0;
-      s_lt = target - before_cta;
+      // the target u * total, formed once in fp64 and held as a float pair
+      const DF target = df_of_double(decision_uniform(seed, offset, b, node, 1u, 0u) * df_val(total));
+      const DF mine{s_all_f[rank][0], s_all_f[rank][1]};
+      s_found = (mine.hi > 0.0f && df_le(before_cta, target) && df_lt(target, df_add(before_cta, mine)))
+                    ? 1 : 0;
+      s_lt = df_add(target, DF{-before_cta.hi, -before_cta.lo});
       s_last = last_all;
     }
     __syncthreads();
     if (s_found) {  // this slice holds the target: find the segment, then the lane
-      const double lt = s_lt;
+      const DF lt = s_lt;
       if (warp == 0) {
         constexpr int kPer = kMaxRounds * kWalkWarps / 32;
         int hit = INT_MAX;
@@ -519,8 +547,8 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
         for (int k = 0; k < kPer; ++k) {
           const int i = lane * kPer + k;
           if (i < nseg) {
-            const double lo = df_val(s_segbase[i]);
-            if (hit == INT_MAX && lo <= lt && lt < lo + df_val(s_seg[i])) hit = i;
+            const DF lo = s_segbase[i];
+            if (hit == INT_MAX && df_le(lo, lt) && df_lt(lt, df_add(lo, s_seg[i]))) hit = i;
           }
         }
         hit = __reduce_min_sync(0xffffffffu, hit);
@@ -535,21 +563,21 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
         for (int k = 0; k < kMaxRounds; ++k)
           if (k == j) mj = m[k];
         const DF incl = warp_scan_df(DF{mj, 0.0f});
-        const double seg_lo = df_val(s_segbase[sp_i]);
-        const double hi = seg_lo + df_val(incl);
-        const double lo = seg_lo + df_val(df_add(incl, DF{-mj, 0.0f}));
-        const bool in = mj > 0.0f && lo <= lt && lt < hi;
+        const DF seg_lo = s_segbase[sp_i];
+        const DF hi = df_add(seg_lo, incl);
+        const DF lo = df_add(seg_lo, df_add(incl, DF{-mj, 0.0f}));
+        const bool in = mj > 0.0f && df_le(lo, lt) && df_lt(lt, hi);
         const unsigned owner = __ballot_sync(0xffffffffu, in);
         if (owner != 0u && lane == __ffs(owner) - 1) {
           // replay the lane's four tokens in order
           const int f = tid + j * kWalkThreads;
           const float4 r = c_p[f];
           const float e[4] = {r.x, r.y, r.z, r.w};
-          double cum = lo;
+          DF cum = lo;
           int pick = -1;
           for (int k = 0; k < 4 && pick < 0; ++k) {
-            cum += (double)e[k];
-            if (cum > lt && e[k] > 0.0f) pick = s_lo + 4 * f + k;
+            cum = df_add(cum, DF{e[k], 0.0f});
+            if (df_lt(lt, cum) && e[k] > 0.0f) pick = s_lo + 4 * f + k;
           }
           if (pick < 0)  // rounding at the lane's end: its last token with mass
             for (int k = 3; k >= 0 && pick < 0; --k)
