@@ -2,7 +2,8 @@
 
 A plain, slow, fp64 statement of every step of the GPU library (tree
 encoding, tree-verify attention, greedy and stochastic acceptance, TALON
-gated expansion), in ``oracle.cpp``, loaded here through ctypes.
+gated expansion, the commit of the accepted branch into the KV cache), in
+``oracle.cpp``, loaded here through ctypes.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the bench's CPU
 baseline leg may import this package.  The GPU library never does, and the
@@ -49,12 +50,13 @@ def _load():
         lib.or_accept_sample.argtypes = [P, P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64,
                                          ctypes.c_uint64, P, P, P, P, P, P, P]
         lib.or_expand_gated.argtypes = [P, P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, P]
+        lib.or_commit_path.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
         lib.or_philox4x64_10.argtypes = [P, P, P]
         lib.or_philox4x64_10.restype = None
         lib.or_draw_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, I, I, I, ctypes.c_uint32]
         lib.or_draw_word.restype = ctypes.c_uint64
         for f in (lib.or_tree_build, lib.or_attn_rows, lib.or_accept_greedy,
-                  lib.or_accept_sample, lib.or_expand_gated):
+                  lib.or_accept_sample, lib.or_expand_gated, lib.or_commit_path):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -195,6 +197,26 @@ def expand_tree(drafter, topk: int, alpha: float, budget: int, max_layers: int =
         layer += 1
     return dict(parent=par[:n].copy(), token=tok[:n].copy(), logscore=ls[:n].copy(), n=n,
                 layers=layer - 1, margins=margins)
+
+
+def commit_path(k, v, kv_len, path, accept_len):
+    """Move each sequence's accepted branch to consecutive cache positions.
+
+    k, v uint16 (bf16 bits) [B, Hkv, Lcap, D] are copied, not modified.
+    Returns (k', v', new_kv_len int32 [B], status int32 [B])."""
+    k2 = np.array(k, dtype=np.uint16, copy=True, order="C")
+    v2 = np.array(v, dtype=np.uint16, copy=True, order="C")
+    B, Hkv, Lcap, D = k2.shape
+    path = np.atleast_2d(np.asarray(path, np.int32))
+    N = path.shape[1]
+    la, lp = _c(kv_len, np.int32)
+    pa, pp = _c(path, np.int32)
+    aa, ap = _c(accept_len, np.int32)
+    new_len = np.zeros(B, np.int32)
+    status = np.zeros(B, np.int32)
+    _check(_load().or_commit_path(k2.ctypes.data, v2.ctypes.data, lp, pp, ap, B, N, Hkv, D, Lcap,
+                                  new_len.ctypes.data, status.ctypes.data))
+    return k2, v2, new_len, status
 
 
 def philox4x64_10(ctr, key) -> np.ndarray:

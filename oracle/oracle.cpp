@@ -21,6 +21,8 @@
 //           alpha gate, budget truncation), §5.2.2 (root Top-K).
 //   [GOOSE] "GOOSE: Anisotropic Speculation Trees", §2C (one forward pass
 //           verifies the whole tree; greedy walk).
+//   The commit of the accepted branch into the cache follows [SPEC] step 4
+//   and [OPT] §2 (see or_commit_path).
 //   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
 //           1, 2, 3" (SC'11): the Philox4x64-10 counter-based generator.
 //
@@ -457,6 +459,44 @@ int or_expand_gated(const float* draft_logits, const int32_t* frontier_node,
     tree_logscore[n0 + t] = (float)pass[t].ls;
   }
   *n_nodes = n0 + (int)pass.size();
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Commit of the accepted branch: [SPEC] "The protocol" step 4 (the accepted
+// tokens and the correction extend the prefix) with [OPT] §2 (the accepted
+// tokens are one root-to-node branch of the tree).  With the branch
+// path[0..a] (path[0] = 0), the K and V rows of its nodes move from their
+// tree slots kv_len + path[d] to the consecutive positions kv_len + d, one
+// row after another in increasing d; the new prefix holds a + 1 more tokens
+// (node 0 and the a accepted draft tokens).  A path that does not start at 0,
+// is not strictly increasing, leaves the tree or the cache is rejected and
+// its sequence left as it was.
+int or_commit_path(uint16_t* k, uint16_t* v, const int32_t* kv_len, const int32_t* path,
+                   const int32_t* accept_len, int B, int N, int Hkv, int D, int Lcap,
+                   int32_t* new_kv_len, int32_t* status) {
+  if (B < 0 || N < 1 || Hkv < 1 || D < 1 || Lcap < 1) return ST_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int L = kv_len[b], a = accept_len[b];
+    const int32_t* pth = path + (size_t)b * N;
+    bool ok = L >= 0 && a >= 0 && a < N && pth[0] == 0;
+    for (int d = 1; ok && d <= a; ++d) ok = pth[d] > pth[d - 1] && pth[d] < N;
+    if (ok) ok = (long long)L + pth[a] < (long long)Lcap;
+    status[b] = ok ? ST_OK : ST_INVALID_ARG;
+    new_kv_len[b] = ok ? L + a + 1 : L;
+    if (!ok) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      const size_t base = ((size_t)b * Hkv + h) * (size_t)Lcap;
+      for (int d = 1; d <= a; ++d) {
+        const size_t dst = (base + (size_t)(L + d)) * D;
+        const size_t src = (base + (size_t)(L + pth[d])) * D;
+        for (int e = 0; e < D; ++e) {
+          k[dst + e] = k[src + e];
+          v[dst + e] = v[src + e];
+        }
+      }
+    }
+  }
   return ST_OK;
 }
 
