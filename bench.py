@@ -232,6 +232,32 @@ def graph_time_us(torch, stream, fn, glen, reps):
     return a.elapsed_time(z) * 1e3 / (reps * glen)
 
 
+def measure_commit(torch, tv, stream, k, v, kv_len, path, accept_len, hbm):
+    """tv_commit_path after the step's acceptance, on a copy of the cache:
+    per-launch time and the bytes it must move (K and V of every accepted
+    node that is not already in place, read and written, every kv head)."""
+    kc, vc = k.clone(), v.clone()
+    B, Hkv, Lcap, D = kc.shape
+    new_len = torch.empty(B, dtype=torch.int32, device=kc.device)
+    st = torch.empty_like(new_len)
+
+    def f_commit():
+        tv.commit_path(kc, vc, kv_len, path, accept_len, new_len, st)
+
+    with torch.cuda.stream(stream):
+        f_commit()
+    torch.cuda.synchronize()
+    assert int(st.max()) == 0
+    pth, al = path.cpu().numpy(), accept_len.cpu().numpy()
+    moved = int(sum(int(np.sum(pth[b, 1:al[b] + 1] != np.arange(1, al[b] + 1))) for b in range(B)))
+    nbytes = 2 * 2 * D * 2 * Hkv * moved
+    us = graph_time_us(torch, stream, f_commit, 20, 5)
+    del kc, vc
+    return {"us_per_launch": us, "moved_rows": moved, "bytes": nbytes,
+            "roofline_us": nbytes / (hbm * 1e9) * 1e6, "frac": nbytes / (hbm * 1e9) * 1e6 / us,
+            "bound": "latency (a few KB per launch)"}
+
+
 def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tflops, l2):
     """One verify step of a configuration: tree -> attention -> acceptance,
     inputs resident (one set; the step's bytes are stated against L2)."""
@@ -296,6 +322,8 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
     us = {k: graph_time_us(torch, stream, f, 20, 5)
           for k, f in (("step", f_step), ("tv_tree_build", f_tree), ("tv_attn_verify", f_attn),
                        ("tv_accept_" + accept, f_acc))}
+    commit = measure_commit(torch, tv, stream, t["k"], t["v"], t["kv_len"], aouts["path"],
+                            aouts["accept_len"], hbm)
     nb = algorithmic_bytes(case)
     if accept == "greedy":
         acc_bytes = nb["greedy"]
@@ -321,6 +349,7 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
         "accept": {"bound": "hbm", "bytes": acc_bytes, "roofline_us": t_acc,
                    **({} if accept == "greedy" else {"visited_nodes": visited}),
                    "frac": t_acc / us["tv_accept_" + accept]},
+        "commit": commit,
         "inputs_resident_mb": resident / 1e6,
         "l2": f"inputs resident, {resident / 1e6:.0f} MB against the {l2 / 1e6:.0f} MB L2",
     }
@@ -384,6 +413,15 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
     stream = torch.cuda.Stream(device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     res = {}
+    case = gen.config2()
+    t = make_sets(case, torch, device, 0)[0][0]
+    depth, _, _ = tv.tree_build(t["parent"])
+    g = tv.accept_greedy(t["logits"], t["tokens"], t["parent"], depth)
+    res["spine_commit"] = dict(workload="tv_commit_path after greedy acceptance on the "
+                               "Llama-3-8B spine step (8 kv heads, head_dim 128)",
+                               **measure_commit(torch, tv, stream, t["k"], t["v"], t["kv_len"],
+                                                g["path"], g["accept_len"], hbm))
+    del t, g
     case = gen.config5(256)
     res["long_context"] = measure_verify_config(
         "long context: prefix 32768, 32/8 heads, head_dim 128, 256-node OPT-Tree-style tree, "

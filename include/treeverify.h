@@ -157,6 +157,35 @@ tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
                          cudaStream_t stream);
 
 /*
+ * tv_commit_path -- commit the accepted branch to the KV cache.
+ * (Speculative Decoding concept page, "The protocol" step 4: the accepted
+ * tokens and the correction become part of the prefix; OPT-Tree §2: the
+ * accepted tokens form one root-to-node branch of the draft tree.)
+ *
+ * For sequence b with the accepted branch path[b, 0..a] (a = accept_len[b],
+ * path[b, 0] = 0, as tv_accept_greedy and tv_accept_sample return it) and
+ * every kv head h:
+ *   k[b, h, kv_len[b] + d, :] <- k[b, h, kv_len[b] + path[b, d], :]   (d = 1..a)
+ * and the same for v, after which the prefix holds a + 1 more tokens (node 0
+ * and the accepted draft tokens; the correction or bonus token is the next
+ * step's node 0):  new_kv_len[b] = kv_len[b] + a + 1.  Slots past
+ * kv_len[b] + a keep whatever they held.
+ *   k, v        bf16 [B, Hkv, Lcap, D] in/out, 16-byte aligned; D a multiple of 8.
+ *   kv_len      int32 [B]   prefix length before the step.
+ *   path        int32 [B, N], accept_len int32 [B]: the acceptance result.
+ *   new_kv_len  int32 [B] out; must not be kv_len itself.
+ *   status      int32 [B] out: 0, or TV_ERR_INVALID_ARG when accept_len[b] is
+ *               outside [0, N - 1] (an acceptance that failed reports -1),
+ *               the branch does not start at 0 or is not strictly increasing
+ *               below N, or kv_len[b] + path[b, a] >= Lcap; that sequence's
+ *               cache is left as it was and new_kv_len[b] = kv_len[b].
+ * Device pointers owned by the caller; enqueued on `stream`; no workspace.
+ */
+tv_status tv_commit_path(tv_bf16* k, tv_bf16* v, const int32_t* kv_len, const int32_t* path,
+                         const int32_t* accept_len, int B, int N, int Hkv, int D, int Lcap,
+                         int32_t* new_kv_len, int32_t* status, cudaStream_t stream);
+
+/*
  * tv_accept_greedy -- greedy acceptance over a verified tree.
  * (OPT-Tree §2: under greedy sampling the longest branch matching the target
  * model's highest-probability sequence is accepted; GOOSE §2C: unified greedy

@@ -8,7 +8,7 @@ import torch
 from ._lib import TV_MAX_NODES, check, lib
 
 __all__ = ["tree_build", "attn_verify", "accept_greedy", "accept_sample", "expand_gated",
-           "expand_tree", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
+           "expand_tree", "commit_path", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
            "sample_workspace_size", "expand_workspace_size"]
 
 _workspaces: dict = {}
@@ -153,6 +153,31 @@ def accept_greedy(logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tens
         outs["path"].data_ptr(), outs["bonus"].data_ptr(), outs["status"].data_ptr(),
         ws.data_ptr(), ws.numel(), _stream(dev)))
     return outs
+
+
+def commit_path(k: torch.Tensor, v: torch.Tensor, kv_len: torch.Tensor, path: torch.Tensor,
+                accept_len: torch.Tensor, new_kv_len: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None):
+    """Move each sequence's accepted branch to consecutive cache slots, in place.
+
+    k, v bf16 [B, Hkv, Lcap, D]; kv_len, accept_len int32 [B]; path int32 [B, N].
+    Returns (new_kv_len int32 [B], status int32 [B])."""
+    _need(k, "k", torch.bfloat16)
+    B, Hkv, Lcap, D = k.shape
+    dev = k.device
+    _need(v, "v", torch.bfloat16, (B, Hkv, Lcap, D), dev)
+    _need(path, "path", torch.int32, None, dev)
+    if path.dim() != 2 or path.shape[0] != B:
+        raise ValueError(f"path must have shape [B, N] with B = {B}")
+    N = path.shape[1]
+    _need(kv_len, "kv_len", torch.int32, (B,), dev)
+    _need(accept_len, "accept_len", torch.int32, (B,), dev)
+    new_kv_len = torch.empty(B, dtype=torch.int32, device=dev) if new_kv_len is None else new_kv_len
+    status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+    check("tv_commit_path", lib.tv_commit_path(
+        k.data_ptr(), v.data_ptr(), kv_len.data_ptr(), path.data_ptr(), accept_len.data_ptr(), B,
+        N, Hkv, D, Lcap, new_kv_len.data_ptr(), status.data_ptr(), _stream(dev)))
+    return new_kv_len, status
 
 
 def accept_sample(p_logits: torch.Tensor, q_logits: torch.Tensor, tokens: torch.Tensor,

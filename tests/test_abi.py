@@ -89,6 +89,18 @@ def test_host_side_argument_errors_launch_nothing(tvlib):
                                dummy, dummy, 1 << 20, None) == tvlib.TV_ERR_INVALID_ARG
     assert lib.tv_expand_gated(dummy, dummy, dummy, 1, 10, 1, 3, 0.3, 5000, dummy, dummy, dummy,
                                dummy, dummy, 1 << 20, None) == tvlib.TV_ERR_UNSUPPORTED
+    # commit: head_dim not a multiple of 8, N = 0, new_kv_len aliasing kv_len, misaligned cache
+    other = ctypes.c_void_p(0x2000)
+    assert lib.tv_commit_path(dummy, dummy, dummy, dummy, dummy, 1, 8, 2, 12, 64, other, dummy,
+                              None) == tvlib.TV_ERR_UNSUPPORTED
+    assert lib.tv_commit_path(dummy, dummy, dummy, dummy, dummy, 1, 0, 2, 64, 64, other, dummy,
+                              None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_commit_path(dummy, dummy, dummy, dummy, dummy, 1, 8, 2, 64, 64, dummy, dummy,
+                              None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_commit_path(ctypes.c_void_p(0x1008), dummy, dummy, dummy, dummy, 1, 8, 2, 64,
+                              64, other, dummy, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_commit_path(dummy, dummy, dummy, dummy, dummy, 0, 8, 2, 64, 64, other, dummy,
+                              None) == tvlib.TV_OK
 
 
 def test_binding_refuses_cpu_tensors(tvlib):
