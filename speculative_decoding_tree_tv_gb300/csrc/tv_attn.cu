@@ -52,14 +52,17 @@ constexpr int kMaxSplit = 64;         // splits of one CTA's key range
 // two loads wait on different barriers, so each has a warp of its own).  Two row
 // blocks share every K/V tile (the cache is streamed once per kv head); one
 // row block gives twice the CTAs.  Both fill 224 KB of shared memory (D = 128):
-//   two row blocks: Q 64 KB, one P buffer 64 KB, two K stages, one V stage;
-//   one row block:  Q 32 KB, two P buffers, two K stages, two V stages.
-// Two K stages let S(t + 1) run during the softmax of tile t; with one V
-// stage, V(t + 1) loads once both PV(t) retired, and the softmax of t + 1
-// covers part of that load.  The second P buffer lets the softmax of tile
-// t + 1 run while PV(t) still reads P(t).
-// One row block also double-buffers S in TMEM, so that S(t + 1) is computed
-// while the softmax of tile t still reads S(t).
+//   two row blocks: Q 64 KB, one P buffer 64 KB, two K stages, one V stage.
+//     Two K stages let S(t + 1) run during the softmax of tile t; with one V
+//     stage, V(t + 1) loads once both PV(t) retired.
+//   one row block:  Q 32 KB, three K stages, three V stages.  S is
+//     double-buffered in TMEM, and the softmax writes P(t) over the first 64
+//     columns of S(t) (bf16 pairs), from where PV(t) reads it: S(t + 1) is
+//     computed while the softmax of tile t runs, and S(t + 2) is issued after
+//     PV(t) (the tensor core runs one thread's instructions in issue order).
+// (P over S was measured for two row blocks as well: with a single S buffer
+// per row block, S_r(t + 1) then waits behind PV_r(t), which cost more than
+// the deeper V ring gained.)
 // TMEM: S of (row block r, buffer u) at column 128 (r kSBufs + u), O_r at
 // 128 RBS kSBufs + 128 r; 512 columns either way.
 template <int RBS>
@@ -69,8 +72,9 @@ struct Shape {
   static constexpr int kProducerWarp = RBS * 4;  // K loads
   static constexpr int kMmaWarp = RBS * 4 + 1;
   static constexpr int kVProducerWarp = RBS * 4 + 2;
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = (RBS == 1) ? 2 : 1;
+  static constexpr bool kPInTmem = (RBS == 1);
+  static constexpr int kKStages = (RBS == 1) ? 3 : 2;
+  static constexpr int kVStages = (RBS == 1) ? 3 : 1;
   static constexpr int kPBufs = (RBS == 1) ? 2 : 1;
   static constexpr int kSBufs = (RBS == 1) ? 2 : 1;
   static constexpr uint32_t kTmemCols = 512u;
@@ -97,7 +101,8 @@ struct Layout {
   static constexpr int kTile = A * kAtomBytes;       // one K or V tile (128 keys)
   static constexpr int kQ = 0;                       // Q [row block][atom]
   static constexpr int kP = kQ + RBS * A * kAtomBytes;  // P [row block][buffer][key half], bf16
-  static constexpr int kK = kP + RBS * Shape<RBS>::kPBufs * 2 * kAtomBytes;  // K ring [stage][atom]
+  static constexpr int kK =                          // K ring [stage][atom]
+      kP + (Shape<RBS>::kPInTmem ? 0 : RBS * Shape<RBS>::kPBufs * 2 * kAtomBytes);
   static constexpr int kV = kK + Shape<RBS>::kKStages * kTile;  // V ring [stage][atom]
   static constexpr int kBytes = kV + Shape<RBS>::kVStages * kTile;
   static constexpr int kDyn = kBytes + 1024;         // slack for 1024-byte alignment
@@ -354,94 +359,156 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
     bool ok = warp_wait(&bar_q, 0);
-    int ns = 0;                          // next S tile
     int npv[2] = {0, (nrb < 2) ? T : 0};  // next PV tile of each row block
     int vzero = -1;                      // tile whose V tail was zeroed
     long long t_idle = clock64();
-    while (ok && min(npv[0], npv[1]) < T) {
-      bool prog = false;
-      // S(t + 1) may go ahead of PV(t); with two P buffers also ahead of PV(t - 1)
-      if (ns < T && ns <= min(npv[0], npv[1]) + kPBufs) {
-        bool ready = false;
-        if (lane == 0) {
-          ready = mbar_test(&bar_k_full[ns % kKStages], (ns / kKStages) & 1);
-          if (ready && ns >= kSBufs) {  // the softmax read S(ns - kSBufs) from this buffer
-            const int u = ns % kSBufs, ph = ((ns - kSBufs) / kSBufs) & 1;
-            ready = mbar_test(&bar_s_free[0][u], ph) &&
-                    (nrb < 2 || mbar_test(&bar_s_free[1][u], ph));
-          }
-        }
-        if (__shfl_sync(0xffffffffu, ready, 0)) {
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t k0 = smem_u32(sK) + (ns % kKStages) * Lay::kTile;
-            for (int r = 0; r < nrb; ++r) {
-              const uint32_t q0 = smem_u32(sQ) + r * A * kAtomBytes;
+    // S_r(t) = Q_r K(t)^T into row block r's S buffer (lane 0)
+    auto issue_s = [&](int r, int t) {
+      const uint32_t k0 = smem_u32(sK) + (t % kKStages) * Lay::kTile;
+      const uint32_t q0 = smem_u32(sQ) + r * A * kAtomBytes;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-                mma_bf16(tmem + 128 * (r * kSBufs + ns % kSBufs), sw128_desc(q0 + off, 16, 1024),
-                         sw128_desc(k0 + off, 16, 1024), idS, kk > 0);
-              }
-              mma_commit(&bar_s_full[r][ns % kSBufs]);
-            }
-            mma_commit(&bar_k_empty[ns % kKStages]);
-          }
-          __syncwarp();
-          ++ns;
-          prog = true;
-        }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+        mma_bf16(tmem + 128 * (r * kSBufs + t % kSBufs), sw128_desc(q0 + off, 16, 1024),
+                 sw128_desc(k0 + off, 16, 1024), idS, kk > 0);
       }
+      mma_commit(&bar_s_full[r][t % kSBufs]);
+    };
+    // O_r += P_r(t) V(t) over the 16-key steps that hold a key of the range;
+    // the V rows of the last step past the range (at most 15) are cleared
+    // first, as the cache may hold anything there (whole warp)
+    auto issue_pv = [&](int r, int t) {
+      const int valid = min(kBN, keys - (t_begin + t) * kBN);
+      const int nk = (valid + 15) >> 4;
+      if (vzero < t) {
+        const int z1 = min(kBN, nk * 16);
+        if (valid < z1) {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = npv[r];
-        if (t >= ns) continue;
-        bool ready = false;
-        if (lane == 0)
-          ready = mbar_test(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
-                  mbar_test(&bar_p_full[r][t % kPBufs], (t / kPBufs) & 1);
-        if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
-        tc_fence_after();
-        // PV runs over the 16-key steps that hold a key of the range; the V
-        // rows of the last step past the range (at most 15) are cleared, as
-        // the cache may hold anything there
-        const int valid = min(kBN, keys - (t_begin + t) * kBN);
-        const int nk = (valid + 15) >> 4;
-        if (vzero < t) {
-          const int z1 = min(kBN, nk * 16);
-          if (valid < z1) {
-#pragma unroll
-            for (int a = 0; a < A; ++a)
-              for (int zr = valid + (lane >> 3); zr < z1; zr += 4)
-                *reinterpret_cast<uint4*>(sV + (t % kVStages) * Lay::kTile + a * kAtomBytes +
-                                          zr * 128 + ((lane & 7) << 4)) =
-                    make_uint4(0, 0, 0, 0);
-            fence_async_smem();
-          }
-          vzero = t;
+          for (int a = 0; a < A; ++a)
+            for (int zr = valid + (lane >> 3); zr < z1; zr += 4)
+              *reinterpret_cast<uint4*>(sV + (t % kVStages) * Lay::kTile + a * kAtomBytes +
+                                        zr * 128 + ((lane & 7) << 4)) = make_uint4(0, 0, 0, 0);
+          fence_async_smem();
         }
-        __syncwarp();
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t v0 = smem_u32(sV) + (t % kVStages) * Lay::kTile;
+        vzero = t;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t v0 = smem_u32(sV) + (t % kVStages) * Lay::kTile;
+        if constexpr (Sh::kPInTmem) {
+          const uint32_t tP = tmem + 128 * (r * kSBufs + t % kSBufs);  // P over S: 8 columns per 16 keys
+          for (int kk = 0; kk < nk; ++kk)
+            mma_bf16_ts(tmem + kOCol + 128 * r, tP + 8 * kk,
+                        sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
+        } else {
           const uint32_t p0 = smem_u32(sP) + (r * kPBufs + t % kPBufs) * 2 * kAtomBytes;
           for (int kk = 0; kk < nk; ++kk)
             mma_bf16(tmem + kOCol + 128 * r,
                      sw128_desc(p0 + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
                      sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
-          mma_commit(&bar_o_done[r][t % kPBufs]);
-          // V(t) is free once both row blocks' PV(t) are done
-          if (npv[r ^ 1] > t) mma_commit(&bar_v_empty[t % kVStages]);
         }
-        __syncwarp();
-        npv[r] = t + 1;
-        prog = true;
+        mma_commit(&bar_o_done[r][t % kPBufs]);
+        // V(t) is free once both row blocks' PV(t) are done
+        if (npv[r ^ 1] > t) mma_commit(&bar_v_empty[t % kVStages]);
       }
-      if (prog) {
-        t_idle = clock64();
-      } else {
-        const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
-        if (__shfl_sync(0xffffffffu, late, 0)) ok = false;
+      __syncwarp();
+      npv[r] = t + 1;
+    };
+    if constexpr (Sh::kPInTmem) {
+      // Per row block, in tile order: S_r(t) once PV_r(t - kSBufs) is issued
+      // (P lives in the S buffer's columns) and K(t) landed; PV_r(t) once the
+      // softmax wrote P_r(t) and V(t) landed.  K(t) is free when every row
+      // block issued S(t).
+      int ns[2] = {0, (nrb < 2) ? T : 0};
+      while (ok && min(npv[0], npv[1]) < T) {
+        bool prog = false;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int t = ns[r];
+          if (t < T && t <= npv[r] + kSBufs - 1) {
+            bool ready = false;
+            if (lane == 0) ready = mbar_test(&bar_k_full[t % kKStages], (t / kKStages) & 1);
+            if (__shfl_sync(0xffffffffu, ready, 0)) {
+              tc_fence_after();
+              if (lane == 0) {
+                issue_s(r, t);
+                if (ns[r ^ 1] > t) mma_commit(&bar_k_empty[t % kKStages]);
+              }
+              __syncwarp();
+              ns[r] = t + 1;
+              prog = true;
+            }
+          }
+          const int u = npv[r];
+          if (u < ns[r]) {
+            bool ready = false;
+            if (lane == 0)
+              ready = mbar_test(&bar_v_full[u % kVStages], (u / kVStages) & 1) &&
+                      mbar_test(&bar_p_full[r][u % kPBufs], (u / kPBufs) & 1);
+            if (__shfl_sync(0xffffffffu, ready, 0)) {
+              tc_fence_after();
+              issue_pv(r, u);
+              prog = true;
+            }
+          }
+        }
+        if (prog) {
+          t_idle = clock64();
+        } else {
+          const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
+          if (__shfl_sync(0xffffffffu, late, 0)) ok = false;
+        }
+      }
+    } else {
+      // Three streams of work, each in tile order: S(t) needs K(t) and both S
+      // buffers read (softmax of t-1); PV_r(t) needs V(t) and P_r(t).  Each is
+      // issued as soon as its inputs are ready: S(t+1) ahead of PV(t), and the
+      // row block whose P is ready first goes first.
+      int ns = 0;  // next S tile
+      while (ok && min(npv[0], npv[1]) < T) {
+        bool prog = false;
+        // S(t + 1) may go ahead of PV(t); with two P buffers also ahead of PV(t - 1)
+        if (ns < T && ns <= min(npv[0], npv[1]) + kPBufs) {
+          bool ready = false;
+          if (lane == 0) {
+            ready = mbar_test(&bar_k_full[ns % kKStages], (ns / kKStages) & 1);
+            if (ready && ns >= kSBufs) {  // the softmax read S(ns - kSBufs) from this buffer
+              const int u = ns % kSBufs, ph = ((ns - kSBufs) / kSBufs) & 1;
+              ready = mbar_test(&bar_s_free[0][u], ph) &&
+                      (nrb < 2 || mbar_test(&bar_s_free[1][u], ph));
+            }
+          }
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            tc_fence_after();
+            if (lane == 0) {
+              for (int r = 0; r < nrb; ++r) issue_s(r, ns);
+              mma_commit(&bar_k_empty[ns % kKStages]);
+            }
+            __syncwarp();
+            ++ns;
+            prog = true;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int t = npv[r];
+          if (t >= ns) continue;
+          bool ready = false;
+          if (lane == 0)
+            ready = mbar_test(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
+                    mbar_test(&bar_p_full[r][t % kPBufs], (t / kPBufs) & 1);
+          if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
+          tc_fence_after();
+          issue_pv(r, t);
+          prog = true;
+        }
+        if (prog) {
+          t_idle = clock64();
+        } else {
+          const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
+          if (__shfl_sync(0xffffffffu, late, 0)) ok = false;
+        }
       }
     }
     if (!ok) s_abort = 1;
@@ -481,7 +548,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_base + 32 * c, sr[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar_s_free[rb][t % kSBufs]);  // the MMA warp may write this S buffer again
+      if constexpr (!Sh::kPInTmem)
+        mbar_arrive(&bar_s_free[rb][t % kSBufs]);  // the MMA warp may write this S buffer again
 
       // hidden keys become -inf; most tiles are all visible (prefix keys)
       if ((vis[0] & vis[1] & vis[2] & vis[3]) != 0xffffffffu) {
@@ -511,8 +579,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         m_run = m_new;
         need = true;
       }
-      // P buffer t % kPBufs is free once PV(t - kPBufs) retired
-      if (t >= kPBufs) {
+      // P buffer t % kPBufs is free once PV(t - kPBufs) retired (with P over S,
+      // S(t) completing means PV(t - kSBufs), issued before it, completed)
+      if (!Sh::kPInTmem && t >= kPBufs) {
         const int u = t - kPBufs;
         ok = warp_wait(&bar_o_done[rb][u % kPBufs], (u / kPBufs) & 1);
         if (!ok) break;
@@ -522,7 +591,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       // hidden key gives 2^-inf = 0.  Four pairwise partial sums.
       float2 ps2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
-      if (m_run == -INFINITY) {  // nothing visible yet: P = 0
+      if constexpr (Sh::kPInTmem) {
+        // 32 keys at a time -> 16 columns of P (bf16 pairs, lower key in the
+        // lower half) over the S columns this thread has already read
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pw[16];
+          if (m_run == -INFINITY) {  // nothing visible yet: P = 0
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pw[i] = 0u;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 y = ffma2(make_float2(__uint_as_float(sr[c][2 * i]),
+                                                 __uint_as_float(sr[c][2 * i + 1])),
+                                     sc2, nm2);
+              const float2 x = make_float2(ex2(y.x), ex2(y.y));
+              ps2[i & 3] = fadd2(ps2[i & 3], x);
+              pw[i] = pack_bf16(x.x, x.y);
+            }
+          }
+          tmem_st16(tS + lane_base + 16 * c, pw);
+        }
+        tmem_wait_st();
+      } else if (m_run == -INFINITY) {  // nothing visible yet: P = 0
 #pragma unroll
         for (int g = 0; g < kBN / 8; ++g)
           *reinterpret_cast<uint4*>(prow + (g >> 3) * kAtomBytes + (((g & 7) ^ (row & 7)) << 4)) =
@@ -567,7 +660,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         tmem_wait_st();
       }
-      fence_async_smem();
+      if constexpr (!Sh::kPInTmem) fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bar_p_full[rb][t % kPBufs]);
     }
