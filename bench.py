@@ -396,7 +396,9 @@ def measure_talon_expansion(torch, tv, device, stream, hbm):
     assert int(n_dev.item()) == tree["n"]
     assert torch.equal(par[:tree["n"]].cpu(), tree["parent"])
     us = graph_time_us(torch, stream, f_expand, 5, 5)
-    nbytes = sum(2 * 4 * f * V for f in F)
+    # the method reads every frontier row's draft logits once (4 V bytes a row);
+    # the kernels' second (filter) pass over a layer's rows hits the L2
+    nbytes = sum(4 * f * V for f in F)
     return tree, {
         "workload": f"TALON context 0: K {K}, alpha {alpha}, budget {budget}, vocab {V}; "
                     f"{len(F)} layers, {tree['n']} nodes",

@@ -186,31 +186,171 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
   if (tid == 0) *ws.ctl = ExpCtl{0, limit, n0, 0};
 }
 
+// One CTA per (frontier row, chunk of the row).  The chunk's candidates (logit
+// >= the row's threshold) are gathered in shared memory with their score keys.
+// When there are more than the layer may keep (`limit`), only the chunk's best
+// `limit` under the output's total order (score desc, then token asc within a
+// row) are appended: the layer's best `limit` overall are among them, and the
+// select kernel then sees at most chunks x limit candidates per row (at the
+// root layer, 10 per chunk instead of all 2048).
 __global__ void __launch_bounds__(kExpThreads)
 exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
+  __shared__ unsigned long long s_key[kExpChunk];
+  __shared__ int s_tok[kExpChunk];
+  __shared__ unsigned int s_hist[256];
+  __shared__ unsigned int s_tiebits[kExpChunk / 32];
+  __shared__ int s_cnt, s_base, s_digit, s_need, s_out;
+  __shared__ unsigned long long s_kmin, s_kmax;
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.y;
   const float thr = ws.rows[row].thr;
   const double off = ws.rows[row].off;
   if (!(thr < INFINITY)) return;
+  const int limit = ws.ctl->limit;
   const float* x = logits + (size_t)row * V;
   const int start = blockIdx.x * kExpChunk;
   const int stop = min(V, start + kExpChunk);
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_cnt = 0;
+    s_out = 0;
+    s_kmin = ~0ull;
+    s_kmax = 0ull;
+  }
+  for (int i = tid; i < kExpChunk / 32; i += kExpThreads) s_tiebits[i] = 0u;
+  __syncthreads();
   for (int base = start; base < stop; base += kExpThreads) {
-    const int e = base + threadIdx.x;
+    const int e = base + tid;
     const float lg = (e < stop) ? __ldg(x + e) : -INFINITY;
     const bool pass = (e < stop) && (lg >= thr);
     const unsigned int bal = __ballot_sync(0xffffffffu, pass);
     if (bal == 0u) continue;
     int slot0 = 0;
-    if (lane == 0) slot0 = atomicAdd(&ws.ctl->count, __popc(bal));
+    if (lane == 0) slot0 = atomicAdd(&s_cnt, __popc(bal));
     slot0 = __shfl_sync(0xffffffffu, slot0, 0);
     if (pass) {
       const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-      ws.list[slot] = ((unsigned long long)row << 32) | (unsigned int)e;
-      ws.keys[slot] = double_key(off + (double)lg);
+      s_key[slot] = double_key(off + (double)lg);
+      s_tok[slot] = e;
+    }
+  }
+  __syncthreads();
+  const int n = s_cnt;
+  if (n == 0) return;
+  const unsigned long long row_hi = (unsigned long long)row << 32;
+  if (n <= limit) {  // everything passes on
+    if (tid == 0) s_base = atomicAdd(&ws.ctl->count, n);
+    __syncthreads();
+    for (int i = tid; i < n; i += kExpThreads) {
+      ws.list[s_base + i] = row_hi | (unsigned int)s_tok[i];
+      ws.keys[s_base + i] = s_key[i];
+    }
+    return;
+  }
+  // radix select of the limit-th largest key T among the n (the bytes above
+  // the highest one in which the smallest and largest key differ are common)
+  unsigned long long kmin = ~0ull, kmax = 0ull;
+  for (int i = tid; i < n; i += kExpThreads) {
+    kmin = min(kmin, s_key[i]);
+    kmax = max(kmax, s_key[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) {
+    atomicMin(&s_kmin, kmin);
+    atomicMax(&s_kmax, kmax);
+  }
+  __syncthreads();
+  const unsigned long long diff = s_kmin ^ s_kmax;
+  const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
+  unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
+  unsigned long long prefix = s_kmax & mask;
+  int need = limit;
+  for (int shift = top; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kExpThreads) s_hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += kExpThreads) {
+      const unsigned long long k = s_key[i];
+      if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255ull], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // digits from the top: lane l holds digits 255 - 8l .. 248 - 8l
+      int cnt[8], lsum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = (int)s_hist[255 - 8 * lane - i];
+        lsum += cnt[i];
+      }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int above = incl - lsum;
+      if (above < need && incl >= need) {
+        int cum = above;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + cnt[i] >= need) {
+            s_digit = 255 - 8 * lane - i;
+            s_need = need - cum;
+            break;
+          }
+          cum += cnt[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (unsigned long long)s_digit << shift;
+    mask |= 0xffull << shift;
+    need = s_need;
+    __syncthreads();
+  }
+  const unsigned long long T = prefix;
+  // ties at T: the `need` lowest tokens, found through a bitmap of the chunk
+  for (int i = tid; i < n; i += kExpThreads)
+    if (s_key[i] == T) atomicOr(&s_tiebits[(s_tok[i] - start) >> 5], 1u << ((s_tok[i] - start) & 31));
+  if (tid == 0) s_base = atomicAdd(&ws.ctl->count, limit);
+  __syncthreads();
+  // the cutoff token: the need-th set bit of the bitmap, by one warp
+  if (warp == 0) {
+    int before = 0;
+    for (int w0 = 0; w0 < kExpChunk / 32; w0 += 32) {
+      const unsigned int bits = s_tiebits[w0 + lane];
+      const int c = __popc(bits);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (before + tot >= need) {
+        const int ex = before + incl - c;  // set bits before this lane's word
+        if (ex < need && ex + c >= need) {
+          unsigned int b = bits;
+          for (int r = need - ex; r > 1; --r) b &= b - 1u;  // drop the lower set bits
+          s_digit = start + ((w0 + lane) << 5) + (__ffs(b) - 1);  // the need-th tie token
+        }
+        break;
+      }
+      before += tot;
+    }
+  }
+  __syncthreads();
+  const int last_tie = s_digit;
+  for (int i = tid; i < n; i += kExpThreads) {
+    const unsigned long long k = s_key[i];
+    if (k > T || (k == T && s_tok[i] <= last_tie)) {
+      const int slot = s_base + atomicAdd(&s_out, 1);
+      ws.list[slot] = row_hi | (unsigned int)s_tok[i];
+      ws.keys[slot] = k;
     }
   }
 }
