@@ -87,6 +87,22 @@ NCU_TRAFFIC = {
 }
 
 
+def slowest_rank_ms(elapsed_ms, dist, device):
+    """The job's time: the maximum of the replicas' times (every rank gets it)."""
+    if dist is None:
+        return float(elapsed_ms)
+    import torch
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(steps_per_rank, world, slowest_ms):
+    """Whole-job steps/s: each of the `world` replicas runs its own steps, and
+    the job lasts as long as the slowest one (weak scaling)."""
+    return steps_per_rank * world / (slowest_ms / 1e3)
+
+
 def sources_sha256(name):
     import hashlib
     h = hashlib.sha256()
@@ -562,10 +578,7 @@ def run_ours(args, rank, world, local_rank):
     elapsed_ms = e0.elapsed_time(e1)
     clocks = sampler.stop()
     assert int(gouts["status"][0]) == 0
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, dist, device)
 
     # per-kernel average launch time, each kernel replayed alone over the same rotation
     per_kernel = {}
@@ -769,9 +782,7 @@ def main():
     hbm, tflops, peak_src = load_peaks()
     nbytes = algorithmic_bytes(case)
     flops = attention_flops(case)
-    sec = r["elapsed_ms"] / 1e3
-    steps_total = args.steps * world
-    value = steps_total / sec
+    value = job_rate(args.steps, world, r["elapsed_ms"])
     ms_per_step = r["elapsed_ms"] / args.steps
     step_bytes = sum(nbytes.values())
     pk = r["per_kernel"]
