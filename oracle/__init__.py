@@ -2,7 +2,8 @@
 
 A plain, slow, fp64 statement of every step of the GPU library (tree
 encoding, tree-verify attention, greedy and stochastic acceptance, TALON
-gated expansion, the commit of the accepted branch into the KV cache), in
+gated expansion, the commit of the accepted branch into the KV cache, the
+expected acceptance length of a tree), in
 ``oracle.cpp``, loaded here through ctypes.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the bench's CPU
@@ -51,12 +52,14 @@ def _load():
                                          ctypes.c_uint64, P, P, P, P, P, P, P]
         lib.or_expand_gated.argtypes = [P, P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, P]
         lib.or_commit_path.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
+        lib.or_expected_accept.argtypes = [P, P, I, I, P, P, P]
         lib.or_philox4x64_10.argtypes = [P, P, P]
         lib.or_philox4x64_10.restype = None
         lib.or_draw_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, I, I, I, ctypes.c_uint32]
         lib.or_draw_word.restype = ctypes.c_uint64
         for f in (lib.or_tree_build, lib.or_attn_rows, lib.or_accept_greedy,
-                  lib.or_accept_sample, lib.or_expand_gated, lib.or_commit_path):
+                  lib.or_accept_sample, lib.or_expand_gated, lib.or_commit_path,
+                  lib.or_expected_accept):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -217,6 +220,22 @@ def commit_path(k, v, kv_len, path, accept_len):
     _check(_load().or_commit_path(k2.ctypes.data, v2.ctypes.data, lp, pp, ap, B, N, Hkv, D, Lcap,
                                   new_len.ctypes.data, status.ctypes.data))
     return k2, v2, new_len, status
+
+
+def expected_accept(parent, prob):
+    """Node scores (products of draft probabilities along the path) and the
+    expected acceptance length (their sum over draft nodes).
+    Returns (score float64 [B, N], expected float64 [B], status int32 [B])."""
+    parent = np.atleast_2d(np.asarray(parent, np.int32))
+    B, N = parent.shape
+    pa, pp = _c(parent, np.int32)
+    qa, qp = _c(np.atleast_2d(prob), np.float32)
+    score = np.zeros((B, N), np.float64)
+    expected = np.zeros(B, np.float64)
+    status = np.zeros(B, np.int32)
+    _check(_load().or_expected_accept(pp, qp, B, N, score.ctypes.data, expected.ctypes.data,
+                                      status.ctypes.data))
+    return score, expected, status
 
 
 def philox4x64_10(ctr, key) -> np.ndarray:

@@ -22,7 +22,8 @@
 //   [GOOSE] "GOOSE: Anisotropic Speculation Trees", §2C (one forward pass
 //           verifies the whole tree; greedy walk).
 //   The commit of the accepted branch into the cache follows [SPEC] step 4
-//   and [OPT] §2 (see or_commit_path).
+//   and [OPT] §2 (see or_commit_path); the expected acceptance length of a
+//   tree follows [OPT] §3 (see or_expected_accept).
 //   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
 //           1, 2, 3" (SC'11): the Philox4x64-10 counter-based generator.
 //
@@ -496,6 +497,41 @@ int or_commit_path(uint16_t* k, uint16_t* v, const int32_t* kv_len, const int32_
         }
       }
     }
+  }
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Expected acceptance length of a draft tree, [OPT] §3: a node's score is
+// the product of the draft probabilities along its path from the root, and
+// the expected acceptance length is approximated by the sum of the scores of
+// the tree's draft nodes (node 0, the last accepted token, scores 1 and
+// counts no draft token).  prob[b, i] is node i's draft probability given its
+// parent; prob[b, 0] is not read.  A tree that is not in topological order or
+// a probability outside [0, 1] sets the sequence's status and leaves its
+// outputs at 0.
+int or_expected_accept(const int32_t* parent, const float* prob, int B, int N, double* score,
+                       double* expected, int32_t* status) {
+  if (B < 0 || N < 1) return ST_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent + (size_t)b * N;
+    const float* pr = prob + (size_t)b * N;
+    expected[b] = 0.0;
+    for (int i = 0; i < N; ++i) score[(size_t)b * N + i] = 0.0;
+    if (!tree_is_valid(par, N)) { status[b] = ST_INVALID_TREE; continue; }
+    bool ok = true;
+    for (int i = 1; i < N; ++i)
+      if (!(pr[i] >= 0.0f && pr[i] <= 1.0f)) ok = false;
+    if (!ok) { status[b] = ST_INVALID_ARG; continue; }
+    status[b] = ST_OK;
+    double e = 0.0;
+    for (int v = 0; v < N; ++v) {
+      double s = 1.0;
+      for (int u = v; u > 0; u = par[u]) s *= (double)pr[u];
+      score[(size_t)b * N + v] = s;
+      if (v > 0) e += s;
+    }
+    expected[b] = e;
   }
   return ST_OK;
 }
