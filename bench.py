@@ -412,6 +412,16 @@ def measure_talon_expansion(torch, tv, device, stream, hbm):
     assert int(n_dev.item()) == tree["n"]
     assert torch.equal(par[:tree["n"]].cpu(), tree["parent"])
     us = graph_time_us(torch, stream, f_expand, 5, 5)
+    # the expanded tree's expected acceptance length (OPT-Tree's objective),
+    # each node's draft probability exp(logscore - parent's logscore)
+    n = tree["n"]
+    par_d = par[:n].clone()[None]
+    prob_d = torch.ones((1, n), dtype=torch.float32, device=device)
+    prob_d[0, 1:] = torch.exp(ls[1:n] - ls[par[1:n].long()]).clamp(max=1.0)
+    ex_out = tv.expected_accept(par_d, prob_d)
+    torch.cuda.synchronize()
+    us_ex = graph_time_us(torch, stream, lambda: tv.expected_accept(par_d, prob_d, *ex_out),
+                          20, 5)
     # the method reads every frontier row's draft logits once (4 V bytes a row);
     # the kernels' second (filter) pass over a layer's rows hits the L2
     nbytes = sum(4 * f * V for f in F)
@@ -421,6 +431,9 @@ def measure_talon_expansion(torch, tv, device, stream, hbm):
         "us_per_expansion": us, "layers": len(F), "frontier_rows": int(sum(F)),
         "bytes": nbytes, "roofline_us": nbytes / (hbm * 1e9) * 1e6,
         "frac": nbytes / (hbm * 1e9) * 1e6 / us,
+        "expected_accept": {"us_per_launch": us_ex, "nodes": n,
+                            "expected_accept_len": float(ex_out[1][0]),
+                            "bound": "latency (one CTA, a few KB)"},
     }
 
 

@@ -186,6 +186,27 @@ tv_status tv_commit_path(tv_bf16* k, tv_bf16* v, const int32_t* kv_len, const in
                          int32_t* new_kv_len, int32_t* status, cudaStream_t stream);
 
 /*
+ * tv_expected_accept -- expected acceptance length of a draft tree.
+ * (OPT-Tree §3: a node's score is the product of the draft probabilities
+ * along its path from the root, and the expected acceptance length is
+ * approximated by the sum of the scores of the tree's nodes; the draft
+ * trees of OPT-Tree, GOOSE and TALON can be compared by it.)
+ *
+ *   parent    int32 [B, N]  the tree (topological order, parent[0] = -1).
+ *   prob      float [B, N]  draft probability of node i given its parent,
+ *                           in [0, 1]; prob[b, 0] is not read.
+ *   score     float [B, N] out, may be NULL: prod of prob over node i's path
+ *                           (node 0 scores 1).
+ *   expected  float [B] out: sum of score over nodes 1 .. N-1.
+ *   status    int32 [B] out: 0, TV_ERR_INVALID_TREE, or TV_ERR_INVALID_ARG for
+ *             a probability outside [0, 1] (outputs then 0).
+ * fp32 products (at most ceil(log2 N) rounds deep per factor); the sum over
+ * the draft nodes is reduced in fp32 per warp and fp64 across warps.
+ */
+tv_status tv_expected_accept(const int32_t* parent, const float* prob, int B, int N, float* score,
+                             float* expected, int32_t* status, cudaStream_t stream);
+
+/*
  * tv_accept_greedy -- greedy acceptance over a verified tree.
  * (OPT-Tree §2: under greedy sampling the longest branch matching the target
  * model's highest-probability sequence is accepted; GOOSE §2C: unified greedy

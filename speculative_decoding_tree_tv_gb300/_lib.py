@@ -57,6 +57,7 @@ _SIGS = {
                               _P, _SZ, _P]),
     "tv_expand_workspace_size": (_SZ, [_I, _I]),
     "tv_commit_path": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "tv_expected_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P]),
     "tv_expand_gated": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _SZ, _P]),
 }
 

@@ -8,7 +8,7 @@ import torch
 from ._lib import TV_MAX_NODES, check, lib
 
 __all__ = ["tree_build", "attn_verify", "accept_greedy", "accept_sample", "expand_gated",
-           "expand_tree", "commit_path", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
+           "expand_tree", "commit_path", "expected_accept", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
            "sample_workspace_size", "expand_workspace_size"]
 
 _workspaces: dict = {}
@@ -178,6 +178,24 @@ def commit_path(k: torch.Tensor, v: torch.Tensor, kv_len: torch.Tensor, path: to
         k.data_ptr(), v.data_ptr(), kv_len.data_ptr(), path.data_ptr(), accept_len.data_ptr(), B,
         N, Hkv, D, Lcap, new_kv_len.data_ptr(), status.data_ptr(), _stream(dev)))
     return new_kv_len, status
+
+
+def expected_accept(parent: torch.Tensor, prob: torch.Tensor, score: Optional[torch.Tensor] = None,
+                    expected: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """Node scores (products of draft probabilities along the path) and the
+    expected acceptance length of each tree.  parent int32 [B, N]; prob float32
+    [B, N].  Returns (score float32 [B, N], expected float32 [B], status int32 [B])."""
+    _need(parent, "parent", torch.int32)
+    B, N = parent.shape
+    dev = parent.device
+    _need(prob, "prob", torch.float32, (B, N), dev)
+    score = torch.empty((B, N), dtype=torch.float32, device=dev) if score is None else score
+    expected = torch.empty(B, dtype=torch.float32, device=dev) if expected is None else expected
+    status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+    check("tv_expected_accept", lib.tv_expected_accept(
+        parent.data_ptr(), prob.data_ptr(), B, N, score.data_ptr(), expected.data_ptr(),
+        status.data_ptr(), _stream(dev)))
+    return score, expected, status
 
 
 def accept_sample(p_logits: torch.Tensor, q_logits: torch.Tensor, tokens: torch.Tensor,
