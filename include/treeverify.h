@@ -320,7 +320,12 @@ tv_status tv_accept_sample(const float* p_logits, const float* q_logits,
  *                     (parent asc, score desc, token asc) order; ties in the
  *                     budget cut go to (parent asc, token asc).
  *   n_nodes           int32 [1], device, in/out: nodes in the tree.
- *   workspace         >= tv_expand_workspace_size(F, V) bytes (any content).
+ *   workspace         >= tv_expand_workspace_size(F, V) bytes, zero-filled before
+ *                     its first use; every call returns its control words (per-row
+ *                     arrival counters, candidate count, anchor) to zero, so the
+ *                     same workspace serves the next call as it is.
+ * Three launches: per-row statistics (the last CTA of a row forms the row's
+ * normaliser and raises the anchor), the gate filter, the budget select.
  * Scores are compared in fp64 (log domain) from fp32 logits.
  */
 size_t tv_expand_workspace_size(int F, int V);

@@ -4,20 +4,22 @@
 // s(c) = prod p_d, anchor = max s, keep s >= alpha * s_anchor, and keep the
 // best-scoring ones when more survive than the remaining budget).
 //
-// Four launches, all on the caller's stream:
-//   1. stats:   per (frontier row, 8192-logit chunk) max and sum exp;
-//   2. control: per-row log-normaliser lse_v, offset off_v = logscore_v - lse_v
-//               (log s of token c in row v is off_v + logit), the anchor, and
-//               a per-row fp32 logit threshold equivalent to the fp64 gate;
-//               resets the candidate counter;
-//   3. filter:  streams the rows again and appends every (row, token) that
-//               passes the gate to a candidate list, with its order-preserving
-//               fp64 score key beside it;
-//   4. select:  one CTA keeps the best `limit` candidates (radix select on the
-//               score keys, starting at the first byte in which the keys
-//               differ, one histogram per warp; ties to the lower
+// Three launches, all on the caller's stream:
+//   1. stats:   per (frontier row, 2048-logit chunk) max and sum exp; the last
+//               CTA of a row to finish forms the row's log-normaliser lse_v
+//               and offset off_v = logscore_v - lse_v (log s of token c in
+//               row v is off_v + logit) and raises the layer's anchor (the
+//               best score) with one atomic max;
+//   2. filter:  each CTA turns the fp64 gate into an fp32 logit threshold for
+//               its row, streams its chunk again and appends the (row, token)
+//               candidates that pass, with their order-preserving fp64 score
+//               keys (at most the layer's limit per chunk, its best ones);
+//   3. select:  one CTA keeps the best `limit` candidates (radix select on the
+//               score keys staged in shared memory, starting at the first
+//               byte in which the keys differ; ties to the lower
 //               (parent, token)), orders them (parent asc, score desc, token
-//               asc) and appends them to the tree.
+//               asc), appends them to the tree and returns the control words
+//               (candidate count, anchor) to zero for the next call.
 // Scores are fp64 in the log domain; logits stay fp32.
 #include <climits>
 
@@ -32,6 +34,7 @@ constexpr int kSelThreads = 1024;
 constexpr int kMaxBudget = 2048;
 constexpr int kTieCap = 1024;
 constexpr int kSelBatch = 8;  // key loads in flight per thread in the select passes
+constexpr int kSelStageKeys = 16384;  // candidates whose keys the select stages in shared memory
 
 struct ExpPartial {
   double s;
@@ -39,29 +42,36 @@ struct ExpPartial {
   float pad;
 };
 struct ExpRow {
-  double off;   // logscore_v - lse_v
-  float thr;    // smallest fp32 logit that passes the gate in this row
+  double off;  // logscore_v - lse_v
+  float m;     // the row's maximum logit
   float pad;
 };
 struct ExpCtl {
-  int count;   // candidates appended by the filter
-  int limit;   // how many may be kept
-  int n0;      // nodes in the tree before this layer
+  int count;                 // candidates appended by the filter (returned to 0)
+  int limit;                 // how many may be kept
+  int n0;                    // nodes in the tree before this layer
   int pad;
+  unsigned long long anchor;  // order-preserving key of the best score (returned to 0)
 };
 
 struct ExpWs {
   ExpCtl* ctl;
+  unsigned int* arrivals;  // [kMaxBudget] stats CTAs of each row done (returned to 0)
   ExpRow* rows;
   ExpPartial* part;
   unsigned long long* list;  // (row << 32) | token
   unsigned long long* keys;  // order-preserving fp64 score key of list[i]
 };
 
+// The control words (ExpCtl, then one arrival counter per possible row) sit at
+// fixed offsets, so that what one call returns to zero is where the next call
+// looks, whatever its number of frontier rows; the per-row and per-chunk
+// regions after them move with F and are written before they are read.
+__host__ __device__ inline size_t exp_arrivals_offset() { return align_up(sizeof(ExpCtl), 256); }
 __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, size_t* part_off,
                                               size_t* list_off, size_t* keys_off) {
   const int chunks = (V + kExpChunk - 1) / kExpChunk;
-  size_t o = align_up(sizeof(ExpCtl), 256);
+  size_t o = exp_arrivals_offset() + align_up((size_t)kMaxBudget * sizeof(unsigned int), 256);
   *rows_off = o;
   o += align_up((size_t)F * sizeof(ExpRow), 256);
   *part_off = o;
@@ -73,10 +83,19 @@ __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, si
   return o;
 }
 
+__device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* p) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
 __global__ void __launch_bounds__(kExpThreads)
-exp_stats_kernel(const float* __restrict__ logits, int V, int chunks, ExpPartial* __restrict__ part) {
+exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
+                 const float* __restrict__ frontier_logscore, ExpWs ws) {
+  __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
+  ExpPartial* __restrict__ part = ws.part;
   const int row = blockIdx.y;
   const float* x = logits + (size_t)row * V;
   const int start = blockIdx.x * kExpChunk;
@@ -125,7 +144,24 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks, ExpPartial
 #pragma unroll
     for (int w = 0; w < kExpThreads / 32; ++w) tot += s_s[w];
     part[(size_t)row * chunks + blockIdx.x] = ExpPartial{tot, m, 0.0f};
+    // the partial is released before the arrival; the last arrival acquires all
+    s_last = (arrive_acq_rel(&ws.arrivals[row]) == (unsigned int)chunks - 1u);
   }
+  __syncthreads();
+  if (!s_last || tid != 0) return;
+  // the last CTA of the row: normaliser, offset and best score of the row.
+  // Chunk scale factors on the SFU (fp32, within a few ulp; fp64 runs at a
+  // small fraction of the fp32 rate here), the sum itself in fp64.
+  ws.arrivals[row] = 0u;
+  const ExpPartial* p = part + (size_t)row * chunks;
+  float mr = -INFINITY;
+  for (int c = 0; c < chunks; ++c) mr = fmaxf(mr, __ldcg(&p[c].m));
+  double sr = 0.0;
+  for (int c = 0; c < chunks; ++c) sr += __ldcg(&p[c].s) * (double)expf(__ldcg(&p[c].m) - mr);
+  const double off = (double)frontier_logscore[row] - ((double)mr + log(sr));
+  ws.rows[row].off = off;
+  ws.rows[row].m = mr;
+  atomicMax(&ws.ctl->anchor, double_key(off + (double)mr));
 }
 
 // Smallest fp32 value >= x (x finite).
@@ -133,57 +169,6 @@ __device__ __forceinline__ float float_ceil_of(double x) {
   float f = (float)x;
   if ((double)f < x) f = nextafterf(f, INFINITY);
   return f;
-}
-
-__global__ void __launch_bounds__(kExpThreads)
-exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunks, int layer,
-                   int topk, float alpha, int budget, const int32_t* __restrict__ n_nodes,
-                   ExpWs ws) {
-  __shared__ unsigned long long s_anchor;
-  __shared__ double s_m_row[kMaxBudget];
-  pdl_trigger();
-  pdl_wait();
-  const int tid = threadIdx.x;
-  if (tid == 0) s_anchor = 0ull;
-  __syncthreads();
-  // per row: lse, offset, best score (row max); anchor = max best score
-  for (int v = tid; v < F; v += kExpThreads) {
-    const ExpPartial* p = ws.part + (size_t)v * chunks;
-    float m = -INFINITY;
-    for (int c = 0; c < chunks; ++c) m = fmaxf(m, p[c].m);
-    // chunk scale factors on the SFU (fp32, within a few ulp; fp64 runs at a
-    // small fraction of the fp32 rate here), the sum itself in fp64
-    double s = 0.0;
-    for (int c = 0; c < chunks; ++c) s += p[c].s * (double)expf(p[c].m - m);
-    const double off = (double)frontier_logscore[v] - ((double)m + log(s));
-    ws.rows[v].off = off;
-    s_m_row[v] = (double)m;
-    atomicMax(&s_anchor, double_key(off + (double)m));
-  }
-  __syncthreads();
-  const int n0 = *n_nodes;
-  const int remaining = budget - n0;
-  int limit = remaining > 0 ? remaining : 0;
-  if (layer == 1) limit = min(limit, topk);
-  // decode the anchor back to a double
-  const unsigned long long ak = s_anchor;
-  const unsigned long long au = (ak & 0x8000000000000000ull) ? (ak & 0x7fffffffffffffffull) : ~ak;
-  const double anchor = __longlong_as_double((long long)au);
-  const double log_alpha = log((double)alpha);
-  for (int v = tid; v < F; v += kExpThreads) {
-    float thr;
-    if (layer == 1 || limit == 0) {
-      thr = limit == 0 ? INFINITY : -INFINITY;
-    } else {
-      // s = off_v + logit >= log(alpha) + anchor  <=>  logit >= m_v + (d_v + log(alpha)),
-      // d_v = anchor - best_v >= 0 (best_v = off_v + m_v), exactly 0 in the anchor's row
-      const double best = ws.rows[v].off + s_m_row[v];
-      const double d = anchor - best;
-      thr = float_ceil_of(s_m_row[v] + (d + log_alpha));
-    }
-    ws.rows[v].thr = thr;
-  }
-  if (tid == 0) *ws.ctl = ExpCtl{0, limit, n0, 0};
 }
 
 // One CTA per (frontier row, chunk of the row).  The chunk's candidates (logit
@@ -194,20 +179,50 @@ exp_control_kernel(const float* __restrict__ frontier_logscore, int F, int chunk
 // select kernel then sees at most chunks x limit candidates per row (at the
 // root layer, 10 per chunk instead of all 2048).
 __global__ void __launch_bounds__(kExpThreads)
-exp_filter_kernel(const float* __restrict__ logits, int V, ExpWs ws) {
+exp_filter_kernel(const float* __restrict__ logits, int V, int layer, int topk, int budget,
+                  double log_alpha, const int32_t* __restrict__ n_nodes, ExpWs ws) {
   __shared__ unsigned long long s_key[kExpChunk];
   __shared__ int s_tok[kExpChunk];
   __shared__ unsigned int s_hist[256];
   __shared__ unsigned int s_tiebits[kExpChunk / 32];
   __shared__ int s_cnt, s_base, s_digit, s_need, s_out;
   __shared__ unsigned long long s_kmin, s_kmax;
+  __shared__ float s_thr;
+  __shared__ int s_limit;
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.y;
-  const float thr = ws.rows[row].thr;
   const double off = ws.rows[row].off;
+  if (threadIdx.x == 0) {
+    const int n0 = *n_nodes;
+    const int remaining = budget - n0;
+    int limit = remaining > 0 ? remaining : 0;
+    if (layer == 1) limit = min(limit, topk);
+    float thr;
+    if (layer == 1 || limit == 0) {
+      thr = limit == 0 ? INFINITY : -INFINITY;
+    } else {
+      // s = off_v + logit >= log(alpha) + anchor  <=>  logit >= m_v + (d_v + log(alpha)),
+      // d_v = anchor - best_v >= 0 (best_v = off_v + m_v), exactly 0 in the anchor's row
+      const unsigned long long ak = ws.ctl->anchor;
+      const unsigned long long au =
+          (ak & 0x8000000000000000ull) ? (ak & 0x7fffffffffffffffull) : ~ak;
+      const double anchor = __longlong_as_double((long long)au);
+      const double m = (double)ws.rows[row].m;
+      const double d = anchor - (off + m);
+      thr = float_ceil_of(m + (d + log_alpha));
+    }
+    if (blockIdx.x == 0 && row == 0) {
+      ws.ctl->limit = limit;
+      ws.ctl->n0 = n0;
+    }
+    s_thr = thr;
+    s_limit = limit;
+  }
+  __syncthreads();
+  const float thr = s_thr;
   if (!(thr < INFINITY)) return;
-  const int limit = ws.ctl->limit;
+  const int limit = s_limit;
   const float* x = logits + (size_t)row * V;
   const int start = blockIdx.x * kExpChunk;
   const int stop = min(V, start + kExpChunk);
@@ -421,6 +436,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
   __shared__ unsigned long long s_ties[kTieCap];
   __shared__ int s_n, s_nt, s_digit, s_need;
   __shared__ unsigned long long s_min, s_kmin, s_kmax;
+  // the candidates' keys, staged once so that the radix passes read shared memory
+  extern __shared__ unsigned long long s_stage[];
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x;
@@ -444,13 +461,19 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     // radix select: T = the limit-th largest key, need = how many keys == T to
     // take.  The bytes above the highest one in which the smallest and the
     // largest key differ are common to all keys and skipped.
+    const bool staged = count <= kSelStageKeys;
+    if (staged) {
+      for (int j = tid; j < count; j += kSelThreads) s_stage[j] = ws.keys[j];
+      __syncthreads();
+    }
+    const unsigned long long* K = staged ? s_stage : ws.keys;
     unsigned long long kmin = ~0ull, kmax = 0ull;
     for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
       unsigned long long kb[kSelBatch];
 #pragma unroll
       for (int u = 0; u < kSelBatch; ++u) {
         const int j = j0 + u * kSelThreads;
-        kb[u] = (j < count) ? ws.keys[j] : ws.keys[0];
+        kb[u] = (j < count) ? K[j] : K[0];
       }
 #pragma unroll
       for (int u = 0; u < kSelBatch; ++u) {
@@ -481,7 +504,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
 #pragma unroll
         for (int u = 0; u < kSelBatch; ++u) {
           const int j = j0 + u * kSelThreads;
-          kb[u] = (j < count) ? ws.keys[j] : ~prefix;  // ~prefix never matches the prefix
+          kb[u] = (j < count) ? K[j] : ~prefix;  // ~prefix never matches the prefix
         }
 #pragma unroll
         for (int u = 0; u < kSelBatch; ++u)
@@ -534,7 +557,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     const unsigned long long T = prefix;
     for (int j = tid; j < count; j += kSelThreads) {
       const unsigned long long c = ws.list[j];
-      const unsigned long long k = ws.keys[j];
+      const unsigned long long k = K[j];
       if (k > T) {
         const int slot = atomicAdd(&s_n, 1);
         s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
@@ -564,7 +587,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
         unsigned long long mine = ~0ull;
         for (int j = tid; j < count; j += kSelThreads) {
           const unsigned long long c = ws.list[j];
-          if ((first || c > last) && c < mine && ws.keys[j] == T) mine = c;
+          if ((first || c > last) && c < mine && K[j] == T) mine = c;
         }
         atomicMin(&s_min, mine);
         __syncthreads();
@@ -590,7 +613,11 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     tree_token[n0 + i] = c.token;
     tree_logscore[n0 + i] = (float)(ws.rows[c.row].off + (double)__ldg(logits + (size_t)c.row * V + c.token));
   }
-  if (tid == 0) *n_nodes = n0 + k;
+  if (tid == 0) {
+    *n_nodes = n0 + k;
+    ws.ctl->count = 0;   // the next call starts from zero
+    ws.ctl->anchor = 0ull;
+  }
 }
 
 }  // namespace
@@ -623,20 +650,29 @@ extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* f
   char* base = static_cast<char*>(workspace);
   tv::ExpWs ws;
   ws.ctl = reinterpret_cast<tv::ExpCtl*>(base);
+  ws.arrivals = reinterpret_cast<unsigned int*>(base + tv::exp_arrivals_offset());
   ws.rows = reinterpret_cast<tv::ExpRow*>(base + rows_off);
   ws.part = reinterpret_cast<tv::ExpPartial*>(base + part_off);
   ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
   ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
   const int chunks = tv::ceil_div(V, tv::kExpChunk);
   dim3 grid(chunks, F);
+  static bool select_smem_set = false;  // the select stages up to kSelStageKeys keys
+  if (!select_smem_set) {
+    if (cudaFuncSetAttribute(tv::exp_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(tv::kSelStageKeys * sizeof(unsigned long long))) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TV_ERR_CUDA;
+    }
+    select_smem_set = true;
+  }
+  const double log_alpha = log((double)alpha);
   if (tv::launch_pdl(tv::exp_stats_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
-                     chunks, ws.part) != cudaSuccess ||
-      tv::launch_pdl(tv::exp_control_kernel, dim3(1), dim3(tv::kExpThreads), 0, stream,
-                     frontier_logscore, F, chunks, layer, topk, alpha, budget,
-                     (const int32_t*)n_nodes, ws) != cudaSuccess ||
+                     chunks, frontier_logscore, ws) != cudaSuccess ||
       tv::launch_pdl(tv::exp_filter_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
-                     ws) != cudaSuccess ||
-      tv::launch_pdl(tv::exp_select_kernel, dim3(1), dim3(tv::kSelThreads), 0, stream, draft_logits,
+                     layer, topk, budget, log_alpha, (const int32_t*)n_nodes, ws) != cudaSuccess ||
+      tv::launch_pdl(tv::exp_select_kernel, dim3(1), dim3(tv::kSelThreads),
+                     (size_t)tv::kSelStageKeys * sizeof(unsigned long long), stream, draft_logits,
                      V, frontier_node, tree_parent, tree_token, tree_logscore, n_nodes,
                      ws) != cudaSuccess) {
     (void)cudaGetLastError();
