@@ -77,10 +77,10 @@ KERNEL_SOURCES = {
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
-    # attention kernel, cold (9,196,032) + merge kernel with L2 warm (1,280 + 164,864)
-    "tv_attn_verify": {"sha256": "b132124cce3f133a82d1dcbd6b31963764c6c5855455e49e83e1ba63997cd6b9", "bytes": 9362176,
+    # attention kernel, cold (9,195,776) + merge kernel with L2 warm (0 + 182,528)
+    "tv_attn_verify": {"sha256": "dbd6627dce2abf7cdcf06e7cc1c9b0b85b260f72ab74a9162024d9a1bfcd3d88", "bytes": 9378304,
                        "profile": "profiles/attn_verify_llama3-8b-spine60.md"},
-    "tv_accept_greedy": {"sha256": "a32564354c402d20b7b443e7ca5c4f0102270046fc5301c5a15ebd0c48b1d70b", "bytes": 30822144,
+    "tv_accept_greedy": {"sha256": "624f793724aaac0ace61a78a01391f4a39ee0c207ce3906766cd1c7f20a62fb9", "bytes": 30822400,
                          "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},
     "tv_tree_build": {"sha256": "7525175311d2e607c52b62e3cebfc56ca5e70ff278fa81af761f2aad43ad32ea", "bytes": 6656,
                       "profile": "profiles/tree_build_kernel_llama3-8b-spine60.md"},
