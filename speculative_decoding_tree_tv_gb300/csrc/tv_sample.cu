@@ -14,15 +14,17 @@
 //     child's slices, the likeliest next visit;
 //   * forms the softmax normalisers with one cluster exchange: every CTA
 //     publishes its slice's (max, sum of exp(x - max)) and each combines the
-//     pairs in rank order;
-//   * scales its slice to probabilities and computes, in parallel, p(x) and
-//     q(x) of every child's token in fp64 for the accept tests;
+//     pairs, one lane per rank, in the same butterfly order;
+//   * computes, one thread per child, p(x) and q(x) of every child's token
+//     for the accept tests;
 //   * tests the children in index order; a rejection is one pass that sums
 //     (r - q)+ over the slice (the update of r itself is applied lazily by
 //     the next pass) and one cluster exchange of the sums.
-// The final draw sums the residual per (round, warp) segment of 128 tokens,
-// exchanges the slices' masses, and only the CTA holding the target searches
-// it: segment, then lane, then the lane's four tokens, replayed in fp64.
+// The final draw gives each thread a contiguous run of the slice, scans the
+// runs' masses across the CTA, exchanges the slices' masses, and only the run
+// holding the target replays its tokens.  The cached slice holds exp(x - its
+// maximum); the factors that make it r and q are applied where it is read, so
+// a visit whose first child is accepted never rescales it.
 //
 // All CTAs of a cluster take the same decisions from the same inputs (accept
 // tests by each CTA's thread 0 from the exchanged normalisers; the draw's
@@ -157,13 +159,12 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
   __shared__ int s_wcount[kWalkWarps];
   __shared__ float s_wmax[2][kWalkWarps];
   __shared__ DF s_wsum[2][kWalkWarps];
-  __shared__ DF s_seg[kMaxRounds * kWalkWarps];      // draw: mass of each 128-token segment
-  __shared__ DF s_segbase[kMaxRounds * kWalkWarps];  // and the mass before it in the slice
+  __shared__ DF s_wtot[kWalkWarps];  // draw: each warp's mass, then the mass before it
   __shared__ float s_norm[4];  // 1/S_p, 1/S_q, M_p, M_q
   __shared__ float s_scale[2];  // this slice's factors exp(m - M) / S
   __shared__ DF s_lt;           // draw: the slice's mass, then the target minus the mass
                                 // before this slice (owner only)
-  __shared__ int s_found, s_zpos, s_last, s_seg_pick, s_result;
+  __shared__ int s_found, s_zpos, s_last, s_result;
   __shared__ int s_err;
   // what this CTA shows the cluster: two phases, so that writing the next
   // value never races with another CTA still reading the previous one
@@ -357,41 +358,25 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       }
     // ---- one exchange: every slice's (max, sum); normalisers in rank order
     exchange(make_float4(mp, tp.hi, tp.lo, 0.0f), make_float4(mq, tq.hi, tq.lo, 0.0f), 0);
-    if (tid == 0) {
-      float Mp = -INFINITY, Mq = -INFINITY;
-      for (int r = 0; r < cl; ++r) {
-        Mp = fmaxf(Mp, s_all_f[r][0]);
-        Mq = fmaxf(Mq, s_all_f[r][4]);
+    if (warp < 2) {  // warp 0: p, warp 1: q; lane r takes rank r's (max, sum)
+      const int k = 4 * warp;
+      const float m_r = (lane < cl) ? s_all_f[lane][k] : -INFINITY;
+      const float M = warp_max(m_r);
+      DF t{0.0f, 0.0f};
+      if (lane < cl && s_all_f[lane][k + 1] > 0.0f)
+        t = df_mul_f(DF{s_all_f[lane][k + 1], s_all_f[lane][k + 2]}, ex2f((m_r - M) * kLog2e));
+      t = warp_sum_df(t);  // the same butterfly in every CTA: identical normalisers
+      if (lane == 0) {
+        const float inv = 1.0f / (t.hi + t.lo);
+        const float mine = (warp == 0) ? mp : mq;
+        s_norm[warp] = inv;
+        s_norm[2 + warp] = M;
+        s_scale[warp] = (mine == -INFINITY) ? 0.0f : ex2f((mine - M) * kLog2e) * inv;
       }
-      DF Sp{0.0f, 0.0f}, Sq{0.0f, 0.0f};
-      for (int r = 0; r < cl; ++r) {
-        if (s_all_f[r][1] > 0.0f)
-          Sp = df_add(Sp, df_mul_f(DF{s_all_f[r][1], s_all_f[r][2]}, ex2f((s_all_f[r][0] - Mp) * kLog2e)));
-        if (s_all_f[r][5] > 0.0f)
-          Sq = df_add(Sq, df_mul_f(DF{s_all_f[r][5], s_all_f[r][6]}, ex2f((s_all_f[r][4] - Mq) * kLog2e)));
-      }
-      const float ip = 1.0f / (Sp.hi + Sp.lo), iq = 1.0f / (Sq.hi + Sq.lo);
-      s_norm[0] = ip;
-      s_norm[1] = iq;
-      s_norm[2] = Mp;
-      s_norm[3] = Mq;
-      s_scale[0] = (mp == -INFINITY) ? 0.0f : ex2f((mp - Mp) * kLog2e) * ip;
-      s_scale[1] = (mq == -INFINITY) ? 0.0f : ex2f((mq - Mq) * kLog2e) * iq;
     }
     __syncthreads();
-    // ---- the slice as probabilities r = p, q; the children's p(x), q(x) in fp64
-    {
-      const float cp = s_scale[0], cq = s_scale[1];
-#pragma unroll 4
-      for (int j = 0; j < rounds; ++j) {
-        const int f = tid + j * kWalkThreads;
-        if (f < n4) {
-          const float4 a = c_p[f], c = c_q[f];
-          c_p[f] = make_float4(a.x * cp, a.y * cp, a.z * cp, a.w * cp);
-          c_q[f] = make_float4(c.x * cq, c.y * cq, c.z * cq, c.w * cq);
-        }
-      }
-    }
+    // the children's p(x), q(x) for the accept tests; the slice itself stays
+    // as exp(x - slice max) and is scaled (by s_scale) where it is read
     if (tid < nkids) {
       s_kpx[tid] = ex2f((kp - s_norm[2]) * kLog2e) * s_norm[0];
       s_kqx[tid] = ex2f((kq - s_norm[3]) * kLog2e) * s_norm[1];
@@ -400,19 +385,25 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
 
     int n_rej = 0;    // residual normalisations so far
     int applied = 0;  // of them applied to the p side of the cache
-    // the residual r of group f with every pending normalisation applied
-    // (r <- (r - q)+ / Z_j), stored back when one was pending
-    auto residual = [&](int f) {
-      float4 r = c_p[f];
+    float rs = s_scale[0];        // the p side holds r / rs until a pass stores r itself
+    const float qs = s_scale[1];  // the q side always holds q / qs
+    // the residual r of group f (and q) with every pending normalisation
+    // applied (r <- (r - q)+ / Z_j); r is stored back when `store` or when an
+    // update was pending, and the pass then sets rs = 1
+    auto residual = [&](int f, float4& q, bool store) {
+      const float4 c = c_q[f];
+      q = make_float4(c.x * qs, c.y * qs, c.z * qs, c.w * qs);
+      const float4 a = c_p[f];
+      float4 r = make_float4(a.x * rs, a.y * rs, a.z * rs, a.w * rs);
       if (applied < n_rej) {
-        const float4 q = c_q[f];
         for (int j = applied; j < n_rej; ++j) {
           const float z = s_invz[j];
           r = make_float4(fmaxf(r.x - q.x, 0.0f) * z, fmaxf(r.y - q.y, 0.0f) * z,
                           fmaxf(r.z - q.z, 0.0f) * z, fmaxf(r.w - q.w, 0.0f) * z);
         }
-        c_p[f] = r;
+        store = true;
       }
+      if (store) c_p[f] = r;
       return r;
     };
     int accepted = -1;
@@ -436,11 +427,13 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       for (int j = 0; j < rounds; ++j) {
         const int f = tid + j * kWalkThreads;
         if (f < n4) {
-          const float4 r = residual(f), q = c_q[f];
+          float4 q;
+          const float4 r = residual(f, q, false);
           zs += (fmaxf(r.x - q.x, 0.0f) + fmaxf(r.y - q.y, 0.0f)) +
                 (fmaxf(r.z - q.z, 0.0f) + fmaxf(r.w - q.w, 0.0f));
         }
       }
+      if (applied < n_rej) rs = 1.0f;  // uniform: every group was stored
       applied = n_rej;
       {
         const DF wz = warp_sum_df(DF{zs, 0.0f});
@@ -466,58 +459,53 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       continue;
     }
     // ---- final draw from the current residual (p_node itself when nothing
-    // was rejected).  Token order is (rank, round, warp, lane, element): a
-    // (round, warp) segment holds 128 consecutive tokens.
-    float m[kMaxRounds];
+    // was rejected).  For the draw, thread t takes a contiguous run of the
+    // slice, float4 groups [t P4, (t + 1) P4), so token order is (rank,
+    // thread, group, element).  It reads its groups in an order rotated by t
+    // (conflict-free), stores r itself, and sums its run as a float pair; a
+    // block-wide scan of the runs gives every thread [lo, hi), and the runs
+    // tile the slice exactly.
+    const int P4 = ceil_div(n4, kWalkThreads);
+    DF run{0.0f, 0.0f};
     int last_pos = -1;
-#pragma unroll
-    for (int j = 0; j < kMaxRounds; ++j) {
-      m[j] = 0.0f;
-      const int f = tid + j * kWalkThreads;
-      if (j < rounds && f < n4) {
-        const float4 r = residual(f);
-        m[j] = ((r.x + r.y) + r.z) + r.w;
-        const int t = s_lo + 4 * f;
-        if (r.w > 0.0f) last_pos = t + 3;
-        else if (r.z > 0.0f) last_pos = t + 2;
-        else if (r.y > 0.0f) last_pos = t + 1;
-        else if (r.x > 0.0f) last_pos = t;
-      }
-      if (j < rounds) {  // uniform over the CTA
-        const DF sg = warp_sum_df(DF{m[j], 0.0f});
-        if (lane == 0) s_seg[j * kWalkWarps + warp] = sg;
+    for (int k = 0; k < P4; ++k) {
+      const int g = tid * P4 + (k + tid) % P4;
+      if (g < n4) {
+        float4 q;
+        const float4 r = residual(g, q, true);
+        run = df_add(run, DF{(r.x + r.y) + (r.z + r.w), 0.0f});
+        const int t = s_lo + 4 * g;
+        const int lp = (r.w > 0.0f) ? t + 3 : (r.z > 0.0f) ? t + 2 : (r.y > 0.0f) ? t + 1
+                                                                      : (r.x > 0.0f) ? t : -1;
+        last_pos = max(last_pos, lp);
       }
     }
     applied = n_rej;
+    rs = 1.0f;
+    const DF incl = warp_scan_df(run);
+    const DF excl = DF{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+    if (lane == 31) s_wtot[warp] = incl;
     if (tid == 0) {
       s_last = -1;
       s_result = -1;
-      s_seg_pick = -1;
     }
     __syncthreads();
     last_pos = __reduce_max_sync(0xffffffffu, last_pos);
     if (lane == 0) atomicMax(&s_last, last_pos);
-    const int nseg = rounds * kWalkWarps;
-    if (warp == 0) {  // mass before every segment of the slice, and the slice's mass
-      constexpr int kPer = kMaxRounds * kWalkWarps / 32;
-      DF loc[kPer];
-      DF run{0.0f, 0.0f};
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = lane * kPer + k;
-        loc[k] = run;
-        if (i < nseg) run = df_add(run, s_seg[i]);
+    if (warp == 0) {  // mass before each warp's runs, and the slice's mass
+      DF base{0.0f, 0.0f};
+      for (int w = 0; w < kWalkWarps; ++w) {
+        const DF tw = s_wtot[w];
+        __syncwarp();
+        if (lane == 0) s_wtot[w] = base;
+        base = df_add(base, tw);
       }
-      const DF incl = warp_scan_df(run);
-      const DF excl = df_add(incl, DF{-run.hi, -run.lo});
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = lane * kPer + k;
-        if (i < nseg) s_segbase[i] = df_add(excl, loc[k]);
-      }
-      if (lane == 31) s_lt = incl;  // the slice's mass, until the exchange
+      if (lane == 0) s_lt = base;  // the slice's mass, until the exchange
     }
     __syncthreads();
+    const DF wbase = s_wtot[warp];
+    const DF lo = (lane == 0) ? wbase : df_add(wbase, excl);
+    const DF hi = df_add(wbase, incl);
     // the slices' masses and last positive tokens, in rank order
     exchange(make_float4(s_lt.hi, s_lt.lo, 0.0f, 0.0f), make_float4(0.0f, 0.0f, 0.0f, 0.0f), s_last);
     if (tid == 0) {
@@ -538,52 +526,23 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       s_last = last_all;
     }
     __syncthreads();
-    if (s_found) {  // this slice holds the target: find the segment, then the lane
+    if (s_found) {  // this slice holds the target: the run holding it replays its tokens
       const DF lt = s_lt;
-      if (warp == 0) {
-        constexpr int kPer = kMaxRounds * kWalkWarps / 32;
-        int hit = INT_MAX;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int i = lane * kPer + k;
-          if (i < nseg) {
-            const DF lo = s_segbase[i];
-            if (hit == INT_MAX && df_le(lo, lt) && df_lt(lt, df_add(lo, s_seg[i]))) hit = i;
-          }
-        }
-        hit = __reduce_min_sync(0xffffffffu, hit);
-        if (lane == 0) s_seg_pick = (hit == INT_MAX) ? -1 : hit;
-      }
-      __syncthreads();
-      const int sp_i = s_seg_pick;
-      if (sp_i >= 0 && warp == sp_i % kWalkWarps) {
-        const int j = sp_i / kWalkWarps;
-        float mj = 0.0f;
-#pragma unroll
-        for (int k = 0; k < kMaxRounds; ++k)
-          if (k == j) mj = m[k];
-        const DF incl = warp_scan_df(DF{mj, 0.0f});
-        const DF seg_lo = s_segbase[sp_i];
-        const DF hi = df_add(seg_lo, incl);
-        const DF lo = df_add(seg_lo, df_add(incl, DF{-mj, 0.0f}));
-        const bool in = mj > 0.0f && df_le(lo, lt) && df_lt(lt, hi);
-        const unsigned owner = __ballot_sync(0xffffffffu, in);
-        if (owner != 0u && lane == __ffs(owner) - 1) {
-          // replay the lane's four tokens in order
-          const int f = tid + j * kWalkThreads;
-          const float4 r = c_p[f];
+      if (df_lt(lo, hi) && df_le(lo, lt) && df_lt(lt, hi)) {
+        DF cum = lo;
+        int pick = -1, last_mine = -1;
+        for (int g = tid * P4; g < min(n4, (tid + 1) * P4); ++g) {
+          const float4 r = c_p[g];
           const float e[4] = {r.x, r.y, r.z, r.w};
-          DF cum = lo;
-          int pick = -1;
-          for (int k = 0; k < 4 && pick < 0; ++k) {
+          for (int k = 0; k < 4; ++k) {
+            if (!(e[k] > 0.0f)) continue;
+            last_mine = s_lo + 4 * g + k;
             cum = df_add(cum, DF{e[k], 0.0f});
-            if (df_lt(lt, cum) && e[k] > 0.0f) pick = s_lo + 4 * f + k;
+            if (pick < 0 && df_lt(lt, cum)) pick = last_mine;
           }
-          if (pick < 0)  // rounding at the lane's end: its last token with mass
-            for (int k = 3; k >= 0 && pick < 0; --k)
-              if (e[k] > 0.0f) pick = s_lo + 4 * f + k;
-          dsmem_st_s32(sm100::dsmem_map(sm100::smem_u32(&s_result), 0), pick);
         }
+        if (pick < 0) pick = last_mine;  // rounding at the run's end: its last token with mass
+        dsmem_st_s32(sm100::dsmem_map(sm100::smem_u32(&s_result), 0), pick);
       }
     }
     result = -2;  // rank 0 reads s_result after the final cluster barrier
