@@ -3,7 +3,7 @@
 A plain, slow, fp64 statement of every step of the GPU library (tree
 encoding, tree-verify attention, greedy and stochastic acceptance, TALON
 gated expansion, the commit of the accepted branch into the KV cache, the
-expected acceptance length of a tree), in
+expected acceptance length of a tree, the GOOSE spine-tree builder), in
 ``oracle.cpp``, loaded here through ctypes.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the bench's CPU
@@ -53,13 +53,14 @@ def _load():
         lib.or_expand_gated.argtypes = [P, P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, P]
         lib.or_commit_path.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
         lib.or_expected_accept.argtypes = [P, P, I, I, P, P, P]
+        lib.or_build_spine_tree.argtypes = [P, I, P, I, I, I, I, ctypes.c_float, P, P, P]
         lib.or_philox4x64_10.argtypes = [P, P, P]
         lib.or_philox4x64_10.restype = None
         lib.or_draw_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, I, I, I, ctypes.c_uint32]
         lib.or_draw_word.restype = ctypes.c_uint64
         for f in (lib.or_tree_build, lib.or_attn_rows, lib.or_accept_greedy,
                   lib.or_accept_sample, lib.or_expand_gated, lib.or_commit_path,
-                  lib.or_expected_accept):
+                  lib.or_expected_accept, lib.or_build_spine_tree):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -236,6 +237,26 @@ def expected_accept(parent, prob):
     _check(_load().or_expected_accept(pp, qp, B, N, score.ctypes.data, expected.ctypes.data,
                                       status.ctypes.data))
     return score, expected, status
+
+
+def build_spine_tree(spine_tokens, branch_tokens, root_token: int, budget: int,
+                     spine_ratio: float):
+    """GOOSE spine tree: (parent int32 [n], tokens int32 [n]).
+
+    spine_tokens int32 [S]; branch_tokens int32 [Sb, K] (row j: candidates
+    for a branch off spine node j, best first, -1 ends a row)."""
+    sp, spp = _c(np.asarray(spine_tokens, np.int32).reshape(-1), np.int32)
+    br = np.asarray(branch_tokens, np.int32)
+    if br.ndim != 2:
+        br = br.reshape(0, 0)
+    ba, bp = _c(br, np.int32)
+    parent = np.zeros(budget, np.int32)
+    tokens = np.zeros(budget, np.int32)
+    n = np.zeros(1, np.int32)
+    _check(_load().or_build_spine_tree(spp, sp.size, bp, br.shape[0], br.shape[1] if br.ndim == 2 else 0,
+                                       int(root_token), int(budget), float(spine_ratio),
+                                       parent.ctypes.data, tokens.ctypes.data, n.ctypes.data))
+    return parent[:n[0]].copy(), tokens[:n[0]].copy()
 
 
 def philox4x64_10(ctr, key) -> np.ndarray:

@@ -536,6 +536,88 @@ int or_expected_accept(const int32_t* parent, const float* prob, int B, int N, d
   return ST_OK;
 }
 
+// ---------------------------------------------------------------------------
+// GOOSE anisotropic spine tree, [GOOSE] §2A (the spine: a chain of
+// context-matched tokens; branches of transition tokens fork off every spine
+// node; more of the budget to the spine where its acceptance is high, the
+// rest as branches wide near the root and narrower deeper down) and §2B
+// Proposition 2 (the optimal branch allocation decreases linearly with
+// depth).  Readings where the pages give no formula:
+//   * the spine takes d = min(S, round(ratio * (budget - 1))) nodes;
+//   * branch point j (spine node j, j = 0 .. m-1, m = min(d + 1, Sb)) gets
+//     w_j = floor(R (m - j) / (m (m + 1) / 2)) of the R = budget - 1 - d
+//     branch nodes, the remainder one each from j = 0 on;
+//   * a branch point with fewer usable candidates (row j of branch_tokens,
+//     best first, -1 ends the row, the spine's own token at that depth
+//     skipped, repeats skipped) passes the rest on to j + 1, j + 2, ...;
+//   * nodes are numbered breadth-first, the spine child first at each depth.
+int or_build_spine_tree(const int32_t* spine_tokens, int S, const int32_t* branch_tokens, int Sb,
+                        int K, int root_token, int budget, float spine_ratio, int32_t* parent,
+                        int32_t* tokens, int32_t* n_nodes) {
+  if (S < 0 || Sb < 0 || K < 0 || budget < 1 || !(spine_ratio >= 0.0f && spine_ratio <= 1.0f))
+    return ST_INVALID_ARG;
+  int d = (int)llround((double)spine_ratio * (double)(budget - 1));
+  d = std::min(d, S);
+  const int R = budget - 1 - d;
+  const int m = std::min(d + 1, Sb);
+  // usable candidates of each branch point
+  std::vector<std::vector<int>> cand(m);
+  for (int j = 0; j < m; ++j) {
+    const int spine_tok = (j < S) ? spine_tokens[j] : -1;  // the spine child's token at depth j+1
+    for (int k = 0; k < K; ++k) {
+      const int t = branch_tokens[(size_t)j * K + k];
+      if (t < 0) break;
+      if (j < d && t == spine_tok) continue;
+      if (std::find(cand[j].begin(), cand[j].end(), t) != cand[j].end()) continue;
+      cand[j].push_back(t);
+    }
+  }
+  std::vector<int> w(m, 0);
+  if (m > 0 && R > 0) {
+    const long long T = (long long)m * (m + 1) / 2;
+    int given = 0;
+    for (int j = 0; j < m; ++j) {
+      w[j] = (int)((long long)R * (m - j) / T);
+      given += w[j];
+    }
+    for (int j = 0; given < R; ++j, ++given) w[j % m] += 1;
+    int carry = 0;
+    for (int j = 0; j < m; ++j) {
+      w[j] += carry;
+      carry = 0;
+      if (w[j] > (int)cand[j].size()) {
+        carry = w[j] - (int)cand[j].size();
+        w[j] = (int)cand[j].size();
+      }
+    }
+  }
+  // breadth-first numbering: depth t holds spine node t (if t <= d), then the
+  // branches of spine node t - 1
+  int n = 0;
+  parent[n] = -1;
+  tokens[n] = root_token;
+  ++n;
+  int spine_id = 0;  // id of spine node t - 1 while depth t is numbered
+  const int depth_max = std::max(d, m);
+  for (int t = 1; t <= depth_max; ++t) {
+    const int up = spine_id;
+    if (t <= d) {
+      parent[n] = up;
+      tokens[n] = spine_tokens[t - 1];
+      spine_id = n;
+      ++n;
+    }
+    if (t - 1 < m)
+      for (int k = 0; k < w[t - 1]; ++k) {
+        parent[n] = up;
+        tokens[n] = cand[t - 1][k];
+        ++n;
+      }
+  }
+  *n_nodes = n;
+  return ST_OK;
+}
+
 // Philox4x64-10 block (exposed for the generator's own pins).
 void or_philox4x64_10(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
   philox4x64_10(ctr, key, out);
