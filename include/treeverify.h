@@ -207,6 +207,40 @@ tv_status tv_expected_accept(const int32_t* parent, const float* prob, int B, in
                              float* expected, int32_t* status, cudaStream_t stream);
 
 /*
+ * tv_build_spine_tree -- GOOSE anisotropic spine tree (host code, no GPU).
+ * (GOOSE §2A: a deep chain of context-matched tokens, the spine, with wide
+ * branches of transition tokens forking off every spine node, wider near the
+ * root; §2B Proposition 2: branch allocation falling linearly with depth.)
+ *
+ *   spine_tokens   int32 [S]      host: the context-matched chain, in order.
+ *   branch_tokens  int32 [Sb, K]  host: row j = candidates for a branch off
+ *                                 spine node j (node 0 = the root), best
+ *                                 first, -1 ends a row.
+ *   root_token     token of node 0 (the last accepted token).
+ *   budget         nodes in the tree, counting the root (>= 1).
+ *   spine_ratio    in [0, 1]: the spine takes min(S, round(ratio (budget-1)))
+ *                  nodes; the rest go to branch points j = 0 .. m-1
+ *                  (m = min(spine + 1, Sb)) with widths proportional to m - j
+ *                  (integer parts, then one each from the root), each capped
+ *                  by its usable candidates (the spine's own token and
+ *                  repeats skipped; a shortfall passes on to deeper points).
+ *   parent, tokens int32 [budget] host out: the tree, breadth-first, the spine
+ *                  child first at every depth; n_nodes host out: its size.
+ * Returns TV_ERR_INVALID_ARG for negative sizes, budget < 1, a ratio outside
+ * [0, 1] or a NULL pointer that is needed.
+ */
+tv_status tv_build_spine_tree(const int32_t* spine_tokens, int S, const int32_t* branch_tokens,
+                              int Sb, int K, int root_token, int budget, float spine_ratio,
+                              int32_t* parent, int32_t* tokens, int32_t* n_nodes);
+
+/*
+ * tv_spine_ratio_update -- GOOSE §2C: the spine ratio follows an exponential
+ * moving average of the observed acceptance rate of the spine tokens:
+ * returns clamp((1 - beta) ratio + beta observed, 0, 1).  Host code.
+ */
+float tv_spine_ratio_update(float ratio, float observed_accept_rate, float beta);
+
+/*
  * tv_accept_greedy -- greedy acceptance over a verified tree.
  * (OPT-Tree §2: under greedy sampling the longest branch matching the target
  * model's highest-probability sequence is accepted; GOOSE §2C: unified greedy

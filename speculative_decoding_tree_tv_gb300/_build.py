@@ -13,7 +13,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtreeverify.so")
 
 SOURCES = ["tv_api.cu", "tv_tree.cu", "tv_greedy.cu", "tv_sample.cu", "tv_expand.cu",
-           "tv_attn.cu", "tv_commit.cu", "tv_expected.cu"]
+           "tv_attn.cu", "tv_commit.cu", "tv_expected.cu", "tv_spine.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-I" + CSRC, "--expt-relaxed-constexpr"]
@@ -47,7 +47,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:

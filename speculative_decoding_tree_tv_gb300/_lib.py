@@ -58,6 +58,8 @@ _SIGS = {
     "tv_expand_workspace_size": (_SZ, [_I, _I]),
     "tv_commit_path": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tv_expected_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P]),
+    "tv_build_spine_tree": (_I, [_P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "tv_spine_ratio_update": (_F, [_F, _F, _F]),
     "tv_expand_gated": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _SZ, _P]),
 }
 

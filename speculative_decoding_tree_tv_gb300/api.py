@@ -8,7 +8,7 @@ import torch
 from ._lib import TV_MAX_NODES, check, lib
 
 __all__ = ["tree_build", "attn_verify", "accept_greedy", "accept_sample", "expand_gated",
-           "expand_tree", "commit_path", "expected_accept", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
+           "expand_tree", "commit_path", "expected_accept", "build_spine_tree", "spine_ratio_update", "workspace", "attn_workspace_size", "attn_plan", "greedy_workspace_size",
            "sample_workspace_size", "expand_workspace_size"]
 
 _workspaces: dict = {}
@@ -196,6 +196,31 @@ def expected_accept(parent: torch.Tensor, prob: torch.Tensor, score: Optional[to
         parent.data_ptr(), prob.data_ptr(), B, N, score.data_ptr(), expected.data_ptr(),
         status.data_ptr(), _stream(dev)))
     return score, expected, status
+
+
+def build_spine_tree(spine_tokens, branch_tokens, root_token: int, budget: int,
+                     spine_ratio: float):
+    """GOOSE spine tree on the host.  spine_tokens int32 [S]; branch_tokens
+    int32 [Sb, K] (row j: branch candidates off spine node j, best first, -1
+    ends a row).  Returns (parent, tokens) as int32 numpy arrays."""
+    import numpy as np
+    sp = np.ascontiguousarray(np.asarray(spine_tokens, dtype=np.int32).reshape(-1))
+    br = np.asarray(branch_tokens, dtype=np.int32)
+    br = np.ascontiguousarray(br if br.ndim == 2 else br.reshape(0, 0))
+    parent = np.zeros(max(int(budget), 1), np.int32)
+    tokens = np.zeros(max(int(budget), 1), np.int32)
+    n = np.zeros(1, np.int32)
+    check("tv_build_spine_tree", lib.tv_build_spine_tree(
+        sp.ctypes.data if sp.size else None, sp.size, br.ctypes.data if br.size else None,
+        br.shape[0], br.shape[1], int(root_token), int(budget), float(spine_ratio),
+        parent.ctypes.data, tokens.ctypes.data, n.ctypes.data))
+    return parent[:n[0]].copy(), tokens[:n[0]].copy()
+
+
+def spine_ratio_update(ratio: float, observed_accept_rate: float, beta: float) -> float:
+    """GOOSE's spine ratio: an exponential moving average of the observed
+    acceptance rate of the spine, clamped to [0, 1]."""
+    return float(lib.tv_spine_ratio_update(float(ratio), float(observed_accept_rate), float(beta)))
 
 
 def accept_sample(p_logits: torch.Tensor, q_logits: torch.Tensor, tokens: torch.Tensor,
