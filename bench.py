@@ -444,6 +444,19 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
     stream = torch.cuda.Stream(device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     res = {}
+    # GOOSE spine tree on the host (a 24-token context-matched spine, 8
+    # transition candidates per position, 60 nodes), as a decode step builds it
+    r = np.random.default_rng(3)
+    spine = r.choice(case_vocab := 128256, 24, replace=False).astype(np.int32)
+    branch = np.stack([r.choice(case_vocab, 8, replace=False) for _ in range(24)]).astype(np.int32)
+    tv.build_spine_tree(spine, branch, 0, 60, 0.4)
+    t0 = time.perf_counter()
+    for _ in range(2000):
+        sp_par, _ = tv.build_spine_tree(spine, branch, 0, 60, 0.4)
+    res["spine_tree_build"] = {"workload": "GOOSE spine tree on the host: 24-token spine, 8 "
+                               "candidates per position, budget 60, ratio 0.4",
+                               "us_per_call": (time.perf_counter() - t0) / 2000 * 1e6,
+                               "nodes": int(len(sp_par)), "where": "host CPU (Python call included)"}
     case = gen.config2()
     t = make_sets(case, torch, device, 0)[0][0]
     depth, _, _ = tv.tree_build(t["parent"])
