@@ -3,7 +3,8 @@
 A plain, slow, fp64 statement of every step of the GPU library (tree
 encoding, tree-verify attention, greedy and stochastic acceptance, TALON
 gated expansion, the commit of the accepted branch into the KV cache, the
-expected acceptance length of a tree, the GOOSE spine-tree builder), in
+expected acceptance length of a tree, the GOOSE spine-tree builder,
+OPT-Tree's greedy expansion and subtree selection), in
 ``oracle.cpp``, loaded here through ctypes.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the bench's CPU
@@ -51,6 +52,8 @@ def _load():
         lib.or_accept_sample.argtypes = [P, P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64,
                                          ctypes.c_uint64, P, P, P, P, P, P, P]
         lib.or_expand_gated.argtypes = [P, P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, P]
+        lib.or_expand_topn.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P]
+        lib.or_select_topn.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P, P]
         lib.or_commit_path.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
         lib.or_expected_accept.argtypes = [P, P, I, I, P, P, P]
         lib.or_build_spine_tree.argtypes = [P, I, P, I, I, I, I, ctypes.c_float, P, P, P]
@@ -201,6 +204,74 @@ def expand_tree(drafter, topk: int, alpha: float, budget: int, max_layers: int =
         layer += 1
     return dict(parent=par[:n].copy(), token=tok[:n].copy(), logscore=ls[:n].copy(), n=n,
                 layers=layer - 1, margins=margins)
+
+
+def expand_topn(draft_logits, frontier_node, frontier_logscore, width: int, capacity: int,
+                tree_parent, tree_token, tree_logscore, n_nodes: int):
+    """One OPT-Tree layer: the `width` best children of the frontier are
+    appended to the tree_* arrays (length >= capacity, updated in place).
+    Returns (new n_nodes, margin)."""
+    dl = np.ascontiguousarray(draft_logits, dtype=np.float32)
+    F, V = dl.shape
+    fn, fnp = _c(frontier_node, np.int32)
+    fl, flp = _c(frontier_logscore, np.float32)
+    assert tree_parent.dtype == np.int32 and tree_token.dtype == np.int32
+    assert tree_logscore.dtype == np.float32 and tree_parent.size >= capacity
+    nn = np.array([n_nodes], np.int32)
+    margin = np.zeros(1, np.float64)
+    _check(_load().or_expand_topn(dl.ctypes.data, fnp, flp, F, V, int(width), int(capacity),
+                                  tree_parent.ctypes.data, tree_token.ctypes.data,
+                                  tree_logscore.ctypes.data, nn.ctypes.data, margin.ctypes.data))
+    return int(nn[0]), float(margin[0])
+
+
+def select_topn(parent, token, logscore, n_nodes, n: int):
+    """OPT-Tree subtree selection over B candidate trees [B, M].
+    Returns dict(parent, token, logscore, src [B, n], expected [B], status [B])."""
+    parent = np.atleast_2d(np.asarray(parent, np.int32))
+    B, M = parent.shape
+    pa, pp = _c(parent, np.int32)
+    ta, tp = _c(np.atleast_2d(token), np.int32)
+    la, lp = _c(np.atleast_2d(logscore), np.float32)
+    ma, mp = _c(np.atleast_1d(n_nodes), np.int32)
+    out = dict(parent=np.zeros((B, n), np.int32), token=np.zeros((B, n), np.int32),
+               logscore=np.zeros((B, n), np.float32), src=np.zeros((B, n), np.int32),
+               expected=np.zeros(B, np.float32), status=np.zeros(B, np.int32))
+    _check(_load().or_select_topn(pp, tp, lp, mp, B, M, int(n), out["parent"].ctypes.data,
+                                  out["token"].ctypes.data, out["logscore"].ctypes.data,
+                                  out["src"].ctypes.data, out["expected"].ctypes.data,
+                                  out["status"].ctypes.data))
+    return out
+
+
+def opt_tree(drafter, width: int, layers: int, n: int):
+    """Grow an OPT-Tree candidate tree for `layers` layers of `width` nodes
+    each (the root's layer is 1), then keep its n best nodes [OPT §3].
+
+    drafter has root_key(), child_key(key, token) and rows(keys).  Returns
+    dict(parent, token, logscore, n (the candidate tree), margins,
+    selected (select_topn's output for the single tree))."""
+    cap = 1 + width * layers
+    par = np.full(cap, -1, np.int32)
+    tok = np.zeros(cap, np.int32)
+    ls = np.zeros(cap, np.float32)
+    keys = [drafter.root_key()]
+    n_nodes = 1
+    lo, hi = 0, 1
+    margins = []
+    for _ in range(layers):
+        rows = drafter.rows(keys[lo:hi])
+        n_new, m = expand_topn(rows, np.arange(lo, hi, dtype=np.int32), ls[lo:hi], width, cap,
+                               par, tok, ls, n_nodes)
+        margins.append(m)
+        for j in range(n_nodes, n_new):
+            keys.append(drafter.child_key(keys[par[j]], tok[j]))
+        lo, hi, n_nodes = n_nodes, n_new, n_new
+    sel = select_topn(par[None, :n_nodes], tok[None, :n_nodes], ls[None, :n_nodes],
+                      [n_nodes], n)
+    return dict(parent=par[:n_nodes].copy(), token=tok[:n_nodes].copy(),
+                logscore=ls[:n_nodes].copy(), n=n_nodes, margins=margins,
+                selected={k: v[0] for k, v in sel.items()})
 
 
 def commit_path(k, v, kv_len, path, accept_len):

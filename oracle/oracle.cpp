@@ -23,7 +23,8 @@
 //           verifies the whole tree; greedy walk).
 //   The commit of the accepted branch into the cache follows [SPEC] step 4
 //   and [OPT] §2 (see or_commit_path); the expected acceptance length of a
-//   tree follows [OPT] §3 (see or_expected_accept).
+//   tree follows [OPT] §3 (see or_expected_accept), and so do OPT-Tree's
+//   greedy expansion and subtree selection (or_expand_topn, or_select_topn).
 //   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
 //           1, 2, 3" (SC'11): the Philox4x64-10 counter-based generator.
 //
@@ -48,6 +49,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <vector>
 
 namespace {
@@ -460,6 +462,137 @@ int or_expand_gated(const float* draft_logits, const int32_t* frontier_node,
     tree_logscore[n0 + t] = (float)pass[t].ls;
   }
   *n_nodes = n0 + (int)pass.size();
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// OPT-Tree greedy expansion, one layer [OPT] §3: a node's score is the
+// product of the draft probabilities along its path (kept as its log); the
+// frontier nodes are expanded, every child of every frontier node is a
+// candidate (log score = the parent's + the child's log draft probability),
+// and the layer keeps the `width` best candidates, which become the next
+// frontier.  Ties go to the lower (parent, token).  The kept candidates are
+// appended at n_nodes.. in (parent asc, score desc, token asc) order; a layer
+// keeps at most capacity - n_nodes.  margin: the score gap at the cut between
+// candidates of different parents (rounding can only reorder those).
+// ---------------------------------------------------------------------------
+int or_expand_topn(const float* draft_logits, const int32_t* frontier_node,
+                   const float* frontier_logscore, int F, int V, int width, int capacity,
+                   int32_t* tree_parent, int32_t* tree_token, float* tree_logscore,
+                   int32_t* n_nodes, double* margin) {
+  *margin = INFINITY;
+  if (F < 0 || V < 1 || width < 1 || capacity < 1) return ST_INVALID_ARG;
+  const int n0 = *n_nodes;
+  const int limit = std::min(width, capacity - n0);
+  if (limit <= 0 || F == 0) return ST_OK;
+  std::vector<Cand> all;
+  all.reserve((size_t)F * V);
+  for (int v = 0; v < F; ++v) {
+    const float* row = draft_logits + (size_t)v * V;
+    const double lse = row_logsumexp(row, V, 1.0);
+    for (int c = 0; c < V; ++c)
+      all.push_back({(double)frontier_logscore[v] + ((double)row[c] - lse), frontier_node[v], c});
+  }
+  auto better = [](const Cand& a, const Cand& b) {
+    if (a.ls != b.ls) return a.ls > b.ls;
+    if (a.parent != b.parent) return a.parent < b.parent;
+    return a.token < b.token;
+  };
+  // the best limit + 1 in order (a library partial sort), then the cut
+  const size_t head = std::min(all.size(), (size_t)limit + 1);
+  std::partial_sort(all.begin(), all.begin() + head, all.end(), better);
+  if (all.size() > (size_t)limit) {
+    if (all[limit - 1].parent != all[limit].parent)
+      *margin = all[limit - 1].ls - all[limit].ls;
+    all.resize(limit);
+  }
+  std::sort(all.begin(), all.end(), [](const Cand& a, const Cand& b) {
+    if (a.parent != b.parent) return a.parent < b.parent;
+    if (a.ls != b.ls) return a.ls > b.ls;
+    return a.token < b.token;
+  });
+  for (size_t t = 0; t < all.size(); ++t) {
+    tree_parent[n0 + t] = all[t].parent;
+    tree_token[n0 + t] = all[t].token;
+    tree_logscore[n0 + t] = (float)all[t].ls;
+  }
+  *n_nodes = n0 + (int)all.size();
+  return ST_OK;
+}
+
+// ---------------------------------------------------------------------------
+// OPT-Tree subtree selection [OPT] §3: of a candidate tree whose scores never
+// rise from a node to its child, keep the n best-scoring nodes (ties to the
+// lower node id, so a parent always ranks before its child); by that
+// monotonicity they contain the root and every kept node's parent, i.e. they
+// form a subtree, the one of n nodes with the largest sum of scores.
+//   parent, token, logscore [B, M]; n_nodes [B] nodes in use (1..M).
+//   out_* [B, n]: the kept nodes renumbered in their original order (so still
+//   topological); out_src = the node's id in the input; rows k..n-1 (k =
+//   min(n, n_nodes)) are -1 / 0.  expected[b] = sum of exp(logscore) over the
+//   kept nodes other than the root (the expected acceptance length).
+//   status: ST_INVALID_TREE for a malformed parent array or a kept node whose
+//   parent is not kept (scores not monotone), ST_INVALID_ARG for a NaN score
+//   or n_nodes outside 1..M; outputs of such a tree are -1 / 0.
+// ---------------------------------------------------------------------------
+int or_select_topn(const int32_t* parent, const int32_t* token, const float* logscore,
+                   const int32_t* n_nodes, int B, int M, int n, int32_t* out_parent,
+                   int32_t* out_token, float* out_logscore, int32_t* out_src, float* expected,
+                   int32_t* status) {
+  if (B < 0 || M < 1 || n < 1) return ST_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent + (size_t)b * M;
+    const float* ls = logscore + (size_t)b * M;
+    int32_t* op = out_parent + (size_t)b * n;
+    int32_t* ot = out_token + (size_t)b * n;
+    float* ol = out_logscore + (size_t)b * n;
+    int32_t* os = out_src + (size_t)b * n;
+    for (int j = 0; j < n; ++j) {
+      op[j] = -1;
+      ot[j] = -1;
+      ol[j] = 0.0f;
+      os[j] = -1;
+    }
+    expected[b] = 0.0f;
+    const int m = n_nodes[b];
+    int st = ST_OK;
+    if (m < 1 || m > M) st = ST_INVALID_ARG;
+    for (int i = 0; st == ST_OK && i < m; ++i) {
+      if (i == 0 ? par[0] != -1 : (par[i] < 0 || par[i] >= i)) st = ST_INVALID_TREE;
+      else if (std::isnan(ls[i])) st = ST_INVALID_ARG;
+    }
+    if (st == ST_OK) {
+      std::vector<int> order(m);
+      for (int i = 0; i < m; ++i) order[i] = i;
+      std::sort(order.begin(), order.end(), [&](int a, int c) {
+        if (ls[a] != ls[c]) return ls[a] > ls[c];
+        return a < c;
+      });
+      const int k = std::min(n, m);
+      std::vector<char> kept(m, 0);
+      for (int r = 0; r < k; ++r) kept[order[r]] = 1;
+      std::vector<int> newid(m, -1);
+      int next = 0;
+      for (int i = 0; i < m; ++i)
+        if (kept[i]) newid[i] = next++;
+      for (int i = 1; i < m; ++i)
+        if (kept[i] && !kept[par[i]]) st = ST_INVALID_TREE;
+      if (st == ST_OK) {
+        double e = 0.0;
+        for (int i = 0; i < m; ++i) {
+          if (!kept[i]) continue;
+          const int j = newid[i];
+          op[j] = i == 0 ? -1 : newid[par[i]];
+          ot[j] = token[(size_t)b * M + i];
+          ol[j] = ls[i];
+          os[j] = i;
+          if (i != 0) e += exp((double)ls[i]);
+        }
+        expected[b] = (float)e;
+      }
+    }
+    status[b] = st;
+  }
   return ST_OK;
 }
 
