@@ -56,6 +56,9 @@ def parse_args():
     p.add_argument("--ncu-steps", type=int, default=0,
                    help="profiling driver: run this many eager steps of the workload on "
                         "one input set (no graphs, no timing) and exit; for ncu captures")
+    p.add_argument("--ncu-workload", choices=["verify", "opt_tree"], default="verify",
+                   help="what --ncu-steps runs: the verify step, or one OPT-Tree growth "
+                        "(16 layers of width 256 over vocab 128256, then the selection)")
     return p.parse_args()
 
 
@@ -437,6 +440,82 @@ def measure_talon_expansion(torch, tv, device, stream, hbm):
     }
 
 
+def opt_tree_setup(torch, tv, device):
+    """OPT-Tree growth at the long-context workload's shape: 16 layers of
+    width 256 over a 128,256-token vocabulary (N(0, 3) draft rows, drawn once
+    per layer and resident), then the 256 best nodes of the 4,097-node
+    candidate tree.  The layer sizes follow from width, vocabulary and
+    capacity, so nothing is read back between layers.  Returns the build and
+    select closures and the state they work on."""
+    width, layers, n_keep, V = 256, 16, 256, 128256
+    cap = 1 + width * layers
+    gen_t = torch.Generator(device=device)
+    gen_t.manual_seed(5)
+    F, lo = [], []
+    a, b = 0, 1          # the frontier is the id range [a, b): the previous layer
+    for _ in range(layers):
+        F.append(b - a)
+        lo.append(a)
+        a, b = b, b + min(width, (b - a) * V, cap - b)
+    rows = [torch.randn((f, V), generator=gen_t, device=device) * 3.0 for f in F]
+    st = dict(width=width, layers=layers, n_keep=n_keep, V=V, cap=cap, F=F, rows=rows,
+              par=torch.full((cap,), -1, dtype=torch.int32, device=device),
+              tok=torch.zeros(cap, dtype=torch.int32, device=device),
+              ls=torch.zeros(cap, dtype=torch.float32, device=device),
+              ids=torch.arange(cap, dtype=torch.int32, device=device),
+              n_dev=torch.ones(1, dtype=torch.int32, device=device),
+              m_dev=torch.full((1,), cap, dtype=torch.int32, device=device))
+    tv.workspace("expand", tv.expand_workspace_size(max(F), V), device)
+    st["sel"] = tv.select_topn(st["par"][None], st["tok"][None], st["ls"][None], st["m_dev"],
+                               n_keep)
+
+    def f_select():
+        tv.select_topn(st["par"][None], st["tok"][None], st["ls"][None], st["m_dev"], n_keep,
+                       st["sel"])
+
+    def f_build():
+        st["n_dev"].fill_(1)
+        for r_, l0, f in zip(rows, lo, F):
+            tv.expand_topn(r_, st["ids"][l0:l0 + f], st["ls"][l0:l0 + f], width, cap, st["par"],
+                           st["tok"], st["ls"], st["n_dev"])
+        f_select()
+
+    return f_build, f_select, st
+
+
+def check_opt_tree(st):
+    par, ls, ids = st["par"], st["ls"], st["ids"]
+    assert int(st["n_dev"].item()) == st["cap"] and int(st["sel"]["status"][0]) == 0
+    assert bool((par[1:] < ids[1:]).all()) and bool((ls[1:] <= ls[par[1:].long()]).all())
+
+
+def measure_opt_tree(torch, tv, device, stream, hbm):
+    """Times opt_tree_setup's growth, every launch from the root replayed in
+    one graph, and the selection alone."""
+    f_build, f_select, st = opt_tree_setup(torch, tv, device)
+    with torch.cuda.stream(stream):
+        f_build()
+    torch.cuda.synchronize()
+    check_opt_tree(st)
+    us = graph_time_us(torch, stream, f_build, 5, 3)
+    us_sel = graph_time_us(torch, stream, f_select, 20, 5)
+    # the method reads every frontier row's draft logits once (4 V bytes a row)
+    V, F = st["V"], st["F"]
+    nbytes = sum(4 * f * V for f in F)
+    out = {
+        "workload": f"OPT-Tree growth: {st['layers']} layers of width {st['width']}, vocab {V}, "
+                    f"N(0, 3) draft rows, then the {st['n_keep']} best of {st['cap']} nodes",
+        "us_per_build": us, "layers": st["layers"], "frontier_rows": int(sum(F)),
+        "bytes": nbytes, "roofline_us": nbytes / (hbm * 1e9) * 1e6,
+        "frac": nbytes / (hbm * 1e9) * 1e6 / us,
+        "select_topn": {"us_per_launch": us_sel, "nodes": st["cap"], "kept": st["n_keep"],
+                        "expected_accept_len": float(st["sel"]["expected"][0]),
+                        "bound": "latency (one CTA, 16 KB of keys)"},
+    }
+    del st
+    return out
+
+
 def measure_other_configs(torch, tv, device, hbm, tflops):
     """Long context (greedy), batched stochastic acceptance, TALON expansion
     and its 512-node verify."""
@@ -477,6 +556,7 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
         "head_dim 128, vocab 128256, p/q acceptance at T = 1", case, "sample", torch, tv, device,
         stream, hbm, tflops, l2)
     del case
+    res["opt_tree_growth"] = measure_opt_tree(torch, tv, device, stream, hbm)
     tree, res["talon_expansion"] = measure_talon_expansion(torch, tv, device, stream, hbm)
     case = gen.config3_verify(tree["parent"].numpy().astype(np.int32), 0,
                               tokens=tree["token"].numpy().astype(np.int32))
@@ -499,6 +579,14 @@ def run_ncu_steps(args):
     from workloads import gen
 
     device = torch.device("cuda", 0)
+    if args.ncu_workload == "opt_tree":
+        f_build, _, st = opt_tree_setup(torch, tv, device)
+        for _ in range(args.ncu_steps):
+            f_build()
+        torch.cuda.synchronize()
+        check_opt_tree(st)
+        print(json.dumps({"ncu_steps": args.ncu_steps, "workload": "opt_tree"}), flush=True)
+        return
     case = gen.config2()
     s = make_sets(case, torch, device, 0)[0][0]
     for _ in range(args.ncu_steps):

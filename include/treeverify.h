@@ -18,6 +18,9 @@
  *                     resampling, Philox4x64-10 random numbers
  *   tv_expand_gated   one layer of TALON's budget-driven, confidence-gated
  *                     tree expansion (root Top-K, anchor, alpha gate, budget)
+ *   tv_expand_topn,   OPT-Tree's greedy expansion (one layer: the `width`
+ *   tv_select_topn    best children of the frontier) and its subtree
+ *                     selection (the n best nodes of the candidate tree)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -368,6 +371,65 @@ tv_status tv_expand_gated(const float* draft_logits, const int32_t* frontier_nod
                           float alpha, int budget, int32_t* tree_parent, int32_t* tree_token,
                           float* tree_logscore, int32_t* n_nodes, void* workspace,
                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tv_expand_topn -- one layer of OPT-Tree's greedy tree expansion.
+ * (OPT-Tree §3: a node's score is the product of the draft probabilities
+ * along its path; the frontier nodes are expanded and the layer keeps the
+ * highest-scoring children, which are the next frontier.)
+ *
+ *   draft_logits      float [F, V]  draft logits of the F frontier nodes.
+ *   frontier_node     int32 [F]     their node ids (ascending).
+ *   frontier_logscore float [F]     their log path scores (root: 0).
+ *   width             children kept by the layer, 1..2048: the best ones over
+ *                     all F x V candidates (log score = the parent's + the
+ *                     child's log-softmax value), ties to the lower
+ *                     (parent, token).  F <= 2048.
+ *   capacity          length of the tree arrays; the layer keeps
+ *                     min(width, F x V, capacity - n_nodes) children, a number
+ *                     the host can know without reading the device.
+ *   tree_parent, tree_token int32 [capacity], tree_logscore float [capacity]:
+ *                     the kept children are appended at ids n_nodes.. in
+ *                     (parent asc, score desc, token asc) order.
+ *   n_nodes, workspace as for tv_expand_gated (the same workspace layout and
+ *                     size, tv_expand_workspace_size(F, V), zero-filled before
+ *                     its first use and returned zero-filled).
+ * The same three launches as tv_expand_gated, without the gate; a chunk that
+ * holds more than `width` candidates raises a floor under the layer's cut so
+ * that later chunks pass on only what can still be kept.
+ */
+tv_status tv_expand_topn(const float* draft_logits, const int32_t* frontier_node,
+                         const float* frontier_logscore, int F, int V, int width, int capacity,
+                         int32_t* tree_parent, int32_t* tree_token, float* tree_logscore,
+                         int32_t* n_nodes, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tv_select_topn -- OPT-Tree's subtree selection: the n best nodes.
+ * (OPT-Tree §3: keep the n highest-scoring nodes of the candidate tree; as a
+ * node never scores above its parent, they form a subtree containing the
+ * root, the one of n nodes with the largest expected acceptance length.)
+ *
+ *   parent, token int32 [B, M], logscore float [B, M]: B candidate trees
+ *                 (topological order, parent[0] = -1), M <= 16384.
+ *   n_nodes       int32 [B]: nodes in use per tree, 1..M.
+ *   n             nodes to keep (>= 1); ties go to the lower node id.
+ *   out_parent, out_token, out_src int32 [B, n], out_logscore float [B, n]:
+ *                 the kept nodes renumbered in their original order (still
+ *                 topological); out_src = a node's id in the input.  Rows
+ *                 k .. n-1, k = min(n, n_nodes[b]), are -1 (0 for scores).
+ *   expected      float [B]: sum of exp(logscore) over the kept nodes other
+ *                 than the root (OPT-Tree's expected acceptance length).
+ *   status        int32 [B]: 0; TV_ERR_INVALID_TREE for a malformed parent
+ *                 array or a kept node whose parent was not kept (scores that
+ *                 rise along a path); TV_ERR_INVALID_ARG for a NaN score or
+ *                 n_nodes outside 1..M.  The outputs of such a tree are -1 / 0.
+ * One CTA per tree: a radix select of the score keys in shared memory, then
+ * block scans over the ids.  Scores are compared as fp32 values (-0 = +0).
+ */
+tv_status tv_select_topn(const int32_t* parent, const int32_t* token, const float* logscore,
+                         const int32_t* n_nodes, int B, int M, int n, int32_t* out_parent,
+                         int32_t* out_token, float* out_logscore, int32_t* out_src,
+                         float* expected, int32_t* status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

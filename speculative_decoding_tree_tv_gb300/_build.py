@@ -13,7 +13,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtreeverify.so")
 
 SOURCES = ["tv_api.cu", "tv_tree.cu", "tv_greedy.cu", "tv_sample.cu", "tv_expand.cu",
-           "tv_attn.cu", "tv_commit.cu", "tv_expected.cu", "tv_spine.cpp"]
+           "tv_attn.cu", "tv_commit.cu", "tv_expected.cu", "tv_topn.cu", "tv_spine.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-I" + CSRC, "--expt-relaxed-constexpr"]

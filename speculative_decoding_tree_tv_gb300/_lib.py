@@ -61,6 +61,8 @@ _SIGS = {
     "tv_build_spine_tree": (_I, [_P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P]),
     "tv_spine_ratio_update": (_F, [_F, _F, _F]),
     "tv_expand_gated": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tv_expand_topn": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tv_select_topn": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 for _name, (_res, _args) in _SIGS.items():

@@ -275,6 +275,94 @@ def expand_gated(draft_logits: torch.Tensor, frontier_node: torch.Tensor,
         ws.numel(), _stream(dev)))
 
 
+def expand_topn(draft_logits: torch.Tensor, frontier_node: torch.Tensor,
+                frontier_logscore: torch.Tensor, width: int, capacity: int,
+                tree_parent: torch.Tensor, tree_token: torch.Tensor, tree_logscore: torch.Tensor,
+                n_nodes: torch.Tensor, ws: Optional[torch.Tensor] = None) -> None:
+    """One OPT-Tree layer: appends the `width` best children of the frontier
+    to the tree_* tensors (length >= capacity) and bumps n_nodes (device int32[1])."""
+    _need(draft_logits, "draft_logits", torch.float32)
+    F, V = draft_logits.shape
+    dev = draft_logits.device
+    _need(frontier_node, "frontier_node", torch.int32, (F,), dev)
+    _need(frontier_logscore, "frontier_logscore", torch.float32, (F,), dev)
+    _need(tree_parent, "tree_parent", torch.int32, device=dev)
+    _need(tree_token, "tree_token", torch.int32, device=dev)
+    _need(tree_logscore, "tree_logscore", torch.float32, device=dev)
+    _need(n_nodes, "n_nodes", torch.int32, (1,), dev)
+    if min(tree_parent.numel(), tree_token.numel(), tree_logscore.numel()) < capacity:
+        raise ValueError("tree arrays must hold `capacity` nodes")
+    ws = workspace("expand", expand_workspace_size(F, V), dev) if ws is None else ws
+    check("tv_expand_topn", lib.tv_expand_topn(
+        draft_logits.data_ptr(), frontier_node.data_ptr(), frontier_logscore.data_ptr(), F, V,
+        int(width), int(capacity), tree_parent.data_ptr(), tree_token.data_ptr(),
+        tree_logscore.data_ptr(), n_nodes.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)))
+
+
+def select_topn(parent: torch.Tensor, token: torch.Tensor, logscore: torch.Tensor,
+                n_nodes: torch.Tensor, n: int, out: Optional[dict] = None) -> dict:
+    """OPT-Tree subtree selection over B candidate trees [B, M]: the n best
+    nodes, renumbered.  Returns dict(parent, token, logscore, src [B, n],
+    expected [B], status [B]) of device tensors (or fills `out`)."""
+    _need(parent, "parent", torch.int32)
+    B, M = parent.shape
+    dev = parent.device
+    _need(token, "token", torch.int32, (B, M), dev)
+    _need(logscore, "logscore", torch.float32, (B, M), dev)
+    _need(n_nodes, "n_nodes", torch.int32, (B,), dev)
+    if out is None:
+        out = dict(parent=torch.empty((B, n), dtype=torch.int32, device=dev),
+                   token=torch.empty((B, n), dtype=torch.int32, device=dev),
+                   logscore=torch.empty((B, n), dtype=torch.float32, device=dev),
+                   src=torch.empty((B, n), dtype=torch.int32, device=dev),
+                   expected=torch.empty(B, dtype=torch.float32, device=dev),
+                   status=torch.empty(B, dtype=torch.int32, device=dev))
+    check("tv_select_topn", lib.tv_select_topn(
+        parent.data_ptr(), token.data_ptr(), logscore.data_ptr(), n_nodes.data_ptr(), B, M,
+        int(n), out["parent"].data_ptr(), out["token"].data_ptr(), out["logscore"].data_ptr(),
+        out["src"].data_ptr(), out["expected"].data_ptr(), out["status"].data_ptr(),
+        _stream(dev)))
+    return out
+
+
+def grow_opt_tree(draft_rows: Callable, root_key, child_key: Callable, width: int, layers: int,
+                  n: int, device) -> dict:
+    """Grow an OPT-Tree candidate tree of `layers` layers (the root's is
+    layer 1) of `width` nodes each, calling the drafter between layers, then
+    keep its n best nodes (OPT-Tree §3).  Layer sizes follow from width, V and
+    the capacity, so the layers are enqueued without reading the device; the
+    drafter's keys for the new nodes are read back once per layer.  Returns
+    dict(parent, token, logscore, n (the candidate tree, cpu), selected
+    (select_topn's output for the one tree, cpu))."""
+    dev = torch.device(device)
+    cap = 1 + width * layers
+    par = torch.full((cap,), -1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(cap, dtype=torch.int32, device=dev)
+    ls = torch.zeros(cap, dtype=torch.float32, device=dev)
+    node_ids = torch.arange(cap, dtype=torch.int32, device=dev)
+    n_dev = torch.ones(1, dtype=torch.int32, device=dev)
+    keys = [root_key]
+    lo, hi = 0, 1
+    for _ in range(layers):
+        rows = torch.as_tensor(draft_rows(keys[lo:hi]), dtype=torch.float32).to(dev).contiguous()
+        F, V = rows.shape
+        k = min(width, F * V, cap - hi)
+        if k <= 0:
+            break
+        expand_topn(rows, node_ids[lo:hi], ls[lo:hi], width, cap, par, tok, ls, n_dev)
+        new_par = par[hi:hi + k].cpu().tolist()
+        new_tok = tok[hi:hi + k].cpu().tolist()
+        for p, t in zip(new_par, new_tok):
+            keys.append(child_key(keys[p], t))
+        lo, hi = hi, hi + k
+    m = hi
+    sel = select_topn(par[None, :m].contiguous(), tok[None, :m].contiguous(),
+                      ls[None, :m].contiguous(), torch.tensor([m], dtype=torch.int32, device=dev),
+                      n)
+    return dict(parent=par[:m].cpu(), token=tok[:m].cpu(), logscore=ls[:m].cpu(), n=m,
+                n_device=int(n_dev.item()), selected={k: v[0].cpu() for k, v in sel.items()})
+
+
 def expand_tree(draft_rows: Callable, root_key, child_key: Callable, topk: int, alpha: float,
                 budget: int, device, max_layers: int = 100000) -> dict:
     """Grow a TALON tree until the budget is spent (TALON §5.1), calling the

@@ -3,6 +3,10 @@
 // expansion: candidate pool = all children of the frontier, path score
 // s(c) = prod p_d, anchor = max s, keep s >= alpha * s_anchor, and keep the
 // best-scoring ones when more survive than the remaining budget).
+// tv_expand_topn: one layer of OPT-Tree's greedy expansion (OPT-Tree §3:
+// every child of every frontier node is a candidate, scored by its path's
+// draft probability, and the layer keeps the `width` best); the same three
+// launches without the gate.
 //
 // Three launches, all on the caller's stream:
 //   1. stats:   per (frontier row, 2048-logit chunk) max and sum exp; the last
@@ -10,17 +14,29 @@
 //               and offset off_v = logscore_v - lse_v (log s of token c in
 //               row v is off_v + logit) and raises the layer's anchor (the
 //               best score) with one atomic max;
-//   2. filter:  each CTA turns the fp64 gate into an fp32 logit threshold for
-//               its row, streams its chunk again and appends the (row, token)
-//               candidates that pass, with their order-preserving fp64 score
-//               keys (at most the layer's limit per chunk, its best ones);
+//   1b. floor:  (OPT-Tree layers only) one CTA sets the layer's floor to
+//               (just under) the limit-th best score among the chunks'
+//               maxima: they are distinct candidates, so the layer's
+//               limit-th best scores at least that much, and it is close to
+//               the cut;
+//   2. filter:  each CTA turns the fp64 gate (if any) and the layer's floor
+//               into an fp32 logit threshold for its row, streams its chunk
+//               again and appends the (row, token) candidates that pass, with
+//               their order-preserving fp64 score keys (at most the layer's
+//               limit per chunk, its best ones).  A chunk holding more than
+//               `limit` candidates raises the floor to its limit-th best key:
+//               the layer's limit-th best is at least that, so chunks that run
+//               later skip everything below it.  The filter visits the
+//               (row, chunk) pairs in the reverse of the stats order, so that
+//               it starts on what the stats pass read last (still in L2);
 //   3. select:  one CTA keeps the best `limit` candidates (radix select on the
 //               score keys staged in shared memory, starting at the first
 //               byte in which the keys differ; ties to the lower
 //               (parent, token)), orders them (parent asc, score desc, token
 //               asc), appends them to the tree and returns the control words
-//               (candidate count, anchor) to zero for the next call.
+//               (candidate count, anchor, floor) to zero for the next call.
 // Scores are fp64 in the log domain; logits stay fp32.
+#include <algorithm>
 #include <climits>
 
 #include "tv_common.cuh"
@@ -29,6 +45,8 @@ namespace tv {
 namespace {
 
 constexpr int kExpThreads = 256;
+constexpr int kStatsWarps = 8;   // chunks per stats CTA, one warp each
+constexpr int kFiltChunks = 4;   // chunks per filter CTA
 constexpr int kExpChunk = 2048;
 constexpr int kSelThreads = 1024;
 constexpr int kMaxBudget = 2048;
@@ -37,8 +55,8 @@ constexpr int kSelBatch = 8;  // key loads in flight per thread in the select pa
 constexpr int kSelStageKeys = 16384;  // candidates whose keys the select stages in shared memory
 
 struct ExpPartial {
-  double s;
-  float m;
+  double s;  // sum of exp(x - m) over the chunk
+  float m;   // the chunk's largest logit
   float pad;
 };
 struct ExpRow {
@@ -52,6 +70,7 @@ struct ExpCtl {
   int n0;                    // nodes in the tree before this layer
   int pad;
   unsigned long long anchor;  // order-preserving key of the best score (returned to 0)
+  unsigned long long floor;   // key no kept candidate lies below (returned to 0)
 };
 
 struct ExpWs {
@@ -83,13 +102,19 @@ __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, si
   return o;
 }
 
-__device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* p) {
+__device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* p, unsigned int n) {
   unsigned int old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(n)
+               : "memory");
   return old;
 }
 
-__global__ void __launch_bounds__(kExpThreads)
+// One warp per 2048-logit chunk (64 logits a lane, all loads in flight at
+// once), kStatsWarps chunks of one row per CTA.  Each warp writes its chunk's
+// partial (max, sum of exp(x - max)); the CTA then arrives on the row's counter
+// with its number of chunks, and warp 0 of the row's last CTA combines the
+// row's partials.
+__global__ void __launch_bounds__(kStatsWarps * 32)
 exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
                  const float* __restrict__ frontier_logscore, ExpWs ws) {
   __shared__ int s_last;
@@ -97,71 +122,72 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
   pdl_wait();
   ExpPartial* __restrict__ part = ws.part;
   const int row = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * kStatsWarps + warp;
   const float* x = logits + (size_t)row * V;
-  const int start = blockIdx.x * kExpChunk;
-  const int stop = min(V, start + kExpChunk);
-  const int tid = threadIdx.x;
-  constexpr int kPer = kExpChunk / kExpThreads;
-  float a[kPer];
-  if ((V & 3) == 0) {
-    const float4* x4 = reinterpret_cast<const float4*>(x);
+  if (c < chunks) {
+    const int start = c * kExpChunk;
+    const int stop = min(V, start + kExpChunk);
+    constexpr int kPer = kExpChunk / 32;
+    float a[kPer];
+    if ((V & 3) == 0) {  // rows 16-byte aligned; a chunk holds whole float4s
+      const float4* x4 = reinterpret_cast<const float4*>(x);
 #pragma unroll
-    for (int u = 0; u < kPer / 4; ++u) {
-      const int e = start + 4 * (tid + u * kExpThreads);
-      const float4 f = (e < stop) ? ld_stream_f4(x4 + (e >> 2))
-                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      a[4 * u + 0] = f.x;
-      a[4 * u + 1] = f.y;
-      a[4 * u + 2] = f.z;
-      a[4 * u + 3] = f.w;
+      for (int u = 0; u < kPer / 4; ++u) {
+        const int e = start + 4 * (lane + 32 * u);
+        const float4 f = (e < stop) ? ld_stream_f4(x4 + (e >> 2))
+                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        a[4 * u + 0] = f.x;
+        a[4 * u + 1] = f.y;
+        a[4 * u + 2] = f.z;
+        a[4 * u + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = start + lane + 32 * u;
+        a[u] = (e < stop) ? __ldg(x + e) : -INFINITY;
+      }
     }
-  } else {
+    float m = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int e = start + tid + u * kExpThreads;
-      a[u] = (e < stop) ? __ldg(x + e) : -INFINITY;
+    for (int u = 0; u < kPer; ++u) m = fmaxf(m, a[u]);
+    m = warp_max(m);
+    float sl = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) sl += (a[u] == -INFINITY) ? 0.0f : expf(a[u] - m);
+    const double sd = warp_sum_d((double)sl);
+    if (lane == 0) {
+      part[(size_t)row * chunks + c] = ExpPartial{sd, m, 0.0f};
+      __threadfence();  // the partial is visible before the CTA arrives
     }
   }
-  float m = -INFINITY;
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) m = fmaxf(m, a[u]);
-  __shared__ float s_m[kExpThreads / 32];
-  __shared__ double s_s[kExpThreads / 32];
-  m = warp_max(m);
-  if ((tid & 31) == 0) s_m[tid >> 5] = m;
   __syncthreads();
-  m = s_m[0];
-#pragma unroll
-  for (int w = 1; w < kExpThreads / 32; ++w) m = fmaxf(m, s_m[w]);
-  float s = 0.0f;
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) s += (a[u] == -INFINITY) ? 0.0f : expf(a[u] - m);
-  const double sd = warp_sum_d((double)s);
-  if ((tid & 31) == 0) s_s[tid >> 5] = sd;
-  __syncthreads();
-  if (tid == 0) {
-    double tot = 0.0;
-#pragma unroll
-    for (int w = 0; w < kExpThreads / 32; ++w) tot += s_s[w];
-    part[(size_t)row * chunks + blockIdx.x] = ExpPartial{tot, m, 0.0f};
-    // the partial is released before the arrival; the last arrival acquires all
-    s_last = (arrive_acq_rel(&ws.arrivals[row]) == (unsigned int)chunks - 1u);
+  if (threadIdx.x == 0) {
+    const unsigned int mine = (unsigned int)min(kStatsWarps, chunks - (int)blockIdx.x * kStatsWarps);
+    // the last arrival (acquire) sees every partial of the row
+    s_last = (arrive_acq_rel(&ws.arrivals[row], mine) + mine == (unsigned int)chunks);
   }
   __syncthreads();
-  if (!s_last || tid != 0) return;
-  // the last CTA of the row: normaliser, offset and best score of the row.
-  // Chunk scale factors on the SFU (fp32, within a few ulp; fp64 runs at a
-  // small fraction of the fp32 rate here), the sum itself in fp64.
-  ws.arrivals[row] = 0u;
+  if (!s_last || warp != 0) return;
+  // warp 0 of the row's last CTA: normaliser, offset and best score of the
+  // row.  Chunk scale factors on the SFU (fp32, within a few ulp; fp64 runs
+  // at a small fraction of the fp32 rate here), the sum itself in fp64.
   const ExpPartial* p = part + (size_t)row * chunks;
   float mr = -INFINITY;
-  for (int c = 0; c < chunks; ++c) mr = fmaxf(mr, __ldcg(&p[c].m));
+  for (int k = lane; k < chunks; k += 32) mr = fmaxf(mr, __ldcg(&p[k].m));
+  mr = warp_max(mr);
   double sr = 0.0;
-  for (int c = 0; c < chunks; ++c) sr += __ldcg(&p[c].s) * (double)expf(__ldcg(&p[c].m) - mr);
-  const double off = (double)frontier_logscore[row] - ((double)mr + log(sr));
-  ws.rows[row].off = off;
-  ws.rows[row].m = mr;
-  atomicMax(&ws.ctl->anchor, double_key(off + (double)mr));
+  for (int k = lane; k < chunks; k += 32)
+    sr += __ldcg(&p[k].s) * (double)expf(__ldcg(&p[k].m) - mr);
+  sr = warp_sum_d(sr);
+  if (lane == 0) {
+    ws.arrivals[row] = 0u;
+    const double off = (double)frontier_logscore[row] - ((double)mr + log(sr));
+    ws.rows[row].off = off;
+    ws.rows[row].m = mr;
+    atomicMax(&ws.ctl->anchor, double_key(off + (double)mr));
+  }
 }
 
 // Smallest fp32 value >= x (x finite).
@@ -171,15 +197,115 @@ __device__ __forceinline__ float float_ceil_of(double x) {
   return f;
 }
 
-// One CTA per (frontier row, chunk of the row).  The chunk's candidates (logit
-// >= the row's threshold) are gathered in shared memory with their score keys.
-// When there are more than the layer may keep (`limit`), only the chunk's best
-// `limit` under the output's total order (score desc, then token asc within a
-// row) are appended: the layer's best `limit` overall are among them, and the
-// select kernel then sees at most chunks x limit candidates per row (at the
-// root layer, 10 per chunk instead of all 2048).
+// Inverse of double_key.
+__device__ __forceinline__ double key_double(unsigned long long k) {
+  const unsigned long long u = (k & 0x8000000000000000ull) ? (k & 0x7fffffffffffffffull) : ~k;
+  return __longlong_as_double((long long)u);
+}
+
+constexpr int kFloorThreads = 1024;
+constexpr int kFloorBins = 2048;      // bins below the anchor ...
+constexpr double kFloorBinsPerNat = 64.0;  // ... each 1/64 nat wide (32 nats in all)
+constexpr int kFloorBatch = 16;       // chunk maxima a thread loads at once
+
+// One CTA: a floor under the layer's limit-th best score from the chunks'
+// maxima (distinct candidates, so at least `limit` candidates score as much
+// as the limit-th best of them).  Each maximum's distance below the anchor
+// (the layer's best score) is counted in 1/64-nat bins; the first bin from
+// the top at which the count reaches `limit` gives the floor, its lower edge
+// less a margin (a little under the exact value, which is all a floor needs).
+// The distances are fp32 (the row's offset from the anchor once per row in
+// fp64); the 1e-3-nat margin covers their rounding.  Maxima more than 32 nats
+// down are not counted; if fewer than `limit` are left there is no floor (it
+// stays 0).  With fewer chunks than `limit` (a few rows: the root layer) every
+// logit of the rows is counted instead.
+__global__ void __launch_bounds__(kFloorThreads)
+exp_floor_kernel(const float* __restrict__ logits, int V, int F, int chunks, int cap, int budget,
+                 const int32_t* __restrict__ n_nodes, ExpWs ws) {
+  __shared__ unsigned int s_hist[kFloorBins];
+  __shared__ float s_av[kMaxBudget];  // anchor - off_v, per frontier row
+  __shared__ unsigned int s_wsum[kFloorThreads / 32];
+  __shared__ int s_bin;
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int remaining = budget - *n_nodes;
+  const int limit = min(remaining > 0 ? remaining : 0, cap);
+  // the values counted: the chunks' maxima, or with too few chunks, every logit
+  const bool all = F * chunks < limit;
+  const int per_row = all ? V : chunks;
+  const int total = F * per_row;
+  if (limit == 0 || total < limit) return;
+  const double anchor = key_double(ws.ctl->anchor);
+  for (int i = tid; i < kFloorBins; i += kFloorThreads) s_hist[i] = 0u;
+  for (int r = tid; r < F; r += kFloorThreads) s_av[r] = (float)(anchor - ws.rows[r].off);
+  if (tid == 0) s_bin = -1;
+  __syncthreads();
+  const float inv_per_row = 1.0f / (float)per_row;
+  for (int i0 = 0; i0 < total; i0 += kFloorBatch * kFloorThreads) {
+    float mx[kFloorBatch];  // a batch of values, their loads in flight together
+#pragma unroll
+    for (int u = 0; u < kFloorBatch; ++u) {
+      const int i = i0 + tid + u * kFloorThreads;
+      mx[u] = (i >= total) ? -INFINITY : all ? __ldg(logits + i) : __ldcg(&ws.part[i].m);
+    }
+#pragma unroll
+    for (int u = 0; u < kFloorBatch; ++u) {
+      const int i = i0 + tid + u * kFloorThreads;
+      int r = (int)((float)i * inv_per_row);  // the row of value i, corrected to be exact
+      r -= (r * per_row > i);
+      r += ((r + 1) * per_row <= i);
+      const float d = (s_av[min(r, F - 1)] - mx[u]) * (float)kFloorBinsPerNat;  // >= 0
+      if (i < total && d < (float)kFloorBins) atomicAdd(&s_hist[max(0, (int)d)], 1u);
+    }
+  }
+  __syncthreads();
+  // cumulative counts from the top bin: each thread holds two adjacent bins
+  const int b0 = 2 * tid;
+  const unsigned int c0 = s_hist[b0], c1 = s_hist[b0 + 1];
+  unsigned int incl = c0 + c1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  unsigned int before = 0u;
+  for (int w = 0; w < warp; ++w) before += s_wsum[w];
+  const unsigned int above = before + incl - (c0 + c1);  // maxima in higher bins
+  const unsigned int need = (unsigned int)limit;
+  if (above < need && above + c0 + c1 >= need) s_bin = (above + c0 >= need) ? b0 : b0 + 1;
+  __syncthreads();
+  if (tid == 0 && s_bin >= 0) {
+    // every maximum counted up to bin b lies above anchor - (b + 1) / 64, up
+    // to the fp32 rounding of its distance, which the margin covers
+    const double fl = anchor - (double)(s_bin + 1) / kFloorBinsPerNat - 1e-3;
+    ws.ctl->floor = double_key(fl);
+  }
+}
+
+// kExpChunk / kExpThreads logits of one chunk per thread
+constexpr int kFiltPer = kExpChunk / kExpThreads;
+
+// Element j of a thread's share of a chunk: with 16-byte rows two float4s
+// (4 (tid + 256 u) + k, j = 4u + k), otherwise tid + 256 j.
+__device__ __forceinline__ int filt_elem(bool vec, int tid, int j) {
+  return vec ? 4 * (tid + kExpThreads * (j >> 2)) + (j & 3) : tid + kExpThreads * j;
+}
+
+// One CTA per (frontier row, kFiltChunks chunks of the row); the loads of all
+// its chunks are issued before anything else.  Per chunk, the candidates
+// (logit >= the row's threshold) are gathered in shared memory with their
+// score keys.  When there are more than the layer may keep (`limit`), only the
+// chunk's best `limit` under the output's total order (score desc, then token
+// asc within a row) are appended: the layer's best `limit` overall are among
+// them, and the select kernel then sees at most chunks x limit candidates per
+// row.  gated: TALON's alpha gate against the anchor (limit = the remaining
+// budget); otherwise every child is a candidate and limit = min(cap,
+// remaining).
 __global__ void __launch_bounds__(kExpThreads)
-exp_filter_kernel(const float* __restrict__ logits, int V, int layer, int topk, int budget,
+exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, int budget,
                   double log_alpha, const int32_t* __restrict__ n_nodes, ExpWs ws) {
   __shared__ unsigned long long s_key[kExpChunk];
   __shared__ int s_tok[kExpChunk];
@@ -191,28 +317,65 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int layer, int topk, 
   __shared__ int s_limit;
   pdl_trigger();
   pdl_wait();
-  const int row = blockIdx.y;
+  const int row = gridDim.y - 1 - blockIdx.y;
+  const int group = gridDim.x - 1 - blockIdx.x;
+  const int chunks = ceil_div(V, kExpChunk);
+  const int c0 = group * kFiltChunks;
+  const int nc = min(kFiltChunks, chunks - c0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* x = logits + (size_t)row * V;
+  const bool vec = (V & 3) == 0;
+  // the group's logits, all loads in flight before the threshold is known
+  float a[kFiltChunks][kFiltPer];
+#pragma unroll
+  for (int cc = 0; cc < kFiltChunks; ++cc) {
+    const int start = (c0 + cc) * kExpChunk;
+    const int stop = (cc < nc) ? min(V, start + kExpChunk) : start;
+    if (vec) {
+      const float4* x4 = reinterpret_cast<const float4*>(x);
+#pragma unroll
+      for (int u = 0; u < kFiltPer / 4; ++u) {
+        const int e = start + 4 * (tid + kExpThreads * u);
+        const float4 f = (e < stop) ? __ldg(x4 + (e >> 2))
+                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        a[cc][4 * u + 0] = f.x;
+        a[cc][4 * u + 1] = f.y;
+        a[cc][4 * u + 2] = f.z;
+        a[cc][4 * u + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kFiltPer; ++j) {
+        const int e = start + tid + kExpThreads * j;
+        a[cc][j] = (e < stop) ? __ldg(x + e) : -INFINITY;
+      }
+    }
+  }
   const double off = ws.rows[row].off;
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     const int n0 = *n_nodes;
     const int remaining = budget - n0;
-    int limit = remaining > 0 ? remaining : 0;
-    if (layer == 1) limit = min(limit, topk);
+    const int limit = min(remaining > 0 ? remaining : 0, cap);
     float thr;
-    if (layer == 1 || limit == 0) {
+    if (!gated || limit == 0) {
       thr = limit == 0 ? INFINITY : -INFINITY;
     } else {
       // s = off_v + logit >= log(alpha) + anchor  <=>  logit >= m_v + (d_v + log(alpha)),
       // d_v = anchor - best_v >= 0 (best_v = off_v + m_v), exactly 0 in the anchor's row
-      const unsigned long long ak = ws.ctl->anchor;
-      const unsigned long long au =
-          (ak & 0x8000000000000000ull) ? (ak & 0x7fffffffffffffffull) : ~ak;
-      const double anchor = __longlong_as_double((long long)au);
+      const double anchor = key_double(ws.ctl->anchor);
       const double m = (double)ws.rows[row].m;
       const double d = anchor - (off + m);
       thr = float_ceil_of(m + (d + log_alpha));
     }
-    if (blockIdx.x == 0 && row == 0) {
+    const unsigned long long fk = *(volatile unsigned long long*)&ws.ctl->floor;
+    if (limit > 0 && fk != 0ull) {
+      // the smallest logit whose score off + logit can round to the floor or
+      // above, taken a little low (a superset passes; the selects are exact)
+      const double fs = key_double(fk);
+      const double xs = (fs - off) - 4e-16 * (fabs(fs) + fabs(off));
+      thr = fmaxf(thr, nextafterf((float)xs, -INFINITY));
+    }
+    if (c0 == 0 && row == 0) {
       ws.ctl->limit = limit;
       ws.ctl->n0 = n0;
     }
@@ -223,150 +386,158 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int layer, int topk, 
   const float thr = s_thr;
   if (!(thr < INFINITY)) return;
   const int limit = s_limit;
-  const float* x = logits + (size_t)row * V;
-  const int start = blockIdx.x * kExpChunk;
-  const int stop = min(V, start + kExpChunk);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    s_cnt = 0;
-    s_out = 0;
-    s_kmin = ~0ull;
-    s_kmax = 0ull;
-  }
-  for (int i = tid; i < kExpChunk / 32; i += kExpThreads) s_tiebits[i] = 0u;
-  __syncthreads();
-  for (int base = start; base < stop; base += kExpThreads) {
-    const int e = base + tid;
-    const float lg = (e < stop) ? __ldg(x + e) : -INFINITY;
-    const bool pass = (e < stop) && (lg >= thr);
-    const unsigned int bal = __ballot_sync(0xffffffffu, pass);
-    if (bal == 0u) continue;
-    int slot0 = 0;
-    if (lane == 0) slot0 = atomicAdd(&s_cnt, __popc(bal));
-    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-    if (pass) {
-      const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-      s_key[slot] = double_key(off + (double)lg);
-      s_tok[slot] = e;
-    }
-  }
-  __syncthreads();
-  const int n = s_cnt;
-  if (n == 0) return;
   const unsigned long long row_hi = (unsigned long long)row << 32;
-  if (n <= limit) {  // everything passes on
-    if (tid == 0) s_base = atomicAdd(&ws.ctl->count, n);
-    __syncthreads();
-    for (int i = tid; i < n; i += kExpThreads) {
-      ws.list[s_base + i] = row_hi | (unsigned int)s_tok[i];
-      ws.keys[s_base + i] = s_key[i];
-    }
-    return;
-  }
-  // radix select of the limit-th largest key T among the n (the bytes above
-  // the highest one in which the smallest and largest key differ are common)
-  unsigned long long kmin = ~0ull, kmax = 0ull;
-  for (int i = tid; i < n; i += kExpThreads) {
-    kmin = min(kmin, s_key[i]);
-    kmax = max(kmax, s_key[i]);
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if (lane == 0) {
-    atomicMin(&s_kmin, kmin);
-    atomicMax(&s_kmax, kmax);
-  }
-  __syncthreads();
-  const unsigned long long diff = s_kmin ^ s_kmax;
-  const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
-  unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
-  unsigned long long prefix = s_kmax & mask;
-  int need = limit;
-  for (int shift = top; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kExpThreads) s_hist[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kExpThreads) {
-      const unsigned long long k = s_key[i];
-      if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255ull], 1u);
+  for (int cc = 0; cc < kFiltChunks; ++cc) {
+    if (cc >= nc) break;
+    const int start = (c0 + cc) * kExpChunk;
+    const int stop = min(V, start + kExpChunk);
+    if (tid == 0) {
+      s_cnt = 0;
+      s_out = 0;
+      s_kmin = ~0ull;
+      s_kmax = 0ull;
     }
     __syncthreads();
-    if (warp == 0) {
-      // digits from the top: lane l holds digits 255 - 8l .. 248 - 8l
-      int cnt[8], lsum = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = (int)s_hist[255 - 8 * lane - i];
-        lsum += cnt[i];
+    for (int j = 0; j < kFiltPer; ++j) {
+      const float lg = a[cc][j];
+      const int e = start + filt_elem(vec, tid, j);
+      const bool pass = (e < stop) && (lg >= thr);
+      const unsigned int bal = __ballot_sync(0xffffffffu, pass);
+      if (bal == 0u) continue;
+      int slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&s_cnt, __popc(bal));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      if (pass) {
+        const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+        s_key[slot] = double_key(off + (double)lg);
+        s_tok[slot] = e;
       }
-      int incl = lsum;
+    }
+    __syncthreads();
+    const int n = s_cnt;
+    if (n == 0) continue;
+    if (n <= limit) {  // everything passes on
+      if (tid == 0) s_base = atomicAdd(&ws.ctl->count, n);
+      __syncthreads();
+      for (int i = tid; i < n; i += kExpThreads) {
+        ws.list[s_base + i] = row_hi | (unsigned int)s_tok[i];
+        ws.keys[s_base + i] = s_key[i];
+      }
+      __syncthreads();
+      continue;
+    }
+    // radix select of the limit-th largest key T among the n (the bytes above
+    // the highest one in which the smallest and largest key differ are common)
+    for (int i = tid; i < kExpChunk / 32; i += kExpThreads) s_tiebits[i] = 0u;
+    unsigned long long kmin = ~0ull, kmax = 0ull;
+    for (int i = tid; i < n; i += kExpThreads) {
+      kmin = min(kmin, s_key[i]);
+      kmax = max(kmax, s_key[i]);
+    }
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) {
+      atomicMin(&s_kmin, kmin);
+      atomicMax(&s_kmax, kmax);
+    }
+    __syncthreads();
+    const unsigned long long diff = s_kmin ^ s_kmax;
+    const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
+    unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
+    unsigned long long prefix = s_kmax & mask;
+    int need = limit;
+    for (int shift = top; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kExpThreads) s_hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < n; i += kExpThreads) {
+        const unsigned long long k = s_key[i];
+        if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255ull], 1u);
       }
-      const int above = incl - lsum;
-      if (above < need && incl >= need) {
-        int cum = above;
+      __syncthreads();
+      if (warp == 0) {
+        // digits from the top: lane l holds digits 255 - 8l .. 248 - 8l
+        int cnt[8], lsum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (cum + cnt[i] >= need) {
-            s_digit = 255 - 8 * lane - i;
-            s_need = need - cum;
-            break;
-          }
-          cum += cnt[i];
+          cnt[i] = (int)s_hist[255 - 8 * lane - i];
+          lsum += cnt[i];
         }
-      }
-    }
-    __syncthreads();
-    prefix |= (unsigned long long)s_digit << shift;
-    mask |= 0xffull << shift;
-    need = s_need;
-    __syncthreads();
-  }
-  const unsigned long long T = prefix;
-  // ties at T: the `need` lowest tokens, found through a bitmap of the chunk
-  for (int i = tid; i < n; i += kExpThreads)
-    if (s_key[i] == T) atomicOr(&s_tiebits[(s_tok[i] - start) >> 5], 1u << ((s_tok[i] - start) & 31));
-  if (tid == 0) s_base = atomicAdd(&ws.ctl->count, limit);
-  __syncthreads();
-  // the cutoff token: the need-th set bit of the bitmap, by one warp
-  if (warp == 0) {
-    int before = 0;
-    for (int w0 = 0; w0 < kExpChunk / 32; w0 += 32) {
-      const unsigned int bits = s_tiebits[w0 + lane];
-      const int c = __popc(bits);
-      int incl = c;
+        int incl = lsum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int tot = __shfl_sync(0xffffffffu, incl, 31);
-      if (before + tot >= need) {
-        const int ex = before + incl - c;  // set bits before this lane's word
-        if (ex < need && ex + c >= need) {
-          unsigned int b = bits;
-          for (int r = need - ex; r > 1; --r) b &= b - 1u;  // drop the lower set bits
-          s_digit = start + ((w0 + lane) << 5) + (__ffs(b) - 1);  // the need-th tie token
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        break;
+        const int above = incl - lsum;
+        if (above < need && incl >= need) {
+          int cum = above;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (cum + cnt[i] >= need) {
+              s_digit = 255 - 8 * lane - i;
+              s_need = need - cum;
+              break;
+            }
+            cum += cnt[i];
+          }
+        }
       }
-      before += tot;
+      __syncthreads();
+      prefix |= (unsigned long long)s_digit << shift;
+      mask |= 0xffull << shift;
+      need = s_need;
+      __syncthreads();
     }
-  }
-  __syncthreads();
-  const int last_tie = s_digit;
-  for (int i = tid; i < n; i += kExpThreads) {
-    const unsigned long long k = s_key[i];
-    if (k > T || (k == T && s_tok[i] <= last_tie)) {
-      const int slot = s_base + atomicAdd(&s_out, 1);
-      ws.list[slot] = row_hi | (unsigned int)s_tok[i];
-      ws.keys[slot] = k;
+    const unsigned long long T = prefix;
+    // at least `limit` candidates of this chunk score T or more
+    if (tid == 0) atomicMax(&ws.ctl->floor, T);
+    // ties at T: the `need` lowest tokens, found through a bitmap of the chunk
+    for (int i = tid; i < n; i += kExpThreads)
+      if (s_key[i] == T)
+        atomicOr(&s_tiebits[(s_tok[i] - start) >> 5], 1u << ((s_tok[i] - start) & 31));
+    if (tid == 0) s_base = atomicAdd(&ws.ctl->count, limit);
+    __syncthreads();
+    // the cutoff token: the need-th set bit of the bitmap, by one warp
+    if (warp == 0) {
+      int before = 0;
+      for (int w0 = 0; w0 < kExpChunk / 32; w0 += 32) {
+        const unsigned int bits = s_tiebits[w0 + lane];
+        const int c = __popc(bits);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int tot = __shfl_sync(0xffffffffu, incl, 31);
+        if (before + tot >= need) {
+          const int ex = before + incl - c;  // set bits before this lane's word
+          if (ex < need && ex + c >= need) {
+            unsigned int b = bits;
+            for (int r = need - ex; r > 1; --r) b &= b - 1u;  // drop the lower set bits
+            s_digit = start + ((w0 + lane) << 5) + (__ffs(b) - 1);  // the need-th tie token
+          }
+          break;
+        }
+        before += tot;
+      }
     }
+    __syncthreads();
+    const int last_tie = s_digit;
+    for (int i = tid; i < n; i += kExpThreads) {
+      const unsigned long long k = s_key[i];
+      if (k > T || (k == T && s_tok[i] <= last_tie)) {
+        const int slot = s_base + atomicAdd(&s_out, 1);
+        ws.list[slot] = row_hi | (unsigned int)s_tok[i];
+        ws.keys[slot] = k;
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -383,6 +554,16 @@ __device__ __forceinline__ bool out_before(const Kept& a, const Kept& b) {
   return a.token < b.token;
 }
 
+// order of the selection: score desc, then the lower (row, token)
+__device__ __forceinline__ bool sel_before(const Kept& a, const Kept& b) {
+  if (a.key != b.key) return a.key > b.key;
+  if (a.row != b.row) return a.row < b.row;
+  return a.token < b.token;
+}
+
+// Ascending bitonic sort of n_pow2 entries under out_before (kOut) or
+// sel_before, by the whole CTA.
+template <bool kOut>
 __device__ void bitonic_sort_kept(Kept* s, int n_pow2) {
   for (int k = 2; k <= n_pow2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
@@ -390,11 +571,12 @@ __device__ void bitonic_sort_kept(Kept* s, int n_pow2) {
         const int ixj = i ^ j;
         if (ixj > i) {
           const bool up = (i & k) == 0;
-          const bool swap = up ? out_before(s[ixj], s[i]) : out_before(s[i], s[ixj]);
-          if (swap) {
-            const Kept t = s[i];
-            s[i] = s[ixj];
-            s[ixj] = t;
+          const Kept a = s[i], b = s[ixj];
+          const bool b_first = kOut ? out_before(b, a) : sel_before(b, a);
+          const bool a_first = kOut ? out_before(a, b) : sel_before(a, b);
+          if (up ? b_first : a_first) {
+            s[i] = b;
+            s[ixj] = a;
           }
         }
       }
@@ -451,6 +633,44 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     s_kmax = 0ull;
   }
   __syncthreads();
+  if (count <= kMaxBudget) {
+    // up to 2048 candidates: sort them all by the selection order (score
+    // desc, then the lower (row, token)) in shared memory, keep the first
+    // `limit` and sort those by the output order
+    int p2 = 1;
+    while (p2 < count) p2 <<= 1;
+    for (int j = tid; j < p2; j += kSelThreads) {
+      if (j < count) {
+        const unsigned long long c = ws.list[j];
+        s_kept[j] = Kept{ws.keys[j], (int)(c >> 32), (int)(c & 0xffffffffu)};
+      } else {
+        s_kept[j] = Kept{0ull, INT_MAX, INT_MAX};  // after every candidate
+      }
+    }
+    __syncthreads();
+    bitonic_sort_kept<false>(s_kept, p2);
+    const int k = min(count, limit);
+    int q2 = 1;
+    while (q2 < k) q2 <<= 1;
+    for (int j = k + tid; j < q2; j += kSelThreads) s_kept[j] = Kept{0ull, INT_MAX, INT_MAX};
+    __syncthreads();
+    bitonic_sort_kept<true>(s_kept, q2);
+    const int n0 = ctl.n0;
+    for (int j = tid; j < k; j += kSelThreads) {
+      const Kept c = s_kept[j];
+      tree_parent[n0 + j] = frontier_node[c.row];
+      tree_token[n0 + j] = c.token;
+      tree_logscore[n0 + j] =
+          (float)(ws.rows[c.row].off + (double)__ldg(logits + (size_t)c.row * V + c.token));
+    }
+    if (tid == 0) {
+      *n_nodes = n0 + k;
+      ws.ctl->count = 0;   // the next call starts from zero
+      ws.ctl->anchor = 0ull;
+      ws.ctl->floor = 0ull;
+    }
+    return;
+  }
   if (count <= limit) {
     for (int j = tid; j < count; j += kSelThreads) {
       const unsigned long long c = ws.list[j];
@@ -605,7 +825,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
   while (p2 < k) p2 <<= 1;
   for (int i = k + tid; i < p2; i += kSelThreads) s_kept[i] = Kept{0ull, INT_MAX, INT_MAX};
   __syncthreads();
-  bitonic_sort_kept(s_kept, p2);
+  bitonic_sort_kept<true>(s_kept, p2);
   const int n0 = ctl.n0;
   for (int i = tid; i < k; i += kSelThreads) {
     const Kept c = s_kept[i];
@@ -617,6 +837,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     *n_nodes = n0 + k;
     ws.ctl->count = 0;   // the next call starts from zero
     ws.ctl->anchor = 0ull;
+    ws.ctl->floor = 0ull;
   }
 }
 
@@ -629,6 +850,70 @@ extern "C" size_t tv_expand_workspace_size(int F, int V) {
   return tv::exp_offsets(F, V, &a, &b, &c, &d);
 }
 
+namespace tv {
+namespace {
+
+// The three launches of one layer; the caller has checked the arguments.
+tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
+                       const float* frontier_logscore, int F, int V, int gated, int cap,
+                       double log_alpha, int budget, int32_t* tree_parent, int32_t* tree_token,
+                       float* tree_logscore, int32_t* n_nodes, void* workspace,
+                       cudaStream_t stream) {
+  size_t rows_off, part_off, list_off, keys_off;
+  exp_offsets(F, V, &rows_off, &part_off, &list_off, &keys_off);
+  char* base = static_cast<char*>(workspace);
+  ExpWs ws;
+  ws.ctl = reinterpret_cast<ExpCtl*>(base);
+  ws.arrivals = reinterpret_cast<unsigned int*>(base + exp_arrivals_offset());
+  ws.rows = reinterpret_cast<ExpRow*>(base + rows_off);
+  ws.part = reinterpret_cast<ExpPartial*>(base + part_off);
+  ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
+  ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
+  const int chunks = ceil_div(V, kExpChunk);
+  static bool smem_set = false;  // the select stages up to kSelStageKeys keys
+  if (!smem_set) {
+    if (cudaFuncSetAttribute(exp_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kSelStageKeys * sizeof(unsigned long long))) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TV_ERR_CUDA;
+    }
+    smem_set = true;
+  }
+  if (launch_pdl(exp_stats_kernel, dim3(ceil_div(chunks, kStatsWarps), F), dim3(kStatsWarps * 32),
+                 0, stream, draft_logits, V, chunks, frontier_logscore, ws) != cudaSuccess ||
+      (!gated && launch_pdl(exp_floor_kernel, dim3(1), dim3(kFloorThreads), 0, stream,
+                            draft_logits, V, F, chunks, cap, budget, (const int32_t*)n_nodes,
+                            ws) != cudaSuccess) ||
+      launch_pdl(exp_filter_kernel, dim3(ceil_div(chunks, kFiltChunks), F), dim3(kExpThreads), 0,
+                 stream, draft_logits, V, gated,
+                 cap, budget, log_alpha, (const int32_t*)n_nodes, ws) != cudaSuccess ||
+      launch_pdl(exp_select_kernel, dim3(1), dim3(kSelThreads),
+                 (size_t)kSelStageKeys * sizeof(unsigned long long), stream, draft_logits, V,
+                 frontier_node, tree_parent, tree_token, tree_logscore, n_nodes,
+                 ws) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
+  return TV_OK;
+}
+
+// Checks shared by both entry points (F == 0 has already returned).
+tv_status check_layer(const float* draft_logits, const int32_t* frontier_node,
+                      const float* frontier_logscore, int F, int V, int32_t* tree_parent,
+                      int32_t* tree_token, float* tree_logscore, int32_t* n_nodes,
+                      void* workspace, size_t ws_bytes) {
+  if (!draft_logits || !frontier_node || !frontier_logscore || !tree_parent || !tree_token ||
+      !tree_logscore || !n_nodes)
+    return TV_ERR_INVALID_ARG;
+  if ((size_t)F * V >= (1ull << 31)) return TV_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < tv_expand_workspace_size(F, V)) return TV_ERR_WORKSPACE;
+  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(draft_logits) & 15)) return TV_ERR_INVALID_ARG;
+  return TV_OK;
+}
+
+}  // namespace
+}  // namespace tv
+
 extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* frontier_node,
                                      const float* frontier_logscore, int F, int V, int layer,
                                      int topk, float alpha, int budget, int32_t* tree_parent,
@@ -639,44 +924,31 @@ extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* f
   if (layer == 1 && (F != 1 || topk < 1)) return TV_ERR_INVALID_ARG;
   if (layer >= 2 && !(alpha > 0.0f && alpha <= 1.0f)) return TV_ERR_INVALID_ARG;
   if (F == 0) return TV_OK;
-  if (!draft_logits || !frontier_node || !frontier_logscore || !tree_parent || !tree_token ||
-      !tree_logscore || !n_nodes)
-    return TV_ERR_INVALID_ARG;
-  if ((size_t)F * V >= (1ull << 31)) return TV_ERR_UNSUPPORTED;
-  if (!workspace || ws_bytes < tv_expand_workspace_size(F, V)) return TV_ERR_WORKSPACE;
-  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(draft_logits) & 15)) return TV_ERR_INVALID_ARG;
-  size_t rows_off, part_off, list_off, keys_off;
-  tv::exp_offsets(F, V, &rows_off, &part_off, &list_off, &keys_off);
-  char* base = static_cast<char*>(workspace);
-  tv::ExpWs ws;
-  ws.ctl = reinterpret_cast<tv::ExpCtl*>(base);
-  ws.arrivals = reinterpret_cast<unsigned int*>(base + tv::exp_arrivals_offset());
-  ws.rows = reinterpret_cast<tv::ExpRow*>(base + rows_off);
-  ws.part = reinterpret_cast<tv::ExpPartial*>(base + part_off);
-  ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
-  ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
-  const int chunks = tv::ceil_div(V, tv::kExpChunk);
-  dim3 grid(chunks, F);
-  static bool select_smem_set = false;  // the select stages up to kSelStageKeys keys
-  if (!select_smem_set) {
-    if (cudaFuncSetAttribute(tv::exp_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(tv::kSelStageKeys * sizeof(unsigned long long))) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
-    select_smem_set = true;
-  }
-  const double log_alpha = log((double)alpha);
-  if (tv::launch_pdl(tv::exp_stats_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
-                     chunks, frontier_logscore, ws) != cudaSuccess ||
-      tv::launch_pdl(tv::exp_filter_kernel, grid, dim3(tv::kExpThreads), 0, stream, draft_logits, V,
-                     layer, topk, budget, log_alpha, (const int32_t*)n_nodes, ws) != cudaSuccess ||
-      tv::launch_pdl(tv::exp_select_kernel, dim3(1), dim3(tv::kSelThreads),
-                     (size_t)tv::kSelStageKeys * sizeof(unsigned long long), stream, draft_logits,
-                     V, frontier_node, tree_parent, tree_token, tree_logscore, n_nodes,
-                     ws) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TV_ERR_CUDA;
-  }
-  return TV_OK;
+  const tv_status st = tv::check_layer(draft_logits, frontier_node, frontier_logscore, F, V,
+                                       tree_parent, tree_token, tree_logscore, n_nodes, workspace,
+                                       ws_bytes);
+  if (st != TV_OK) return st;
+  // the root layer keeps its Top-K ungated; deeper layers gate, up to the budget
+  const int gated = layer >= 2;
+  const int cap = gated ? INT_MAX : topk;
+  return tv::launch_layer(draft_logits, frontier_node, frontier_logscore, F, V, gated, cap,
+                          gated ? log((double)alpha) : 0.0, budget, tree_parent, tree_token,
+                          tree_logscore, n_nodes, workspace, stream);
+}
+
+extern "C" tv_status tv_expand_topn(const float* draft_logits, const int32_t* frontier_node,
+                                    const float* frontier_logscore, int F, int V, int width,
+                                    int capacity, int32_t* tree_parent, int32_t* tree_token,
+                                    float* tree_logscore, int32_t* n_nodes, void* workspace,
+                                    size_t ws_bytes, cudaStream_t stream) {
+  if (F < 0 || V < 1 || width < 1 || capacity < 1) return TV_ERR_INVALID_ARG;
+  if (width > tv::kMaxBudget || F > tv::kMaxBudget) return TV_ERR_UNSUPPORTED;
+  if (F == 0) return TV_OK;
+  const tv_status st = tv::check_layer(draft_logits, frontier_node, frontier_logscore, F, V,
+                                       tree_parent, tree_token, tree_logscore, n_nodes, workspace,
+                                       ws_bytes);
+  if (st != TV_OK) return st;
+  return tv::launch_layer(draft_logits, frontier_node, frontier_logscore, F, V, 0, width, 0.0,
+                          capacity, tree_parent, tree_token, tree_logscore, n_nodes, workspace,
+                          stream);
 }

@@ -103,6 +103,24 @@ def test_host_side_argument_errors_launch_nothing(tvlib):
                               None) == tvlib.TV_OK
 
 
+def test_opt_tree_host_side_errors(tvlib):
+    lib = tvlib.lib
+    d = ctypes.c_void_p(0x1000)
+    ws = 1 << 30
+    # width 0, capacity 0, width above 2048, F above 2048, F = 0, workspace too small
+    assert lib.tv_expand_topn(d, d, d, 1, 10, 0, 8, d, d, d, d, d, ws, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_expand_topn(d, d, d, 1, 10, 4, 0, d, d, d, d, d, ws, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_expand_topn(d, d, d, 1, 10, 3000, 8, d, d, d, d, d, ws, None) == tvlib.TV_ERR_UNSUPPORTED
+    assert lib.tv_expand_topn(d, d, d, 3000, 10, 4, 8, d, d, d, d, d, ws, None) == tvlib.TV_ERR_UNSUPPORTED
+    assert lib.tv_expand_topn(d, d, d, 0, 10, 4, 8, d, d, d, d, d, ws, None) == tvlib.TV_OK
+    assert lib.tv_expand_topn(d, d, d, 4, 1000, 4, 8, d, d, d, d, d, 64, None) == tvlib.TV_ERR_WORKSPACE
+    # selection: M above 16384, n = 0, B = 0, a missing output
+    assert lib.tv_select_topn(d, d, d, d, 1, 16385, 8, d, d, d, d, d, d, None) == tvlib.TV_ERR_UNSUPPORTED
+    assert lib.tv_select_topn(d, d, d, d, 1, 100, 0, d, d, d, d, d, d, None) == tvlib.TV_ERR_INVALID_ARG
+    assert lib.tv_select_topn(d, d, d, d, 0, 100, 8, d, d, d, d, d, d, None) == tvlib.TV_OK
+    assert lib.tv_select_topn(d, d, d, d, 1, 100, 8, d, d, d, d, None, d, None) == tvlib.TV_ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors(tvlib):
     import torch
     parent = torch.tensor([[-1, 0]], dtype=torch.int32)
