@@ -109,6 +109,15 @@ __device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* p, unsigned
   return old;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x on the special-function unit (ex2.approx.ftz): relative error about
+// 2^-22, below the fp32 rounding of the logits it is applied to.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One warp per 2048-logit chunk (64 logits a lane, all loads in flight at
 // once), kStatsWarps chunks of one row per CTA.  Each warp writes its chunk's
 // partial (max, sum of exp(x - max)); the CTA then arrives on the row's counter
@@ -153,9 +162,11 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
 #pragma unroll
     for (int u = 0; u < kPer; ++u) m = fmaxf(m, a[u]);
     m = warp_max(m);
+    const float ml = m * kLog2e;
     float sl = 0.0f;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) sl += (a[u] == -INFINITY) ? 0.0f : expf(a[u] - m);
+    for (int u = 0; u < kPer; ++u)
+      sl += (a[u] == -INFINITY) ? 0.0f : ex2_approx(fmaf(a[u], kLog2e, -ml));
     const double sd = warp_sum_d((double)sl);
     if (lane == 0) {
       part[(size_t)row * chunks + c] = ExpPartial{sd, m, 0.0f};
@@ -171,15 +182,15 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
   __syncthreads();
   if (!s_last || warp != 0) return;
   // warp 0 of the row's last CTA: normaliser, offset and best score of the
-  // row.  Chunk scale factors on the SFU (fp32, within a few ulp; fp64 runs
-  // at a small fraction of the fp32 rate here), the sum itself in fp64.
+  // row.  Exponentials on the SFU (fp32; fp64 runs at a small fraction of the
+  // fp32 rate here), the sum itself in fp64.
   const ExpPartial* p = part + (size_t)row * chunks;
   float mr = -INFINITY;
   for (int k = lane; k < chunks; k += 32) mr = fmaxf(mr, __ldcg(&p[k].m));
   mr = warp_max(mr);
   double sr = 0.0;
   for (int k = lane; k < chunks; k += 32)
-    sr += __ldcg(&p[k].s) * (double)expf(__ldcg(&p[k].m) - mr);
+    sr += __ldcg(&p[k].s) * (double)ex2_approx((__ldcg(&p[k].m) - mr) * kLog2e);
   sr = warp_sum_d(sr);
   if (lane == 0) {
     ws.arrivals[row] = 0u;
