@@ -397,6 +397,18 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
   const float thr = s_thr;
   if (!(thr < INFINITY)) return;
   const int limit = s_limit;
+  // most groups hold no candidate at all (above an OPT-Tree floor nearly none
+  // do): one block vote, and they are done
+  int any = 0;
+#pragma unroll
+  for (int cc = 0; cc < kFiltChunks; ++cc) {
+    const int start = (c0 + cc) * kExpChunk;
+    const int stop = (cc < nc) ? min(V, start + kExpChunk) : start;
+#pragma unroll
+    for (int j = 0; j < kFiltPer; ++j)
+      any |= (start + filt_elem(vec, tid, j) < stop) && (a[cc][j] >= thr);
+  }
+  if (!__syncthreads_or(any)) return;
   const unsigned long long row_hi = (unsigned long long)row << 32;
 #pragma unroll
   for (int cc = 0; cc < kFiltChunks; ++cc) {
