@@ -694,154 +694,147 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     }
     return;
   }
-  if (count <= limit) {
-    for (int j = tid; j < count; j += kSelThreads) {
-      const unsigned long long c = ws.list[j];
-      s_kept[j] = Kept{ws.keys[j], (int)(c >> 32), (int)(c & 0xffffffffu)};
+  // more than 2048 candidates (more than any layer keeps): radix select of
+  // T = the limit-th largest key, need = how many keys == T to take.  The
+  // bytes above the highest one in which the smallest and the largest key
+  // differ are common to all keys and skipped.
+  const bool staged = count <= kSelStageKeys;
+  if (staged) {
+    for (int j = tid; j < count; j += kSelThreads) s_stage[j] = ws.keys[j];
+    __syncthreads();
+  }
+  const unsigned long long* K = staged ? s_stage : ws.keys;
+  unsigned long long kmin = ~0ull, kmax = 0ull;
+  for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
+    unsigned long long kb[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int j = j0 + u * kSelThreads;
+      kb[u] = (j < count) ? K[j] : K[0];
     }
-    if (tid == 0) s_n = count;
-  } else {
-    // radix select: T = the limit-th largest key, need = how many keys == T to
-    // take.  The bytes above the highest one in which the smallest and the
-    // largest key differ are common to all keys and skipped.
-    const bool staged = count <= kSelStageKeys;
-    if (staged) {
-      for (int j = tid; j < count; j += kSelThreads) s_stage[j] = ws.keys[j];
-      __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      kmin = min(kmin, kb[u]);
+      kmax = max(kmax, kb[u]);
     }
-    const unsigned long long* K = staged ? s_stage : ws.keys;
-    unsigned long long kmin = ~0ull, kmax = 0ull;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) {
+    atomicMin(&s_kmin, kmin);
+    atomicMax(&s_kmax, kmax);
+  }
+  __syncthreads();
+  const unsigned long long diff = s_kmin ^ s_kmax;
+  const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
+  unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
+  unsigned long long prefix = s_kmax & mask;
+  int need = limit;
+  for (int shift = top; shift >= 0; shift -= 8) {
+    for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&s_hist[0][0])[i] = 0u;
+    __syncthreads();
     for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
       unsigned long long kb[kSelBatch];
 #pragma unroll
       for (int u = 0; u < kSelBatch; ++u) {
         const int j = j0 + u * kSelThreads;
-        kb[u] = (j < count) ? K[j] : K[0];
+        kb[u] = (j < count) ? K[j] : ~prefix;  // ~prefix never matches the prefix
       }
 #pragma unroll
-      for (int u = 0; u < kSelBatch; ++u) {
-        kmin = min(kmin, kb[u]);
-        kmax = max(kmax, kb[u]);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    }
-    if (lane == 0) {
-      atomicMin(&s_kmin, kmin);
-      atomicMax(&s_kmax, kmax);
+      for (int u = 0; u < kSelBatch; ++u)
+        if ((kb[u] & mask) == prefix && (j0 + u * kSelThreads) < count)
+          atomicAdd(&s_hist[warp][(kb[u] >> shift) & 255ull], 1u);
     }
     __syncthreads();
-    const unsigned long long diff = s_kmin ^ s_kmax;
-    const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
-    unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
-    unsigned long long prefix = s_kmax & mask;
-    int need = limit;
-    for (int shift = top; shift >= 0; shift -= 8) {
-      for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&s_hist[0][0])[i] = 0u;
-      __syncthreads();
-      for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
-        unsigned long long kb[kSelBatch];
-#pragma unroll
-        for (int u = 0; u < kSelBatch; ++u) {
-          const int j = j0 + u * kSelThreads;
-          kb[u] = (j < count) ? K[j] : ~prefix;  // ~prefix never matches the prefix
-        }
-#pragma unroll
-        for (int u = 0; u < kSelBatch; ++u)
-          if ((kb[u] & mask) == prefix && (j0 + u * kSelThreads) < count)
-            atomicAdd(&s_hist[warp][(kb[u] >> shift) & 255ull], 1u);
-      }
-      __syncthreads();
-      if (tid < 256) {
-        unsigned int t = 0u;
+    if (tid < 256) {
+      unsigned int t = 0u;
 #pragma unroll 8
-        for (int w = 0; w < kSelThreads / 32; ++w) t += s_hist[w][tid];
-        s_hist[0][tid] = t;
+      for (int w = 0; w < kSelThreads / 32; ++w) t += s_hist[w][tid];
+      s_hist[0][tid] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // digits from the top: lane l sums digits 255 - 8l .. 248 - 8l, an
+      // exclusive scan over lanes gives the count above each lane's digits
+      int cnt[8], lsum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = (int)s_hist[0][255 - 8 * lane - i];
+        lsum += cnt[i];
       }
-      __syncthreads();
-      if (warp == 0) {
-        // digits from the top: lane l sums digits 255 - 8l .. 248 - 8l, an
-        // exclusive scan over lanes gives the count above each lane's digits
-        int cnt[8], lsum = 0;
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int above = incl - lsum;
+      if (above < need && incl >= need) {
+        int cum = above;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          cnt[i] = (int)s_hist[0][255 - 8 * lane - i];
-          lsum += cnt[i];
-        }
-        int incl = lsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int above = incl - lsum;
-        if (above < need && incl >= need) {
-          int cum = above;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (cum + cnt[i] >= need) {
-              s_digit = 255 - 8 * lane - i;
-              s_need = need - cum;
-              break;
-            }
-            cum += cnt[i];
+          if (cum + cnt[i] >= need) {
+            s_digit = 255 - 8 * lane - i;
+            s_need = need - cum;
+            break;
           }
+          cum += cnt[i];
         }
-      }
-      __syncthreads();
-      prefix |= (unsigned long long)s_digit << shift;
-      mask |= 0xffull << shift;
-      need = s_need;
-      __syncthreads();
-    }
-    const unsigned long long T = prefix;
-    for (int j = tid; j < count; j += kSelThreads) {
-      const unsigned long long c = ws.list[j];
-      const unsigned long long k = K[j];
-      if (k > T) {
-        const int slot = atomicAdd(&s_n, 1);
-        s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
-      } else if (k == T) {
-        const int slot = atomicAdd(&s_nt, 1);
-        if (slot < kTieCap) s_ties[slot] = c;
       }
     }
     __syncthreads();
-    const int n_gt = s_n, n_ties = s_nt;
-    if (n_ties <= kTieCap) {
-      // take the `need` lowest (row, token) among the ties
-      int p2 = 1;
-      while (p2 < n_ties) p2 <<= 1;
-      for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
-      __syncthreads();
-      bitonic_sort_u64(s_ties, p2);
-      for (int i = tid; i < need; i += kSelThreads)
-        s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
-    } else {
-      // very many exact ties: pick them one by one in (row, token) order
-      unsigned long long last = 0ull;
-      bool first = true;
-      for (int r = 0; r < need; ++r) {
-        if (tid == 0) s_min = ~0ull;
-        __syncthreads();
-        unsigned long long mine = ~0ull;
-        for (int j = tid; j < count; j += kSelThreads) {
-          const unsigned long long c = ws.list[j];
-          if ((first || c > last) && c < mine && K[j] == T) mine = c;
-        }
-        atomicMin(&s_min, mine);
-        __syncthreads();
-        last = s_min;
-        first = false;
-        if (tid == 0) s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
-        __syncthreads();
-      }
-    }
-    if (tid == 0) s_n = limit;
+    prefix |= (unsigned long long)s_digit << shift;
+    mask |= 0xffull << shift;
+    need = s_need;
+    __syncthreads();
   }
+  const unsigned long long T = prefix;
+  for (int j = tid; j < count; j += kSelThreads) {
+    const unsigned long long c = ws.list[j];
+    const unsigned long long k = K[j];
+    if (k > T) {
+      const int slot = atomicAdd(&s_n, 1);
+      s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
+    } else if (k == T) {
+      const int slot = atomicAdd(&s_nt, 1);
+      if (slot < kTieCap) s_ties[slot] = c;
+    }
+  }
+  __syncthreads();
+  const int n_gt = s_n, n_ties = s_nt;
+  if (n_ties <= kTieCap) {
+    // take the `need` lowest (row, token) among the ties
+    int p2 = 1;
+    while (p2 < n_ties) p2 <<= 1;
+    for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
+    __syncthreads();
+    bitonic_sort_u64(s_ties, p2);
+    for (int i = tid; i < need; i += kSelThreads)
+      s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
+  } else {
+    // very many exact ties: pick them one by one in (row, token) order
+    unsigned long long last = 0ull;
+    bool first = true;
+    for (int r = 0; r < need; ++r) {
+      if (tid == 0) s_min = ~0ull;
+      __syncthreads();
+      unsigned long long mine = ~0ull;
+      for (int j = tid; j < count; j += kSelThreads) {
+        const unsigned long long c = ws.list[j];
+        if ((first || c > last) && c < mine && K[j] == T) mine = c;
+      }
+      atomicMin(&s_min, mine);
+      __syncthreads();
+      last = s_min;
+      first = false;
+      if (tid == 0) s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
+      __syncthreads();
+    }
+  }
+  if (tid == 0) s_n = limit;
   __syncthreads();
   const int k = s_n;
   int p2 = 1;
