@@ -451,12 +451,8 @@ def opt_tree_setup(torch, tv, device):
     cap = 1 + width * layers
     gen_t = torch.Generator(device=device)
     gen_t.manual_seed(5)
-    F, lo = [], []
-    a, b = 0, 1          # the frontier is the id range [a, b): the previous layer
-    for _ in range(layers):
-        F.append(b - a)
-        lo.append(a)
-        a, b = b, b + min(width, (b - a) * V, cap - b)
+    sizes = tv.opt_tree_layer_sizes(width, layers, V, cap)
+    lo, F = [a for a, _ in sizes], [f for _, f in sizes]
     rows = [torch.randn((f, V), generator=gen_t, device=device) * 3.0 for f in F]
     st = dict(width=width, layers=layers, n_keep=n_keep, V=V, cap=cap, F=F, rows=rows,
               par=torch.full((cap,), -1, dtype=torch.int32, device=device),

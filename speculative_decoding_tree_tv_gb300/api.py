@@ -325,6 +325,22 @@ def select_topn(parent: torch.Tensor, token: torch.Tensor, logscore: torch.Tenso
     return out
 
 
+def opt_tree_layer_sizes(width: int, layers: int, V: int, capacity: int) -> list:
+    """Frontier id ranges (lo, F) of an OPT-Tree growth from the root: layer l
+    expands the nodes layer l - 1 added, and a layer adds min(width, F x V,
+    capacity - nodes so far) nodes (tv_expand_topn).  Stops early when a layer
+    would add nothing.  Host arithmetic only: no device value is read."""
+    out = []
+    lo, hi = 0, 1
+    for _ in range(layers):
+        k = min(width, (hi - lo) * V, capacity - hi)
+        if k <= 0:
+            break
+        out.append((lo, hi - lo))
+        lo, hi = hi, hi + k
+    return out
+
+
 def grow_opt_tree(draft_rows: Callable, root_key, child_key: Callable, width: int, layers: int,
                   n: int, device) -> dict:
     """Grow an OPT-Tree candidate tree of `layers` layers (the root's is
@@ -342,20 +358,25 @@ def grow_opt_tree(draft_rows: Callable, root_key, child_key: Callable, width: in
     node_ids = torch.arange(cap, dtype=torch.int32, device=dev)
     n_dev = torch.ones(1, dtype=torch.int32, device=dev)
     keys = [root_key]
-    lo, hi = 0, 1
-    for _ in range(layers):
-        rows = torch.as_tensor(draft_rows(keys[lo:hi]), dtype=torch.float32).to(dev).contiguous()
-        F, V = rows.shape
-        k = min(width, F * V, cap - hi)
-        if k <= 0:
-            break
-        expand_topn(rows, node_ids[lo:hi], ls[lo:hi], width, cap, par, tok, ls, n_dev)
-        new_par = par[hi:hi + k].cpu().tolist()
-        new_tok = tok[hi:hi + k].cpu().tolist()
+    m = 1
+    sizes = None
+    for li in range(layers):
+        lo, F = (0, 1) if sizes is None else sizes[li]
+        rows = torch.as_tensor(draft_rows(keys[lo:lo + F]), dtype=torch.float32).to(dev)
+        rows = rows.contiguous()
+        if sizes is None:   # the vocabulary is known once the drafter has answered
+            sizes = opt_tree_layer_sizes(width, layers, rows.shape[1], cap)
+            if not sizes:
+                break
+        expand_topn(rows, node_ids[lo:lo + F], ls[lo:lo + F], width, cap, par, tok, ls, n_dev)
+        k = min(width, F * rows.shape[1], cap - m)
+        new_par = par[m:m + k].cpu().tolist()
+        new_tok = tok[m:m + k].cpu().tolist()
         for p, t in zip(new_par, new_tok):
             keys.append(child_key(keys[p], t))
-        lo, hi = hi, hi + k
-    m = hi
+        m += k
+        if li + 1 >= len(sizes):
+            break
     sel = select_topn(par[None, :m].contiguous(), tok[None, :m].contiguous(),
                       ls[None, :m].contiguous(), torch.tensor([m], dtype=torch.int32, device=dev),
                       n)
