@@ -5,36 +5,39 @@
 // best-scoring ones when more survive than the remaining budget).
 // tv_expand_topn: one layer of OPT-Tree's greedy expansion (OPT-Tree §3:
 // every child of every frontier node is a candidate, scored by its path's
-// draft probability, and the layer keeps the `width` best); the same three
-// launches without the gate.
+// draft probability, and the layer keeps the `width` best); the same
+// launches without the gate, plus the floor kernel.
 //
-// Three launches, all on the caller's stream:
-//   1. stats:   per (frontier row, 2048-logit chunk) max and sum exp; the last
-//               CTA of a row to finish forms the row's log-normaliser lse_v
-//               and offset off_v = logscore_v - lse_v (log s of token c in
-//               row v is off_v + logit) and raises the layer's anchor (the
-//               best score) with one atomic max;
+// Three launches (four for OPT-Tree layers), all on the caller's stream:
+//   1. stats:   per (frontier row, 2048-logit chunk) max and sum exp, one warp
+//               per chunk and eight chunks per CTA; warp 0 of the last CTA of
+//               a row to finish forms the row's log-normaliser lse_v and
+//               offset off_v = logscore_v - lse_v (log s of token c in row v
+//               is off_v + logit) and raises the layer's anchor (the best
+//               score) with one atomic max;
 //   1b. floor:  (OPT-Tree layers only) one CTA sets the layer's floor to
 //               (just under) the limit-th best score among the chunks'
 //               maxima: they are distinct candidates, so the layer's
 //               limit-th best scores at least that much, and it is close to
 //               the cut;
-//   2. filter:  each CTA turns the fp64 gate (if any) and the layer's floor
-//               into an fp32 logit threshold for its row, streams its chunk
-//               again and appends the (row, token) candidates that pass, with
-//               their order-preserving fp64 score keys (at most the layer's
-//               limit per chunk, its best ones).  A chunk holding more than
-//               `limit` candidates raises the floor to its limit-th best key:
-//               the layer's limit-th best is at least that, so chunks that run
+//   2. filter:  each CTA loads four chunks of a row, turns the fp64 gate (if
+//               any) and the layer's floor into an fp32 logit threshold for
+//               the row, and (after one block vote, when any value passes)
+//               appends the (row, token) candidates that pass, with their
+//               order-preserving fp64 score keys (at most the layer's limit
+//               per chunk, its best ones).  A chunk holding more than `limit`
+//               candidates raises the floor to its limit-th best key: the
+//               layer's limit-th best is at least that, so chunks that run
 //               later skip everything below it.  The filter visits the
 //               (row, chunk) pairs in the reverse of the stats order, so that
 //               it starts on what the stats pass read last (still in L2);
-//   3. select:  one CTA keeps the best `limit` candidates (radix select on the
-//               score keys staged in shared memory, starting at the first
-//               byte in which the keys differ; ties to the lower
-//               (parent, token)), orders them (parent asc, score desc, token
-//               asc), appends them to the tree and returns the control words
-//               (candidate count, anchor, floor) to zero for the next call.
+//   3. select:  one CTA keeps the best `limit` candidates (up to 2048 of them
+//               by two bitonic sorts in shared memory; beyond that a radix
+//               select on the score keys, starting at the first byte in which
+//               the keys differ), ties to the lower (parent, token), orders
+//               them (parent asc, score desc, token asc), appends them to the
+//               tree and returns the control words (candidate count, anchor,
+//               floor) to zero for the next call.
 // Scores are fp64 in the log domain; logits stay fp32.
 #include <algorithm>
 #include <climits>
@@ -75,7 +78,7 @@ struct ExpCtl {
 
 struct ExpWs {
   ExpCtl* ctl;
-  unsigned int* arrivals;  // [kMaxBudget] stats CTAs of each row done (returned to 0)
+  unsigned int* arrivals;  // [kMaxBudget] chunks of each row done by the stats pass (returned to 0)
   ExpRow* rows;
   ExpPartial* part;
   unsigned long long* list;  // (row << 32) | token
