@@ -546,6 +546,21 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
         "long context: prefix 32768, 32/8 heads, head_dim 128, 256-node OPT-Tree-style tree, "
         "vocab 128256, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2)
     del case
+    # the same workload's node-count sweep (16, 64 and 512 nodes; 256 is above)
+    sweep = {}
+    for n in (16, 64, 512):
+        case = None
+        try:
+            case = gen.config5(n)
+            r5 = measure_verify_config(
+                f"long context, {n}-node tree", case, "greedy", torch, tv, device, stream, hbm,
+                tflops, l2)
+            sweep[str(n)] = {k: r5[k] for k in ("us_per_step", "us_per_launch",
+                                                "roofline_step_us", "roofline_step_frac", "attn")}
+        except Exception as e:  # recorded in the line rather than ending the run
+            sweep[str(n)] = {"error": repr(e)[:200]}
+        del case
+    res["long_context_sweep"] = sweep
     case = gen.config4()
     res["batched_stochastic"] = measure_verify_config(
         "batched stochastic: 16 sequences, prefixes in [512, 8192], 64-node trees, 32/8 heads, "

@@ -132,6 +132,13 @@ def test_config5_long_context_sampled(tv, oracle_mod):
     sampled_check(tv, oracle_mod, gen.config5(256, V=5000), 24, 6, "config5")
 
 
+@pytest.mark.parametrize("n", [16, 64, 512])
+def test_config5_long_context_sweep_sampled(tv, oracle_mod, n):
+    """The long-context workload's node-count sweep: 16, 64 and 512 OPT-Tree
+    nodes over the 32,768-key prefix (256 is the case above)."""
+    sampled_check(tv, oracle_mod, gen.config5(n, V=64), 16, 9 + n, f"config5-n{n}")
+
+
 def test_config3_talon_tree_sampled(tv, oracle_mod):
     d = gen.config3_drafter(1)
     tree = oracle_mod.expand_tree(d, 10, 0.3, 512)
