@@ -126,6 +126,12 @@ def test_binding_refuses_cpu_tensors(tvlib):
     parent = torch.tensor([[-1, 0]], dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         tvlib.tree_build(parent)
+    i32 = torch.zeros(4, dtype=torch.int32)
+    f32 = torch.zeros(4, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        tvlib.expand_topn(torch.zeros((1, 8)), i32[:1], f32[:1], 2, 4, i32, i32, f32, i32[:1])
+    with pytest.raises(ValueError, match="CUDA"):
+        tvlib.select_topn(parent, parent, torch.zeros((1, 2)), i32[:1], 2)
 
 
 # --------------------------------------------------------------- attention plan
