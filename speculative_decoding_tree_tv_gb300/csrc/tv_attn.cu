@@ -46,6 +46,7 @@ constexpr int kBN = 128;              // keys per tile
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale max while within 2^8
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
 constexpr int kMaxSplit = 64;         // splits of one CTA's key range
+constexpr int kPrefetchTiles = 4;     // tiles of a split's range prefetched into the L2
 
 // Shape of a CTA: RBS row blocks of 128 query rows (one or two), 128 softmax
 // threads per row block, then the K producer, MMA and V producer warps (the
@@ -81,6 +82,8 @@ struct Shape {
 };
 
 struct AttnParams {
+  const uint16_t* k;  // caches, for the L2 prefetch of a split's first tiles
+  const uint16_t* v;
   uint16_t* out;
   float* lse;
   int32_t* status;
@@ -257,6 +260,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      // This CTA's Q rows and the first tiles of its key range into the L2
+      // while the previous kernel finishes.  Prefetches are hints (the L2 is
+      // where every SM reads and writes), so they change no result even if
+      // the previous kernel writes these inputs; the loads come after the wait.
+      for (int r = 0; r < nrb; ++r)
+#pragma unroll
+        for (int a = 0; a < A; ++a) tma_prefetch_l2_3d(&tmQ, a * 64, kvh * G, b * N + node0 + r * nb);
+      const int rows = min(min(t_end - t_begin, kPrefetchTiles) * kBN, p.Lcap - t_begin * kBN);
+      if (rows > 0) {
+        bulk_prefetch_l2(p.k + (size_t)y0 * D, (uint32_t)rows * D * 2u);
+        bulk_prefetch_l2(p.v + (size_t)y0 * D, (uint32_t)rows * D * 2u);
+      }
     }
   }
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
@@ -416,49 +431,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       npv[r] = t + 1;
     };
     if constexpr (Sh::kPInTmem) {
-      // Per row block, in tile order: S_r(t) once PV_r(t - kSBufs) is issued
-      // (P lives in the S buffer's columns) and K(t) landed; PV_r(t) once the
-      // softmax wrote P_r(t) and V(t) landed.  K(t) is free when every row
-      // block issued S(t).
-      int ns[2] = {0, (nrb < 2) ? T : 0};
-      while (ok && min(npv[0], npv[1]) < T) {
-        bool prog = false;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int t = ns[r];
-          if (t < T && t <= npv[r] + kSBufs - 1) {
-            bool ready = false;
-            if (lane == 0) ready = mbar_test(&bar_k_full[t % kKStages], (t / kKStages) & 1);
-            if (__shfl_sync(0xffffffffu, ready, 0)) {
-              tc_fence_after();
-              if (lane == 0) {
-                issue_s(r, t);
-                if (ns[r ^ 1] > t) mma_commit(&bar_k_empty[t % kKStages]);
-              }
-              __syncwarp();
-              ns[r] = t + 1;
-              prog = true;
-            }
-          }
-          const int u = npv[r];
-          if (u < ns[r]) {
-            bool ready = false;
-            if (lane == 0)
-              ready = mbar_test(&bar_v_full[u % kVStages], (u / kVStages) & 1) &&
-                      mbar_test(&bar_p_full[r][u % kPBufs], (u / kPBufs) & 1);
-            if (__shfl_sync(0xffffffffu, ready, 0)) {
-              tc_fence_after();
-              issue_pv(r, u);
-              prog = true;
-            }
-          }
+      // One row block: the tensor-core order is fixed -- S(0), S(1), then for
+      // each tile PV(t) followed by S(t + 2), which reuses the S buffer that
+      // held P(t) (the tensor core runs one thread's instructions in issue
+      // order).  Each input is awaited with a blocking wait, which leaves the
+      // issue slots of this scheduler to the softmax warp that shares it.
+      auto s_in_order = [&](int t) -> bool {
+        if (!warp_wait(&bar_k_full[t % kKStages], (t / kKStages) & 1)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(0, t);
+          mma_commit(&bar_k_empty[t % kKStages]);  // K(t) is free once S(t) is done
         }
-        if (prog) {
-          t_idle = clock64();
-        } else {
-          const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
-          if (__shfl_sync(0xffffffffu, late, 0)) ok = false;
-        }
+        __syncwarp();
+        return true;
+      };
+      for (int t = 0; ok && t < min(T, kSBufs); ++t) ok = s_in_order(t);
+      for (int t = 0; ok && t < T; ++t) {
+        ok = warp_wait(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
+             warp_wait(&bar_p_full[0][t % kPBufs], (t / kPBufs) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, t);
+        if (t + kSBufs < T) ok = s_in_order(t + kSBufs);
       }
     } else {
       // Three streams of work, each in tile order: S(t) needs K(t) and both S
@@ -945,16 +940,7 @@ size_t plan_workspace(const SplitPlan& sp, int D) {
 
 template <int D, int RBS>
 bool set_smem_once() {
-  static bool done = false;
-  if (!done) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<D, RBS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<D, RBS>::kDyn) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    done = true;
-  }
-  return true;
+  return set_dyn_smem(attn_tc_kernel<D, RBS>, Layout<D, RBS>::kDyn);
 }
 
 template <int D, int RBS>
@@ -1011,6 +997,8 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
       return TV_ERR_INVALID_ARG;
   }
   AttnParams p;
+  p.k = reinterpret_cast<const uint16_t*>(k);
+  p.v = reinterpret_cast<const uint16_t*>(v);
   p.out = out;
   p.lse = lse;
   p.status = status;

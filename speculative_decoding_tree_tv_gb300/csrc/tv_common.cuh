@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <map>
+#include <mutex>
 #include <utility>
 
 #include "treeverify.h"
@@ -155,20 +158,62 @@ __device__ __forceinline__ double decision_uniform(uint64_t seed, uint64_t offse
 }
 
 // ------------------------------------------------------------------- host
-// SMs of the current device (152 on GB300 when no device can be queried).
-inline int device_sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else {
-      (void)cudaGetLastError();
-      n = 152;
-    }
+constexpr int kMaxDevicesCached = 64;
+
+// Ordinal of the current device, or -1 if none can be queried.
+inline int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
   }
-  return n;
+  return dev;
+}
+
+// SMs of the current device (152 on GB300 when no device can be queried),
+// looked up once per device.
+inline int device_sm_count() {
+  static std::atomic<int> cache[kMaxDevicesCached];
+  const int dev = current_device();
+  if (dev >= 0 && dev < kMaxDevicesCached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int v = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      v <= 0) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  if (dev < kMaxDevicesCached) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Set a kernel attribute on the current device.  Attributes are per device,
+// so each (kernel, attribute) pair is set once per device: a registry of
+// device bit-words under a lock.
+inline bool set_func_attr(const void* kernel, cudaFuncAttribute attr, int value) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, uint64_t> done;
+  const int dev = current_device();
+  if (dev < 0) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  uint64_t& word = done[{kernel, (int)attr}];
+  if (bit && (word & bit)) return true;
+  if (cudaFuncSetAttribute(kernel, attr, value) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  word |= bit;
+  return true;
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device.
+template <typename Kernel>
+inline bool set_dyn_smem(Kernel kernel, int bytes) {
+  return set_func_attr(reinterpret_cast<const void*>(kernel),
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // Launch with programmatic stream serialisation (see pdl_wait/pdl_trigger).

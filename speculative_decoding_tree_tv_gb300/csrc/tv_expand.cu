@@ -889,15 +889,9 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
   ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
   ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
   const int chunks = ceil_div(V, kExpChunk);
-  static bool smem_set = false;  // the select stages up to kSelStageKeys keys
-  if (!smem_set) {
-    if (cudaFuncSetAttribute(exp_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kSelStageKeys * sizeof(unsigned long long))) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
-    smem_set = true;
-  }
+  // the select stages up to kSelStageKeys keys
+  if (!set_dyn_smem(exp_select_kernel, (int)(kSelStageKeys * sizeof(unsigned long long))))
+    return TV_ERR_CUDA;
   if (launch_pdl(exp_stats_kernel, dim3(ceil_div(chunks, kStatsWarps), F), dim3(kStatsWarps * 32),
                  0, stream, draft_logits, V, chunks, frontier_logscore, ws) != cudaSuccess ||
       (!gated && launch_pdl(exp_floor_kernel, dim3(1), dim3(kFloorThreads), 0, stream,

@@ -90,7 +90,7 @@ __device__ __forceinline__ void prefetch_tree(const GreedyArgs& g, int b) {
   if (t < 3 * lines) {
     const int32_t* arr = (t < lines) ? g.parent : (t < 2 * lines) ? g.tokens : g.depth;
     const char* addr = reinterpret_cast<const char*>(arr + (size_t)b * g.N) + (t % lines) * 128;
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+    sm100::line_prefetch_l2(addr);
   }
 }
 
@@ -101,6 +101,22 @@ __device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
   const int tid = threadIdx.x;
   const int N = g.N;
   const size_t o = (size_t)b * N;
+  int32_t* pth = g.path + o;
+  if (err != TV_OK) {
+    // a copy of some CTA timed out: report it without reading the row keys,
+    // and without touching shared memory, where a copy may still be landing
+    for (int i = tid; i < N; i += kGreedyThreads) {
+      (void)atomicExch(g.ws.keys + o + i, 0ull);
+      g.argmax[o + i] = -1;
+      pth[i] = -1;
+    }
+    if (tid == 0) {
+      g.ws.arrivals[b] = 0u;
+      g.accept_len[b] = g.end_node[b] = g.bonus[b] = -1;
+      g.status[b] = err;
+    }
+    return;
+  }
   int bad_tree = 0, bad_tok = 0;
   __syncthreads();
   for (int i = tid; i < N; i += kGreedyThreads) {
@@ -127,12 +143,11 @@ __device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
   }
   bad_tree = __syncthreads_or(bad_tree);
   bad_tok = __syncthreads_or(bad_tok);
-  int32_t* pth = g.path + o;
-  if (bad_tree || bad_tok || err != TV_OK) {
+  if (bad_tree || bad_tok) {
     for (int i = tid; i < N; i += kGreedyThreads) pth[i] = -1;
     if (tid == 0) {
       g.accept_len[b] = g.end_node[b] = g.bonus[b] = -1;
-      g.status[b] = err != TV_OK ? err : bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
+      g.status[b] = bad_tree ? TV_ERR_INVALID_TREE : TV_ERR_INVALID_TOKEN;
     }
     return;
   }
@@ -391,9 +406,15 @@ greedy_bulk_kernel(const GreedyArgs g) {
   }
   __syncthreads();
   pdl_trigger();
+  // The chunk (and the tree) into the L2 while the previous kernel finishes.
+  // A prefetch changes no result: if the previous kernel writes the logits,
+  // its writes land in the same L2 and the copies below, issued after the
+  // wait, read them.
+  const float4* src = reinterpret_cast<const float4*>(g.logits + row * (long long)g.V) + base;
+  if (tid == 0) sm100::bulk_prefetch_l2(src, (uint32_t)n * 16u);
+  prefetch_tree(g, b);
   pdl_wait();  // the logits may come from the previous kernel
   if (tid == 0) {
-    const float4* src = reinterpret_cast<const float4*>(g.logits + row * (long long)g.V) + base;
     for (int q = 0; q < kGreedyPieces; ++q) {
       const int q0 = q * per, qn = min(per, n - q0);
       if (qn <= 0) break;
@@ -402,11 +423,7 @@ greedy_bulk_kernel(const GreedyArgs g) {
     }
   }
   TreeRegs tr{};
-  if (g.N <= kWarpScanMax) {
-    if (tid < 32) tr = load_tree_regs(g, b);
-  } else {
-    prefetch_tree(g, b);
-  }
+  if (g.N <= kWarpScanMax && tid < 32) tr = load_tree_regs(g, b);
   // four independent compare chains, one per float4 lane: each sees its
   // indices in increasing order, so a strict compare keeps the lowest index
   // of its maximum, and the combine below breaks ties to the lower index
@@ -419,7 +436,7 @@ greedy_bulk_kernel(const GreedyArgs g) {
     const int q0 = q * per, qn = min(per, n - q0);
     if (qn <= 0) break;
     if (!sm100::mbar_wait(&s_bar[q], 0)) {
-      ok = false;  // every copy of this CTA is waited for (bounded) below
+      ok = false;  // every copy of this CTA is waited for again (bounded) below
       continue;
     }
 #pragma unroll 4
@@ -435,6 +452,13 @@ greedy_bulk_kernel(const GreedyArgs g) {
   ArgMax best = argmax_combine(argmax_combine(c4[0], c4[1]), argmax_combine(c4[2], c4[3]));
   if (best.i == INT_MAX) best.i = 4 * base;  // only -inf seen: lowest index of the chunk
   const bool timed_out = __syncthreads_or(!ok) != 0;
+  if (timed_out && tid == 0) {
+    // no copy may still be landing when the CTA leaves or the last CTA reuses
+    // the chunk buffer for the tree scan: a second bounded wait on every piece
+    // (the scan skips shared memory altogether when a timeout is reported)
+    for (int q = 0; q < kGreedyPieces; ++q)
+      if (q * per < n) (void)sm100::mbar_wait(&s_bar[q], 0);
+  }
   // the chunk buffer is dead once every thread has reduced it (the block
   // reduction below starts with a barrier)
   finish_item(g, row, b, best, s_red, &s_last, timed_out, *reinterpret_cast<ScanSmem*>(g_smem),
@@ -449,19 +473,18 @@ greedy_scalar_kernel(const GreedyArgs g) {
   __shared__ ScanSmem s_scan;
   const int tid = threadIdx.x;
   pdl_trigger();
-  pdl_wait();  // the logits may come from the previous kernel
   const long long row = blockIdx.x / g.chunks;
   const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;
   const int n = min(g.chunk_units, g.V - base);
   const int b = (int)(row / g.N);
-  TreeRegs tr{};
-  if (g.N <= kWarpScanMax) {
-    if (tid < 32) tr = load_tree_regs(g, b);
-  } else {
-    prefetch_tree(g, b);
-  }
-  ArgMax best{-INFINITY, INT_MAX};
   const float* x = g.logits + row * (long long)g.V + base;
+  // the chunk's lines (and the tree) into the L2 before the wait (a hint)
+  for (int k = tid * 32; k < n; k += kGreedyThreads * 32) sm100::line_prefetch_l2(x + k);
+  prefetch_tree(g, b);
+  pdl_wait();  // the logits may come from the previous kernel
+  TreeRegs tr{};
+  if (g.N <= kWarpScanMax && tid < 32) tr = load_tree_regs(g, b);
+  ArgMax best{-INFINITY, INT_MAX};
   for (int k = tid; k < n; k += kGreedyThreads) {
     const float v = __ldg(x + k);
     if (v > best.v) best = {v, base + k};
@@ -491,15 +514,7 @@ tv_status launch_greedy(const GreedyArgs& in, cudaStream_t stream) {
   cudaError_t err;
   if (bulk) {
     const size_t smem = max((size_t)g.chunk_units * 16, sizeof(ScanSmem));
-    static bool smem_set = false;
-    if (!smem_set) {
-      if (cudaFuncSetAttribute(greedy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGreedyChunkMaxBytes) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return TV_ERR_CUDA;
-      }
-      smem_set = true;
-    }
+    if (!set_dyn_smem(greedy_bulk_kernel, kGreedyChunkMaxBytes)) return TV_ERR_CUDA;
     err = launch_pdl(greedy_bulk_kernel, dim3((unsigned)ctas), dim3(kGreedyThreads), smem, stream, g);
   } else {
     err = launch_pdl(greedy_scalar_kernel, dim3((unsigned)ctas), dim3(kGreedyThreads), 0, stream, g);

@@ -138,9 +138,6 @@ __device__ __forceinline__ void dsmem_st_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 // Ask the L2 for `bytes` (a multiple of 16, 16-byte aligned) of global memory.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 __global__ void __launch_bounds__(kWalkThreads)
 walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logits,
@@ -288,8 +285,8 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     }
     if (bulk && tid == 0 && nkids > 0 && slice_bytes > 0) {  // the likeliest next visit
       const size_t row1 = (size_t)b * N + s_kids[0];
-      prefetch_l2_bulk(p_logits + row1 * V + s_lo, slice_bytes);
-      prefetch_l2_bulk(q_logits + row1 * V + s_lo, slice_bytes);
+      sm100::bulk_prefetch_l2(p_logits + row1 * V + s_lo, slice_bytes);
+      sm100::bulk_prefetch_l2(q_logits + row1 * V + s_lo, slice_bytes);
     }
     if (bulk && slice_bytes > 0) {
       bool ok = sm100::mbar_wait(&s_bar, bar_parity);
@@ -572,15 +569,10 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
 // The walk kernel as clusters of `cl` CTAs, with programmatic dependent launch.
 template <typename... Args>
 cudaError_t launch_walk(int B, int cl, size_t smem, cudaStream_t stream, Args... args) {
-  static bool attrs_set = false;
-  if (!attrs_set) {
-    cudaError_t e = cudaFuncSetAttribute(walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kWalkCacheMax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(walk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    attrs_set = true;
-  }
+  if (!set_dyn_smem(walk_kernel, (int)kWalkCacheMax) ||
+      !set_func_attr(reinterpret_cast<const void*>(walk_kernel),
+                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * cl), 1, 1);
   cfg.blockDim = dim3(kWalkThreads, 1, 1);

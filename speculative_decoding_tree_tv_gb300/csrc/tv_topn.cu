@@ -242,15 +242,9 @@ extern "C" tv_status tv_select_topn(const int32_t* parent, const int32_t* token,
   if (!parent || !token || !logscore || !n_nodes || !out_parent || !out_token || !out_logscore ||
       !out_src || !expected || !status)
     return TV_ERR_INVALID_ARG;
-  static bool smem_set = false;  // up to 64 KB of keys
-  if (!smem_set) {
-    if (cudaFuncSetAttribute(tv::select_topn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(tv::kTopnMaxNodes * sizeof(unsigned int))) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TV_ERR_CUDA;
-    }
-    smem_set = true;
-  }
+  // up to 64 KB of keys
+  if (!tv::set_dyn_smem(tv::select_topn_kernel, (int)(tv::kTopnMaxNodes * sizeof(unsigned int))))
+    return TV_ERR_CUDA;
   if (tv::launch_pdl(tv::select_topn_kernel, dim3((unsigned)B), dim3(tv::kTopnThreads),
                      (size_t)M * sizeof(unsigned int), stream, parent, token, logscore, n_nodes, M,
                      n, out_parent, out_token, out_logscore, out_src, expected,

@@ -1,6 +1,7 @@
 // tv_tree_build: parent[] -> depth[] and ancestor-or-self bitmasks, the tree
 // attention mask of OPT-Tree §2 (a node attends to its ancestors and itself).
 #include "tv_common.cuh"
+#include "tv_sm100.cuh"
 
 namespace tv {
 namespace {
@@ -16,9 +17,12 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ uint64_t s_anc[kMaxNodes * kMaxWords];
   pdl_trigger();
-  pdl_wait();
   const int b = blockIdx.x;
   const int32_t* par = parent + (size_t)b * N;
+  // the parent row into the L2 while the previous kernel finishes (a hint:
+  // the reads below come after the wait)
+  if (threadIdx.x * 32 < N) sm100::line_prefetch_l2(par + threadIdx.x * 32);
+  pdl_wait();
   int32_t* dep = depth + (size_t)b * N;
   uint64_t* anc = anc_mask + (size_t)b * N * W;
 
