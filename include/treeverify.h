@@ -133,7 +133,10 @@ tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
  *             key range in one CTA; workspace may then be NULL.  Otherwise
  *             the key range of every 128-row tile is split over several CTAs
  *             and the call launches a second (merge) kernel; a workspace that
- *             is NULL, misaligned or smaller returns TV_ERR_WORKSPACE.
+ *             is NULL, misaligned or smaller returns TV_ERR_WORKSPACE.  The
+ *             partial rows are held as bf16 (the fp32 exponent range, so any
+ *             finite bf16 value of v survives the split), with fp32 row
+ *             maxima and sums.
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= TV_MAX_NODES; Lcap >= N.
  */
 size_t tv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int Lcap);

@@ -34,7 +34,8 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         fd, tmp = tempfile.mkstemp(suffix=".so", dir=_DIR)
         os.close(fd)
-        subprocess.check_call(["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-o", tmp, _SRC])
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fopenmp", "-shared", "-fPIC", "-o", tmp,
+                               _SRC])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -50,7 +51,9 @@ def _load():
         lib.or_attn_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, I, P, P]
         lib.or_accept_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P, P]
         lib.or_accept_sample.argtypes = [P, P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64,
-                                         ctypes.c_uint64, P, P, P, P, P, P, P]
+                                         ctypes.c_uint64, P, P, P, P, P, P, P, P, P]
+        lib.or_set_threads.argtypes = [I]
+        lib.or_set_threads.restype = None
         lib.or_expand_gated.argtypes = [P, P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, P]
         lib.or_expand_topn.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P]
         lib.or_select_topn.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P, P]
@@ -67,6 +70,12 @@ def _load():
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's loops over independent rows (n <= 0: one per
+    core, the default)."""
+    _load().or_set_threads(int(n))
 
 
 def _c(a, dtype):
@@ -148,13 +157,15 @@ def accept_sample(p_logits, q_logits, tokens, parent, temperature: float, seed: 
     r = dict(accept_len=np.zeros(B, np.int32), end_node=np.zeros(B, np.int32),
              path=np.zeros((B, N), np.int32), out_token=np.zeros(B, np.int32),
              status=np.zeros(B, np.int32), margin_accept=np.zeros(B, np.float64),
-             margin_draw=np.zeros(B, np.float64))
+             margin_path=np.zeros((B, N), np.float64), margin_draw=np.zeros(B, np.float64),
+             draw_alt=np.zeros(B, np.int32))
     _check(_load().or_accept_sample(ppl, qpl, tp, pp, B, N, V, float(temperature),
                                     int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
                                     r["accept_len"].ctypes.data, r["end_node"].ctypes.data,
                                     r["path"].ctypes.data, r["out_token"].ctypes.data,
                                     r["status"].ctypes.data, r["margin_accept"].ctypes.data,
-                                    r["margin_draw"].ctypes.data))
+                                    r["margin_path"].ctypes.data, r["margin_draw"].ctypes.data,
+                                    r["draw_alt"].ctypes.data))
     return r
 
 

@@ -7,7 +7,10 @@
 //
 // Everything is written as the plain definition: explicit ancestor sets
 // obtained by walking parent links, fp64 arithmetic, full sorts, brute force.
-// No blocking, fusion or reordering beyond what the definition states.
+// No blocking, fusion or reordering beyond what the definition states.  Loops
+// over independent rows (attention rows, argmax rows) may run on several
+// threads (OpenMP); each row is still computed start to finish by one thread
+// in the order written, so the results do not depend on the thread count.
 //
 // Sources (page title, section):
 //   [OPT]   "OPT-Tree: Speculative Decoding with Adaptive Draft Tree Structure",
@@ -51,6 +54,10 @@
 #include <algorithm>
 #include <cmath>
 #include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 namespace {
 
@@ -177,6 +184,16 @@ int or_tree_build(const int32_t* parent, int B, int N, int32_t* depth, uint64_t*
 // rows[3r..3r+2] = (b, i, h).  out[r*D + d] gets the output, lse[r] the
 // natural-log normaliser log sum_j exp(scale * q.k_j).
 // ---------------------------------------------------------------------------
+// Threads used by the loops over independent rows (OpenMP); n <= 0 keeps
+// the runtime's default (one per core).
+void or_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 int or_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                  const int32_t* kv_len, const int32_t* parent, int B, int N, int Hq,
                  int Hkv, int D, int Lcap, double scale, const int32_t* rows, int n_rows,
@@ -187,10 +204,15 @@ int or_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   for (int r = 0; r < n_rows; ++r) {
     const int b = rows[3 * r], i = rows[3 * r + 1], h = rows[3 * r + 2];
     if (b < 0 || b >= B || i < 0 || i >= N || h < 0 || h >= Hq) return ST_INVALID_ARG;
+    if (!tree_is_valid(parent + (size_t)b * N, N)) return ST_INVALID_TREE;
+    if (kv_len[b] < 0 || kv_len[b] + N > Lcap) return ST_INVALID_ARG;
+  }
+  // Rows are independent: each is computed by one thread, start to finish.
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < n_rows; ++r) {
+    const int b = rows[3 * r], i = rows[3 * r + 1], h = rows[3 * r + 2];
     const int32_t* par = parent + (size_t)b * N;
-    if (!tree_is_valid(par, N)) return ST_INVALID_TREE;
     const int L = kv_len[b];
-    if (L < 0 || L + N > Lcap) return ST_INVALID_ARG;
     const int kvh = h / G;
 
     std::vector<int> keys;  // cache positions visible to (b, i)
@@ -212,12 +234,17 @@ int or_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
       s[t] = dot * scale;
       m = std::max(m, s[t]);
     }
+    // softmax weights w_t = exp(s_t - max), the normaliser their sum
+    std::vector<double> w(keys.size());
     double denom = 0.0;
-    for (size_t t = 0; t < keys.size(); ++t) denom += exp(s[t] - m);
+    for (size_t t = 0; t < keys.size(); ++t) {
+      w[t] = exp(s[t] - m);
+      denom += w[t];
+    }
     for (int d = 0; d < D; ++d) {
       double acc = 0.0;
       for (size_t t = 0; t < keys.size(); ++t)
-        acc += exp(s[t] - m) * bf16_to_double(vbase[(size_t)keys[t] * D + d]);
+        acc += w[t] * bf16_to_double(vbase[(size_t)keys[t] * D + d]);
       out[(size_t)r * D + d] = acc / denom;
     }
     lse[r] = m + log(denom);
@@ -239,17 +266,19 @@ int or_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* 
                      int N, int V, int32_t* argmax, int32_t* accept_len, int32_t* end_node,
                      int32_t* path, int32_t* bonus, int32_t* status) {
   if (B < 0 || N < 1 || V < 1) return ST_INVALID_ARG;
+  // argmax of every node row (rows are independent: one thread each)
+#pragma omp parallel for schedule(static)
+  for (long long row_i = 0; row_i < (long long)B * N; ++row_i) {
+    const float* row = logits + (size_t)row_i * V;
+    int best = 0;
+    for (int t = 1; t < V; ++t)
+      if (row[t] > row[best]) best = t;
+    argmax[row_i] = best;
+  }
   for (int b = 0; b < B; ++b) {
     const int32_t* par = parent + (size_t)b * N;
     const int32_t* tok = tokens + (size_t)b * N;
-    int32_t* am = argmax + (size_t)b * N;
-    for (int i = 0; i < N; ++i) {
-      const float* row = logits + ((size_t)b * N + i) * V;
-      int best = 0;
-      for (int t = 1; t < V; ++t)
-        if (row[t] > row[best]) best = t;
-      am[i] = best;
-    }
+    const int32_t* am = argmax + (size_t)b * N;
     for (int i = 0; i < N; ++i) path[(size_t)b * N + i] = -1;
     accept_len[b] = end_node[b] = bonus[b] = -1;
     if (!tree_is_valid(par, N)) { status[b] = ST_INVALID_TREE; continue; }
@@ -289,29 +318,36 @@ int or_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* 
 //
 // Random words: Philox4x64-10 keyed by (seed, 0), counter (offset, b, v,
 // purpose<<32 | ordinal), each turned into a 53-bit uniform u.  Accept
-// tests compare u with the fp64 ratio.  The final draw keeps an fp64 running
-// sum of the probabilities rounded to fp32 (the precision in which the GPU
-// holds them element by element): the token is the smallest k whose
+// tests compare u with the fp64 ratio.  The final draw walks the fp64
+// probabilities in ascending token order: the token is the smallest k whose
 // cumulative mass exceeds u * (total mass); if rounding leaves none, the last
 // token with positive mass.
 //
 // margin_accept[b] = smallest |u - ratio| / ratio over tree b's accept tests;
+// margin_path[b, d] = the same over the accept tests made at the walk's node
+// of depth d (INFINITY where none was made), so a comparison can locate the
+// first decision that sits near its threshold;
 // margin_draw[b] = distance of u * total from the nearest cumulative boundary
-// of its final draw, divided by total.
+// of its final draw, divided by total; draw_alt[b] = the token a draw would
+// give on the other side of that boundary (the previous or next token with
+// positive mass; -1 if there is none).
 // ---------------------------------------------------------------------------
 int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t* tokens,
                      const int32_t* parent, int B, int N, int V, float temperature,
                      uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* end_node,
                      int32_t* path, int32_t* out_token, int32_t* status, double* margin_accept,
-                     double* margin_draw) {
+                     double* margin_path, double* margin_draw, int32_t* draw_alt) {
   if (B < 0 || N < 1 || V < 1 || !(temperature > 0.0f)) return ST_INVALID_ARG;
   const double T = (double)temperature;
   std::vector<double> r(V), q(V);
   for (int b = 0; b < B; ++b) {
     const int32_t* par = parent + (size_t)b * N;
     const int32_t* tok = tokens + (size_t)b * N;
-    for (int i = 0; i < N; ++i) path[(size_t)b * N + i] = -1;
-    accept_len[b] = end_node[b] = out_token[b] = -1;
+    for (int i = 0; i < N; ++i) {
+      path[(size_t)b * N + i] = -1;
+      margin_path[(size_t)b * N + i] = INFINITY;
+    }
+    accept_len[b] = end_node[b] = out_token[b] = draw_alt[b] = -1;
     margin_accept[b] = margin_draw[b] = INFINITY;
     if (!tree_is_valid(par, N)) { status[b] = ST_INVALID_TREE; continue; }
     bool tok_ok = true;
@@ -320,7 +356,7 @@ int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t
     if (!tok_ok) { status[b] = ST_INVALID_TOKEN; continue; }
     status[b] = ST_OK;
 
-    int node = 0;
+    int node = 0, node_depth = 0;
     int out = -1;
     for (;;) {
       const float* prow = p_logits + ((size_t)b * N + node) * V;
@@ -345,7 +381,12 @@ int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t
         } else {
           const double ratio = r[x] / q[x];
           acc = u < ratio;
-          if (ratio > 0.0) margin_accept[b] = std::min(margin_accept[b], fabs(u - ratio) / ratio);
+          if (ratio > 0.0) {
+            const double mg = fabs(u - ratio) / ratio;
+            margin_accept[b] = std::min(margin_accept[b], mg);
+            double& md = margin_path[(size_t)b * N + node_depth];
+            md = std::min(md, mg);
+          }
         }
         if (acc) { accepted = kids[o]; break; }
         double z = 0.0;
@@ -353,26 +394,39 @@ int or_accept_sample(const float* p_logits, const float* q_logits, const int32_t
         if (z > 0.0)
           for (int t = 0; t < V; ++t) r[t] = std::max(r[t] - q[t], 0.0) / z;
       }
-      if (accepted >= 0) { node = accepted; continue; }
+      if (accepted >= 0) {
+        node = accepted;
+        ++node_depth;
+        continue;
+      }
 
       // Final draw from r (the residual, or p_node at a leaf).
       const double u = uniform53(draw_word(seed, offset, b, node, PURPOSE_SAMPLE, 0));
       double total = 0.0;
-      for (int t = 0; t < V; ++t) total += (double)(float)r[t];
+      for (int t = 0; t < V; ++t) total += r[t];
       const double target = u * total;
       double cum = 0.0;
       int last_pos = -1;
+      bool lower_closer = false;  // the nearest boundary lies below the drawn token
       for (int t = 0; t < V; ++t) {
-        const double rt = (double)(float)r[t];
+        const double rt = r[t];
         if (rt > 0.0) last_pos = t;
         const double before = cum;
         cum += rt;
         if (out < 0 && cum > target) {
           out = t;
           margin_draw[b] = std::min(cum - target, target - before) / total;
+          lower_closer = (target - before) <= (cum - target);
         }
       }
       if (out < 0) out = last_pos;
+      if (lower_closer) {
+        for (int t = out - 1; t >= 0 && draw_alt[b] < 0; --t)
+          if (r[t] > 0.0) draw_alt[b] = t;
+      } else {
+        for (int t = out + 1; t < V && draw_alt[b] < 0; ++t)
+          if (r[t] > 0.0) draw_alt[b] = t;
+      }
       break;
     }
     std::vector<int> anc = ancestors_of(par, node);

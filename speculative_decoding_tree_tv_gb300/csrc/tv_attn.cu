@@ -22,7 +22,7 @@
 //                   softmax; zeroes V rows past the end of the key range so
 //                   that stale cache slots never reach a result.
 // Unsplit, each softmax thread normalises its row and writes it.  When the
-// key range is split across CTAs, each split stores its normalised fp16
+// key range is split across CTAs, each split stores its normalised bf16
 // partial rows to the workspace with one bulk copy, with (max, sum) pairs
 // beside them, and a merge kernel chained by programmatic dependent launch
 // combines the partials of every row.  Every wait is bounded.
@@ -31,7 +31,6 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include "tv_common.cuh"
 #include "tv_sm100.cuh"
@@ -89,7 +88,7 @@ struct AttnParams {
   int32_t* status;
   const int32_t* kv_len;
   const uint64_t* anc;
-  __half* part;     // split partials [unit][nsplit][D / 8][CTA rows] 16-byte chunks of 8 fp16
+  uint16_t* part;   // split partials [unit][nsplit][D / 8][CTA rows] 16-byte chunks of 8 bf16
   float2* part_ml;  // their (running max in the log2 domain, running sum) [unit][nsplit][CTA rows]
   int N, Hq, Hkv, G, Lcap, W;
   int nb;           // nodes per row block: floor(128 / G)
@@ -115,9 +114,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+// Two bf16 halves of a 32-bit word back to fp32 (exact).
+__device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Two fp32 lanes at once (Blackwell f32x2 instructions), round to nearest.
@@ -682,7 +681,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + lane_base + 32 * c, o[c]);  // warp-wide
       tmem_wait_ld();
       if (split_kv) {
-        // normalised fp16 partial row, chunk-major: the lanes of a warp hold
+        // normalised bf16 partial row (bf16 keeps the fp32 exponent range), chunk-major: the lanes of a warp hold
         // consecutive rows, so every store instruction writes 512 contiguous bytes
         uint4* dst = reinterpret_cast<uint4*>(p.part) + slot * (D / 8) * Sh::kRows + crow;
 #pragma unroll
@@ -690,10 +689,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             dst[(size_t)(4 * c + q) * Sh::kRows] = make_uint4(
-                pack_f16(__uint_as_float(o[c][8 * q + 0]) * inv, __uint_as_float(o[c][8 * q + 1]) * inv),
-                pack_f16(__uint_as_float(o[c][8 * q + 2]) * inv, __uint_as_float(o[c][8 * q + 3]) * inv),
-                pack_f16(__uint_as_float(o[c][8 * q + 4]) * inv, __uint_as_float(o[c][8 * q + 5]) * inv),
-                pack_f16(__uint_as_float(o[c][8 * q + 6]) * inv, __uint_as_float(o[c][8 * q + 7]) * inv));
+                pack_bf16(__uint_as_float(o[c][8 * q + 0]) * inv, __uint_as_float(o[c][8 * q + 1]) * inv),
+                pack_bf16(__uint_as_float(o[c][8 * q + 2]) * inv, __uint_as_float(o[c][8 * q + 3]) * inv),
+                pack_bf16(__uint_as_float(o[c][8 * q + 4]) * inv, __uint_as_float(o[c][8 * q + 5]) * inv),
+                pack_bf16(__uint_as_float(o[c][8 * q + 6]) * inv, __uint_as_float(o[c][8 * q + 7]) * inv));
       } else if (valid_row) {
         // the whole key range was here: write the output row
         uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + node) * p.Hq + h) * D);
@@ -720,7 +719,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
 // Merge of the split-KV partials: for every query row, weights
 // 2^(m_s - M) * l_s over the nsplit partials, normalised, applied to the
-// normalised fp16 partial rows.  A CTA takes 32 rows x 2 chunks of one unit;
+// normalised bf16 partial rows.  A CTA takes 32 rows x 2 chunks of one unit;
 // its 8 warps are (chunk, slot group): warp (c, g) takes slots g, g + 4, ...
 // of chunk c for 32 consecutive rows, so every load is one contiguous 512-byte
 // (chunk) or 256-byte (statistics) segment and all of a thread's loads are in
@@ -787,7 +786,7 @@ attn_merge_kernel(const AttnParams p) {
       const uint32_t xw[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[e]));
+        const float2 f = unpack_bf16(xw[e]);
         acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
         acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
       }
@@ -931,7 +930,7 @@ SplitPlan plan_splits(int B, int N, int Hq, int Hkv, int Lcap, int D) {
   return best_sp;
 }
 
-// Workspace bytes of a plan: fp16 partial rows, then their (max, sum) pairs.
+// Workspace bytes of a plan: bf16 partial rows, then their (max, sum) pairs.
 size_t plan_workspace(const SplitPlan& sp, int D) {
   if (sp.nsplit <= 1) return 0;
   const size_t rows = (size_t)sp.units * sp.nsplit * kRB * sp.rbs;
@@ -1009,7 +1008,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   if (need > 0) {
     const size_t rows = (size_t)sp.units * sp.nsplit * kRB * sp.rbs;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.part = reinterpret_cast<__half*>(ws);
+    p.part = reinterpret_cast<uint16_t*>(ws);
     p.part_ml = reinterpret_cast<float2*>(ws + align_up(rows * D * 2, 256));
   }
   p.N = N;

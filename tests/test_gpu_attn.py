@@ -124,26 +124,110 @@ def test_bad_kv_len_is_flagged(tv):
     assert (out[1:] == 0).all()
 
 
-def test_config4_ragged_batch_sampled(tv, oracle_mod):
-    sampled_check(tv, oracle_mod, gen.config4(V=8), 48, 5, "config4")
+def unit_rows(tv, case, seqs):
+    """Every (node, head) row of the first and the last node tile of the
+    sequences `seqs` under the plan the call takes: whole CTA units, so every
+    split of the key range, both row blocks of a 256-row CTA and every kv head
+    of those nodes are compared."""
+    plan = tv.attn_plan(case.B, case.N, case.Hq, case.Hkv, case.D, case.Lcap)
+    G = case.Hq // case.Hkv
+    per_tile = (plan["rows_per_cta"] // 128) * (128 // G)
+    last0 = (plan["node_tiles"] - 1) * per_tile
+    nodes = sorted(set(range(0, min(per_tile, case.N))) | set(range(last0, case.N)))
+    rows = np.array([(b, n, h) for b in seqs for n in nodes for h in range(case.Hq)], np.int64)
+    return rows, plan
 
 
-def test_config5_long_context_sampled(tv, oracle_mod):
-    sampled_check(tv, oracle_mod, gen.config5(256, V=5000), 24, 6, "config5")
+def unit_check(tv, oracle_mod, case, seqs, what):
+    out, lse, status = run_attn(tv, case)
+    assert (status == 0).all()
+    rows, plan = unit_rows(tv, case, seqs)
+    ref, ref_lse = oracle_mod.attn_rows(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq,
+                                        case.Hkv, rows)
+    check_attn(out[rows[:, 0], rows[:, 1], rows[:, 2]], ref, what)
+    np.testing.assert_allclose(lse[rows[:, 0], rows[:, 1], rows[:, 2]], ref_lse, atol=2e-3)
+    return out, plan
+
+
+def test_config4_ragged_batch_units(tv, oracle_mod):
+    """Batched ragged workload: whole node tiles of the first sequence and of
+    the one with the longest prefix (every head, every key)."""
+    case = gen.config4(V=8)
+    longest = int(np.argmax(case.kv_len))
+    unit_check(tv, oracle_mod, case, sorted({0, longest}), "config4")
+    sampled_check(tv, oracle_mod, case, 48, 5, "config4-sampled")
+
+
+def test_config5_long_context_units(tv, oracle_mod):
+    """Long context, 256 nodes: the first and last node tiles in full (a plan
+    of 256-row CTAs over several key splits: both row blocks, every split)."""
+    case = gen.config5(256, V=5000)
+    _, plan = unit_check(tv, oracle_mod, case, [0], "config5")
+    assert plan["splits"] > 1
 
 
 @pytest.mark.parametrize("n", [16, 64, 512])
-def test_config5_long_context_sweep_sampled(tv, oracle_mod, n):
-    """The long-context workload's node-count sweep: 16, 64 and 512 OPT-Tree
-    nodes over the 32,768-key prefix (256 is the case above)."""
-    sampled_check(tv, oracle_mod, gen.config5(n, V=64), 16, 9 + n, f"config5-n{n}")
+def test_config5_long_context_sweep(tv, oracle_mod, n):
+    """The long-context workload's node-count sweep (16, 64 and 512 nodes over
+    the 32,768-key prefix; 256 is the case above): every row at 16 nodes, the
+    first and last node tiles in full at 64 and 512."""
+    case = gen.config5(n, V=64)
+    if n == 16:
+        full_check(tv, oracle_mod, case, "config5-n16")
+    else:
+        unit_check(tv, oracle_mod, case, [0], f"config5-n{n}")
 
 
-def test_config3_talon_tree_sampled(tv, oracle_mod):
+def test_config3_talon_chain(tv, oracle_mod):
+    """The TALON workload end to end on the GPU -- gated expansion, tree
+    encoding, attention, greedy acceptance -- against the same chain on the
+    oracle: the tree and the acceptance result bit-exact, the attention rows
+    of the first and last node tiles in full within the attention tolerance."""
     d = gen.config3_drafter(1)
-    tree = oracle_mod.expand_tree(d, 10, 0.3, 512)
-    case = gen.config3_verify(tree["parent"], 1, tokens=tree["token"])
-    sampled_check(tv, oracle_mod, case, 24, 7, "config3")
+    g = tv.expand_tree(d.rows, d.root_key(), d.child_key, 10, 0.3, 512, dev())
+    o = oracle_mod.expand_tree(d, 10, 0.3, 512)
+    assert g["n"] == o["n"] == 512
+    gpar, gtok = g["parent"].numpy()[:512], g["token"].numpy()[:512]
+    assert np.array_equal(gpar, o["parent"]) and np.array_equal(gtok, o["token"])
+    case = gen.config3_verify(gpar, 1, tokens=gtok)
+    t = case_tensors(case)
+    depth, anc, tstat = tv.tree_build(t["parent"])
+    out, lse, astat = tv.attn_verify(t["q"], t["k"], t["v"], t["kv_len"], anc)
+    res = tv.accept_greedy(t["logits"], t["tokens"], t["parent"], depth)
+    torch.cuda.synchronize()
+    od, oa, ost = oracle_mod.tree_build(case.parent)
+    assert np.array_equal(np_(depth), od) and np.array_equal(np_(anc).view(np.uint64), oa)
+    assert (np_(tstat) == 0).all() and (np_(astat) == 0).all()
+    rows, _ = unit_rows(tv, case, [0])
+    ref, _ = oracle_mod.attn_rows(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq,
+                                  case.Hkv, rows)
+    check_attn(bf16_np(out)[rows[:, 0], rows[:, 1], rows[:, 2]], ref, "config3-chain")
+    og = oracle_mod.accept_greedy(case.logits, case.tokens, case.parent)
+    for k in ("argmax", "accept_len", "end_node", "path", "bonus", "status"):
+        assert np.array_equal(np_(res[k]), og[k]), k
+
+
+def test_split_partials_keep_the_range(tv, oracle_mod, monkeypatch):
+    """Split plans hold partial rows in bf16, which keeps the fp32 exponent
+    range: values of v of magnitude 1e5 and more (beyond fp16) survive the
+    merge.  The output is bf16, so the comparison is relative to the values'
+    scale: max-abs within 3e-2 of the largest |v| and rel-L2 within 1e-2."""
+    case = gen.make_case(41, B=1, N=60, L=1500, Hq=32, Hkv=8, D=128, V=64, tree="spine60")
+    big = case.v.copy()
+    f = gen.f32_from_bf16(big) * np.float32(3e5)
+    big = gen.bf16_from_f32(f)
+    case.v = big
+    for plan in ("128,4", "256,3", "128,1"):
+        monkeypatch.setenv("TV_ATTN_PLAN", plan)
+        out, lse, status = run_attn(tv, case)
+        assert (status == 0).all()
+        ref, ref_lse = oracle_mod.attn_all(case.q, case.k, case.v, case.kv_len, case.parent,
+                                           case.Hq, case.Hkv)
+        scale = float(np.abs(gen.f32_from_bf16(case.v)).max())
+        assert np.isfinite(out).all(), plan
+        err = np.abs(out - ref)
+        assert err.max() <= 3e-2 * scale, (plan, err.max() / scale)
+        assert np.linalg.norm(out - ref) <= 1e-2 * np.linalg.norm(ref), plan
 
 
 def test_merge_kernel_path_large_batch(tv, oracle_mod):

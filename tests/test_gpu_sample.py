@@ -2,15 +2,27 @@
 concept page, "The protocol" step 3: min(1, p/q) acceptance with (p - q)+
 residual resampling).
 
-Both sides draw the same Philox4x64-10 words and take every decision in fp64;
-they can only disagree where a decision sits within rounding distance of its
-threshold.  The oracle reports, per tree, the smallest relative distance of an
-accept test from its threshold (|u - r/q| / (r/q)) and the distance of the
-final draw from the nearest cumulative-mass boundary (as a fraction of the
-total mass).  The GPU holds each probability in fp32 (about 1e-6 relative
-error) and sums them in fp64 or compensated fp32, so accept tests closer than
-1e-5 and draws closer than 1e-7 are "ambiguous": those trees are checked for
-validity only (and counted); all other trees must match bit for bit."""
+Both sides draw the same Philox4x64-10 words.  The oracle takes every decision
+in fp64; the GPU holds each probability in fp32, made with the special-function
+unit's 2^x (about 2^-22 relative error) and fp32 products, so each probability
+is within about 5e-7 of its fp64 value, relative.  Two kinds of decision can
+therefore go either way, and only those:
+  * an accept test u < r(x)/q(x) whose ratio lies within 1e-5 of u, relative
+    to the ratio (5e-7 per probability, amplified by the cancellation in a
+    residual (r - q)+ up to twenty-fold);
+  * the final draw, when u times the total mass lies within 1e-6 of the total
+    from a cumulative boundary (cumulative masses and the target each within
+    5e-7 of the total).
+With a 128,256-token vocabulary each token holds about 8e-6 of the mass, so a
+uniform target falls that close to a boundary in roughly one draw in eight;
+at the batched configuration's seeds no accept test is closer than 2e-2 to its
+threshold and five of the 32 draws are inside the draw margin.
+The oracle reports the margin of every decision along its walk.  A tree whose
+decisions all clear their margins must match bit for bit.  Otherwise the GPU's
+walk must agree with the oracle's on every node reached before the first
+near-threshold decision, its path must be the root chain of its end node, and
+a draw-only ambiguity must give the oracle's token or the one across the
+nearest boundary."""
 import numpy as np
 import pytest
 import torch
@@ -23,8 +35,8 @@ from _gpu_util import case_tensors, i32, f32, np_
 
 pytestmark = pytest.mark.gpu
 
-MARGIN_ACCEPT = 1e-5
-MARGIN_DRAW = 1e-7
+MARGIN_ACCEPT = 1e-5   # relative to r(x)/q(x)
+MARGIN_DRAW = 1e-6     # fraction of the total mass
 
 
 @pytest.fixture(scope="module")
@@ -42,18 +54,47 @@ def run_sample(tv, case, seed, offset, T=1.0):
     return {k: np_(v) for k, v in res.items()}
 
 
-def compare(g, o, parent):
-    ambiguous = 0
+def compare(g, o, parent, V):
+    """Check every tree; return the indices of the trees with a decision
+    inside its rounding margin."""
+    ambiguous = []
     for b in range(len(o["status"])):
-        assert g["status"][b] == o["status"][b]
-        if o["margin_accept"][b] < MARGIN_ACCEPT or o["margin_draw"][b] < MARGIN_DRAW:
-            ambiguous += 1
-            e = g["end_node"][b]
-            assert 0 <= e < parent.shape[1]
-            assert g["accept_len"][b] == gen.depth_of(parent[b])[e]
+        assert g["status"][b] == o["status"][b], b
+        if o["status"][b] != 0:
+            assert g["end_node"][b] == -1 and g["out_token"][b] == -1, b
             continue
-        for k in ("accept_len", "end_node", "path", "out_token"):
-            assert np.array_equal(g[k][b], o[k][b]), (k, b)
+        od = int(o["accept_len"][b])
+        amb_depth = np.nonzero(o["margin_path"][b, :od + 1] < MARGIN_ACCEPT)[0]
+        draw_amb = o["margin_draw"][b] < MARGIN_DRAW
+        if len(amb_depth) == 0 and not draw_amb:
+            for k in ("accept_len", "end_node", "path", "out_token"):
+                assert np.array_equal(g[k][b], o[k][b]), (k, b)
+            continue
+        ambiguous.append(b)
+        # the GPU's result is a valid walk: its path is the root chain of its
+        # end node, padded with -1, and its token lies in the vocabulary
+        e = int(g["end_node"][b])
+        assert 0 <= e < parent.shape[1]
+        chain = [e]
+        while parent[b][chain[-1]] >= 0:
+            chain.append(int(parent[b][chain[-1]]))
+        chain = chain[::-1]
+        assert g["accept_len"][b] == len(chain) - 1
+        assert g["path"][b][:len(chain)].tolist() == chain
+        assert (g["path"][b][len(chain):] == -1).all()
+        assert 0 <= g["out_token"][b] < V
+        if len(amb_depth):
+            # every decision before the first near-threshold accept test is
+            # exact: both walks reach the node that makes it
+            d0 = int(amb_depth[0])
+            assert g["accept_len"][b] >= d0
+            assert np.array_equal(g["path"][b][:d0 + 1], o["path"][b][:d0 + 1]), b
+        else:
+            # only the final draw is near a boundary: same walk, and the token
+            # is the oracle's or the one across that boundary
+            for k in ("accept_len", "end_node", "path"):
+                assert np.array_equal(g[k][b], o[k][b]), (k, b)
+            assert g["out_token"][b] in (o["out_token"][b], o["draw_alt"][b]), b
     return ambiguous
 
 
@@ -63,7 +104,12 @@ def test_config4_batched_ragged(tv, oracle_mod):
         g = run_sample(tv, case, 0x5EED, offset)
         o = oracle_mod.accept_sample(case.p_logits, case.q_logits, case.tokens, case.parent, 1.0,
                                      0x5EED, offset)
-        assert compare(g, o, case.parent) <= 2
+        amb = compare(g, o, case.parent, case.V)
+        # the ambiguous trees are the ones the oracle's margins mark: here only
+        # final draws (no accept test of these seeds is within 2e-2 of its threshold)
+        assert all(o["margin_path"][b].min() > 1e-2 for b in range(case.B)), offset
+        print(f"offset {offset}: draws inside the margin in trees {amb}, margins "
+              f"{[float(o['margin_draw'][b]) for b in amb]}")
 
 
 @pytest.mark.parametrize("seed,B,N,V,T,noise", [
@@ -74,13 +120,11 @@ def test_config4_batched_ragged(tv, oracle_mod):
 def test_sample_fuzz(tv, oracle_mod, seed, B, N, V, T, noise):
     case = gen.make_case(seed, B=B, N=N, L=4, V=V, mode="sample", tree="random", max_depth=8,
                          q_noise=noise, temperature=T, with_attn=False)
-    total_amb = 0
     for offset in range(3):
         g = run_sample(tv, case, seed * 1000 + 1, offset, T)
         o = oracle_mod.accept_sample(case.p_logits, case.q_logits, case.tokens, case.parent, T,
                                      seed * 1000 + 1, offset)
-        total_amb += compare(g, o, case.parent)
-    assert total_amb <= max(2, (3 * B) // 5)
+        compare(g, o, case.parent, V)
 
 
 def test_q_equals_p_and_one_hot(tv, oracle_mod):
@@ -89,7 +133,7 @@ def test_q_equals_p_and_one_hot(tv, oracle_mod):
     case.q_logits = case.p_logits.copy()
     g = run_sample(tv, case, 3, 0)
     o = oracle_mod.accept_sample(case.p_logits, case.q_logits, case.tokens, case.parent, 1.0, 3, 0)
-    compare(g, o, case.parent)
+    compare(g, o, case.parent, case.V)
     for b in range(case.B):     # every first child accepted down to a leaf
         kids = gen.children_of(case.parent[b])
         v = 0

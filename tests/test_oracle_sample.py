@@ -218,3 +218,62 @@ def test_bad_inputs(oracle_mod):
     assert res["status"].tolist() == [0, 2, 6]
     with pytest.raises(ValueError):
         oracle_mod.accept_sample(lp, lp, tokens, parent, 0.0, 0, 0)
+
+
+def test_draw_margin_and_alternative_token(oracle_mod):
+    """The final draw (concept page, "The protocol" step 3; inverse CDF in
+    ascending token order) recomputed with numpy for root-only trees, where
+    the draw is from p_root: the drawn token, its distance from the nearest
+    cumulative boundary and the token on the other side of that boundary."""
+    r = gen.rng(91)
+    for trial in range(40):
+        V = int(r.integers(2, 300))
+        lp = r.standard_normal((1, 1, V)).astype(np.float32) * 2
+        lp[0, 0, r.integers(0, V, 3)] = -np.inf if trial % 5 == 0 else lp[0, 0, 0]
+        lq = lp.copy()
+        o = oracle_mod.accept_sample(lp, lq, np.zeros((1, 1), np.int32),
+                                     np.array([[-1]], np.int32), 1.0, 500 + trial, 0)
+        p = np.exp(lp[0, 0].astype(np.float64) - np.logaddexp.reduce(lp[0, 0].astype(np.float64)))
+        w = oracle_mod.draw_word(500 + trial, 0, 0, 0, oracle_mod.PURPOSE_SAMPLE, 0)
+        u = (w >> 11) * 2.0 ** -53
+        cum = np.cumsum(p)
+        target = u * cum[-1]
+        k = int(np.searchsorted(cum, target, side="right"))
+        assert o["out_token"][0] == k
+        lo = cum[k - 1] if k > 0 else 0.0
+        margin = min(cum[k] - target, target - lo) / cum[-1]
+        assert abs(o["margin_draw"][0] - margin) <= 1e-12
+        pos = np.nonzero(p > 0)[0]
+        if target - lo <= cum[k] - target:
+            below = pos[pos < k]
+            alt = int(below[-1]) if len(below) else -1
+        else:
+            above = pos[pos > k]
+            alt = int(above[0]) if len(above) else -1
+        assert o["draw_alt"][0] == alt
+
+
+def test_margin_path_locates_each_accept_test(oracle_mod):
+    """margin_path[b, d] is the smallest |u - r/q| / (r/q) over the accept
+    tests made at the walk's node of depth d: recomputed for a chain, where
+    each node has one child and r = p at every test."""
+    r = gen.rng(92)
+    N, V = 6, 40
+    parent = np.arange(-1, N - 1, dtype=np.int32)[None]
+    lp = r.standard_normal((1, N, V)).astype(np.float32)
+    lq = (lp + r.normal(0, 1.0, (1, N, V))).astype(np.float32)
+    tok = r.integers(0, V, (1, N)).astype(np.int32)
+    o = oracle_mod.accept_sample(lp, lq, tok, parent, 1.0, 77, 3)
+    sm = lambda x: np.exp(x - np.logaddexp.reduce(x))
+    end = o["accept_len"][0]
+    for d in range(N):
+        if d > end or d == N - 1:
+            assert np.isinf(o["margin_path"][0, d])
+            continue
+        p = sm(lp[0, d].astype(np.float64))
+        q = sm(lq[0, d].astype(np.float64))
+        x = tok[0, d + 1]
+        u = (oracle_mod.draw_word(77, 3, 0, d, oracle_mod.PURPOSE_ACCEPT, 0) >> 11) * 2.0 ** -53
+        ratio = p[x] / q[x]
+        assert abs(o["margin_path"][0, d] - abs(u - ratio) / ratio) <= 1e-9 * max(1.0, ratio)
+        assert (u < ratio) == (d < end)

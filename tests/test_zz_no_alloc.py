@@ -5,11 +5,13 @@ where they run acceptance -- a serving loop whose memory was planned once at
 start-up, a plug-in that is handed no allocator, a real-time path that must
 not allocate.  It keeps its scratch in a fixed array inside the library
 instead of a caller workspace.  This test calls it directly through the C ABI
-twice in a row (two different tree batches, so the second call runs on
-whatever the first left in the array) and checks every output against the
-workspace-taking tv_accept_greedy on the same inputs: acceptance results are
-integers, so they must be identical.  It lives in a file of its own that is
-collected last, and it needs nothing from the other tests.
+three times in a row (different tree batches, so each call runs on whatever
+the previous one left in the array; the third has 200-node trees and an odd
+vocabulary, which take the shared-memory tree scan and the scalar-load
+kernel) and checks every output against the workspace-taking
+tv_accept_greedy on the same inputs and against the CPU oracle: acceptance
+results are integers, so they must be identical.  It lives in a file of its
+own that is collected last, and it needs nothing from the other tests.
 """
 import ctypes
 
@@ -38,12 +40,14 @@ def _inputs(case, dev):
     return t
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(oracle_mod):
     tv, fn = _noalloc_fn()
     dev = torch.device("cuda:0")
     cases = [gen.make_case(901, B=3, N=40, L=4, V=20000, tree="random", max_depth=9,
                            with_attn=False),
              gen.make_case(902, B=8, N=64, L=4, V=128256, tree="random", max_depth=8,
+                           with_attn=False),
+             gen.make_case(903, B=2, N=200, L=4, V=1001, tree="random", max_depth=20,
                            with_attn=False)]
     for case in cases:
         t = _inputs(case, dev)
@@ -61,6 +65,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         for k in ref:
             assert torch.equal(out[k], ref[k]), k
         assert int(ref["status"].abs().sum()) == 0
+        og = oracle_mod.accept_greedy(case.logits, case.tokens, case.parent)
+        for k in ("argmax", "accept_len", "end_node", "path", "bonus", "status"):
+            assert np.array_equal(out[k].cpu().numpy(), og[k]), k
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
