@@ -277,9 +277,12 @@ def measure_commit(torch, tv, stream, k, v, kv_len, path, accept_len, hbm):
             "bound": "latency (a few KB per launch)"}
 
 
-def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tflops, l2):
-    """One verify step of a configuration: tree -> attention -> acceptance,
-    inputs resident (one set; the step's bytes are stated against L2)."""
+def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tflops, l2,
+                          oracle_budget_s=0.0):
+    """One verify step of a configuration: tree -> attention -> acceptance.
+    The timed graphs cycle over enough copies of the inputs that the steps
+    in flight read at least three times the L2 size, so every step reads HBM
+    (one copy when a single step's inputs already exceed that)."""
     def bf16(u):
         return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).to(device).view(
             torch.bfloat16)
@@ -294,6 +297,15 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
     else:
         t["p"] = torch.from_numpy(case.p_logits).to(device)
         t["q_l"] = torch.from_numpy(case.q_logits).to(device)
+    set_bytes = sum(x.numel() * x.element_size() for x in t.values())
+    # enough copies to read 3x the L2 per cycle, at most 64 (a tiny workload
+    # then stays in the L2, which its line says)
+    M = min(64, max(1, int(np.ceil(3 * l2 / set_bytes))))
+    sets = [t] + [{k: x.clone() for k, x in t.items()} for _ in range(M - 1)]
+    cur = [0]   # the set the next call uses; advanced by each whole step
+
+    def s_():
+        return sets[cur[0] % M]
     W = (N + 63) // 64
     depth = torch.empty((B, N), dtype=torch.int32, device=device)
     anc = torch.empty((B, N, W), dtype=torch.int64, device=device)
@@ -315,30 +327,37 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
                      out_token=torch.empty(B, dtype=torch.int32, device=device),
                      status=torch.empty(B, dtype=torch.int32, device=device))
 
-    def f_tree():
-        tv.tree_build(t["parent"], depth, anc, tst)
+    def f_tree(advance=True):
+        tv.tree_build(s_()["parent"], depth, anc, tst)
+        cur[0] += advance
 
-    def f_attn():
-        tv.attn_verify(t["q"], t["k"], t["v"], t["kv_len"], anc, out=out, lse=lse, status=ast)
+    def f_attn(advance=True):
+        x = s_()
+        tv.attn_verify(x["q"], x["k"], x["v"], x["kv_len"], anc, out=out, lse=lse, status=ast)
+        cur[0] += advance
 
-    def f_acc():
+    def f_acc(advance=True):
+        x = s_()
         if accept == "greedy":
-            tv.accept_greedy(t["logits"], t["tokens"], t["parent"], depth, outs=aouts)
+            tv.accept_greedy(x["logits"], x["tokens"], x["parent"], depth, outs=aouts)
         else:
-            tv.accept_sample(t["p"], t["q_l"], t["tokens"], t["parent"], depth, 1.0, 1234, 0,
+            tv.accept_sample(x["p"], x["q_l"], x["tokens"], x["parent"], depth, 1.0, 1234, 0,
                              outs=aouts)
+        cur[0] += advance
 
     def f_step():
-        f_tree()
-        f_attn()
-        f_acc()
+        f_tree(False)
+        f_attn(False)
+        f_acc(False)
+        cur[0] += 1
 
     with torch.cuda.stream(stream):
         for _ in range(3):
             f_step()
     torch.cuda.synchronize()
     assert int(tst.max()) == 0 and int(ast.max()) == 0 and int(aouts["status"].max()) == 0
-    us = {k: graph_time_us(torch, stream, f, 20, 5)
+    glen = M * max(1, -(-20 // M))
+    us = {k: graph_time_us(torch, stream, f, glen, 5)
           for k, f in (("step", f_step), ("tv_tree_build", f_tree), ("tv_attn_verify", f_attn),
                        ("tv_accept_" + accept, f_acc))}
     commit = measure_commit(torch, tv, stream, t["k"], t["v"], t["kv_len"], aouts["path"],
@@ -356,9 +375,17 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
     t_attn = max(nb["attn"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
     t_acc = acc_bytes / (hbm * 1e9) * 1e6
     t_tree = nb["tree"] / (hbm * 1e9) * 1e6
-    resident = sum(x.numel() * x.element_size() for x in t.values())
+    resident = set_bytes
+    oracle_line = None
+    if oracle_budget_s > 0:
+        cores = os.cpu_count() or 1
+        v_all, what = oracle_rate(case, accept, oracle_budget_s, cores)
+        v_one, _ = oracle_rate(case, accept, oracle_budget_s, 1)
+        oracle_line = {"steps_per_s": v_all, "cores": cores, "steps_per_s_1_thread": v_one,
+                       "sample": what}
     return {
         "workload": name, "us_per_step": us["step"],
+        "oracle": oracle_line,
         "us_per_launch": {k: v for k, v in us.items() if k != "step"},
         "roofline_step_us": t_attn + t_acc + t_tree,
         "roofline_step_frac": (t_attn + t_acc + t_tree) / us["step"],
@@ -370,7 +397,11 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
                    "frac": t_acc / us["tv_accept_" + accept]},
         "commit": commit,
         "inputs_resident_mb": resident / 1e6,
-        "l2": f"inputs resident, {resident / 1e6:.0f} MB against the {l2 / 1e6:.0f} MB L2",
+        "l2": (f"{M} rotating input sets of {resident / 1e6:.1f} MB" if M > 1 else
+               f"one input set of {resident / 1e6:.0f} MB") +
+              (f" (>= 3x the {l2 / 1e6:.0f} MB L2 per cycle of the timed graph)"
+               if M * resident >= 3 * l2 else
+               f" (L2-resident: {M * resident / 1e6:.1f} MB against the {l2 / 1e6:.0f} MB L2)"),
     }
 
 
@@ -512,9 +543,10 @@ def measure_opt_tree(torch, tv, device, stream, hbm):
     return out
 
 
-def measure_other_configs(torch, tv, device, hbm, tflops):
-    """Long context (greedy), batched stochastic acceptance, TALON expansion
-    and its 512-node verify."""
+def measure_other_configs(torch, tv, device, hbm, tflops, oracle_budget_s=0.0):
+    """Tiny, long context (greedy), batched stochastic acceptance, TALON
+    expansion and its 512-node verify; with oracle_budget_s > 0 the oracle is
+    timed beside each verify configuration."""
     from workloads import gen
     stream = torch.cuda.Stream(device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -541,10 +573,16 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
                                **measure_commit(torch, tv, stream, t["k"], t["v"], t["kv_len"],
                                                 g["path"], g["accept_len"], hbm))
     del t, g
+    case = gen.config1()
+    res["tiny"] = measure_verify_config(
+        "tiny: prefix 128, 8/8 heads, head_dim 64, 16-node random tree, vocab 1000, greedy",
+        case, "greedy", torch, tv, device, stream, hbm, tflops, l2, oracle_budget_s)
+    del case
     case = gen.config5(256)
     res["long_context"] = measure_verify_config(
         "long context: prefix 32768, 32/8 heads, head_dim 128, 256-node OPT-Tree-style tree, "
-        "vocab 128256, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2)
+        "vocab 128256, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2,
+        oracle_budget_s)
     del case
     # the same workload's node-count sweep (16, 64 and 512 nodes; 256 is above)
     sweep = {}
@@ -565,7 +603,7 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
     res["batched_stochastic"] = measure_verify_config(
         "batched stochastic: 16 sequences, prefixes in [512, 8192], 64-node trees, 32/8 heads, "
         "head_dim 128, vocab 128256, p/q acceptance at T = 1", case, "sample", torch, tv, device,
-        stream, hbm, tflops, l2)
+        stream, hbm, tflops, l2, oracle_budget_s)
     del case
     res["opt_tree_growth"] = measure_opt_tree(torch, tv, device, stream, hbm)
     tree, res["talon_expansion"] = measure_talon_expansion(torch, tv, device, stream, hbm)
@@ -573,7 +611,8 @@ def measure_other_configs(torch, tv, device, hbm, tflops):
                               tokens=tree["token"].numpy().astype(np.int32))
     res["talon_verify"] = measure_verify_config(
         f"TALON verify: prefix 4096, 64/8 heads, head_dim 128, the {case.N}-node expanded tree, "
-        "vocab 32000, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2)
+        "vocab 32000, greedy", case, "greedy", torch, tv, device, stream, hbm, tflops, l2,
+        oracle_budget_s)
     torch.cuda.synchronize()
     return res
 
@@ -839,23 +878,75 @@ def oracle_step_sample(case, rows_attn, rows_greedy, rng):
                              np.ascontiguousarray(case.parent[:, :rows_greedy]))
 
 
-def cpu_baseline(case, budget_s=12.0):
-    """Whole oracle steps on one host core until about budget_s seconds."""
+def cpu_model():
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                             text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def oracle_rate(case, accept, budget_s, threads, seed=0):
+    """Oracle verify steps/s of a workload on `threads` host threads: tree
+    encoding, attention rows, acceptance.  Whole steps when they fit the
+    budget; otherwise a random sample of the attention rows, scaled to the
+    whole step (the tree encoding and the acceptance are always whole).
+    Returns (steps/s, description of the sample)."""
     import oracle
     oracle.build()
-    rng = np.random.default_rng(0)
+    oracle.set_threads(threads)
+    rng = np.random.default_rng(seed)
+    total_rows = case.B * case.N * case.Hq
+
+    def accept_once():
+        if accept == "greedy":
+            oracle.accept_greedy(case.logits, case.tokens, case.parent)
+        else:
+            oracle.accept_sample(case.p_logits, case.q_logits, case.tokens, case.parent, 1.0,
+                                 1234, 0)
+
     t0 = time.perf_counter()
-    done = 0
-    while True:
-        oracle_step_sample(case, case.N * case.Hq, case.N, rng)
-        done += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} full step(s) of the workload (tree encoding, all "
-                      f"{case.N * case.Hq} attention rows in fp64, greedy over all {case.N} "
-                      f"rows), single thread, {dt:.1f} s"}
+    oracle.tree_build(case.parent)
+    accept_once()
+    t_fixed = time.perf_counter() - t0
+    # probe the cost of a row, then size the sample to the budget
+    probe = min(total_rows, max(threads, 8))
+
+    def rows_time(k):
+        idx = rng.choice(total_rows, size=k, replace=False)
+        rows = np.stack([idx // (case.N * case.Hq), (idx // case.Hq) % case.N, idx % case.Hq],
+                        axis=1)
+        t1 = time.perf_counter()
+        oracle.attn_rows(case.q, case.k, case.v, case.kv_len, case.parent, case.Hq, case.Hkv,
+                         rows)
+        return time.perf_counter() - t1
+
+    t_probe = rows_time(probe) / probe
+    k = int(min(total_rows, max(probe, (budget_s - t_fixed) / max(t_probe, 1e-9))))
+    t_rows = rows_time(k)
+    step_s = t_fixed + t_rows * total_rows / k
+    what = ("whole step" if k == total_rows else
+            f"{k} of {total_rows} attention rows scaled to the step") + \
+        f", tree encoding and {accept} acceptance whole"
+    oracle.set_threads(0)
+    return 1.0 / step_s, what
+
+
+def cpu_baseline(case, budget_s=8.0):
+    """The oracle on the headline workload: all host cores (OpenMP over
+    independent rows, the arithmetic unchanged) and one core."""
+    cores = os.cpu_count() or 1
+    v_all, what_all = oracle_rate(case, "greedy", budget_s, cores)
+    v_one, what_one = oracle_rate(case, "greedy", budget_s, 1)
+    return {"value": v_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{what_all} ({cores} threads); one thread: {v_one:.3g} steps/s "
+                      f"({what_one}); CPU: {cpu_model()}",
+            "single_thread": {"value": v_one, "cores": 1}, "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank, world):
@@ -866,6 +957,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     oracle.build()
+    oracle.set_threads(0)   # every host core (independent rows in parallel)
+    cores = os.cpu_count() or 1
     case = gen.config2()
     rng = np.random.default_rng(1)
     # size the per-step sample so the whole run takes about 90 s
@@ -890,8 +983,9 @@ def run_reference(args, rank, world):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample_per_step": f"{rows} of {case.N * case.Hq} "
                        f"attention rows + {g_rows} greedy rows, scaled to whole steps"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{rows} attention rows per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{rows} attention rows per step, {cores} threads; "
+                                       f"CPU: {cpu_model()}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     return line
@@ -971,7 +1065,8 @@ def main():
         import torch
         import speculative_decoding_tree_tv_gb300 as tv
         line["other_configs"] = measure_other_configs(
-            torch, tv, torch.device("cuda", local_rank), hbm, tflops)
+            torch, tv, torch.device("cuda", local_rank), hbm, tflops,
+            0.0 if args.no_cpu_baseline else 4.0)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case)
     print(json.dumps(line), flush=True)

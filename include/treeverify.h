@@ -275,6 +275,27 @@ tv_status tv_accept_greedy(const float* logits, const int32_t* tokens, const int
                            size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * tv_debug_set_wait_limit -- test hook for failure detection (the pages have
+ * no counterpart).  Every wait of a kernel in this library is bounded: when
+ * its limit (about a second of SM clock) runs out, the kernel stops waiting,
+ * reports TV_ERR_TIMEOUT in status[b] and leaves with no copy in flight.
+ * This call sets, for the current device, the limit of one such wait -- the
+ * wait of tv_accept_greedy's CTAs for their logit chunks -- so that a test
+ * can make it run out without a fault or a hang:
+ *   cycles >= 1                 limit in SM cycles;
+ *   cycles == 0                 a single non-blocking test of the copies
+ *                               (a call then reports TV_ERR_TIMEOUT, since
+ *                               its copies have only just been issued);
+ *   cycles == TV_WAIT_LIMIT_DEFAULT  restores the regular limit.
+ * The second wait that keeps copies from outliving a CTA keeps the regular
+ * limit.  Host call, synchronous with respect to the device's default
+ * stream; it must not overlap a tv_accept_greedy call on the device.
+ * Returns TV_ERR_INVALID_ARG for other negative values.
+ */
+#define TV_WAIT_LIMIT_DEFAULT (-1LL)
+tv_status tv_debug_set_wait_limit(long long cycles);
+
+/*
  * tv_accept_greedy_noalloc -- tv_accept_greedy without a workspace.
  * The method description has no counterpart for this call: it exists for
  * callers that cannot allocate device memory where they run acceptance (a

@@ -8,7 +8,8 @@ no CPU path.  Import fails loudly when the compiled library is missing.
 """
 from ._lib import (  # noqa: F401
     TV_OK, TV_ERR_INVALID_ARG, TV_ERR_INVALID_TREE, TV_ERR_UNSUPPORTED, TV_ERR_CUDA,
-    TV_ERR_TIMEOUT, TV_ERR_INVALID_TOKEN, TV_ERR_WORKSPACE, TV_MAX_NODES, TVError,
+    TV_ERR_TIMEOUT, TV_ERR_INVALID_TOKEN, TV_ERR_WORKSPACE, TV_MAX_NODES, TV_WAIT_LIMIT_DEFAULT,
+    TVError,
     lib, library_path, status_string, version,
 )
 from .api import (  # noqa: F401

@@ -15,6 +15,7 @@ TV_ERR_TIMEOUT = 5
 TV_ERR_INVALID_TOKEN = 6
 TV_ERR_WORKSPACE = 7
 TV_MAX_NODES = 512
+TV_WAIT_LIMIT_DEFAULT = -1
 
 
 class TVError(RuntimeError):
@@ -63,6 +64,7 @@ _SIGS = {
     "tv_expand_gated": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tv_expand_topn": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tv_select_topn": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "tv_debug_set_wait_limit": (_I, [ctypes.c_longlong]),
 }
 
 for _name, (_res, _args) in _SIGS.items():

@@ -1058,6 +1058,7 @@ extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv
                                     int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,
                                     float* lse, int32_t* status, void* workspace, size_t ws_bytes,
                                     cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_attn_verify");
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Lcap < N) return TV_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return TV_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return TV_ERR_UNSUPPORTED;

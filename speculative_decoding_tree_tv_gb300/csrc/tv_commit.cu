@@ -80,6 +80,7 @@ extern "C" tv_status tv_commit_path(tv_bf16* k, tv_bf16* v, const int32_t* kv_le
                                     const int32_t* path, const int32_t* accept_len, int B, int N,
                                     int Hkv, int D, int Lcap, int32_t* new_kv_len,
                                     int32_t* status, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_commit_path");
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hkv < 1 || Lcap < 1) return TV_ERR_INVALID_ARG;
   if (D < 8 || D % 8 != 0 || D > 1024) return TV_ERR_UNSUPPORTED;
   if (B == 0) return TV_OK;

@@ -10,6 +10,7 @@
 #include <utility>
 
 #include "treeverify.h"
+#include "tv_nvtx.h"
 
 #define TV_CHECK_LAUNCH()                                   \
   do {                                                      \

@@ -932,6 +932,7 @@ extern "C" tv_status tv_expand_gated(const float* draft_logits, const int32_t* f
                                      int topk, float alpha, int budget, int32_t* tree_parent,
                                      int32_t* tree_token, float* tree_logscore, int32_t* n_nodes,
                                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_expand_gated");
   if (F < 0 || V < 1 || layer < 1 || budget < 1) return TV_ERR_INVALID_ARG;
   if (budget > tv::kMaxBudget || F > tv::kMaxBudget) return TV_ERR_UNSUPPORTED;
   if (layer == 1 && (F != 1 || topk < 1)) return TV_ERR_INVALID_ARG;
@@ -954,6 +955,7 @@ extern "C" tv_status tv_expand_topn(const float* draft_logits, const int32_t* fr
                                     int capacity, int32_t* tree_parent, int32_t* tree_token,
                                     float* tree_logscore, int32_t* n_nodes, void* workspace,
                                     size_t ws_bytes, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_expand_topn");
   if (F < 0 || V < 1 || width < 1 || capacity < 1) return TV_ERR_INVALID_ARG;
   if (width > tv::kMaxBudget || F > tv::kMaxBudget) return TV_ERR_UNSUPPORTED;
   if (F == 0) return TV_OK;

@@ -74,6 +74,7 @@ expected_kernel(const int32_t* __restrict__ parent, const float* __restrict__ pr
 extern "C" tv_status tv_expected_accept(const int32_t* parent, const float* prob, int B, int N,
                                         float* score, float* expected, int32_t* status,
                                         cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_expected_accept");
   if (B < 0 || N < 1 || N > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
   if (B == 0) return TV_OK;
   if (!parent || !prob || !expected || !status) return TV_ERR_INVALID_ARG;

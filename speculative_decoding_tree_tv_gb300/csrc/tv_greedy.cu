@@ -29,6 +29,12 @@ namespace tv {
 namespace {
 
 constexpr int kGreedyThreads = 256;
+
+// Reporting limit (SM cycles) of the waits for a CTA's chunk copies: the
+// regular bound unless a test has shortened it (tv_debug_set_wait_limit).
+// The second wait that keeps copies from outliving the CTA always takes the
+// regular bound.
+__constant__ long long c_copy_wait_limit = sm100::kWaitLimitCycles;
 constexpr int kGreedyCtasPerSm = 4;  // resident CTAs per SM assumed when sizing chunks
 constexpr int kScanNodesPerThread = (kMaxNodes + kGreedyThreads - 1) / kGreedyThreads;
 
@@ -435,7 +441,7 @@ greedy_bulk_kernel(const GreedyArgs g) {
   for (int q = 0; q < kGreedyPieces; ++q) {
     const int q0 = q * per, qn = min(per, n - q0);
     if (qn <= 0) break;
-    if (!sm100::mbar_wait(&s_bar[q], 0)) {
+    if (!sm100::mbar_wait_for(&s_bar[q], 0, c_copy_wait_limit)) {
       ok = false;  // every copy of this CTA is waited for again (bounded) below
       continue;
     }
@@ -556,6 +562,7 @@ extern "C" tv_status tv_accept_greedy(const float* logits, const int32_t* tokens
                                       int32_t* end_node, int32_t* path, int32_t* bonus,
                                       int32_t* status, void* workspace, size_t ws_bytes,
                                       cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_accept_greedy");
   const tv_status st = tv::check_greedy_args(logits, tokens, parent, depth, B, N, V, argmax,
                                              accept_len, end_node, path, bonus, status);
   if (st != TV_OK || B == 0) return st;
@@ -613,6 +620,7 @@ extern "C" tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t
                                               int N, int V, int32_t* argmax, int32_t* accept_len,
                                               int32_t* end_node, int32_t* path, int32_t* bonus,
                                               int32_t* status, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_accept_greedy_noalloc");
   const tv_status st = tv::check_greedy_args(logits, tokens, parent, depth, B, N, V, argmax,
                                              accept_len, end_node, path, bonus, status);
   if (st != TV_OK || B == 0) return st;
@@ -663,4 +671,17 @@ extern "C" tv_status tv_accept_greedy_noalloc(const float* logits, const int32_t
   g.ws.keys = reinterpret_cast<unsigned long long*>(b8);
   g.ws.arrivals = reinterpret_cast<unsigned int*>(b8 + tv::kStaticKeyBytes);
   return tv::launch_greedy(g, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Test hook: the reporting limit of tv_accept_greedy's chunk-copy waits on the
+// current device (see the header).
+extern "C" tv_status tv_debug_set_wait_limit(long long cycles) {
+  if (cycles < 0 && cycles != TV_WAIT_LIMIT_DEFAULT) return TV_ERR_INVALID_ARG;
+  const long long v = (cycles == TV_WAIT_LIMIT_DEFAULT) ? tv::sm100::kWaitLimitCycles : cycles;
+  if (cudaMemcpyToSymbol(tv::c_copy_wait_limit, &v, sizeof(v)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TV_ERR_CUDA;
+  }
+  return TV_OK;
 }

@@ -607,6 +607,7 @@ extern "C" tv_status tv_accept_sample(const float* p_logits, const float* q_logi
                                       int32_t* accept_len, int32_t* end_node, int32_t* path,
                                       int32_t* out_token, int32_t* status, void* workspace,
                                       size_t ws_bytes, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_accept_sample");
   (void)workspace;
   (void)ws_bytes;
   if (B < 0 || N < 1 || N > TV_MAX_NODES || V < 1) return TV_ERR_INVALID_ARG;

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "treeverify.h"
+#include "tv_nvtx.h"
 
 namespace {
 
@@ -38,6 +39,7 @@ extern "C" tv_status tv_build_spine_tree(const int32_t* spine_tokens, int S,
                                          const int32_t* branch_tokens, int Sb, int K,
                                          int root_token, int budget, float spine_ratio,
                                          int32_t* parent, int32_t* tokens, int32_t* n_nodes) {
+  TV_NVTX_RANGE("tv_build_spine_tree");
   if (S < 0 || Sb < 0 || K < 0 || budget < 1 || !parent || !tokens || !n_nodes)
     return TV_ERR_INVALID_ARG;
   if (!(spine_ratio >= 0.0f && spine_ratio <= 1.0f)) return TV_ERR_INVALID_ARG;

@@ -236,6 +236,7 @@ extern "C" tv_status tv_select_topn(const int32_t* parent, const int32_t* token,
                                     int n, int32_t* out_parent, int32_t* out_token,
                                     float* out_logscore, int32_t* out_src, float* expected,
                                     int32_t* status, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_select_topn");
   if (B < 0 || M < 1 || n < 1) return TV_ERR_INVALID_ARG;
   if (M > tv::kTopnMaxNodes) return TV_ERR_UNSUPPORTED;
   if (B == 0) return TV_OK;

@@ -75,6 +75,7 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
 
 extern "C" tv_status tv_tree_build(const int32_t* parent, int B, int N, int32_t* depth,
                                    uint64_t* anc_mask, int32_t* status, cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_tree_build");
   if (B < 0 || N < 1 || N > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
   if (B == 0) return TV_OK;
   if (!parent || !depth || !anc_mask || !status) return TV_ERR_INVALID_ARG;

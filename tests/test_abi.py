@@ -173,3 +173,8 @@ def test_attention_plan_override(tvlib, monkeypatch):
         tvlib.attn_plan(0, 60, 32, 8, 128, 2108)
     with pytest.raises(tvlib.TVError):
         tvlib.attn_plan(1, 60, 32, 8, 96, 2108)
+
+
+def test_wait_limit_hook_rejects_bad_values(tvlib):
+    """Other negative limits are refused on the host, before any device access."""
+    assert tvlib.lib.tv_debug_set_wait_limit(-5) == tvlib.TV_ERR_INVALID_ARG
