@@ -2,9 +2,10 @@
 """Tree-verify step throughput on GB300.
 
 One step = one pass of the verify hot path over one synthetic draft tree:
-tv_tree_build -> tv_attn_verify (one attention layer over the KV prefix plus
-the tree) -> tv_accept_greedy (argmax over every node's vocabulary row and
-the longest matching branch).  Workload: Llama-3-8B-shaped GOOSE spine tree
+the tree encoding and one attention layer over the KV prefix plus the tree
+(tv_attn_verify_tree: tv_tree_build and tv_attn_verify in one launch for
+trees of up to 64 nodes) -> tv_accept_greedy (argmax over every node's
+vocabulary row and the longest matching branch).  Workload: Llama-3-8B-shaped GOOSE spine tree
 (batch 1, KV prefix 2048, 32 query / 8 KV heads, head_dim 128, 60 nodes,
 vocab 128256).
 
@@ -56,9 +57,14 @@ def parse_args():
     p.add_argument("--ncu-steps", type=int, default=0,
                    help="profiling driver: run this many eager steps of the workload on "
                         "one input set (no graphs, no timing) and exit; for ncu captures")
-    p.add_argument("--ncu-workload", choices=["verify", "opt_tree"], default="verify",
-                   help="what --ncu-steps runs: the verify step, or one OPT-Tree growth "
-                        "(16 layers of width 256 over vocab 128256, then the selection)")
+    p.add_argument("--ncu-workload", default="verify",
+                   choices=["verify", "opt_tree", "talon_verify", "long_context", "batched_small",
+                            "talon_expand"],
+                   help="what --ncu-steps runs: the verify step (Llama-3-8B spine), one OPT-Tree "
+                        "growth (16 layers of width 256 over vocab 128256, then the selection), "
+                        "the TALON verify step (512 nodes, 64/8 heads, prefix 4096), the "
+                        "long-context step (256 nodes, prefix 32768), the batched stochastic "
+                        "step on its first 4 sequences, or one TALON growth (vocab 32000)")
     return p.parse_args()
 
 
@@ -77,6 +83,7 @@ def dist_env():
 KERNEL_SOURCES = {
     "tv_tree_build": ["tv_tree.cu", "tv_common.cuh"],
     "tv_attn_verify": ["tv_attn.cu", "tv_sm100.cuh", "tv_common.cuh"],
+    "tv_attn_verify_tree": ["tv_attn.cu", "tv_sm100.cuh", "tv_common.cuh"],
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
@@ -345,9 +352,14 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
                              outs=aouts)
         cur[0] += advance
 
+    def f_attn_tree(advance=True):
+        x = s_()
+        tv.attn_verify_tree(x["q"], x["k"], x["v"], x["kv_len"], x["parent"], out=out, lse=lse,
+                            status=ast, depth=depth, anc_mask=anc, tree_status=tst)
+        cur[0] += advance
+
     def f_step():
-        f_tree(False)
-        f_attn(False)
+        f_attn_tree(False)
         f_acc(False)
         cur[0] += 1
 
@@ -358,7 +370,8 @@ def measure_verify_config(name, case, accept, torch, tv, device, stream, hbm, tf
     assert int(tst.max()) == 0 and int(ast.max()) == 0 and int(aouts["status"].max()) == 0
     glen = M * max(1, -(-20 // M))
     us = {k: graph_time_us(torch, stream, f, glen, 5)
-          for k, f in (("step", f_step), ("tv_tree_build", f_tree), ("tv_attn_verify", f_attn),
+          for k, f in (("step", f_step), ("tv_attn_verify_tree", f_attn_tree),
+                       ("tv_tree_build", f_tree), ("tv_attn_verify", f_attn),
                        ("tv_accept_" + accept, f_acc))}
     commit = measure_commit(torch, tv, stream, t["k"], t["v"], t["kv_len"], aouts["path"],
                             aouts["accept_len"], hbm)
@@ -629,6 +642,46 @@ def run_ncu_steps(args):
     from workloads import gen
 
     device = torch.device("cuda", 0)
+    if args.ncu_workload in ("talon_verify", "long_context", "batched_small"):
+        if args.ncu_workload == "talon_verify":
+            d = gen.config3_drafter(0)
+            tree = tv.expand_tree(d.rows, d.root_key(), d.child_key, 10, 0.3, 512, device)
+            case = gen.config3_verify(tree["parent"].numpy().astype(np.int32), 0,
+                                      tokens=tree["token"].numpy().astype(np.int32))
+            accept = "greedy"
+        elif args.ncu_workload == "long_context":
+            case, accept = gen.config5(256), "greedy"
+        else:
+            case, accept = gen.config4(B=4), "sample"
+        t = {"parent": torch.from_numpy(case.parent).to(device),
+             "tokens": torch.from_numpy(case.tokens).to(device),
+             "kv_len": torch.from_numpy(case.kv_len).to(device)}
+        for k in ("q", "k", "v"):
+            t[k] = torch.from_numpy(np.ascontiguousarray(getattr(case, k)).view(np.int16)).to(
+                device).view(torch.bfloat16)
+        for k in ("logits", "p_logits", "q_logits"):
+            if getattr(case, k) is not None:
+                t[k] = torch.from_numpy(getattr(case, k)).to(device)
+        for _ in range(args.ncu_steps):
+            out, lse, astat, depth, anc, tstat = tv.attn_verify_tree(
+                t["q"], t["k"], t["v"], t["kv_len"], t["parent"])
+            if accept == "greedy":
+                res = tv.accept_greedy(t["logits"], t["tokens"], t["parent"], depth)
+            else:
+                res = tv.accept_sample(t["p_logits"], t["q_logits"], t["tokens"], t["parent"],
+                                       depth, 1.0, 1234, 0)
+        torch.cuda.synchronize()
+        assert int(tstat.max()) == 0 and int(astat.max()) == 0 and int(res["status"].max()) == 0
+        print(json.dumps({"ncu_steps": args.ncu_steps, "workload": args.ncu_workload}), flush=True)
+        return
+    if args.ncu_workload == "talon_expand":
+        d = gen.config3_drafter(0)
+        for _ in range(args.ncu_steps):
+            tree = tv.expand_tree(d.rows, d.root_key(), d.child_key, 10, 0.3, 512, device)
+        torch.cuda.synchronize()
+        assert tree["n"] == 512
+        print(json.dumps({"ncu_steps": args.ncu_steps, "workload": args.ncu_workload}), flush=True)
+        return
     if args.ncu_workload == "opt_tree":
         f_build, _, st = opt_tree_setup(torch, tv, device)
         for _ in range(args.ncu_steps):
@@ -640,8 +693,8 @@ def run_ncu_steps(args):
     case = gen.config2()
     s = make_sets(case, torch, device, 0)[0][0]
     for _ in range(args.ncu_steps):
-        depth, anc, tstat = tv.tree_build(s["parent"])
-        out, lse, astat = tv.attn_verify(s["q"], s["k"], s["v"], s["kv_len"], anc)
+        out, lse, astat, depth, anc, tstat = tv.attn_verify_tree(
+            s["q"], s["k"], s["v"], s["kv_len"], s["parent"])
         res = tv.accept_greedy(s["logits"], s["tokens"], s["parent"], depth)
     torch.cuda.synchronize()
     assert int(tstat[0]) == 0 and int(astat[0]) == 0 and int(res["status"][0]) == 0
@@ -685,12 +738,15 @@ def run_ours(args, rank, world, local_rank):
     def k_attn(s):
         tv.attn_verify(s["q"], s["k"], s["v"], s["kv_len"], anc, out=out, lse=lse, status=astat)
 
+    def k_attn_tree(s):
+        tv.attn_verify_tree(s["q"], s["k"], s["v"], s["kv_len"], s["parent"], out=out, lse=lse,
+                            status=astat, depth=depth, anc_mask=anc, tree_status=tstat)
+
     def k_greedy(s):
         tv.accept_greedy(s["logits"], s["tokens"], s["parent"], depth, outs=gouts)
 
     def step(s):
-        k_tree(s)
-        k_attn(s)
+        k_attn_tree(s)
         k_greedy(s)
 
     stream = torch.cuda.Stream(device)
@@ -757,8 +813,8 @@ def run_ours(args, rank, world, local_rank):
     # per-kernel average launch time, each kernel replayed alone over the same rotation
     per_kernel = {}
     nk = min(args.steps, 20000)
-    for name, fn in (("tv_tree_build", k_tree), ("tv_attn_verify", k_attn),
-                     ("tv_accept_greedy", k_greedy)):
+    for name, fn in (("tv_attn_verify_tree", k_attn_tree), ("tv_accept_greedy", k_greedy),
+                     ("tv_tree_build", k_tree), ("tv_attn_verify", k_attn)):
         g = capture(fn, C)
         with torch.cuda.stream(stream):
             g.replay()
@@ -776,9 +832,11 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = measure_e2e(args, torch, tv, case, sets, step, gouts, stream, device)
 
-    # tree, attention (+ its split-KV merge when the plan splits), greedy
-    launches = 3 + int(tv.attn_workspace_size(case.B, case.N, case.Hq, case.Hkv, case.D,
-                                               case.Lcap) > 0)
+    # tree encoding and attention (one launch up to 64 nodes; + the split-KV
+    # merge when the plan splits), greedy
+    launches = (2 + int(case.N > 64) +
+                int(tv.attn_workspace_size(case.B, case.N, case.Hq, case.Hkv, case.D,
+                                           case.Lcap) > 0))
     return dict(case=case, elapsed_ms=elapsed_ms, per_kernel=per_kernel, clocks=clocks, M=M,
                 set_bytes=set_bytes, l2=l2, e2e=e2e, launches_per_step=launches)
 
@@ -1017,6 +1075,7 @@ def main():
     pk = r["per_kernel"]
     g_us = pk["tv_accept_greedy"]
     a_us = pk["tv_attn_verify"]
+    at_us = pk["tv_attn_verify_tree"]
     greedy_gbs = nbytes["greedy"] / (g_us * 1e-6) / 1e9
     attn_gbs = nbytes["attn"] / (a_us * 1e-6) / 1e9
     t_roof_us = sum(max(nbytes[k] / (hbm * 1e9), (flops if k == "attn" else 0) / (tflops * 1e12))
@@ -1024,12 +1083,15 @@ def main():
     # roofline of the dominant entry point (largest measured time per launch).
     # Attention: its algorithmic bytes take longer at the HBM peak than its
     # flops at the bf16 tensor peak, so it is HBM-bound too.
-    key = {"tv_tree_build": "tree", "tv_attn_verify": "attn", "tv_accept_greedy": "greedy"}
-    dom = max(pk, key=lambda k: pk[k])
-    dom_gbs = nbytes[key[dom]] / (pk[dom] * 1e-6) / 1e9
+    # the step's two entry points: the fused tree encoding + attention, and greedy
+    step_bytes_of = {"tv_attn_verify_tree": nbytes["attn"] + nbytes["tree"],
+                     "tv_accept_greedy": nbytes["greedy"]}
+    key = {"tv_attn_verify_tree": "attn", "tv_accept_greedy": "greedy"}
+    dom = max(step_bytes_of, key=lambda k: pk[k])
+    dom_gbs = step_bytes_of[dom] / (pk[dom] * 1e-6) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": dom_gbs / hbm, "traffic": ncu_traffic(dom),
-                "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": nbytes[key[dom]],
+                "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": step_bytes_of[dom],
                 "us_per_launch": pk[dom]}
 
     line = {
@@ -1059,6 +1121,13 @@ def main():
          "hbm_frac": greedy_gbs / hbm, "traffic": ncu_traffic("tv_accept_greedy")})
     line["kernels"]["tv_tree_build"].update({"algorithmic_bytes": nbytes["tree"],
                                              "traffic": ncu_traffic("tv_tree_build")})
+    at_bytes = nbytes["attn"] + nbytes["tree"]
+    line["kernels"]["tv_attn_verify_tree"].update(
+        {"algorithmic_bytes": at_bytes, "flops": flops,
+         "achieved_gbs": at_bytes / (at_us * 1e-6) / 1e9,
+         "hbm_frac": at_bytes / (at_us * 1e-6) / 1e9 / hbm,
+         "traffic": ncu_traffic("tv_attn_verify_tree"),
+         "note": "the step's tree encoding and attention in one launch (plus the split merge)"})
     if r["e2e"] is not None:
         line["e2e"] = r["e2e"]
     if world == 1 and not args.no_configs:

@@ -247,6 +247,33 @@ tv_status tv_build_spine_tree(const int32_t* spine_tokens, int S, const int32_t*
 float tv_spine_ratio_update(float ratio, float observed_accept_rate, float beta);
 
 /*
+ * tv_attn_verify_tree -- tv_tree_build and tv_attn_verify in one call (OPT-Tree
+ * §2: the tree attention mask is derived from the draft tree; the same single
+ * target pass verifies every node).  For trees of up to 64 nodes it is one
+ * launch: every attention CTA builds the ancestor masks of its sequence in
+ * shared memory from parent[], and the first CTA of each sequence also writes
+ * depth, anc_mask and tree_status exactly as tv_tree_build would (an invalid
+ * tree: depth -1, empty masks, TV_ERR_INVALID_TREE; the attention then runs
+ * on those empty masks, as the two calls would).  Larger trees take the two
+ * launches.  A model with several attention layers calls this for its first
+ * layer of a step and tv_attn_verify with the returned masks for the others.
+ *   parent       int32 [B, N]        in   as for tv_tree_build.
+ *   q, k, v, kv_len, B, N, Hq, Hkv, D, Lcap, scale, out, lse, status,
+ *   workspace, ws_bytes              as for tv_attn_verify (same workspace size).
+ *   depth        int32 [B, N]        out  as tv_tree_build's depth.
+ *   anc_mask     uint64 [B, N, W]    out  as tv_tree_build's masks.
+ *   tree_status  int32 [B]           out  as tv_tree_build's status.
+ * Outputs are identical, bit for bit, to tv_tree_build followed by
+ * tv_attn_verify.  Errors as for those calls.
+ */
+tv_status tv_attn_verify_tree(const int32_t* parent, const tv_bf16* q, const tv_bf16* k,
+                              const tv_bf16* v, const int32_t* kv_len, int B, int N, int Hq,
+                              int Hkv, int D, int Lcap, float scale, tv_bf16* out, float* lse,
+                              int32_t* status, int32_t* depth, uint64_t* anc_mask,
+                              int32_t* tree_status, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
  * tv_accept_greedy -- greedy acceptance over a verified tree.
  * (OPT-Tree §2: under greedy sampling the longest branch matching the target
  * model's highest-probability sequence is accepted; GOOSE §2C: unified greedy

@@ -13,7 +13,7 @@ from ._lib import (  # noqa: F401
     lib, library_path, status_string, version,
 )
 from .api import (  # noqa: F401
-    tree_build, attn_verify, accept_greedy, accept_sample, expand_gated, expand_tree, expand_topn, select_topn, grow_opt_tree, opt_tree_layer_sizes, commit_path, expected_accept, build_spine_tree, spine_ratio_update,
+    tree_build, attn_verify, attn_verify_tree, accept_greedy, accept_sample, expand_gated, expand_tree, expand_topn, select_topn, grow_opt_tree, opt_tree_layer_sizes, commit_path, expected_accept, build_spine_tree, spine_ratio_update,
     workspace, attn_workspace_size, attn_plan, greedy_workspace_size, sample_workspace_size,
     expand_workspace_size,
 )

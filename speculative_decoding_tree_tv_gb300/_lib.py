@@ -65,6 +65,8 @@ _SIGS = {
     "tv_expand_topn": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tv_select_topn": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "tv_debug_set_wait_limit": (_I, [ctypes.c_longlong]),
+    "tv_attn_verify_tree": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
+                                 _P, _P, _SZ, _P]),
 }
 
 for _name, (_res, _args) in _SIGS.items():

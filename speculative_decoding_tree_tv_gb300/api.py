@@ -129,6 +129,49 @@ def attn_verify(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_len: torch
     return out, lse, status
 
 
+def attn_verify_tree(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_len: torch.Tensor,
+                     parent: torch.Tensor, scale: float = 0.0, out=None, lse=None, status=None,
+                     depth=None, anc_mask=None, tree_status=None, want_lse: bool = True,
+                     ws: Optional[torch.Tensor] = None):
+    """Tree encoding and tree-verify attention in one call (one launch for
+    trees of up to 64 nodes).  parent int32 [B,N]; q, k, v, kv_len as for
+    attn_verify.  Returns (out, lse, status, depth, anc_mask, tree_status)."""
+    _need(q, "q", torch.bfloat16)
+    B, N, Hq, D = q.shape
+    dev = q.device
+    _need(k, "k", torch.bfloat16, device=dev)
+    _, Hkv, Lcap, Dk = k.shape
+    if k.shape[0] != B or Dk != D:
+        raise ValueError("k must be [B, Hkv, Lcap, D]")
+    _need(v, "v", torch.bfloat16, tuple(k.shape), dev)
+    _need(kv_len, "kv_len", torch.int32, (B,), dev)
+    _need(parent, "parent", torch.int32, (B, N), dev)
+    W = (N + 63) // 64
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if want_lse and lse is None:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, N, Hq), dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev) if status is None else status
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev) if depth is None else depth
+    anc_mask = (torch.empty((B, N, W), dtype=torch.int64, device=dev)
+                if anc_mask is None else anc_mask)
+    tree_status = torch.empty(B, dtype=torch.int32, device=dev) if tree_status is None else tree_status
+    _need(status, "status", torch.int32, (B,), dev)
+    _need(depth, "depth", torch.int32, (B, N), dev)
+    _need(anc_mask, "anc_mask", torch.int64, (B, N, W), dev)
+    _need(tree_status, "tree_status", torch.int32, (B,), dev)
+    need = attn_workspace_size(B, N, Hq, Hkv, D, Lcap)
+    ws = workspace("attn", need, dev) if ws is None else ws
+    check("tv_attn_verify_tree", lib.tv_attn_verify_tree(
+        parent.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), kv_len.data_ptr(), B, N,
+        Hq, Hkv, D, Lcap, float(scale), out.data_ptr(), _ptr(lse), status.data_ptr(),
+        depth.data_ptr(), anc_mask.data_ptr(), tree_status.data_ptr(), ws.data_ptr(), ws.numel(),
+        _stream(dev)))
+    return out, lse, status, depth, anc_mask, tree_status
+
+
 def accept_greedy(logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tensor,
                   depth: torch.Tensor, outs: Optional[dict] = None,
                   ws: Optional[torch.Tensor] = None) -> dict:

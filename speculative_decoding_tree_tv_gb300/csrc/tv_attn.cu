@@ -81,6 +81,14 @@ struct Shape {
 };
 
 struct AttnParams {
+  // tree encoding in the same launch (trees of up to 64 nodes): the parent
+  // array in; depth, ancestor masks and tree status out (written by the first
+  // CTA of each sequence); each CTA keeps the masks it needs in shared memory
+  const int32_t* parent;
+  int32_t* depth_out;
+  uint64_t* anc_out;
+  int32_t* tree_status;
+  int fuse_tree;
   const uint16_t* k;  // caches, for the L2 prefetch of a split's first tiles
   const uint16_t* v;
   uint16_t* out;
@@ -152,8 +160,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 // 32 bits of the ancestor bit-string starting at bit `pos` (0 <= pos < 64*W).
 __device__ __forceinline__ uint32_t anc_bits32(const uint64_t* anc, int W, int pos) {
   const int wi = pos >> 6, sh = pos & 63;
-  const uint64_t lo = __ldg(anc + wi);
-  const uint64_t hi = (sh != 0 && wi + 1 < W) ? __ldg(anc + wi + 1) : 0ull;
+  const uint64_t lo = anc[wi];  // global (from tv_tree_build) or shared (built in this launch)
+  const uint64_t hi = (sh != 0 && wi + 1 < W) ? anc[wi + 1] : 0ull;
   return (uint32_t)((lo >> sh) | (sh ? (hi << (64 - sh)) : 0ull));
 }
 
@@ -171,6 +179,79 @@ __device__ __forceinline__ uint32_t visibility32(int c, int j0, int L, int keys,
   const int x = lo - pre;   // tree index of column lo
   if (x + 32 > 0 && x < N) tm = (x >= 0) ? anc_bits32(anc, W, x) : (anc_bits32(anc, W, 0) << (-x));
   return (pm | tm) & em;
+}
+
+constexpr int kFusedTreeMax = 64;  // nodes a fused tree encoding handles (one mask word)
+
+// Node j's value from a tree held by a warp (node i in lane i % 32, slot i / 32).
+__device__ __forceinline__ int gather_i(const int (&v)[2], int j) {
+  const int lo = __shfl_sync(0xffffffffu, v[0], j & 31);
+  const int hi = __shfl_sync(0xffffffffu, v[1], j & 31);
+  return j < 32 ? lo : hi;
+}
+__device__ __forceinline__ uint64_t gather_u64(const uint64_t (&v)[2], int j) {
+  const uint64_t lo = __shfl_sync(0xffffffffu, v[0], j & 31);
+  const uint64_t hi = __shfl_sync(0xffffffffu, v[1], j & 31);
+  return j < 32 ? lo : hi;
+}
+
+// Tree encoding of sequence b by one warp (N <= 64; OPT-Tree §2: a node
+// attends to its ancestors and itself): depth and ancestor-or-self masks by
+// pointer jumping -- after round r a node's mask holds itself and its 2^(r+1)
+// - 1 nearest ancestors, and its depth counts the edges jumped.  An invalid
+// parent array (parent[0] != -1, or parent[i] outside [0, i)) gives depth -1
+// and empty masks, as tv_tree_build does.  The masks go to shared memory; the
+// first CTA of the sequence also writes the outputs of tv_tree_build.
+__device__ void tree_in_warp(const AttnParams& p, int b, uint64_t* s_anc, bool write_out) {
+  const int lane = threadIdx.x & 31, N = p.N;
+  const int32_t* par_g = p.parent + (size_t)b * N;
+  int par[2], jmp[2], dep[2];
+  uint64_t anc[2];
+  int bad = 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    par[s] = i < N ? par_g[i] : -1;
+    if (i < N) bad |= (i == 0) ? (par[s] != -1) : (par[s] < 0 || par[s] >= i);
+    anc[s] = i < N ? (1ull << i) : 0ull;
+    jmp[s] = par[s];
+    dep[s] = (i < N && par[s] >= 0) ? 1 : 0;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (!bad) {
+#pragma unroll
+    for (int r = 0; r < 6; ++r) {
+      int nj[2], nd[2];
+      uint64_t na[2];
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int j = jmp[s], jj = max(j, 0);
+        const int dj = gather_i(dep, jj), jjmp = gather_i(jmp, jj);
+        const uint64_t aj = gather_u64(anc, jj);
+        nd[s] = j >= 0 ? dep[s] + dj : dep[s];
+        na[s] = j >= 0 ? (anc[s] | aj) : anc[s];
+        nj[s] = j >= 0 ? jjmp : -1;
+      }
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        dep[s] = nd[s];
+        anc[s] = na[s];
+        jmp[s] = nj[s];
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    if (i >= N) continue;
+    const uint64_t a = bad ? 0ull : anc[s];
+    s_anc[i] = a;
+    if (write_out) {
+      p.depth_out[(size_t)b * N + i] = bad ? -1 : dep[s];
+      p.anc_out[(size_t)b * N + i] = a;
+    }
+  }
+  if (write_out && lane == 0) p.tree_status[b] = bad ? TV_ERR_INVALID_TREE : TV_OK;
 }
 
 template <int D, int RBS>
@@ -206,6 +287,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __shared__ __align__(8) uint64_t bar_o_done[2][kPBufs];  // PV(t) of a row block, per P buffer
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ uint64_t s_anc[kFusedTreeMax];     // masks built in this launch
+  __shared__ __align__(8) uint64_t bar_tree;    // they are ready
 
   // Barriers, TMEM and descriptor prefetches need nothing from the previous
   // kernel, so they are set up before waiting for it.
@@ -245,6 +328,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       mbar_init(&bar_v_empty[st], 1);
     }
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_tree, 32);
     for (int r = 0; r < 2; ++r) {
       for (int u = 0; u < kSBufs; ++u) {
         mbar_init(&bar_s_full[r][u], 1);
@@ -266,6 +350,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int r = 0; r < nrb; ++r)
 #pragma unroll
         for (int a = 0; a < A; ++a) tma_prefetch_l2_3d(&tmQ, a * 64, kvh * G, b * N + node0 + r * nb);
+      if (p.fuse_tree)  // the parent row, 256 bytes at most: every line it touches
+        for (int i = 0; i < N; i += 32) line_prefetch_l2(p.parent + (size_t)b * N + i);
       const int rows = min(min(t_end - t_begin, kPrefetchTiles) * kBN, p.Lcap - t_begin * kBN);
       if (rows > 0) {
         bulk_prefetch_l2(p.k + (size_t)y0 * D, (uint32_t)rows * D * 2u);
@@ -308,6 +394,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+
+  // fused tree encoding: the V producer warp builds the masks before its own
+  // work (the first V tiles were issued during setup), in the CTAs whose key
+  // range reaches the tree's own slots and in the first CTA of the sequence,
+  // which writes the encoding out; softmax warps wait for the masks before the
+  // first tile that needs them
+  const bool writes_tree = split == 0 && mt == 0 && kvh == 0;
+  if (p.fuse_tree && warp == kVProducerWarp && (writes_tree || t_end * kBN > L)) {
+    tree_in_warp(p, b, s_anc, writes_tree);
+    mbar_arrive(&bar_tree);  // every lane: its shared-memory writes are released
+  }
 
   if (L < 0 || L + N > p.Lcap) {  // uniform over the CTA; the merge kernel skips it too
     if (split == 0 && valid_row) {
@@ -513,16 +610,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     __syncwarp();
   } else if (T > 0 && act) {
     // ------------------------------------------------------------- softmax
-    const uint64_t* anc = p.anc + ((size_t)b * N + (valid_row ? node : 0)) * p.W;
+    const uint64_t* anc = p.fuse_tree ? s_anc + (valid_row ? node : 0)
+                                      : p.anc + ((size_t)b * N + (valid_row ? node : 0)) * p.W;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS0 = tmem + 128 * (rb * kSBufs), tO = tmem + kOCol + 128 * rb;
     const float sc = p.scale_log2;
     uint8_t* const prow0 = sP + rb * kPBufs * 2 * kAtomBytes + row * 128;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    bool tree_ready = !p.fuse_tree;  // masks built in this launch: awaited when first needed
+    for (int t = 0; ok && t < T; ++t) {
       uint8_t* const prow = prow0 + (t % kPBufs) * 2 * kAtomBytes;
       // the mask words (their ancestor loads) are ready before S is
       const int j0 = (t_begin + t) * kBN;
+      if (!tree_ready && j0 + kBN > L) {  // this tile reaches the tree's own key slots
+        ok = warp_wait(&bar_tree, 0);
+        if (!ok) break;
+        tree_ready = true;
+      }
       uint32_t vis[4] = {0u, 0u, 0u, 0u};
       if (valid_row) {
         if (j0 + kBN <= L) {  // all prefix keys
@@ -955,11 +1059,20 @@ cudaError_t launch_grids(const SplitPlan& sp, int BH, cudaStream_t stream, const
                     stream, p);
 }
 
+// Tree encoding done in the attention launch (nullptr parent: masks given).
+struct FusedTree {
+  const int32_t* parent = nullptr;
+  int32_t* depth = nullptr;
+  uint64_t* anc_mask = nullptr;
+  int32_t* status = nullptr;
+};
+
 template <int D>
 tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, const int32_t* kv_len,
                       const uint64_t* anc_mask, int B, int N, int Hq, int Hkv, int Lcap,
                       float scale_log2, tv_bf16* out, float* lse, int32_t* status,
-                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                      void* workspace, size_t ws_bytes, cudaStream_t stream,
+                      const FusedTree& ft = FusedTree()) {
   const SplitPlan sp = plan_splits(B, N, Hq, Hkv, Lcap, D);
   const size_t need = plan_workspace(sp, D);
   if (need > 0 && (workspace == nullptr || ws_bytes < need ||
@@ -996,6 +1109,11 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
       return TV_ERR_INVALID_ARG;
   }
   AttnParams p;
+  p.parent = ft.parent;
+  p.depth_out = ft.depth;
+  p.anc_out = ft.anc_mask;
+  p.tree_status = ft.status;
+  p.fuse_tree = ft.parent != nullptr;
   p.k = reinterpret_cast<const uint16_t*>(k);
   p.v = reinterpret_cast<const uint16_t*>(v);
   p.out = out;
@@ -1053,30 +1171,83 @@ extern "C" tv_status tv_attn_plan(int B, int N, int Hq, int Hkv, int D, int Lcap
   return TV_OK;
 }
 
-extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
-                                    const int32_t* kv_len, const uint64_t* anc_mask, int B, int N,
-                                    int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,
-                                    float* lse, int32_t* status, void* workspace, size_t ws_bytes,
-                                    cudaStream_t stream) {
-  TV_NVTX_RANGE("tv_attn_verify");
+namespace tv {
+namespace {
+
+// Host-side checks shared by both attention entry points.
+tv_status check_attn_args(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
+                          const int32_t* kv_len, const void* mask_or_parent, int B, int N, int Hq,
+                          int Hkv, int D, int Lcap, float scale, const tv_bf16* out) {
   if (B < 0 || N < 1 || N > TV_MAX_NODES || Hq < 1 || Hkv < 1 || Lcap < N) return TV_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return TV_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return TV_ERR_UNSUPPORTED;
-  if (Hq / Hkv > tv::kRB) return TV_ERR_UNSUPPORTED;
+  if (Hq / Hkv > kRB) return TV_ERR_UNSUPPORTED;
   if (!(scale >= 0.0f) || !isfinite(scale)) return TV_ERR_INVALID_ARG;
   if (B == 0) return TV_OK;
-  if (!q || !k || !v || !kv_len || !anc_mask || !out) return TV_ERR_INVALID_ARG;
+  if (!q || !k || !v || !kv_len || !mask_or_parent || !out) return TV_ERR_INVALID_ARG;
   if ((long long)B * Hkv > 65535 || (long long)B * Hkv * Lcap > 0x7fffffffll ||
       (long long)B * N > 0x7fffffffll)
     return TV_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
     return TV_ERR_INVALID_ARG;
+  return TV_OK;
+}
+
+tv_status attn_dispatch(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
+                        const int32_t* kv_len, const uint64_t* anc_mask, int B, int N, int Hq,
+                        int Hkv, int D, int Lcap, float scale, tv_bf16* out, float* lse,
+                        int32_t* status, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                        const FusedTree& ft) {
   const float sc = (scale == 0.0f) ? 1.0f / sqrtf((float)D) : scale;
   const float scale_log2 = sc * 1.4426950408889634f;
   if (D == 128)
-    return tv::launch_attn<128>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out,
-                                lse, status, workspace, ws_bytes, stream);
-  return tv::launch_attn<64>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out, lse,
-                             status, workspace, ws_bytes, stream);
+    return launch_attn<128>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out,
+                            lse, status, workspace, ws_bytes, stream, ft);
+  return launch_attn<64>(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, Lcap, scale_log2, out, lse,
+                         status, workspace, ws_bytes, stream, ft);
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" tv_status tv_attn_verify(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v,
+                                    const int32_t* kv_len, const uint64_t* anc_mask, int B, int N,
+                                    int Hq, int Hkv, int D, int Lcap, float scale, tv_bf16* out,
+                                    float* lse, int32_t* status, void* workspace, size_t ws_bytes,
+                                    cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_attn_verify");
+  const tv_status st =
+      tv::check_attn_args(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, D, Lcap, scale, out);
+  if (st != TV_OK || B == 0) return st;
+  return tv::attn_dispatch(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, D, Lcap, scale, out, lse,
+                           status, workspace, ws_bytes, stream, tv::FusedTree());
+}
+
+extern "C" tv_status tv_attn_verify_tree(const int32_t* parent, const tv_bf16* q,
+                                         const tv_bf16* k, const tv_bf16* v,
+                                         const int32_t* kv_len, int B, int N, int Hq, int Hkv,
+                                         int D, int Lcap, float scale, tv_bf16* out, float* lse,
+                                         int32_t* status, int32_t* depth, uint64_t* anc_mask,
+                                         int32_t* tree_status, void* workspace, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  TV_NVTX_RANGE("tv_attn_verify_tree");
+  const tv_status st =
+      tv::check_attn_args(q, k, v, kv_len, parent, B, N, Hq, Hkv, D, Lcap, scale, out);
+  if (st != TV_OK || B == 0) return st;
+  if (!depth || !anc_mask || !tree_status) return TV_ERR_INVALID_ARG;
+  if (N > tv::kFusedTreeMax) {
+    // masks of more than one word: the tree encoding runs as its own launch
+    const tv_status ts = tv_tree_build(parent, B, N, depth, anc_mask, tree_status, stream);
+    if (ts != TV_OK) return ts;
+    return tv::attn_dispatch(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, D, Lcap, scale, out, lse,
+                             status, workspace, ws_bytes, stream, tv::FusedTree());
+  }
+  tv::FusedTree ft;
+  ft.parent = parent;
+  ft.depth = depth;
+  ft.anc_mask = anc_mask;
+  ft.status = tree_status;
+  return tv::attn_dispatch(q, k, v, kv_len, anc_mask, B, N, Hq, Hkv, D, Lcap, scale, out, lse,
+                           status, workspace, ws_bytes, stream, ft);
 }

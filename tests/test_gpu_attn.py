@@ -279,3 +279,51 @@ def test_bad_kv_len_in_a_split_plan(tv, oracle_mod):
     rows = np.array([(0, n, h) for n in range(0, 40, 3) for h in range(8)], np.int64)
     ref, ref_lse = oracle_mod.attn_rows(case.q, case.k, case.v, good, case.parent, 8, 2, rows)
     check_attn(out[rows[:, 0], rows[:, 1], rows[:, 2]], ref, "split-bad-kv")
+
+
+@pytest.mark.parametrize("seed,B,N,L,Hq,Hkv,D,tree,plan", [
+    (61, 1, 60, 2048, 32, 8, 128, "spine60", None),   # the Llama-3-8B spine step (split plan)
+    (62, 3, 64, (10, 700), 16, 4, 64, "random", None),
+    (63, 2, 33, 300, 8, 8, 128, "chain", "256,1"),
+    (64, 1, 1, 0, 8, 2, 64, "chain", None),
+    (65, 2, 50, 900, 32, 8, 128, "random", "128,4"),
+    (66, 1, 100, 500, 8, 2, 64, "random", None),       # more than 64 nodes: two launches
+])
+def test_attn_verify_tree_equals_two_calls(tv, oracle_mod, monkeypatch, seed, B, N, L, Hq, Hkv,
+                                           D, tree, plan):
+    """tv_attn_verify_tree (the tree encoding inside the attention launch for
+    trees of up to 64 nodes) gives, bit for bit, what tv_tree_build followed by
+    tv_attn_verify gives, and matches the oracle."""
+    if plan:
+        monkeypatch.setenv("TV_ATTN_PLAN", plan)
+    case = gen.make_case(seed, B=B, N=N, L=L, Hq=Hq, Hkv=Hkv, D=D, V=64, tree=tree, max_depth=12)
+    t = case_tensors(case)
+    depth, anc, tst = tv.tree_build(t["parent"])
+    out, lse, ast = tv.attn_verify(t["q"], t["k"], t["v"], t["kv_len"], anc)
+    f_out, f_lse, f_ast, f_depth, f_anc, f_tst = tv.attn_verify_tree(
+        t["q"], t["k"], t["v"], t["kv_len"], t["parent"])
+    torch.cuda.synchronize()
+    for a, b_, what in ((out.view(torch.int16), f_out.view(torch.int16), "out"),
+                        (lse.view(torch.int32), f_lse.view(torch.int32), "lse"),
+                        (ast, f_ast, "status"), (depth, f_depth, "depth"), (anc, f_anc, "anc"),
+                        (tst, f_tst, "tree_status")):
+        assert torch.equal(a, b_), what
+    ref, ref_lse = oracle_mod.attn_all(case.q, case.k, case.v, case.kv_len, case.parent, Hq, Hkv)
+    check_attn(bf16_np(f_out), ref, f"fused-{seed}")
+
+
+def test_attn_verify_tree_invalid_tree(tv):
+    """An invalid parent array: the fused call reports it in tree_status with
+    depth -1 and empty masks, exactly as tv_tree_build does, and the attention
+    runs on the empty masks as the two calls would."""
+    case = gen.make_case(67, B=3, N=20, L=100, Hq=8, Hkv=2, D=64, V=64)
+    case.parent[1, 7] = 9          # a parent after its child
+    case.parent[2, 0] = 0          # the root has a parent
+    t = case_tensors(case)
+    depth, anc, tst = tv.tree_build(t["parent"])
+    out, lse, ast = tv.attn_verify(t["q"], t["k"], t["v"], t["kv_len"], anc)
+    f = tv.attn_verify_tree(t["q"], t["k"], t["v"], t["kv_len"], t["parent"])
+    torch.cuda.synchronize()
+    assert np_(f[5]).tolist() == np_(tst).tolist() == [0, 2, 2]
+    assert torch.equal(f[3], depth) and torch.equal(f[4], anc)
+    assert torch.equal(f[0].view(torch.int16), out.view(torch.int16))
