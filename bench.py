@@ -87,13 +87,12 @@ KERNEL_SOURCES = {
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
-    # attention kernel, cold (9,195,776) + merge kernel with L2 warm (0 + 182,528)
-    "tv_attn_verify": {"sha256": "dbd6627dce2abf7cdcf06e7cc1c9b0b85b260f72ab74a9162024d9a1bfcd3d88", "bytes": 9378304,
-                       "profile": "profiles/attn_verify_llama3-8b-spine60.md"},
-    "tv_accept_greedy": {"sha256": "624f793724aaac0ace61a78a01391f4a39ee0c207ce3906766cd1c7f20a62fb9", "bytes": 30822400,
+    # attention kernel with the tree encoding, cold (9,197,568) + merge kernel
+    # with the L2 as the step leaves it (256 + 157,952)
+    "tv_attn_verify_tree": {"sha256": "648a782d497f5d8c26520c05e310b38642211e085af19811bfecfb2b623df94a", "bytes": 9355776,
+                            "profile": "profiles/attn_verify_tree_llama3-8b-spine60.md"},
+    "tv_accept_greedy": {"sha256": "8367fbf90e4e120a720f62ebc2fd67a39c5153f39aa0d5153fe1f70d4d703de1", "bytes": 30827776,
                          "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},
-    "tv_tree_build": {"sha256": "7525175311d2e607c52b62e3cebfc56ca5e70ff278fa81af761f2aad43ad32ea", "bytes": 6656,
-                      "profile": "profiles/tree_build_kernel_llama3-8b-spine60.md"},
 }
 
 
@@ -634,7 +633,7 @@ def measure_other_configs(torch, tv, device, hbm, tflops, oracle_budget_s=0.0):
 # our implementation
 # ----------------------------------------------------------------------------
 def run_ncu_steps(args):
-    """K eager steps (tree -> attention -> greedy) on one input set, for ncu:
+    """K eager steps (tree encoding + attention, then acceptance) on one input set, for ncu:
     each launch is a separate, serialised kernel there, so the per-launch
     counters of the same kernels as in the timed run can be read."""
     import torch
