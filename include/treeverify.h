@@ -323,6 +323,38 @@ tv_status tv_accept_greedy(const float* logits, const int32_t* tokens, const int
 tv_status tv_debug_set_wait_limit(long long cycles);
 
 /*
+ * Bounds-checked build (the pages have no counterpart; a debugging aid).
+ * libtreeverify_checked.so is this library compiled with TV_CHECKED defined:
+ * the same entry points, in which every index a kernel computes from its
+ * inputs or its launch geometry is checked before the access it guards.  A
+ * failed check skips that access (no trap, no fault) and records its site in
+ * a device word of its source unit; results are then unspecified, but every
+ * access stays inside the caller's buffers.
+ *
+ * tv_checked_build      1 in the checked build, 0 in the regular one.
+ * tv_debug_check_take   synchronises the current device, then writes to
+ *                       *site the first failed check recorded since the
+ *                       previous call, as (unit << 16) | source line, or 0
+ *                       (always 0 in the regular build), and clears the
+ *                       record.  Units: 1 tree, 2 greedy, 3 sample,
+ *                       4 expand, 5 attention, 6 commit, 7 expected,
+ *                       8 top-n selection, 9 library.  Host call; it must not
+ *                       overlap a launch of this library on the device.
+ *                       TV_ERR_INVALID_ARG if site is NULL, TV_ERR_CUDA if
+ *                       the device reports an error.
+ * tv_debug_check_selftest  test of the mechanism itself: writes buf[i] = i for
+ *                       i < n, each store guarded by the check
+ *                       0 <= i < logical_n.  buf: device int32 [n], caller-
+ *                       owned.  The regular build writes all n entries; the
+ *                       checked build writes the first min(n, logical_n) and,
+ *                       if n > logical_n, records a failed check (unit 9).
+ *                       Every store lies inside buf either way.
+ */
+int tv_checked_build(void);
+tv_status tv_debug_check_take(int32_t* site);
+tv_status tv_debug_check_selftest(int32_t* buf, int n, int logical_n, cudaStream_t stream);
+
+/*
  * tv_accept_greedy_noalloc -- tv_accept_greedy without a workspace.
  * The method description has no counterpart for this call: it exists for
  * callers that cannot allocate device memory where they run acceptance (a

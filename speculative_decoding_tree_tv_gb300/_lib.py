@@ -4,7 +4,12 @@ from __future__ import annotations
 import ctypes
 import os
 
-from ._build import LIB_PATH
+from ._build import CHECKED_LIB_PATH, LIB_PATH
+
+# TV_CHECKED=1 in the environment loads the bounds-checked build instead (same
+# entry points; a failed index check is recorded, see tv_debug_check_take).
+CHECKED = os.environ.get("TV_CHECKED", "0") not in ("", "0")
+_PATH = CHECKED_LIB_PATH if CHECKED else LIB_PATH
 
 TV_OK = 0
 TV_ERR_INVALID_ARG = 1
@@ -25,16 +30,16 @@ class TVError(RuntimeError):
 
 
 def library_path() -> str:
-    return LIB_PATH
+    return _PATH
 
 
-if not os.path.exists(LIB_PATH):
+if not os.path.exists(_PATH):
     raise ImportError(
-        f"libtreeverify.so not found at {LIB_PATH}; build it first "
+        f"{os.path.basename(_PATH)} not found at {_PATH}; build it first "
         "(python -c 'import __graft_entry__ as g; g.build()' or "
         "python speculative_decoding_tree_tv_gb300/_build.py)")
 
-lib = ctypes.CDLL(LIB_PATH)
+lib = ctypes.CDLL(_PATH)
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -65,6 +70,9 @@ _SIGS = {
     "tv_expand_topn": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tv_select_topn": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "tv_debug_set_wait_limit": (_I, [ctypes.c_longlong]),
+    "tv_checked_build": (_I, []),
+    "tv_debug_check_take": (_I, [_P]),
+    "tv_debug_check_selftest": (_I, [_P, _I, _I, _P]),
     "tv_attn_verify_tree": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
                                  _P, _P, _SZ, _P]),
 }
@@ -86,3 +94,13 @@ def version() -> int:
 def check(fn: str, code: int) -> None:
     if code != TV_OK:
         raise TVError(fn, code)
+
+
+def check_take() -> int:
+    """The first failed index check since the last call (checked build), as
+    (source unit << 16) | line, or 0; clears it.  Synchronises the device."""
+    site = ctypes.c_int32(0)
+    rc = lib.tv_debug_check_take(ctypes.byref(site))
+    if rc != TV_OK:
+        raise TVError("tv_debug_check_take", rc)
+    return int(site.value)

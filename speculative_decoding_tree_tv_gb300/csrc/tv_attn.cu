@@ -26,6 +26,7 @@
 // partial rows to the workspace with one bulk copy, with (max, sum) pairs
 // beside them, and a merge kernel chained by programmatic dependent launch
 // combines the partials of every row.  Every wait is bounded.
+#define TV_UNIT 5
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cstdio>
@@ -102,6 +103,7 @@ struct AttnParams {
   int nb;           // nodes per row block: floor(128 / G)
   int mtiles;       // CTAs along the node axis: ceil(N / (row blocks x nb))
   int nsplit;       // splits of the key range
+  int units;        // (sequence, kv head, node tile) units: B x Hkv x mtiles
   float scale_log2;
 };
 
@@ -159,7 +161,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 
 // 32 bits of the ancestor bit-string starting at bit `pos` (0 <= pos < 64*W).
 __device__ __forceinline__ uint32_t anc_bits32(const uint64_t* anc, int W, int pos) {
-  const int wi = pos >> 6, sh = pos & 63;
+  const int wi = TV_IN(pos >> 6, W) ? pos >> 6 : 0, sh = pos & 63;
   const uint64_t lo = anc[wi];  // global (from tv_tree_build) or shared (built in this launch)
   const uint64_t hi = (sh != 0 && wi + 1 < W) ? anc[wi + 1] : 0ull;
   return (uint32_t)((lo >> sh) | (sh ? (hi << (64 - sh)) : 0ull));
@@ -305,8 +307,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int nodel = row / G;
   const int node = node0 + rb * nb + nodel;
   const bool act = is_softmax && rb < nrb;       // warp-uniform
-  const bool valid_row = act && nodel < nb && node < N;
   const int h = kvh * G + row % G;
+  const bool valid_row = act && nodel < nb && node < N && TV_CHECK(h < p.Hq && bh < p.units);
 
   // Split ranges come from the cache capacity, so the first tile's loads can
   // be issued before kv_len arrives; tiles past the key range are dropped.
@@ -778,8 +780,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
     const int crow = rb * kRB + row;  // row of the CTA
     const size_t slot = unit * p.nsplit + split;
-    if (split_kv) p.part_ml[slot * Sh::kRows + crow] = make_float2(m_run, l_run);
-    if (T > 0) {
+    const bool slot_ok = !split_kv || TV_CHECK(unit < (size_t)p.units && split < p.nsplit);
+    if (split_kv && slot_ok) p.part_ml[slot * Sh::kRows + crow] = make_float2(m_run, l_run);
+    if (T > 0 && slot_ok) {
       uint32_t o[D / 32][32];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + lane_base + 32 * c, o[c]);  // warp-wide
@@ -846,6 +849,7 @@ attn_merge_kernel(const AttnParams p) {
   pdl_wait();  // the partials come from the attention kernel
   const int unit = blockIdx.x / kCtaPerUnit;
   const int sub = blockIdx.x % kCtaPerUnit;
+  if (!TV_IN(unit, p.units)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cl = warp % kMergeChunks, g = warp / kMergeChunks;
   const int crow = (sub % (kRows / kMergeRows)) * kMergeRows + lane;
@@ -908,6 +912,7 @@ attn_merge_kernel(const AttnParams p) {
   const int node = mt * RBS * p.nb + rbk * p.nb + nodel;
   if (nodel >= p.nb || node >= p.N) return;
   const int h = kvh * p.G + rl % p.G;
+  if (!TV_IN(h, p.Hq)) return;
   float Mt = -INFINITY;
 #pragma unroll
   for (int q = 0; q < kMergeGroups; ++q) Mt = fmaxf(Mt, s_m[q][cl][lane]);
@@ -1138,6 +1143,7 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.nb = sp.nb;
   p.mtiles = sp.mtiles;
   p.nsplit = sp.nsplit;
+  p.units = B * Hkv * sp.mtiles;
   p.scale_log2 = scale_log2;
   const cudaError_t e = sp.rbs == 2 ? launch_grids<D, 2>(sp, B * Hkv, stream, tmQ, tmK, tmV, p)
                                      : launch_grids<D, 1>(sp, B * Hkv, stream, tmQ, tmK, tmV, p);

@@ -10,6 +10,7 @@
 // sources (16-byte chunks, coalesced along the row) before any thread writes
 // a destination, and every later batch reads only slots past this batch's
 // destinations, so the copy is exact in place.
+#define TV_UNIT 6
 #include "tv_common.cuh"
 
 namespace tv {
@@ -29,7 +30,7 @@ commit_kernel(uint4* __restrict__ k, uint4* __restrict__ v, const int32_t* __res
   const int b = blockIdx.x / Hkv, h = blockIdx.x % Hkv;
   const int tid = threadIdx.x;
   const int L = __ldg(kv_len + b), a = __ldg(accept_len + b);
-  int bad = !(L >= 0 && a >= 0 && a < N);
+  int bad = !(L >= 0 && a >= 0 && a < N && TV_CHECK(N <= kMaxNodes));
   if (!bad)
     for (int d = tid; d <= a; d += kCommitThreads) {
       const int p = __ldg(path + (size_t)b * N + d);
@@ -57,7 +58,8 @@ commit_kernel(uint4* __restrict__ k, uint4* __restrict__ v, const int32_t* __res
       const int w = tid + u * kCommitThreads;
       if (w < items) {
         const int d = d0 + w / per_row, t = (w / C) & 1, c = w % C;
-        if (s_path[d] != d) buf[u] = (t ? v : k)[(base + s_path[d]) * C + c];
+        if (s_path[d] != d && TV_CHECK(s_path[d] > 0 && L + s_path[d] < Lcap))
+          buf[u] = (t ? v : k)[(base + s_path[d]) * C + c];
       }
     }
     __syncthreads();  // every source of the batch is read before any destination is written
@@ -66,7 +68,7 @@ commit_kernel(uint4* __restrict__ k, uint4* __restrict__ v, const int32_t* __res
       const int w = tid + u * kCommitThreads;
       if (w < items) {
         const int d = d0 + w / per_row, t = (w / C) & 1, c = w % C;
-        if (s_path[d] != d) (t ? v : k)[(base + d) * C + c] = buf[u];
+        if (s_path[d] != d && TV_CHECK(L + d < Lcap)) (t ? v : k)[(base + d) * C + c] = buf[u];
       }
     }
     __syncthreads();

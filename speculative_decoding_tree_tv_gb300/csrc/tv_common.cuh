@@ -20,7 +20,53 @@
     }                                                       \
   } while (0)
 
+// Bounds-checked builds.  Compiled with -DTV_CHECKED, every index a kernel
+// computes from its inputs or its launch geometry is checked before the
+// access it guards: a failed check skips that access and records the first
+// failing site of the translation unit, (TV_UNIT << 16) | line, in a device
+// word that tv_debug_check_take() reads and clears.  No check traps.  In the
+// regular build TV_CHECK(cond) is the constant true and the guarded access is
+// unconditional.  Each source file defines TV_UNIT (its number in
+// treeverify.h) before including this header.
+#ifndef TV_UNIT
+#define TV_UNIT 0
+#endif
+
 namespace tv {
+
+// the host-side reader of one translation unit's check word (checked builds):
+// returns the recorded site (0: none) and clears it, or -1 on a CUDA error
+using CheckReader = int (*)();
+void register_check_reader(CheckReader reader);
+
+#ifdef TV_CHECKED
+namespace {
+__device__ int g_check_site;
+int take_check_site() {
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_check_site, sizeof v) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_check_site, &zero, sizeof zero) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return v;
+}
+struct CheckRegistrar {
+  CheckRegistrar() { register_check_reader(&take_check_site); }
+};
+const CheckRegistrar g_check_registrar;
+}  // namespace
+__device__ __forceinline__ bool check_site(bool ok, int line) {
+  if (!ok) atomicCAS(&g_check_site, 0, (TV_UNIT << 16) | line);
+  return ok;
+}
+#define TV_CHECK(cond) (::tv::check_site(static_cast<bool>(cond), __LINE__))
+#else
+#define TV_CHECK(cond) true
+#endif
+// 0 <= i < n
+#define TV_IN(i, n) TV_CHECK((i) >= 0 && (i) < (n))
 
 constexpr int kMaxNodes = TV_MAX_NODES;
 constexpr int kMaxWords = (kMaxNodes + 63) / 64;

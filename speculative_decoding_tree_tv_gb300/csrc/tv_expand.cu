@@ -10,7 +10,10 @@
 //
 // Three launches (four for OPT-Tree layers), all on the caller's stream:
 //   1. stats:   per (frontier row, 2048-logit chunk) max and sum exp, one warp
-//               per chunk and eight chunks per CTA; warp 0 of the last CTA of
+//               per chunk and eight chunks per CTA; each lane also lists the
+//               largest of the 64 logits it read (value and token) and the
+//               chunk records a bound u over everything else (the largest
+//               lane's second largest); warp 0 of the last CTA of
 //               a row to finish forms the row's log-normaliser lse_v and
 //               offset off_v = logscore_v - lse_v (log s of token c in row v
 //               is off_v + logit) and raises the layer's anchor (the best
@@ -20,17 +23,19 @@
 //               maxima: they are distinct candidates, so the layer's
 //               limit-th best scores at least that much, and it is close to
 //               the cut;
-//   2. filter:  each CTA loads four chunks of a row, turns the fp64 gate (if
+//   2. filter:  each CTA takes four chunks of a row, turns the fp64 gate (if
 //               any) and the layer's floor into an fp32 logit threshold for
-//               the row, and (after one block vote, when any value passes)
-//               appends the (row, token) candidates that pass, with their
-//               order-preserving fp64 score keys (at most the layer's limit
-//               per chunk, its best ones).  A chunk holding more than `limit`
-//               candidates raises the floor to its limit-th best key: the
-//               layer's limit-th best is at least that, so chunks that run
-//               later skip everything below it.  The filter visits the
-//               (row, chunk) pairs in the reverse of the stats order, so that
-//               it starts on what the stats pass read last (still in L2);
+//               the row, and appends the (row, token) candidates that pass,
+//               with their order-preserving fp64 score keys (at most the
+//               layer's limit per chunk, its best ones).  It reads the logits
+//               again only for a chunk whose bound u is at or above the
+//               threshold; otherwise the chunk's maximum (no candidate) or its
+//               lane-maximum list (every candidate) decides, so the rows
+//               stream from memory once per layer when few candidates share a
+//               chunk, the usual case above an OPT-Tree floor.  A chunk holding
+//               more than `limit` candidates raises the floor to its limit-th
+//               best key: the layer's limit-th best is at least that, so
+//               chunks that run later skip everything below it;
 //   3. select:  one CTA keeps the best `limit` candidates (up to 2048 of them
 //               by two bitonic sorts in shared memory; beyond that a radix
 //               select on the score keys, starting at the first byte in which
@@ -39,6 +44,7 @@
 //               tree and returns the control words (candidate count, anchor,
 //               floor) to zero for the next call.
 // Scores are fp64 in the log domain; logits stay fp32.
+#define TV_UNIT 4
 #include <algorithm>
 #include <climits>
 
@@ -60,7 +66,13 @@ constexpr int kSelStageKeys = 16384;  // candidates whose keys the select stages
 struct ExpPartial {
   double s;  // sum of exp(x - m) over the chunk
   float m;   // the chunk's largest logit
-  float pad;
+  float u;   // every logit of the chunk outside its lane-maximum list is <= u
+};
+// One entry of a chunk's lane-maximum list: the largest logit of the 64 a
+// lane of the stats warp read, and its token (-1: the lane read nothing).
+struct ExpCand {
+  float v;
+  int t;
 };
 struct ExpRow {
   double off;  // logscore_v - lse_v
@@ -81,6 +93,7 @@ struct ExpWs {
   unsigned int* arrivals;  // [kMaxBudget] chunks of each row done by the stats pass (returned to 0)
   ExpRow* rows;
   ExpPartial* part;
+  ExpCand* cand;             // [row][chunk][32] lane maxima of each chunk
   unsigned long long* list;  // (row << 32) | token
   unsigned long long* keys;  // order-preserving fp64 score key of list[i]
 };
@@ -91,13 +104,16 @@ struct ExpWs {
 // regions after them move with F and are written before they are read.
 __host__ __device__ inline size_t exp_arrivals_offset() { return align_up(sizeof(ExpCtl), 256); }
 __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, size_t* part_off,
-                                              size_t* list_off, size_t* keys_off) {
+                                              size_t* cand_off, size_t* list_off,
+                                              size_t* keys_off) {
   const int chunks = (V + kExpChunk - 1) / kExpChunk;
   size_t o = exp_arrivals_offset() + align_up((size_t)kMaxBudget * sizeof(unsigned int), 256);
   *rows_off = o;
   o += align_up((size_t)F * sizeof(ExpRow), 256);
   *part_off = o;
   o += align_up((size_t)F * chunks * sizeof(ExpPartial), 256);
+  *cand_off = o;
+  o += align_up((size_t)F * chunks * 32 * sizeof(ExpCand), 256);
   *list_off = o;
   o += align_up((size_t)F * V * sizeof(unsigned long long), 256);
   *keys_off = o;
@@ -161,10 +177,27 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
         a[u] = (e < stop) ? __ldg(x + e) : -INFINITY;
       }
     }
-    float m = -INFINITY;
+    // the lane's largest logit (first of its ties) and second largest (a tie
+    // with the largest counts): everything the lane read but did not list is
+    // <= its second largest
+    float v1 = -INFINITY, v2 = -INFINITY;
+    int u1 = -1;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) m = fmaxf(m, a[u]);
-    m = warp_max(m);
+    for (int u = 0; u < kPer; ++u) {
+      if (a[u] > v1) {
+        v2 = v1;
+        v1 = a[u];
+        u1 = u;
+      } else {
+        v2 = fmaxf(v2, a[u]);
+      }
+    }
+    const int t1 = (u1 < 0) ? -1
+                   : ((V & 3) == 0) ? start + 4 * (lane + 32 * (u1 >> 2)) + (u1 & 3)
+                                    : start + lane + 32 * u1;
+    ws.cand[((size_t)row * chunks + c) * 32 + lane] = ExpCand{v1, t1};
+    const float ub = warp_max(v2);
+    const float m = warp_max(v1);
     const float ml = m * kLog2e;
     float sl = 0.0f;
 #pragma unroll
@@ -172,7 +205,7 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
       sl += (a[u] == -INFINITY) ? 0.0f : ex2_approx(fmaf(a[u], kLog2e, -ml));
     const double sd = warp_sum_d((double)sl);
     if (lane == 0) {
-      part[(size_t)row * chunks + c] = ExpPartial{sd, m, 0.0f};
+      part[(size_t)row * chunks + c] = ExpPartial{sd, m, ub};
       __threadfence();  // the partial is visible before the CTA arrives
     }
   }
@@ -180,7 +213,8 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
   if (threadIdx.x == 0) {
     const unsigned int mine = (unsigned int)min(kStatsWarps, chunks - (int)blockIdx.x * kStatsWarps);
     // the last arrival (acquire) sees every partial of the row
-    s_last = (arrive_acq_rel(&ws.arrivals[row], mine) + mine == (unsigned int)chunks);
+    s_last = TV_IN(row, kMaxBudget) &&
+             (arrive_acq_rel(&ws.arrivals[row], mine) + mine == (unsigned int)chunks);
   }
   __syncthreads();
   if (!s_last || warp != 0) return;
@@ -249,7 +283,7 @@ exp_floor_kernel(const float* __restrict__ logits, int V, int F, int chunks, int
   const bool all = F * chunks < limit;
   const int per_row = all ? V : chunks;
   const int total = F * per_row;
-  if (limit == 0 || total < limit) return;
+  if (limit == 0 || total < limit || !TV_CHECK(F <= kMaxBudget)) return;
   const double anchor = key_double(ws.ctl->anchor);
   for (int i = tid; i < kFloorBins; i += kFloorThreads) s_hist[i] = 0u;
   for (int r = tid; r < F; r += kFloorThreads) s_av[r] = (float)(anchor - ws.rows[r].off);
@@ -308,16 +342,20 @@ __device__ __forceinline__ int filt_elem(bool vec, int tid, int j) {
   return vec ? 4 * (tid + kExpThreads * (j >> 2)) + (j & 3) : tid + kExpThreads * j;
 }
 
-// One CTA per (frontier row, kFiltChunks chunks of the row); the loads of all
-// its chunks are issued before anything else.  Per chunk, the candidates
-// (logit >= the row's threshold) are gathered in shared memory with their
-// score keys.  When there are more than the layer may keep (`limit`), only the
-// chunk's best `limit` under the output's total order (score desc, then token
-// asc within a row) are appended: the layer's best `limit` overall are among
-// them, and the select kernel then sees at most chunks x limit candidates per
-// row.  gated: TALON's alpha gate against the anchor (limit = the remaining
-// budget); otherwise every child is a candidate and limit = min(cap,
-// remaining).
+// One CTA per (frontier row, kFiltChunks chunks of the row).  Thread 0 turns
+// the fp64 gate (if any) and the layer's floor into an fp32 logit threshold
+// for the row.  Per chunk, the candidates (logit >= the threshold) are
+// gathered in shared memory with their score keys, from one of three places:
+// none if the chunk's maximum is below the threshold (most chunks); the
+// chunk's lane-maximum list if the threshold lies above the chunk's bound u
+// (every logit outside the list is <= u, so the list holds every candidate);
+// else the chunk itself, read again.  When there are more candidates than
+// the layer may keep (`limit`), only the chunk's best `limit` under the
+// output's total order (score desc, then token asc within a row) are
+// appended: the layer's best `limit` overall are among them, and the select
+// kernel then sees at most chunks x limit candidates per row.  gated: TALON's
+// alpha gate against the anchor (limit = the remaining budget); otherwise
+// every child is a candidate and limit = min(cap, remaining).
 __global__ void __launch_bounds__(kExpThreads)
 exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, int budget,
                   double log_alpha, const int32_t* __restrict__ n_nodes, ExpWs ws) {
@@ -339,32 +377,6 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* x = logits + (size_t)row * V;
   const bool vec = (V & 3) == 0;
-  // the group's logits, all loads in flight before the threshold is known
-  float a[kFiltChunks][kFiltPer];
-#pragma unroll
-  for (int cc = 0; cc < kFiltChunks; ++cc) {
-    const int start = (c0 + cc) * kExpChunk;
-    const int stop = (cc < nc) ? min(V, start + kExpChunk) : start;
-    if (vec) {
-      const float4* x4 = reinterpret_cast<const float4*>(x);
-#pragma unroll
-      for (int u = 0; u < kFiltPer / 4; ++u) {
-        const int e = start + 4 * (tid + kExpThreads * u);
-        const float4 f = (e < stop) ? __ldg(x4 + (e >> 2))
-                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        a[cc][4 * u + 0] = f.x;
-        a[cc][4 * u + 1] = f.y;
-        a[cc][4 * u + 2] = f.z;
-        a[cc][4 * u + 3] = f.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kFiltPer; ++j) {
-        const int e = start + tid + kExpThreads * j;
-        a[cc][j] = (e < stop) ? __ldg(x + e) : -INFINITY;
-      }
-    }
-  }
   const double off = ws.rows[row].off;
   if (tid == 0) {
     const int n0 = *n_nodes;
@@ -400,24 +412,29 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
   const float thr = s_thr;
   if (!(thr < INFINITY)) return;
   const int limit = s_limit;
-  // most groups hold no candidate at all (above an OPT-Tree floor nearly none
-  // do): one block vote, and they are done
-  int any = 0;
-#pragma unroll
-  for (int cc = 0; cc < kFiltChunks; ++cc) {
-    const int start = (c0 + cc) * kExpChunk;
-    const int stop = (cc < nc) ? min(V, start + kExpChunk) : start;
-#pragma unroll
-    for (int j = 0; j < kFiltPer; ++j)
-      any |= (start + filt_elem(vec, tid, j) < stop) && (a[cc][j] >= thr);
-  }
-  if (!__syncthreads_or(any)) return;
   const unsigned long long row_hi = (unsigned long long)row << 32;
-#pragma unroll
-  for (int cc = 0; cc < kFiltChunks; ++cc) {
-    if (cc >= nc) break;
-    const int start = (c0 + cc) * kExpChunk;
+  // a whole warp offers one value per lane; the passing ones go to the
+  // chunk's candidate list in shared memory
+  auto push = [&](bool pass, float lg, int e) {
+    const unsigned int bal = __ballot_sync(0xffffffffu, pass);
+    if (bal == 0u) return;
+    int slot0 = 0;
+    if (lane == 0) slot0 = atomicAdd(&s_cnt, __popc(bal));
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    if (pass) {
+      const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+      if (TV_IN(slot, kExpChunk)) {
+        s_key[slot] = double_key(off + (double)lg);
+        s_tok[slot] = e;
+      }
+    }
+  };
+  for (int cc = 0; cc < nc; ++cc) {
+    const int c = c0 + cc;
+    const int start = c * kExpChunk;
     const int stop = min(V, start + kExpChunk);
+    const ExpPartial pc = ws.part[(size_t)row * chunks + c];
+    if (pc.m < thr) continue;  // uniform: no candidate in this chunk
     if (tid == 0) {
       s_cnt = 0;
       s_out = 0;
@@ -425,20 +442,38 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
       s_kmax = 0ull;
     }
     __syncthreads();
+    if (thr > pc.u) {
+      // every candidate is some lane's maximum: the list has them all
+      if (warp == 0) {
+        const ExpCand e = ws.cand[((size_t)row * chunks + c) * 32 + lane];
+        push(e.t >= 0 && e.v >= thr && TV_IN(e.t - start, stop - start), e.v, e.t);
+      }
+    } else {
+      // the chunk again, all of a thread's loads in flight at once
+      float a[kFiltPer];
+      if (vec) {
+        const float4* x4 = reinterpret_cast<const float4*>(x);
 #pragma unroll
-    for (int j = 0; j < kFiltPer; ++j) {
-      const float lg = a[cc][j];
-      const int e = start + filt_elem(vec, tid, j);
-      const bool pass = (e < stop) && (lg >= thr);
-      const unsigned int bal = __ballot_sync(0xffffffffu, pass);
-      if (bal == 0u) continue;
-      int slot0 = 0;
-      if (lane == 0) slot0 = atomicAdd(&s_cnt, __popc(bal));
-      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-      if (pass) {
-        const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-        s_key[slot] = double_key(off + (double)lg);
-        s_tok[slot] = e;
+        for (int u = 0; u < kFiltPer / 4; ++u) {
+          const int e = start + 4 * (tid + kExpThreads * u);
+          const float4 f = (e < stop) ? __ldg(x4 + (e >> 2))
+                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          a[4 * u + 0] = f.x;
+          a[4 * u + 1] = f.y;
+          a[4 * u + 2] = f.z;
+          a[4 * u + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kFiltPer; ++j) {
+          const int e = start + tid + kExpThreads * j;
+          a[j] = (e < stop) ? __ldg(x + e) : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kFiltPer; ++j) {
+        const int e = start + filt_elem(vec, tid, j);
+        push((e < stop) && (a[j] >= thr), a[j], e);
       }
     }
     __syncthreads();
@@ -448,6 +483,7 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
       if (tid == 0) s_base = atomicAdd(&ws.ctl->count, n);
       __syncthreads();
       for (int i = tid; i < n; i += kExpThreads) {
+        if (!TV_IN((long long)s_base + i, (long long)gridDim.y * V)) continue;
         ws.list[s_base + i] = row_hi | (unsigned int)s_tok[i];
         ws.keys[s_base + i] = s_key[i];
       }
@@ -524,7 +560,7 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
     if (tid == 0) atomicMax(&ws.ctl->floor, T);
     // ties at T: the `need` lowest tokens, found through a bitmap of the chunk
     for (int i = tid; i < n; i += kExpThreads)
-      if (s_key[i] == T)
+      if (s_key[i] == T && TV_IN(s_tok[i] - start, kExpChunk))
         atomicOr(&s_tiebits[(s_tok[i] - start) >> 5], 1u << ((s_tok[i] - start) & 31));
     if (tid == 0) s_base = atomicAdd(&ws.ctl->count, limit);
     __syncthreads();
@@ -559,6 +595,7 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
       const unsigned long long k = s_key[i];
       if (k > T || (k == T && s_tok[i] <= last_tie)) {
         const int slot = s_base + atomicAdd(&s_out, 1);
+        if (!TV_IN((long long)slot, (long long)gridDim.y * V)) continue;
         ws.list[slot] = row_hi | (unsigned int)s_tok[i];
         ws.keys[slot] = k;
       }
@@ -632,7 +669,8 @@ __device__ void bitonic_sort_u64(unsigned long long* s, int n_pow2) {
 }
 
 __global__ void __launch_bounds__(kSelThreads)
-exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __restrict__ frontier_node,
+exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
+                  const int32_t* __restrict__ frontier_node,
                   int32_t* __restrict__ tree_parent, int32_t* __restrict__ tree_token,
                   float* __restrict__ tree_logscore, int32_t* __restrict__ n_nodes, ExpWs ws) {
   // the per-warp histograms of the radix passes and the kept list are never
@@ -684,6 +722,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     const int n0 = ctl.n0;
     for (int j = tid; j < k; j += kSelThreads) {
       const Kept c = s_kept[j];
+      if (!(TV_IN(c.row, F) && TV_IN(c.token, V) && TV_IN(n0 + j, budget))) continue;
       tree_parent[n0 + j] = frontier_node[c.row];
       tree_token[n0 + j] = c.token;
       tree_logscore[n0 + j] =
@@ -800,7 +839,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     const unsigned long long k = K[j];
     if (k > T) {
       const int slot = atomicAdd(&s_n, 1);
-      s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
+      if (TV_IN(slot, kMaxBudget)) s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
     } else if (k == T) {
       const int slot = atomicAdd(&s_nt, 1);
       if (slot < kTieCap) s_ties[slot] = c;
@@ -816,7 +855,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
     __syncthreads();
     bitonic_sort_u64(s_ties, p2);
     for (int i = tid; i < need; i += kSelThreads)
-      s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
+      if (TV_IN(n_gt + i, kMaxBudget) && TV_IN(i, kTieCap))
+        s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
   } else {
     // very many exact ties: pick them one by one in (row, token) order
     unsigned long long last = 0ull;
@@ -848,6 +888,7 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
   const int n0 = ctl.n0;
   for (int i = tid; i < k; i += kSelThreads) {
     const Kept c = s_kept[i];
+    if (!(TV_IN(c.row, F) && TV_IN(c.token, V) && TV_IN(n0 + i, budget))) continue;
     tree_parent[n0 + i] = frontier_node[c.row];
     tree_token[n0 + i] = c.token;
     tree_logscore[n0 + i] = (float)(ws.rows[c.row].off + (double)__ldg(logits + (size_t)c.row * V + c.token));
@@ -865,8 +906,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, const int32_t* __rest
 
 extern "C" size_t tv_expand_workspace_size(int F, int V) {
   if (F <= 0 || V <= 0) return 256;
-  size_t a, b, c, d;
-  return tv::exp_offsets(F, V, &a, &b, &c, &d);
+  size_t a, b, c, d, e;
+  return tv::exp_offsets(F, V, &a, &b, &c, &d, &e);
 }
 
 namespace tv {
@@ -878,14 +919,15 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
                        double log_alpha, int budget, int32_t* tree_parent, int32_t* tree_token,
                        float* tree_logscore, int32_t* n_nodes, void* workspace,
                        cudaStream_t stream) {
-  size_t rows_off, part_off, list_off, keys_off;
-  exp_offsets(F, V, &rows_off, &part_off, &list_off, &keys_off);
+  size_t rows_off, part_off, cand_off, list_off, keys_off;
+  exp_offsets(F, V, &rows_off, &part_off, &cand_off, &list_off, &keys_off);
   char* base = static_cast<char*>(workspace);
   ExpWs ws;
   ws.ctl = reinterpret_cast<ExpCtl*>(base);
   ws.arrivals = reinterpret_cast<unsigned int*>(base + exp_arrivals_offset());
   ws.rows = reinterpret_cast<ExpRow*>(base + rows_off);
   ws.part = reinterpret_cast<ExpPartial*>(base + part_off);
+  ws.cand = reinterpret_cast<ExpCand*>(base + cand_off);
   ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
   ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
   const int chunks = ceil_div(V, kExpChunk);
@@ -901,8 +943,8 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
                  stream, draft_logits, V, gated,
                  cap, budget, log_alpha, (const int32_t*)n_nodes, ws) != cudaSuccess ||
       launch_pdl(exp_select_kernel, dim3(1), dim3(kSelThreads),
-                 (size_t)kSelStageKeys * sizeof(unsigned long long), stream, draft_logits, V,
-                 frontier_node, tree_parent, tree_token, tree_logscore, n_nodes,
+                 (size_t)kSelStageKeys * sizeof(unsigned long long), stream, draft_logits, V, F,
+                 budget, frontier_node, tree_parent, tree_token, tree_logscore, n_nodes,
                  ws) != cudaSuccess) {
     (void)cudaGetLastError();
     return TV_ERR_CUDA;

@@ -8,6 +8,7 @@
 // 2^r - 1 nearest ancestors (node 0 contributes 1) and points to its 2^r-th
 // ancestor, so ceil(log2 N) rounds give every node its whole path.  The sum
 // over draft nodes is reduced per warp in fp32 and across warps in fp64.
+#define TV_UNIT 7
 #include "tv_common.cuh"
 
 namespace tv {
@@ -25,7 +26,7 @@ expected_kernel(const int32_t* __restrict__ parent, const float* __restrict__ pr
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x, i = threadIdx.x;
-  const bool in = i < N;
+  const bool in = i < N && TV_CHECK(N <= kMaxNodes);
   int bad_tree = 0, bad_prob = 0;
   if (in) {
     const int p = __ldg(parent + (size_t)b * N + i);
@@ -48,7 +49,8 @@ expected_kernel(const int32_t* __restrict__ parent, const float* __restrict__ pr
   int cur = 0;
   for (int span = 1; span < N; span <<= 1) {
     if (in) {
-      const int j = s_jump[cur][i];
+      int j = s_jump[cur][i];
+      if (!TV_CHECK(j < i)) j = -1;
       s_prod[cur ^ 1][i] = (j < 0) ? s_prod[cur][i] : s_prod[cur][i] * s_prod[cur][j];
       s_jump[cur ^ 1][i] = (j < 0) ? -1 : s_jump[cur][j];
     }

@@ -19,6 +19,7 @@
 //   end      = deepest valid node, ties to the lowest index,
 // and returns the workspace to zero (keys swapped out with atomicExch,
 // counter reset).  No CTA waits for another.
+#define TV_UNIT 2
 #include <climits>
 #include <mutex>
 
@@ -123,11 +124,12 @@ __device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
     }
     return;
   }
-  int bad_tree = 0, bad_tok = 0;
+  int bad_tree = !TV_CHECK(N <= kMaxNodes), bad_tok = 0;
   __syncthreads();
-  for (int i = tid; i < N; i += kGreedyThreads) {
+  for (int i = tid; i < N && !bad_tree; i += kGreedyThreads) {
     const unsigned long long key = atomicExch(g.ws.keys + o + i, 0ull);
-    const int am = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
+    int am = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
+    if (!TV_IN(am, g.V)) am = 0;
     sm.am[i] = am;
     g.argmax[o + i] = am;
     const int p = __ldcg(g.parent + o + i);
@@ -158,7 +160,7 @@ __device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
     return;
   }
   for (int i = tid; i < N; i += kGreedyThreads) {
-    sm.valid[i] = (i == 0) ? 1 : (sm.tok[i] == sm.am[sm.par[i]]);
+    sm.valid[i] = (i == 0) ? 1 : TV_IN(sm.par[i], i) && (sm.tok[i] == sm.am[sm.par[i]]);
     sm.jump[i] = sm.par[i];
   }
   __syncthreads();
@@ -169,7 +171,8 @@ __device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
     for (int k = 0; k < kScanNodesPerThread; ++k) {
       const int i = tid + k * kGreedyThreads;
       if (i < N) {
-        const int j = sm.jump[i];
+        int j = sm.jump[i];
+        if (!TV_CHECK(j < i)) j = -1;
         nv[k] = sm.valid[i] & (j < 0 ? 1 : sm.valid[j]);
         nj[k] = j < 0 ? -1 : sm.jump[j];
       }
@@ -193,12 +196,14 @@ __device__ void tree_scan(const GreedyArgs& g, int b, ScanSmem& sm, int err) {
   for (int w = 16; w > 0; w >>= 1) mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, w));
   if ((tid & 31) == 0) atomicMax(&sm.best, mine);
   __syncthreads();
-  const int end = (int)(0xffffu - (sm.best & 0xffffu));
+  int end = (int)(0xffffu - (sm.best & 0xffffu));
+  if (!TV_IN(end, N)) end = 0;
   const int end_depth = sm.dep[end];
   for (int i = tid; i < N; i += kGreedyThreads)
     if (i > end_depth) pth[i] = -1;
   if (tid == 0) {
-    for (int x = end, d = end_depth; x >= 0; x = sm.par[x], --d) pth[d] = x;
+    for (int x = end, d = end_depth; x >= 0 && TV_IN(d, N) && TV_IN(x, N); x = sm.par[x], --d)
+      pth[d] = x;
     g.accept_len[b] = end_depth;
     g.end_node[b] = end;
     g.bonus[b] = sm.am[end];
@@ -266,6 +271,7 @@ __device__ void warp_scan(const GreedyArgs& g, int b, int err, const TreeRegs& t
     in[s] = i < N;
     const unsigned long long key = in[s] ? atomicExch(g.ws.keys + o + i, 0ull) : 0ull;
     am[s] = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
+    if (in[s] && !TV_IN(am[s], g.V)) am[s] = 0;
     if (in[s]) g.argmax[o + i] = am[s];
   }
   if (lane == 0) g.ws.arrivals[b] = 0u;
@@ -371,7 +377,8 @@ __device__ __forceinline__ void finish_item(const GreedyArgs& g, long long row, 
   if (threadIdx.x == 0) {
     // the key update needs no answer; the arrival is a release (ordering the
     // update before it) and an acquire (the last arrival sees every update)
-    red_max_u64(g.ws.keys + row, pack_key(best));
+    if (TV_IN(row, (long long)g.B * g.N) && TV_IN(best.i, g.V))
+      red_max_u64(g.ws.keys + row, pack_key(best));
     const unsigned int prev = atom_add_acq_rel(g.ws.arrivals + b, timed_out ? 0x80000001u : 1u);
     const bool last = ((prev & 0x7fffffffu) == (unsigned int)(g.N * g.chunks - 1));
     *s_last = last ? (((prev >> 31) | (timed_out ? 1u : 0u)) ? 2 : 1) : 0;
@@ -405,7 +412,7 @@ greedy_bulk_kernel(const GreedyArgs g) {
   const int base = (int)(blockIdx.x % g.chunks) * g.chunk_units;
   const int n = min(g.chunk_units, U - base);
   const int b = (int)(row / g.N);
-  const int per = ceil_div(n, kGreedyPieces);
+  const int per = TV_CHECK(n >= 1 && n <= g.chunk_units) ? ceil_div(n, kGreedyPieces) : 0;
   if (tid == 0) {
     for (int q = 0; q < kGreedyPieces; ++q) sm100::mbar_init(&s_bar[q], 1);
     sm100::mbar_fence_init();

@@ -11,7 +11,8 @@
 // both contiguous across a warp.  A visit
 //   * brings the node's two row slices in by bulk copies (rows 16-byte
 //     aligned; plain coalesced loads otherwise) and asks the L2 for the first
-//     child's slices, the likeliest next visit;
+//     child's slices, the likeliest next visit (the root's slices are asked
+//     for before the dependent-launch wait);
 //   * forms the softmax normalisers with one cluster exchange: every CTA
 //     publishes its slice's (max, sum of exp(x - max)) and each combines the
 //     pairs, one lane per rank, in the same butterfly order;
@@ -33,6 +34,7 @@
 // (TwoSum), combined in a fixed order.  fp64 runs at a small fraction of the
 // fp32 rate on this part, so it is used only where the 53-bit uniform meets a
 // probability: the accept comparison and the draw's target.
+#define TV_UNIT 3
 #include <climits>
 
 #include "tv_common.cuh"
@@ -170,11 +172,28 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
   __shared__ __align__(16) float s_all_f[kMaxCluster][8];
   __shared__ int s_all_i[kMaxCluster];
   pdl_trigger();
-  pdl_wait();
   const int cl = (int)cluster_nctarank();
   const int rank = (int)sm100::cluster_ctarank();
   const int b = blockIdx.x / cl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool bulk = (V & 3) == 0;
+  const int S = slice_len(V, cl);
+  const int s_lo = min(V, rank * S), s_hi = min(V, s_lo + S);
+  const uint32_t slice_bytes = (uint32_t)(s_hi - s_lo) * 4u;
+  // Every walk starts at the root: its two slices, and the tree arrays, into
+  // the L2 while the previous kernel finishes.  A prefetch changes no result
+  // (the loads proper come after the wait and read the L2, where the
+  // previous kernel's writes land).
+  if (bulk && tid == 0 && slice_bytes > 0) {
+    sm100::bulk_prefetch_l2(p_logits + (size_t)b * N * V + s_lo, slice_bytes);
+    sm100::bulk_prefetch_l2(q_logits + (size_t)b * N * V + s_lo, slice_bytes);
+  }
+  if (tid * 32 < N) {
+    sm100::line_prefetch_l2(parent + (size_t)b * N + tid * 32);
+    sm100::line_prefetch_l2(tokens + (size_t)b * N + tid * 32);
+    sm100::line_prefetch_l2(depth + (size_t)b * N + tid * 32);
+  }
+  pdl_wait();
   int phase = 0;
   // publish eight floats and an int, wait for the cluster, read everyone's in
   // rank order
@@ -230,19 +249,17 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     return;
   }
 
-  const bool bulk = (V & 3) == 0;
-  const int S = slice_len(V, cl);
-  const int s_lo = min(V, rank * S), s_hi = min(V, s_lo + S);
   const int n4 = (s_hi - s_lo + 3) / 4;  // float4 groups; a ragged last one is padded
   const int rounds = ceil_div(n4, kWalkThreads);
   float4* const c_p = reinterpret_cast<float4*>(s_cache);
   float4* const c_q = reinterpret_cast<float4*>(s_cache + S);
-  const uint32_t slice_bytes = (uint32_t)(s_hi - s_lo) * 4u;
   uint32_t bar_parity = 0;
 
   int node = 0;
   int result = -1;
+  (void)TV_CHECK(s_hi - s_lo <= S && cl <= kMaxCluster && N <= kMaxNodes);
   for (;;) {
+    if (!TV_IN(node, N)) node = 0;
     const float* prow = p_logits + ((size_t)b * N + node) * V;
     const float* qrow = q_logits + ((size_t)b * N + node) * V;
     // ---- the node's two row slices into shared memory (every thread's
@@ -275,13 +292,16 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
       before += (w < warp) ? s_wcount[w] : 0;
       nkids += s_wcount[w];
     }
-    if (is_kid) s_kids[before + __popc(kb & ((1u << lane) - 1u))] = tid;
+    if (is_kid && TV_IN(before + __popc(kb & ((1u << lane) - 1u)), N))
+      s_kids[before + __popc(kb & ((1u << lane) - 1u))] = tid;
     __syncthreads();
     float kp = 0.0f, kq = 0.0f;
     if (tid < nkids) {  // the children's tokens' logits, for the accept tests
       const int x = s_tok[s_kids[tid]];
-      kp = __ldg(prow + x) * inv_t;
-      kq = __ldg(qrow + x) * inv_t;
+      if (TV_IN(x, V)) {
+        kp = __ldg(prow + x) * inv_t;
+        kq = __ldg(qrow + x) * inv_t;
+      }
     }
     if (bulk && tid == 0 && nkids > 0 && slice_bytes > 0) {  // the likeliest next visit
       const size_t row1 = (size_t)b * N + s_kids[0];
@@ -555,11 +575,13 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     return;
   }
   if (result == -2) result = (s_result >= 0) ? s_result : s_last;
+  if (!TV_IN(result, V)) result = -1;
   const int end_depth = s_dep[node];
   for (int i = tid; i < N; i += kWalkThreads)
     if (i > end_depth) pth[i] = -1;
   if (tid == 0) {
-    for (int x = node, d = end_depth; x >= 0; x = s_par[x], --d) pth[d] = x;
+    for (int x = node, d = end_depth; x >= 0 && TV_IN(d, N) && TV_IN(x, N); x = s_par[x], --d)
+      pth[d] = x;
     accept_len[b] = end_depth;
     end_node[b] = node;
     out_token[b] = result;

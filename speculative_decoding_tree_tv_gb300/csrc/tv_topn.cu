@@ -19,6 +19,7 @@
 //      id; a kept node whose parent was cut (scores that rise along a path)
 //      marks the tree invalid.  The sum of exp(score) over the kept draft
 //      nodes (the expected acceptance length) is reduced in fp64.
+#define TV_UNIT 8
 #include "tv_common.cuh"
 
 namespace tv {
@@ -158,7 +159,7 @@ select_topn_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
   }
   // 3. ranks of the ties, then the new numbers, over contiguous runs of ids
   const int run = (m + kTopnThreads - 1) / kTopnThreads;
-  const int lo = min(m, tid * run), hi = min(m, lo + run);
+  const int lo = min(m, tid * run), hi = TV_CHECK(run <= 32) ? min(m, lo + run) : lo;
   unsigned int keep = 0u;  // bit j: id lo + j is kept
   if (k > 0) {
     if (k == m) {
@@ -196,7 +197,8 @@ select_topn_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
       }
       int np = -1;
       if (i > 0) {
-        const unsigned int pj = s_key[__ldg(par + i)];
+        const int pi = __ldg(par + i);
+        const unsigned int pj = TV_IN(pi, m) ? s_key[pi] : kCut;
         broken |= (pj == kCut);
         np = (int)pj;
       }

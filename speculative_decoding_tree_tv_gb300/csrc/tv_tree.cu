@@ -1,5 +1,6 @@
 // tv_tree_build: parent[] -> depth[] and ancestor-or-self bitmasks, the tree
 // attention mask of OPT-Tree §2 (a node attends to its ancestors and itself).
+#define TV_UNIT 1
 #include "tv_common.cuh"
 #include "tv_sm100.cuh"
 
@@ -27,6 +28,7 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
   uint64_t* anc = anc_mask + (size_t)b * N * W;
 
   int bad = 0;
+  if (!TV_CHECK(N <= kMaxNodes && N * W <= kMaxNodes * kMaxWords)) return;
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     const int p = par[i];
     s_par[i] = p;
@@ -47,7 +49,7 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
     for (int i = threadIdx.x; i < N; i += blockDim.x) {
       int d = -1;
       uint64_t m = 0ull;
-      for (int x = i; x >= 0; x = s_par[x]) {
+      for (int x = i; x >= 0 && TV_IN(x, N); x = s_par[x]) {
         m |= 1ull << x;
         ++d;
       }
@@ -58,7 +60,7 @@ tree_build_kernel(const int32_t* __restrict__ parent, int N, int W, int32_t* __r
     for (int i = threadIdx.x; i < N; i += blockDim.x) {
       int d = -1;
       uint64_t* row = s_anc + i * W;
-      for (int x = i; x >= 0; x = s_par[x]) {
+      for (int x = i; x >= 0 && TV_IN(x, N); x = s_par[x]) {
         row[x >> 6] |= 1ull << (x & 63);
         ++d;
       }

@@ -18,3 +18,17 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _no_failed_index_check(request):
+    """Under the bounds-checked build (TV_CHECKED=1), every GPU test must end
+    with no failed index check recorded by the library."""
+    yield
+    if os.environ.get("TV_CHECKED", "0") in ("", "0") or request.node.get_closest_marker("gpu") is None:
+        return
+    import speculative_decoding_tree_tv_gb300 as tv
+    site = tv.check_take()
+    if request.node.name.startswith("test_selftest"):
+        return
+    assert site == 0, f"failed index check at unit {site >> 16}, line {site & 0xffff}"

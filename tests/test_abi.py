@@ -178,3 +178,23 @@ def test_attention_plan_override(tvlib, monkeypatch):
 def test_wait_limit_hook_rejects_bad_values(tvlib):
     """Other negative limits are refused on the host, before any device access."""
     assert tvlib.lib.tv_debug_set_wait_limit(-5) == tvlib.TV_ERR_INVALID_ARG
+
+
+def test_checked_build_exports_every_symbol(tvlib):
+    """The bounds-checked twin exports the same entry points and says which
+    build it is; its debug calls refuse bad arguments on the host."""
+    from speculative_decoding_tree_tv_gb300._build import CHECKED_LIB_PATH, LIB_PATH
+    checked = ctypes.CDLL(CHECKED_LIB_PATH)
+    regular = ctypes.CDLL(LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(checked, n)]
+    assert not missing, missing
+    assert checked.tv_checked_build() == 1
+    assert regular.tv_checked_build() == 0
+    for lib in (checked, regular):
+        lib.tv_debug_check_take.argtypes = [ctypes.c_void_p]
+        assert lib.tv_debug_check_take(None) == tvlib.TV_ERR_INVALID_ARG
+        lib.tv_debug_check_selftest.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_void_p]
+        assert lib.tv_debug_check_selftest(None, 4, 2, None) == tvlib.TV_ERR_INVALID_ARG
+        assert lib.tv_debug_check_selftest(ctypes.c_void_p(0x1000), -1, 2, None) == \
+            tvlib.TV_ERR_INVALID_ARG
