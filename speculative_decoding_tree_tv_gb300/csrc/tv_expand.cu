@@ -23,26 +23,30 @@
 //               maxima: they are distinct candidates, so the layer's
 //               limit-th best scores at least that much, and it is close to
 //               the cut;
-//   2. filter:  each CTA takes four chunks of a row, turns the fp64 gate (if
+//   2. filter:  one CTA per row turns the fp64 gate (if
 //               any) and the layer's floor into an fp32 logit threshold for
 //               the row, and appends the (row, token) candidates that pass,
 //               with their order-preserving fp64 score keys (at most the
 //               layer's limit per chunk, its best ones).  It reads the logits
 //               again only for a chunk whose bound u is at or above the
 //               threshold; otherwise the chunk's maximum (no candidate) or its
-//               lane-maximum list (every candidate) decides, so the rows
-//               stream from memory once per layer when few candidates share a
-//               chunk, the usual case above an OPT-Tree floor.  A chunk holding
+//               lane-maximum list (every candidate; one warp per such chunk
+//               appends them directly), so the rows stream from memory once
+//               per layer when few candidates share a chunk, the usual case
+//               above an OPT-Tree floor.  A re-read chunk holding
 //               more than `limit` candidates raises the floor to its limit-th
 //               best key: the layer's limit-th best is at least that, so
 //               chunks that run later skip everything below it;
-//   3. select:  one CTA keeps the best `limit` candidates (up to 2048 of them
-//               by two bitonic sorts in shared memory; beyond that a radix
-//               select on the score keys, starting at the first byte in which
-//               the keys differ), ties to the lower (parent, token), orders
-//               them (parent asc, score desc, token asc), appends them to the
-//               tree and returns the control words (candidate count, anchor,
-//               floor) to zero for the next call.
+//   3. select:  one CTA keeps the best `limit` candidates, ties to the lower
+//               (parent, token): up to 1024 candidates by their ranks (each
+//               counted by up to 32 threads), beyond that by a radix select on
+//               the score keys starting at the first byte in which the keys
+//               differ; it orders them
+//               (parent asc, score desc, token asc: each kept candidate's
+//               position is the number of kept candidates before it, counted
+//               by up to 32 threads; a bitonic sort beyond 1024 kept),
+//               appends them to the tree and returns the control words
+//               (candidate count, anchor, floor) to zero for the next call.
 // Scores are fp64 in the log domain; logits stay fp32.
 #define TV_UNIT 4
 #include <algorithm>
@@ -55,7 +59,7 @@ namespace {
 
 constexpr int kExpThreads = 256;
 constexpr int kStatsWarps = 8;   // chunks per stats CTA, one warp each
-constexpr int kFiltChunks = 4;   // chunks per filter CTA
+constexpr int kFiltGroup = 256;  // chunks per filter CTA at most (one thread each for the flags)
 constexpr int kExpChunk = 2048;
 constexpr int kSelThreads = 1024;
 constexpr int kMaxBudget = 2048;
@@ -342,7 +346,8 @@ __device__ __forceinline__ int filt_elem(bool vec, int tid, int j) {
   return vec ? 4 * (tid + kExpThreads * (j >> 2)) + (j & 3) : tid + kExpThreads * j;
 }
 
-// One CTA per (frontier row, kFiltChunks chunks of the row).  Thread 0 turns
+// One CTA per (frontier row, up to kFiltGroup chunks of the row: the whole row
+// below half a million tokens).  Thread 0 turns
 // the fp64 gate (if any) and the layer's floor into an fp32 logit threshold
 // for the row.  Per chunk, the candidates (logit >= the threshold) are
 // gathered in shared memory with their score keys, from one of three places:
@@ -367,13 +372,15 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
   __shared__ unsigned long long s_kmin, s_kmax;
   __shared__ float s_thr;
   __shared__ int s_limit;
+  __shared__ int s_chunks[kFiltGroup];  // (chunk offset << 2) | 1 list or 2 re-read
+  __shared__ int s_wcount[kExpThreads / 32];
   pdl_trigger();
   pdl_wait();
   const int row = gridDim.y - 1 - blockIdx.y;
   const int group = gridDim.x - 1 - blockIdx.x;
   const int chunks = ceil_div(V, kExpChunk);
-  const int c0 = group * kFiltChunks;
-  const int nc = min(kFiltChunks, chunks - c0);
+  const int c0 = group * kFiltGroup;
+  const int nc = min(kFiltGroup, chunks - c0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* x = logits + (size_t)row * V;
   const bool vec = (V & 3) == 0;
@@ -429,12 +436,52 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
       }
     }
   };
-  for (int cc = 0; cc < nc; ++cc) {
-    const int c = c0 + cc;
+  // the chunks holding a candidate, in order, one thread per chunk: by the
+  // list when the threshold lies above the chunk's bound, else by a re-read
+  int flag = 0;
+  if (tid < nc) {
+    const ExpPartial pc = ws.part[(size_t)row * chunks + c0 + tid];
+    flag = (pc.m >= thr) ? ((thr > pc.u) ? 1 : 2) : 0;
+  }
+  const unsigned int fb = __ballot_sync(0xffffffffu, flag != 0);
+  if (lane == 0) s_wcount[warp] = __popc(fb);
+  __syncthreads();
+  int before = 0, nflag = 0;
+#pragma unroll
+  for (int w = 0; w < kExpThreads / 32; ++w) {
+    before += (w < warp) ? s_wcount[w] : 0;
+    nflag += s_wcount[w];
+  }
+  if (flag) s_chunks[before + __popc(fb & ((1u << lane) - 1u))] = (tid << 2) | flag;
+  __syncthreads();
+  // chunks decided by their list: one warp each, appended straight to the
+  // layer's candidates (at most 32 from a chunk)
+  for (int q = warp; q < nflag; q += kExpThreads / 32) {
+    if ((s_chunks[q] & 3) != 1) continue;  // warp-uniform
+    const int c = c0 + (s_chunks[q] >> 2);
     const int start = c * kExpChunk;
     const int stop = min(V, start + kExpChunk);
-    const ExpPartial pc = ws.part[(size_t)row * chunks + c];
-    if (pc.m < thr) continue;  // uniform: no candidate in this chunk
+    const ExpCand e = ws.cand[((size_t)row * chunks + c) * 32 + lane];
+    const bool pass = e.t >= 0 && e.v >= thr && TV_IN(e.t - start, stop - start);
+    const unsigned int bal = __ballot_sync(0xffffffffu, pass);
+    if (bal == 0u) continue;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&ws.ctl->count, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (pass) {
+      const int slot = base + __popc(bal & ((1u << lane) - 1u));
+      if (TV_IN((long long)slot, (long long)gridDim.y * V)) {
+        ws.list[slot] = row_hi | (unsigned int)e.t;
+        ws.keys[slot] = double_key(off + (double)e.v);
+      }
+    }
+  }
+  // chunks read again, by the whole CTA one after another
+  for (int q = 0; q < nflag; ++q) {
+    const int c = c0 + (s_chunks[q] >> 2);
+    if ((s_chunks[q] & 3) == 1) continue;  // uniform: done above
+    const int start = c * kExpChunk;
+    const int stop = min(V, start + kExpChunk);
     if (tid == 0) {
       s_cnt = 0;
       s_out = 0;
@@ -442,13 +489,7 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
       s_kmax = 0ull;
     }
     __syncthreads();
-    if (thr > pc.u) {
-      // every candidate is some lane's maximum: the list has them all
-      if (warp == 0) {
-        const ExpCand e = ws.cand[((size_t)row * chunks + c) * 32 + lane];
-        push(e.t >= 0 && e.v >= thr && TV_IN(e.t - start, stop - start), e.v, e.t);
-      }
-    } else {
+    {
       // the chunk again, all of a thread's loads in flight at once
       float a[kFiltPer];
       if (vec) {
@@ -668,6 +709,14 @@ __device__ void bitonic_sort_u64(unsigned long long* s, int n_pow2) {
   }
 }
 
+// Threads per candidate when ranking k candidates with kSelThreads threads:
+// the largest power of two <= kSelThreads / k, at most a warp.
+__device__ __forceinline__ int rank_split(int k) {
+  int t = 1;
+  while (t < 32 && 2 * t * k <= kSelThreads) t <<= 1;
+  return t;
+}
+
 __global__ void __launch_bounds__(kSelThreads)
 exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
                   const int32_t* __restrict__ frontier_node,
@@ -682,7 +731,8 @@ exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
   __shared__ unsigned long long s_ties[kTieCap];
   __shared__ int s_n, s_nt, s_digit, s_need;
   __shared__ unsigned long long s_min, s_kmin, s_kmax;
-  // the candidates' keys, staged once so that the radix passes read shared memory
+  // the candidates' keys, staged once so that the radix passes read shared
+  // memory; once the kept set is known, the same space holds it in output order
   extern __shared__ unsigned long long s_stage[];
   pdl_trigger();
   pdl_wait();
@@ -697,197 +747,215 @@ exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
     s_kmax = 0ull;
   }
   __syncthreads();
-  if (count <= kMaxBudget) {
-    // up to 2048 candidates: sort them all by the selection order (score
-    // desc, then the lower (row, token)) in shared memory, keep the first
-    // `limit` and sort those by the output order
-    int p2 = 1;
-    while (p2 < count) p2 <<= 1;
-    for (int j = tid; j < p2; j += kSelThreads) {
-      if (j < count) {
-        const unsigned long long c = ws.list[j];
-        s_kept[j] = Kept{ws.keys[j], (int)(c >> 32), (int)(c & 0xffffffffu)};
-      } else {
-        s_kept[j] = Kept{0ull, INT_MAX, INT_MAX};  // after every candidate
-      }
-    }
-    __syncthreads();
-    bitonic_sort_kept<false>(s_kept, p2);
-    const int k = min(count, limit);
-    int q2 = 1;
-    while (q2 < k) q2 <<= 1;
-    for (int j = k + tid; j < q2; j += kSelThreads) s_kept[j] = Kept{0ull, INT_MAX, INT_MAX};
-    __syncthreads();
-    bitonic_sort_kept<true>(s_kept, q2);
-    const int n0 = ctl.n0;
+  int k;  // candidates kept, in s_kept[0, k) in no particular order
+  if (count <= limit) {
+    // every candidate is kept
+    k = TV_CHECK(count <= kMaxBudget) ? count : 0;
     for (int j = tid; j < k; j += kSelThreads) {
-      const Kept c = s_kept[j];
-      if (!(TV_IN(c.row, F) && TV_IN(c.token, V) && TV_IN(n0 + j, budget))) continue;
-      tree_parent[n0 + j] = frontier_node[c.row];
-      tree_token[n0 + j] = c.token;
-      tree_logscore[n0 + j] =
-          (float)(ws.rows[c.row].off + (double)__ldg(logits + (size_t)c.row * V + c.token));
+      const unsigned long long c = ws.list[j];
+      s_kept[j] = Kept{ws.keys[j], (int)(c >> 32), (int)(c & 0xffffffffu)};
     }
-    if (tid == 0) {
-      *n_nodes = n0 + k;
-      ws.ctl->count = 0;   // the next call starts from zero
-      ws.ctl->anchor = 0ull;
-      ws.ctl->floor = 0ull;
-    }
-    return;
-  }
-  // more than 2048 candidates (more than any layer keeps): radix select of
-  // T = the limit-th largest key, need = how many keys == T to take.  The
-  // bytes above the highest one in which the smallest and the largest key
-  // differ are common to all keys and skipped.
-  const bool staged = count <= kSelStageKeys;
-  if (staged) {
-    for (int j = tid; j < count; j += kSelThreads) s_stage[j] = ws.keys[j];
     __syncthreads();
-  }
-  const unsigned long long* K = staged ? s_stage : ws.keys;
-  unsigned long long kmin = ~0ull, kmax = 0ull;
-  for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
-    unsigned long long kb[kSelBatch];
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const int j = j0 + u * kSelThreads;
-      kb[u] = (j < count) ? K[j] : K[0];
+  } else if (count <= kSelThreads) {
+    // a few more than are kept: each candidate's rank under the selection
+    // order (score desc, then the lower (row, token)) is the number of
+    // candidates before it, counted by rank_split(count) threads; the first
+    // `limit` ranks land in order at the start of s_stage and are copied back
+    for (int j = tid; j < count; j += kSelThreads) {
+      const unsigned long long c = ws.list[j];
+      s_kept[j] = Kept{ws.keys[j], (int)(c >> 32), (int)(c & 0xffffffffu)};
     }
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      kmin = min(kmin, kb[u]);
-      kmax = max(kmax, kb[u]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if (lane == 0) {
-    atomicMin(&s_kmin, kmin);
-    atomicMax(&s_kmax, kmax);
-  }
-  __syncthreads();
-  const unsigned long long diff = s_kmin ^ s_kmax;
-  const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
-  unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
-  unsigned long long prefix = s_kmax & mask;
-  int need = limit;
-  for (int shift = top; shift >= 0; shift -= 8) {
-    for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&s_hist[0][0])[i] = 0u;
     __syncthreads();
+    Kept* s_sel = reinterpret_cast<Kept*>(s_stage);
+    const int tpc = rank_split(count);
+    const int i = tid / tpc, part = tid % tpc;
+    int r = 0;
+    Kept me{};
+    if (i < count) {
+      me = s_kept[i];
+      for (int j = part; j < count; j += tpc) r += sel_before(s_kept[j], me);
+    }
+    for (int o = tpc >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    if (i < count && part == 0 && r < limit) s_sel[r] = me;
+    __syncthreads();
+    k = limit;
+    for (int j = tid; j < k; j += kSelThreads) s_kept[j] = s_sel[j];
+    __syncthreads();
+  } else {
+    // radix select of T = the limit-th largest key, need = how many keys == T
+    // to take.  The bytes above the highest one in which the smallest and the
+    // largest key differ are common to all keys and skipped.
+    const bool staged = count <= kSelStageKeys;
+    if (staged) {
+      for (int j = tid; j < count; j += kSelThreads) s_stage[j] = ws.keys[j];
+      __syncthreads();
+    }
+    const unsigned long long* K = staged ? s_stage : ws.keys;
+    unsigned long long kmin = ~0ull, kmax = 0ull;
     for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
       unsigned long long kb[kSelBatch];
 #pragma unroll
       for (int u = 0; u < kSelBatch; ++u) {
         const int j = j0 + u * kSelThreads;
-        kb[u] = (j < count) ? K[j] : ~prefix;  // ~prefix never matches the prefix
+        kb[u] = (j < count) ? K[j] : K[0];
       }
 #pragma unroll
-      for (int u = 0; u < kSelBatch; ++u)
-        if ((kb[u] & mask) == prefix && (j0 + u * kSelThreads) < count)
-          atomicAdd(&s_hist[warp][(kb[u] >> shift) & 255ull], 1u);
+      for (int u = 0; u < kSelBatch; ++u) {
+        kmin = min(kmin, kb[u]);
+        kmax = max(kmax, kb[u]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) {
+      atomicMin(&s_kmin, kmin);
+      atomicMax(&s_kmax, kmax);
     }
     __syncthreads();
-    if (tid < 256) {
-      unsigned int t = 0u;
+    const unsigned long long diff = s_kmin ^ s_kmax;
+    const int top = diff ? ((63 - __clzll((long long)diff)) & ~7) : 0;
+    unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
+    unsigned long long prefix = s_kmax & mask;
+    int need = limit;
+    for (int shift = top; shift >= 0; shift -= 8) {
+      for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&s_hist[0][0])[i] = 0u;
+      __syncthreads();
+      for (int j0 = tid; j0 < count; j0 += kSelBatch * kSelThreads) {
+        unsigned long long kb[kSelBatch];
+#pragma unroll
+        for (int u = 0; u < kSelBatch; ++u) {
+          const int j = j0 + u * kSelThreads;
+          kb[u] = (j < count) ? K[j] : ~prefix;  // ~prefix never matches the prefix
+        }
+#pragma unroll
+        for (int u = 0; u < kSelBatch; ++u)
+          if ((kb[u] & mask) == prefix && (j0 + u * kSelThreads) < count)
+            atomicAdd(&s_hist[warp][(kb[u] >> shift) & 255ull], 1u);
+      }
+      __syncthreads();
+      if (tid < 256) {
+        unsigned int t = 0u;
 #pragma unroll 8
-      for (int w = 0; w < kSelThreads / 32; ++w) t += s_hist[w][tid];
-      s_hist[0][tid] = t;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // digits from the top: lane l sums digits 255 - 8l .. 248 - 8l, an
-      // exclusive scan over lanes gives the count above each lane's digits
-      int cnt[8], lsum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = (int)s_hist[0][255 - 8 * lane - i];
-        lsum += cnt[i];
+        for (int w = 0; w < kSelThreads / 32; ++w) t += s_hist[w][tid];
+        s_hist[0][tid] = t;
       }
-      int incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int above = incl - lsum;
-      if (above < need && incl >= need) {
-        int cum = above;
+      __syncthreads();
+      if (warp == 0) {
+        // digits from the top: lane l sums digits 255 - 8l .. 248 - 8l, an
+        // exclusive scan over lanes gives the count above each lane's digits
+        int cnt[8], lsum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (cum + cnt[i] >= need) {
-            s_digit = 255 - 8 * lane - i;
-            s_need = need - cum;
-            break;
+          cnt[i] = (int)s_hist[0][255 - 8 * lane - i];
+          lsum += cnt[i];
+        }
+        int incl = lsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int above = incl - lsum;
+        if (above < need && incl >= need) {
+          int cum = above;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (cum + cnt[i] >= need) {
+              s_digit = 255 - 8 * lane - i;
+              s_need = need - cum;
+              break;
+            }
+            cum += cnt[i];
           }
-          cum += cnt[i];
         }
       }
-    }
-    __syncthreads();
-    prefix |= (unsigned long long)s_digit << shift;
-    mask |= 0xffull << shift;
-    need = s_need;
-    __syncthreads();
-  }
-  const unsigned long long T = prefix;
-  for (int j = tid; j < count; j += kSelThreads) {
-    const unsigned long long c = ws.list[j];
-    const unsigned long long k = K[j];
-    if (k > T) {
-      const int slot = atomicAdd(&s_n, 1);
-      if (TV_IN(slot, kMaxBudget)) s_kept[slot] = Kept{k, (int)(c >> 32), (int)(c & 0xffffffffu)};
-    } else if (k == T) {
-      const int slot = atomicAdd(&s_nt, 1);
-      if (slot < kTieCap) s_ties[slot] = c;
-    }
-  }
-  __syncthreads();
-  const int n_gt = s_n, n_ties = s_nt;
-  if (n_ties <= kTieCap) {
-    // take the `need` lowest (row, token) among the ties
-    int p2 = 1;
-    while (p2 < n_ties) p2 <<= 1;
-    for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
-    __syncthreads();
-    bitonic_sort_u64(s_ties, p2);
-    for (int i = tid; i < need; i += kSelThreads)
-      if (TV_IN(n_gt + i, kMaxBudget) && TV_IN(i, kTieCap))
-        s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
-  } else {
-    // very many exact ties: pick them one by one in (row, token) order
-    unsigned long long last = 0ull;
-    bool first = true;
-    for (int r = 0; r < need; ++r) {
-      if (tid == 0) s_min = ~0ull;
       __syncthreads();
-      unsigned long long mine = ~0ull;
-      for (int j = tid; j < count; j += kSelThreads) {
+      prefix |= (unsigned long long)s_digit << shift;
+      mask |= 0xffull << shift;
+      need = s_need;
+      __syncthreads();
+    }
+    const unsigned long long T = prefix;
+    for (int j = tid; j < count; j += kSelThreads) {
+      const unsigned long long kj = K[j];
+      if (kj > T) {
         const unsigned long long c = ws.list[j];
-        if ((first || c > last) && c < mine && K[j] == T) mine = c;
+        const int slot = atomicAdd(&s_n, 1);
+        if (TV_IN(slot, kMaxBudget)) s_kept[slot] = Kept{kj, (int)(c >> 32), (int)(c & 0xffffffffu)};
+      } else if (kj == T) {
+        const int slot = atomicAdd(&s_nt, 1);
+        if (slot < kTieCap) s_ties[slot] = ws.list[j];
       }
-      atomicMin(&s_min, mine);
-      __syncthreads();
-      last = s_min;
-      first = false;
-      if (tid == 0) s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
-      __syncthreads();
     }
+    __syncthreads();
+    const int n_gt = s_n, n_ties = s_nt;
+    if (n_ties <= kTieCap) {
+      // take the `need` lowest (row, token) among the ties
+      int p2 = 1;
+      while (p2 < n_ties) p2 <<= 1;
+      for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
+      __syncthreads();
+      bitonic_sort_u64(s_ties, p2);
+      for (int i = tid; i < need; i += kSelThreads)
+        if (TV_IN(n_gt + i, kMaxBudget) && TV_IN(i, kTieCap))
+          s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
+    } else {
+      // very many exact ties: pick them one by one in (row, token) order
+      unsigned long long last = 0ull;
+      bool first = true;
+      for (int r = 0; r < need; ++r) {
+        if (tid == 0) s_min = ~0ull;
+        __syncthreads();
+        unsigned long long mine = ~0ull;
+        for (int j = tid; j < count; j += kSelThreads) {
+          const unsigned long long c = ws.list[j];
+          if ((first || c > last) && c < mine && K[j] == T) mine = c;
+        }
+        atomicMin(&s_min, mine);
+        __syncthreads();
+        last = s_min;
+        first = false;
+        if (tid == 0 && TV_IN(n_gt + r, kMaxBudget))
+          s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
+        __syncthreads();
+      }
+    }
+    k = limit;
+    __syncthreads();
   }
-  if (tid == 0) s_n = limit;
-  __syncthreads();
-  const int k = s_n;
-  int p2 = 1;
-  while (p2 < k) p2 <<= 1;
-  for (int i = k + tid; i < p2; i += kSelThreads) s_kept[i] = Kept{0ull, INT_MAX, INT_MAX};
-  __syncthreads();
-  bitonic_sort_kept<true>(s_kept, p2);
+  // the output order (parent asc, score desc, token asc).  Up to 1024 kept:
+  // each candidate's position is the number of kept candidates before it,
+  // counted by rank_split(k) threads over interleaved shares; the positions
+  // are distinct (the order is total) and the candidates land in s_stage,
+  // whose keys are no longer needed.  More: a bitonic sort in place.
+  const Kept* ordered = s_kept;
+  if (k <= kSelThreads) {
+    Kept* s_ord = reinterpret_cast<Kept*>(s_stage);
+    const int tpc = rank_split(k);
+    const int i = tid / tpc, part = tid % tpc;
+    int pos = 0;
+    Kept me{};
+    if (i < k) {
+      me = s_kept[i];
+      for (int j = part; j < k; j += tpc) pos += out_before(s_kept[j], me);
+    }
+    for (int o = tpc >> 1; o > 0; o >>= 1) pos += __shfl_xor_sync(0xffffffffu, pos, o);
+    if (i < k && part == 0 && TV_IN(pos, k)) s_ord[pos] = me;
+    __syncthreads();
+    ordered = s_ord;
+  } else {
+    int p2 = 1;
+    while (p2 < k) p2 <<= 1;
+    for (int i = k + tid; i < p2; i += kSelThreads) s_kept[i] = Kept{0ull, INT_MAX, INT_MAX};
+    __syncthreads();
+    bitonic_sort_kept<true>(s_kept, p2);
+  }
   const int n0 = ctl.n0;
   for (int i = tid; i < k; i += kSelThreads) {
-    const Kept c = s_kept[i];
+    const Kept c = ordered[i];
     if (!(TV_IN(c.row, F) && TV_IN(c.token, V) && TV_IN(n0 + i, budget))) continue;
     tree_parent[n0 + i] = frontier_node[c.row];
     tree_token[n0 + i] = c.token;
@@ -939,7 +1007,7 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
       (!gated && launch_pdl(exp_floor_kernel, dim3(1), dim3(kFloorThreads), 0, stream,
                             draft_logits, V, F, chunks, cap, budget, (const int32_t*)n_nodes,
                             ws) != cudaSuccess) ||
-      launch_pdl(exp_filter_kernel, dim3(ceil_div(chunks, kFiltChunks), F), dim3(kExpThreads), 0,
+      launch_pdl(exp_filter_kernel, dim3(ceil_div(chunks, kFiltGroup), F), dim3(kExpThreads), 0,
                  stream, draft_logits, V, gated,
                  cap, budget, log_alpha, (const int32_t*)n_nodes, ws) != cudaSuccess ||
       launch_pdl(exp_select_kernel, dim3(1), dim3(kSelThreads),
