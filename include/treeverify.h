@@ -329,7 +329,9 @@ tv_status tv_debug_set_wait_limit(long long cycles);
  * inputs or its launch geometry is checked before the access it guards.  A
  * failed check skips that access (no trap, no fault) and records its site in
  * a device word of its source unit; results are then unspecified, but every
- * access stays inside the caller's buffers.
+ * access stays inside the caller's buffers.  The attention kernel also
+ * records there the site of a bounded wait that gave up, so that a
+ * TV_ERR_TIMEOUT can be traced to the barrier it waited on.
  *
  * tv_checked_build      1 in the checked build, 0 in the regular one.
  * tv_debug_check_take   synchronises the current device, then writes to

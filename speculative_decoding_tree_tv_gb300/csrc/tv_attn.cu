@@ -23,7 +23,8 @@
 //                   that stale cache slots never reach a result.
 // Unsplit, each softmax thread normalises its row and writes it.  When the
 // key range is split across CTAs, each split stores its normalised bf16
-// partial rows to the workspace with one bulk copy, with (max, sum) pairs
+// partial rows to the workspace (chunk-major: each warp store writes 512
+// contiguous bytes), with (max, sum) pairs
 // beside them, and a merge kernel chained by programmatic dependent launch
 // combines the partials of every row.  Every wait is bounded.
 #define TV_UNIT 5
@@ -446,7 +447,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       int issued = isV ? preV : preK;
       for (int t = issued; t < T; ++t) {
         const int st = t % stages;
-        if (!mbar_wait(&empty[st], ((t / stages) & 1) ^ 1) || s_abort) {
+        const bool freed = mbar_wait(&empty[st], ((t / stages) & 1) ^ 1);
+        if (!freed || s_abort) {
+          // checked build: which ring gave up
+          if (!freed && isV) (void)TV_CHECK(false);
+          if (!freed && !isV) (void)TV_CHECK(false);
           s_abort = 1;
           break;
         }
@@ -472,6 +477,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
     bool ok = warp_wait(&bar_q, 0);
+    if (!ok) (void)TV_CHECK(false);
     int npv[2] = {0, (nrb < 2) ? T : 0};  // next PV tile of each row block
     int vzero = -1;                      // tile whose V tail was zeroed
     long long t_idle = clock64();
@@ -553,6 +559,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         issue_pv(0, t);
         if (t + kSBufs < T) ok = s_in_order(t + kSBufs);
       }
+      if (!ok) (void)TV_CHECK(false);
     } else {
       // Three streams of work, each in tile order: S(t) needs K(t) and both S
       // buffers read (softmax of t-1); PV_r(t) needs V(t) and P_r(t).  Each is
@@ -600,7 +607,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           t_idle = clock64();
         } else {
           const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
-          if (__shfl_sync(0xffffffffu, late, 0)) ok = false;
+          if (__shfl_sync(0xffffffffu, late, 0)) {
+            ok = false;
+            // checked build: what the loop waited for when it gave up
+            if (lane == 0) {
+              if (ns < T) (void)TV_CHECK(false);                            // K(ns), S buffers
+              else if (npv[0] < T && npv[0] < ns) (void)TV_CHECK(false);  // V or P of block 0
+              else (void)TV_CHECK(false);                                   // V or P of block 1
+            }
+          }
         }
       }
     }
@@ -626,6 +641,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const int j0 = (t_begin + t) * kBN;
       if (!tree_ready && j0 + kBN > L) {  // this tile reaches the tree's own key slots
         ok = warp_wait(&bar_tree, 0);
+        if (!ok) (void)TV_CHECK(false);
         if (!ok) break;
         tree_ready = true;
       }
@@ -640,6 +656,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
       }
       ok = warp_wait(&bar_s_full[rb][t % kSBufs], (t / kSBufs) & 1);
+      if (!ok) (void)TV_CHECK(false);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -684,6 +701,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (!Sh::kPInTmem && t >= kPBufs) {
         const int u = t - kPBufs;
         ok = warp_wait(&bar_o_done[rb][u % kPBufs], (u / kPBufs) & 1);
+        if (!ok) (void)TV_CHECK(false);
         if (!ok) break;
         tc_fence_after();
       }
@@ -746,6 +764,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (__any_sync(0xffffffffu, need)) {
         if (kPBufs > 1) {  // O holds every tile up to t - 1 once PV(t - 1) retired
           ok = warp_wait(&bar_o_done[rb][(t - 1) % kPBufs], ((t - 1) / kPBufs) & 1);
+          if (!ok) (void)TV_CHECK(false);
           if (!ok) break;
           tc_fence_after();
         }
@@ -764,7 +783,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&bar_p_full[rb][t % kPBufs]);
     }
-    if (ok) ok = warp_wait(&bar_o_done[rb][(T - 1) % kPBufs], ((T - 1) / kPBufs) & 1);
+    if (ok) {
+      ok = warp_wait(&bar_o_done[rb][(T - 1) % kPBufs], ((T - 1) / kPBufs) & 1);
+      if (!ok) (void)TV_CHECK(false);
+    }
     if (!ok) s_abort = 1;
     tc_fence_after();
   }
