@@ -269,8 +269,9 @@ constexpr int kFloorBatch = 16;       // chunk maxima a thread loads at once
 // The distances are fp32 (the row's offset from the anchor once per row in
 // fp64); the 1e-3-nat margin covers their rounding.  Maxima more than 32 nats
 // down are not counted; if fewer than `limit` are left there is no floor (it
-// stays 0).  With fewer chunks than `limit` (a few rows: the root layer) every
-// logit of the rows is counted instead.
+// stays 0).  With fewer chunks than `limit` (a few rows: the root layer) the
+// lanes' maxima of the statistics pass (32 per chunk, also distinct
+// candidates) are counted instead, and with fewer of those every logit.
 __global__ void __launch_bounds__(kFloorThreads)
 exp_floor_kernel(const float* __restrict__ logits, int V, int F, int chunks, int cap, int budget,
                  const int32_t* __restrict__ n_nodes, ExpWs ws) {
@@ -283,9 +284,11 @@ exp_floor_kernel(const float* __restrict__ logits, int V, int F, int chunks, int
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int remaining = budget - *n_nodes;
   const int limit = min(remaining > 0 ? remaining : 0, cap);
-  // the values counted: the chunks' maxima, or with too few chunks, every logit
-  const bool all = F * chunks < limit;
-  const int per_row = all ? V : chunks;
+  // the values counted: the chunks' maxima; with fewer chunks than `limit`,
+  // the lanes' maxima of the statistics pass (32 per chunk); with fewer
+  // still, every logit.  Each is a distinct candidate.
+  const int mode = (F * chunks >= limit) ? 0 : ((long long)F * chunks * 32 >= limit) ? 1 : 2;
+  const int per_row = mode == 0 ? chunks : mode == 1 ? chunks * 32 : V;
   const int total = F * per_row;
   if (limit == 0 || total < limit || !TV_CHECK(F <= kMaxBudget)) return;
   const double anchor = key_double(ws.ctl->anchor);
@@ -299,7 +302,10 @@ exp_floor_kernel(const float* __restrict__ logits, int V, int F, int chunks, int
 #pragma unroll
     for (int u = 0; u < kFloorBatch; ++u) {
       const int i = i0 + tid + u * kFloorThreads;
-      mx[u] = (i >= total) ? -INFINITY : all ? __ldg(logits + i) : __ldcg(&ws.part[i].m);
+      mx[u] = (i >= total) ? -INFINITY
+              : mode == 0  ? __ldcg(&ws.part[i].m)
+              : mode == 1  ? __ldcg(&ws.cand[i].v)
+                           : __ldg(logits + i);
     }
 #pragma unroll
     for (int u = 0; u < kFloorBatch; ++u) {
@@ -346,8 +352,9 @@ __device__ __forceinline__ int filt_elem(bool vec, int tid, int j) {
   return vec ? 4 * (tid + kExpThreads * (j >> 2)) + (j & 3) : tid + kExpThreads * j;
 }
 
-// One CTA per (frontier row, up to kFiltGroup chunks of the row: the whole row
-// below half a million tokens).  Thread 0 turns
+// One CTA per (frontier row, group of chunks): the whole row (up to
+// kFiltGroup chunks) once there are 32 rows or more, else four chunks, so
+// that the root layer's re-read chunks spread over CTAs.  Thread 0 turns
 // the fp64 gate (if any) and the layer's floor into an fp32 logit threshold
 // for the row.  Per chunk, the candidates (logit >= the threshold) are
 // gathered in shared memory with their score keys, from one of three places:
@@ -362,7 +369,7 @@ __device__ __forceinline__ int filt_elem(bool vec, int tid, int j) {
 // alpha gate against the anchor (limit = the remaining budget); otherwise
 // every child is a candidate and limit = min(cap, remaining).
 __global__ void __launch_bounds__(kExpThreads)
-exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, int budget,
+exp_filter_kernel(const float* __restrict__ logits, int V, int cpc, int gated, int cap, int budget,
                   double log_alpha, const int32_t* __restrict__ n_nodes, ExpWs ws) {
   __shared__ unsigned long long s_key[kExpChunk];
   __shared__ int s_tok[kExpChunk];
@@ -379,8 +386,8 @@ exp_filter_kernel(const float* __restrict__ logits, int V, int gated, int cap, i
   const int row = gridDim.y - 1 - blockIdx.y;
   const int group = gridDim.x - 1 - blockIdx.x;
   const int chunks = ceil_div(V, kExpChunk);
-  const int c0 = group * kFiltGroup;
-  const int nc = min(kFiltGroup, chunks - c0);
+  const int c0 = group * cpc;
+  const int nc = min(min(cpc, kFiltGroup), chunks - c0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* x = logits + (size_t)row * V;
   const bool vec = (V & 3) == 0;
@@ -999,6 +1006,10 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
   ws.list = reinterpret_cast<unsigned long long*>(base + list_off);
   ws.keys = reinterpret_cast<unsigned long long*>(base + keys_off);
   const int chunks = ceil_div(V, kExpChunk);
+  // chunks per filter CTA: a whole row once there are enough rows to fill the
+  // GPU; a few rows (the root layer) spread over more CTAs, since the chunks a
+  // list cannot decide are read again one after another within a CTA
+  const int cpc = F >= 32 ? kFiltGroup : 4;
   // the select stages up to kSelStageKeys keys
   if (!set_dyn_smem(exp_select_kernel, (int)(kSelStageKeys * sizeof(unsigned long long))))
     return TV_ERR_CUDA;
@@ -1007,8 +1018,8 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
       (!gated && launch_pdl(exp_floor_kernel, dim3(1), dim3(kFloorThreads), 0, stream,
                             draft_logits, V, F, chunks, cap, budget, (const int32_t*)n_nodes,
                             ws) != cudaSuccess) ||
-      launch_pdl(exp_filter_kernel, dim3(ceil_div(chunks, kFiltGroup), F), dim3(kExpThreads), 0,
-                 stream, draft_logits, V, gated,
+      launch_pdl(exp_filter_kernel, dim3(ceil_div(chunks, cpc), F), dim3(kExpThreads), 0,
+                 stream, draft_logits, V, cpc, gated,
                  cap, budget, log_alpha, (const int32_t*)n_nodes, ws) != cudaSuccess ||
       launch_pdl(exp_select_kernel, dim3(1), dim3(kSelThreads),
                  (size_t)kSelStageKeys * sizeof(unsigned long long), stream, draft_logits, V, F,

@@ -36,6 +36,7 @@
 // probability: the accept comparison and the draw's target.
 #define TV_UNIT 3
 #include <climits>
+#include <cstdlib>
 
 #include "tv_common.cuh"
 #include "tv_sm100.cuh"
@@ -58,12 +59,21 @@ __host__ __device__ inline int slice_len(int V, int cluster) {
 __host__ __device__ inline size_t cache_bytes(int V, int cluster) {
   return (size_t)2 * slice_len(V, cluster) * sizeof(float);
 }
-// 8 CTAs per tree when the slices fit, else 16, else 0 (unsupported).
+inline bool walk_cluster_fits(int V, int cl) {
+  return cache_bytes(V, cl) <= kWalkCacheMax &&
+         ceil_div(slice_len(V, cl) / 4, kWalkThreads) <= kMaxRounds;
+}
+// 8 CTAs per tree when the slices fit, else 16, else 0 (unsupported).  The
+// environment variable TV_WALK_CLUSTER=16 (or 8) replaces the choice where
+// the slices fit, for tests and tuning; it is read on every call.
 inline int walk_cluster(int V) {
+  const char* e = getenv("TV_WALK_CLUSTER");
+  if (e) {
+    const int want = atoi(e);
+    if ((want == 8 || want == 16) && walk_cluster_fits(V, want)) return want;
+  }
   for (int cl = 8; cl <= kMaxCluster; cl *= 2)
-    if (cache_bytes(V, cl) <= kWalkCacheMax &&
-        ceil_div(slice_len(V, cl) / 4, kWalkThreads) <= kMaxRounds)
-      return cl;
+    if (walk_cluster_fits(V, cl)) return cl;
   return 0;
 }
 
