@@ -827,6 +827,12 @@ exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
     unsigned long long mask = (top >= 56) ? 0ull : (~0ull << (top + 8));
     unsigned long long prefix = s_kmax & mask;
     int need = limit;
+    // Once the digit holding the limit-th key has at most kSelThreads keys
+    // (the bucket [b_lo, b_hi]), the keys above it are kept, and the `need`
+    // best of the bucket are found by their ranks: the remaining passes and
+    // the ties are skipped.
+    bool bucketed = false;
+    unsigned long long b_lo = 0ull, b_hi = 0ull;
     for (int shift = top; shift >= 0; shift -= 8) {
       for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&s_hist[0][0])[i] = 0u;
       __syncthreads();
@@ -880,58 +886,98 @@ exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
         }
       }
       __syncthreads();
+      const int bucket = (int)s_hist[0][s_digit];
       prefix |= (unsigned long long)s_digit << shift;
       mask |= 0xffull << shift;
       need = s_need;
       __syncthreads();
+      if (bucket <= kSelThreads && limit - need + bucket <= kMaxBudget) {  // uniform
+        bucketed = true;
+        b_lo = prefix;
+        b_hi = prefix | ((1ull << shift) - 1ull);
+        break;
+      }
     }
-    const unsigned long long T = prefix;
-    for (int j = tid; j < count; j += kSelThreads) {
-      const unsigned long long kj = K[j];
-      if (kj > T) {
+    if (bucketed) {
+      // the keys above the bucket go to s_kept[0, limit - need), the bucket
+      // after them; then the bucket's `need` best, by their ranks, are placed
+      // in s_stage (its keys are no longer needed) and copied back
+      const int n_gt = limit - need;
+      for (int j = tid; j < count; j += kSelThreads) {
+        const unsigned long long kj = K[j];
+        if (kj < b_lo) continue;
         const unsigned long long c = ws.list[j];
-        const int slot = atomicAdd(&s_n, 1);
+        const int slot = (kj > b_hi) ? atomicAdd(&s_n, 1) : n_gt + atomicAdd(&s_nt, 1);
         if (TV_IN(slot, kMaxBudget)) s_kept[slot] = Kept{kj, (int)(c >> 32), (int)(c & 0xffffffffu)};
-      } else if (kj == T) {
-        const int slot = atomicAdd(&s_nt, 1);
-        if (slot < kTieCap) s_ties[slot] = ws.list[j];
       }
-    }
-    __syncthreads();
-    const int n_gt = s_n, n_ties = s_nt;
-    if (n_ties <= kTieCap) {
-      // take the `need` lowest (row, token) among the ties
-      int p2 = 1;
-      while (p2 < n_ties) p2 <<= 1;
-      for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
       __syncthreads();
-      bitonic_sort_u64(s_ties, p2);
-      for (int i = tid; i < need; i += kSelThreads)
-        if (TV_IN(n_gt + i, kMaxBudget) && TV_IN(i, kTieCap))
-          s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
-    } else {
-      // very many exact ties: pick them one by one in (row, token) order
-      unsigned long long last = 0ull;
-      bool first = true;
-      for (int r = 0; r < need; ++r) {
-        if (tid == 0) s_min = ~0ull;
-        __syncthreads();
-        unsigned long long mine = ~0ull;
-        for (int j = tid; j < count; j += kSelThreads) {
-          const unsigned long long c = ws.list[j];
-          if ((first || c > last) && c < mine && K[j] == T) mine = c;
-        }
-        atomicMin(&s_min, mine);
-        __syncthreads();
-        last = s_min;
-        first = false;
-        if (tid == 0 && TV_IN(n_gt + r, kMaxBudget))
-          s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
-        __syncthreads();
+      const int nb = s_nt;
+      Kept* s_win = reinterpret_cast<Kept*>(s_stage);
+      const Kept* s_bk = s_kept + n_gt;
+      const int tpc = rank_split(nb);
+      const int i = tid / tpc, part = tid % tpc;
+      int r = 0;
+      Kept me{};
+      if (i < nb) {
+        me = s_bk[i];
+        for (int j = part; j < nb; j += tpc) r += sel_before(s_bk[j], me);
       }
+      for (int o = tpc >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+      if (i < nb && part == 0 && r < need) s_win[r] = me;
+      __syncthreads();
+      for (int j = tid; j < need; j += kSelThreads)
+        if (TV_IN(n_gt + j, kMaxBudget)) s_kept[n_gt + j] = s_win[j];
+      k = limit;
+      __syncthreads();
+    } else {
+      const unsigned long long T = prefix;
+      for (int j = tid; j < count; j += kSelThreads) {
+        const unsigned long long kj = K[j];
+        if (kj > T) {
+          const unsigned long long c = ws.list[j];
+          const int slot = atomicAdd(&s_n, 1);
+          if (TV_IN(slot, kMaxBudget)) s_kept[slot] = Kept{kj, (int)(c >> 32), (int)(c & 0xffffffffu)};
+        } else if (kj == T) {
+          const int slot = atomicAdd(&s_nt, 1);
+          if (slot < kTieCap) s_ties[slot] = ws.list[j];
+        }
+      }
+      __syncthreads();
+      const int n_gt = s_n, n_ties = s_nt;
+      if (n_ties <= kTieCap) {
+        // take the `need` lowest (row, token) among the ties
+        int p2 = 1;
+        while (p2 < n_ties) p2 <<= 1;
+        for (int i = n_ties + tid; i < p2; i += kSelThreads) s_ties[i] = ~0ull;
+        __syncthreads();
+        bitonic_sort_u64(s_ties, p2);
+        for (int i = tid; i < need; i += kSelThreads)
+          if (TV_IN(n_gt + i, kMaxBudget) && TV_IN(i, kTieCap))
+            s_kept[n_gt + i] = Kept{T, (int)(s_ties[i] >> 32), (int)(s_ties[i] & 0xffffffffu)};
+      } else {
+        // very many exact ties: pick them one by one in (row, token) order
+        unsigned long long last = 0ull;
+        bool first = true;
+        for (int r = 0; r < need; ++r) {
+          if (tid == 0) s_min = ~0ull;
+          __syncthreads();
+          unsigned long long mine = ~0ull;
+          for (int j = tid; j < count; j += kSelThreads) {
+            const unsigned long long c = ws.list[j];
+            if ((first || c > last) && c < mine && K[j] == T) mine = c;
+          }
+          atomicMin(&s_min, mine);
+          __syncthreads();
+          last = s_min;
+          first = false;
+          if (tid == 0 && TV_IN(n_gt + r, kMaxBudget))
+            s_kept[n_gt + r] = Kept{T, (int)(last >> 32), (int)(last & 0xffffffffu)};
+          __syncthreads();
+        }
+      }
+      k = limit;
+      __syncthreads();
     }
-    k = limit;
-    __syncthreads();
   }
   // the output order (parent asc, score desc, token asc).  Up to 1024 kept:
   // each candidate's position is the number of kept candidates before it,
