@@ -87,11 +87,11 @@ KERNEL_SOURCES = {
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
-    # attention kernel with the tree encoding, cold (9,197,568) + merge kernel
-    # with the L2 as the step leaves it (256 + 157,952)
-    "tv_attn_verify_tree": {"sha256": "648a782d497f5d8c26520c05e310b38642211e085af19811bfecfb2b623df94a", "bytes": 9355776,
+    # attention kernel with the tree encoding, cold (9,197,056) + merge kernel
+    # with the L2 as the step leaves it (0 + 169,472)
+    "tv_attn_verify_tree": {"sha256": "490b63b7db565f94978e6a57d2e79c753f73e635d98f7e6d84dbdfbc20e647df", "bytes": 9366528,
                             "profile": "profiles/attn_verify_tree_llama3-8b-spine60.md"},
-    "tv_accept_greedy": {"sha256": "8367fbf90e4e120a720f62ebc2fd67a39c5153f39aa0d5153fe1f70d4d703de1", "bytes": 30827776,
+    "tv_accept_greedy": {"sha256": "76c77e809430f25b2b72d1ee6af89e42c4c43d851e632172ac898ffa9450de7b", "bytes": 30825216,
                          "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},
 }
 
