@@ -1012,7 +1012,9 @@ exp_select_kernel(const float* __restrict__ logits, int V, int F, int budget,
     if (!(TV_IN(c.row, F) && TV_IN(c.token, V) && TV_IN(n0 + i, budget))) continue;
     tree_parent[n0 + i] = frontier_node[c.row];
     tree_token[n0 + i] = c.token;
-    tree_logscore[n0 + i] = (float)(ws.rows[c.row].off + (double)__ldg(logits + (size_t)c.row * V + c.token));
+    // the key is the order-preserving image of the fp64 score off + logit the
+    // filter formed: the score itself, without reading the logit again
+    tree_logscore[n0 + i] = (float)key_double(c.key);
   }
   if (tid == 0) {
     *n_nodes = n0 + k;
