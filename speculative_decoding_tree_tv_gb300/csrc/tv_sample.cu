@@ -36,6 +36,9 @@
 // probability: the accept comparison and the draw's target.
 #define TV_UNIT 3
 #include <climits>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cstdlib>
 
 #include "tv_common.cuh"
@@ -63,6 +66,9 @@ inline bool walk_cluster_fits(int V, int cl) {
   return cache_bytes(V, cl) <= kWalkCacheMax &&
          ceil_div(slice_len(V, cl) / 4, kWalkThreads) <= kMaxRounds;
 }
+// Trees a walk launch orders by depth (more than the clusters resident at once).
+constexpr int kMaxOrderTrees = 64;
+
 // 8 CTAs per tree when the slices fit, else 16, else 0 (unsupported).  The
 // environment variable TV_WALK_CLUSTER=16 (or 8) replaces the choice where
 // the slices fit, for tests and tuning; it is read on every call.
@@ -157,7 +163,7 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
             const int32_t* __restrict__ depth, int N, int V, float inv_t, uint64_t seed,
             uint64_t offset, int32_t* __restrict__ accept_len, int32_t* __restrict__ end_node,
             int32_t* __restrict__ path, int32_t* __restrict__ out_token,
-            int32_t* __restrict__ status) {
+            int32_t* __restrict__ status, int order_trees) {
   // this CTA's slices of the visited node's rows, token-major: p side (logit,
   // then probability, then residual), then q side
   extern __shared__ __align__(16) float s_cache[];
@@ -184,7 +190,7 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
   pdl_trigger();
   const int cl = (int)cluster_nctarank();
   const int rank = (int)sm100::cluster_ctarank();
-  const int b = blockIdx.x / cl;
+  int b = blockIdx.x / cl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool bulk = (V & 3) == 0;
   const int S = slice_len(V, cl);
@@ -204,6 +210,30 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
     sm100::line_prefetch_l2(depth + (size_t)b * N + tid * 32);
   }
   pdl_wait();
+  if (order_trees) {
+    // More trees than clusters fit on the GPU at once: the clusters that
+    // start first take the deepest trees (a walk visits at most depth + 1
+    // nodes), ties to the lower index, so that the ones left for the
+    // clusters that start late are the shortest.  Every CTA of a cluster
+    // computes the same permutation from the same depth arrays.
+    __shared__ int s_maxdep[kMaxOrderTrees];
+    __shared__ int s_b;
+    const int nb = (int)gridDim.x / cl;
+    for (int i = tid; i < nb; i += kWalkThreads) s_maxdep[i] = 0;
+    if (tid == 0) s_b = b;
+    __syncthreads();
+    for (int i = tid; i < nb * N; i += kWalkThreads)
+      if (TV_IN(i / N, kMaxOrderTrees)) atomicMax(&s_maxdep[i / N], __ldg(depth + i));
+    __syncthreads();
+    for (int t = tid; t < nb; t += kWalkThreads) {
+      int r = 0;
+      for (int u = 0; u < nb; ++u)
+        r += (s_maxdep[u] > s_maxdep[t]) || (s_maxdep[u] == s_maxdep[t] && u < t);
+      if (r == b) s_b = t;  // b is still this cluster's position
+    }
+    __syncthreads();
+    b = s_b;
+  }
   int phase = 0;
   // publish eight floats and an int, wait for the cluster, read everyone's in
   // rank order
@@ -599,12 +629,44 @@ walk_kernel(const float* __restrict__ p_logits, const float* __restrict__ q_logi
 }
 
 // The walk kernel as clusters of `cl` CTAs, with programmatic dependent launch.
+// Clusters of `cl` walk CTAs (with `smem` bytes each) the device holds at
+// once, per device and shape (0 if the query fails).
+int resident_walk_clusters(int cl, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> cache;
+  const auto key = std::make_tuple(current_device(), cl, smem);
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(cl * kMaxOrderTrees), 1, 1);
+  cfg.blockDim = dim3(kWalkThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cl;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, walk_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
 template <typename... Args>
 cudaError_t launch_walk(int B, int cl, size_t smem, cudaStream_t stream, Args... args) {
   if (!set_dyn_smem(walk_kernel, (int)kWalkCacheMax) ||
       !set_func_attr(reinterpret_cast<const void*>(walk_kernel),
                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1))
     return cudaErrorInvalidValue;
+  // deepest trees first when some clusters must wait for others to finish
+  const int resident = resident_walk_clusters(cl, smem);
+  const int order_trees = (resident > 0 && B > resident && B <= kMaxOrderTrees) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * cl), 1, 1);
   cfg.blockDim = dim3(kWalkThreads, 1, 1);
@@ -619,7 +681,7 @@ cudaError_t launch_walk(int B, int cl, size_t smem, cudaStream_t stream, Args...
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, walk_kernel, args...);
+  return cudaLaunchKernelEx(&cfg, walk_kernel, args..., order_trees);
 }
 
 }  // namespace
