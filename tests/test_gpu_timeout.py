@@ -23,9 +23,11 @@ def tv():
     return m
 
 
-@pytest.mark.parametrize("N", [40, 200])   # warp scan (N <= 64) and block scan
-def test_greedy_copy_wait_runs_out(tv, oracle_mod, N):
-    case = gen.make_case(950 + N, B=3, N=N, L=4, V=128256, tree="random", max_depth=12,
+# (B, N): one wave of CTAs with the warp scan (1 x 60: 600 items), and several
+# waves with the warp scan (3 x 40) and the block scan (3 x 200)
+@pytest.mark.parametrize("B,N", [(1, 60), (3, 40), (3, 200)])
+def test_greedy_copy_wait_runs_out(tv, oracle_mod, B, N):
+    case = gen.make_case(950 + N, B=B, N=N, L=4, V=128256, tree="random", max_depth=12,
                          with_attn=False)
     t = case_tensors(case)
     depth, _, _ = tv.tree_build(t["parent"])
