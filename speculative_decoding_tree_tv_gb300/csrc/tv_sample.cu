@@ -4,7 +4,8 @@
 // rejection; the accepted sequence follows the target exactly).
 //
 // One launch: a thread-block cluster of 8 CTAs (16 for vocabularies above
-// 204,800) per sequence walks that sequence's tree.  CTA `rank` owns a slice
+// 204,800) per sequence walks that sequence's tree (when there are more trees
+// than clusters resident at once, the clusters take them deepest first).  CTA `rank` owns a slice
 // of the vocabulary and keeps, for the node being visited, its slice of the p
 // and q rows in shared memory, token-major; thread t owns the float4 groups
 // t, t + 512, t + 1024, ... of the slice, so global and shared accesses are
