@@ -48,6 +48,7 @@ constexpr float kRescaleLog2 = 8.0f;  // keep a stale max while within 2^8
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
 constexpr int kMaxSplit = 64;         // splits of one CTA's key range
 constexpr int kPrefetchTiles = 4;     // tiles of a split's range prefetched into the L2
+constexpr int kMaxOrderSeqs = 64;     // sequences a launch orders longest first
 
 // Shape of a CTA: RBS row blocks of 128 query rows (one or two), 128 softmax
 // threads per row block, then the K producer, MMA and V producer warps (the
@@ -105,6 +106,7 @@ struct AttnParams {
   int mtiles;       // CTAs along the node axis: ceil(N / (row blocks x nb))
   int nsplit;       // splits of the key range
   int units;        // (sequence, kv head, node tile) units: B x Hkv x mtiles
+  int order_seqs;   // launch the sequences longest first (more CTAs than one wave)
   float scale_log2;
 };
 
@@ -296,8 +298,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   // Barriers, TMEM and descriptor prefetches need nothing from the previous
   // kernel, so they are set up before waiting for it.
   pdl_trigger();
-  const int split = blockIdx.x, mt = blockIdx.y, bh = blockIdx.z;
-  const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+  const int split = blockIdx.x, mt = blockIdx.y;
+  // With order_seqs the CTAs' sequences are set after the wait (longest
+  // first); kv heads and node tiles keep their launch order.
+  int b = (int)blockIdx.z / p.Hkv;
+  const int kvh = (int)blockIdx.z % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N, G = p.G, nb = p.nb;
   const int node0 = mt * RBS * nb;               // first node of this CTA
@@ -309,7 +314,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int node = node0 + rb * nb + nodel;
   const bool act = is_softmax && rb < nrb;       // warp-uniform
   const int h = kvh * G + row % G;
-  const bool valid_row = act && nodel < nb && node < N && TV_CHECK(h < p.Hq && bh < p.units);
+  const bool valid_row = act && nodel < nb && node < N && TV_CHECK(h < p.Hq && (int)blockIdx.z < p.units);
 
   // Split ranges come from the cache capacity, so the first tile's loads can
   // be issued before kv_len arrives; tiles past the key range are dropped.
@@ -319,7 +324,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   // tiles issued during setup, one per stage
   const int preK = min(kKStages, t_end - t_begin), preV = min(kVStages, t_end - t_begin);
   const bool first_issued = preK > 0;
-  const int y0 = bh * p.Lcap + t_begin * kBN;
+  __shared__ int s_kvl[kMaxOrderSeqs];
+  __shared__ int s_b;
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     for (int st = 0; st < kKStages; ++st) {
@@ -346,6 +352,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+    }
+    if (first_issued && !p.order_seqs) {
+      const int y0 = (int)blockIdx.z * p.Lcap + t_begin * kBN;
       // This CTA's Q rows and the first tiles of its key range into the L2
       // while the previous kernel finishes.  Prefetches are hints (the L2 is
       // where every SM reads and writes), so they change no result even if
@@ -364,6 +373,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   }
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
   pdl_wait();  // everything below may read what the previous kernel wrote
+  if (p.order_seqs) {
+    // the sequence at this CTA's launch position among the sequences sorted
+    // by key range, longest first (ties to the lower index): the CTAs that
+    // start late, after the first wave, get the short ones
+    const int nbs = (int)gridDim.z / p.Hkv;
+    if (tid < nbs && TV_IN(tid, kMaxOrderSeqs)) s_kvl[tid] = __ldg(p.kv_len + tid);
+    if (tid == 0) s_b = b;
+    __syncthreads();
+    if (tid < nbs && TV_IN(tid, kMaxOrderSeqs)) {
+      int r = 0;
+      for (int u = 0; u < nbs; ++u) r += (s_kvl[u] > s_kvl[tid]) || (s_kvl[u] == s_kvl[tid] && u < tid);
+      if (r == b) s_b = tid;  // b is still the launch position
+    }
+    __syncthreads();
+    b = s_b;
+  }
+  const int bh = b * p.Hkv + kvh;
+  const int y0 = bh * p.Lcap + t_begin * kBN;
   const int L = __ldg(p.kv_len + b);
   if (tid == 0) {
     if (first_issued) {
@@ -1166,6 +1193,10 @@ tv_status launch_attn(const tv_bf16* q, const tv_bf16* k, const tv_bf16* v, cons
   p.mtiles = sp.mtiles;
   p.nsplit = sp.nsplit;
   p.units = B * Hkv * sp.mtiles;
+  // more CTAs than one wave (one CTA per SM) and several sequences: the
+  // longest start first, so that the CTAs left for later waves are short
+  p.order_seqs = (B > 1 && B <= kMaxOrderSeqs &&
+                  (long long)sp.nsplit * sp.units > (long long)device_sm_count()) ? 1 : 0;
   p.scale_log2 = scale_log2;
   const cudaError_t e = sp.rbs == 2 ? launch_grids<D, 2>(sp, B * Hkv, stream, tmQ, tmK, tmV, p)
                                      : launch_grids<D, 1>(sp, B * Hkv, stream, tmQ, tmK, tmV, p);
