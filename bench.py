@@ -87,9 +87,9 @@ KERNEL_SOURCES = {
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
-    # attention kernel with the tree encoding, cold (9,198,592) + merge kernel
-    # with the L2 as the step leaves it (0 + 143,104)
-    "tv_attn_verify_tree": {"sha256": "a41b3534702c7ba6f6d3640ec03a84825a60352660b6024db66f1e4a14fa27c3", "bytes": 9341696,
+    # attention kernel with the tree encoding, cold (9,199,104) + merge kernel
+    # with the L2 as the step leaves it (256 + 188,672)
+    "tv_attn_verify_tree": {"sha256": "ad744423bccd9b96aad1144e856fff11b14ad85457f3badc961b3189c3c7fb8e", "bytes": 9388032,
                             "profile": "profiles/attn_verify_tree_llama3-8b-spine60.md"},
     "tv_accept_greedy": {"sha256": "76c77e809430f25b2b72d1ee6af89e42c4c43d851e632172ac898ffa9450de7b", "bytes": 30825216,
                          "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},

@@ -54,18 +54,18 @@ constexpr int kMaxOrderSeqs = 64;     // sequences a launch orders longest first
 // threads per row block, then the K producer, MMA and V producer warps (the
 // two loads wait on different barriers, so each has a warp of its own).  Two row
 // blocks share every K/V tile (the cache is streamed once per kv head); one
-// row block gives twice the CTAs.  Both fill 224 KB of shared memory (D = 128):
-//   two row blocks: Q 64 KB, one P buffer 64 KB, two K stages, one V stage.
-//     Two K stages let S(t + 1) run during the softmax of tile t; with one V
-//     stage, V(t + 1) loads once both PV(t) retired.
+// row block gives twice the CTAs.  In both the softmax writes P(t) over the
+// first 64 columns of the S buffer it read (bf16 pairs), from where PV(t)
+// reads it (tcgen05.mma with A in TMEM), and a later S into that buffer is
+// issued after PV(t) (the tensor core runs one thread's instructions in issue
+// order).  Both fill 224 KB of shared memory (D = 128):
 //   one row block:  Q 32 KB, three K stages, three V stages.  S is
-//     double-buffered in TMEM, and the softmax writes P(t) over the first 64
-//     columns of S(t) (bf16 pairs), from where PV(t) reads it: S(t + 1) is
-//     computed while the softmax of tile t runs, and S(t + 2) is issued after
-//     PV(t) (the tensor core runs one thread's instructions in issue order).
-// (P over S was measured for two row blocks as well: with a single S buffer
-// per row block, S_r(t + 1) then waits behind PV_r(t), which cost more than
-// the deeper V ring gained.)
+//     double-buffered in TMEM: S(t + 1) is computed while the softmax of tile
+//     t runs, and S(t + 2) follows PV(t).
+//   two row blocks: Q 64 KB, two K stages, three V stages.  One S buffer per
+//     row block (S and O of two row blocks fill the 512 columns), so S_r(t + 1)
+//     follows PV_r(t); the two row blocks run half a tile apart, so that one
+//     row block's softmax overlaps the other's products.
 // TMEM: S of (row block r, buffer u) at column 128 (r kSBufs + u), O_r at
 // 128 RBS kSBufs + 128 r; 512 columns either way.
 template <int RBS>
@@ -75,9 +75,8 @@ struct Shape {
   static constexpr int kProducerWarp = RBS * 4;  // K loads
   static constexpr int kMmaWarp = RBS * 4 + 1;
   static constexpr int kVProducerWarp = RBS * 4 + 2;
-  static constexpr bool kPInTmem = (RBS == 1);
   static constexpr int kKStages = (RBS == 1) ? 3 : 2;
-  static constexpr int kVStages = (RBS == 1) ? 3 : 1;
+  static constexpr int kVStages = 3;
   static constexpr int kPBufs = (RBS == 1) ? 2 : 1;
   static constexpr int kSBufs = (RBS == 1) ? 2 : 1;
   static constexpr uint32_t kTmemCols = 512u;
@@ -115,9 +114,7 @@ struct Layout {
   static constexpr int A = D / 64;                   // 128-byte atoms per row of Q, K, V
   static constexpr int kTile = A * kAtomBytes;       // one K or V tile (128 keys)
   static constexpr int kQ = 0;                       // Q [row block][atom]
-  static constexpr int kP = kQ + RBS * A * kAtomBytes;  // P [row block][buffer][key half], bf16
-  static constexpr int kK =                          // K ring [stage][atom]
-      kP + (Shape<RBS>::kPInTmem ? 0 : RBS * Shape<RBS>::kPBufs * 2 * kAtomBytes);
+  static constexpr int kK = kQ + RBS * A * kAtomBytes;  // K ring [stage][atom]
   static constexpr int kV = kK + Shape<RBS>::kKStages * kTile;  // V ring [stage][atom]
   static constexpr int kBytes = kV + Shape<RBS>::kVStages * kTile;
   static constexpr int kDyn = kBytes + 1024;         // slack for 1024-byte alignment
@@ -276,7 +273,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + Lay::kQ;
-  uint8_t* sP = smem + Lay::kP;
   uint8_t* sK = smem + Lay::kK;
   uint8_t* sV = smem + Lay::kV;
 
@@ -284,7 +280,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __shared__ __align__(8) uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   __shared__ __align__(8) uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
   __shared__ __align__(8) uint64_t bar_drain;
-  __shared__ __align__(8) uint64_t bar_s_full[2][kSBufs], bar_s_free[2][kSBufs];
+  __shared__ __align__(8) uint64_t bar_s_full[2][kSBufs];
   // one P barrier per P buffer: with two buffers the softmax may finish P(t + 1)
   // before the MMA warp has seen P(t), and a shared barrier would then be two
   // phases ahead of the parity it is tested for
@@ -339,10 +335,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_tree, 32);
     for (int r = 0; r < 2; ++r) {
-      for (int u = 0; u < kSBufs; ++u) {
-        mbar_init(&bar_s_full[r][u], 1);
-        mbar_init(&bar_s_free[r][u], kRB);
-      }
+      for (int u = 0; u < kSBufs; ++u) mbar_init(&bar_s_full[r][u], 1);
       for (int u = 0; u < kPBufs; ++u) mbar_init(&bar_p_full[r][u], kRB);
       for (int u = 0; u < kPBufs; ++u) mbar_init(&bar_o_done[r][u], 1);
     }
@@ -497,17 +490,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
   } else if (T > 0 && warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    // Three streams of work, each in tile order: S(t) needs K(t) and both S
-    // buffers read (softmax of t-1); PV_r(t) needs V(t) and P_r(t).  Each is
-    // issued as soon as its inputs are ready: S(t+1) ahead of PV(t), and the
-    // row block whose P is ready first goes first.
+    // S_r(t) needs K(t) and the S buffer free (the PV that read P from it
+    // issued before); PV_r(t) needs V(t) and P_r(t).
     constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
     bool ok = warp_wait(&bar_q, 0);
     if (!ok) (void)TV_CHECK(false);
     int npv[2] = {0, (nrb < 2) ? T : 0};  // next PV tile of each row block
     int vzero = -1;                      // tile whose V tail was zeroed
-    long long t_idle = clock64();
     // S_r(t) = Q_r K(t)^T into row block r's S buffer (lane 0)
     auto issue_s = [&](int r, int t) {
       const uint32_t k0 = smem_u32(sK) + (t % kKStages) * Lay::kTile;
@@ -542,18 +532,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (lane == 0) {
         tc_fence_after();
         const uint32_t v0 = smem_u32(sV) + (t % kVStages) * Lay::kTile;
-        if constexpr (Sh::kPInTmem) {
-          const uint32_t tP = tmem + 128 * (r * kSBufs + t % kSBufs);  // P over S: 8 columns per 16 keys
-          for (int kk = 0; kk < nk; ++kk)
-            mma_bf16_ts(tmem + kOCol + 128 * r, tP + 8 * kk,
-                        sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
-        } else {
-          const uint32_t p0 = smem_u32(sP) + (r * kPBufs + t % kPBufs) * 2 * kAtomBytes;
-          for (int kk = 0; kk < nk; ++kk)
-            mma_bf16(tmem + kOCol + 128 * r,
-                     sw128_desc(p0 + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
-                     sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
-        }
+        const uint32_t tP = tmem + 128 * (r * kSBufs + t % kSBufs);  // P over S: 8 columns per 16 keys
+        for (int kk = 0; kk < nk; ++kk)
+          mma_bf16_ts(tmem + kOCol + 128 * r, tP + 8 * kk,
+                      sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
         mma_commit(&bar_o_done[r][t % kPBufs]);
         // V(t) is free once both row blocks' PV(t) are done
         if (npv[r ^ 1] > t) mma_commit(&bar_v_empty[t % kVStages]);
@@ -561,91 +543,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       __syncwarp();
       npv[r] = t + 1;
     };
-    if constexpr (Sh::kPInTmem) {
-      // One row block: the tensor-core order is fixed -- S(0), S(1), then for
-      // each tile PV(t) followed by S(t + 2), which reuses the S buffer that
-      // held P(t) (the tensor core runs one thread's instructions in issue
-      // order).  Each input is awaited with a blocking wait, which leaves the
-      // issue slots of this scheduler to the softmax warp that shares it.
-      auto s_in_order = [&](int t) -> bool {
-        if (!warp_wait(&bar_k_full[t % kKStages], (t / kKStages) & 1)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, t);
-          mma_commit(&bar_k_empty[t % kKStages]);  // K(t) is free once S(t) is done
-        }
-        __syncwarp();
-        return true;
-      };
-      for (int t = 0; ok && t < min(T, kSBufs); ++t) ok = s_in_order(t);
+    // Each input is awaited with a blocking wait, which leaves the issue slots
+    // of this scheduler to the softmax warps that share it.
+    auto s_in_order = [&](int r, int t) -> bool {
+      if (!warp_wait(&bar_k_full[t % kKStages], (t / kKStages) & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(r, t);
+        // K(t) is free once the S(t) of every row block is done
+        if (r == nrb - 1) mma_commit(&bar_k_empty[t % kKStages]);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto pv_in_order = [&](int r, int t) -> bool {
+      if (!(warp_wait(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
+            warp_wait(&bar_p_full[r][t % kPBufs], (t / kPBufs) & 1)))
+        return false;
+      tc_fence_after();
+      issue_pv(r, t);
+      return true;
+    };
+    if constexpr (RBS == 1) {
+      // One row block: S(0), S(1), then for each tile PV(t) followed by
+      // S(t + 2), which reuses the S buffer that held P(t).
+      for (int t = 0; ok && t < min(T, kSBufs); ++t) ok = s_in_order(0, t);
       for (int t = 0; ok && t < T; ++t) {
-        ok = warp_wait(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
-             warp_wait(&bar_p_full[0][t % kPBufs], (t / kPBufs) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(0, t);
-        if (t + kSBufs < T) ok = s_in_order(t + kSBufs);
+        ok = pv_in_order(0, t);
+        if (ok && t + kSBufs < T) ok = s_in_order(0, t + kSBufs);
       }
-      if (!ok) (void)TV_CHECK(false);
     } else {
-      // Three streams of work, each in tile order: S(t) needs K(t) and both S
-      // buffers read (softmax of t-1); PV_r(t) needs V(t) and P_r(t).  Each is
-      // issued as soon as its inputs are ready: S(t+1) ahead of PV(t), and the
-      // row block whose P is ready first goes first.
-      int ns = 0;  // next S tile
-      while (ok && min(npv[0], npv[1]) < T) {
-        bool prog = false;
-        // S(t + 1) may go ahead of PV(t); with two P buffers also ahead of PV(t - 1)
-        if (ns < T && ns <= min(npv[0], npv[1]) + kPBufs) {
-          bool ready = false;
-          if (lane == 0) {
-            ready = mbar_test(&bar_k_full[ns % kKStages], (ns / kKStages) & 1);
-            if (ready && ns >= kSBufs) {  // the softmax read S(ns - kSBufs) from this buffer
-              const int u = ns % kSBufs, ph = ((ns - kSBufs) / kSBufs) & 1;
-              ready = mbar_test(&bar_s_free[0][u], ph) &&
-                      (nrb < 2 || mbar_test(&bar_s_free[1][u], ph));
-            }
-          }
-          if (__shfl_sync(0xffffffffu, ready, 0)) {
-            tc_fence_after();
-            if (lane == 0) {
-              for (int r = 0; r < nrb; ++r) issue_s(r, ns);
-              mma_commit(&bar_k_empty[ns % kKStages]);
-            }
-            __syncwarp();
-            ++ns;
-            prog = true;
-          }
+      // Two row blocks, each in its own order S_r(0), PV_r(0), S_r(1), ...
+      // (S_r(t + 1) reuses the columns that held P_r(t)), interleaved half a
+      // tile apart: S_0(0), S_1(0), then for each tile PV_0(t), S_0(t + 1),
+      // PV_1(t), S_1(t + 1).  While one row block's softmax runs, the tensor
+      // core computes the other's PV and next S.
+      for (int r = 0; ok && r < nrb; ++r) ok = s_in_order(r, 0);
+      for (int t = 0; ok && t < T; ++t)
+        for (int r = 0; ok && r < nrb; ++r) {
+          ok = pv_in_order(r, t);
+          if (ok && t + 1 < T) ok = s_in_order(r, t + 1);
         }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int t = npv[r];
-          if (t >= ns) continue;
-          bool ready = false;
-          if (lane == 0)
-            ready = mbar_test(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
-                    mbar_test(&bar_p_full[r][t % kPBufs], (t / kPBufs) & 1);
-          if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
-          tc_fence_after();
-          issue_pv(r, t);
-          prog = true;
-        }
-        if (prog) {
-          t_idle = clock64();
-        } else {
-          const bool late = (lane == 0) && (clock64() - t_idle > kWaitLimitCycles);
-          if (__shfl_sync(0xffffffffu, late, 0)) {
-            ok = false;
-            // checked build: what the loop waited for when it gave up
-            if (lane == 0) {
-              if (ns < T) (void)TV_CHECK(false);                            // K(ns), S buffers
-              else if (npv[0] < T && npv[0] < ns) (void)TV_CHECK(false);  // V or P of block 0
-              else (void)TV_CHECK(false);                                   // V or P of block 1
-            }
-          }
-        }
-      }
     }
+    if (!ok) (void)TV_CHECK(false);
     if (!ok) s_abort = 1;
     if (lane == 0) {  // all issued tensor-core work retires before TMEM is read or released
       mma_commit(&bar_drain);
@@ -659,11 +599,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS0 = tmem + 128 * (rb * kSBufs), tO = tmem + kOCol + 128 * rb;
     const float sc = p.scale_log2;
-    uint8_t* const prow0 = sP + rb * kPBufs * 2 * kAtomBytes + row * 128;
     bool ok = true;
     bool tree_ready = !p.fuse_tree;  // masks built in this launch: awaited when first needed
     for (int t = 0; ok && t < T; ++t) {
-      uint8_t* const prow = prow0 + (t % kPBufs) * 2 * kAtomBytes;
       // the mask words (their ancestor loads) are ready before S is
       const int j0 = (t_begin + t) * kBN;
       if (!tree_ready && j0 + kBN > L) {  // this tile reaches the tree's own key slots
@@ -692,8 +630,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_base + 32 * c, sr[c]);
       tmem_wait_ld();
       tc_fence_before();
-      if constexpr (!Sh::kPInTmem)
-        mbar_arrive(&bar_s_free[rb][t % kSBufs]);  // the MMA warp may write this S buffer again
 
       // hidden keys become -inf; most tiles are all visible (prefix keys)
       if ((vis[0] & vis[1] & vis[2] & vis[3]) != 0xffffffffu) {
@@ -723,20 +659,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         m_run = m_new;
         need = true;
       }
-      // P buffer t % kPBufs is free once PV(t - kPBufs) retired (with P over S,
-      // S(t) completing means PV(t - kSBufs), issued before it, completed)
-      if (!Sh::kPInTmem && t >= kPBufs) {
-        const int u = t - kPBufs;
-        ok = warp_wait(&bar_o_done[rb][u % kPBufs], (u / kPBufs) & 1);
-        if (!ok) (void)TV_CHECK(false);
-        if (!ok) break;
-        tc_fence_after();
-      }
       // 2^(s sc - m) pairwise (f32x2 FMA, then the special-function unit); a
       // hidden key gives 2^-inf = 0.  Four pairwise partial sums.
       float2 ps2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
-      if constexpr (Sh::kPInTmem) {
+      {
         // 32 keys at a time -> 16 columns of P (bf16 pairs, lower key in the
         // lower half) over the S columns this thread has already read
         const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
@@ -760,36 +687,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           tmem_st16(tS + lane_base + 16 * c, pw);
         }
         tmem_wait_st();
-      } else if (m_run == -INFINITY) {  // nothing visible yet: P = 0
-#pragma unroll
-        for (int g = 0; g < kBN / 8; ++g)
-          *reinterpret_cast<uint4*>(prow + (g >> 3) * kAtomBytes + (((g & 7) ^ (row & 7)) << 4)) =
-              make_uint4(0, 0, 0, 0);
-      } else {
-        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
-#pragma unroll
-        for (int g = 0; g < kBN / 8; ++g) {  // 8 keys -> one 16-byte chunk of P
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = 8 * g + 2 * e;
-            const float2 y = ffma2(make_float2(__uint_as_float(sr[k >> 5][k & 31]),
-                                               __uint_as_float(sr[k >> 5][(k & 31) + 1])),
-                                   sc2, nm2);
-            const float2 x = make_float2(ex2(y.x), ex2(y.y));
-            ps2[e] = fadd2(ps2[e], x);
-            w[e] = pack_bf16(x.x, x.y);
-          }
-          *reinterpret_cast<uint4*>(prow + (g >> 3) * kAtomBytes + (((g & 7) ^ (row & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
       }
       const float2 ps_a = fadd2(ps2[0], ps2[1]), ps_b = fadd2(ps2[2], ps2[3]);
       const float2 ps_ab = fadd2(ps_a, ps_b);
       l_run = l_run * corr + (ps_ab.x + ps_ab.y);
       // rescale O after the exponentials, when S no longer holds registers
       if (__any_sync(0xffffffffu, need)) {
-        if (kPBufs > 1) {  // O holds every tile up to t - 1 once PV(t - 1) retired
+        // O holds every tile up to t - 1 once PV(t - 1) retired: with one S
+        // buffer, S(t) was issued after it and has completed
+        if (kSBufs > 1) {
           ok = warp_wait(&bar_o_done[rb][(t - 1) % kPBufs], ((t - 1) / kPBufs) & 1);
           if (!ok) (void)TV_CHECK(false);
           if (!ok) break;
@@ -806,7 +712,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         tmem_wait_st();
       }
-      if constexpr (!Sh::kPInTmem) fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bar_p_full[rb][t % kPBufs]);
     }
@@ -1021,8 +926,9 @@ struct SplitPlan {
 // and long-context shapes:
 //   * a CTA's fixed part (launch into the SM, setup, the first tile's loads
 //     and compute, epilogue), for 128-row and 256-row CTAs;
-//   * each further 128-key tile.  A 256-row CTA has a single V stage, so each
-//     tile's PV waits for its own V load.  A 128-row CTA pipelines two tiles, but
+//   * each further 128-key tile.  A 256-row CTA's tile is four 128 x 128 x 128
+//     products (S and PV of each row block), about 0.5 us each on the tensor
+//     core at this instruction shape.  A 128-row CTA pipelines two tiles, but
 //     the L2 serves each kv head's tile once per node tile, and its period
 //     grows with the number of node tiles streaming the same cache;
 //   * the merge kernel: mostly its launch boundary, plus the partial bytes.
