@@ -52,7 +52,9 @@ constexpr int kMaxOrderSeqs = 64;     // sequences a launch orders longest first
 
 // Shape of a CTA: RBS row blocks of 128 query rows (one or two), 128 softmax
 // threads per row block, then the K producer, MMA and V producer warps (the
-// two loads wait on different barriers, so each has a warp of its own).  Two row
+// two loads wait on different barriers, so each has a warp of its own) and,
+// with two row blocks, a second MMA warp: each row block's products are issued
+// by a warp of their own.  Two row
 // blocks share every K/V tile (the cache is streamed once per kv head); one
 // row block gives twice the CTAs.  In both the softmax writes P(t) over the
 // first 64 columns of the S buffer it read (bf16 pairs), from where PV(t)
@@ -64,17 +66,18 @@ constexpr int kMaxOrderSeqs = 64;     // sequences a launch orders longest first
 //     t runs, and S(t + 2) follows PV(t).
 //   two row blocks: Q 64 KB, two K stages, three V stages.  One S buffer per
 //     row block (S and O of two row blocks fill the 512 columns), so S_r(t + 1)
-//     follows PV_r(t); the two row blocks run half a tile apart, so that one
-//     row block's softmax overlaps the other's products.
+//     follows PV_r(t); the two row blocks settle half a tile apart, one row
+//     block's softmax overlapping the other's products.
 // TMEM: S of (row block r, buffer u) at column 128 (r kSBufs + u), O_r at
 // 128 RBS kSBufs + 128 r; 512 columns either way.
 template <int RBS>
 struct Shape {
   static constexpr int kRows = RBS * kRB;
-  static constexpr int kThreads = RBS * kRB + 96;
+  static constexpr int kThreads = RBS * kRB + 32 * (RBS == 2 ? 4 : 3);
   static constexpr int kProducerWarp = RBS * 4;  // K loads
-  static constexpr int kMmaWarp = RBS * 4 + 1;
+  static constexpr int kMmaWarp = RBS * 4 + 1;   // products of row block 0
   static constexpr int kVProducerWarp = RBS * 4 + 2;
+  static constexpr int kMmaWarp1 = RBS * 4 + 3;  // products of row block 1 (two row blocks)
   static constexpr int kKStages = (RBS == 1) ? 3 : 2;
   static constexpr int kVStages = 3;
   static constexpr int kPBufs = (RBS == 1) ? 2 : 1;
@@ -280,6 +283,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __shared__ __align__(8) uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   __shared__ __align__(8) uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
   __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ __align__(8) uint64_t bar_vzero;  // the last tile's V rows past the range are cleared
   __shared__ __align__(8) uint64_t bar_s_full[2][kSBufs];
   // one P barrier per P buffer: with two buffers the softmax may finish P(t + 1)
   // before the MMA warp has seen P(t), and a shared barrier would then be two
@@ -324,15 +328,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __shared__ int s_b;
   if (tid == 0) {
     mbar_init(&bar_q, 1);
+    // a K or V stage is free, and the tensor core idle at the end, once the
+    // products of every row block holding a node are done (one commit each)
     for (int st = 0; st < kKStages; ++st) {
       mbar_init(&bar_k_full[st], 1);
-      mbar_init(&bar_k_empty[st], 1);
+      mbar_init(&bar_k_empty[st], nrb);
     }
     for (int st = 0; st < kVStages; ++st) {
       mbar_init(&bar_v_full[st], 1);
-      mbar_init(&bar_v_empty[st], 1);
+      mbar_init(&bar_v_empty[st], nrb);
     }
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain, nrb);
+    mbar_init(&bar_vzero, 1);
     mbar_init(&bar_tree, 32);
     for (int r = 0; r < 2; ++r) {
       for (int u = 0; u < kSBufs; ++u) mbar_init(&bar_s_full[r][u], 1);
@@ -488,18 +495,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int t = max(0, issued - stages); t < issued; ++t)
         mbar_wait(&full[t % stages], (t / stages) & 1);
     }
-  } else if (T > 0 && warp == kMmaWarp) {
+  } else if (T > 0 && (warp == kMmaWarp || (RBS == 2 && warp == Sh::kMmaWarp1 && nrb == 2))) {
     // ----------------------------------------------------------------- MMA
-    // S_r(t) needs K(t) and the S buffer free (the PV that read P from it
-    // issued before); PV_r(t) needs V(t) and P_r(t).
+    // One warp per row block r issues its products in the fixed order
+    // S_r(0), [S_r(1),] then PV_r(t) followed by the next S into the buffer
+    // that held P_r(t) (the tensor core runs one thread's instructions in issue
+    // order).  S_r(t) needs K(t); PV_r(t) needs V(t) and P_r(t).  With two row
+    // blocks the two warps issue independently: while one waits for its
+    // softmax, the other's products keep the tensor core busy, and neither
+    // warp's own issue overhead leaves it idle.
+    const int r = (warp == kMmaWarp) ? 0 : 1;
     constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
     bool ok = warp_wait(&bar_q, 0);
     if (!ok) (void)TV_CHECK(false);
-    int npv[2] = {0, (nrb < 2) ? T : 0};  // next PV tile of each row block
-    int vzero = -1;                      // tile whose V tail was zeroed
     // S_r(t) = Q_r K(t)^T into row block r's S buffer (lane 0)
-    auto issue_s = [&](int r, int t) {
+    auto issue_s = [&](int t) {
       const uint32_t k0 = smem_u32(sK) + (t % kKStages) * Lay::kTile;
       const uint32_t q0 = smem_u32(sQ) + r * A * kAtomBytes;
 #pragma unroll
@@ -509,24 +520,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                  sw128_desc(k0 + off, 16, 1024), idS, kk > 0);
       }
       mma_commit(&bar_s_full[r][t % kSBufs]);
+      mma_commit(&bar_k_empty[t % kKStages]);  // K(t) is free once every S(t) is done
     };
-    // O_r += P_r(t) V(t) over the 16-key steps that hold a key of the range;
-    // the V rows of the last step past the range (at most 15) are cleared
-    // first, as the cache may hold anything there (whole warp)
-    auto issue_pv = [&](int r, int t) {
+    // O_r += P_r(t) V(t) over the 16-key steps that hold a key of the range.
+    // The V rows of the last step past the range (at most 15; only the tile
+    // that ends the key range has them) are cleared first, as the cache may
+    // hold anything there: by row block 0's warp, which row block 1's waits for.
+    auto issue_pv = [&](int t) -> bool {
       const int valid = min(kBN, keys - (t_begin + t) * kBN);
       const int nk = (valid + 15) >> 4;
-      if (vzero < t) {
-        const int z1 = min(kBN, nk * 16);
-        if (valid < z1) {
+      const int z1 = min(kBN, nk * 16);
+      if (valid < z1) {
+        if (r == 0) {
 #pragma unroll
           for (int a = 0; a < A; ++a)
             for (int zr = valid + (lane >> 3); zr < z1; zr += 4)
               *reinterpret_cast<uint4*>(sV + (t % kVStages) * Lay::kTile + a * kAtomBytes +
                                         zr * 128 + ((lane & 7) << 4)) = make_uint4(0, 0, 0, 0);
           fence_async_smem();
+          __syncwarp();
+          if (nrb == 2 && lane == 0) mbar_arrive(&bar_vzero);
+        } else if (!warp_wait(&bar_vzero, 0)) {
+          return false;
         }
-        vzero = t;
       }
       __syncwarp();
       if (lane == 0) {
@@ -537,59 +553,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           mma_bf16_ts(tmem + kOCol + 128 * r, tP + 8 * kk,
                       sw128_desc(v0 + kk * 16 * 128, kAtomBytes, 1024), idO, (t > 0) || (kk > 0));
         mma_commit(&bar_o_done[r][t % kPBufs]);
-        // V(t) is free once both row blocks' PV(t) are done
-        if (npv[r ^ 1] > t) mma_commit(&bar_v_empty[t % kVStages]);
-      }
-      __syncwarp();
-      npv[r] = t + 1;
-    };
-    // Each input is awaited with a blocking wait, which leaves the issue slots
-    // of this scheduler to the softmax warps that share it.
-    auto s_in_order = [&](int r, int t) -> bool {
-      if (!warp_wait(&bar_k_full[t % kKStages], (t / kKStages) & 1)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        issue_s(r, t);
-        // K(t) is free once the S(t) of every row block is done
-        if (r == nrb - 1) mma_commit(&bar_k_empty[t % kKStages]);
+        mma_commit(&bar_v_empty[t % kVStages]);  // V(t) is free once every PV(t) is done
       }
       __syncwarp();
       return true;
     };
-    auto pv_in_order = [&](int r, int t) -> bool {
+    // Each input is awaited with a blocking wait, which leaves the issue slots
+    // of this scheduler to the softmax warps that share it.
+    auto s_in_order = [&](int t) -> bool {
+      if (!warp_wait(&bar_k_full[t % kKStages], (t / kKStages) & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) issue_s(t);
+      __syncwarp();
+      return true;
+    };
+    auto pv_in_order = [&](int t) -> bool {
       if (!(warp_wait(&bar_v_full[t % kVStages], (t / kVStages) & 1) &&
             warp_wait(&bar_p_full[r][t % kPBufs], (t / kPBufs) & 1)))
         return false;
       tc_fence_after();
-      issue_pv(r, t);
-      return true;
+      return issue_pv(t);
     };
-    if constexpr (RBS == 1) {
-      // One row block: S(0), S(1), then for each tile PV(t) followed by
-      // S(t + 2), which reuses the S buffer that held P(t).
-      for (int t = 0; ok && t < min(T, kSBufs); ++t) ok = s_in_order(0, t);
-      for (int t = 0; ok && t < T; ++t) {
-        ok = pv_in_order(0, t);
-        if (ok && t + kSBufs < T) ok = s_in_order(0, t + kSBufs);
-      }
-    } else {
-      // Two row blocks, each in its own order S_r(0), PV_r(0), S_r(1), ...
-      // (S_r(t + 1) reuses the columns that held P_r(t)), interleaved half a
-      // tile apart: S_0(0), S_1(0), then for each tile PV_0(t), S_0(t + 1),
-      // PV_1(t), S_1(t + 1).  While one row block's softmax runs, the tensor
-      // core computes the other's PV and next S.
-      for (int r = 0; ok && r < nrb; ++r) ok = s_in_order(r, 0);
-      for (int t = 0; ok && t < T; ++t)
-        for (int r = 0; ok && r < nrb; ++r) {
-          ok = pv_in_order(r, t);
-          if (ok && t + 1 < T) ok = s_in_order(r, t + 1);
-        }
+    for (int t = 0; ok && t < min(T, kSBufs); ++t) ok = s_in_order(t);
+    for (int t = 0; ok && t < T; ++t) {
+      ok = pv_in_order(t);
+      if (ok && t + kSBufs < T) ok = s_in_order(t + kSBufs);
     }
     if (!ok) (void)TV_CHECK(false);
     if (!ok) s_abort = 1;
     if (lane == 0) {  // all issued tensor-core work retires before TMEM is read or released
       mma_commit(&bar_drain);
-      mbar_wait(&bar_drain, 0);
+      // (a warp that gave up may leave the other's commit missing: bounded)
+      if (!mbar_wait(&bar_drain, 0)) s_abort = 1;
     }
     __syncwarp();
   } else if (T > 0 && act) {
