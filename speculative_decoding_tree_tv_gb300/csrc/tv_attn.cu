@@ -66,8 +66,9 @@ constexpr int kMaxOrderSeqs = 64;     // sequences a launch orders longest first
 //     t runs, and S(t + 2) follows PV(t).
 //   two row blocks: Q 64 KB, two K stages, three V stages.  One S buffer per
 //     row block (S and O of two row blocks fill the 512 columns), so S_r(t + 1)
-//     follows PV_r(t); the two row blocks settle half a tile apart, one row
-//     block's softmax overlapping the other's products.
+//     follows PV_r(t).  The two row blocks run in step: both softmaxes, then
+//     the four products back to back (a product run beside a softmax shares
+//     TMEM traffic with it and runs slower).
 // TMEM: S of (row block r, buffer u) at column 128 (r kSBufs + u), O_r at
 // 128 RBS kSBufs + 128 r; 512 columns either way.
 template <int RBS>
@@ -501,9 +502,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     // S_r(0), [S_r(1),] then PV_r(t) followed by the next S into the buffer
     // that held P_r(t) (the tensor core runs one thread's instructions in issue
     // order).  S_r(t) needs K(t); PV_r(t) needs V(t) and P_r(t).  With two row
-    // blocks the two warps issue independently: while one waits for its
-    // softmax, the other's products keep the tensor core busy, and neither
-    // warp's own issue overhead leaves it idle.
+    // blocks the two warps issue independently, so that neither warp's own
+    // issue overhead leaves the tensor core idle between products.
     const int r = (warp == kMmaWarp) ? 0 : 1;
     constexpr uint32_t idS = idesc_bf16_f32(kRB, kBN, 0, 0);
     constexpr uint32_t idO = idesc_bf16_f32(kRB, D, 0, 1);
