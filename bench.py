@@ -87,9 +87,9 @@ KERNEL_SOURCES = {
     "tv_accept_greedy": ["tv_greedy.cu", "tv_sm100.cuh", "tv_common.cuh"],
 }
 NCU_TRAFFIC = {
-    # attention kernel with the tree encoding, cold (9,199,104) + merge kernel
-    # with the L2 as the step leaves it (256 + 188,672)
-    "tv_attn_verify_tree": {"sha256": "ad744423bccd9b96aad1144e856fff11b14ad85457f3badc961b3189c3c7fb8e", "bytes": 9388032,
+    # attention kernel with the tree encoding, cold (9,198,848) + merge kernel
+    # with the L2 as the step leaves it (0 + 165,376)
+    "tv_attn_verify_tree": {"sha256": "0316274025701df97e9f535d1f7d7a65c7f1603c3b4a8860453db587d5c455be", "bytes": 9364224,
                             "profile": "profiles/attn_verify_tree_llama3-8b-spine60.md"},
     "tv_accept_greedy": {"sha256": "76c77e809430f25b2b72d1ee6af89e42c4c43d851e632172ac898ffa9450de7b", "bytes": 30825216,
                          "profile": "profiles/greedy_bulk_kernel_llama3-8b-spine60.md"},
