@@ -66,6 +66,7 @@ constexpr int kMaxBudget = 2048;
 constexpr int kTieCap = 1024;
 constexpr int kSelBatch = 8;  // key loads in flight per thread in the select passes
 constexpr int kSelStageKeys = 16384;  // candidates whose keys the select stages in shared memory
+constexpr int kFoldBins = 2048;  // the statistics pass's floor histogram: 1/64-nat bins, 32 nats
 
 struct ExpPartial {
   double s;  // sum of exp(x - m) over the chunk
@@ -87,7 +88,7 @@ struct ExpCtl {
   int count;                 // candidates appended by the filter (returned to 0)
   int limit;                 // how many may be kept
   int n0;                    // nodes in the tree before this layer
-  int pad;
+  unsigned int rows_done;    // rows whose statistics are complete (returned to 0)
   unsigned long long anchor;  // order-preserving key of the best score (returned to 0)
   unsigned long long floor;   // key no kept candidate lies below (returned to 0)
 };
@@ -95,6 +96,7 @@ struct ExpCtl {
 struct ExpWs {
   ExpCtl* ctl;
   unsigned int* arrivals;  // [kMaxBudget] chunks of each row done by the stats pass (returned to 0)
+  unsigned int* hist;      // [kFoldBins] chunk maxima per distance bin (returned to 0)
   ExpRow* rows;
   ExpPartial* part;
   ExpCand* cand;             // [row][chunk][32] lane maxima of each chunk
@@ -107,11 +109,14 @@ struct ExpWs {
 // looks, whatever its number of frontier rows; the per-row and per-chunk
 // regions after them move with F and are written before they are read.
 __host__ __device__ inline size_t exp_arrivals_offset() { return align_up(sizeof(ExpCtl), 256); }
+__host__ __device__ inline size_t exp_hist_offset() {
+  return exp_arrivals_offset() + align_up((size_t)kMaxBudget * sizeof(unsigned int), 256);
+}
 __host__ __device__ inline size_t exp_offsets(int F, int V, size_t* rows_off, size_t* part_off,
                                               size_t* cand_off, size_t* list_off,
                                               size_t* keys_off) {
   const int chunks = (V + kExpChunk - 1) / kExpChunk;
-  size_t o = exp_arrivals_offset() + align_up((size_t)kMaxBudget * sizeof(unsigned int), 256);
+  size_t o = exp_hist_offset() + align_up((size_t)kFoldBins * sizeof(unsigned int), 256);
   *rows_off = o;
   o += align_up((size_t)F * sizeof(ExpRow), 256);
   *part_off = o;
@@ -146,10 +151,29 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // partial (max, sum of exp(x - max)); the CTA then arrives on the row's counter
 // with its number of chunks, and warp 0 of the row's last CTA combines the
 // row's partials.
+//
+// fold (OPT-Tree layers with at least `cap` chunks): the floor under the
+// layer's limit-th best score is found here instead of by exp_floor_kernel.
+// Its reference is A0, the best frontier score, which no child's score
+// exceeds (a row's normaliser is at least its largest term), so every
+// distance below it is >= 0; the layer's best score lies within log V of it
+// (a row's best child has probability >= 1 / V).  The row's last CTA counts
+// each chunk maximum's distance below A0 in 1/64-nat bins (32 nats), and the
+// layer's last row (acquiring every row's counts; its whole CTA, 8 bins a
+// thread) finds the first bin from the top at which the count reaches
+// `limit`: the floor is that bin's lower edge less a 1e-3
+// nat margin for the fp32 distances, a little under the limit-th best chunk
+// maximum and so under the limit-th best score (chunk maxima are distinct
+// candidates).  Fewer than `limit` counted: no floor, as in exp_floor_kernel.
+// The histogram and the row counter are returned to zero.
 __global__ void __launch_bounds__(kStatsWarps * 32)
 exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
-                 const float* __restrict__ frontier_logscore, ExpWs ws) {
+                 const float* __restrict__ frontier_logscore, int fold, int cap, int budget,
+                 const int32_t* __restrict__ n_nodes, ExpWs ws) {
   __shared__ int s_last;
+  __shared__ unsigned int s_done;
+  __shared__ float s_a0;
+  __shared__ unsigned int s_wsum[kStatsWarps];
   pdl_trigger();
   pdl_wait();
   ExpPartial* __restrict__ part = ws.part;
@@ -221,25 +245,93 @@ exp_stats_kernel(const float* __restrict__ logits, int V, int chunks,
              (arrive_acq_rel(&ws.arrivals[row], mine) + mine == (unsigned int)chunks);
   }
   __syncthreads();
-  if (!s_last || warp != 0) return;
-  // warp 0 of the row's last CTA: normaliser, offset and best score of the
-  // row.  Exponentials on the SFU (fp32; fp64 runs at a small fraction of the
-  // fp32 rate here), the sum itself in fp64.
-  const ExpPartial* p = part + (size_t)row * chunks;
-  float mr = -INFINITY;
-  for (int k = lane; k < chunks; k += 32) mr = fmaxf(mr, __ldcg(&p[k].m));
-  mr = warp_max(mr);
-  double sr = 0.0;
-  for (int k = lane; k < chunks; k += 32)
-    sr += __ldcg(&p[k].s) * (double)ex2_approx((__ldcg(&p[k].m) - mr) * kLog2e);
-  sr = warp_sum_d(sr);
-  if (lane == 0) {
-    ws.arrivals[row] = 0u;
-    const double off = (double)frontier_logscore[row] - ((double)mr + log(sr));
-    ws.rows[row].off = off;
-    ws.rows[row].m = mr;
-    atomicMax(&ws.ctl->anchor, double_key(off + (double)mr));
+  if (!s_last) return;  // uniform over the CTA
+  const int F = (int)gridDim.y;
+  if (warp == 0) {
+    // warp 0 of the row's last CTA: normaliser, offset and best score of the
+    // row.  Exponentials on the SFU (fp32; fp64 runs at a small fraction of
+    // the fp32 rate here), the sum itself in fp64, the logarithm in one lane.
+    const ExpPartial* p = part + (size_t)row * chunks;
+    float mr = -INFINITY;
+    for (int k = lane; k < chunks; k += 32) mr = fmaxf(mr, __ldcg(&p[k].m));
+    mr = warp_max(mr);
+    double sr = 0.0;
+    for (int k = lane; k < chunks; k += 32)
+      sr += __ldcg(&p[k].s) * (double)ex2_approx((__ldcg(&p[k].m) - mr) * kLog2e);
+    sr = warp_sum_d(sr);
+    double off = 0.0;
+    if (lane == 0) {
+      off = (double)frontier_logscore[row] - ((double)mr + log(sr));
+      ws.arrivals[row] = 0u;
+      ws.rows[row].off = off;
+      ws.rows[row].m = mr;
+      atomicMax(&ws.ctl->anchor, double_key(off + (double)mr));
+    }
+    if (fold) {
+      off = __shfl_sync(0xffffffffu, off, 0);
+      float a0 = -INFINITY;
+      for (int r = lane; r < F; r += 32) a0 = fmaxf(a0, __ldg(frontier_logscore + r));
+      a0 = warp_max(a0);
+      const float av = (float)((double)a0 - off);  // A0 - off, once per row in fp64
+      for (int k = lane; k < chunks; k += 32) {
+        const float d = (av - __ldcg(&p[k].m)) * 64.0f;  // >= 0 up to rounding
+        if (d < (float)kFoldBins) atomicAdd(&ws.hist[max(0, (int)d)], 1u);
+      }
+      __threadfence();  // this lane's counts are performed before the row arrives
+      __syncwarp();
+      if (lane == 0) {
+        s_done = arrive_acq_rel(&ws.ctl->rows_done, 1u) + 1u;
+        s_a0 = a0;
+      }
+    }
   }
+  if (!fold) return;
+  __syncthreads();
+  if (s_done != (unsigned int)F) return;
+  // the layer's last row: every row's counts are in (acquired by thread 0;
+  // the barrier orders the reads below after it).  Thread t holds bins
+  // [8t, 8t + 8), nearest to A0 first.
+  static_assert(kFoldBins == 8 * kStatsWarps * 32, "8 bins a thread");
+  const int t = threadIdx.x;
+  const uint4 h0 = __ldcg(reinterpret_cast<const uint4*>(ws.hist) + 2 * t);
+  const uint4 h1 = __ldcg(reinterpret_cast<const uint4*>(ws.hist) + 2 * t + 1);
+  const unsigned int hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  unsigned int tsum = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tsum += hb[i];
+  unsigned int incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) incl += s_wsum[w];
+  const unsigned int above = incl - tsum;  // maxima in bins nearer to A0
+  const int remaining = budget - __ldcg(n_nodes);
+  const int limit = min(remaining > 0 ? remaining : 0, cap);
+  const unsigned int need = (unsigned int)limit;
+  if (limit > 0 && above < need && incl >= need) {
+    // the first of this thread's bins (nearest A0 first) at which the count
+    // reaches `need`
+    int bin = 8 * t + 7;
+    unsigned int run = above;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      run += hb[i];
+      if (run >= need) {
+        bin = 8 * t + i;
+        break;
+      }
+    }
+    // every maximum counted up to this bin lies above A0 - (bin + 1) / 64, up
+    // to the fp32 rounding of its distance, which the margin covers
+    ws.ctl->floor = double_key((double)s_a0 - (double)(bin + 1) / 64.0 - 1e-3);
+  }
+  reinterpret_cast<uint4*>(ws.hist)[2 * t] = make_uint4(0u, 0u, 0u, 0u);
+  reinterpret_cast<uint4*>(ws.hist)[2 * t + 1] = make_uint4(0u, 0u, 0u, 0u);
+  if (t == 0) ws.ctl->rows_done = 0u;
 }
 
 // Smallest fp32 value >= x (x finite).
@@ -1048,6 +1140,7 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
   ExpWs ws;
   ws.ctl = reinterpret_cast<ExpCtl*>(base);
   ws.arrivals = reinterpret_cast<unsigned int*>(base + exp_arrivals_offset());
+  ws.hist = reinterpret_cast<unsigned int*>(base + exp_hist_offset());
   ws.rows = reinterpret_cast<ExpRow*>(base + rows_off);
   ws.part = reinterpret_cast<ExpPartial*>(base + part_off);
   ws.cand = reinterpret_cast<ExpCand*>(base + cand_off);
@@ -1061,9 +1154,13 @@ tv_status launch_layer(const float* draft_logits, const int32_t* frontier_node,
   // the select stages up to kSelStageKeys keys
   if (!set_dyn_smem(exp_select_kernel, (int)(kSelStageKeys * sizeof(unsigned long long))))
     return TV_ERR_CUDA;
+  // OPT-Tree layers with at least `cap` chunks (every one but the root's) find
+  // their floor in the statistics pass; the others launch the floor kernel
+  const int fold = (!gated && (long long)F * chunks >= cap) ? 1 : 0;
   if (launch_pdl(exp_stats_kernel, dim3(ceil_div(chunks, kStatsWarps), F), dim3(kStatsWarps * 32),
-                 0, stream, draft_logits, V, chunks, frontier_logscore, ws) != cudaSuccess ||
-      (!gated && launch_pdl(exp_floor_kernel, dim3(1), dim3(kFloorThreads), 0, stream,
+                 0, stream, draft_logits, V, chunks, frontier_logscore, fold, cap, budget,
+                 (const int32_t*)n_nodes, ws) != cudaSuccess ||
+      (!gated && !fold && launch_pdl(exp_floor_kernel, dim3(1), dim3(kFloorThreads), 0, stream,
                             draft_logits, V, F, chunks, cap, budget, (const int32_t*)n_nodes,
                             ws) != cudaSuccess) ||
       launch_pdl(exp_filter_kernel, dim3(ceil_div(chunks, cpc), F), dim3(kExpThreads), 0,
