@@ -444,10 +444,14 @@ tv_status tv_accept_sample(const float* p_logits, const float* q_logits,
  *   n_nodes           int32 [1], device, in/out: nodes in the tree.
  *   workspace         >= tv_expand_workspace_size(F, V) bytes, zero-filled before
  *                     its first use; every call returns its control words (per-row
- *                     arrival counters, candidate count, anchor) to zero, so the
- *                     same workspace serves the next call as it is.
+ *                     arrival counters, candidate count, anchor, the floor's
+ *                     histogram) to zero, so the same workspace serves the next
+ *                     call as it is.
  * Three launches: per-row statistics (the last CTA of a row forms the row's
- * normaliser and raises the anchor), the gate filter, the budget select.
+ * normaliser and raises the anchor), the gate filter, the budget select.  The
+ * root layer's Top-K also gets a floor under its cut from the chunk maxima:
+ * found in the statistics pass when the row has at least `topk` chunks of
+ * 2048 logits, else by a fourth launch before the filter.
  * Scores are compared in fp64 (log domain) from fp32 logits.
  */
 size_t tv_expand_workspace_size(int F, int V);
@@ -479,9 +483,12 @@ tv_status tv_expand_gated(const float* draft_logits, const int32_t* frontier_nod
  *   n_nodes, workspace as for tv_expand_gated (the same workspace layout and
  *                     size, tv_expand_workspace_size(F, V), zero-filled before
  *                     its first use and returned zero-filled).
- * The same three launches as tv_expand_gated, without the gate; a chunk that
- * holds more than `width` candidates raises a floor under the layer's cut so
- * that later chunks pass on only what can still be kept.
+ * The same three launches as tv_expand_gated, without the gate.  The floor
+ * under the layer's cut comes from the chunk maxima: in the statistics pass
+ * when the frontier has at least `width` chunks of 2048 logits, else by a
+ * fourth launch before the filter; a chunk that holds more than `width`
+ * candidates raises it further, so that later chunks pass on only what can
+ * still be kept.
  */
 tv_status tv_expand_topn(const float* draft_logits, const int32_t* frontier_node,
                          const float* frontier_logscore, int F, int V, int width, int capacity,
