@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, results):
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this multi-threaded process
         results = m.dict()
         mp.spawn(_rank_main, args=(world, port, results), nprocs=world, join=True)
         res = dict(results)
