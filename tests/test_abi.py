@@ -198,3 +198,19 @@ def test_checked_build_exports_every_symbol(tvlib):
         assert lib.tv_debug_check_selftest(None, 4, 2, None) == tvlib.TV_ERR_INVALID_ARG
         assert lib.tv_debug_check_selftest(ctypes.c_void_p(0x1000), -1, 2, None) == \
             tvlib.TV_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """A copy of the binding without its built library refuses to import, with
+    the build command in the message: there is no fallback to run instead."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "speculative_decoding_tree_tv_gb300")
+    shutil.copytree(pkg, tmp_path / "speculative_decoding_tree_tv_gb300",
+                    ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__", "csrc"))
+    r = subprocess.run([sys.executable, "-c", "import speculative_decoding_tree_tv_gb300"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=300,
+                       env={**os.environ, "PYTHONPATH": str(tmp_path), "TV_CHECKED": "0"})
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libtreeverify.so not found" in r.stderr
